@@ -1,0 +1,222 @@
+"""CPU oracle for the W4A16 mixed-input GEMM.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+this module. The library (``weight_only_quantized_wq4_gb300``) never imports, links or calls it,
+and it shares no code with the CUDA path: both receive the seeded inputs of ``wq4_inputs`` and
+nothing else.
+
+What it computes (plain definitions, fp64, no blocking or reordering):
+
+* dequantisation, after "machete_mainloop.cuh", ``transform_A_kblock`` and
+  ``get_conversion_mode``: a 4-bit code q is up-converted, offset by its zero point (8 for the
+  uint4b8 type, the stored per-group z in zero-point mode) and multiplied by its group's scale:
+  W[n, k] = (q[n, k] - z[n, k // G]) * s[n, k // G].  The value is formed exactly in fp64; where
+  and how a kernel rounds it is the kernel's business, the oracle holds the exact number.
+* the product, after the header comment of "machete_mainloop.cuh" (Y = X W^t, computed there as
+  Y^t = W^t X^t): Y[m, n] = sum_k X[m, k] * W[n, k], in fp64 with ``numpy.matmul``.
+* one scale row per group of G consecutive K elements, groups starting at K = 0, G, 2G, ...
+  ("machete_mainloop.cuh", ``to_underlying_arguments``: scale_k = ceil(K / group_size), and
+  ``load``: the scale row of a k-tile is k_tile / ceil(group_size / tile_k)).
+* the grouped (pointer-array) variant: each problem on its own, after
+  "sm90_gemm_array_tma_warpspecialized_cooperative.hpp" (one GEMM per group index L).
+* the prepacked weight blob, the library's own tile-ordered layout (the pages prepack weights
+  offline, "machete_mainloop.cuh" header comment, but print no layout for this hardware). The blob
+  format is defined in this module's ``prepack`` docstring and restated independently by the GPU
+  prepack kernel.
+
+Pins (tests/test_oracle_pins.py) tie each function to something other than itself: exact
+rational brute force with hand-decoded floating-point bits, closed forms (one-hot, identity,
+all-zero), the per-group scale invariant, the uint4b8 == zero-point(8) identity, IEEE bit
+patterns, the nibble order, and a per-element brute-force placement of the blob layout.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 128
+TILE_N = 128            # weight rows per blob tile
+TILE_K = 128            # K elements per blob tile (one quantisation group)
+HEADER_BYTES = 256
+BLOB_MAGIC = 0x50345157  # bytes "WQ4P" little-endian
+BLOB_VERSION = 1
+DTYPE_CODE = {"bf16": 0, "fp16": 1}
+QTYPE_CODE = {"u4b8": 0, "u4_zp": 1}
+
+
+# --------------------------------------------------------------------------------------------
+# Formats
+# --------------------------------------------------------------------------------------------
+def decode16(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact fp64 value of raw bf16 / fp16 bit patterns (both widen exactly to fp64)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == "fp16":
+        return bits.view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def unpack_u4(words: np.ndarray, length: int) -> np.ndarray:
+    """Inverse of the API packing: element 8*j + i of a row is bits [4i, 4i+4) of word j."""
+    words = np.asarray(words, dtype=np.uint32)
+    shifts = 4 * np.arange(8, dtype=np.uint32)
+    nib = (words[..., :, None] >> shifts) & np.uint32(0xF)
+    out = nib.reshape(words.shape[:-1] + (words.shape[-1] * 8,)).astype(np.uint8)
+    if out.shape[-1] != length:
+        raise ValueError("packed length does not match")
+    return out
+
+
+# --------------------------------------------------------------------------------------------
+# Dequantisation and product
+# --------------------------------------------------------------------------------------------
+def zero_points(N: int, K: int, qtype: str, Z_words=None, group_size: int = GROUP) -> np.ndarray:
+    """z[g, n]: 8 for uint4b8 (the stored value minus 8); the stored nibble in zero-point mode."""
+    ng = K // group_size
+    if qtype == "u4b8":
+        return np.full((ng, N), 8, dtype=np.int64)
+    if qtype == "u4_zp":
+        return unpack_u4(Z_words, N).astype(np.int64).reshape(ng, N)
+    raise ValueError(qtype)
+
+
+def dequantize(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
+               group_size: int = GROUP) -> np.ndarray:
+    """W[n, k] = (q[n, k] - z[k // G, n]) * s[k // G, n] in fp64 (exact: |q - z| <= 15 times a
+    16-bit scale needs at most 15 significant bits)."""
+    if K % group_size:
+        raise ValueError("K must be a multiple of the group size")
+    q = unpack_u4(Wq, K).astype(np.int64)                       # [N][K]
+    z = zero_points(N, K, qtype, Z_words, group_size)           # [K/G][N]
+    s = decode16(S_bits, dtype)                                 # [K/G][N]
+    g_of_k = np.arange(K) // group_size
+    zk = z[g_of_k, :].T                                         # [N][K]
+    sk = s[g_of_k, :].T                                         # [N][K]
+    return (q - zk).astype(np.float64) * sk
+
+
+def mm(X_bits, Wq, S_bits, M: int, N: int, K: int, dtype: str, qtype: str, Z_words=None,
+       group_size: int = GROUP, rows=None) -> np.ndarray:
+    """Y_ref[M, N] = X . dequant(Wq)^T in fp64.  ``rows`` restricts the result to those rows of
+    X (same definition, fewer outputs) for workloads too large to check in full."""
+    X = decode16(X_bits, dtype).reshape(M, K)
+    if rows is not None:
+        X = X[np.asarray(rows)]
+    W = dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+    return np.matmul(X, W.T)
+
+
+def mm_problem(p, rows=None) -> np.ndarray:
+    """``mm`` on a ``wq4_inputs.Problem``."""
+    return mm(p.X_bits, p.Wq, p.S_bits, p.M, p.N, p.K, p.dtype, p.qtype, p.Z, p.group_size, rows)
+
+
+def grouped_mm(problems) -> list:
+    """The pointer-array variant: every problem independently (empty problems give empty Y)."""
+    return [mm_problem(p) for p in problems]
+
+
+def check_tolerance(Y_out: np.ndarray, Y_ref: np.ndarray, atol: float = 1e-2, rtol: float = 1e-2) -> dict:
+    """Per-element test |Y - Y_ref| <= atol + rtol * |Y_ref| and its summary statistics."""
+    Y_out = np.asarray(Y_out, dtype=np.float64)
+    Y_ref = np.asarray(Y_ref, dtype=np.float64)
+    err = np.abs(Y_out - Y_ref)
+    tol = atol + rtol * np.abs(Y_ref)
+    ratio = err / tol if err.size else np.zeros(0)
+    return {
+        "n": int(err.size),
+        "violations": int(np.count_nonzero(~(err <= tol))),
+        "max_abs_err": float(err.max()) if err.size else 0.0,
+        "max_err_over_tol": float(ratio.max()) if err.size else 0.0,
+    }
+
+
+# --------------------------------------------------------------------------------------------
+# Prepacked blob (the library's weight format)
+# --------------------------------------------------------------------------------------------
+def tile_bytes(qtype: str) -> int:
+    """Bytes of one (128-row, 128-K) tile record: 8192 B of codes, 256 B of scales and, in
+    zero-point mode, 64 B of zero points, padded to a multiple of 128 B."""
+    raw = 8192 + 256 + (64 if qtype == "u4_zp" else 0)
+    return (raw + 127) // 128 * 128
+
+
+def prepacked_bytes(N: int, K: int, qtype: str, group_size: int = GROUP) -> int:
+    return HEADER_BYTES + (N // TILE_N) * (K // TILE_K) * tile_bytes(qtype)
+
+
+# position of element e (0..7) of an 8-element run inside its 32-bit word: even elements take
+# nibbles 0..3, odd elements nibbles 4..7, so (word >> 4i) & 0x000F000F holds elements 2i, 2i+1.
+NIBBLE_POS = np.array([0, 4, 1, 5, 2, 6, 3, 7], dtype=np.uint32)
+
+
+def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
+            group_size: int = GROUP) -> np.ndarray:
+    """Blob bytes (uint8) for one weight.
+
+    Layout:
+      * header, 256 B of little-endian uint32: magic "WQ4P", version 1, N, K, group size,
+        dtype code (bf16 0, fp16 1), qtype code (u4b8 0, u4_zp 1), tile bytes, N/128, K/128,
+        then zeros.
+      * tile records in order (nt, g), nt = 0..N/128-1 outer, g = 0..K/128-1 inner, record
+        (nt, g) at byte 256 + (nt * K/128 + g) * tile_bytes.  Inside a record:
+          - codes, 8192 B: 16-byte chunk number (j * 128 + r) holds row n = 128 nt + r and
+            K elements 128 g + 32 j + [0, 32), j = 0..3.  Word w = 0..3 of the chunk holds the
+            eight elements 128 g + 32 j + 8 w + e, e = 0..7, element e in nibble NIBBLE_POS[e].
+          - scales, 256 B at offset 8192: the 16-bit scale of (row 128 nt + r, group g) at 2 r.
+          - zero points (u4_zp only), 64 B at offset 8448: the zero point of (row 128 nt + r,
+            group g) in bits [4 (r % 8), 4 (r % 8) + 4) of little-endian word r // 8.
+          - zero padding up to tile_bytes.
+    """
+    if group_size != GROUP or N % TILE_N or K % TILE_K:
+        raise ValueError("the blob format needs group 128 and N, K multiples of 128")
+    nT, nG = N // TILE_N, K // TILE_K
+    tb = tile_bytes(qtype)
+    blob = np.zeros(prepacked_bytes(N, K, qtype), dtype=np.uint8)
+    hdr = np.zeros(HEADER_BYTES // 4, dtype=np.uint32)
+    hdr[:10] = [BLOB_MAGIC, BLOB_VERSION, N, K, group_size, DTYPE_CODE[dtype], QTYPE_CODE[qtype],
+                tb, nT, nG]
+    blob[:HEADER_BYTES] = hdr.view(np.uint8)
+
+    q = unpack_u4(Wq, K).astype(np.uint32)                      # [N][K]
+    # axes: nt, r, g, j, w, e
+    q6 = q.reshape(nT, TILE_N, nG, 4, 4, 8)
+    words = np.bitwise_or.reduce(q6 << (4 * NIBBLE_POS), axis=-1)   # [nt][r][g][j][w]
+    words = words.transpose(0, 2, 3, 1, 4)                      # [nt][g][j][r][w]
+    codes = np.ascontiguousarray(words).view(np.uint8).reshape(nT, nG, 8192)
+
+    recs = blob[HEADER_BYTES:].reshape(nT, nG, tb)
+    recs[:, :, :8192] = codes
+    S = np.asarray(S_bits, dtype=np.uint16).reshape(nG, nT, TILE_N)        # [g][nt][r]
+    recs[:, :, 8192:8448] = np.ascontiguousarray(S.transpose(1, 0, 2)).view(np.uint8).reshape(nT, nG, 256)
+    if qtype == "u4_zp":
+        z = unpack_u4(Z_words, N).reshape(nG, nT, TILE_N)                  # [g][nt][r]
+        zw = _pack_rows(z.transpose(1, 0, 2))                              # [nt][g][16] uint32
+        recs[:, :, 8448:8512] = np.ascontiguousarray(zw).view(np.uint8).reshape(nT, nG, 64)
+    return blob
+
+
+def _pack_rows(z: np.ndarray) -> np.ndarray:
+    """Eight 4-bit values per little-endian uint32 along the last axis."""
+    z8 = z.astype(np.uint32).reshape(z.shape[:-1] + (z.shape[-1] // 8, 8))
+    return np.bitwise_or.reduce(z8 << (4 * np.arange(8, dtype=np.uint32)), axis=-1)
+
+
+def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str):
+    """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] or None)."""
+    nT, nG = N // TILE_N, K // TILE_K
+    tb = tile_bytes(qtype)
+    recs = np.asarray(blob, dtype=np.uint8)[HEADER_BYTES:HEADER_BYTES + nT * nG * tb].reshape(nT, nG, tb)
+    words = np.ascontiguousarray(recs[:, :, :8192]).view(np.uint32).reshape(nT, nG, 4, TILE_N, 4)
+    words = words.transpose(0, 3, 1, 2, 4)                      # [nt][r][g][j][w]
+    q6 = (words[..., None] >> (4 * NIBBLE_POS)) & np.uint32(0xF)  # [..][e]
+    q = q6.reshape(N, K).astype(np.uint8)
+    S = np.ascontiguousarray(recs[:, :, 8192:8448]).view(np.uint16).reshape(nT, nG, TILE_N)
+    S_bits = np.ascontiguousarray(S.transpose(1, 0, 2)).reshape(nG, N)
+    Z = None
+    if qtype == "u4_zp":
+        zw = np.ascontiguousarray(recs[:, :, 8448:8512]).view(np.uint32).reshape(nT, nG, 16)
+        z = unpack_u4(zw, TILE_N)                                # [nt][g][r]
+        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2)).reshape(nG, N))
+    Wq = _pack_rows(q)
+    return Wq.astype(np.uint32), S_bits, (None if Z is None else Z.astype(np.uint32))

@@ -1,0 +1,93 @@
+"""The pins are sharp: each plausible mistake planted in the oracle (on the CPU, by patching one
+of its functions for the duration of a test) makes at least one pin fail."""
+import numpy as np
+import pytest
+
+import oracle.wq4_oracle as W
+import tests.test_oracle_pins as pins
+
+_good_dequantize = W.dequantize
+_good_unpack = W.unpack_u4
+_good_decode = W.decode16
+
+
+def _dq_zero_index_mod(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    q = W.unpack_u4(Wq, K).astype(np.int64)
+    z = W.zero_points(N, K, qtype, Z_words, group_size)
+    s = W.decode16(S_bits, dtype)
+    g = np.arange(K) // group_size
+    gz = np.arange(K) % (K // group_size)          # wrong index for the zero point
+    return (q - z[gz, :].T).astype(np.float64) * s[g, :].T
+
+
+def _dq_sign(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    return -_good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+
+
+def _dq_drop_zero(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    q = W.unpack_u4(Wq, K).astype(np.float64)
+    s = W.decode16(S_bits, dtype)
+    return q * s[np.arange(K) // group_size, :].T
+
+
+def _dq_group_64(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    q = W.unpack_u4(Wq, K).astype(np.int64)
+    z = W.zero_points(N, K, qtype, Z_words, group_size)
+    s = W.decode16(S_bits, dtype)
+    g = np.minimum(np.arange(K) // 64, K // group_size - 1)   # wrong group size
+    return (q - z[g, :].T).astype(np.float64) * s[g, :].T
+
+
+def _dq_scale_rows_swapped(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    out = _good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+    return out[::-1].copy()                          # rows of W attached to the wrong outputs
+
+
+def _unpack_big_endian(words, length):
+    words = np.asarray(words, dtype=np.uint32)
+    shifts = 28 - 4 * np.arange(8, dtype=np.uint32)
+    nib = (words[..., :, None] >> shifts) & np.uint32(0xF)
+    return nib.reshape(words.shape[:-1] + (words.shape[-1] * 8,)).astype(np.uint8)
+
+
+def _decode_bf16_as_fp16(bits, dtype):
+    return _good_decode(bits, "fp16")
+
+
+MUTANTS = {
+    "zero point indexed by k mod groups": ("dequantize", _dq_zero_index_mod),
+    "sign flipped": ("dequantize", _dq_sign),
+    "zero point dropped": ("dequantize", _dq_drop_zero),
+    "group size 64": ("dequantize", _dq_group_64),
+    "weight rows permuted": ("dequantize", _dq_scale_rows_swapped),
+    "big-endian nibbles": ("unpack_u4", _unpack_big_endian),
+    "bf16 decoded as fp16": ("decode16", _decode_bf16_as_fp16),
+}
+
+
+def _pins_all_pass():
+    checks = [
+        lambda: pins.test_oracle_equals_exact_brute_force("bf16", "u4_zp", (2, 8, 384)),
+        lambda: pins.test_oracle_equals_exact_brute_force("bf16", "u4b8", (3, 16, 256)),
+        lambda: pins.test_one_hot_closed_form("u4_zp"),
+        lambda: pins.test_group_scale_invariant("u4b8"),
+        lambda: pins.test_decode16_bit_patterns(),
+        lambda: pins.test_nibble_order_is_little_endian(),
+    ]
+    for c in checks:
+        try:
+            c()
+        except Exception:
+            return False
+    return True
+
+
+def test_unmutated_oracle_passes():
+    assert _pins_all_pass()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(W, attr, fn)
+    assert not _pins_all_pass(), name
