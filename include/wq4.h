@@ -1,0 +1,145 @@
+/*
+ * wq4 — W4A16 mixed-input GEMM for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * Computes Y[M,N] = X[M,K] . dequant(Wq)[N,K]^T with X, the scales and Y in bf16 or fp16,
+ * 4-bit weight codes, one scale per group of 128 consecutive K elements and fp32 accumulation.
+ *
+ * The problem statement follows "aphrodite-engine/kernels/quantization/machete/
+ * machete_mainloop.cuh": its header comment (weights prepacked once, then Y = mm(X, B_prepacked);
+ * the product computed as the transpose Y^t = W^t X^t so the narrow type is the MMA's A side),
+ * get_conversion_mode (scale-only and scale-with-zero modes), Arguments (pointers, strides, group
+ * size, zero pointer) and can_implement (the argument rules reproduced under "Errors" below).
+ * The grouped variant follows "sm90_gemm_array_tma_warpspecialized_cooperative.hpp" (one GEMM per
+ * group index L, all in one persistent launch).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named X, Wq, scales, zeros, Wp, Y and workspace are DEVICE pointers. Arrays of
+ *    shapes and of per-problem pointers in the grouped call are HOST arrays.
+ *  - The caller owns every buffer. The library allocates no device memory.
+ *  - Calls that take a stream are asynchronous on it; NULL means the legacy default stream.
+ *  - Arguments are checked before anything is launched; on a negative status nothing was
+ *    launched and no buffer was touched.
+ *  - dtype: WQ4_BF16 or WQ4_FP16; X, the scales and Y share it. qtype: WQ4_U4B8 (value =
+ *    code - 8) or WQ4_U4_ZP (value = code - z with a 4-bit zero point per group and row).
+ *  - group_size must be 128; N and K multiples of 128; M >= 0.
+ */
+#ifndef WQ4_H_
+#define WQ4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* wq4_stream_t;
+
+enum {
+    WQ4_OK = 0,
+    WQ4_ERR_INVALID = -1,      /* bad shape, null pointer, zero pointer given/missing, bad enum */
+    WQ4_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned (TMA rule) */
+    WQ4_ERR_UNSUPPORTED = -3,  /* valid for the method, not built here (group size != 128, ...) */
+    WQ4_ERR_WORKSPACE = -4,    /* workspace missing or smaller than the *_workspace_bytes answer */
+    WQ4_ERR_CUDA = -5,         /* a CUDA runtime call failed (no device, launch failure, ...) */
+    WQ4_ERR_TIMEOUT = -6       /* a kernel's bounded pipeline wait ran out (see wq4_get_last_error) */
+};
+enum { WQ4_BF16 = 0, WQ4_FP16 = 1 };
+enum { WQ4_U4B8 = 0, WQ4_U4_ZP = 1 };
+
+/* Library version (major * 10000 + minor * 100 + patch) and a text for a status code. */
+int wq4_version(void);
+const char* wq4_status_string(int status);
+
+/* ------------------------------------------------------------------------------------------ *
+ * Prepack ("machete_mainloop.cuh", header comment: weights reordered once into the layout the
+ * mainloop consumes, so each thread fetches several MMAs' worth with one 128-bit load).
+ * ------------------------------------------------------------------------------------------ */
+
+/* Bytes of the prepacked blob for an N x K weight (256-byte header + one record per
+ * 128-row x 128-K tile). Returns 0 if the shape is not supported. */
+size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype);
+
+/* Reorders a weight into the prepacked blob.
+ *   Wq      [N][K/8] uint32, code of element k = 8j+i in bits [4i, 4i+4) of word j.
+ *   scales  [K/128][N] dtype, N contiguous (one scale per group and row).
+ *   zeros   [K/128][N/8] uint32, zero point of row n = 8j+i in bits [4i, 4i+4) of word j;
+ *           required for WQ4_U4_ZP and must be NULL for WQ4_U4B8.
+ *   Wp_out  wq4_prepacked_bytes(...) bytes, 16-byte aligned; fully overwritten.
+ * Integer work: the blob is a bit-exact permutation of the inputs. */
+int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros,
+                int N, int K, int group_size, int dtype, int qtype,
+                void* Wp_out, wq4_stream_t stream);
+
+/* Exact inverse of wq4_prepack (a test and export aid). zeros_out must be NULL for U4B8. */
+int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype,
+                  uint32_t* Wq_out, void* scales_out, uint32_t* zeros_out, wq4_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
+ * GEMM ("machete_mainloop.cuh": transform_A_kblock defines the dequantised value (code - zero)
+ * times the group's scale; mma/load define one scale row per group of K).
+ * ------------------------------------------------------------------------------------------ */
+
+/* Workspace bytes wq4_mm needs on the current device for this shape (partial sums of K-split
+ * tiles and their arrival counters). The workspace must be zero-filled once when allocated;
+ * every completed call leaves its counters at zero again. Calls that may overlap on the GPU
+ * need separate workspaces. */
+int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
+
+/* Y = X . dequant(Wp)^T.
+ *   X   [M][K] dtype row-major, 16-byte aligned.
+ *   Wp  blob from wq4_prepack with the same N, K, group_size, dtype and qtype.
+ *   Y   [M][N] dtype row-major, fully overwritten (fp32 sums rounded to nearest even).
+ *   workspace / workspace_bytes: see wq4_workspace_bytes.
+ * M == 0 is a no-op. Results are identical from run to run (fixed reduction order). */
+int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size,
+           int dtype, int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream);
+
+/* Workspace bytes for wq4_grouped_mm with these P problems (host arrays of shapes). */
+int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
+                                size_t* bytes);
+
+/* P independent problems Y_p = X_p . dequant(Wp_p)^T in one launch (P <= 64).
+ *   M, N, K            host arrays of P shapes; M[p] == 0 skips problem p (its pointers are
+ *                      not dereferenced and may be NULL).
+ *   X, Wp, Y           host arrays of P device pointers, per-problem layouts as in wq4_mm.
+ * All problems share group_size, dtype and qtype. */
+int wq4_grouped_mm(int P, const int* M, const int* N, const int* K,
+                   const void* const* X, const void* const* Wp, void* const* Y,
+                   int group_size, int dtype, int qtype,
+                   void* workspace, size_t workspace_bytes, wq4_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ *
+ * Errors and options.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Synchronises the stream, then reports (and clears) a device-side pipeline timeout recorded
+ * by any wq4 kernel on the current device (WQ4_ERR_TIMEOUT), else a pending CUDA error
+ * (WQ4_ERR_CUDA), else WQ4_OK. */
+int wq4_get_last_error(wq4_stream_t stream);
+
+/* Process-wide tuning and test options (not thread-safe; set before launching):
+ *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64 or 128); 0 = automatic
+ *   WQ4_OPT_GRID            force the number of persistent CTAs; 0 = automatic
+ *   WQ4_OPT_SPLIT_ALL       1 = every tile goes through the K-split path (tests)
+ *   WQ4_OPT_TIMEOUT_CYCLES  bound of every pipeline wait in SM clock cycles; 0 = default
+ *   WQ4_OPT_TRACE           1 = print each dispatch decision to stderr
+ *   WQ4_OPT_A_IN_SMEM       1 = stage the dequantised operand in shared memory instead of tensor
+ *                           memory (both give the same result; for comparison)
+ * Returns WQ4_ERR_INVALID for an unknown key or value. */
+enum {
+    WQ4_OPT_TOKEN_TILE = 1,
+    WQ4_OPT_GRID = 2,
+    WQ4_OPT_SPLIT_ALL = 3,
+    WQ4_OPT_TIMEOUT_CYCLES = 4,
+    WQ4_OPT_TRACE = 5,
+    WQ4_OPT_A_IN_SMEM = 6
+};
+int wq4_set_option(int key, long long value);
+long long wq4_get_option(int key);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ4_H_ */

@@ -20,5 +20,6 @@ def lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import weight_only_quantized_wq4_gb300 as wq4
+    wq4.build()
     wq4.load_library()
     return wq4

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports every function include/wq4.h declares, and its
+argument checks (after "machete_mainloop.cuh", can_implement) reject bad calls before any
+CUDA work — these run without a GPU."""
+import ctypes
+
+import pytest
+
+import weight_only_quantized_wq4_gb300 as wq4
+
+
+@pytest.fixture(scope="module")
+def clib():
+    wq4.build()
+    return wq4.load_library()
+
+
+def test_exports_every_declared_symbol(clib):
+    names = wq4.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(clib, n), n
+
+
+def test_status_strings(clib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert clib.wq4_status_string(code)
+    assert clib.wq4_version() >= 100
+
+
+def test_prepacked_bytes(clib):
+    assert clib.wq4_prepacked_bytes(4096, 4096, 128, 0) == 256 + 32 * 32 * 8448
+    assert clib.wq4_prepacked_bytes(14336, 4096, 128, 1) == 256 + 112 * 32 * 8576
+    assert clib.wq4_prepacked_bytes(100, 4096, 128, 0) == 0       # N not a multiple of 128
+    assert clib.wq4_prepacked_bytes(128, 4096, 64, 0) == 0        # group size 64 not built
+
+
+A16 = ctypes.c_void_p(0x10000)     # 16-byte aligned fake device addresses (never dereferenced)
+A16b = ctypes.c_void_p(0x20000)
+A16c = ctypes.c_void_p(0x30000)
+MIS = ctypes.c_void_p(0x10008)
+
+
+def _mm(clib, X=A16, W=A16b, Y=A16c, M=8, N=128, K=128, G=128, dt=0, qt=0):
+    return clib.wq4_mm(X, W, Y, M, N, K, G, dt, qt, None, 0, None)
+
+
+def test_mm_argument_rules(clib):
+    assert _mm(clib, M=-1) == wq4.ERR_INVALID
+    assert _mm(clib, N=0) == wq4.ERR_INVALID
+    assert _mm(clib, N=100) == wq4.ERR_UNSUPPORTED
+    assert _mm(clib, K=200) == wq4.ERR_UNSUPPORTED
+    assert _mm(clib, G=0) == wq4.ERR_INVALID                      # group size must be non-zero
+    assert _mm(clib, G=64) == wq4.ERR_UNSUPPORTED
+    assert _mm(clib, dt=7) == wq4.ERR_INVALID
+    assert _mm(clib, qt=9) == wq4.ERR_INVALID
+    assert _mm(clib, X=None) == wq4.ERR_INVALID
+    assert _mm(clib, W=None) == wq4.ERR_INVALID
+    assert _mm(clib, X=MIS) == wq4.ERR_ALIGN                      # 128-bit alignment for TMA
+    assert _mm(clib, Y=MIS) == wq4.ERR_ALIGN
+    assert _mm(clib, M=0, X=None, W=None, Y=None) == wq4.OK       # empty problem: nothing to do
+
+
+def test_prepack_argument_rules(clib):
+    pp = clib.wq4_prepack
+    assert pp(A16, A16b, None, 128, 128, 128, 0, 0, A16c, None) != wq4.ERR_INVALID   # valid (fails later, no GPU)
+    assert pp(A16, A16b, A16c, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_INVALID   # zeros given in u4b8 mode
+    assert pp(A16, A16b, None, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_INVALID   # zeros missing in zp mode
+    assert pp(A16, None, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_INVALID   # scales missing
+    assert pp(MIS, A16b, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN
+    assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
+
+
+def test_grouped_argument_rules(clib):
+    arr = ctypes.c_int * 2
+    ptrs = ctypes.c_void_p * 2
+    g = clib.wq4_grouped_mm
+    X, W, Y = ptrs(A16, A16), ptrs(A16b, A16b), ptrs(A16c, A16c)
+    assert g(0, arr(8, 8), arr(128, 128), arr(128, 128), X, W, Y, 128, 0, 0, None, 0, None) == wq4.ERR_INVALID
+    assert g(65, arr(8, 8), arr(128, 128), arr(128, 128), X, W, Y, 128, 0, 0, None, 0, None) == wq4.ERR_UNSUPPORTED
+    assert g(2, arr(8, -1), arr(128, 128), arr(128, 128), X, W, Y, 128, 0, 0, None, 0, None) == wq4.ERR_INVALID
+    assert g(2, arr(8, 8), arr(128, 96), arr(128, 128), X, W, Y, 128, 0, 0, None, 0, None) == wq4.ERR_UNSUPPORTED
+    Xbad = ptrs(A16, MIS)
+    assert g(2, arr(8, 8), arr(128, 128), arr(128, 128), Xbad, W, Y, 128, 0, 0, None, 0, None) == wq4.ERR_ALIGN
+    # an empty problem's pointers are never looked at
+    Xnull = ptrs(A16, None)
+    rc = g(2, arr(8, 0), arr(128, 128), arr(128, 128), Xnull, W, ptrs(A16c, None), 128, 0, 0, None, 0, None)
+    assert rc not in (wq4.ERR_INVALID, wq4.ERR_ALIGN)
+
+
+def test_options(clib):
+    assert clib.wq4_set_option(1, 64) == wq4.OK
+    assert clib.wq4_get_option(1) == 64
+    assert clib.wq4_set_option(1, 48) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(1, 0) == wq4.OK
+    assert clib.wq4_set_option(99, 1) == wq4.ERR_INVALID
+    assert clib.wq4_get_option(99) == -1

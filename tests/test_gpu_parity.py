@@ -1,0 +1,172 @@
+"""GPU path vs the CPU oracle through the C ABI: prepack bit-exact, GEMM within
+|Y - Y_ref| <= 1e-2 + 1e-2 |Y_ref| (fp32 accumulation, output rounded to bf16/fp16 once)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import wq4_inputs as I
+from tests.wq4_testutil import (assert_parity, from_cuda16, from_cuda32, gpu_mm, gpu_prepack, to_cuda16,
+                                y_as_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture
+def opts(lib):
+    """Options set inside a test are reset afterwards."""
+    yield lib
+    for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES):
+        lib.set_option(key, 0)
+
+
+# ------------------------------------------------------------------------------ prepack
+PREPACK_SHAPES = [(128, 128, "bf16", "u4b8"), (256, 512, "fp16", "u4b8"), (384, 256, "bf16", "u4_zp"),
+                  (512, 640, "fp16", "u4_zp"), (4096, 4096, "bf16", "u4b8"), (14336, 4096, "bf16", "u4_zp")]
+
+
+@pytest.mark.parametrize("N,K,dtype,qtype", PREPACK_SHAPES)
+def test_prepack_bit_exact(lib, N, K, dtype, qtype):
+    p = I.make_problem(1, N, K, dtype, qtype, seed=N + K)
+    blob = gpu_prepack(lib, p).cpu().numpy()
+    ref = O.prepack(p.Wq, p.S_bits, N, K, dtype, qtype, p.Z)
+    assert blob.shape == ref.shape
+    assert np.array_equal(blob, ref)
+
+
+@pytest.mark.parametrize("N,K,dtype,qtype", PREPACK_SHAPES[:4])
+def test_unprepack_round_trip(lib, N, K, dtype, qtype):
+    p = I.make_problem(1, N, K, dtype, qtype, seed=3 * N + K)
+    Wq, S, Z = lib.unprepack(gpu_prepack(lib, p), N, K, dtype, qtype)
+    assert np.array_equal(from_cuda32(Wq), p.Wq)
+    assert np.array_equal(from_cuda16(S), p.S_bits)
+    if qtype == "u4_zp":
+        assert np.array_equal(from_cuda32(Z), p.Z)
+    else:
+        assert Z is None
+
+
+# ------------------------------------------------------------------------------ GEMM
+SMALL = [
+    (1, 128, 128, "bf16", "u4b8"),
+    (8, 256, 512, "bf16", "u4b8"),
+    (16, 256, 512, "fp16", "u4b8"),
+    (17, 384, 640, "bf16", "u4_zp"),
+    (33, 128, 256, "fp16", "u4_zp"),
+    (64, 256, 384, "bf16", "u4b8"),
+    (65, 384, 256, "bf16", "u4b8"),
+    (128, 256, 512, "bf16", "u4_zp"),
+    (129, 128, 384, "fp16", "u4b8"),
+    (300, 512, 1024, "bf16", "u4b8"),
+    (777, 256, 256, "bf16", "u4_zp"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,qtype", SMALL)
+def test_mm_small(lib, M, N, K, dtype, qtype):
+    p = I.make_problem(M, N, K, dtype, qtype, seed=M * 7 + N + K)
+    Y = gpu_mm(lib, p)
+    assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), str((M, N, K, dtype, qtype)))
+
+
+@pytest.mark.parametrize("token_tile", [16, 64, 128])
+@pytest.mark.parametrize("grid", [0, 3, 7])
+@pytest.mark.parametrize("split_all", [0, 1])
+def test_mm_schedules(opts, token_tile, grid, split_all):
+    """Every token tile with whole tiles, K-split tiles and tiles split over 2+ CTAs."""
+    lib = opts
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    lib.set_option(lib.OPT_GRID, grid)
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)
+    p = I.make_problem(150, 384, 1280, "bf16", "u4_zp", seed=token_tile + grid)
+    Y = gpu_mm(lib, p)
+    assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "tile %d grid %d split %d" % (token_tile, grid, split_all))
+
+
+@pytest.mark.parametrize("token_tile", [16, 128])
+def test_mm_a_operand_in_smem(opts, token_tile):
+    lib = opts
+    lib.set_option(lib.OPT_A_IN_SMEM, 1)
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    p = I.make_problem(40, 256, 512, "fp16", "u4b8", seed=5)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "fp16"), O.mm_problem(p), "A in smem")
+
+
+def test_mm_deterministic(opts):
+    lib = opts
+    lib.set_option(lib.OPT_GRID, 5)
+    lib.set_option(lib.OPT_SPLIT_ALL, 1)
+    p = I.make_problem(24, 256, 2048, "bf16", "u4b8", seed=11)
+    blob = gpu_prepack(lib, p)
+    a = from_cuda16(gpu_mm(lib, p, blob))
+    b = from_cuda16(gpu_mm(lib, p, blob))
+    assert np.array_equal(a, b)
+
+
+def test_mm_m0_is_noop(lib):
+    import torch
+    p = I.make_problem(0, 128, 128, "bf16", "u4b8", seed=1)
+    blob = gpu_prepack(lib, p)
+    X = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    Y = lib.mm(X, blob, 128)
+    assert Y.shape == (0, 128)
+    assert lib.get_last_error() == 0
+
+
+def test_workspace_reuse_keeps_counters_zero(opts):
+    """A K-split call leaves its arrival counters at zero, so the workspace can be reused."""
+    lib = opts
+    lib.set_option(lib.OPT_GRID, 6)
+    p = I.make_problem(10, 256, 1024, "bf16", "u4b8", seed=12)
+    blob = gpu_prepack(lib, p)
+    ws = lib.alloc_workspace(lib.workspace_bytes(10, 256, 1024))
+    for _ in range(3):
+        Y = lib.mm(to_cuda16(p.X_bits, "bf16"), blob, 256, workspace=ws)
+        assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "reuse")
+    assert lib.get_last_error() == 0
+
+
+# ------------------------------------------------------------------------------ grouped
+def _grouped(lib, probs, qtype):
+    blobs = [gpu_prepack(lib, p) for p in probs]
+    Xs = [to_cuda16(p.X_bits, p.dtype) if p.M > 0 else to_cuda16(np.zeros((0, p.K), np.uint16), p.dtype)
+          for p in probs]
+    return lib.grouped_mm(Xs, blobs, [p.N for p in probs], qtype=qtype)
+
+
+@pytest.mark.parametrize("M_list", [[0, 17, 0, 40], [5], [130, 1, 64, 0, 200], [0, 0, 33]])
+def test_grouped_small(lib, M_list):
+    probs = I.make_grouped(sum(M_list), len(M_list), 256, 384, "bf16", "u4b8", seed=len(M_list), M_list=M_list)
+    outs = _grouped(lib, probs, "u4b8")
+    for p, Y in zip(probs, outs):
+        assert Y.shape == (p.M, p.N)
+        if p.M:
+            assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "grouped M=%d" % p.M)
+
+
+def test_grouped_mixed_shapes(lib):
+    """Per-problem N and K differ."""
+    shapes = [(9, 128, 256), (70, 384, 128), (0, 256, 512), (150, 256, 640)]
+    probs = [I.make_problem(m, n, k, "fp16", "u4_zp", seed=i) for i, (m, n, k) in enumerate(shapes)]
+    outs = _grouped(lib, probs, "u4_zp")
+    for p, Y in zip(probs, outs):
+        if p.M:
+            assert_parity(y_as_f64(Y, "fp16"), O.mm_problem(p), "mixed %s" % ((p.M, p.N, p.K),))
+
+
+# ------------------------------------------------------------------------------ workloads
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["tiny_m16_n256_k512_fp16_u4b8", "decode_m8_n4096_k4096_bf16_u4b8",
+                                  "asym_m128_n14336_k4096_bf16_u4zp", "prefill_m4096_n4096_k14336_bf16_u4b8"])
+def test_workload_full(lib, name):
+    p = I.make_workload(name)
+    Y = y_as_f64(gpu_mm(lib, p), p.dtype)
+    st = assert_parity(Y, O.mm_problem(p), name)
+    print(name, st)
+
+
+@pytest.mark.slow
+def test_grouped_workload_full(lib):
+    probs = I.make_workload("grouped_8x_n14336_k4096_summ1024_bf16_u4b8")
+    outs = _grouped(lib, probs, "u4b8")
+    for i, (p, Y) in enumerate(zip(probs, outs)):
+        assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "problem %d M=%d" % (i, p.M))

@@ -1,0 +1,218 @@
+"""Python binding of the wq4 C ABI (include/wq4.h): W4A16 GEMM for GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels of libwq4.so.
+Tensors are passed by device pointer together with torch's current CUDA stream; torch supplies
+device memory and streams and nothing else. There is no CPU fallback: the calls raise if the
+library is missing or a tensor is not on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import List, Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libwq4.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "wq4.h")
+
+OK, ERR_INVALID, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+DTYPES = {"bf16": 0, "fp16": 1}
+QTYPES = {"u4b8": 0, "u4_zp": 1}
+OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM = 1, 2, 3, 4, 5, 6
+GROUP = 128
+
+_lib = None
+
+
+class Wq4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _lib.wq4_status_string(status).decode() if _lib else "?", status))
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libwq4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libwq4.so is not built: run `python -m weight_only_quantized_wq4_gb300.build`")
+    lib = ctypes.CDLL(path)
+    c_int, c_size, vp, ll = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_longlong
+    ip = ctypes.POINTER(ctypes.c_int)
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    sigs = {
+        "wq4_version": (c_int, []),
+        "wq4_status_string": (ctypes.c_char_p, [c_int]),
+        "wq4_prepacked_bytes": (c_size, [c_int, c_int, c_int, c_int]),
+        "wq4_prepack": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]),
+        "wq4_unprepack": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp]),
+        "wq4_workspace_bytes": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]),
+        "wq4_mm": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_grouped_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
+        "wq4_grouped_mm": (c_int, [c_int, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_get_last_error": (c_int, [vp]),
+        "wq4_set_option": (c_int, [c_int, ll]),
+        "wq4_get_option": (ll, [c_int]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER) -> List[str]:
+    """Names of the functions include/wq4.h declares."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wq4_[a-z_]+)\s*\(", text)))
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise Wq4Error(status, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(device) -> ctypes.c_void_p:
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _cuda(t, name: str):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPES["bf16"]
+    if t.dtype == torch.float16:
+        return DTYPES["fp16"]
+    raise ValueError("activations and scales must be bfloat16 or float16")
+
+
+# ------------------------------------------------------------------------------------ API
+def set_option(key: int, value: int) -> None:
+    _check(load_library().wq4_set_option(key, value), "wq4_set_option")
+
+
+def get_option(key: int) -> int:
+    return int(load_library().wq4_get_option(key))
+
+
+def get_last_error(device=None) -> int:
+    """Synchronise torch's current stream and return the library's status (0 = ok)."""
+    return int(load_library().wq4_get_last_error(_stream(device)))
+
+
+def prepacked_bytes(N: int, K: int, qtype: str = "u4b8") -> int:
+    return int(load_library().wq4_prepacked_bytes(N, K, GROUP, QTYPES[qtype]))
+
+
+def prepack(Wq, scales, zeros=None, qtype: str = "u4b8"):
+    """Wq: int32 [N][K/8] (packed codes), scales: bf16/fp16 [K/128][N], zeros: int32 [K/128][N/8]
+    or None. Returns the prepacked blob (uint8 CUDA tensor)."""
+    torch = _torch()
+    lib = load_library()
+    N, K = Wq.shape[0], Wq.shape[1] * 8
+    nbytes = prepacked_bytes(N, K, qtype)
+    if nbytes == 0:
+        raise Wq4Error(ERR_UNSUPPORTED, "wq4_prepacked_bytes")
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=Wq.device)
+    zp = _cuda(zeros, "zeros") if zeros is not None else None
+    _check(lib.wq4_prepack(_cuda(Wq, "Wq"), _cuda(scales, "scales"), zp, N, K, GROUP, _dtype_code(scales),
+                           QTYPES[qtype], _cuda(blob, "blob"), _stream(Wq.device)), "wq4_prepack")
+    return blob
+
+
+def unprepack(blob, N: int, K: int, dtype: str = "bf16", qtype: str = "u4b8"):
+    """Inverse of prepack: (Wq int32 [N][K/8], scales [K/128][N], zeros int32 [K/128][N/8] or None)."""
+    torch = _torch()
+    lib = load_library()
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=blob.device)
+    sc = torch.empty((K // GROUP, N), dtype=tdt, device=blob.device)
+    zs = torch.empty((K // GROUP, N // 8), dtype=torch.int32, device=blob.device) if qtype == "u4_zp" else None
+    _check(lib.wq4_unprepack(_cuda(blob, "blob"), N, K, GROUP, DTYPES[dtype], QTYPES[qtype], _cuda(Wq, "Wq"),
+                             _cuda(sc, "scales"), _cuda(zs, "zeros") if zs is not None else None,
+                             _stream(blob.device)), "wq4_unprepack")
+    return Wq, sc, zs
+
+
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().wq4_workspace_bytes(M, N, K, GROUP, ctypes.byref(out)), "wq4_workspace_bytes")
+    return int(out.value)
+
+
+def grouped_workspace_bytes(Ms: Sequence[int], Ns: Sequence[int], Ks: Sequence[int]) -> int:
+    P = len(Ms)
+    arr = ctypes.c_int * P
+    out = ctypes.c_size_t(0)
+    _check(load_library().wq4_grouped_workspace_bytes(P, arr(*Ms), arr(*Ns), arr(*Ks), GROUP, ctypes.byref(out)),
+           "wq4_grouped_workspace_bytes")
+    return int(out.value)
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    """A zero-filled workspace (the library needs it zeroed once; calls keep it so)."""
+    torch = _torch()
+    return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None):
+    """Y[M,N] = X[M,K] . dequant(W)^T for a prepacked weight blob."""
+    torch = _torch()
+    lib = load_library()
+    M, K = X.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=X.dtype, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(M, N, K), X.device) if M > 0 else None
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_n = workspace.numel() if workspace is not None else 0
+    _check(lib.wq4_mm(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K, GROUP,
+                      _dtype_code(X), QTYPES[qtype], ws_ptr, ws_n, _stream(X.device)), "wq4_mm")
+    return out
+
+
+def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4b8", workspace=None,
+               outs: Optional[Sequence] = None):
+    """Independent problems Y_p = X_p . dequant(W_p)^T in one launch."""
+    torch = _torch()
+    lib = load_library()
+    P = len(Xs)
+    Ms = [int(x.shape[0]) for x in Xs]
+    Ks = [int(x.shape[1]) for x in Xs]
+    Ns = [int(n) for n in N]
+    if outs is None:
+        outs = [torch.empty((m, n), dtype=x.dtype, device=x.device) for x, m, n in zip(Xs, Ms, Ns)]
+    if workspace is None:
+        workspace = alloc_workspace(grouped_workspace_bytes(Ms, Ns, Ks), Xs[0].device)
+    arr = ctypes.c_int * P
+    ptrs = ctypes.c_void_p * P
+    xp = ptrs(*[x.data_ptr() if m > 0 else None for x, m in zip(Xs, Ms)])
+    wp = ptrs(*[b.data_ptr() for b in blobs])
+    yp = ptrs(*[y.data_ptr() if m > 0 else None for y, m in zip(outs, Ms)])
+    _check(lib.wq4_grouped_mm(P, arr(*Ms), arr(*Ns), arr(*Ks), xp, wp, yp, GROUP, _dtype_code(Xs[0]), QTYPES[qtype],
+                              _cuda(workspace, "workspace"), workspace.numel(), _stream(Xs[0].device)),
+           "wq4_grouped_mm")
+    return list(outs)

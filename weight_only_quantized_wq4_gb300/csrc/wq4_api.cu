@@ -1,0 +1,457 @@
+// Host side of the C ABI declared in include/wq4.h: argument checks, the tile/work plan, the
+// activation tensor maps and the launches.
+//
+// Argument rules follow "machete_mainloop.cuh", can_implement: 128-bit alignment of every
+// operand for TMA; group_size == K or a multiple of the K tile, and non-zero; the scale pointer
+// present in the scaled modes; the zero pointer present exactly in the zero-point mode. This
+// build supports group_size == 128 (one group per K tile, "machete_mainloop.cuh", load:
+// one scale row per k-tile) and N, K multiples of 128.
+//
+// The work plan mirrors the grouped persistent kernel of
+// "sm90_gemm_array_tma_warpspecialized_cooperative.hpp" (grid sized from the SM count, a
+// problem-shape array walked by one scheduler, work tiles past the last real one ending the CTA)
+// with a data-parallel / K-split hybrid: whole waves of tiles go one per CTA, the remaining
+// tiles' (tile, group) units are divided evenly over the CTAs and K-split tiles are summed in a
+// fixed order (deterministic).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/wq4.h"
+#include "wq4_launch.h"
+#include "wq4_params.h"
+
+namespace wq4 {
+namespace {
+
+__device__ unsigned int g_status;   // device-side error word (bounded-wait timeouts)
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultTimeoutCycles = 4000000000LL;   // ~2 s at 2 GHz
+
+struct Options {
+    int token_tile = 0;
+    int grid = 0;
+    int split_all = 0;
+    long long timeout_cycles = 0;
+    int trace = -1;
+    int a_in_smem = 0;
+};
+Options g_opt;
+
+struct DeviceInfo {
+    bool init = false;
+    int sm_count = 0;
+    unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+bool trace_on() {
+    if (g_opt.trace < 0) {
+        const char* e = std::getenv("WQ4_TRACE");
+        g_opt.trace = (e && e[0] == '1') ? 1 : 0;
+    }
+    return g_opt.trace == 1;
+}
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ4_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return WQ4_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return WQ4_ERR_CUDA;
+        d.status = static_cast<unsigned int*>(p);
+        d.init = true;
+    }
+    *out = &d;
+    return WQ4_OK;
+}
+
+// Bound of every pipeline wait: the option if set, else WQ4_TIMEOUT_CYCLES from the environment,
+// else about two seconds.
+long long timeout_cycles() {
+    if (g_opt.timeout_cycles > 0) return g_opt.timeout_cycles;
+    static long long env = -1;
+    if (env < 0) {
+        const char* e = std::getenv("WQ4_TIMEOUT_CYCLES");
+        env = e ? std::atoll(e) : 0;
+    }
+    return env > 0 ? env : kDefaultTimeoutCycles;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_types(int group_size, int dtype, int qtype) {
+    if (dtype != WQ4_BF16 && dtype != WQ4_FP16) return WQ4_ERR_INVALID;
+    if (qtype != WQ4_U4B8 && qtype != WQ4_U4_ZP) return WQ4_ERR_INVALID;
+    if (group_size <= 0) return WQ4_ERR_INVALID;
+    if (group_size != kTileK) return WQ4_ERR_UNSUPPORTED;
+    return WQ4_OK;
+}
+
+int check_nk(int N, int K) {
+    if (N <= 0 || K <= 0) return WQ4_ERR_INVALID;
+    if (N % kTileN || K % kTileK) return WQ4_ERR_UNSUPPORTED;
+    return WQ4_OK;
+}
+
+// ---------------------------------------------------------------------------- planning
+struct Shape {
+    int M, N, K;
+};
+
+struct Plan {
+    int nt = 0;              // token tile
+    int grid = 0;
+    int total_tiles = 0;
+    int dp_tiles = 0;
+    int sk_unit_begin = 0;
+    int sk_units = 0;
+    size_t counters_bytes = 0;
+    size_t partials_bytes = 0;
+    std::vector<int> m_tiles, tile_begin, unit_begin;
+    size_t workspace() const { return counters_bytes + partials_bytes; }
+};
+
+int pick_token_tile(const std::vector<Shape>& shapes) {
+    if (g_opt.token_tile) return g_opt.token_tile;
+    int maxM = 0;
+    for (const Shape& s : shapes) maxM = std::max(maxM, s.M);
+    return maxM <= 16 ? 16 : maxM <= 64 ? 64 : 128;
+}
+
+int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
+    pl->nt = pick_token_tile(shapes);
+    long long tiles = 0, units = 0;
+    for (const Shape& s : shapes) {
+        const int mt = s.M > 0 ? (s.M + pl->nt - 1) / pl->nt : 0;
+        pl->m_tiles.push_back(mt);
+        pl->tile_begin.push_back(static_cast<int>(tiles));
+        pl->unit_begin.push_back(static_cast<int>(units));
+        const long long t = static_cast<long long>(mt) * (s.N / kTileN);
+        tiles += t;
+        units += t * (s.K / kTileK);
+        if (units >= (1LL << 30) || tiles >= (1LL << 30)) return WQ4_ERR_UNSUPPORTED;
+    }
+    pl->total_tiles = static_cast<int>(tiles);
+    if (tiles == 0) return WQ4_OK;
+
+    int C = g_opt.grid ? g_opt.grid : sm_count;
+    // whole waves of tiles are processed data-parallel; the rest is K-split over all CTAs
+    int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
+    if (dp == tiles && !g_opt.split_all) {
+        pl->grid = C;
+        pl->dp_tiles = dp;
+        pl->sk_unit_begin = static_cast<int>(units);
+        pl->sk_units = 0;
+        return WQ4_OK;
+    }
+    // units of the K-split region
+    auto units_before = [&](int tile) {
+        int p = 0;
+        while (p + 1 < static_cast<int>(shapes.size()) && pl->tile_begin[p + 1] <= tile) ++p;
+        return pl->unit_begin[p] + static_cast<long long>(tile - pl->tile_begin[p]) * (shapes[p].K / kTileK);
+    };
+    long long sk_begin = units_before(dp);
+    // a thin remainder (under two units per CTA) takes one more wave into the split region
+    if (dp >= C && units - sk_begin < 2LL * C) {
+        dp -= C;
+        sk_begin = units_before(dp);
+    }
+    const long long sk_units = units - sk_begin;
+    // a K-split CTA should get at least a few groups; with little work use fewer CTAs
+    if (dp == 0 && !g_opt.grid) {
+        const long long want = std::max<long long>(1, sk_units / 4);
+        C = static_cast<int>(std::min<long long>(C, want));
+    }
+    if (sk_units * static_cast<long long>(C) >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
+    pl->grid = C;
+    pl->dp_tiles = dp;
+    pl->sk_unit_begin = static_cast<int>(sk_begin);
+    pl->sk_units = static_cast<int>(sk_units);
+    pl->counters_bytes = ((static_cast<size_t>(tiles - dp) * 4) + 255) / 256 * 256;
+    pl->partials_bytes = static_cast<size_t>(2) * C * pl->nt * kTileN * 4;
+    return WQ4_OK;
+}
+
+// ---------------------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// X [M][K] 16-bit row-major; box = 64 K elements (128 B) x nt rows, 128-byte swizzle; rows past M
+// read as zero.
+int encode_x_map(CUtensorMap* map, const void* X, int M, int K, int dtype, int nt) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return WQ4_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(nt)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dtype == WQ4_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
+cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int grid, cudaStream_t st) {
+    const bool bf16 = dtype == WQ4_BF16, zp = qtype == WQ4_U4_ZP, a_tmem = !g_opt.a_in_smem;
+    switch (nt) {
+        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, st);
+        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, st);
+        default: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, st);
+    }
+}
+
+template <int MAXP>
+int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void* const* Wp, void* const* Y,
+             int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    Plan pl;
+    rc = make_plan(shapes, dev->sm_count, &pl);
+    if (rc) return rc;
+    if (pl.total_tiles == 0) return WQ4_OK;
+    if (pl.workspace() > 0 && (workspace == nullptr || workspace_bytes < pl.workspace())) return WQ4_ERR_WORKSPACE;
+    if (pl.workspace() > 0 && !aligned16(workspace)) return WQ4_ERR_ALIGN;
+
+    auto* prm = new (std::nothrow) GemmParams<MAXP>();
+    if (!prm) return WQ4_ERR_CUDA;
+    std::memset(static_cast<void*>(prm), 0, sizeof(GemmParams<MAXP>));
+    for (size_t p = 0; p < shapes.size(); ++p) {
+        ProblemDesc& d = prm->prob[p];
+        d.wp = static_cast<const uint8_t*>(Wp[p]) + kBlobHeader;
+        d.y = Y[p];
+        d.M = shapes[p].M;
+        d.N = shapes[p].N;
+        d.K = shapes[p].K;
+        d.n_tiles = shapes[p].N / kTileN;
+        d.m_tiles = pl.m_tiles[p];
+        d.k_groups = shapes[p].K / kTileK;
+        d.tile_begin = pl.tile_begin[p];
+        d.unit_begin = pl.unit_begin[p];
+        if (d.M > 0) {
+            rc = encode_x_map(&prm->xmap[p], X[p], d.M, d.K, dtype, pl.nt);
+            if (rc) {
+                delete prm;
+                return rc;
+            }
+        }
+    }
+    prm->num_problems = static_cast<int>(shapes.size());
+    prm->total_tiles = pl.total_tiles;
+    prm->dp_tiles = pl.dp_tiles;
+    prm->num_ctas = pl.grid;
+    prm->sk_unit_begin = pl.sk_unit_begin;
+    prm->sk_units = pl.sk_units;
+    prm->counters = pl.counters_bytes ? static_cast<int*>(workspace) : nullptr;
+    prm->partials = pl.partials_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes)
+                                      : nullptr;
+    prm->status = dev->status;
+    prm->timeout_cycles = timeout_cycles();
+
+    if (trace_on()) {
+        std::fprintf(stderr,
+                     "[wq4] problems=%zu token_tile=%d grid=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s ws=%zu\n",
+                     shapes.size(), pl.nt, pl.grid, pl.total_tiles, pl.dp_tiles, pl.sk_units,
+                     g_opt.a_in_smem ? "smem" : "tmem", pl.workspace());
+    }
+    const cudaError_t e = dispatch(prm, MAXP > 1, pl.nt, dtype, qtype, pl.grid, st);
+    delete prm;
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace wq4
+
+using namespace wq4;
+
+extern "C" {
+
+int wq4_version(void) { return 100; }
+
+const char* wq4_status_string(int status) {
+    switch (status) {
+        case WQ4_OK: return "ok";
+        case WQ4_ERR_INVALID: return "invalid argument";
+        case WQ4_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case WQ4_ERR_UNSUPPORTED: return "unsupported shape or group size";
+        case WQ4_ERR_WORKSPACE: return "workspace missing or too small";
+        case WQ4_ERR_CUDA: return "CUDA error";
+        case WQ4_ERR_TIMEOUT: return "device pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype) {
+    if (check_types(group_size, WQ4_BF16, qtype) || check_nk(N, K)) return 0;
+    return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype == WQ4_U4_ZP);
+}
+
+int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros, int N, int K, int group_size,
+                int dtype, int qtype, void* Wp_out, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if ((rc = check_nk(N, K))) return rc;
+    if (!Wq || !scales || !Wp_out) return WQ4_ERR_INVALID;
+    if ((qtype == WQ4_U4_ZP) != (zeros != nullptr)) return WQ4_ERR_INVALID;
+    if (!aligned16(Wq) || !aligned16(scales) || !aligned16(Wp_out) || (zeros && !aligned16(zeros)))
+        return WQ4_ERR_ALIGN;
+    const cudaError_t e = launch_prepack(Wq, scales, zeros, N, K, dtype, qtype, Wp_out, stream);
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
+int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype, uint32_t* Wq_out,
+                  void* scales_out, uint32_t* zeros_out, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if ((rc = check_nk(N, K))) return rc;
+    if (!Wp || !Wq_out || !scales_out) return WQ4_ERR_INVALID;
+    if ((qtype == WQ4_U4_ZP) != (zeros_out != nullptr)) return WQ4_ERR_INVALID;
+    if (!aligned16(Wp) || !aligned16(Wq_out) || !aligned16(scales_out) || (zeros_out && !aligned16(zeros_out)))
+        return WQ4_ERR_ALIGN;
+    const cudaError_t e = launch_unprepack(Wp, N, K, qtype, Wq_out, scales_out, zeros_out, stream);
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
+int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size, size_t* bytes) {
+    if (!bytes || P <= 0 || P > kMaxGroupedProblems || !M || !N || !K) return WQ4_ERR_INVALID;
+    int rc = check_types(group_size, WQ4_BF16, WQ4_U4B8);
+    if (rc) return rc;
+    std::vector<Shape> shapes;
+    for (int p = 0; p < P; ++p) {
+        if (M[p] < 0) return WQ4_ERR_INVALID;
+        if ((rc = check_nk(N[p], K[p]))) return rc;
+        shapes.push_back({M[p], N[p], K[p]});
+    }
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    Plan pl;
+    if ((rc = make_plan(shapes, dev->sm_count, &pl))) return rc;
+    *bytes = pl.workspace();
+    return WQ4_OK;
+}
+
+int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
+    return wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
+}
+
+int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
+           void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if (M < 0) return WQ4_ERR_INVALID;
+    if ((rc = check_nk(N, K))) return rc;
+    if (M == 0) return WQ4_OK;
+    if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
+    if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
+    std::vector<Shape> shapes{{M, N, K}};
+    const void* xs[1] = {X};
+    const void* ws[1] = {Wp};
+    void* ys[1] = {Y};
+    return run_gemm<1>(shapes, xs, ws, ys, dtype, qtype, workspace, workspace_bytes, stream);
+}
+
+int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* const* X, const void* const* Wp,
+                   void* const* Y, int group_size, int dtype, int qtype, void* workspace, size_t workspace_bytes,
+                   wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if (P <= 0 || !M || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
+    if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
+    std::vector<Shape> shapes;
+    for (int p = 0; p < P; ++p) {
+        if (M[p] < 0) return WQ4_ERR_INVALID;
+        if ((rc = check_nk(N[p], K[p]))) return rc;
+        if (M[p] > 0) {
+            if (!X[p] || !Wp[p] || !Y[p]) return WQ4_ERR_INVALID;
+            if (!aligned16(X[p]) || !aligned16(Wp[p]) || !aligned16(Y[p])) return WQ4_ERR_ALIGN;
+        }
+        shapes.push_back({M[p], N[p], K[p]});
+    }
+    return run_gemm<kMaxGroupedProblems>(shapes, X, Wp, Y, dtype, qtype, workspace, workspace_bytes, stream);
+}
+
+int wq4_get_last_error(wq4_stream_t stream) {
+    const cudaError_t se = cudaStreamSynchronize(stream);
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    unsigned int st = 0;
+    if (cudaMemcpy(&st, dev->status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return WQ4_ERR_CUDA;
+    if (st) {
+        const unsigned int zero = 0;
+        cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return WQ4_ERR_TIMEOUT;
+    }
+    if (se != cudaSuccess || cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
+    return WQ4_OK;
+}
+
+int wq4_set_option(int key, long long value) {
+    switch (key) {
+        case WQ4_OPT_TOKEN_TILE:
+            if (value != 0 && value != 16 && value != 64 && value != 128) return WQ4_ERR_INVALID;
+            g_opt.token_tile = static_cast<int>(value);
+            return WQ4_OK;
+        case WQ4_OPT_GRID:
+            if (value < 0 || value > 4096) return WQ4_ERR_INVALID;
+            g_opt.grid = static_cast<int>(value);
+            return WQ4_OK;
+        case WQ4_OPT_SPLIT_ALL:
+            g_opt.split_all = value ? 1 : 0;
+            return WQ4_OK;
+        case WQ4_OPT_TIMEOUT_CYCLES:
+            if (value < 0) return WQ4_ERR_INVALID;
+            g_opt.timeout_cycles = value;
+            return WQ4_OK;
+        case WQ4_OPT_TRACE:
+            g_opt.trace = value ? 1 : 0;
+            return WQ4_OK;
+        case WQ4_OPT_A_IN_SMEM:
+            g_opt.a_in_smem = value ? 1 : 0;
+            return WQ4_OK;
+        default: return WQ4_ERR_INVALID;
+    }
+}
+
+long long wq4_get_option(int key) {
+    switch (key) {
+        case WQ4_OPT_TOKEN_TILE: return g_opt.token_tile;
+        case WQ4_OPT_GRID: return g_opt.grid;
+        case WQ4_OPT_SPLIT_ALL: return g_opt.split_all;
+        case WQ4_OPT_TIMEOUT_CYCLES: return g_opt.timeout_cycles;
+        case WQ4_OPT_TRACE: return trace_on() ? 1 : 0;
+        case WQ4_OPT_A_IN_SMEM: return g_opt.a_in_smem;
+        default: return -1;
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,512 @@
+// The W4A16 GEMM kernel for sm_103a.
+//
+// Problem (after "machete_mainloop.cuh", header comment): Y = X W^T is computed transposed,
+// Y^T = W X^T, so that the 4-bit weight is the MMA's A operand: 128 weight rows form the MMA's
+// M = 128 side (one row per TMEM lane) and a tile of NT tokens the N side.
+//
+// Dequantisation (after "machete_mainloop.cuh", transform_A_kblock and get_conversion_mode):
+// the value of a weight is (code - zero) * scale with zero = 8 (uint4b8) or the stored per-group
+// zero point. The pages round each scaled weight to the 16-bit type before the MMA; that
+// rounding, summed over K = 4096..14336, exceeds the required |dY| <= 1e-2 + 1e-2 |Y|. Here the
+// MMA operand is the exact integer (code - zero) (|v| <= 15 is exact in bf16 and fp16), every
+// 128-K group's product P_g = (q - z) . X^T lands in its own TMEM buffer, and the group's scale
+// is applied in fp32: acc += s[n, g] * P_g[n, :], one scalar per TMEM lane.
+//
+// Warp roles in one CTA (one CTA per SM, persistent):
+//   warp 0        TMA producer: per group, one bulk copy of the prepacked weight record (codes,
+//                 scales, zero points) and two 2-D tensor copies of the activation tile (two
+//                 64-element K panels, 128-byte swizzle) into a ring of shared-memory stages.
+//                 (After "machete_mainloop.cuh", load: A, B, scale and zero per stage.)
+//   warp 1        MMA issuer: one thread issues 8 tcgen05.mma (K = 16 each) per group into P[b],
+//                 b = group parity, then commits to the fold, dequant and stage barriers.
+//                 (After "sm100_implicit_gemm_umma_warpspecialized.hpp", mma.)
+//   dequant warps turn the 4-bit codes of a stage into the 16-bit integer operand (q - z) with
+//                 bit logic and one packed subtraction per pair, written to tensor memory (or to
+//                 a swizzled shared-memory tile), double buffered.
+//   fold warps    read P[b] from TMEM (lane = weight row), acc = s * P + acc in registers, and at
+//                 the end of a tile round to bf16/fp16 and store Y, or (for a tile split over
+//                 CTAs) write fp32 partials to the workspace, the last CTA to arrive summing them
+//                 in CTA order (after the split-K fixup in
+//                 "sm90_gemm_array_tma_warpspecialized_cooperative.hpp", TileScheduler::fixup).
+//
+// Every wait is bounded (see mbar_wait); a timed-out wait records WQ4_ERR_TIMEOUT in the status
+// word, the CTA stops issuing work, drains its copies and MMAs, frees its TMEM and returns.
+#pragma once
+
+#include "wq4_device.cuh"
+#include "wq4_params.h"
+
+namespace wq4 {
+
+template <int NT, bool ZP, bool ATMEM>
+struct GemmCfg {
+    static_assert(NT == 16 || NT == 64 || NT == 128, "token tile");
+    static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
+    static constexpr int kFW = NT <= 64 ? 4 : 8;             // fold / epilogue warps
+    static constexpr int kWarps = 2 + kDQW + kFW;             // warp 0 TMA, warp 1 MMA, then the rest
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kKParts = kDQW / 4;                 // dequant warps per TMEM lane quarter
+    static constexpr int kChunks = 4 / kKParts;              // 32-element K chunks per dequant thread
+    static constexpr int kColParts = kFW / 4;                // fold warps per TMEM lane quarter
+    static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
+    static constexpr int kRec = tile_record_bytes(ZP);
+    static constexpr int kRecAlloc = (kRec + 1023) / 1024 * 1024;
+    static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
+    static constexpr int kStageBytes = 2 * kXPanel + kRecAlloc;
+    static constexpr int kABuf = 128 * 128 * 2;              // one 128 x 128 16-bit operand tile
+    static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
+    static constexpr int kBarBytes = 512;
+    static constexpr int kMaxDynSmem = 232448;
+    static constexpr int kStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kABytes + kBarBytes;
+    static constexpr uint32_t kTxBytes = kRec + 2 * kXPanel;
+    static constexpr int kColA = 2 * NT;                     // TMEM column of A buffer 0
+    static constexpr int kTmemNeed = 2 * NT + (ATMEM ? 128 : 0);
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                     : kTmemNeed <= 256 ? 256 : 512;
+    static_assert(kStages >= 2, "shared memory");
+    static_assert(kSmemBytes <= kMaxDynSmem, "shared memory");
+    static_assert(kTmemNeed <= 512, "tensor memory");
+};
+
+struct Seg {
+    int prob, tile, nt, mt, g0, g1, slot;
+};
+
+template <int MAXP>
+struct Sched {
+    const GemmParams<MAXP>& prm;
+    int cta;
+    int dp_t;
+    int u, u_end;
+    bool first_sk;
+
+    __device__ Sched(const GemmParams<MAXP>& p, int c) : prm(p), cta(c), dp_t(c), first_sk(true) {
+        u = p.sk_unit_begin + (p.sk_units * c) / p.num_ctas;
+        u_end = p.sk_unit_begin + (p.sk_units * (c + 1)) / p.num_ctas;
+    }
+
+    __device__ int problem_of_tile(int t) const {
+        int p = 0;
+        while (p + 1 < prm.num_problems && prm.prob[p + 1].tile_begin <= t) ++p;
+        return p;
+    }
+
+    __device__ int problem_of_unit(int v) const {
+        int p = 0;
+        while (p + 1 < prm.num_problems && prm.prob[p + 1].unit_begin <= v) ++p;
+        return p;
+    }
+
+    __device__ bool next(Seg& s) {
+        if (dp_t < prm.dp_tiles) {
+            const int t = dp_t;
+            dp_t += prm.num_ctas;
+            const int p = problem_of_tile(t);
+            const ProblemDesc& P = prm.prob[p];
+            const int local = t - P.tile_begin;
+            s.prob = p;
+            s.tile = t;
+            s.mt = local / P.n_tiles;
+            s.nt = local % P.n_tiles;
+            s.g0 = 0;
+            s.g1 = P.k_groups;
+            s.slot = -1;
+            return true;
+        }
+        if (u < u_end) {
+            const int p = problem_of_unit(u);
+            const ProblemDesc& P = prm.prob[p];
+            const int local = u - P.unit_begin;
+            const int tl = local / P.k_groups;
+            const int g = local - tl * P.k_groups;
+            const int left = u_end - u;
+            const int take = left < (P.k_groups - g) ? left : (P.k_groups - g);
+            s.prob = p;
+            s.tile = P.tile_begin + tl;
+            s.mt = tl / P.n_tiles;
+            s.nt = tl % P.n_tiles;
+            s.g0 = g;
+            s.g1 = g + take;
+            const bool whole = (g == 0 && take == P.k_groups);
+            s.slot = whole ? -1 : 2 * cta + (first_sk ? 0 : 1);
+            first_sk = false;
+            u += take;
+            return true;
+        }
+        return false;
+    }
+};
+
+// CTA whose K-split range holds split-relative unit v (ranges [floor(c U / C), floor((c+1) U / C))).
+__device__ __forceinline__ int sk_cta_of(int v, int U, int C) {
+    return ((v + 1) * C - 1) / U;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
+    if constexpr (BF16) {
+        __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    } else {
+        __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+}
+
+// Two codes (in bits [0,4) and [16,20) of `w`) to two exact 16-bit integers code - zero.
+// OR-ing a code into the low mantissa bits of 128.0 (bf16 0x4300) or 1024.0 (fp16 0x6400), whose
+// unit in the last place is 1, gives 128 + q (1024 + q) exactly; subtracting 128 + z (1024 + z),
+// also exact, leaves q - z.
+template <bool BF16>
+__device__ __forceinline__ uint32_t codes_to_pair(uint32_t w, uint32_t sub) {
+    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
+    return sub2<BF16>((w & 0x000F000Fu) | kMagic, sub);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float scale_to_float(uint16_t bits) {
+    if constexpr (BF16) {
+        return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    } else {
+        return __half2float(__ushort_as_half(bits));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t float_to_out(float v) {
+    if constexpr (BF16) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    } else {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
+__global__ void __launch_bounds__(GemmCfg<NT, ZP, ATMEM>::kThreads, 1)
+wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
+    using C = GemmCfg<NT, ZP, ATMEM>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+    uint8_t* const gbase = smem_raw + (sbase - raw_s);
+
+    const uint32_t s_stage0 = sbase;
+    const uint32_t s_A = sbase + C::kStages * C::kStageBytes;
+    const uint32_t s_bar = s_A + C::kABytes;
+    auto full_bar = [&](int s) { return s_bar + 8u * s; };
+    auto empty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
+    auto afull_bar = [&](int b) { return s_bar + 8u * (32 + b); };
+    auto aempty_bar = [&](int b) { return s_bar + 8u * (34 + b); };
+    auto pfull_bar = [&](int b) { return s_bar + 8u * (36 + b); };
+    auto pempty_bar = [&](int b) { return s_bar + 8u * (38 + b); };
+    const uint32_t drain_bar = s_bar + 8u * 40;
+    const uint32_t fsync_bar = s_bar + 8u * 41;   // fold warps meet here in the split epilogue
+    uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 48;
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
+    volatile int* const fin_flag = reinterpret_cast<volatile int*>(gmisc + 8);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), C::kDQW + 1 + C::kFW);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(afull_bar(b), C::kDQW);
+            mbar_init(aempty_bar(b), 1);
+            mbar_init(pfull_bar(b), 1);
+            mbar_init(pempty_bar(b), C::kFW);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(fsync_bar, C::kFW);
+        *abort_flag = 0;
+        *fin_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int p = 0; p < prm.num_problems; ++p) {
+            if (prm.prob[p].m_tiles > 0) prefetch_tensormap(&prm.xmap[p]);   // empty problems have no map
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first();
+            const uint64_t pol_keep = policy_evict_last();
+            Sched<MAXP> sch(prm, blockIdx.x);
+            Seg seg;
+            int i = 0;
+            bool ok = true;
+            while (ok && sch.next(seg)) {
+                const ProblemDesc& P = prm.prob[seg.prob];
+                const uint64_t pol_w = P.m_tiles == 1 ? pol_stream : pol_keep;
+                const uint8_t* wrec = P.wp + (static_cast<size_t>(seg.nt) * P.k_groups + seg.g0) * C::kRec;
+                const CUtensorMap* xmap = &prm.xmap[seg.prob];
+                for (int g = seg.g0; g < seg.g1; ++g, ++i, wrec += C::kRec) {
+                    const int s = i % C::kStages;
+                    if (!mbar_wait(empty_bar(s), ((i / C::kStages) & 1) ^ 1, ctl)) { ok = false; break; }
+                    const uint32_t stage = s_stage0 + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
+                    bulk_load(stage + 2 * C::kXPanel, wrec, C::kRec, full_bar(s), pol_w);
+                    tma_load_2d(stage, xmap, full_bar(s), g * kTileK, seg.mt * NT, pol_keep);
+                    tma_load_2d(stage + C::kXPanel, xmap, full_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                }
+            }
+            if (!ok || *abort_flag) {
+                // Let every copy already issued land before the CTA can exit.
+                const int first = i > C::kStages ? i - C::kStages : 0;
+                for (int j = first; j < i; ++j) mbar_wait_plain(full_bar(j % C::kStages), (j / C::kStages) & 1, prm.timeout_cycles);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            Sched<MAXP> sch(prm, blockIdx.x);
+            Seg seg;
+            int i = 0;
+            bool ok = true;
+            while (ok && sch.next(seg)) {
+                const ProblemDesc& P = prm.prob[seg.prob];
+                const int rows = P.M - seg.mt * NT;
+                const int n_valid = rows < NT ? rows : NT;
+                const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
+                for (int g = seg.g0; g < seg.g1; ++g, ++i) {
+                    const int s = i % C::kStages;
+                    const int b = i & 1;
+                    const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                    if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                    if (!mbar_wait(afull_bar(b), u, ctl)) { ok = false; break; }
+                    if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * NT);
+                    const uint32_t xs = s_stage0 + s * C::kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t bdesc = make_sdesc_sw128(xs + (kk >> 2) * C::kXPanel + (kk & 3) * 32);
+                        if constexpr (ATMEM) {
+                            mma_ts(d_tmem, tmem_base + C::kColA + b * 64 + kk * 8, bdesc, idesc, kk > 0);
+                        } else {
+                            const uint64_t adesc = make_sdesc_sw128(s_A + b * C::kABuf + (kk >> 2) * (C::kABuf / 2) + (kk & 3) * 32);
+                            mma_ss(d_tmem, adesc, bdesc, idesc, kk > 0);
+                        }
+                    }
+                    mma_commit(pfull_bar(b));
+                    mma_commit(aempty_bar(b));
+                    mma_commit(empty_bar(s));
+                }
+            }
+            // Every MMA issued so far completes before the CTA frees its tensor memory.
+            mma_commit(drain_bar);
+            mbar_wait_plain(drain_bar, 0, prm.timeout_cycles);
+        }
+        __syncwarp();
+    } else if (warp < 2 + C::kDQW) {
+        // ------------------------------------------------------------------ dequant
+        // Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
+        const int q4 = warp & 3;
+        const int part = (warp - 2) >> 2;
+        const int r = 32 * q4 + lane;
+        Sched<MAXP> sch(prm, blockIdx.x);
+        Seg seg;
+        int i = 0;
+        bool ok = true;
+        while (ok && sch.next(seg)) {
+            for (int g = seg.g0; g < seg.g1; ++g, ++i) {
+                const int s = i % C::kStages;
+                const int b = i & 1;
+                const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                if (!mbar_wait(aempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
+                const uint32_t rec = s_stage0 + s * C::kStageBytes + 2 * C::kXPanel;
+                uint32_t sub;
+                if constexpr (ZP) {
+                    uint32_t zb;
+                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + 8448 + (r >> 1)));
+                    const uint32_t z = (zb >> ((r & 1) * 4)) & 0xFu;
+                    sub = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
+                } else {
+                    sub = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
+                }
+#pragma unroll
+                for (int jj = 0; jj < C::kChunks; ++jj) {
+                    const int j = part * C::kChunks + jj;
+                    const uint4 v = lds128(rec + (j * 128 + r) * 16);
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t out[16];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub);
+                    }
+                    if constexpr (ATMEM) {
+                        tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + b * 64 + 16 * j, out);
+                    } else {
+                        const uint32_t pbase = s_A + b * C::kABuf + (j >> 1) * (C::kABuf / 2) + r * 128;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint32_t chunk = static_cast<uint32_t>((4 * (j & 1) + w) ^ (r & 7));
+                            sts128(pbase + chunk * 16, out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+                        }
+                    }
+                }
+                if constexpr (ATMEM) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(afull_bar(b));
+                    mbar_arrive(empty_bar(s));
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ fold + epilogue
+        const int f = warp - 2 - C::kDQW;
+        const int q4 = warp & 3;
+        const int col0 = (f >> 2) * C::kNC;
+        const int r = 32 * q4 + lane;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * q4) << 16);
+        float acc[C::kNC];
+        uint32_t fs_phase = 0;
+        // Bounded rendezvous of the fold warps (an mbarrier, so that an abort cannot strand them).
+        auto fold_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(fsync_bar);
+            const bool r_ok = mbar_wait(fsync_bar, fs_phase, ctl);
+            fs_phase ^= 1u;
+            return r_ok;
+        };
+        Sched<MAXP> sch(prm, blockIdx.x);
+        Seg seg;
+        int i = 0;
+        bool ok = true;
+        while (ok && sch.next(seg)) {
+            for (int g = seg.g0; g < seg.g1; ++g, ++i) {
+                const int s = i % C::kStages;
+                const int b = i & 1;
+                const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                if (!mbar_wait(pfull_bar(b), u, ctl)) { ok = false; break; }
+                if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t rec = s_stage0 + s * C::kStageBytes + 2 * C::kXPanel;
+                uint32_t sbits;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + 8192 + 2 * r));
+                const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
+                const bool first = (g == seg.g0);
+#pragma unroll
+                for (int c = 0; c < C::kNC; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(t_lane + b * NT + col0 + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float pv = __uint_as_float(v[j]);
+                        acc[c + j] = first ? sc * pv : fmaf(sc, pv, acc[c + j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(pempty_bar(b));
+                    mbar_arrive(empty_bar(s));
+                }
+            }
+            if (!ok) break;
+
+            // ---------------------------------------------------------- tile epilogue
+            const ProblemDesc& P = prm.prob[seg.prob];
+            const int n = seg.nt * kTileN + r;
+            const int m0 = seg.mt * NT + col0;
+            if (seg.slot >= 0) {
+                float* mine = prm.partials + static_cast<size_t>(seg.slot) * (NT * 128);
+#pragma unroll
+                for (int j = 0; j < C::kNC; ++j) mine[(col0 + j) * 128 + r] = acc[j];
+                __threadfence();
+                if (!fold_sync()) break;
+                // the units of this tile, relative to the start of the K-split region
+                const int U = prm.sk_units;
+                const int t_u0 = P.unit_begin + (seg.tile - P.tile_begin) * P.k_groups - prm.sk_unit_begin;
+                const int c_first = sk_cta_of(t_u0, U, prm.num_ctas);
+                const int c_last = sk_cta_of(t_u0 + P.k_groups - 1, U, prm.num_ctas);
+                if (f == 0 && lane == 0) {
+                    // CTAs whose range is empty (fewer units than CTAs) hold no part of the tile
+                    int nseg = 0;
+                    for (int cc = c_first; cc <= c_last; ++cc)
+                        nseg += ((cc * U) / prm.num_ctas < ((cc + 1) * U) / prm.num_ctas) ? 1 : 0;
+                    int* cnt = prm.counters + (seg.tile - prm.dp_tiles);
+                    const int old = atomicAdd(cnt, 1);
+                    const int last = (old == nseg - 1) ? 1 : 0;
+                    if (last) atomicExch(cnt, 0);
+                    *fin_flag = last;
+                }
+                if (!fold_sync()) break;
+                if (!*fin_flag) continue;
+                __threadfence();
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const int start = (cc * U) / prm.num_ctas;
+                    if (start == ((cc + 1) * U) / prm.num_ctas) continue;   // empty range
+                    const int sl = 2 * cc + ((cc == c_first && start < t_u0) ? 1 : 0);
+                    const float* src = prm.partials + static_cast<size_t>(sl) * (NT * 128) + r;
+#pragma unroll
+                    for (int j = 0; j < C::kNC; ++j) {
+                        const float v = __ldcg(src + (col0 + j) * 128);
+                        acc[j] = (cc == c_first) ? v : acc[j] + v;
+                    }
+                }
+            }
+            uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
+#pragma unroll
+            for (int j = 0; j < C::kNC; ++j) {
+                const int m = m0 + j;
+                if (m < P.M) y[static_cast<size_t>(m) * P.N + n] = float_to_out<BF16>(acc[j]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// Host-side launcher for one instantiation.
+template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
+cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, cudaStream_t stream) {
+    using C = GemmCfg<NT, ZP, ATMEM>;
+    auto kern = wq4_gemm_kernel<NT, BF16, ZP, MAXP, ATMEM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace wq4

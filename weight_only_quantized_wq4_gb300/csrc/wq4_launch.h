@@ -1,0 +1,23 @@
+// Launchers of the GEMM instantiations (one translation unit per token tile) and of prepack.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace wq4 {
+
+// `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
+cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+                             cudaStream_t st);
+cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+                             cudaStream_t st);
+cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+                              cudaStream_t st);
+
+cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K,
+                           int dtype, int qtype, void* blob, cudaStream_t st);
+cudaError_t launch_unprepack(const void* blob, int N, int K, int qtype, uint32_t* wq, void* scales,
+                             uint32_t* zeros, cudaStream_t st);
+
+}  // namespace wq4

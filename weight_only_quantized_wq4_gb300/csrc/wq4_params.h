@@ -1,0 +1,51 @@
+// Kernel parameter blocks shared by the host planner and the GEMM kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace wq4 {
+
+constexpr int kTileN = 128;          // weight rows per tile (the MMA's M side after the transpose)
+constexpr int kTileK = 128;          // K elements per tile = one quantisation group
+constexpr int kBlobHeader = 256;     // bytes before the first tile record of a prepacked blob
+constexpr int kMaxGroupedProblems = 64;
+
+// Bytes of one (128-row, 128-K) record of the prepacked blob: 8192 B of codes, 256 B of
+// scales, 64 B of zero points in zero-point mode, padded to 128 B.
+constexpr int tile_record_bytes(bool zp) { return zp ? 8576 : 8448; }
+
+struct ProblemDesc {
+    const uint8_t* wp;       // first tile record (blob + kBlobHeader)
+    void* y;                 // [M][N] row-major
+    int M, N, K;
+    int n_tiles;             // N / 128
+    int m_tiles;             // ceil(M / token tile), 0 for an empty problem
+    int k_groups;            // K / 128
+    int tile_begin;          // global index of the problem's first tile
+    int unit_begin;          // global index of the problem's first (tile, group) unit
+};
+
+// A tile is (problem, m_tile, n_tile); inside a problem tiles run m-major (consecutive tiles
+// share the same activation rows and walk the weight tiles), so the CTAs working at one time
+// share operands in L2. Tiles [0, dp_tiles) are processed whole, tile t by CTA t % num_ctas.
+// The units (tile, group) of tiles [dp_tiles, total_tiles) are split evenly and contiguously
+// over the CTAs (CTA c takes units [floor(c U / C), floor((c+1) U / C)) counted from
+// sk_unit_begin); a tile split between CTAs is summed in the workspace in CTA order.
+template <int MAXP>
+struct GemmParams {
+    CUtensorMap xmap[MAXP];  // activations of each problem: 2-D (K, M), box (64, token tile), 128B swizzle
+    ProblemDesc prob[MAXP];
+    int num_problems;
+    int total_tiles;
+    int dp_tiles;
+    int num_ctas;
+    int sk_unit_begin;
+    int sk_units;            // the host keeps sk_units * num_ctas < 2^31 (32-bit index math)
+    float* partials;         // [2 * num_ctas][token tile * 128] fp32
+    int* counters;           // [total_tiles - dp_tiles], zero between calls
+    unsigned int* status;    // device status word (timeouts)
+    long long timeout_cycles;
+};
+
+}  // namespace wq4
