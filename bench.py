@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4A16 GEMM on GB300 (one JSON line on stdout).
+
+A step is one call of the hot path (wq4_mm, or wq4_grouped_mm for the grouped workload) on one
+batch of seeded synthetic input already resident in HBM; the weight is prepacked once before
+timing (prepack is the offline step of the method). K steps are replayed from a CUDA graph
+over rotating copies of every input so that the data each launch reads was evicted from L2 by
+the launches in between (the rotating set is larger than L2). Time is taken with CUDA events
+on the launching stream, max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own replica of the workload
+(weak scaling; the GEMM needs no exchange) and value = all ranks' work / max time.
+--impl reference times the CPU oracle (fp64 NumPy) on this host's cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import wq4_inputs as I  # noqa: E402
+
+METRIC = "W4A16 GEMM TFLOP/s and HBM GB/s vs GB300 roofline, M=8..4096 (1 GPU)"
+DEFAULT_WORKLOAD = "decode_m8_n4096_k4096_bf16_u4b8"
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sust": p["bf16_tflops_sustained"],
+                "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "src": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_quantized_wq4_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def workload_shapes(name, probs):
+    if isinstance(probs, list):
+        Ms = [p.M for p in probs]
+        byts = sum(I.algorithmic_bytes(p.M, p.N, p.K, p.qtype) for p in probs)
+        flops = sum(I.algorithmic_flops(p.M, p.N, p.K) for p in probs)
+        cfg = {"workload": name, "problems": len(probs), "M_list": Ms, "N": probs[0].N, "K": probs[0].K,
+               "group_size": 128, "qtype": probs[0].qtype}
+        return byts, flops, cfg, probs[0].dtype
+    p = probs
+    cfg = {"workload": name, "M": p.M, "N": p.N, "K": p.K, "group_size": 128, "qtype": p.qtype}
+    return I.algorithmic_bytes(p.M, p.N, p.K, p.qtype), I.algorithmic_flops(p.M, p.N, p.K), cfg, p.dtype
+
+
+def bound_of(byts, flops, pk):
+    # ridge point of the measured rooflines
+    return "tensor" if flops / byts > (pk["bf16"] * 1e12) / (pk["hbm_gbs"] * 1e9) else "hbm"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if t0 <= ts <= t1:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import weight_only_quantized_wq4_gb300 as wq4
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wq4.build()
+    wq4.load_library()
+    if args.a_in_smem:
+        wq4.set_option(wq4.OPT_A_IN_SMEM, 1)
+    pk = peaks()
+
+    probs = I.make_workload(args.workload)
+    grouped = isinstance(probs, list)
+    plist = probs if grouped else [probs]
+    byts, flops, cfg, dtype = workload_shapes(args.workload, probs)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+
+    def c16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
+
+    def c32(words):
+        return torch.from_numpy(np.ascontiguousarray(words).view(np.int32)).to(dev)
+
+    # one resident copy of the inputs, prepacked once
+    base_X = [c16(p.X_bits) if p.M > 0 else torch.empty((0, p.K), dtype=tdt, device=dev) for p in plist]
+    base_W = [wq4.prepack(c32(p.Wq), c16(p.S_bits), c32(p.Z) if p.Z is not None else None, qtype=p.qtype)
+              for p in plist]
+    torch.cuda.synchronize()
+    qtype = plist[0].qtype
+    if grouped:
+        ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
+    else:
+        ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K)
+    set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in base_W) + \
+        sum(p.M * p.N * 2 for p in plist) + ws_bytes
+    R = max(2, math.ceil(3 * L2_BYTES / set_bytes))
+    copies = []
+    for r in range(R):
+        Xs = [x.clone() for x in base_X]
+        Ws = [w.clone() for w in base_W]
+        Ys = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
+        ws = wq4.alloc_workspace(ws_bytes, dev)
+        copies.append((Xs, Ws, Ys, ws))
+    torch.cuda.synchronize()
+
+    def step(c):
+        Xs, Ws, Ys, ws = copies[c % R]
+        if grouped:
+            wq4.grouped_mm(Xs, Ws, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys)
+        else:
+            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0])
+
+    stream = torch.cuda.Stream(dev)
+    K, W = args.steps, args.warmup
+    use_graph = not args.no_graph
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+        torch.cuda.synchronize()
+        graph = None
+        if use_graph:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(K):
+                    step(i)
+            torch.cuda.synchronize()
+    assert wq4.get_last_error(dev) == 0
+
+    def timed_region():
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for i in range(K):
+                    step(i)
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
+
+    sampler = ClockSampler(local_rank)
+    if not args.profile_run:
+        sampler.start()
+        time.sleep(0.3)
+    # soak (not timed): the same replay, so that the clock samples below see this load
+    t_soak = time.time()
+    while not args.profile_run and time.time() - t_soak < 1.0:
+        timed_region()
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms_total = timed_region()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    _barrier(world)
+    sampler.stop()
+    clocks = sampler.summary(t_soak, t1)
+    assert wq4.get_last_error(dev) == 0
+    ms_total = _max_over_ranks(ms_total, world)
+
+    ms = ms_total / K
+    gbs = byts / (ms * 1e-3) / 1e9
+    tfl = flops / (ms * 1e-3) / 1e12
+    bound = bound_of(byts, flops, pk)
+
+    # end to end through the public API from pinned host buffers: H2D of the step's inputs
+    # (activations and the prepacked weight), the call, D2H of the result.
+    e2e = None if args.profile_run else run_e2e(args, wq4, plist, base_W, grouped, qtype, ws_bytes, dev, tdt,
+                                                 byts, flops, bound)
+
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            tr = json.load(f)
+        ent = tr.get(args.workload)
+        if ent and ent.get("kernel_hash") == kernel_source_hash():
+            traffic = ent["bytes_per_launch"]
+    except Exception:
+        pass
+
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": pk["src"] + " (burst copy)"}
+        value, unit = gbs * world, "GB/s"
+    else:
+        roof = {"bound": "tensor", "achieved": round(tfl, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": round(tfl / pk["bf16"], 4), "traffic": traffic,
+                "peak_source": pk["src"] + " (bf16 burst)",
+                "frac_vs_sustained": round(tfl / pk["bf16_sust"], 4)}
+        value, unit = tfl * world, "TFLOP/s"
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic (seeded numpy, wq4_inputs)",
+        "config": dict(cfg, l2="rotating %d input copies (%.0f MB) > L2 per launch" % (R, R * set_bytes / 1e6),
+                       launch="CUDA graph of K launches" if use_graph else "eager launches",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "tflops": round(tfl, 3), "gbs": round(gbs, 1),
+        "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 4),
+        "roofline": roof,
+        "gpu_launches": K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run:
+        out["cpu_baseline"] = cpu_baseline(args.workload, probs, byts, flops, bound, budget_s=args.cpu_seconds)
+    return out
+
+
+def run_e2e(args, wq4, plist, base_W, grouped, qtype, ws_bytes, dev, tdt, byts, flops, bound):
+    import torch
+    steps = max(3, min(args.steps, 20))
+    hX = [torch.from_numpy(np.ascontiguousarray(p.X_bits).view(np.int16)).view(tdt).pin_memory() for p in plist]
+    hW = [w.cpu().pin_memory() for w in base_W]
+    hY = [torch.empty((p.M, p.N), dtype=tdt).pin_memory() for p in plist]
+    dX = [torch.empty_like(x, device=dev) for x in hX]
+    dW = [torch.empty_like(w, device=dev) for w in hW]
+    dY = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
+    ws = wq4.alloc_workspace(ws_bytes, dev)
+    stream = torch.cuda.Stream(dev)
+    h2d = sum(x.numel() * 2 for x in hX) + sum(w.numel() for w in hW)
+    d2h = sum(y.numel() * 2 for y in hY)
+
+    def one():
+        for a, b in zip(dX, hX):
+            a.copy_(b, non_blocking=True)
+        for a, b in zip(dW, hW):
+            a.copy_(b, non_blocking=True)
+        if grouped:
+            wq4.grouped_mm(dX, dW, [p.N for p in plist], qtype=qtype, workspace=ws, outs=dY)
+        else:
+            wq4.mm(dX[0], dW[0], plist[0].N, qtype=qtype, workspace=ws, out=dY[0])
+        for a, b in zip(hY, dY):
+            a.copy_(b, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if bound == "hbm":
+        v, u = byts / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        v, u = flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    return {"value": round(v, 3), "unit": u, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms, "steps": steps}
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+def _rows_of(p, n):
+    """The sub-problem made of the first n weight rows (outputs Y[:, :n] of the full problem)."""
+    return I.Problem(p.M, n, p.K, p.dtype, p.qtype, p.X_bits, p.q[:n], p.Wq[:n], p.S_bits[:, :n],
+                     None if p.z is None else p.z[:, :n], None if p.Z is None else p.Z[:, :n // 8])
+
+
+def oracle_step(probs, frac):
+    """The oracle on a fraction of every problem's weight rows (its dequantisation and product
+    both scale linearly with the rows)."""
+    import oracle as O
+    plist = probs if isinstance(probs, list) else [probs]
+    out = []
+    for p in plist:
+        if p.M == 0:
+            continue
+        n = max(128, int(round(p.N * frac / 128)) * 128) if frac < 1 else p.N
+        out.append(O.mm_problem(_rows_of(p, n)))
+    return out
+
+
+def calibrate(probs, seconds):
+    """Fraction of weight rows that makes one oracle step take about `seconds`."""
+    plist = probs if isinstance(probs, list) else [probs]
+    f0 = min(1.0, 1024.0 / max(p.N for p in plist))
+    t0 = time.perf_counter()
+    oracle_step(probs, f0)
+    dt = time.perf_counter() - t0
+    f = min(1.0, f0 * seconds / max(dt, 1e-6))
+    n_rows = max(p.N for p in plist)
+    return max(128.0 / n_rows, round(f * n_rows / 128) * 128 / n_rows)
+
+
+def _sample_text(probs, frac):
+    plist = probs if isinstance(probs, list) else [probs]
+    if frac >= 1:
+        return "the whole step"
+    return "the first %d of %d weight rows of every problem (all tokens), time scaled by %d/%d" % (
+        max(128, int(round(plist[0].N * frac / 128)) * 128), plist[0].N, plist[0].N,
+        max(128, int(round(plist[0].N * frac / 128)) * 128))
+
+
+def _scaled_step_time(probs, frac, dt):
+    plist = probs if isinstance(probs, list) else [probs]
+    if frac >= 1:
+        return dt
+    n = max(128, int(round(plist[0].N * frac / 128)) * 128)
+    return dt * plist[0].N / n
+
+
+def _as_metric(bound, byts, flops, dt):
+    if bound == "hbm":
+        return byts / dt / 1e9, "GB/s"
+    return flops / dt / 1e12, "TFLOP/s"
+
+
+def cpu_baseline(name, probs, byts, flops, bound, budget_s=15.0):
+    """The oracle as it stands on this host's cores, about budget_s seconds of work."""
+    frac = calibrate(probs, 1.0)
+    oracle_step(probs, frac)          # warm-up
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(probs, frac)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = _scaled_step_time(probs, frac, (time.perf_counter() - t0) / n)
+    v, u = _as_metric(bound, byts, flops, dt)
+    return {"value": v, "unit": u, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d repetition(s) of %s" % (n, _sample_text(probs, frac)),
+            "seconds_per_step": dt, "note": "fp64 NumPy dequantise + matmul; a baseline, not a target"}
+
+
+def run_reference(args, rank, world):
+    pk = peaks()
+    probs = I.make_workload(args.workload)
+    byts, flops, cfg, dtype = workload_shapes(args.workload, probs)
+    bound = bound_of(byts, flops, pk)
+    per_step = max(0.05, min(2.0, 120.0 / (args.steps + args.warmup)))
+    frac = calibrate(probs, per_step)
+    for _ in range(args.warmup):
+        oracle_step(probs, frac)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(probs, frac)
+    dt = _scaled_step_time(probs, frac, (time.perf_counter() - t0) / args.steps)
+    v, u = _as_metric(bound, byts, flops, dt)
+    sample = "each step: " + _sample_text(probs, frac)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": u, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy, wq4_inputs)", "config": cfg,
+            "cpu_baseline": {"value": v, "unit": u, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": u, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------------------ ranks
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(v, world):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="wq4", choices=["wq4", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--a-in-smem", action="store_true", help="dequantised operand via shared memory")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only warm-up and the timed replay (for profiler runs): no soak, e2e or CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -127,6 +127,9 @@ int wq4_get_last_error(wq4_stream_t stream);
  *   WQ4_OPT_TRACE           1 = print each dispatch decision to stderr
  *   WQ4_OPT_A_IN_SMEM       1 = stage the dequantised operand in shared memory instead of tensor
  *                           memory (both give the same result; for comparison)
+ *   WQ4_OPT_CLUSTER         0 = automatic, -1 = never, 2..8 = force the cluster split: each tile's
+ *                           K range split over a cluster of that many CTAs whose partial sums are
+ *                           added through distributed shared memory
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,
@@ -134,7 +137,8 @@ enum {
     WQ4_OPT_SPLIT_ALL = 3,
     WQ4_OPT_TIMEOUT_CYCLES = 4,
     WQ4_OPT_TRACE = 5,
-    WQ4_OPT_A_IN_SMEM = 6
+    WQ4_OPT_A_IN_SMEM = 6,
+    WQ4_OPT_CLUSTER = 7
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

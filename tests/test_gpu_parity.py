@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 def opts(lib):
     """Options set inside a test are reset afterwards."""
     yield lib
-    for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES):
+    for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES,
+                lib.OPT_CLUSTER):
         lib.set_option(key, 0)
 
 
@@ -80,6 +81,35 @@ def test_mm_schedules(opts, token_tile, grid, split_all):
     p = I.make_problem(150, 384, 1280, "bf16", "u4_zp", seed=token_tile + grid)
     Y = gpu_mm(lib, p)
     assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "tile %d grid %d split %d" % (token_tile, grid, split_all))
+
+
+@pytest.mark.parametrize("token_tile", [16, 64, 128])
+@pytest.mark.parametrize("cluster", [2, 3, 4, 8])
+def test_mm_cluster_split(opts, token_tile, cluster):
+    """Each tile's K range split over a cluster; partials added through distributed shared memory."""
+    lib = opts
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    lib.set_option(lib.OPT_CLUSTER, cluster)
+    p = I.make_problem(100, 256, 1152, "bf16", "u4b8", seed=cluster * 100 + token_tile)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "cluster %d tile %d" % (cluster, token_tile))
+
+
+def test_mm_cluster_larger_than_groups(opts):
+    """A cluster never gets more CTAs than the tile has groups (here K = 256: two groups)."""
+    lib = opts
+    lib.set_option(lib.OPT_CLUSTER, 8)
+    p = I.make_problem(12, 384, 256, "fp16", "u4_zp", seed=4)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "fp16"), O.mm_problem(p), "cluster capped")
+
+
+def test_grouped_cluster_split(opts):
+    lib = opts
+    lib.set_option(lib.OPT_CLUSTER, 4)
+    probs = I.make_grouped(30, 3, 256, 768, "bf16", "u4_zp", seed=21, M_list=[7, 0, 23])
+    outs = _grouped(lib, probs, "u4_zp")
+    for p, Y in zip(probs, outs):
+        if p.M:
+            assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "grouped cluster M=%d" % p.M)
 
 
 @pytest.mark.parametrize("token_tile", [16, 128])

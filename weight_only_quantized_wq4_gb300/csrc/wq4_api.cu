@@ -24,7 +24,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/wq4.h"
+#include "wq4.h"
 #include "wq4_launch.h"
 #include "wq4_params.h"
 
@@ -43,6 +43,7 @@ struct Options {
     long long timeout_cycles = 0;
     int trace = -1;
     int a_in_smem = 0;
+    int cluster = 0;          // 0 automatic, -1 never, S >= 2 force clusters of S
 };
 Options g_opt;
 
@@ -118,6 +119,7 @@ struct Plan {
     int dp_tiles = 0;
     int sk_unit_begin = 0;
     int sk_units = 0;
+    int cluster = 0;
     size_t counters_bytes = 0;
     size_t partials_bytes = 0;
     std::vector<int> m_tiles, tile_begin, unit_begin;
@@ -146,6 +148,28 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     }
     pl->total_tiles = static_cast<int>(tiles);
     if (tiles == 0) return WQ4_OK;
+
+    // Few tiles (e.g. decode-sized M): clusters of S CTAs split each tile's K range and add their
+    // partial sums through distributed shared memory (no global workspace, no atomics).
+    int min_kg = 1 << 30;
+    for (size_t p = 0; p < shapes.size(); ++p)
+        if (pl->m_tiles[p] > 0) min_kg = std::min(min_kg, shapes[p].K / kTileK);
+    int S = 0;
+    if (g_opt.cluster >= 2) {
+        S = g_opt.cluster;
+    } else if (g_opt.cluster == 0 && !g_opt.split_all && !g_opt.grid && tiles * 2 <= sm_count) {
+        S = static_cast<int>(std::min<long long>(8, sm_count / tiles));
+    }
+    S = std::min(S, min_kg);
+    if (S >= 2) {
+        if (tiles * S >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
+        pl->cluster = S;
+        pl->grid = static_cast<int>(tiles * S);
+        pl->dp_tiles = 0;
+        pl->sk_unit_begin = static_cast<int>(units);
+        pl->sk_units = 0;
+        return WQ4_OK;
+    }
 
     int C = g_opt.grid ? g_opt.grid : sm_count;
     // whole waves of tiles are processed data-parallel; the rest is K-split over all CTAs
@@ -271,6 +295,7 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
     prm->num_ctas = pl.grid;
     prm->sk_unit_begin = pl.sk_unit_begin;
     prm->sk_units = pl.sk_units;
+    prm->cluster_split = pl.cluster;
     prm->counters = pl.counters_bytes ? static_cast<int*>(workspace) : nullptr;
     prm->partials = pl.partials_bytes ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.counters_bytes)
                                       : nullptr;
@@ -279,8 +304,9 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
 
     if (trace_on()) {
         std::fprintf(stderr,
-                     "[wq4] problems=%zu token_tile=%d grid=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s ws=%zu\n",
-                     shapes.size(), pl.nt, pl.grid, pl.total_tiles, pl.dp_tiles, pl.sk_units,
+                     "[wq4] problems=%zu token_tile=%d grid=%d cluster=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s "
+                     "ws=%zu\n",
+                     shapes.size(), pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.dp_tiles, pl.sk_units,
                      g_opt.a_in_smem ? "smem" : "tmem", pl.workspace());
     }
     const cudaError_t e = dispatch(prm, MAXP > 1, pl.nt, dtype, qtype, pl.grid, st);
@@ -438,6 +464,10 @@ int wq4_set_option(int key, long long value) {
         case WQ4_OPT_A_IN_SMEM:
             g_opt.a_in_smem = value ? 1 : 0;
             return WQ4_OK;
+        case WQ4_OPT_CLUSTER:
+            if (value < -1 || value == 1 || value > 8) return WQ4_ERR_INVALID;
+            g_opt.cluster = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -450,6 +480,7 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_TIMEOUT_CYCLES: return g_opt.timeout_cycles;
         case WQ4_OPT_TRACE: return trace_on() ? 1 : 0;
         case WQ4_OPT_A_IN_SMEM: return g_opt.a_in_smem;
+        case WQ4_OPT_CLUSTER: return g_opt.cluster;
         default: return -1;
     }
 }

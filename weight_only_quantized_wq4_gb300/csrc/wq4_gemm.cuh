@@ -70,9 +70,11 @@ struct GemmCfg {
     static_assert(kTmemNeed <= 512, "tensor memory");
 };
 
+// slot: -1 whole tile, >= 0 workspace slot of a K-split part, kSlotCluster a cluster part.
 struct Seg {
     int prob, tile, nt, mt, g0, g1, slot;
 };
+constexpr int kSlotCluster = -2;
 
 template <int MAXP>
 struct Sched {
@@ -81,6 +83,7 @@ struct Sched {
     int dp_t;
     int u, u_end;
     bool first_sk;
+    bool cluster_done = false;
 
     __device__ Sched(const GemmParams<MAXP>& p, int c) : prm(p), cta(c), dp_t(c), first_sk(true) {
         u = p.sk_unit_begin + (p.sk_units * c) / p.num_ctas;
@@ -100,6 +103,23 @@ struct Sched {
     }
 
     __device__ bool next(Seg& s) {
+        if (prm.cluster_split > 0) {
+            if (cluster_done) return false;
+            cluster_done = true;
+            const int S = prm.cluster_split;
+            const int t = cta / S, q = cta % S;
+            const int p = problem_of_tile(t);
+            const ProblemDesc& P = prm.prob[p];
+            const int local = t - P.tile_begin;
+            s.prob = p;
+            s.tile = t;
+            s.mt = local / P.n_tiles;
+            s.nt = local % P.n_tiles;
+            s.g0 = (q * P.k_groups) / S;
+            s.g1 = ((q + 1) * P.k_groups) / S;
+            s.slot = kSlotCluster;
+            return true;
+        }
         if (dp_t < prm.dp_tiles) {
             const int t = dp_t;
             dp_t += prm.num_ctas;
@@ -444,11 +464,19 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             const ProblemDesc& P = prm.prob[seg.prob];
             const int n = seg.nt * kTileN + r;
             const int m0 = seg.mt * NT + col0;
+            if (seg.slot == kSlotCluster) {
+                // partial sum to this CTA's shared memory (the stages are idle now); rank 0 of the
+                // cluster adds the S partials after the cluster barrier below
+#pragma unroll
+                for (int j = 0; j < C::kNC; ++j)
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_stage0 + ((col0 + j) * 128 + r) * 4), "f"(acc[j])
+                                 : "memory");
+                continue;
+            }
             if (seg.slot >= 0) {
                 float* mine = prm.partials + static_cast<size_t>(seg.slot) * (NT * 128);
 #pragma unroll
                 for (int j = 0; j < C::kNC; ++j) mine[(col0 + j) * 128 + r] = acc[j];
-                __threadfence();
                 if (!fold_sync()) break;
                 // the units of this tile, relative to the start of the K-split region
                 const int U = prm.sk_units;
@@ -460,24 +488,44 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     int nseg = 0;
                     for (int cc = c_first; cc <= c_last; ++cc)
                         nseg += ((cc * U) / prm.num_ctas < ((cc + 1) * U) / prm.num_ctas) ? 1 : 0;
+                    // release this CTA's partial (written by all fold threads before the rendezvous
+                    // above) and, for the last arrival, acquire everyone else's
                     int* cnt = prm.counters + (seg.tile - prm.dp_tiles);
-                    const int old = atomicAdd(cnt, 1);
+                    const int old = atomic_add_acq_rel_gpu(cnt, 1);
                     const int last = (old == nseg - 1) ? 1 : 0;
-                    if (last) atomicExch(cnt, 0);
+                    if (last) st_relaxed_gpu(cnt, 0);
                     *fin_flag = last;
                 }
                 if (!fold_sync()) break;
                 if (!*fin_flag) continue;
-                __threadfence();
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                    const int start = (cc * U) / prm.num_ctas;
-                    if (start == ((cc + 1) * U) / prm.num_ctas) continue;   // empty range
-                    const int sl = 2 * cc + ((cc == c_first && start < t_u0) ? 1 : 0);
-                    const float* src = prm.partials + static_cast<size_t>(sl) * (NT * 128) + r;
+                // sum the parts in CTA order, loading kBatch parts at a time
+                constexpr int kBatch = C::kNC <= 16 ? 4 : 2;
 #pragma unroll
-                    for (int j = 0; j < C::kNC; ++j) {
-                        const float v = __ldcg(src + (col0 + j) * 128);
-                        acc[j] = (cc == c_first) ? v : acc[j] + v;
+                for (int c = 0; c < C::kNC; c += 16) {
+                    bool firstv = true;
+                    for (int cc = c_first; cc <= c_last; cc += kBatch) {
+                        float v[kBatch][16];
+                        bool use[kBatch];
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            const int c2 = cc + b;
+                            const int start = (c2 * U) / prm.num_ctas;
+                            use[b] = c2 <= c_last && start < ((c2 + 1) * U) / prm.num_ctas;
+                            if (use[b]) {
+                                const int sl = 2 * c2 + ((c2 == c_first && start < t_u0) ? 1 : 0);
+                                const float* src = prm.partials + static_cast<size_t>(sl) * (NT * 128) + r;
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[b][j] = __ldcg(src + (col0 + c + j) * 128);
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            if (use[b]) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) acc[c + j] = firstv ? v[b][j] : acc[c + j] + v[b][j];
+                                firstv = false;
+                            }
+                        }
                     }
                 }
             }
@@ -488,6 +536,49 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (m < P.M) y[static_cast<size_t>(m) * P.N + n] = float_to_out<BF16>(acc[j]);
             }
         }
+        if (prm.cluster_split > 0) {
+            cluster_sync();   // every rank's partial is in its shared memory
+            if (cluster_rank() == 0) {
+                const ProblemDesc& P = prm.prob[seg.prob];
+                const int S = prm.cluster_split;
+                const int n = seg.nt * kTileN + r;
+                const int m0 = seg.mt * NT + col0;
+                constexpr int kBatch = C::kNC <= 16 ? 4 : 2;
+                uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
+#pragma unroll
+                for (int c = 0; c < C::kNC; c += 16) {
+                    float sum[16];
+                    for (int q0 = 0; q0 < S; q0 += kBatch) {
+                        float v[kBatch][16];
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            if (q0 + b < S) {
+                                const uint32_t base = map_to_rank(s_stage0, static_cast<uint32_t>(q0 + b));
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[b][j] = ld_cluster_f32(base + ((col0 + c + j) * 128 + r) * 4);
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < kBatch; ++b) {
+                            if (q0 + b < S) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) sum[j] = (q0 + b == 0) ? v[b][j] : sum[j] + v[b][j];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m0 + c + j;
+                        if (m < P.M) y[static_cast<size_t>(m) * P.N + n] = float_to_out<BF16>(sum[j]);
+                    }
+                }
+            }
+            cluster_sync();   // no CTA leaves while rank 0 still reads its shared memory
+        }
+    }
+    if (prm.cluster_split > 0 && warp < 2 + C::kDQW) {
+        cluster_sync();
+        cluster_sync();
     }
 
     tc_fence_before();
@@ -498,14 +589,27 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     }
 }
 
-// Host-side launcher for one instantiation.
+// Host-side launcher for one instantiation (cluster = S CTAs per cluster in cluster mode, else 1).
 template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
 cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, cudaStream_t stream) {
     using C = GemmCfg<NT, ZP, ATMEM>;
     auto kern = wq4_gemm_kernel<NT, BF16, ZP, MAXP, ATMEM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cluster_split > 0 ? p.cluster_split : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

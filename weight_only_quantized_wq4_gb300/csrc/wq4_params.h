@@ -32,6 +32,9 @@ struct ProblemDesc {
 // The units (tile, group) of tiles [dp_tiles, total_tiles) are split evenly and contiguously
 // over the CTAs (CTA c takes units [floor(c U / C), floor((c+1) U / C)) counted from
 // sk_unit_begin); a tile split between CTAs is summed in the workspace in CTA order.
+// Cluster mode (few tiles, e.g. decode-sized M): the grid is tiles x S CTAs in clusters of S;
+// cluster t computes tile t, its CTA of rank q the groups [q kg / S, (q+1) kg / S), and the S
+// partial sums are added in rank order through distributed shared memory (no workspace).
 template <int MAXP>
 struct GemmParams {
     CUtensorMap xmap[MAXP];  // activations of each problem: 2-D (K, M), box (64, token tile), 128B swizzle
@@ -42,6 +45,7 @@ struct GemmParams {
     int num_ctas;
     int sk_unit_begin;
     int sk_units;            // the host keeps sk_units * num_ctas < 2^31 (32-bit index math)
+    int cluster_split;       // S > 0: cluster mode (below); 0: the data-parallel / K-split plan above
     float* partials;         // [2 * num_ctas][token tile * 128] fp32
     int* counters;           // [total_tiles - dp_tiles], zero between calls
     unsigned int* status;    // device status word (timeouts)
