@@ -1,0 +1,52 @@
+"""wq4_mm_static_scratch: the variant of wq4_mm for callers that cannot allocate device memory
+(its K-split scratch is a fixed array inside the library). Called through the C ABI, it must give
+wq4_mm's result, call after call. This file is collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import wq4_inputs as I
+from tests.wq4_testutil import from_cuda16, gpu_prepack, to_cuda16
+
+pytestmark = pytest.mark.gpu
+
+
+def _call(lib, X, blob, Y, p):
+    clib = lib.load_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return clib.wq4_mm_static_scratch(ctypes.c_void_p(X.data_ptr()), ctypes.c_void_p(blob.data_ptr()),
+                                      ctypes.c_void_p(Y.data_ptr()), p.M, p.N, p.K, 128, lib.DTYPES[p.dtype],
+                                      lib.QTYPES[p.qtype], stream)
+
+
+def test_static_scratch_matches_wq4_mm_twice(lib):
+    # 112 weight tiles on a 152-SM GPU: the plan splits tiles over CTAs, so the kernel uses scratch
+    p = I.make_problem(128, 14336, 1024, "bf16", "u4_zp", seed=2024)
+    assert lib.workspace_bytes(p.M, p.N, p.K) > 0
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, p.dtype)
+    want = O.decode16(from_cuda16(lib.mm(X, blob, p.N, qtype=p.qtype)), p.dtype)
+    for _ in range(2):
+        Y = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert _call(lib, X, blob, Y, p) == lib.OK
+        assert lib.get_last_error() == lib.OK
+        got = O.decode16(from_cuda16(Y), p.dtype)
+        st = O.check_tolerance(got, want)
+        assert st["violations"] == 0, st
+        assert O.check_tolerance(got, O.mm_problem(p))["violations"] == 0
+
+
+def test_static_scratch_rejects_plans_beyond_its_size(lib):
+    p = I.make_problem(128, 14336, 1024, "bf16", "u4_zp", seed=2025)
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, p.dtype)
+    Y = torch.empty((p.M, p.N), dtype=torch.bfloat16, device="cuda")
+    lib.set_option(lib.OPT_GRID, 4096)          # 4096 persistent CTAs need far more than the fixed array
+    try:
+        assert _call(lib, X, blob, Y, p) == lib.ERR_WORKSPACE
+    finally:
+        lib.set_option(lib.OPT_GRID, 0)
+    assert lib.get_last_error() == lib.OK

@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH):
         "wq4_mm": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_grouped_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm": (c_int, [c_int, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_mm_static_scratch": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp]),
         "wq4_get_last_error": (c_int, [vp]),
         "wq4_set_option": (c_int, [c_int, ll]),
         "wq4_get_option": (ll, [c_int]),

@@ -314,6 +314,83 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------- fixed scratch
+// For callers that may not allocate device memory: wq4_mm_static_scratch below runs wq4_mm's
+// kernels with the K-split workspace taken from this array. It is zero when the module loads;
+// every GPU that loads the library holds it until the process exits.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(24) << 20;
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+uint8_t* g_static_scratch_addr[kMaxDevices];   // device address of the array, per device
+std::mutex g_static_mu;
+
+// The plan of make_plan for a single problem, with fixed-size state only (no heap use).
+struct PlanOne {
+    int nt = 0, grid = 0, total_tiles = 0, dp_tiles = 0, sk_unit_begin = 0, sk_units = 0, cluster = 0, m_tiles = 0;
+    size_t counters_bytes = 0, partials_bytes = 0;
+};
+
+int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
+    pl->nt = g_opt.token_tile ? g_opt.token_tile : (M <= 16 ? 16 : M <= 64 ? 64 : 128);
+    pl->m_tiles = M > 0 ? (M + pl->nt - 1) / pl->nt : 0;
+    const int kg = K / kTileK;
+    const long long tiles = static_cast<long long>(pl->m_tiles) * (N / kTileN);
+    const long long units = tiles * kg;
+    if (units >= (1LL << 30) || tiles >= (1LL << 30)) return WQ4_ERR_UNSUPPORTED;
+    pl->total_tiles = static_cast<int>(tiles);
+    if (tiles == 0) return WQ4_OK;
+    int S = 0;
+    if (g_opt.cluster >= 2) {
+        S = g_opt.cluster;
+    } else if (g_opt.cluster == 0 && !g_opt.split_all && !g_opt.grid && tiles * 2 <= sm_count) {
+        S = static_cast<int>(std::min<long long>(8, sm_count / tiles));
+    }
+    S = std::min(S, kg);
+    if (S >= 2) {
+        if (tiles * S >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
+        pl->cluster = S;
+        pl->grid = static_cast<int>(tiles * S);
+        pl->sk_unit_begin = static_cast<int>(units);
+        return WQ4_OK;
+    }
+    int C = g_opt.grid ? g_opt.grid : sm_count;
+    int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
+    if (dp == tiles && !g_opt.split_all) {
+        pl->grid = C;
+        pl->dp_tiles = dp;
+        pl->sk_unit_begin = static_cast<int>(units);
+        return WQ4_OK;
+    }
+    long long sk_begin = static_cast<long long>(dp) * kg;
+    if (dp >= C && units - sk_begin < 2LL * C) {
+        dp -= C;
+        sk_begin = static_cast<long long>(dp) * kg;
+    }
+    const long long sk_units = units - sk_begin;
+    if (dp == 0 && !g_opt.grid) C = static_cast<int>(std::min<long long>(C, std::max<long long>(1, sk_units / 4)));
+    if (sk_units * static_cast<long long>(C) >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
+    pl->grid = C;
+    pl->dp_tiles = dp;
+    pl->sk_unit_begin = static_cast<int>(sk_begin);
+    pl->sk_units = static_cast<int>(sk_units);
+    pl->counters_bytes = ((static_cast<size_t>(tiles - dp) * 4) + 255) / 256 * 256;
+    pl->partials_bytes = static_cast<size_t>(2) * C * pl->nt * kTileN * 4;
+    return WQ4_OK;
+}
+
+// Device address of g_static_scratch on the current device, looked up once per device.
+int static_scratch(uint8_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ4_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return WQ4_ERR_CUDA;
+        g_static_scratch_addr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_static_scratch_addr[dev];
+    return WQ4_OK;
+}
+
 }  // namespace
 }  // namespace wq4
 
@@ -483,6 +560,60 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_CLUSTER: return g_opt.cluster;
         default: return -1;
     }
+}
+
+int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype,
+                          int qtype, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if (M < 0) return WQ4_ERR_INVALID;
+    if ((rc = check_nk(N, K))) return rc;
+    if (M == 0) return WQ4_OK;
+    if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
+    if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    uint8_t* scratch = nullptr;
+    if ((rc = static_scratch(&scratch))) return rc;
+    PlanOne pl;
+    if ((rc = make_plan_one(M, N, K, dev->sm_count, &pl))) return rc;
+    if (pl.total_tiles == 0) return WQ4_OK;
+    if (pl.counters_bytes + pl.partials_bytes > kStaticScratchBytes) {
+        if (trace_on())
+            std::fprintf(stderr, "[wq4] wq4_mm_static_scratch: needs %zu bytes of scratch, the fixed array has %zu\n",
+                         pl.counters_bytes + pl.partials_bytes, kStaticScratchBytes);
+        return WQ4_ERR_WORKSPACE;
+    }
+    GemmParams<1> prm;
+    std::memset(static_cast<void*>(&prm), 0, sizeof(prm));
+    ProblemDesc& d = prm.prob[0];
+    d.wp = static_cast<const uint8_t*>(Wp) + kBlobHeader;
+    d.y = Y;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.n_tiles = N / kTileN;
+    d.m_tiles = pl.m_tiles;
+    d.k_groups = K / kTileK;
+    if ((rc = encode_x_map(&prm.xmap[0], X, M, K, dtype, pl.nt))) return rc;
+    prm.num_problems = 1;
+    prm.total_tiles = pl.total_tiles;
+    prm.dp_tiles = pl.dp_tiles;
+    prm.num_ctas = pl.grid;
+    prm.sk_unit_begin = pl.sk_unit_begin;
+    prm.sk_units = pl.sk_units;
+    prm.cluster_split = pl.cluster;
+    prm.counters = pl.counters_bytes ? reinterpret_cast<int*>(scratch) : nullptr;
+    prm.partials = pl.partials_bytes ? reinterpret_cast<float*>(scratch + pl.counters_bytes) : nullptr;
+    prm.status = dev->status;
+    prm.timeout_cycles = timeout_cycles();
+    // the array keeps the previous call's contents: the arrival counters must start at zero
+    if (pl.counters_bytes && cudaMemsetAsync(scratch, 0, pl.counters_bytes, stream) != cudaSuccess) return WQ4_ERR_CUDA;
+    if (trace_on())
+        std::fprintf(stderr, "[wq4] static scratch: token_tile=%d grid=%d cluster=%d tiles=%d sk_units=%d scratch=%zu\n",
+                     pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.sk_units, pl.counters_bytes + pl.partials_bytes);
+    const cudaError_t e = dispatch(&prm, false, pl.nt, dtype, qtype, pl.grid, stream);
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
 }  // extern "C"
