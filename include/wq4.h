@@ -136,7 +136,7 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
 int wq4_get_last_error(wq4_stream_t stream);
 
 /* Process-wide tuning and test options (not thread-safe; set before launching):
- *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64 or 128); 0 = automatic
+ *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64, 128 or 192); 0 = automatic
  *   WQ4_OPT_GRID            force the number of persistent CTAs; 0 = automatic
  *   WQ4_OPT_SPLIT_ALL       1 = every tile goes through the K-split path (tests)
  *   WQ4_OPT_TIMEOUT_CYCLES  bound of every pipeline wait in SM clock cycles; 0 = default
@@ -146,6 +146,9 @@ int wq4_get_last_error(wq4_stream_t stream);
  *   WQ4_OPT_CLUSTER         0 = automatic, -1 = never, 2..8 = force the cluster split: each tile's
  *                           K range split over a cluster of that many CTAs whose partial sums are
  *                           added through distributed shared memory
+ *   WQ4_OPT_DECODE          0 = automatic, -1 = never, 1 = whenever the shape allows: wq4_mm with at
+ *                           most 32 tokens uses a warp-level-MMA kernel that keeps whole weight rows
+ *                           per CTA (no workspace)
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,
@@ -154,7 +157,8 @@ enum {
     WQ4_OPT_TIMEOUT_CYCLES = 4,
     WQ4_OPT_TRACE = 5,
     WQ4_OPT_A_IN_SMEM = 6,
-    WQ4_OPT_CLUSTER = 7
+    WQ4_OPT_CLUSTER = 7,
+    WQ4_OPT_DECODE = 8
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

@@ -16,7 +16,7 @@ def opts(lib):
     """Options set inside a test are reset afterwards."""
     yield lib
     for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES,
-                lib.OPT_CLUSTER):
+                lib.OPT_CLUSTER, lib.OPT_DECODE):
         lib.set_option(key, 0)
 
 
@@ -69,7 +69,7 @@ def test_mm_small(lib, M, N, K, dtype, qtype):
     assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), str((M, N, K, dtype, qtype)))
 
 
-@pytest.mark.parametrize("token_tile", [16, 64, 128])
+@pytest.mark.parametrize("token_tile", [16, 64, 128, 192])
 @pytest.mark.parametrize("grid", [0, 3, 7])
 @pytest.mark.parametrize("split_all", [0, 1])
 def test_mm_schedules(opts, token_tile, grid, split_all):
@@ -78,12 +78,12 @@ def test_mm_schedules(opts, token_tile, grid, split_all):
     lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
     lib.set_option(lib.OPT_GRID, grid)
     lib.set_option(lib.OPT_SPLIT_ALL, split_all)
-    p = I.make_problem(150, 384, 1280, "bf16", "u4_zp", seed=token_tile + grid)
+    p = I.make_problem(250, 384, 1280, "bf16", "u4_zp", seed=token_tile + grid)
     Y = gpu_mm(lib, p)
     assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "tile %d grid %d split %d" % (token_tile, grid, split_all))
 
 
-@pytest.mark.parametrize("token_tile", [16, 64, 128])
+@pytest.mark.parametrize("token_tile", [16, 64, 128, 192])
 @pytest.mark.parametrize("cluster", [2, 3, 4, 8])
 def test_mm_cluster_split(opts, token_tile, cluster):
     """Each tile's K range split over a cluster; partials added through distributed shared memory."""
@@ -92,6 +92,33 @@ def test_mm_cluster_split(opts, token_tile, cluster):
     lib.set_option(lib.OPT_CLUSTER, cluster)
     p = I.make_problem(100, 256, 1152, "bf16", "u4b8", seed=cluster * 100 + token_tile)
     assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "cluster %d tile %d" % (cluster, token_tile))
+
+
+DECODE = [
+    (1, 128, 128, "bf16", "u4b8"), (5, 256, 384, "fp16", "u4_zp"), (8, 4096, 4096, "bf16", "u4b8"),
+    (8, 384, 8960, "bf16", "u4_zp"), (9, 512, 1024, "bf16", "u4b8"), (16, 1024, 2048, "fp16", "u4b8"),
+    (17, 256, 640, "bf16", "u4_zp"), (24, 128, 1024, "fp16", "u4b8"), (32, 2048, 2048, "bf16", "u4_zp"),
+    (3, 14336, 512, "bf16", "u4b8"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,qtype", DECODE)
+def test_decode_kernel(opts, M, N, K, dtype, qtype):
+    """The warp-level-MMA kernel for at most 32 tokens (forced on)."""
+    lib = opts
+    lib.set_option(lib.OPT_DECODE, 1)
+    p = I.make_problem(M, N, K, dtype, qtype, seed=M * 13 + N + K)
+    assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "decode %s" % ((M, N, K, dtype, qtype),))
+
+
+def test_decode_kernel_deterministic(opts):
+    lib = opts
+    lib.set_option(lib.OPT_DECODE, 1)
+    p = I.make_problem(8, 2048, 4096, "bf16", "u4b8", seed=99)
+    blob = gpu_prepack(lib, p)
+    a = from_cuda16(gpu_mm(lib, p, blob))
+    b = from_cuda16(gpu_mm(lib, p, blob))
+    assert np.array_equal(a, b)
 
 
 def test_mm_cluster_larger_than_groups(opts):
@@ -112,7 +139,7 @@ def test_grouped_cluster_split(opts):
             assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "grouped cluster M=%d" % p.M)
 
 
-@pytest.mark.parametrize("token_tile", [16, 128])
+@pytest.mark.parametrize("token_tile", [16, 128, 192])
 def test_mm_a_operand_in_smem(opts, token_tile):
     lib = opts
     lib.set_option(lib.OPT_A_IN_SMEM, 1)

@@ -44,6 +44,7 @@ struct Options {
     int trace = -1;
     int a_in_smem = 0;
     int cluster = 0;          // 0 automatic, -1 never, S >= 2 force clusters of S
+    int decode = 0;           // 0 automatic, -1 never, 1 always when the shape allows it
 };
 Options g_opt;
 
@@ -130,7 +131,7 @@ int pick_token_tile(const std::vector<Shape>& shapes) {
     if (g_opt.token_tile) return g_opt.token_tile;
     int maxM = 0;
     for (const Shape& s : shapes) maxM = std::max(maxM, s.M);
-    return maxM <= 16 ? 16 : maxM <= 64 ? 64 : 128;
+    return maxM <= 16 ? 16 : maxM <= 64 ? 64 : maxM <= 128 ? 128 : 192;
 }
 
 int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
@@ -249,7 +250,8 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
     switch (nt) {
         case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, st);
         case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, st);
-        default: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, st);
+        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, st);
+        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, st);
     }
 }
 
@@ -330,7 +332,7 @@ struct PlanOne {
 };
 
 int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
-    pl->nt = g_opt.token_tile ? g_opt.token_tile : (M <= 16 ? 16 : M <= 64 ? 64 : 128);
+    pl->nt = g_opt.token_tile ? g_opt.token_tile : (M <= 16 ? 16 : M <= 64 ? 64 : M <= 128 ? 128 : 192);
     pl->m_tiles = M > 0 ? (M + pl->nt - 1) / pl->nt : 0;
     const int kg = K / kTileK;
     const long long tiles = static_cast<long long>(pl->m_tiles) * (N / kTileN);
@@ -475,6 +477,23 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
     if (M == 0) return WQ4_OK;
     if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
+    // decode-sized M: the warp-level MMA kernel (whole row blocks per CTA, no workspace)
+    const bool decode_ok = decode_fits(M, K);
+    const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
+                             !g_opt.cluster && !g_opt.a_in_smem;
+    if (decode_ok && (g_opt.decode == 1 || auto_decode)) {
+        DeviceInfo* dev = nullptr;
+        if ((rc = device_info(&dev))) return rc;
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return WQ4_ERR_CUDA;
+        int grid = 0, rb = 0;
+        const cudaError_t e = launch_decode(X, Wp, Y, M, N, K, dtype, qtype, dev->sm_count, dev->status,
+                                            timeout_cycles(), reinterpret_cast<void*>(fn), &grid, &rb, stream);
+        if (trace_on())
+            std::fprintf(stderr, "[wq4] decode kernel: M=%d N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n", M, N, K,
+                         grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+        return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+    }
     std::vector<Shape> shapes{{M, N, K}};
     const void* xs[1] = {X};
     const void* ws[1] = {Wp};
@@ -521,7 +540,7 @@ int wq4_get_last_error(wq4_stream_t stream) {
 int wq4_set_option(int key, long long value) {
     switch (key) {
         case WQ4_OPT_TOKEN_TILE:
-            if (value != 0 && value != 16 && value != 64 && value != 128) return WQ4_ERR_INVALID;
+            if (value != 0 && value != 16 && value != 64 && value != 128 && value != 192) return WQ4_ERR_INVALID;
             g_opt.token_tile = static_cast<int>(value);
             return WQ4_OK;
         case WQ4_OPT_GRID:
@@ -545,6 +564,10 @@ int wq4_set_option(int key, long long value) {
             if (value < -1 || value == 1 || value > 8) return WQ4_ERR_INVALID;
             g_opt.cluster = static_cast<int>(value);
             return WQ4_OK;
+        case WQ4_OPT_DECODE:
+            if (value < -1 || value > 1) return WQ4_ERR_INVALID;
+            g_opt.decode = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -558,6 +581,7 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_TRACE: return trace_on() ? 1 : 0;
         case WQ4_OPT_A_IN_SMEM: return g_opt.a_in_smem;
         case WQ4_OPT_CLUSTER: return g_opt.cluster;
+        case WQ4_OPT_DECODE: return g_opt.decode;
         default: return -1;
     }
 }

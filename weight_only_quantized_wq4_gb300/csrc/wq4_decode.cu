@@ -1,0 +1,365 @@
+// W4A16 GEMM for decode-sized M (at most 32 tokens), sm_103a.
+//
+// At a few tokens the tensor core's per-instruction floor decides: a tcgen05.mma with M = 128
+// costs the same ~78 cycles for any N up to 128, so 8 tokens (padded to N = 16) use a few percent
+// of it, while mma.sync m16n8k16 takes exactly 8 tokens as its N and sustains ~1000 FMA/clk/SM.
+// This kernel therefore keeps the pages' register-sourced design ("machete_mainloop.cuh",
+// header comment and transform_A_kblock: the narrow weight is the MMA's A operand, up-converted
+// in registers right before the MMA) on the warp-level MMA:
+//
+//   * each CTA owns RB blocks of 16 weight rows over all of K, so no partial sum leaves the CTA;
+//     its warps split K (slice ks takes groups ks, ks + KS, ...) and add their parts through
+//     shared memory in slice order (deterministic);
+//   * every warp streams its own weight pieces (16-byte cp.async from the prepacked records) into
+//     a private ring of DEPTH group stages; the activations arrive once per CTA through one 3-D
+//     tensor copy (K/64 panels x Mpad token rows x 128 B, 128-byte swizzle, rows past M zero);
+//   * lane (g, c) of a warp reads word c of each 32-element chunk of rows g and g + 8; the k order
+//     inside a chunk is permuted identically for A and B (slot 2c + t and 2c + 8 + t of k-step h
+//     hold elements 8c + 4h + t and 8c + 4h + 2 + t), so a lane's B fragments for the chunk's two
+//     k-steps are one 16-byte shared load;
+//   * per group: P = sum over the group's 128 K of (q - z) x (exact integer operands, fp32
+//     accumulate), then acc += s[row, group] * P in fp32 (the group scale, as in the tcgen05 path).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "wq4_device.cuh"
+#include "wq4_params.h"
+
+namespace wq4 {
+
+struct DecodeParams {
+    CUtensorMap xmap;        // 3-D (64, M, K/64), strides (2K, 128) bytes, box (64, Mpad, K/64)
+    const uint8_t* wp;       // first tile record
+    void* y;                 // [M][N]
+    int M, N, K;
+    int k_groups;
+    int n_blocks;            // N / 16
+    int rb;                  // row blocks per CTA
+    unsigned int* status;
+    long long timeout_cycles;
+};
+
+constexpr int kDecWarps = 16;
+constexpr int kDecDepth = 4;                                  // group stages per warp
+constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, zero points
+constexpr int kDecMaxX = 140 * 1024;                          // activation bytes held per CTA
+
+template <int NB>
+struct DecCfg {
+    static constexpr int kMpad = 8 * NB;
+    static constexpr int kRedBytes = kDecWarps * NB * 32 * 16;  // per-warp partials for the final sum
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t dec_sub2(uint32_t a, uint32_t b) {
+    if constexpr (BF16) {
+        __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    } else {
+        __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+template <int NB, bool BF16, bool ZP>
+__global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
+    using C = DecCfg<NB>;
+    constexpr int kRec = tile_record_bytes(ZP);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+    const int x_bytes = C::kMpad * prm.K * 2;
+    const uint32_t s_x = sbase;                                       // activations (swizzled panels)
+    const uint32_t s_w = sbase + ((x_bytes + 127) & ~127);            // per-warp stage rings
+    const uint32_t s_red = s_w + kDecWarps * kDecDepth * kDecStage;   // slice partials
+    const uint32_t s_bar = s_red + C::kRedBytes;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (s_bar + 8 - raw_s));
+    const uint8_t* const sm = smem_raw + (sbase - raw_s);              // generic view of the aligned base
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int KS = kDecWarps / prm.rb;                                // K slices
+    const int bl = warp % prm.rb, ks = warp / prm.rb;
+    const int block = blockIdx.x * prm.rb + bl;                       // 16-row block of this warp
+    const bool active = (ks < KS) && block < prm.n_blocks;
+
+    if (threadIdx.x == 0) {
+        mbar_init(s_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&prm.xmap);
+        mbar_arrive_expect_tx(s_bar, static_cast<uint32_t>(x_bytes));
+        tma_load_3d(s_x, &prm.xmap, s_bar, 0, 0, 0);
+    }
+
+    float acc[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nb][i] = 0.f;
+
+    // this warp's groups: ks, ks + KS, ...
+    const int n_my = active ? (prm.k_groups - ks + KS - 1) / KS : 0;
+    const int nt = block >> 3, rblk = (block & 7) * 16;               // n-tile and first row inside it
+    const uint32_t my_ring = s_w + warp * (kDecDepth * kDecStage);
+    // per-lane constants of the copy pattern: this lane moves code pieces lane and lane + 32
+    // (piece = chunk j * 16 + row), lanes 0..1 the two 16-byte halves of the scales, lane 2 the
+    // eight bytes of zero points; a group's record advances by KS records per step
+    const size_t rec_step = static_cast<size_t>(KS) * kRec;
+    const uint8_t* rec_next = prm.wp + (static_cast<size_t>(nt) * prm.k_groups + ks) * kRec;
+    const uint32_t goff0 = ((lane >> 4) * 128 + rblk + (lane & 15)) * 16;
+    const uint32_t goff1 = (((lane + 32) >> 4) * 128 + rblk + (lane & 15)) * 16;
+    const uint32_t soff_side = lane < 2 ? 1024 + lane * 16 : 1056;
+    const uint32_t goff_side = lane < 2 ? 8192 + 2 * rblk + lane * 16 : 8448 + rblk / 2;
+    auto issue = [&](int slot) {
+        const uint32_t st = my_ring + slot * kDecStage;
+        cp_async16(st + lane * 16, rec_next + goff0);
+        cp_async16(st + lane * 16 + 512, rec_next + goff1);
+        if (lane < 2) cp_async16(st + soff_side, rec_next + goff_side);
+        if constexpr (ZP) {
+            if (lane == 2) cp_async8(st + soff_side, rec_next + goff_side);
+        }
+        rec_next += rec_step;
+    };
+    const int pre = n_my < kDecDepth ? n_my : kDecDepth;
+    for (int i = 0; i < kDecDepth; ++i) {
+        if (i < pre) issue(i);
+        cp_async_commit();                                            // empty groups keep the count uniform
+    }
+
+    // activations have landed (bounded wait)
+    const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
+    const bool x_ok = mbar_wait(s_bar, 0, ctl);
+
+    // activation addresses: token row m = 8 nb + g sits at 128-byte row (panel * Mpad + m) whose
+    // swizzle key is (row & 7) = g; the lane's 16-byte chunk in a panel is (4 (j & 1) + c) ^ g
+    const uint32_t xo_even = g * 128 + ((c ^ g) << 4);
+    const uint32_t xo_odd = g * 128 + (((4 + c) ^ g) << 4);
+    const uint32_t x_grp_step = static_cast<uint32_t>(KS) * 2 * C::kMpad * 128;
+    uint32_t x_grp = s_x + static_cast<uint32_t>(ks) * 2 * C::kMpad * 128;
+    const uint32_t a_off = g * 16 + 4 * c;                            // word c of row g in a chunk
+
+    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
+    for (int i = 0; i < n_my && x_ok; ++i) {
+        cp_async_wait<kDecDepth - 1>();
+        __syncwarp();
+        const int slot = i & (kDecDepth - 1);
+        const uint32_t st = my_ring + slot * kDecStage;
+        uint32_t sub_lo, sub_hi;                                      // 128 + z (bf16) per row
+        const uint8_t* const stp = sm + (st - sbase);
+        if constexpr (ZP) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(stp + 1056);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(stp + 1060);
+            const uint32_t z0 = (w0 >> (g * 4)) & 0xFu, z1 = (w1 >> (g * 4)) & 0xFu;
+            sub_lo = ((BF16 ? 0x4300u : 0x6400u) | z0) * 0x10001u;
+            sub_hi = ((BF16 ? 0x4300u : 0x6400u) | z1) * 0x10001u;
+        } else {
+            sub_lo = sub_hi = BF16 ? 0x43084308u : 0x64086408u;
+        }
+        const uint8_t* const a_base = stp + a_off;
+        const uint8_t* const xe = sm + (x_grp - sbase) + xo_even;
+        const uint8_t* const xd = sm + (x_grp - sbase) + xo_odd;
+        float p[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) p[nb][t] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // word c of rows g and g + 8
+            const uint32_t wlo = *reinterpret_cast<const uint32_t*>(a_base + j * 256);
+            const uint32_t whi = *reinterpret_cast<const uint32_t*>(a_base + j * 256 + 128);
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                lo[e] = dec_sub2<BF16>(((wlo >> (4 * e)) & 0x000F000Fu) | kMagic, sub_lo);
+                hi[e] = dec_sub2<BF16>(((whi >> (4 * e)) & 0x000F000Fu) | kMagic, sub_hi);
+            }
+            const uint32_t a0[4] = {lo[0], hi[0], lo[1], hi[1]};
+            const uint32_t a1[4] = {lo[2], hi[2], lo[3], hi[3]};
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const uint4 xb = *reinterpret_cast<const uint4*>(((j & 1) ? xd : xe) +
+                                                                 (j >> 1) * C::kMpad * 128 + nb * 8 * 128);
+                mma16816<BF16>(p[nb], a0, xb.x, xb.y);
+                mma16816<BF16>(p[nb], a1, xb.z, xb.w);
+            }
+        }
+        x_grp += x_grp_step;
+        // group scale (rows g and g + 8), then release the stage and fetch the group DEPTH ahead
+        const uint32_t sbits_lo = *reinterpret_cast<const uint16_t*>(stp + 1024 + 2 * g);
+        const uint32_t sbits_hi = *reinterpret_cast<const uint16_t*>(stp + 1040 + 2 * g);
+        float s_lo, s_hi;
+        if constexpr (BF16) {
+            s_lo = __uint_as_float(sbits_lo << 16);
+            s_hi = __uint_as_float(sbits_hi << 16);
+        } else {
+            s_lo = __half2float(__ushort_as_half(static_cast<uint16_t>(sbits_lo)));
+            s_hi = __half2float(__ushort_as_half(static_cast<uint16_t>(sbits_hi)));
+        }
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            acc[nb][0] = fmaf(s_lo, p[nb][0], acc[nb][0]);
+            acc[nb][1] = fmaf(s_lo, p[nb][1], acc[nb][1]);
+            acc[nb][2] = fmaf(s_hi, p[nb][2], acc[nb][2]);
+            acc[nb][3] = fmaf(s_hi, p[nb][3], acc[nb][3]);
+        }
+        __syncwarp();
+        if (i + kDecDepth < n_my) issue(slot);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // slice partials -> shared memory, then slice 0 adds them in slice order and writes Y
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+        sts128(s_red + ((warp * NB + nb) * 32 + lane) * 16, __float_as_uint(acc[nb][0]), __float_as_uint(acc[nb][1]),
+               __float_as_uint(acc[nb][2]), __float_as_uint(acc[nb][3]));
+    __syncthreads();
+    if (active && ks == 0) {
+        uint16_t* y = reinterpret_cast<uint16_t*>(prm.y);
+        const int n0 = block * 16 + g;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int s = 0; s < KS; ++s) {
+                const uint4 q = lds128(s_red + (((s * prm.rb + bl) * NB + nb) * 32 + lane) * 16);
+                v[0] += __uint_as_float(q.x);
+                v[1] += __uint_as_float(q.y);
+                v[2] += __uint_as_float(q.z);
+                v[3] += __uint_as_float(q.w);
+            }
+            // fragment: (row g, tokens 2c, 2c+1), (row g + 8, tokens 2c, 2c+1)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int m = nb * 8 + 2 * c + (t & 1);
+                const int n = n0 + (t >> 1) * 8;
+                if (m < prm.M) {
+                    uint16_t o;
+                    if constexpr (BF16) {
+                        o = __bfloat16_as_ushort(__float2bfloat16_rn(v[t]));
+                    } else {
+                        o = __half_as_ushort(__float2half_rn(v[t]));
+                    }
+                    y[static_cast<size_t>(m) * prm.N + n] = o;
+                }
+            }
+        }
+    }
+}
+
+int decode_smem_bytes(int nb, int K) {
+    const int mpad = 8 * nb;
+    const int x = (mpad * K * 2 + 127) & ~127;
+    return 1024 + x + kDecWarps * kDecDepth * kDecStage + kDecWarps * nb * 32 * 16 + 64;
+}
+
+bool decode_fits(int M, int K) {
+    if (M < 1 || M > 32 || K / 64 > 256) return false;
+    const int nb = (M + 7) / 8;
+    const int mpad = 8 * (nb == 3 ? 4 : nb);
+    return mpad * K * 2 <= kDecMaxX && decode_smem_bytes(mpad / 8, K) <= 232448;
+}
+
+template <int NB, bool BF16, bool ZP>
+static cudaError_t go_decode(const DecodeParams& p, int grid, cudaStream_t st) {
+    auto kern = wq4_decode_kernel<NB, BF16, ZP>;
+    const int smem = decode_smem_bytes(NB, p.K);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kDecWarps * 32, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int NB>
+static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int grid, cudaStream_t st) {
+    if (bf16) return zp ? go_decode<NB, true, true>(p, grid, st) : go_decode<NB, true, false>(p, grid, st);
+    return zp ? go_decode<NB, false, true>(p, grid, st) : go_decode<NB, false, false>(p, grid, st);
+}
+
+// Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
+cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
+                          int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
+                          int* grid_out, int* rb_out, cudaStream_t st) {
+    using Enc = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    int nb = (M + 7) / 8;
+    if (nb == 3) nb = 4;
+    DecodeParams p;
+    std::memset(static_cast<void*>(&p), 0, sizeof(p));
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(8 * nb), static_cast<cuuint32_t>(K / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = reinterpret_cast<Enc>(encode_fn_ptr)(
+        &p.xmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+        const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    p.wp = static_cast<const uint8_t*>(Wp) + kBlobHeader;
+    p.y = Y;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.k_groups = K / kTileK;
+    p.n_blocks = N / 16;
+    // fewest row blocks per CTA that keeps the grid within one wave; each CTA's warps split K
+    int rb = (p.n_blocks + sm_count - 1) / sm_count;
+    while (kDecWarps % rb) ++rb;                                      // whole K slices per block
+    if (rb > kDecWarps) rb = kDecWarps;
+    p.rb = rb;
+    p.status = status;
+    p.timeout_cycles = timeout_cycles;
+    const int grid = (p.n_blocks + rb - 1) / rb;
+    *grid_out = grid;
+    *rb_out = rb;
+    const bool bf16 = dtype == 0, zp = qtype == 1;
+    switch (nb) {
+        case 1: return pick_decode<1>(p, bf16, zp, grid, st);
+        case 2: return pick_decode<2>(p, bf16, zp, grid, st);
+        default: return pick_decode<4>(p, bf16, zp, grid, st);
+    }
+}
+
+}  // namespace wq4

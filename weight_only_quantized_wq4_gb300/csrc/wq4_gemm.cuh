@@ -40,10 +40,20 @@ namespace wq4 {
 
 template <int NT, bool ZP, bool ATMEM>
 struct GemmCfg {
-    static_assert(NT == 16 || NT == 64 || NT == 128, "token tile");
+    static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 192, "token tile");
+    // Four warpgroups: WG0 = TMA warp, MMA warp and two idle warps; then the dequant warps; then
+    // the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
     static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
     static constexpr int kFW = NT <= 64 ? 4 : 8;             // fold / epilogue warps
-    static constexpr int kWarps = 2 + kDQW + kFW;             // warp 0 TMA, warp 1 MMA, then the rest
+    static constexpr int kWarps = 4 + kDQW + kFW;
+    // With wide token tiles the fold warps hold 64..96 fp32 accumulators each: registers move
+    // to them from the other warpgroups (setmaxnreg). Launched with 128 per thread, the split
+    // (128 x 56 + 128 x 96 + 256 x 176 = 64512 for NT >= 128; 128 x 56 + 256 x 96 + 128 x 200 =
+    // 57344 for NT = 64) stays within the 512 x 128 = 65536 launched.
+    static constexpr bool kRegSplit = NT >= 64;
+    static constexpr int kRegWg0 = 56, kRegDequant = 96, kRegFold = NT == 64 ? 200 : 176;
+    static_assert(!kRegSplit || (128 * kRegWg0 + 32 * kDQW * kRegDequant + 32 * kFW * kRegFold <= kWarps * 32 * 128),
+                  "register split exceeds the launched registers");
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kKParts = kDQW / 4;                 // dequant warps per TMEM lane quarter
     static constexpr int kChunks = 4 / kKParts;              // 32-element K chunks per dequant thread
@@ -203,6 +213,16 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
     }
 }
 
+// (d0, d1) += a * (b0, b1) with one packed fp32 FMA (fma.rn.f32x2).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a, uint32_t b0, uint32_t b1) {
+    uint64_t d, bb, cc, aa;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(bb) : "r"(b0), "r"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(cc) : "f"(d0), "f"(d1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(aa) : "f"(a));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(aa), "l"(bb), "l"(cc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
 __device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -271,6 +291,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
 
+    if (warp < 4) {
+        if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegWg0));
+    }
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -344,11 +367,13 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             mbar_wait_plain(drain_bar, 0, prm.timeout_cycles);
         }
         __syncwarp();
-    } else if (warp < 2 + C::kDQW) {
+    } else if (warp < 4) {
+        // idle warps of the first warpgroup
+    } else if (warp < 4 + C::kDQW) {
         // ------------------------------------------------------------------ dequant
-        // Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
+        if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegDequant));
         const int q4 = warp & 3;
-        const int part = (warp - 2) >> 2;
+        const int part = (warp - 4) >> 2;
         const int r = 32 * q4 + lane;
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
@@ -408,7 +433,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
     } else {
         // ------------------------------------------------------------------ fold + epilogue
-        const int f = warp - 2 - C::kDQW;
+        if constexpr (C::kRegSplit) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegFold));
+        const int f = warp - 4 - C::kDQW;
         const int q4 = warp & 3;
         const int col0 = (f >> 2) * C::kNC;
         const int r = 32 * q4 + lane;
@@ -439,17 +465,17 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 uint32_t sbits;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + 8192 + 2 * r));
                 const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
-                const bool first = (g == seg.g0);
+                if (g == seg.g0) {
+#pragma unroll
+                    for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
+                }
 #pragma unroll
                 for (int c = 0; c < C::kNC; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(t_lane + b * NT + col0 + c, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float pv = __uint_as_float(v[j]);
-                        acc[c + j] = first ? sc * pv : fmaf(sc, pv, acc[c + j]);
-                    }
+                    for (int j = 0; j < 16; j += 2) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -576,7 +602,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             cluster_sync();   // no CTA leaves while rank 0 still reads its shared memory
         }
     }
-    if (prm.cluster_split > 0 && warp < 2 + C::kDQW) {
+    if (prm.cluster_split > 0 && warp < 4 + C::kDQW) {
         cluster_sync();
         cluster_sync();
     }
@@ -594,6 +620,17 @@ template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
 cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, cudaStream_t stream) {
     using C = GemmCfg<NT, ZP, ATMEM>;
     auto kern = wq4_gemm_kernel<NT, BF16, ZP, MAXP, ATMEM>;
+    if constexpr (C::kRegSplit) {
+        // The register split assumes 128 registers per thread at launch; a build that launched
+        // with fewer would leave the fold warps' setmaxnreg.inc waiting forever. Refuse it.
+        static int launch_regs = -1;
+        if (launch_regs < 0) {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return cudaErrorInvalidDeviceFunction;
+            launch_regs = fa.numRegs;
+        }
+        if (launch_regs != 128) return cudaErrorInvalidConfiguration;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

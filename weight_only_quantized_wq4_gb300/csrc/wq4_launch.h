@@ -14,6 +14,14 @@ cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, bool z
                              cudaStream_t st);
 cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
                               cudaStream_t st);
+cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+                              cudaStream_t st);
+
+// Decode-sized M (<= 32 tokens): warp-level MMA kernel, no workspace.
+bool decode_fits(int M, int K);
+cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
+                          int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
+                          int* grid_out, int* rb_out, cudaStream_t st);
 
 cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K,
                            int dtype, int qtype, void* blob, cudaStream_t st);

@@ -13,7 +13,7 @@ constexpr int kMaxGroupedProblems = 64;
 
 // Bytes of one (128-row, 128-K) record of the prepacked blob: 8192 B of codes, 256 B of
 // scales, 64 B of zero points in zero-point mode, padded to 128 B.
-constexpr int tile_record_bytes(bool zp) { return zp ? 8576 : 8448; }
+__host__ __device__ constexpr int tile_record_bytes(bool zp) { return zp ? 8576 : 8448; }
 
 struct ProblemDesc {
     const uint8_t* wp;       // first tile record (blob + kBlobHeader)
