@@ -41,15 +41,21 @@ struct DecodeParams {
     long long timeout_cycles;
 };
 
-constexpr int kDecWarps = 16;
-constexpr int kDecDepth = 4;                                  // group stages per warp
 constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, zero points
 constexpr int kDecMaxX = 140 * 1024;                          // activation bytes held per CTA
+
+// warps per CTA: more warps hide the MMA and shared-memory latencies; with one token block a
+// thread needs few registers, so 32 warps fit
+__host__ __device__ constexpr int dec_warps(int nb) { return nb == 1 ? 32 : 16; }
+// group stages per warp (with 32 warps two stages already keep 64 groups in flight per CTA)
+__host__ __device__ constexpr int dec_depth(int nb) { return nb == 1 ? 2 : 4; }
 
 template <int NB>
 struct DecCfg {
     static constexpr int kMpad = 8 * NB;
-    static constexpr int kRedBytes = kDecWarps * NB * 32 * 16;  // per-warp partials for the final sum
+    static constexpr int kWarps = dec_warps(NB);
+    static constexpr int kDepth = dec_depth(NB);
+    static constexpr int kRedBytes = kWarps * NB * 32 * 16;     // per-warp partials for the final sum
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -72,13 +78,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t dec_sub2(uint32_t a, uint32_t b) {
+    // packed 16-bit subtraction on the raw 32-bit registers (no pair-struct round trip)
+    uint32_t d;
     if constexpr (BF16) {
-        __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     } else {
-        __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     }
+    return d;
 }
 
 template <bool BF16>
@@ -99,23 +106,24 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 template <int NB, bool BF16, bool ZP>
-__global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
+__global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
     using C = DecCfg<NB>;
     constexpr int kRec = tile_record_bytes(ZP);
+    constexpr int kDecDepth = C::kDepth;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
     const int x_bytes = C::kMpad * prm.K * 2;
     const uint32_t s_x = sbase;                                       // activations (swizzled panels)
     const uint32_t s_w = sbase + ((x_bytes + 127) & ~127);            // per-warp stage rings
-    const uint32_t s_red = s_w + kDecWarps * kDecDepth * kDecStage;   // slice partials
+    const uint32_t s_red = s_w + C::kWarps * kDecDepth * kDecStage;   // slice partials
     const uint32_t s_bar = s_red + C::kRedBytes;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (s_bar + 8 - raw_s));
     const uint8_t* const sm = smem_raw + (sbase - raw_s);              // generic view of the aligned base
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int KS = kDecWarps / prm.rb;                                // K slices
+    const int KS = C::kWarps / prm.rb;                                // K slices
     const int bl = warp % prm.rb, ks = warp / prm.rb;
     const int block = blockIdx.x * prm.rb + bl;                       // 16-row block of this warp
     const bool active = (ks < KS) && block < prm.n_blocks;
@@ -126,11 +134,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&prm.xmap);
-        mbar_arrive_expect_tx(s_bar, static_cast<uint32_t>(x_bytes));
-        tma_load_3d(s_x, &prm.xmap, s_bar, 0, 0, 0);
-    }
+    // Programmatic dependent launch: the next kernel on the stream may begin its own prologue and
+    // weight prefetch now; this one waits for its predecessor before touching activations or
+    // outputs (griddepcontrol is a no-op when the launch carries no programmatic dependency).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) prefetch_tensormap(&prm.xmap);
 
     float acc[NB][4];
 #pragma unroll
@@ -166,6 +174,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
         if (i < pre) issue(i);
         cp_async_commit();                                            // empty groups keep the count uniform
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(s_bar, static_cast<uint32_t>(x_bytes));
+        tma_load_3d(s_x, &prm.xmap, s_bar, 0, 0, 0);
+    }
 
     // activations have landed (bounded wait)
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
@@ -199,11 +212,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
         const uint8_t* const a_base = stp + a_off;
         const uint8_t* const xe = sm + (x_grp - sbase) + xo_even;
         const uint8_t* const xd = sm + (x_grp - sbase) + xo_odd;
-        float p[NB][4];
+        float p[NB][4], p2[NB][4];                                    // two chains: even / odd chunks
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int t = 0; t < 4; ++t) p[nb][t] = 0.f;
+            for (int t = 0; t < 4; ++t) p[nb][t] = p2[nb][t] = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             // word c of rows g and g + 8
@@ -221,8 +234,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
             for (int nb = 0; nb < NB; ++nb) {
                 const uint4 xb = *reinterpret_cast<const uint4*>(((j & 1) ? xd : xe) +
                                                                  (j >> 1) * C::kMpad * 128 + nb * 8 * 128);
-                mma16816<BF16>(p[nb], a0, xb.x, xb.y);
-                mma16816<BF16>(p[nb], a1, xb.z, xb.w);
+                if (j & 1) {
+                    mma16816<BF16>(p2[nb], a0, xb.x, xb.y);
+                    mma16816<BF16>(p2[nb], a1, xb.z, xb.w);
+                } else {
+                    mma16816<BF16>(p[nb], a0, xb.x, xb.y);
+                    mma16816<BF16>(p[nb], a1, xb.z, xb.w);
+                }
             }
         }
         x_grp += x_grp_step;
@@ -239,10 +257,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
         }
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-            acc[nb][0] = fmaf(s_lo, p[nb][0], acc[nb][0]);
-            acc[nb][1] = fmaf(s_lo, p[nb][1], acc[nb][1]);
-            acc[nb][2] = fmaf(s_hi, p[nb][2], acc[nb][2]);
-            acc[nb][3] = fmaf(s_hi, p[nb][3], acc[nb][3]);
+            acc[nb][0] = fmaf(s_lo, p[nb][0] + p2[nb][0], acc[nb][0]);
+            acc[nb][1] = fmaf(s_lo, p[nb][1] + p2[nb][1], acc[nb][1]);
+            acc[nb][2] = fmaf(s_hi, p[nb][2] + p2[nb][2], acc[nb][2]);
+            acc[nb][3] = fmaf(s_hi, p[nb][3] + p2[nb][3], acc[nb][3]);
         }
         __syncwarp();
         if (i + kDecDepth < n_my) issue(slot);
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) wq4_decode_kernel(const __g
 int decode_smem_bytes(int nb, int K) {
     const int mpad = 8 * nb;
     const int x = (mpad * K * 2 + 127) & ~127;
-    return 1024 + x + kDecWarps * kDecDepth * kDecStage + kDecWarps * nb * 32 * 16 + 64;
+    return 1024 + x + dec_warps(nb) * dec_depth(nb) * kDecStage + dec_warps(nb) * nb * 32 * 16 + 64;
 }
 
 bool decode_fits(int M, int K) {
@@ -307,7 +325,18 @@ static cudaError_t go_decode(const DecodeParams& p, int grid, cudaStream_t st) {
     const int smem = decode_smem_bytes(NB, p.K);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecWarps * 32, smem, st>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(dec_warps(NB) * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -345,9 +374,10 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     p.k_groups = K / kTileK;
     p.n_blocks = N / 16;
     // fewest row blocks per CTA that keeps the grid within one wave; each CTA's warps split K
+    const int warps = dec_warps(nb);
     int rb = (p.n_blocks + sm_count - 1) / sm_count;
-    while (kDecWarps % rb) ++rb;                                      // whole K slices per block
-    if (rb > kDecWarps) rb = kDecWarps;
+    while (warps % rb) ++rb;                                          // whole K slices per block
+    if (rb > warps) rb = warps;
     p.rb = rb;
     p.status = status;
     p.timeout_cycles = timeout_cycles;

@@ -60,22 +60,30 @@ struct GemmCfg {
     static constexpr int kColParts = kFW / 4;                // fold warps per TMEM lane quarter
     static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
     static constexpr int kRec = tile_record_bytes(ZP);
-    static constexpr int kRecAlloc = (kRec + 1023) / 1024 * 1024;
     static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
-    static constexpr int kStageBytes = 2 * kXPanel + kRecAlloc;
+    // Two rings: activation tiles (two panels per group; consumed by the MMA, released by its
+    // commit) and weight records (codes + scales + zeros; released once the dequant warps and
+    // the fold warps are done with them). The weight ring is deep so that dequantisation can run
+    // ahead of the MMA; the activation ring only has to cover the copy latency.
+    static constexpr int kXStageBytes = 2 * kXPanel;
+    static constexpr int kWStageBytes = (kRec + 127) / 128 * 128;
     static constexpr int kABuf = 128 * 128 * 2;              // one 128 x 128 16-bit operand tile
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
-    static constexpr int kBarBytes = 512;
+    static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
-    static constexpr int kStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kABytes + kBarBytes;
-    static constexpr uint32_t kTxBytes = kRec + 2 * kXPanel;
+    static constexpr int kWStages = NT <= 16 ? 16 : (ATMEM ? 8 : 6);
+    // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
+    static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
+    static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kWRingBytes) / kXStageBytes;
+    static constexpr int kXStages = kXStagesFit > 16 ? 16 : kXStagesFit;
+    static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
     static constexpr int kColA = 2 * NT;                     // TMEM column of A buffer 0
     static constexpr int kTmemNeed = 2 * NT + (ATMEM ? 128 : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
-    static_assert(kStages >= 2, "shared memory");
+    static_assert(kXStages >= 2 && kWStages <= 16, "shared memory");
+    static_assert(kXStageBytes % 1024 == 0 && kWRingBytes % 1024 == 0, "1024-byte aligned operand tiles");
+    static_assert(kXStages * kXStageBytes >= NT * 128 * 4, "cluster reduction buffer");
     static_assert(kSmemBytes <= kMaxDynSmem, "shared memory");
     static_assert(kTmemNeed <= 512, "tensor memory");
 };
@@ -176,13 +184,14 @@ __device__ __forceinline__ int sk_cta_of(int v, int U, int C) {
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
+    // packed 16-bit subtraction on the raw 32-bit registers (no pair-struct round trip)
+    uint32_t d;
     if constexpr (BF16) {
-        __nv_bfloat162 r = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     } else {
-        __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     }
+    return d;
 }
 
 // Two codes (in bits [0,4) and [16,20) of `w`) to two exact 16-bit integers code - zero.
@@ -240,18 +249,22 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (sbase - raw_s);
 
-    const uint32_t s_stage0 = sbase;
-    const uint32_t s_A = sbase + C::kStages * C::kStageBytes;
+    const uint32_t s_x0 = sbase;                                         // activation ring
+    const uint32_t s_w0 = s_x0 + C::kXStages * C::kXStageBytes;           // weight-record ring
+    const uint32_t s_A = s_w0 + C::kWRingBytes;
     const uint32_t s_bar = s_A + C::kABytes;
-    auto full_bar = [&](int s) { return s_bar + 8u * s; };
-    auto empty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
-    auto afull_bar = [&](int b) { return s_bar + 8u * (32 + b); };
-    auto aempty_bar = [&](int b) { return s_bar + 8u * (34 + b); };
-    auto pfull_bar = [&](int b) { return s_bar + 8u * (36 + b); };
-    auto pempty_bar = [&](int b) { return s_bar + 8u * (38 + b); };
-    const uint32_t drain_bar = s_bar + 8u * 40;
-    const uint32_t fsync_bar = s_bar + 8u * 41;   // fold warps meet here in the split epilogue
-    uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 48;
+    auto xfull_bar = [&](int s) { return s_bar + 8u * s; };
+    auto xempty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
+    auto wfull_bar = [&](int s) { return s_bar + 8u * (32 + s); };
+    auto wempty_bar = [&](int s) { return s_bar + 8u * (48 + s); };
+    auto afull_bar = [&](int b) { return s_bar + 8u * (64 + b); };
+    auto aempty_bar = [&](int b) { return s_bar + 8u * (66 + b); };
+    auto pfull_bar = [&](int b) { return s_bar + 8u * (68 + b); };
+    auto pempty_bar = [&](int b) { return s_bar + 8u * (70 + b); };
+    auto wrec_of = [&](int i) { return s_w0 + (i % C::kWStages) * C::kWStageBytes; };
+    const uint32_t drain_bar = s_bar + 8u * 72;
+    const uint32_t fsync_bar = s_bar + 8u * 73;   // fold warps meet here in the split epilogue
+    uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 80;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
     volatile int* const fin_flag = reinterpret_cast<volatile int*>(gmisc + 8);
@@ -260,9 +273,13 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), C::kDQW + 1 + C::kFW);
+        for (int s = 0; s < C::kXStages; ++s) {
+            mbar_init(xfull_bar(s), 1);
+            mbar_init(xempty_bar(s), 1);
+        }
+        for (int s = 0; s < C::kWStages; ++s) {
+            mbar_init(wfull_bar(s), 1);
+            mbar_init(wempty_bar(s), C::kDQW + C::kFW);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(afull_bar(b), C::kDQW);
@@ -294,11 +311,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     if (warp < 4) {
         if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegWg0));
     }
-    if (warp == 0) {
-        // ------------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------------ producers
+        // warp 0: activation tiles (two 2-D tensor copies per group); warp 2: weight records (one
+        // bulk copy per group, up to kWStages groups ahead)
         if (lane == 0) {
+            const bool is_x = warp == 0;
             const uint64_t pol_stream = policy_evict_first();
             const uint64_t pol_keep = policy_evict_last();
+            const int depth = is_x ? C::kXStages : C::kWStages;
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
             int i = 0;
@@ -309,19 +330,27 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const uint8_t* wrec = P.wp + (static_cast<size_t>(seg.nt) * P.k_groups + seg.g0) * C::kRec;
                 const CUtensorMap* xmap = &prm.xmap[seg.prob];
                 for (int g = seg.g0; g < seg.g1; ++g, ++i, wrec += C::kRec) {
-                    const int s = i % C::kStages;
-                    if (!mbar_wait(empty_bar(s), ((i / C::kStages) & 1) ^ 1, ctl)) { ok = false; break; }
-                    const uint32_t stage = s_stage0 + s * C::kStageBytes;
-                    mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
-                    bulk_load(stage + 2 * C::kXPanel, wrec, C::kRec, full_bar(s), pol_w);
-                    tma_load_2d(stage, xmap, full_bar(s), g * kTileK, seg.mt * NT, pol_keep);
-                    tma_load_2d(stage + C::kXPanel, xmap, full_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                    const int s = i % depth;
+                    const uint32_t par = ((i / depth) & 1) ^ 1;
+                    if (is_x) {
+                        if (!mbar_wait(xempty_bar(s), par, ctl)) { ok = false; break; }
+                        const uint32_t stage = s_x0 + s * C::kXStageBytes;
+                        mbar_arrive_expect_tx(xfull_bar(s), 2 * C::kXPanel);
+                        tma_load_2d(stage, xmap, xfull_bar(s), g * kTileK, seg.mt * NT, pol_keep);
+                        tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                    } else {
+                        if (!mbar_wait(wempty_bar(s), par, ctl)) { ok = false; break; }
+                        mbar_arrive_expect_tx(wfull_bar(s), C::kRec);
+                        bulk_load(s_w0 + s * C::kWStageBytes, wrec, C::kRec, wfull_bar(s), pol_w);
+                    }
                 }
             }
             if (!ok || *abort_flag) {
                 // Let every copy already issued land before the CTA can exit.
-                const int first = i > C::kStages ? i - C::kStages : 0;
-                for (int j = first; j < i; ++j) mbar_wait_plain(full_bar(j % C::kStages), (j / C::kStages) & 1, prm.timeout_cycles);
+                const int first = i > depth ? i - depth : 0;
+                for (int j = first; j < i; ++j)
+                    mbar_wait_plain(is_x ? xfull_bar(j % depth) : wfull_bar(j % depth), (j / depth) & 1,
+                                    prm.timeout_cycles);
             }
         }
         __syncwarp();
@@ -338,15 +367,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                    const int s = i % C::kStages;
+                    const int s = i % C::kXStages;
                     const int b = i & 1;
                     const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
-                    if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                    if (!mbar_wait(xfull_bar(s), (i / C::kXStages) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(afull_bar(b), u, ctl)) { ok = false; break; }
                     if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * NT);
-                    const uint32_t xs = s_stage0 + s * C::kStageBytes;
+                    const uint32_t xs = s_x0 + s * C::kXStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = make_sdesc_sw128(xs + (kk >> 2) * C::kXPanel + (kk & 3) * 32);
@@ -359,7 +388,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     }
                     mma_commit(pfull_bar(b));
                     mma_commit(aempty_bar(b));
-                    mma_commit(empty_bar(s));
+                    mma_commit(xempty_bar(s));
                 }
             }
             // Every MMA issued so far completes before the CTA frees its tensor memory.
@@ -368,7 +397,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
         __syncwarp();
     } else if (warp < 4) {
-        // idle warps of the first warpgroup
+        // warp 3: idle
     } else if (warp < 4 + C::kDQW) {
         // ------------------------------------------------------------------ dequant
         if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegDequant));
@@ -381,12 +410,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         bool ok = true;
         while (ok && sch.next(seg)) {
             for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                const int s = i % C::kStages;
+                const int s = i % C::kWStages;
                 const int b = i & 1;
                 const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
-                if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
                 if (!mbar_wait(aempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
-                const uint32_t rec = s_stage0 + s * C::kStageBytes + 2 * C::kXPanel;
+                const uint32_t rec = wrec_of(i);
                 uint32_t sub;
                 if constexpr (ZP) {
                     uint32_t zb;
@@ -427,7 +456,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(afull_bar(b));
-                    mbar_arrive(empty_bar(s));
+                    mbar_arrive(wempty_bar(s));
                 }
             }
         }
@@ -455,13 +484,13 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         bool ok = true;
         while (ok && sch.next(seg)) {
             for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                const int s = i % C::kStages;
+                const int s = i % C::kWStages;
                 const int b = i & 1;
                 const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
                 if (!mbar_wait(pfull_bar(b), u, ctl)) { ok = false; break; }
-                if (!mbar_wait(full_bar(s), (i / C::kStages) & 1, ctl)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t rec = s_stage0 + s * C::kStageBytes + 2 * C::kXPanel;
+                const uint32_t rec = wrec_of(i);
                 uint32_t sbits;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + 8192 + 2 * r));
                 const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
@@ -469,19 +498,23 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
                 }
+                // P in batches of up to 64 columns per wait (the loads of a batch overlap)
+                constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
 #pragma unroll
-                for (int c = 0; c < C::kNC; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(t_lane + b * NT + col0 + c, v);
+                for (int c = 0; c < C::kNC; c += kBatchCols) {
+                    uint32_t v[kBatchCols];
+#pragma unroll
+                    for (int q = 0; q < kBatchCols; q += 16)
+                        tmem_ld16(t_lane + b * NT + col0 + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                    for (int j = 0; j < kBatchCols; j += 2) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(pempty_bar(b));
-                    mbar_arrive(empty_bar(s));
+                    mbar_arrive(wempty_bar(s));
                 }
             }
             if (!ok) break;
@@ -495,7 +528,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 // cluster adds the S partials after the cluster barrier below
 #pragma unroll
                 for (int j = 0; j < C::kNC; ++j)
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_stage0 + ((col0 + j) * 128 + r) * 4), "f"(acc[j])
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_x0 + ((col0 + j) * 128 + r) * 4), "f"(acc[j])
                                  : "memory");
                 continue;
             }
@@ -579,7 +612,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                         for (int b = 0; b < kBatch; ++b) {
                             if (q0 + b < S) {
-                                const uint32_t base = map_to_rank(s_stage0, static_cast<uint32_t>(q0 + b));
+                                const uint32_t base = map_to_rank(s_x0, static_cast<uint32_t>(q0 + b));
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) v[b][j] = ld_cluster_f32(base + ((col0 + c + j) * 128 + r) * 4);
                             }
