@@ -149,6 +149,9 @@ int wq4_get_last_error(wq4_stream_t stream);
  *   WQ4_OPT_DECODE          0 = automatic, -1 = never, 1 = whenever the shape allows: wq4_mm with at
  *                           most 32 tokens uses a warp-level-MMA kernel that keeps whole weight rows
  *                           per CTA (no workspace)
+ *   WQ4_OPT_PDL             0 = the decode kernel is launched with programmatic dependent launch
+ *                           (it may start its prologue and L2 weight prefetch while the previous
+ *                           kernel on the stream finishes); -1 = plain stream order
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,
@@ -158,7 +161,8 @@ enum {
     WQ4_OPT_TRACE = 5,
     WQ4_OPT_A_IN_SMEM = 6,
     WQ4_OPT_CLUSTER = 7,
-    WQ4_OPT_DECODE = 8
+    WQ4_OPT_DECODE = 8,
+    WQ4_OPT_PDL = 9
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

@@ -5,7 +5,7 @@ import pytest
 
 import oracle as O
 import wq4_inputs as I
-from tests.wq4_testutil import (assert_parity, from_cuda16, from_cuda32, gpu_mm, gpu_prepack, to_cuda16,
+from tests.wq4_testutil import (assert_parity, from_cuda16, from_cuda32, gpu_mm, gpu_prepack, to_cuda16, to_cuda32,
                                 y_as_f64)
 
 pytestmark = pytest.mark.gpu
@@ -16,7 +16,7 @@ def opts(lib):
     """Options set inside a test are reset afterwards."""
     yield lib
     for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES,
-                lib.OPT_CLUSTER, lib.OPT_DECODE):
+                lib.OPT_CLUSTER, lib.OPT_DECODE, lib.OPT_PDL):
         lib.set_option(key, 0)
 
 
@@ -119,6 +119,26 @@ def test_decode_kernel_deterministic(opts):
     a = from_cuda16(gpu_mm(lib, p, blob))
     b = from_cuda16(gpu_mm(lib, p, blob))
     assert np.array_equal(a, b)
+    lib.set_option(lib.OPT_PDL, -1)                                   # plain stream order: same bits
+    c = from_cuda16(gpu_mm(lib, p, blob))
+    assert np.array_equal(a, c)
+
+
+def test_decode_after_prepack_same_stream(opts):
+    """prepack and the decode call back to back on one stream (no synchronisation between them):
+    the decode kernel may start early under programmatic launch but reads the weights only after
+    the prepack kernel has finished."""
+    import torch
+    lib = opts
+    lib.set_option(lib.OPT_DECODE, 1)
+    p = I.make_problem(8, 4096, 4096, "bf16", "u4b8", seed=7)
+    ref = O.mm_problem(p)
+    for _ in range(3):
+        Wq, S, X = to_cuda32(p.Wq), to_cuda16(p.S_bits, "bf16"), to_cuda16(p.X_bits, "bf16")
+        torch.cuda.synchronize()
+        blob = lib.prepack(Wq, S, None, qtype="u4b8")
+        y = lib.mm(X, blob, p.N, qtype="u4b8")
+        assert_parity(y_as_f64(y, "bf16"), ref, "decode right after prepack")
 
 
 def test_mm_cluster_larger_than_groups(opts):

@@ -45,6 +45,7 @@ struct Options {
     int a_in_smem = 0;
     int cluster = 0;          // 0 automatic, -1 never, S >= 2 force clusters of S
     int decode = 0;           // 0 automatic, -1 never, 1 always when the shape allows it
+    int pdl = 0;              // 0 programmatic dependent launch on, -1 off
 };
 Options g_opt;
 
@@ -488,7 +489,8 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
         if (!fn) return WQ4_ERR_CUDA;
         int grid = 0, rb = 0;
         const cudaError_t e = launch_decode(X, Wp, Y, M, N, K, dtype, qtype, dev->sm_count, dev->status,
-                                            timeout_cycles(), reinterpret_cast<void*>(fn), &grid, &rb, stream);
+                                            timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0, &grid,
+                                            &rb, stream);
         if (trace_on())
             std::fprintf(stderr, "[wq4] decode kernel: M=%d N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n", M, N, K,
                          grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
@@ -568,6 +570,10 @@ int wq4_set_option(int key, long long value) {
             if (value < -1 || value > 1) return WQ4_ERR_INVALID;
             g_opt.decode = static_cast<int>(value);
             return WQ4_OK;
+        case WQ4_OPT_PDL:
+            if (value < -1 || value > 0) return WQ4_ERR_INVALID;
+            g_opt.pdl = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -582,6 +588,7 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_A_IN_SMEM: return g_opt.a_in_smem;
         case WQ4_OPT_CLUSTER: return g_opt.cluster;
         case WQ4_OPT_DECODE: return g_opt.decode;
+        case WQ4_OPT_PDL: return g_opt.pdl;
         default: return -1;
     }
 }

@@ -11,8 +11,11 @@
 //     its warps split K (slice ks takes groups ks, ks + KS, ...) and add their parts through
 //     shared memory in slice order (deterministic);
 //   * every warp streams its own weight pieces (16-byte cp.async from the prepacked records) into
-//     a private ring of DEPTH group stages; the activations arrive once per CTA through one 3-D
-//     tensor copy (K/64 panels x Mpad token rows x 128 B, 128-byte swizzle, rows past M zero);
+//     a private ring of 2 or 4 group stages; the activations arrive through 4 to 8 3-D tensor copies
+//     per CTA (each a run of the K/64 panels x Mpad token rows x 128 B, 128-byte swizzle, rows past
+//     M zero), each on its own barrier, so the first groups start before all of X is in;
+//   * programmatic dependent launch: the prologue (barriers, tensor-map prefetch) overlaps the
+//     previous kernel's tail; every global access waits for griddepcontrol.wait;
 //   * lane (g, c) of a warp reads word c of each 32-element chunk of rows g and g + 8; the k order
 //     inside a chunk is permuted identically for A and B (slot 2c + t and 2c + 8 + t of k-step h
 //     hold elements 8c + 4h + t and 8c + 4h + 2 + t), so a lane's B fragments for the chunk's two
@@ -30,31 +33,32 @@
 namespace wq4 {
 
 struct DecodeParams {
-    CUtensorMap xmap;        // 3-D (64, M, K/64), strides (2K, 128) bytes, box (64, Mpad, K/64)
+    CUtensorMap xmap;        // 3-D (64, M, K/64), strides (2K, 128) bytes, box (64, Mpad, 2 x_gp)
     const uint8_t* wp;       // first tile record
     void* y;                 // [M][N]
     int M, N, K;
     int k_groups;
     int n_blocks;            // N / 16
     int rb;                  // row blocks per CTA
+    int depth;               // group stages per warp ring (2 or 4)
+    int x_gp;                // groups per activation piece
+    int x_pieces;            // activation pieces (at most kDecXPieces)
     unsigned int* status;
     long long timeout_cycles;
 };
 
 constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, zero points
 constexpr int kDecMaxX = 140 * 1024;                          // activation bytes held per CTA
+constexpr int kDecXPieces = 8;                                // most activation copies per CTA
 
 // warps per CTA: more warps hide the MMA and shared-memory latencies; with one token block a
 // thread needs few registers, so 32 warps fit
 __host__ __device__ constexpr int dec_warps(int nb) { return nb == 1 ? 32 : 16; }
-// group stages per warp (with 32 warps two stages already keep 64 groups in flight per CTA)
-__host__ __device__ constexpr int dec_depth(int nb) { return nb == 1 ? 2 : 4; }
 
 template <int NB>
 struct DecCfg {
     static constexpr int kMpad = 8 * NB;
     static constexpr int kWarps = dec_warps(NB);
-    static constexpr int kDepth = dec_depth(NB);
     static constexpr int kRedBytes = kWarps * NB * 32 * 16;     // per-warp partials for the final sum
 };
 
@@ -105,20 +109,30 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
+// Bounded wait without the abort protocol (used only on the way out of an aborted CTA).
+__device__ __forceinline__ bool mbar_wait_plain_dec(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
 template <int NB, bool BF16, bool ZP>
 __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
     using C = DecCfg<NB>;
     constexpr int kRec = tile_record_bytes(ZP);
-    constexpr int kDecDepth = C::kDepth;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
-    const int x_bytes = C::kMpad * prm.K * 2;
+    const int depth = prm.depth;
+    const uint32_t x_piece_bytes = static_cast<uint32_t>(C::kMpad * prm.x_gp * 256);
+    const uint32_t x_bytes = x_piece_bytes * prm.x_pieces;
     const uint32_t s_x = sbase;                                       // activations (swizzled panels)
-    const uint32_t s_w = sbase + ((x_bytes + 127) & ~127);            // per-warp stage rings
-    const uint32_t s_red = s_w + C::kWarps * kDecDepth * kDecStage;   // slice partials
-    const uint32_t s_bar = s_red + C::kRedBytes;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (s_bar + 8 - raw_s));
+    const uint32_t s_w = sbase + ((x_bytes + 1023) & ~1023u);          // per-warp stage rings
+    const uint32_t s_red = s_w + C::kWarps * depth * kDecStage;       // slice partials
+    const uint32_t s_bar = s_red + C::kRedBytes;                      // one barrier per activation piece
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (s_bar + 8 * kDecXPieces - raw_s));
     const uint8_t* const sm = smem_raw + (sbase - raw_s);              // generic view of the aligned base
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     const bool active = (ks < KS) && block < prm.n_blocks;
 
     if (threadIdx.x == 0) {
-        mbar_init(s_bar, 1);
+        for (int q = 0; q < prm.x_pieces; ++q) mbar_init(s_bar + 8 * q, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -139,6 +153,10 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     // outputs (griddepcontrol is a no-op when the launch carries no programmatic dependency).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) prefetch_tensormap(&prm.xmap);
+    // Nothing else happens before griddepcontrol.wait: the weights may be written by the kernel
+    // ahead of this one on the stream (a prepack), whose writes are only guaranteed visible after
+    // the wait. (An L2 prefetch of the weights ahead of the wait was measured slower: it queues
+    // the activation copy behind weight traffic.)
 
     float acc[NB][4];
 #pragma unroll
@@ -149,7 +167,7 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     // this warp's groups: ks, ks + KS, ...
     const int n_my = active ? (prm.k_groups - ks + KS - 1) / KS : 0;
     const int nt = block >> 3, rblk = (block & 7) * 16;               // n-tile and first row inside it
-    const uint32_t my_ring = s_w + warp * (kDecDepth * kDecStage);
+    const uint32_t my_ring = s_w + warp * (depth * kDecStage);
     // per-lane constants of the copy pattern: this lane moves code pieces lane and lane + 32
     // (piece = chunk j * 16 + row), lanes 0..1 the two 16-byte halves of the scales, lane 2 the
     // eight bytes of zero points; a group's record advances by KS records per step
@@ -169,20 +187,23 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
         }
         rec_next += rec_step;
     };
-    const int pre = n_my < kDecDepth ? n_my : kDecDepth;
-    for (int i = 0; i < kDecDepth; ++i) {
+    const int pre = n_my < depth ? n_my : depth;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        // the activations in pieces of x_gp groups, so that the first groups start early
+        for (int q = 0; q < prm.x_pieces; ++q) {
+            mbar_arrive_expect_tx(s_bar + 8 * q, x_piece_bytes);
+            tma_load_3d(s_x + q * x_piece_bytes, &prm.xmap, s_bar + 8 * q, 0, 0, 2 * prm.x_gp * q);
+        }
+    }
+    for (int i = 0; i < depth; ++i) {
         if (i < pre) issue(i);
         cp_async_commit();                                            // empty groups keep the count uniform
     }
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(s_bar, static_cast<uint32_t>(x_bytes));
-        tma_load_3d(s_x, &prm.xmap, s_bar, 0, 0, 0);
-    }
 
-    // activations have landed (bounded wait)
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
-    const bool x_ok = mbar_wait(s_bar, 0, ctl);
+    bool ok = true;
+    int x_piece = -1;                                                 // last activation piece waited for
 
     // activation addresses: token row m = 8 nb + g sits at 128-byte row (panel * Mpad + m) whose
     // swizzle key is (row & 7) = g; the lane's 16-byte chunk in a panel is (4 (j & 1) + c) ^ g
@@ -193,10 +214,19 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     const uint32_t a_off = g * 16 + 4 * c;                            // word c of row g in a chunk
 
     constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
-    for (int i = 0; i < n_my && x_ok; ++i) {
-        cp_async_wait<kDecDepth - 1>();
+    for (int i = 0; i < n_my && ok; ++i) {
+        const int piece = (ks + i * KS) / prm.x_gp;                   // activation piece of this group
+        if (piece != x_piece) {
+            ok = mbar_wait(s_bar + 8 * piece, 0, ctl);
+            x_piece = piece;
+            if (!ok) break;
+        }
+        if (depth == 4)
+            cp_async_wait<3>();
+        else
+            cp_async_wait<1>();
         __syncwarp();
-        const int slot = i & (kDecDepth - 1);
+        const int slot = i & (depth - 1);
         const uint32_t st = my_ring + slot * kDecStage;
         uint32_t sub_lo, sub_hi;                                      // 128 + z (bf16) per row
         const uint8_t* const stp = sm + (st - sbase);
@@ -263,10 +293,14 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
             acc[nb][3] = fmaf(s_hi, p[nb][3] + p2[nb][3], acc[nb][3]);
         }
         __syncwarp();
-        if (i + kDecDepth < n_my) issue(slot);
+        if (i + depth < n_my) issue(slot);
         cp_async_commit();
     }
     cp_async_wait<0>();
+    if (!ok && threadIdx.x == 0) {
+        // let the activation copies already issued land before the CTA exits (bounded)
+        for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain_dec(s_bar + 8 * q, 0, prm.timeout_cycles);
+    }
 
     // slice partials -> shared memory, then slice 0 adds them in slice order and writes Y
 #pragma unroll
@@ -306,23 +340,45 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     }
 }
 
-int decode_smem_bytes(int nb, int K) {
-    const int mpad = 8 * nb;
-    const int x = (mpad * K * 2 + 127) & ~127;
-    return 1024 + x + dec_warps(nb) * dec_depth(nb) * kDecStage + dec_warps(nb) * nb * 32 * 16 + 64;
+// Activation pieces: groups per piece and piece count, 4 to 8 pieces with the least padding (the
+// last piece may run past K; the copy fills what lies beyond the tensor with zeros and the kernel
+// never reads it, but shared memory must hold it).
+static void dec_x_geometry(int K, int* gp, int* pieces) {
+    const int kg = K / kTileK;
+    int best_gp = kg, best_waste = 1 << 30;
+    for (int target = 4; target <= kDecXPieces; ++target) {
+        const int g = (kg + target - 1) / target;
+        const int waste = g * ((kg + g - 1) / g) - kg;
+        if (waste < best_waste) {
+            best_waste = waste;
+            best_gp = g;
+        }
+    }
+    *gp = best_gp;
+    *pieces = (kg + best_gp - 1) / best_gp;
 }
+
+static int decode_smem_bytes(int nb, int K, int depth) {
+    int gp, pieces;
+    dec_x_geometry(K, &gp, &pieces);
+    const int x = (8 * nb * gp * pieces * 256 + 1023) & ~1023;
+    return 1024 + x + dec_warps(nb) * depth * kDecStage + dec_warps(nb) * nb * 32 * 16 + 8 * kDecXPieces + 32;
+}
+
+// Deepest per-warp ring that fits next to the activations.
+static int decode_depth(int nb, int K) { return decode_smem_bytes(nb, K, 4) <= 232448 ? 4 : 2; }
 
 bool decode_fits(int M, int K) {
     if (M < 1 || M > 32 || K / 64 > 256) return false;
     const int nb = (M + 7) / 8;
     const int mpad = 8 * (nb == 3 ? 4 : nb);
-    return mpad * K * 2 <= kDecMaxX && decode_smem_bytes(mpad / 8, K) <= 232448;
+    return mpad * K * 2 <= kDecMaxX && decode_smem_bytes(mpad / 8, K, 2) <= 232448;
 }
 
 template <int NB, bool BF16, bool ZP>
-static cudaError_t go_decode(const DecodeParams& p, int grid, cudaStream_t st) {
+static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStream_t st) {
     auto kern = wq4_decode_kernel<NB, BF16, ZP>;
-    const int smem = decode_smem_bytes(NB, p.K);
+    const int smem = decode_smem_bytes(NB, p.K, p.depth);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -334,22 +390,22 @@ static cudaError_t go_decode(const DecodeParams& p, int grid, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <int NB>
-static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int grid, cudaStream_t st) {
-    if (bf16) return zp ? go_decode<NB, true, true>(p, grid, st) : go_decode<NB, true, false>(p, grid, st);
-    return zp ? go_decode<NB, false, true>(p, grid, st) : go_decode<NB, false, false>(p, grid, st);
+static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int grid, bool pdl, cudaStream_t st) {
+    if (bf16) return zp ? go_decode<NB, true, true>(p, grid, pdl, st) : go_decode<NB, true, false>(p, grid, pdl, st);
+    return zp ? go_decode<NB, false, true>(p, grid, pdl, st) : go_decode<NB, false, false>(p, grid, pdl, st);
 }
 
 // Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
 cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
                           int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
-                          int* grid_out, int* rb_out, cudaStream_t st) {
+                          bool pdl, int* grid_out, int* rb_out, cudaStream_t st) {
     using Enc = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -359,7 +415,9 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     std::memset(static_cast<void*>(&p), 0, sizeof(p));
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(8 * nb), static_cast<cuuint32_t>(K / 64)};
+    int gp, pieces;
+    dec_x_geometry(K, &gp, &pieces);
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(8 * nb), static_cast<cuuint32_t>(2 * gp)};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = reinterpret_cast<Enc>(encode_fn_ptr)(
         &p.xmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -379,6 +437,9 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     while (warps % rb) ++rb;                                          // whole K slices per block
     if (rb > warps) rb = warps;
     p.rb = rb;
+    p.depth = decode_depth(nb, K);
+    p.x_gp = gp;
+    p.x_pieces = pieces;
     p.status = status;
     p.timeout_cycles = timeout_cycles;
     const int grid = (p.n_blocks + rb - 1) / rb;
@@ -386,9 +447,9 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     *rb_out = rb;
     const bool bf16 = dtype == 0, zp = qtype == 1;
     switch (nb) {
-        case 1: return pick_decode<1>(p, bf16, zp, grid, st);
-        case 2: return pick_decode<2>(p, bf16, zp, grid, st);
-        default: return pick_decode<4>(p, bf16, zp, grid, st);
+        case 1: return pick_decode<1>(p, bf16, zp, grid, pdl, st);
+        case 2: return pick_decode<2>(p, bf16, zp, grid, pdl, st);
+        default: return pick_decode<4>(p, bf16, zp, grid, pdl, st);
     }
 }
 
