@@ -17,8 +17,9 @@
 //                 scales, zero points) and two 2-D tensor copies of the activation tile (two
 //                 64-element K panels, 128-byte swizzle) into a ring of shared-memory stages.
 //                 (After "machete_mainloop.cuh", load: A, B, scale and zero per stage.)
-//   warp 1        MMA issuer: one thread issues 8 tcgen05.mma (K = 16 each) per group into P[b],
-//                 b = group parity, then commits to the fold, dequant and stage barriers.
+//   warps 1, 3    MMA issuers (warp 1 even groups, warp 3 odd groups): one thread each issues
+//                 8 tcgen05.mma (K = 16 each) per group into P[b], b = group parity, then
+//                 commits to the fold, dequant and stage barriers.
 //                 (After "sm100_implicit_gemm_umma_warpspecialized.hpp", mma.)
 //   dequant warps turn the 4-bit codes of a stage into the 16-bit integer operand (q - z) with
 //                 bit logic and one packed subtraction per pair, written to tensor memory (or to
@@ -41,8 +42,8 @@ namespace wq4 {
 template <int NT, bool ZP, bool ATMEM>
 struct GemmCfg {
     static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 192, "token tile");
-    // Four warpgroups: WG0 = TMA warp, MMA warp and two idle warps; then the dequant warps; then
-    // the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
+    // Four warpgroups: WG0 = the two TMA producer warps (0, 2) and the two MMA warps (1, 3);
+    // then the dequant warps; then the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
     static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
     static constexpr int kFW = NT <= 64 ? 4 : 8;             // fold / epilogue warps
     static constexpr int kWarps = 4 + kDQW + kFW;
@@ -287,7 +288,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             mbar_init(pfull_bar(b), 1);
             mbar_init(pempty_bar(b), C::kFW);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(drain_bar, 2);                 // one commit from each MMA warp
         mbar_init(fsync_bar, C::kFW);
         *abort_flag = 0;
         *fin_flag = 0;
@@ -354,8 +355,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Two issuing threads: warp 1 takes the even groups, warp 3 the odd ones (the P and A
+        // buffers alternate with the group's parity, the X stages are distinct). One thread
+        // alone leaves the tensor pipe idle between groups while it checks the next group's
+        // three barriers and runs its loop (measured ~0.3 us of a ~0.85 us group at 192
+        // tokens); with two, one thread's checks overlap the other's MMAs. Each thread's
+        // tcgen05.commit tracks only the MMAs that thread issued.
+        const int mine = warp == 1 ? 0 : 1;
         if (lane == 0) {
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
@@ -367,6 +375,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
+                    if ((i & 1) != mine) continue;
                     const int s = i % C::kXStages;
                     const int b = i & 1;
                     const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
@@ -396,8 +405,6 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             mbar_wait_plain(drain_bar, 0, prm.timeout_cycles);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // warp 3: idle
     } else if (warp < 4 + C::kDQW) {
         // ------------------------------------------------------------------ dequant
         if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegDequant));
