@@ -136,7 +136,7 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
 int wq4_get_last_error(wq4_stream_t stream);
 
 /* Process-wide tuning and test options (not thread-safe; set before launching):
- *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64, 128 or 192); 0 = automatic
+ *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64, 128, 160 or 192); 0 = automatic
  *   WQ4_OPT_GRID            force the number of persistent CTAs; 0 = automatic
  *   WQ4_OPT_SPLIT_ALL       1 = every tile goes through the K-split path (tests)
  *   WQ4_OPT_TIMEOUT_CYCLES  bound of every pipeline wait in SM clock cycles; 0 = default

@@ -91,6 +91,7 @@ def test_options(clib):
     assert clib.wq4_set_option(1, 64) == wq4.OK
     assert clib.wq4_get_option(1) == 64
     assert clib.wq4_set_option(1, 48) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(1, 160) == wq4.OK
     assert clib.wq4_set_option(1, 0) == wq4.OK
     assert clib.wq4_set_option(wq4.OPT_PDL, 1) == wq4.ERR_INVALID
     assert clib.wq4_set_option(wq4.OPT_PDL, -1) == wq4.OK

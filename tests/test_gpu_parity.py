@@ -69,7 +69,7 @@ def test_mm_small(lib, M, N, K, dtype, qtype):
     assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), str((M, N, K, dtype, qtype)))
 
 
-@pytest.mark.parametrize("token_tile", [16, 64, 128, 192])
+@pytest.mark.parametrize("token_tile", [16, 64, 128, 160, 192])
 @pytest.mark.parametrize("grid", [0, 3, 7])
 @pytest.mark.parametrize("split_all", [0, 1])
 def test_mm_schedules(opts, token_tile, grid, split_all):
@@ -83,7 +83,7 @@ def test_mm_schedules(opts, token_tile, grid, split_all):
     assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "tile %d grid %d split %d" % (token_tile, grid, split_all))
 
 
-@pytest.mark.parametrize("token_tile", [16, 64, 128, 192])
+@pytest.mark.parametrize("token_tile", [16, 64, 128, 160, 192])
 @pytest.mark.parametrize("cluster", [2, 3, 4, 8])
 def test_mm_cluster_split(opts, token_tile, cluster):
     """Each tile's K range split over a cluster; partials added through distributed shared memory."""
@@ -92,6 +92,16 @@ def test_mm_cluster_split(opts, token_tile, cluster):
     lib.set_option(lib.OPT_CLUSTER, cluster)
     p = I.make_problem(100, 256, 1152, "bf16", "u4b8", seed=cluster * 100 + token_tile)
     assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "cluster %d tile %d" % (cluster, token_tile))
+
+
+@pytest.mark.parametrize("token_tile", [16, 64, 128, 160, 192])
+def test_mm_long_k(opts, token_tile):
+    """64 groups per tile: the operand buffers (2, 3 or 4 of them, by token tile) and both MMA
+    issuers cycle through many phases; two m-tiles, one of them ragged."""
+    lib = opts
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    p = I.make_problem(token_tile + 37, 256, 8192, "bf16", "u4b8", seed=token_tile * 3 + 1)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "long K, tile %d" % token_tile)
 
 
 DECODE = [
@@ -159,7 +169,7 @@ def test_grouped_cluster_split(opts):
             assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "grouped cluster M=%d" % p.M)
 
 
-@pytest.mark.parametrize("token_tile", [16, 128, 192])
+@pytest.mark.parametrize("token_tile", [16, 128, 160, 192])
 def test_mm_a_operand_in_smem(opts, token_tile):
     lib = opts
     lib.set_option(lib.OPT_A_IN_SMEM, 1)

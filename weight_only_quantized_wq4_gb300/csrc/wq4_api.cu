@@ -128,11 +128,36 @@ struct Plan {
     size_t workspace() const { return counters_bytes + partials_bytes; }
 };
 
-int pick_token_tile(const std::vector<Shape>& shapes) {
+// Token tile for a launch (one tile size serves every problem of a grouped call). Up to 64 tokens
+// the narrow tiles; beyond, the tile of 128, 160 or 192 tokens that minimises the padded work
+// sum_p ceil(M_p / NT) * t(NT), t = the measured time of one (tile, group) step of the GEMM
+// kernel on GB300 at M = 4096 (584, 633 and 693 ns: a wider tile costs more per step but less
+// per token, and a narrower one holds more operand buffers in tensor memory).
+int token_tile_for(const int* M, int P) {
     if (g_opt.token_tile) return g_opt.token_tile;
     int maxM = 0;
-    for (const Shape& s : shapes) maxM = std::max(maxM, s.M);
-    return maxM <= 16 ? 16 : maxM <= 64 ? 64 : maxM <= 128 ? 128 : 192;
+    for (int p = 0; p < P; ++p) maxM = std::max(maxM, M[p]);
+    if (maxM <= 16) return 16;
+    if (maxM <= 64) return 64;
+    static const int kTiles[3] = {128, 160, 192};
+    static const long long kStepNs[3] = {584, 633, 693};
+    int best = 192;
+    long long best_cost = -1;
+    for (int t = 0; t < 3; ++t) {
+        long long cost = 0;
+        for (int p = 0; p < P; ++p) cost += static_cast<long long>((M[p] + kTiles[t] - 1) / kTiles[t]) * kStepNs[t];
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = kTiles[t];
+        }
+    }
+    return best;
+}
+
+int pick_token_tile(const std::vector<Shape>& shapes) {
+    std::vector<int> Ms;
+    for (const Shape& s : shapes) Ms.push_back(s.M);
+    return token_tile_for(Ms.data(), static_cast<int>(Ms.size()));
 }
 
 int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
@@ -252,6 +277,7 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
         case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, st);
         case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, st);
         case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, st);
+        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, grid, st);
         default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, st);
     }
 }
@@ -333,7 +359,7 @@ struct PlanOne {
 };
 
 int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
-    pl->nt = g_opt.token_tile ? g_opt.token_tile : (M <= 16 ? 16 : M <= 64 ? 64 : M <= 128 ? 128 : 192);
+    pl->nt = token_tile_for(&M, 1);
     pl->m_tiles = M > 0 ? (M + pl->nt - 1) / pl->nt : 0;
     const int kg = K / kTileK;
     const long long tiles = static_cast<long long>(pl->m_tiles) * (N / kTileN);
@@ -542,7 +568,8 @@ int wq4_get_last_error(wq4_stream_t stream) {
 int wq4_set_option(int key, long long value) {
     switch (key) {
         case WQ4_OPT_TOKEN_TILE:
-            if (value != 0 && value != 16 && value != 64 && value != 128 && value != 192) return WQ4_ERR_INVALID;
+            if (value != 0 && value != 16 && value != 64 && value != 128 && value != 160 && value != 192)
+                return WQ4_ERR_INVALID;
             g_opt.token_tile = static_cast<int>(value);
             return WQ4_OK;
         case WQ4_OPT_GRID:

@@ -41,7 +41,7 @@ namespace wq4 {
 
 template <int NT, bool ZP, bool ATMEM>
 struct GemmCfg {
-    static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 192, "token tile");
+    static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 160 || NT == 192, "token tile");
     // Four warpgroups: WG0 = the two TMA producer warps (0, 2) and the two MMA warps (1, 3);
     // then the dequant warps; then the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
     static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
@@ -69,6 +69,11 @@ struct GemmCfg {
     static constexpr int kXStageBytes = 2 * kXPanel;
     static constexpr int kWStageBytes = (kRec + 127) / 128 * 128;
     static constexpr int kABuf = 128 * 128 * 2;              // one 128 x 128 16-bit operand tile
+    // Dequantised operand buffers: as many as tensor memory holds beside the two P buffers
+    // (64 columns each). With two, the dequantisation of group g waits for the MMAs of group
+    // g - 2 and that chain, not the tensor pipe, sets the pace; a third or fourth buffer lets it
+    // run further ahead. In shared memory (the comparison path) two.
+    static constexpr int kABufs = !ATMEM ? 2 : (512 - 2 * NT) / 64 >= 4 ? 4 : (512 - 2 * NT) / 64;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
@@ -79,14 +84,14 @@ struct GemmCfg {
     static constexpr int kXStages = kXStagesFit > 16 ? 16 : kXStagesFit;
     static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
     static constexpr int kColA = 2 * NT;                     // TMEM column of A buffer 0
-    static constexpr int kTmemNeed = 2 * NT + (ATMEM ? 128 : 0);
+    static constexpr int kTmemNeed = 2 * NT + (ATMEM ? 64 * kABufs : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
     static_assert(kXStages >= 2 && kWStages <= 16, "shared memory");
     static_assert(kXStageBytes % 1024 == 0 && kWRingBytes % 1024 == 0, "1024-byte aligned operand tiles");
     static_assert(kXStages * kXStageBytes >= NT * 128 * 4, "cluster reduction buffer");
     static_assert(kSmemBytes <= kMaxDynSmem, "shared memory");
-    static_assert(kTmemNeed <= 512, "tensor memory");
+    static_assert(kTmemNeed <= 512 && kABufs >= 2 && kABufs <= 4, "tensor memory");
 };
 
 // slot: -1 whole tile, >= 0 workspace slot of a K-split part, kSlotCluster a cluster part.
@@ -258,13 +263,13 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     auto xempty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
     auto wfull_bar = [&](int s) { return s_bar + 8u * (32 + s); };
     auto wempty_bar = [&](int s) { return s_bar + 8u * (48 + s); };
-    auto afull_bar = [&](int b) { return s_bar + 8u * (64 + b); };
-    auto aempty_bar = [&](int b) { return s_bar + 8u * (66 + b); };
-    auto pfull_bar = [&](int b) { return s_bar + 8u * (68 + b); };
-    auto pempty_bar = [&](int b) { return s_bar + 8u * (70 + b); };
+    auto afull_bar = [&](int a) { return s_bar + 8u * (64 + a); };
+    auto aempty_bar = [&](int a) { return s_bar + 8u * (68 + a); };
+    auto pfull_bar = [&](int b) { return s_bar + 8u * (72 + b); };
+    auto pempty_bar = [&](int b) { return s_bar + 8u * (74 + b); };
     auto wrec_of = [&](int i) { return s_w0 + (i % C::kWStages) * C::kWStageBytes; };
-    const uint32_t drain_bar = s_bar + 8u * 72;
-    const uint32_t fsync_bar = s_bar + 8u * 73;   // fold warps meet here in the split epilogue
+    const uint32_t drain_bar = s_bar + 8u * 76;
+    const uint32_t fsync_bar = s_bar + 8u * 77;   // fold warps meet here in the split epilogue
     uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 80;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
@@ -282,9 +287,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             mbar_init(wfull_bar(s), 1);
             mbar_init(wempty_bar(s), C::kDQW + C::kFW);
         }
+        for (int a = 0; a < C::kABufs; ++a) {
+            mbar_init(afull_bar(a), C::kDQW);
+            mbar_init(aempty_bar(a), 1);
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(afull_bar(b), C::kDQW);
-            mbar_init(aempty_bar(b), 1);
             mbar_init(pfull_bar(b), 1);
             mbar_init(pempty_bar(b), C::kFW);
         }
@@ -377,10 +384,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
                     if ((i & 1) != mine) continue;
                     const int s = i % C::kXStages;
-                    const int b = i & 1;
+                    const int b = i & 1;                        // P buffer
                     const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                    const int a = i % C::kABufs;                // A buffer
                     if (!mbar_wait(xfull_bar(s), (i / C::kXStages) & 1, ctl)) { ok = false; break; }
-                    if (!mbar_wait(afull_bar(b), u, ctl)) { ok = false; break; }
+                    if (!mbar_wait(afull_bar(a), (i / C::kABufs) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * NT);
@@ -389,14 +397,14 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t bdesc = make_sdesc_sw128(xs + (kk >> 2) * C::kXPanel + (kk & 3) * 32);
                         if constexpr (ATMEM) {
-                            mma_ts(d_tmem, tmem_base + C::kColA + b * 64 + kk * 8, bdesc, idesc, kk > 0);
+                            mma_ts(d_tmem, tmem_base + C::kColA + a * 64 + kk * 8, bdesc, idesc, kk > 0);
                         } else {
-                            const uint64_t adesc = make_sdesc_sw128(s_A + b * C::kABuf + (kk >> 2) * (C::kABuf / 2) + (kk & 3) * 32);
+                            const uint64_t adesc = make_sdesc_sw128(s_A + a * C::kABuf + (kk >> 2) * (C::kABuf / 2) + (kk & 3) * 32);
                             mma_ss(d_tmem, adesc, bdesc, idesc, kk > 0);
                         }
                     }
                     mma_commit(pfull_bar(b));
-                    mma_commit(aempty_bar(b));
+                    mma_commit(aempty_bar(a));
                     mma_commit(xempty_bar(s));
                 }
             }
@@ -418,10 +426,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         while (ok && sch.next(seg)) {
             for (int g = seg.g0; g < seg.g1; ++g, ++i) {
                 const int s = i % C::kWStages;
-                const int b = i & 1;
-                const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                const int a = i % C::kABufs;
                 if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
-                if (!mbar_wait(aempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
+                if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
                 const uint32_t rec = wrec_of(i);
                 uint32_t sub;
                 if constexpr (ZP) {
@@ -444,9 +451,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub);
                     }
                     if constexpr (ATMEM) {
-                        tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + b * 64 + 16 * j, out);
+                        tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + a * 64 + 16 * j, out);
                     } else {
-                        const uint32_t pbase = s_A + b * C::kABuf + (j >> 1) * (C::kABuf / 2) + r * 128;
+                        const uint32_t pbase = s_A + a * C::kABuf + (j >> 1) * (C::kABuf / 2) + r * 128;
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
                             const uint32_t chunk = static_cast<uint32_t>((4 * (j & 1) + w) ^ (r & 7));
@@ -462,7 +469,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(afull_bar(b));
+                    mbar_arrive(afull_bar(a));
                     mbar_arrive(wempty_bar(s));
                 }
             }
@@ -506,16 +513,20 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
                 }
                 // P in batches of up to 64 columns per wait (the loads of a batch overlap)
+                // (the last batch may be shorter: 80 columns = 48 + 32)
                 constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
 #pragma unroll
                 for (int c = 0; c < C::kNC; c += kBatchCols) {
+                    constexpr int kLeft = C::kNC;
+                    const int nbc = kLeft - c < kBatchCols ? kLeft - c : kBatchCols;
                     uint32_t v[kBatchCols];
 #pragma unroll
                     for (int q = 0; q < kBatchCols; q += 16)
-                        tmem_ld16(t_lane + b * NT + col0 + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
+                        if (q < nbc) tmem_ld16(t_lane + b * NT + col0 + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < kBatchCols; j += 2) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                    for (int j = 0; j < kBatchCols; j += 2)
+                        if (j < nbc) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
                 }
                 tc_fence_before();
                 __syncwarp();

@@ -14,6 +14,8 @@ cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, bool z
                              cudaStream_t st);
 cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
                               cudaStream_t st);
+cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+                              cudaStream_t st);
 cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
                               cudaStream_t st);
 
