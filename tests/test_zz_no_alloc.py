@@ -23,20 +23,25 @@ def _call(lib, X, blob, Y, p):
 
 
 def test_static_scratch_matches_wq4_mm_twice(lib):
-    # 112 weight tiles on a 152-SM GPU: the plan splits tiles over CTAs, so the kernel uses scratch
+    # Every tile goes through the K-split path (split over CTAs, partial sums and tile counters
+    # in scratch), whatever the planner would pick for this shape on its own.
     p = I.make_problem(128, 14336, 1024, "bf16", "u4_zp", seed=2024)
-    assert lib.workspace_bytes(p.M, p.N, p.K) > 0
-    blob = gpu_prepack(lib, p)
-    X = to_cuda16(p.X_bits, p.dtype)
-    want = O.decode16(from_cuda16(lib.mm(X, blob, p.N, qtype=p.qtype)), p.dtype)
-    for _ in range(2):
-        Y = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        assert _call(lib, X, blob, Y, p) == lib.OK
-        assert lib.get_last_error() == lib.OK
-        got = O.decode16(from_cuda16(Y), p.dtype)
-        st = O.check_tolerance(got, want)
-        assert st["violations"] == 0, st
-        assert O.check_tolerance(got, O.mm_problem(p))["violations"] == 0
+    lib.set_option(lib.OPT_SPLIT_ALL, 1)
+    try:
+        assert lib.workspace_bytes(p.M, p.N, p.K) > 0
+        blob = gpu_prepack(lib, p)
+        X = to_cuda16(p.X_bits, p.dtype)
+        want = O.decode16(from_cuda16(lib.mm(X, blob, p.N, qtype=p.qtype)), p.dtype)
+        for _ in range(2):
+            Y = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            assert _call(lib, X, blob, Y, p) == lib.OK
+            assert lib.get_last_error() == lib.OK
+            got = O.decode16(from_cuda16(Y), p.dtype)
+            st = O.check_tolerance(got, want)
+            assert st["violations"] == 0, st
+            assert O.check_tolerance(got, O.mm_problem(p))["violations"] == 0
+    finally:
+        lib.set_option(lib.OPT_SPLIT_ALL, 0)
 
 
 def test_static_scratch_rejects_plans_beyond_its_size(lib):

@@ -35,6 +35,7 @@ __device__ unsigned int g_status;   // device-side error word (bounded-wait time
 
 constexpr int kMaxDevices = 64;
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;   // ~2 s at 2 GHz
+constexpr long long kFixupSteps = 10;   // cost of a K-split tile's fixup, in (tile, group) steps
 
 struct Options {
     int token_tile = 0;
@@ -160,6 +161,18 @@ int pick_token_tile(const std::vector<Shape>& shapes) {
     return token_tile_for(Ms.data(), static_cast<int>(Ms.size()));
 }
 
+// Splitting the last partial wave of tiles over all CTAs pays only if it saves more (tile, group)
+// steps than the fixup of the split tiles costs (the last CTA of a tile reads and adds the
+// others' fp32 partials: about kFixupSteps steps, measured). Otherwise every tile stays whole and
+// the last wave is partly idle.
+bool keep_tiles_whole(long long tiles, long long units, int C) {
+    if (g_opt.split_all || g_opt.grid) return false;
+    const long long kg_avg = (units + tiles - 1) / tiles;
+    const long long whole = (tiles + C - 1) / C * kg_avg;
+    const long long split = (tiles / C) * kg_avg + ((tiles % C) * kg_avg + C - 1) / C + kFixupSteps;
+    return whole <= split;
+}
+
 int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     pl->nt = pick_token_tile(shapes);
     long long tiles = 0, units = 0;
@@ -201,8 +214,9 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     int C = g_opt.grid ? g_opt.grid : sm_count;
     // whole waves of tiles are processed data-parallel; the rest is K-split over all CTAs
     int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
+    if (dp < tiles && keep_tiles_whole(tiles, units, C)) dp = static_cast<int>(tiles);
     if (dp == tiles && !g_opt.split_all) {
-        pl->grid = C;
+        pl->grid = static_cast<int>(std::min<long long>(C, tiles));
         pl->dp_tiles = dp;
         pl->sk_unit_begin = static_cast<int>(units);
         pl->sk_units = 0;
@@ -383,8 +397,9 @@ int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
     }
     int C = g_opt.grid ? g_opt.grid : sm_count;
     int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
+    if (dp < tiles && keep_tiles_whole(tiles, units, C)) dp = static_cast<int>(tiles);
     if (dp == tiles && !g_opt.split_all) {
-        pl->grid = C;
+        pl->grid = static_cast<int>(std::min<long long>(C, tiles));
         pl->dp_tiles = dp;
         pl->sk_unit_begin = static_cast<int>(units);
         return WQ4_OK;

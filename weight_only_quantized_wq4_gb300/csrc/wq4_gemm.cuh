@@ -576,7 +576,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (!fold_sync()) break;
                 if (!*fin_flag) continue;
                 // sum the parts in CTA order, loading kBatch parts at a time
-                constexpr int kBatch = C::kNC <= 16 ? 4 : 2;
+                constexpr int kBatch = C::kNC <= 64 ? 4 : 2;   // parts of a 16-column batch loaded together
 #pragma unroll
                 for (int c = 0; c < C::kNC; c += 16) {
                     bool firstv = true;
@@ -620,7 +620,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int S = prm.cluster_split;
                 const int n = seg.nt * kTileN + r;
                 const int m0 = seg.mt * NT + col0;
-                constexpr int kBatch = C::kNC <= 16 ? 4 : 2;
+                constexpr int kBatch = C::kNC <= 64 ? 4 : 2;   // parts of a 16-column batch loaded together
                 uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
 #pragma unroll
                 for (int c = 0; c < C::kNC; c += 16) {
