@@ -149,9 +149,10 @@ int wq4_get_last_error(wq4_stream_t stream);
  *   WQ4_OPT_DECODE          0 = automatic, -1 = never, 1 = whenever the shape allows: wq4_mm with at
  *                           most 32 tokens uses a warp-level-MMA kernel that keeps whole weight rows
  *                           per CTA (no workspace)
- *   WQ4_OPT_PDL             0 = the decode kernel is launched with programmatic dependent launch
- *                           (it may start its prologue and L2 weight prefetch while the previous
- *                           kernel on the stream finishes); -1 = plain stream order
+ *   WQ4_OPT_PDL             0 = both kernels are launched with programmatic dependent launch (a
+ *                           call's set-up overlaps the end of the previous kernel on the stream;
+ *                           it touches global memory only after that kernel has completed);
+ *                           -1 = plain stream order
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,

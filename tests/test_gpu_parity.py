@@ -1,5 +1,7 @@
 """GPU path vs the CPU oracle through the C ABI: prepack bit-exact, GEMM within
 |Y - Y_ref| <= 1e-2 + 1e-2 |Y_ref| (fp32 accumulation, output rounded to bf16/fp16 once)."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -149,6 +151,55 @@ def test_decode_after_prepack_same_stream(opts):
         blob = lib.prepack(Wq, S, None, qtype="u4b8")
         y = lib.mm(X, blob, p.N, qtype="u4b8")
         assert_parity(y_as_f64(y, "bf16"), ref, "decode right after prepack")
+
+
+@pytest.mark.parametrize("M,split_all", [(128, 0), (500, 0), (500, 1)])
+def test_gemm_back_to_back_in_a_graph(opts, M, split_all):
+    """Programmatic dependent launch: a graph of GEMM calls where each call's activations are the
+    previous call's output (Y_i feeds X_{i+1}, N = K) and one weight is prepacked inside the
+    graph right before its use. The result must equal the same chain run with plain stream order."""
+    import torch
+    lib = opts
+    K = 1024
+    ps = [I.make_problem(M, K, K, "bf16", "u4b8", seed=700 + i) for i in range(4)]
+    Wq = [to_cuda32(p.Wq) for p in ps]
+    S = [to_cuda16(p.S_bits, "bf16") for p in ps]
+    blobs = [gpu_prepack(lib, p) for p in ps[:3]]
+    X0 = to_cuda16(ps[0].X_bits, "bf16")
+
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)   # 1: every tile split, counters reused call to call
+
+    def chain(pdl):
+        lib.set_option(lib.OPT_PDL, pdl)
+        st = torch.cuda.Stream()
+        outs = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+        blob3 = torch.empty(lib.prepacked_bytes(K, K), dtype=torch.uint8, device="cuda")
+        ws = lib.alloc_workspace(max(lib.workspace_bytes(M, K, K), 16))
+        clib = lib.load_library()
+        with torch.cuda.stream(st):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                x = X0
+                for i in range(4):
+                    if i == 3:   # prepack the last weight inside the graph, right before its use
+                        assert clib.wq4_prepack(ctypes.c_void_p(Wq[3].data_ptr()), ctypes.c_void_p(S[3].data_ptr()),
+                                                None, K, K, 128, 0, 0, ctypes.c_void_p(blob3.data_ptr()),
+                                                ctypes.c_void_p(st.cuda_stream)) == lib.OK
+                    lib.mm(x, blobs[i] if i < 3 else blob3, K, qtype="u4b8", workspace=ws, out=outs[i])
+                    x = outs[i]
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+        assert lib.get_last_error() == lib.OK
+        return [from_cuda16(o) for o in outs]
+
+    a = chain(0)
+    b = chain(-1)
+    for i in range(4):
+        assert np.array_equal(a[i], b[i]), "call %d differs with programmatic launch" % i
+    # and the first call of the chain matches the oracle
+    assert_parity(O.decode16(a[0], "bf16"), O.mm_problem(ps[0]), "chain call 0")
 
 
 def test_mm_cluster_larger_than_groups(opts):

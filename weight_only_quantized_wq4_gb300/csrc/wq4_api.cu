@@ -287,12 +287,13 @@ int encode_x_map(CUtensorMap* map, const void* X, int M, int K, int dtype, int n
 
 cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int grid, cudaStream_t st) {
     const bool bf16 = dtype == WQ4_BF16, zp = qtype == WQ4_U4_ZP, a_tmem = !g_opt.a_in_smem;
+    const bool pdl = g_opt.pdl == 0;
     switch (nt) {
-        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, st);
-        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, st);
-        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, st);
-        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, grid, st);
-        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, st);
+        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
+        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
+        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
+        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
+        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
     }
 }
 

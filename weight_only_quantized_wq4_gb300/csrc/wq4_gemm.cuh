@@ -314,6 +314,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Programmatic dependent launch: the set-up above (barriers, tensor maps, tensor memory)
+    // overlaps the tail of the kernel ahead on the stream; every global access below (copies,
+    // split counters and partials, Y) waits for it to complete. Both are no-ops when the launch
+    // carries no programmatic dependency.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
 
     if (warp < 4) {
@@ -668,7 +674,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 
 // Host-side launcher for one instantiation (cluster = S CTAs per cluster in cluster mode, else 1).
 template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
-cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, bool pdl, cudaStream_t stream) {
     using C = GemmCfg<NT, ZP, ATMEM>;
     auto kern = wq4_gemm_kernel<NT, BF16, ZP, MAXP, ATMEM>;
     if constexpr (C::kRegSplit) {
@@ -689,13 +695,15 @@ cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, cudaStream_t stream
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = p.cluster_split > 0 ? p.cluster_split : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

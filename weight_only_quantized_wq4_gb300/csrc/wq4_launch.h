@@ -9,15 +9,15 @@ namespace wq4 {
 
 // `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
 cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
-                             cudaStream_t st);
+                             bool pdl, cudaStream_t st);
 cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
-                             cudaStream_t st);
+                             bool pdl, cudaStream_t st);
 cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
-                              cudaStream_t st);
+                              bool pdl, cudaStream_t st);
 cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
-                              cudaStream_t st);
+                              bool pdl, cudaStream_t st);
 cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
-                              cudaStream_t st);
+                              bool pdl, cudaStream_t st);
 
 // Decode-sized M (<= 32 tokens): warp-level MMA kernel, no workspace.
 bool decode_fits(int M, int K);
