@@ -41,6 +41,7 @@ BLOB_MAGIC = 0x50345157  # bytes "WQ4P" little-endian
 BLOB_VERSION = 1
 DTYPE_CODE = {"bf16": 0, "fp16": 1}
 QTYPE_CODE = {"u4b8": 0, "u4_zp": 1}
+ONE_BITS = {"bf16": 0x3F80, "fp16": 0x3C00}   # 1.0, the scale slot of a weight without scales
 
 
 # --------------------------------------------------------------------------------------------
@@ -83,12 +84,14 @@ def zero_points(N: int, K: int, qtype: str, Z_words=None, group_size: int = GROU
 def dequantize(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
                group_size: int = GROUP) -> np.ndarray:
     """W[n, k] = (q[n, k] - z[k // G, n]) * s[k // G, n] in fp64 (exact: |q - z| <= 15 times a
-    16-bit scale needs at most 15 significant bits)."""
+    16-bit scale needs at most 15 significant bits).  Without scales (``S_bits`` None) the value
+    is the converted code itself, q - z: the direct-conversion mode of "machete_mainloop.cuh",
+    ``get_conversion_mode`` (no scale operand given)."""
     if K % group_size:
         raise ValueError("K must be a multiple of the group size")
     q = unpack_u4(Wq, K).astype(np.int64)                       # [N][K]
     z = zero_points(N, K, qtype, Z_words, group_size)           # [K/G][N]
-    s = decode16(S_bits, dtype)                                 # [K/G][N]
+    s = decode16(S_bits, dtype) if S_bits is not None else np.ones((K // group_size, N))
     g_of_k = np.arange(K) // group_size
     zk = z[g_of_k, :].T                                         # [N][K]
     sk = s[g_of_k, :].T                                         # [N][K]
@@ -154,6 +157,10 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
             group_size: int = GROUP) -> np.ndarray:
     """Blob bytes (uint8) for one weight.
 
+    Group sizes: G a multiple of 128 dividing K (G = K: one scale per row). Record g of the layout
+    below takes the scale (and zero point) of quantisation group 128 g // G, so every 128-K record
+    carries its own copy. ``S_bits`` None (no scales): every scale slot holds 1.0.
+
     Layout:
       * header, 256 B of little-endian uint32: magic "WQ4P", version 1, N, K, group size,
         dtype code (bf16 0, fp16 1), qtype code (u4b8 0, u4_zp 1), tile bytes, N/128, K/128,
@@ -168,9 +175,12 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
             group g) in bits [4 (r % 8), 4 (r % 8) + 4) of little-endian word r // 8.
           - zero padding up to tile_bytes.
     """
-    if group_size != GROUP or N % TILE_N or K % TILE_K:
-        raise ValueError("the blob format needs group 128 and N, K multiples of 128")
+    if group_size % TILE_K or K % group_size or N % TILE_N or K % TILE_K:
+        raise ValueError("the blob format needs N, K multiples of 128 and a group size that is a "
+                         "multiple of 128 dividing K")
     nT, nG = N // TILE_N, K // TILE_K
+    # record g (K elements 128 g ... 128 g + 127) lies in quantisation group (128 g) // G
+    src = (np.arange(nG) * TILE_K) // group_size
     tb = tile_bytes(qtype)
     blob = np.zeros(prepacked_bytes(N, K, qtype), dtype=np.uint8)
     hdr = np.zeros(HEADER_BYTES // 4, dtype=np.uint32)
@@ -187,10 +197,14 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
 
     recs = blob[HEADER_BYTES:].reshape(nT, nG, tb)
     recs[:, :, :8192] = codes
-    S = np.asarray(S_bits, dtype=np.uint16).reshape(nG, nT, TILE_N)        # [g][nt][r]
+    if S_bits is None:                                          # no scales: 1.0 in every slot
+        S_rows = np.full((nG, N), ONE_BITS[dtype], dtype=np.uint16)
+    else:
+        S_rows = np.asarray(S_bits, dtype=np.uint16).reshape(K // group_size, N)[src]
+    S = S_rows.reshape(nG, nT, TILE_N)                          # [g][nt][r]
     recs[:, :, 8192:8448] = np.ascontiguousarray(S.transpose(1, 0, 2)).view(np.uint8).reshape(nT, nG, 256)
     if qtype == "u4_zp":
-        z = unpack_u4(Z_words, N).reshape(nG, nT, TILE_N)                  # [g][nt][r]
+        z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, TILE_N)  # [g][nt][r]
         zw = _pack_rows(z.transpose(1, 0, 2))                              # [nt][g][16] uint32
         recs[:, :, 8448:8512] = np.ascontiguousarray(zw).view(np.uint8).reshape(nT, nG, 64)
     return blob
@@ -202,9 +216,11 @@ def _pack_rows(z: np.ndarray) -> np.ndarray:
     return np.bitwise_or.reduce(z8 << (4 * np.arange(8, dtype=np.uint32)), axis=-1)
 
 
-def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str):
-    """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] or None)."""
+def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str, group_size: int = GROUP):
+    """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] or None);
+    quantisation group j is read from its first record, 128-K record j G / 128."""
     nT, nG = N // TILE_N, K // TILE_K
+    first = (np.arange(K // group_size) * group_size) // TILE_K
     tb = tile_bytes(qtype)
     recs = np.asarray(blob, dtype=np.uint8)[HEADER_BYTES:HEADER_BYTES + nT * nG * tb].reshape(nT, nG, tb)
     words = np.ascontiguousarray(recs[:, :, :8192]).view(np.uint32).reshape(nT, nG, 4, TILE_N, 4)
@@ -212,11 +228,11 @@ def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str):
     q6 = (words[..., None] >> (4 * NIBBLE_POS)) & np.uint32(0xF)  # [..][e]
     q = q6.reshape(N, K).astype(np.uint8)
     S = np.ascontiguousarray(recs[:, :, 8192:8448]).view(np.uint16).reshape(nT, nG, TILE_N)
-    S_bits = np.ascontiguousarray(S.transpose(1, 0, 2)).reshape(nG, N)
+    S_bits = np.ascontiguousarray(np.ascontiguousarray(S.transpose(1, 0, 2)).reshape(nG, N)[first])
     Z = None
     if qtype == "u4_zp":
         zw = np.ascontiguousarray(recs[:, :, 8448:8512]).view(np.uint32).reshape(nT, nG, 16)
         z = unpack_u4(zw, TILE_N)                                # [nt][g][r]
-        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2)).reshape(nG, N))
+        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2)).reshape(nG, N)[first])
     Wq = _pack_rows(q)
     return Wq.astype(np.uint32), S_bits, (None if Z is None else Z.astype(np.uint32))

@@ -60,7 +60,7 @@ def brute_force(p):
                 qv = nibble_hex(p.Wq[n, k // 8], k % 8)
                 g = k // G
                 zv = 8 if p.qtype == "u4b8" else nibble_hex(p.Z[g, n // 8], n % 8)
-                sv = exact16(int(p.S_bits[g, n]), p.dtype)
+                sv = exact16(int(p.S_bits[g, n]), p.dtype) if p.S_bits is not None else Fraction(1)
                 xv = exact16(int(p.X_bits[m, k]), p.dtype)
                 acc += xv * (qv - zv) * sv
                 aabs += abs(xv * (qv - zv) * sv)
@@ -116,6 +116,28 @@ def test_oracle_equals_exact_brute_force(dtype, qtype, shape):
             # every product is exact in fp64; any summation order errs by <= K * 2^-53 * sum|terms|
             bound = p.K * 2.0 ** -53 * float(sum_abs[m][n]) * 1.01
             assert abs(Yref[m, n] - float(exact[m][n])) <= bound, (m, n, Yref[m, n], float(exact[m][n]))
+
+
+# one scale row per 256 K, one per row (G = K), and no scales at all (direct conversion)
+GMODES = [(256, True), ("K", True), (128, False)]
+
+
+@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])
+@pytest.mark.parametrize("gmode", GMODES)
+@pytest.mark.parametrize("shape", [(1, 8, 256), (2, 8, 512)])
+def test_oracle_group_sizes_equal_exact_brute_force(qtype, gmode, shape):
+    M, N, K = shape
+    G, scaled = (K if gmode[0] == "K" else gmode[0]), gmode[1]
+    if not scaled and qtype == "u4_zp":
+        pytest.skip("direct conversion has no zero points")
+    p = I.make_problem(M, N, K, "bf16", qtype, seed=K + G + M, group_size=G, scaled=scaled)
+    assert (p.S_bits is None) == (not scaled) and (scaled is False or p.S_bits.shape == (K // G, N))
+    Yref = O.mm_problem(p)
+    exact, sum_abs = brute_force(p)
+    for m in range(M):
+        for n in range(N):
+            bound = p.K * 2.0 ** -53 * float(sum_abs[m][n]) * 1.01
+            assert abs(Yref[m, n] - float(exact[m][n])) <= bound, (m, n)
 
 
 # ---------------------------------------------------------------- closed forms
@@ -235,11 +257,13 @@ def test_tolerance_check():
 
 # ---------------------------------------------------------------- blob layout
 def _brute_blob(p) -> np.ndarray:
-    """The blob built one element at a time straight from the layout's wording."""
+    """The blob built one element at a time straight from the layout's wording (record g carries
+    the scale and zero point of quantisation group 128 g // G; no scales: 1.0 = 0x3F80 / 0x3C00)."""
     tb = O.tile_bytes(p.qtype)
     nG = p.K // 128
+    G = p.group_size
     blob = np.zeros(O.prepacked_bytes(p.N, p.K, p.qtype), np.uint8)
-    hdr = [O.BLOB_MAGIC, 1, p.N, p.K, 128, O.DTYPE_CODE[p.dtype], O.QTYPE_CODE[p.qtype], tb, p.N // 128, nG]
+    hdr = [O.BLOB_MAGIC, 1, p.N, p.K, G, O.DTYPE_CODE[p.dtype], O.QTYPE_CODE[p.qtype], tb, p.N // 128, nG]
     for i, v in enumerate(hdr):
         blob[4 * i:4 * i + 4] = list(int(v).to_bytes(4, "little"))
     pos = {0: 0, 2: 1, 4: 2, 6: 3, 1: 4, 3: 5, 5: 6, 7: 7}
@@ -255,9 +279,10 @@ def _brute_blob(p) -> np.ndarray:
         for n in range(p.N):
             rec = 256 + ((n // 128) * nG + g) * tb
             r = n % 128
-            blob[rec + 8192 + 2 * r: rec + 8192 + 2 * r + 2] = list(int(p.S_bits[g, n]).to_bytes(2, "little"))
+            sbits = int(p.S_bits[(128 * g) // G, n]) if p.S_bits is not None else (0x3F80 if p.dtype == "bf16" else 0x3C00)
+            blob[rec + 8192 + 2 * r: rec + 8192 + 2 * r + 2] = list(sbits.to_bytes(2, "little"))
             if p.qtype == "u4_zp":
-                blob[rec + 8448 + r // 2] |= int(p.z[g, n]) << (4 * (r % 2))
+                blob[rec + 8448 + r // 2] |= int(p.z[(128 * g) // G, n]) << (4 * (r % 2))
     return blob
 
 
@@ -265,6 +290,27 @@ def _brute_blob(p) -> np.ndarray:
 def test_blob_layout_brute_force(qtype):
     p = I.make_problem(1, 256, 256, "bf16", qtype, seed=13)
     assert np.array_equal(O.prepack(p.Wq, p.S_bits, p.N, p.K, p.dtype, p.qtype, p.Z), _brute_blob(p))
+
+
+@pytest.mark.parametrize("qtype,G,scaled,dtype", [("u4_zp", 256, True, "bf16"), ("u4b8", 512, True, "fp16"),
+                                                  ("u4b8", 128, False, "bf16"), ("u4b8", 256, False, "fp16")])
+def test_blob_layout_group_sizes_brute_force(qtype, G, scaled, dtype):
+    p = I.make_problem(1, 256, 512, dtype, qtype, seed=G + 1, group_size=G, scaled=scaled)
+    blob = O.prepack(p.Wq, p.S_bits, p.N, p.K, p.dtype, p.qtype, p.Z, group_size=G)
+    assert np.array_equal(blob, _brute_blob(p))
+    Wq, S, Z = O.unprepack(blob, p.N, p.K, dtype, qtype, group_size=G)
+    assert np.array_equal(Wq, p.Wq)
+    if scaled:
+        assert np.array_equal(S, p.S_bits)
+    if qtype == "u4_zp":
+        assert np.array_equal(Z, p.Z)
+
+
+def test_blob_rejects_unsupported_group_sizes():
+    p = I.make_problem(1, 128, 512, "bf16", "u4b8", seed=3)
+    for G in (64, 384):
+        with pytest.raises(ValueError):
+            O.prepack(p.Wq, np.zeros((512 // 64, 128), np.uint16), p.N, p.K, p.dtype, p.qtype, group_size=G)
 
 
 @pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])

@@ -67,7 +67,7 @@ class Problem:
     X_bits: np.ndarray               # uint16 [M][K]
     q: np.ndarray                    # uint8  [N][K]  (the codes before packing, for tests)
     Wq: np.ndarray                   # uint32 [N][K/8]
-    S_bits: np.ndarray               # uint16 [K/G][N]
+    S_bits: Optional[np.ndarray]     # uint16 [K/G][N]; None = no scales (direct conversion)
     z: Optional[np.ndarray] = None   # uint8  [K/G][N]
     Z: Optional[np.ndarray] = None   # uint32 [K/G][N/8]
     group_size: int = GROUP
@@ -77,7 +77,7 @@ def problem_from_codes(X_bits, q, S_bits, z, dtype, qtype, group_size=GROUP) -> 
     """Build a Problem from explicit arrays (used by hand-made test cases)."""
     X_bits = np.ascontiguousarray(X_bits, dtype=np.uint16)
     q = np.ascontiguousarray(q, dtype=np.uint8)
-    S_bits = np.ascontiguousarray(S_bits, dtype=np.uint16)
+    S_bits = None if S_bits is None else np.ascontiguousarray(S_bits, dtype=np.uint16)
     M, K = X_bits.shape
     N = q.shape[0]
     Z = None
@@ -89,19 +89,24 @@ def problem_from_codes(X_bits, q, S_bits, z, dtype, qtype, group_size=GROUP) -> 
     return Problem(M, N, K, dtype, qtype, X_bits, q, pack_u4(q), S_bits, z, Z, group_size)
 
 
-def _draw(rng, M, N, K, dtype, qtype, X_bits=None):
+def _draw(rng, M, N, K, dtype, qtype, X_bits=None, group_size=GROUP, scaled=True):
     if X_bits is None:
         X_bits = f32_to_bits(rng.standard_normal((M, K), dtype=np.float32), dtype)
     q = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
-    S_bits = f32_to_bits(rng.uniform(0.005, 0.02, size=(K // GROUP, N)).astype(np.float32), dtype)
-    z = rng.integers(6, 10, size=(K // GROUP, N), dtype=np.uint8) if qtype == U4_ZP else None
-    return problem_from_codes(X_bits, q, S_bits, z, dtype, qtype)
+    ng = K // group_size
+    S_bits = f32_to_bits(rng.uniform(0.005, 0.02, size=(ng, N)).astype(np.float32), dtype) if scaled else None
+    z = rng.integers(6, 10, size=(ng, N), dtype=np.uint8) if qtype == U4_ZP else None
+    return problem_from_codes(X_bits, q, S_bits, z, dtype, qtype, group_size)
 
 
-def make_problem(M: int, N: int, K: int, dtype: str = BF16, qtype: str = U4B8, seed: int = 0) -> Problem:
-    """One seeded problem of the given shape, drawn by the recipe in the module docstring."""
+def make_problem(M: int, N: int, K: int, dtype: str = BF16, qtype: str = U4B8, seed: int = 0,
+                 group_size: int = GROUP, scaled: bool = True) -> Problem:
+    """One seeded problem of the given shape, drawn by the recipe in the module docstring; one
+    scale (and zero point) row per ``group_size`` K elements, or no scales if not ``scaled``."""
+    if K % group_size:
+        raise ValueError("K must be a multiple of the group size")
     rng = np.random.default_rng(seed)
-    return _draw(rng, M, N, K, dtype, qtype)
+    return _draw(rng, M, N, K, dtype, qtype, group_size=group_size, scaled=scaled)
 
 
 def make_grouped(sum_M: int, P: int, N: int, K: int, dtype: str = BF16, qtype: str = U4B8,
