@@ -21,7 +21,10 @@
  *    launched and no buffer was touched.
  *  - dtype: WQ4_BF16 or WQ4_FP16; X, the scales and Y share it. qtype: WQ4_U4B8 (value =
  *    code - 8) or WQ4_U4_ZP (value = code - z with a 4-bit zero point per group and row).
- *  - group_size must be 128; N and K multiples of 128; M >= 0.
+ *  - group_size G: a multiple of 128 that divides K (G == K: one scale per row, channel-wise;
+ *    "machete_mainloop.cuh", can_implement and load); other sizes give WQ4_ERR_UNSUPPORTED.
+ *    N and K multiples of 128; M >= 0. The G passed to the GEMM calls must be the one the
+ *    weight was prepacked with (the blob itself holds one scale per 128-K record).
  */
 #ifndef WQ4_H_
 #define WQ4_H_
@@ -63,8 +66,10 @@ size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype);
 
 /* Reorders a weight into the prepacked blob.
  *   Wq      [N][K/8] uint32, code of element k = 8j+i in bits [4i, 4i+4) of word j.
- *   scales  [K/128][N] dtype, N contiguous (one scale per group and row).
- *   zeros   [K/128][N/8] uint32, zero point of row n = 8j+i in bits [4i, 4i+4) of word j;
+ *   scales  [K/G][N] dtype, N contiguous (one scale per group and row); NULL for a weight
+ *           without scales (WQ4_U4B8 only: the value is code - 8, the direct conversion of
+ *           "machete_mainloop.cuh", get_conversion_mode), stored as 1.0.
+ *   zeros   [K/G][N/8] uint32, zero point of row n = 8j+i in bits [4i, 4i+4) of word j;
  *           required for WQ4_U4_ZP and must be NULL for WQ4_U4B8.
  *   Wp_out  wq4_prepacked_bytes(...) bytes, 16-byte aligned; fully overwritten.
  * Integer work: the blob is a bit-exact permutation of the inputs. */
@@ -72,7 +77,9 @@ int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros,
                 int N, int K, int group_size, int dtype, int qtype,
                 void* Wp_out, wq4_stream_t stream);
 
-/* Exact inverse of wq4_prepack (a test and export aid). zeros_out must be NULL for U4B8. */
+/* Exact inverse of wq4_prepack (a test and export aid), with the same G: group j of scales_out
+ * [K/G][N] and zeros_out is read from its first 128-K record. zeros_out must be NULL for U4B8;
+ * scales_out may be NULL (not written). */
 int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype,
                   uint32_t* Wq_out, void* scales_out, uint32_t* zeros_out, wq4_stream_t stream);
 

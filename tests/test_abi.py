@@ -32,6 +32,9 @@ def test_prepacked_bytes(clib):
     assert clib.wq4_prepacked_bytes(14336, 4096, 128, 1) == 256 + 112 * 32 * 8576
     assert clib.wq4_prepacked_bytes(100, 4096, 128, 0) == 0       # N not a multiple of 128
     assert clib.wq4_prepacked_bytes(128, 4096, 64, 0) == 0        # group size 64 not built
+    assert clib.wq4_prepacked_bytes(128, 1024, 384, 0) == 0       # 384 does not divide K
+    assert clib.wq4_prepacked_bytes(128, 1024, 256, 0) == 256 + 8 * 8448   # one record per 128 K
+    assert clib.wq4_prepacked_bytes(128, 640, 640, 1) == 256 + 5 * 8576    # channel-wise (G = K)
 
 
 A16 = ctypes.c_void_p(0x10000)     # 16-byte aligned fake device addresses (never dereferenced)
@@ -65,7 +68,11 @@ def test_prepack_argument_rules(clib):
     assert pp(A16, A16b, None, 128, 128, 128, 0, 0, A16c, None) != wq4.ERR_INVALID   # valid (fails later, no GPU)
     assert pp(A16, A16b, A16c, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_INVALID   # zeros given in u4b8 mode
     assert pp(A16, A16b, None, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_INVALID   # zeros missing in zp mode
-    assert pp(A16, None, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_INVALID   # scales missing
+    assert pp(A16, None, None, 128, 128, 128, 0, 0, A16c, None) != wq4.ERR_INVALID   # no scales: direct conversion
+    assert pp(A16, None, A16c, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_INVALID   # zero points need scales
+    assert pp(A16, A16b, None, 128, 256, 256, 0, 0, A16c, None) != wq4.ERR_UNSUPPORTED  # G = 256 divides K
+    assert pp(A16, A16b, None, 128, 256, 384, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED  # G does not divide K
+    assert pp(A16, A16b, None, 128, 256, 64, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED   # G not a multiple of 128
     assert pp(MIS, A16b, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN
     assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
 

@@ -64,6 +64,41 @@ SMALL = [
 ]
 
 
+# group sizes other than 128 (a multiple of 128 dividing K; G = K is channel-wise) and weights
+# without scales (uint4b8 direct conversion)
+GROUP_MODES = [
+    (256, 512, "bf16", "u4_zp", 256, True), (384, 640, "fp16", "u4b8", 640, True),
+    (256, 384, "bf16", "u4b8", 128, False), (128, 1024, "fp16", "u4b8", 512, False),
+]
+
+
+@pytest.mark.parametrize("N,K,dtype,qtype,G,scaled", GROUP_MODES)
+def test_prepack_group_sizes_bit_exact(lib, N, K, dtype, qtype, G, scaled):
+    p = I.make_problem(1, N, K, dtype, qtype, seed=N + K + G, group_size=G, scaled=scaled)
+    blob = gpu_prepack(lib, p)
+    assert np.array_equal(blob.cpu().numpy(), O.prepack(p.Wq, p.S_bits, N, K, dtype, qtype, p.Z, group_size=G))
+    Wq, S, Z = lib.unprepack(blob, N, K, dtype, qtype, group_size=G)
+    assert np.array_equal(from_cuda32(Wq), p.Wq)
+    if scaled:
+        assert np.array_equal(from_cuda16(S), p.S_bits)
+    if qtype == "u4_zp":
+        assert np.array_equal(from_cuda32(Z), p.Z)
+
+
+GROUP_MM = [
+    (40, 256, 1024, "bf16", "u4_zp", 256, True), (200, 384, 512, "fp16", "u4b8", 512, True),
+    (64, 256, 768, "bf16", "u4b8", 128, False), (130, 256, 2048, "bf16", "u4b8", 2048, True),
+    (8, 512, 1024, "bf16", "u4_zp", 512, True), (5, 256, 640, "fp16", "u4b8", 128, False),
+]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,qtype,G,scaled", GROUP_MM)
+def test_mm_group_sizes(lib, M, N, K, dtype, qtype, G, scaled):
+    """Both kernels (M <= 32 takes the decode kernel) on every mode."""
+    p = I.make_problem(M, N, K, dtype, qtype, seed=M + N + G, group_size=G, scaled=scaled)
+    assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "G=%d scaled=%s" % (G, scaled))
+
+
 @pytest.mark.parametrize("M,N,K,dtype,qtype", SMALL)
 def test_mm_small(lib, M, N, K, dtype, qtype):
     p = I.make_problem(M, N, K, dtype, qtype, seed=M * 7 + N + K)

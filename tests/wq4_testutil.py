@@ -31,12 +31,13 @@ def from_cuda32(t) -> np.ndarray:
 
 def gpu_prepack(wq4, p):
     Z = to_cuda32(p.Z) if p.Z is not None else None
-    return wq4.prepack(to_cuda32(p.Wq), to_cuda16(p.S_bits, p.dtype), Z, qtype=p.qtype)
+    S = to_cuda16(p.S_bits, p.dtype) if p.S_bits is not None else None
+    return wq4.prepack(to_cuda32(p.Wq), S, Z, qtype=p.qtype, group_size=p.group_size, dtype=p.dtype)
 
 
 def gpu_mm(wq4, p, blob=None, **kw):
     blob = gpu_prepack(wq4, p) if blob is None else blob
-    Y = wq4.mm(to_cuda16(p.X_bits, p.dtype), blob, p.N, qtype=p.qtype, **kw)
+    Y = wq4.mm(to_cuda16(p.X_bits, p.dtype), blob, p.N, qtype=p.qtype, group_size=p.group_size, **kw)
     return Y
 
 

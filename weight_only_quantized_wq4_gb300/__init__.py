@@ -125,43 +125,46 @@ def get_last_error(device=None) -> int:
     return int(load_library().wq4_get_last_error(_stream(device)))
 
 
-def prepacked_bytes(N: int, K: int, qtype: str = "u4b8") -> int:
-    return int(load_library().wq4_prepacked_bytes(N, K, GROUP, QTYPES[qtype]))
+def prepacked_bytes(N: int, K: int, qtype: str = "u4b8", group_size: int = GROUP) -> int:
+    return int(load_library().wq4_prepacked_bytes(N, K, group_size, QTYPES[qtype]))
 
 
-def prepack(Wq, scales, zeros=None, qtype: str = "u4b8"):
-    """Wq: int32 [N][K/8] (packed codes), scales: bf16/fp16 [K/128][N], zeros: int32 [K/128][N/8]
-    or None. Returns the prepacked blob (uint8 CUDA tensor)."""
+def prepack(Wq, scales, zeros=None, qtype: str = "u4b8", group_size: int = GROUP, dtype: str = "bf16"):
+    """Wq: int32 [N][K/8] (packed codes), scales: bf16/fp16 [K/G][N] or None (no scales, uint4b8
+    only; ``dtype`` then names the activation type), zeros: int32 [K/G][N/8] or None. Returns the
+    prepacked blob (uint8 CUDA tensor)."""
     torch = _torch()
     lib = load_library()
     N, K = Wq.shape[0], Wq.shape[1] * 8
-    nbytes = prepacked_bytes(N, K, qtype)
+    nbytes = prepacked_bytes(N, K, qtype, group_size)
     if nbytes == 0:
         raise Wq4Error(ERR_UNSUPPORTED, "wq4_prepacked_bytes")
     blob = torch.empty(nbytes, dtype=torch.uint8, device=Wq.device)
     zp = _cuda(zeros, "zeros") if zeros is not None else None
-    _check(lib.wq4_prepack(_cuda(Wq, "Wq"), _cuda(scales, "scales"), zp, N, K, GROUP, _dtype_code(scales),
-                           QTYPES[qtype], _cuda(blob, "blob"), _stream(Wq.device)), "wq4_prepack")
+    sp = _cuda(scales, "scales") if scales is not None else None
+    code = _dtype_code(scales) if scales is not None else DTYPES[dtype]
+    _check(lib.wq4_prepack(_cuda(Wq, "Wq"), sp, zp, N, K, group_size, code, QTYPES[qtype], _cuda(blob, "blob"),
+                           _stream(Wq.device)), "wq4_prepack")
     return blob
 
 
-def unprepack(blob, N: int, K: int, dtype: str = "bf16", qtype: str = "u4b8"):
-    """Inverse of prepack: (Wq int32 [N][K/8], scales [K/128][N], zeros int32 [K/128][N/8] or None)."""
+def unprepack(blob, N: int, K: int, dtype: str = "bf16", qtype: str = "u4b8", group_size: int = GROUP):
+    """Inverse of prepack: (Wq int32 [N][K/8], scales [K/G][N], zeros int32 [K/G][N/8] or None)."""
     torch = _torch()
     lib = load_library()
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     Wq = torch.empty((N, K // 8), dtype=torch.int32, device=blob.device)
-    sc = torch.empty((K // GROUP, N), dtype=tdt, device=blob.device)
-    zs = torch.empty((K // GROUP, N // 8), dtype=torch.int32, device=blob.device) if qtype == "u4_zp" else None
-    _check(lib.wq4_unprepack(_cuda(blob, "blob"), N, K, GROUP, DTYPES[dtype], QTYPES[qtype], _cuda(Wq, "Wq"),
+    sc = torch.empty((K // group_size, N), dtype=tdt, device=blob.device)
+    zs = torch.empty((K // group_size, N // 8), dtype=torch.int32, device=blob.device) if qtype == "u4_zp" else None
+    _check(lib.wq4_unprepack(_cuda(blob, "blob"), N, K, group_size, DTYPES[dtype], QTYPES[qtype], _cuda(Wq, "Wq"),
                              _cuda(sc, "scales"), _cuda(zs, "zeros") if zs is not None else None,
                              _stream(blob.device)), "wq4_unprepack")
     return Wq, sc, zs
 
 
-def workspace_bytes(M: int, N: int, K: int) -> int:
+def workspace_bytes(M: int, N: int, K: int, group_size: int = GROUP) -> int:
     out = ctypes.c_size_t(0)
-    _check(load_library().wq4_workspace_bytes(M, N, K, GROUP, ctypes.byref(out)), "wq4_workspace_bytes")
+    _check(load_library().wq4_workspace_bytes(M, N, K, group_size, ctypes.byref(out)), "wq4_workspace_bytes")
     return int(out.value)
 
 
@@ -180,18 +183,18 @@ def alloc_workspace(nbytes: int, device="cuda"):
     return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
 
 
-def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None):
-    """Y[M,N] = X[M,K] . dequant(W)^T for a prepacked weight blob."""
+def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_size: int = GROUP):
+    """Y[M,N] = X[M,K] . dequant(W)^T for a prepacked weight blob (prepacked with group_size)."""
     torch = _torch()
     lib = load_library()
     M, K = X.shape
     if out is None:
         out = torch.empty((M, N), dtype=X.dtype, device=X.device)
     if workspace is None:
-        workspace = alloc_workspace(workspace_bytes(M, N, K), X.device) if M > 0 else None
+        workspace = alloc_workspace(workspace_bytes(M, N, K, group_size), X.device) if M > 0 else None
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_n = workspace.numel() if workspace is not None else 0
-    _check(lib.wq4_mm(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K, GROUP,
+    _check(lib.wq4_mm(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K, group_size,
                       _dtype_code(X), QTYPES[qtype], ws_ptr, ws_n, _stream(X.device)), "wq4_mm")
     return out
 

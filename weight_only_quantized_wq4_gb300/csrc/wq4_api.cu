@@ -4,8 +4,9 @@
 // Argument rules follow "machete_mainloop.cuh", can_implement: 128-bit alignment of every
 // operand for TMA; group_size == K or a multiple of the K tile, and non-zero; the scale pointer
 // present in the scaled modes; the zero pointer present exactly in the zero-point mode. This
-// build supports group_size == 128 (one group per K tile, "machete_mainloop.cuh", load:
-// one scale row per k-tile) and N, K multiples of 128.
+// build supports group sizes that are multiples of 128 dividing K (group_size == K included;
+// "machete_mainloop.cuh", load: the scale row of a k-tile is k_tile / (group_size / tile_k)),
+// the no-scale mode for uint4b8 (get_conversion_mode: direct conversion) and N, K multiples of 128.
 //
 // The work plan mirrors the grouped persistent kernel of
 // "sm90_gemm_array_tma_warpspecialized_cooperative.hpp" (grid sized from the SM count, a
@@ -100,7 +101,13 @@ int check_types(int group_size, int dtype, int qtype) {
     if (dtype != WQ4_BF16 && dtype != WQ4_FP16) return WQ4_ERR_INVALID;
     if (qtype != WQ4_U4B8 && qtype != WQ4_U4_ZP) return WQ4_ERR_INVALID;
     if (group_size <= 0) return WQ4_ERR_INVALID;
-    if (group_size != kTileK) return WQ4_ERR_UNSUPPORTED;
+    return WQ4_OK;
+}
+
+// Group sizes of this build: multiples of the 128-element K tile that divide K (group_size == K is
+// the channel-wise case); every 128-K record of the blob then carries its group's scale.
+int check_group(int group_size, int K) {
+    if (group_size % kTileK || K % group_size) return WQ4_ERR_UNSUPPORTED;
     return WQ4_OK;
 }
 
@@ -459,7 +466,7 @@ const char* wq4_status_string(int status) {
 }
 
 size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype) {
-    if (check_types(group_size, WQ4_BF16, qtype) || check_nk(N, K)) return 0;
+    if (check_types(group_size, WQ4_BF16, qtype) || check_nk(N, K) || check_group(group_size, K)) return 0;
     return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype == WQ4_U4_ZP);
 }
 
@@ -468,11 +475,13 @@ int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros, i
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if ((rc = check_nk(N, K))) return rc;
-    if (!Wq || !scales || !Wp_out) return WQ4_ERR_INVALID;
+    if ((rc = check_group(group_size, K))) return rc;
+    if (!Wq || !Wp_out) return WQ4_ERR_INVALID;
+    if (!scales && qtype == WQ4_U4_ZP) return WQ4_ERR_INVALID;    // zero points need scales
     if ((qtype == WQ4_U4_ZP) != (zeros != nullptr)) return WQ4_ERR_INVALID;
-    if (!aligned16(Wq) || !aligned16(scales) || !aligned16(Wp_out) || (zeros && !aligned16(zeros)))
+    if (!aligned16(Wq) || (scales && !aligned16(scales)) || !aligned16(Wp_out) || (zeros && !aligned16(zeros)))
         return WQ4_ERR_ALIGN;
-    const cudaError_t e = launch_prepack(Wq, scales, zeros, N, K, dtype, qtype, Wp_out, stream);
+    const cudaError_t e = launch_prepack(Wq, scales, zeros, N, K, group_size, dtype, qtype, Wp_out, stream);
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
@@ -481,11 +490,13 @@ int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int q
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if ((rc = check_nk(N, K))) return rc;
-    if (!Wp || !Wq_out || !scales_out) return WQ4_ERR_INVALID;
+    if ((rc = check_group(group_size, K))) return rc;
+    if (!Wp || !Wq_out) return WQ4_ERR_INVALID;
     if ((qtype == WQ4_U4_ZP) != (zeros_out != nullptr)) return WQ4_ERR_INVALID;
-    if (!aligned16(Wp) || !aligned16(Wq_out) || !aligned16(scales_out) || (zeros_out && !aligned16(zeros_out)))
+    if (!aligned16(Wp) || !aligned16(Wq_out) || (scales_out && !aligned16(scales_out)) ||
+        (zeros_out && !aligned16(zeros_out)))
         return WQ4_ERR_ALIGN;
-    const cudaError_t e = launch_unprepack(Wp, N, K, qtype, Wq_out, scales_out, zeros_out, stream);
+    const cudaError_t e = launch_unprepack(Wp, N, K, group_size, qtype, Wq_out, scales_out, zeros_out, stream);
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
@@ -497,6 +508,7 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
         if ((rc = check_nk(N[p], K[p]))) return rc;
+        if ((rc = check_group(group_size, K[p]))) return rc;
         shapes.push_back({M[p], N[p], K[p]});
     }
     DeviceInfo* dev = nullptr;
@@ -517,6 +529,7 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
     if (rc) return rc;
     if (M < 0) return WQ4_ERR_INVALID;
     if ((rc = check_nk(N, K))) return rc;
+    if ((rc = check_group(group_size, K))) return rc;
     if (M == 0) return WQ4_OK;
     if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
@@ -556,6 +569,7 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
         if ((rc = check_nk(N[p], K[p]))) return rc;
+        if ((rc = check_group(group_size, K[p]))) return rc;
         if (M[p] > 0) {
             if (!X[p] || !Wp[p] || !Y[p]) return WQ4_ERR_INVALID;
             if (!aligned16(X[p]) || !aligned16(Wp[p]) || !aligned16(Y[p])) return WQ4_ERR_ALIGN;
@@ -642,6 +656,7 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
     if (rc) return rc;
     if (M < 0) return WQ4_ERR_INVALID;
     if ((rc = check_nk(N, K))) return rc;
+    if ((rc = check_group(group_size, K))) return rc;
     if (M == 0) return WQ4_OK;
     if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;

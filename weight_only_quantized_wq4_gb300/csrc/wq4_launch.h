@@ -25,9 +25,9 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
                           int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
                           bool pdl, int* grid_out, int* rb_out, cudaStream_t st);
 
-cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K,
+cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st);
-cudaError_t launch_unprepack(const void* blob, int N, int K, int qtype, uint32_t* wq, void* scales,
+cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, uint32_t* wq, void* scales,
                              uint32_t* zeros, cudaStream_t st);
 
 }  // namespace wq4

@@ -10,7 +10,9 @@
 //     e in nibble e/2 + 4 (e % 2), so that (word >> 4i) & 0x000F000F holds elements 2i, 2i+1.
 //     A dequant thread then reads its row's 32-element runs with one 128-bit load, and the 32
 //     threads of a warp read 512 consecutive bytes;
-//   * 256 B of scales, row r at byte 2r;
+//   * 256 B of scales, row r at byte 2r (the scale of the quantisation group the record lies in:
+//     with a group size G that is a multiple of 128, record g carries group 128 g / G; without
+//     scales every slot holds 1.0);
 //   * (zero-point mode) 64 B of zero points, row r in nibble r % 8 of word r / 8; then zero
 //     padding to 8576 B.
 #include <cuda_runtime.h>
@@ -69,7 +71,8 @@ __global__ void unprepack_codes_kernel(const uint8_t* __restrict__ recs, uint32_
 // Scales (one thread per (group, row)), zero-point words (one per (group, 8 rows)), record
 // padding and the header.
 __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const uint32_t* __restrict__ zeros,
-                                    uint8_t* __restrict__ blob, int N, int K, int dtype, int qtype, int rec) {
+                                    uint8_t* __restrict__ blob, int N, int K, int G, int dtype, int qtype, int rec) {
+    const uint16_t one = dtype == 0 ? 0x3F80u : 0x3C00u;     // 1.0 in bf16 / fp16
     const int ng = K / 128, nT = N / 128;
     uint8_t* recs = blob + kBlobHeader;
     const long long n_scale = static_cast<long long>(ng) * N;
@@ -81,13 +84,15 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
             const int g = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+            const int src = (g * 128) / G;                           // quantisation group of record g
             uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            reinterpret_cast<uint16_t*>(r + 8192)[n & 127] = scales[idx];
+            reinterpret_cast<uint16_t*>(r + 8192)[n & 127] = scales ? scales[static_cast<size_t>(src) * N + n] : one;
         } else if (idx < n_scale + n_zero) {
             const long long z = idx - n_scale;
             const int g = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
+            const int src = (g * 128) / G;
             uint8_t* r = recs + (static_cast<size_t>(wz >> 4) * ng + g) * rec;
-            reinterpret_cast<uint32_t*>(r + 8448)[wz & 15] = zeros[z];
+            reinterpret_cast<uint32_t*>(r + 8448)[wz & 15] = zeros[static_cast<size_t>(src) * (N / 8) + wz];
         } else if (idx < n_scale + n_zero + n_pad) {
             const long long z = idx - n_scale - n_zero;
             const long long rr = z / pad_words;
@@ -102,7 +107,7 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
                 case 1: v = 1u; break;
                 case 2: v = static_cast<uint32_t>(N); break;
                 case 3: v = static_cast<uint32_t>(K); break;
-                case 4: v = 128u; break;
+                case 4: v = static_cast<uint32_t>(G); break;
                 case 5: v = static_cast<uint32_t>(dtype); break;
                 case 6: v = static_cast<uint32_t>(qtype); break;
                 case 7: v = static_cast<uint32_t>(rec); break;
@@ -115,21 +120,24 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
     }
 }
 
+// Output row j (quantisation group j) is read from its first record, 128-K record j G / 128.
 __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t* __restrict__ scales,
-                                      uint32_t* __restrict__ zeros, int N, int K, int rec) {
-    const int ng = K / 128;
+                                      uint32_t* __restrict__ zeros, int N, int K, int G, int rec) {
+    const int ng = K / 128, nq = K / G;
     const uint8_t* recs = blob + kBlobHeader;
-    const long long n_scale = static_cast<long long>(ng) * N;
-    const long long n_zero = zeros ? static_cast<long long>(ng) * (N / 8) : 0;
+    const long long n_scale = scales ? static_cast<long long>(nq) * N : 0;
+    const long long n_zero = zeros ? static_cast<long long>(nq) * (N / 8) : 0;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n_scale + n_zero;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
-            const int g = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+            const int j = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+            const int g = (j * G) / 128;
             const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
             scales[idx] = reinterpret_cast<const uint16_t*>(r + 8192)[n & 127];
         } else {
             const long long z = idx - n_scale;
-            const int g = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
+            const int j = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
+            const int g = (j * G) / 128;
             const uint8_t* r = recs + (static_cast<size_t>(wz >> 4) * ng + g) * rec;
             zeros[z] = reinterpret_cast<const uint32_t*>(r + 8448)[wz & 15];
         }
@@ -143,7 +151,7 @@ static int grid_for(long long work, int threads) {
     return static_cast<int>(b);
 }
 
-cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K,
+cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st) {
     const int rec = tile_record_bytes(qtype == 1);
     uint8_t* b = static_cast<uint8_t*>(blob);
@@ -152,12 +160,12 @@ cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
-    prepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(static_cast<const uint16_t*>(scales), zeros, b, N, K,
+    prepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(static_cast<const uint16_t*>(scales), zeros, b, N, K, G,
                                                             dtype, qtype, rec);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unprepack(const void* blob, int N, int K, int qtype, uint32_t* wq, void* scales,
+cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, uint32_t* wq, void* scales,
                              uint32_t* zeros, cudaStream_t st) {
     const int rec = tile_record_bytes(qtype == 1);
     const uint8_t* b = static_cast<const uint8_t*>(blob);
@@ -166,7 +174,8 @@ cudaError_t launch_unprepack(const void* blob, int N, int K, int qtype, uint32_t
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
-    unprepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(b, static_cast<uint16_t*>(scales), zeros, N, K, rec);
+    unprepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(b, static_cast<uint16_t*>(scales), zeros, N, K, G,
+                                                              rec);
     return cudaGetLastError();
 }
 
