@@ -139,7 +139,9 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
 
 /* Synchronises the stream, then reports (and clears) a device-side pipeline timeout recorded
  * by any wq4 kernel on the current device (WQ4_ERR_TIMEOUT), else a pending CUDA error
- * (WQ4_ERR_CUDA), else WQ4_OK. */
+ * (WQ4_ERR_CUDA), else WQ4_OK. A call whose waits ran out stops early and leaves its outputs
+ * undefined; the context stays usable, but a workspace it used must be zero-filled again
+ * before the next call (its split counters may be left non-zero). */
 int wq4_get_last_error(wq4_stream_t stream);
 
 /* Process-wide tuning and test options (not thread-safe; set before launching):
@@ -160,6 +162,10 @@ int wq4_get_last_error(wq4_stream_t stream);
  *                           call's set-up overlaps the end of the previous kernel on the stream;
  *                           it touches global memory only after that kernel has completed);
  *                           -1 = plain stream order
+ *   WQ4_OPT_TEST_STALL      1 = (tests of the failure path) every kernel makes one wait per CTA
+ *                           on a barrier that nothing arrives on; it runs out after the
+ *                           WQ4_OPT_TIMEOUT_CYCLES bound, the call stops early and
+ *                           wq4_get_last_error reports WQ4_ERR_TIMEOUT. 0 = off
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,
@@ -170,7 +176,8 @@ enum {
     WQ4_OPT_A_IN_SMEM = 6,
     WQ4_OPT_CLUSTER = 7,
     WQ4_OPT_DECODE = 8,
-    WQ4_OPT_PDL = 9
+    WQ4_OPT_PDL = 9,
+    WQ4_OPT_TEST_STALL = 10
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

@@ -104,5 +104,7 @@ def test_options(clib):
     assert clib.wq4_set_option(wq4.OPT_PDL, -1) == wq4.OK
     assert clib.wq4_get_option(wq4.OPT_PDL) == -1
     assert clib.wq4_set_option(wq4.OPT_PDL, 0) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_TEST_STALL, 2) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_TEST_STALL, 0) == wq4.OK
     assert clib.wq4_set_option(99, 1) == wq4.ERR_INVALID
     assert clib.wq4_get_option(99) == -1

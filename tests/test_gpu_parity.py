@@ -18,7 +18,7 @@ def opts(lib):
     """Options set inside a test are reset afterwards."""
     yield lib
     for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES,
-                lib.OPT_CLUSTER, lib.OPT_DECODE, lib.OPT_PDL):
+                lib.OPT_CLUSTER, lib.OPT_DECODE, lib.OPT_PDL, lib.OPT_TEST_STALL):
         lib.set_option(key, 0)
 
 
@@ -235,6 +235,34 @@ def test_gemm_back_to_back_in_a_graph(opts, M, split_all):
         assert np.array_equal(a[i], b[i]), "call %d differs with programmatic launch" % i
     # and the first call of the chain matches the oracle
     assert_parity(O.decode16(a[0], "bf16"), O.mm_problem(ps[0]), "chain call 0")
+
+
+@pytest.mark.parametrize("M,N,K,split_all", [(100, 256, 1152, 0), (200, 14336, 256, 0), (200, 14336, 256, 1),
+                                           (8, 512, 1024, 0), (24, 256, 512, 0)])
+def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
+    """Failure detection without a fault: each CTA waits once on a barrier that nothing arrives on
+    (WQ4_OPT_TEST_STALL) under a short bound (2e5 cycles, ~0.1 ms); the wait runs out, the CTA
+    stops, lets its copies and MMAs finish, frees its tensor memory and exits. The host reads
+    WQ4_ERR_TIMEOUT, the status word is cleared, and the next call (normal bound, fresh
+    workspace) is correct. Cluster (M=100), data-parallel, K-split and both decode shapes."""
+    import torch
+    lib = opts
+    p = I.make_problem(M, N, K, "bf16", "u4b8", seed=M + N + K)
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, "bf16")
+    torch.cuda.synchronize()
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)
+    lib.set_option(lib.OPT_TIMEOUT_CYCLES, 200000)
+    lib.set_option(lib.OPT_TEST_STALL, 1)
+    try:
+        lib.mm(X, blob, p.N)
+        status = lib.get_last_error()
+    finally:
+        lib.set_option(lib.OPT_TEST_STALL, 0)
+        lib.set_option(lib.OPT_TIMEOUT_CYCLES, 0)
+    assert status == lib.ERR_TIMEOUT
+    assert lib.get_last_error() == lib.OK
+    assert_parity(y_as_f64(lib.mm(X, blob, p.N), "bf16"), O.mm_problem(p), "after a timeout")
 
 
 def test_mm_cluster_larger_than_groups(opts):

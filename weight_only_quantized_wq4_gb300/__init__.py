@@ -20,7 +20,7 @@ OK, ERR_INVALID, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOU
 DTYPES = {"bf16": 0, "fp16": 1}
 QTYPES = {"u4b8": 0, "u4_zp": 1}
 OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM, OPT_CLUSTER = 1, 2, 3, 4, 5, 6, 7
-OPT_DECODE, OPT_PDL = 8, 9
+OPT_DECODE, OPT_PDL, OPT_TEST_STALL = 8, 9, 10
 GROUP = 128
 
 _lib = None

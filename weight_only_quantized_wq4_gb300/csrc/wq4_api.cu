@@ -48,6 +48,7 @@ struct Options {
     int cluster = 0;          // 0 automatic, -1 never, S >= 2 force clusters of S
     int decode = 0;           // 0 automatic, -1 never, 1 always when the shape allows it
     int pdl = 0;              // 0 programmatic dependent launch on, -1 off
+    int test_stall = 0;       // 1: kernels wait once on a barrier nothing arrives on (tests)
 };
 Options g_opt;
 
@@ -352,6 +353,7 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
                                       : nullptr;
     prm->status = dev->status;
     prm->timeout_cycles = timeout_cycles();
+    prm->test_stall = g_opt.test_stall;
 
     if (trace_on()) {
         std::fprintf(stderr,
@@ -544,8 +546,8 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
         if (!fn) return WQ4_ERR_CUDA;
         int grid = 0, rb = 0;
         const cudaError_t e = launch_decode(X, Wp, Y, M, N, K, dtype, qtype, dev->sm_count, dev->status,
-                                            timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0, &grid,
-                                            &rb, stream);
+                                            timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0,
+                                            g_opt.test_stall, &grid, &rb, stream);
         if (trace_on())
             std::fprintf(stderr, "[wq4] decode kernel: M=%d N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n", M, N, K,
                          grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
@@ -631,6 +633,10 @@ int wq4_set_option(int key, long long value) {
             if (value < -1 || value > 0) return WQ4_ERR_INVALID;
             g_opt.pdl = static_cast<int>(value);
             return WQ4_OK;
+        case WQ4_OPT_TEST_STALL:
+            if (value < 0 || value > 1) return WQ4_ERR_INVALID;
+            g_opt.test_stall = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -646,6 +652,7 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_CLUSTER: return g_opt.cluster;
         case WQ4_OPT_DECODE: return g_opt.decode;
         case WQ4_OPT_PDL: return g_opt.pdl;
+        case WQ4_OPT_TEST_STALL: return g_opt.test_stall;
         default: return -1;
     }
 }
@@ -696,6 +703,7 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
     prm.partials = pl.partials_bytes ? reinterpret_cast<float*>(scratch + pl.counters_bytes) : nullptr;
     prm.status = dev->status;
     prm.timeout_cycles = timeout_cycles();
+    prm.test_stall = g_opt.test_stall;
     // the array keeps the previous call's contents: the arrival counters must start at zero
     if (pl.counters_bytes && cudaMemsetAsync(scratch, 0, pl.counters_bytes, stream) != cudaSuccess) return WQ4_ERR_CUDA;
     if (trace_on())

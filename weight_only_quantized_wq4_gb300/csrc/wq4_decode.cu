@@ -45,6 +45,7 @@ struct DecodeParams {
     int x_pieces;            // activation pieces (at most kDecXPieces)
     unsigned int* status;
     long long timeout_cycles;
+    int test_stall;          // 1: thread 0 of each CTA waits on a barrier nothing arrives on (tests)
 };
 
 constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, zero points
@@ -142,8 +143,10 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     const int block = blockIdx.x * prm.rb + bl;                       // 16-row block of this warp
     const bool active = (ks < KS) && block < prm.n_blocks;
 
+    const uint32_t stall_bar = s_bar + 8 * kDecXPieces + 8;            // after the abort flag
     if (threadIdx.x == 0) {
         for (int q = 0; q < prm.x_pieces; ++q) mbar_init(s_bar + 8 * q, 1);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -202,7 +205,9 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     }
 
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
-    bool ok = true;
+    // (tests) a wait that nothing ends: it runs out, records the timeout and stops this warp
+    bool ok = !(prm.test_stall && threadIdx.x == 0) || mbar_wait(stall_bar, 0, ctl);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;                 // the whole warp stops with it
     int x_piece = -1;                                                 // last activation piece waited for
 
     // activation addresses: token row m = 8 nb + g sits at 128-byte row (panel * Mpad + m) whose
@@ -297,10 +302,6 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
         cp_async_commit();
     }
     cp_async_wait<0>();
-    if (!ok && threadIdx.x == 0) {
-        // let the activation copies already issued land before the CTA exits (bounded)
-        for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain_dec(s_bar + 8 * q, 0, prm.timeout_cycles);
-    }
 
     // slice partials -> shared memory, then slice 0 adds them in slice order and writes Y
 #pragma unroll
@@ -308,6 +309,11 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
         sts128(s_red + ((warp * NB + nb) * 32 + lane) * 16, __float_as_uint(acc[nb][0]), __float_as_uint(acc[nb][1]),
                __float_as_uint(acc[nb][2]), __float_as_uint(acc[nb][3]));
     __syncthreads();
+    // A CTA that gave up (the flag is final after the barrier above; a warp waits only for the
+    // activation pieces of its own groups) lets every activation copy land before it exits.
+    if (threadIdx.x == 0 && *abort_flag) {
+        for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain_dec(s_bar + 8 * q, 0, drain_limit(prm.timeout_cycles));
+    }
     if (active && ks == 0) {
         uint16_t* y = reinterpret_cast<uint16_t*>(prm.y);
         const int n0 = block * 16 + g;
@@ -405,7 +411,7 @@ static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int gr
 // Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
 cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
                           int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
-                          bool pdl, int* grid_out, int* rb_out, cudaStream_t st) {
+                          bool pdl, int test_stall, int* grid_out, int* rb_out, cudaStream_t st) {
     using Enc = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -442,6 +448,7 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     p.x_pieces = pieces;
     p.status = status;
     p.timeout_cycles = timeout_cycles;
+    p.test_stall = test_stall;
     const int grid = (p.n_blocks + rb - 1) / rb;
     *grid_out = grid;
     *rb_out = rb;

@@ -53,6 +53,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bound of the waits that let work already in flight finish before a CTA that gave up exits
+// (copies landing in its shared memory, MMAs reading it): independent of the pipeline bound,
+// which a caller may shorten, so that an early give-up never leaves a copy unaccounted for.
+constexpr long long kDrainCycles = 4000000000LL;   // ~2 s at 2 GHz
+__host__ __device__ inline long long drain_limit(long long timeout_cycles) {
+    return timeout_cycles > kDrainCycles ? timeout_cycles : kDrainCycles;
+}
+
 // Shared state every role consults so that one timed-out wait stops the whole CTA.
 struct WaitCtl {
     volatile int* abort_flag;      // shared memory

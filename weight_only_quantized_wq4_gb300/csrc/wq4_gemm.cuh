@@ -270,6 +270,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     auto wrec_of = [&](int i) { return s_w0 + (i % C::kWStages) * C::kWStageBytes; };
     const uint32_t drain_bar = s_bar + 8u * 76;
     const uint32_t fsync_bar = s_bar + 8u * 77;   // fold warps meet here in the split epilogue
+    const uint32_t stall_bar = s_bar + 8u * 78;   // never arrived on (test of the timeout path)
     uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 80;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
@@ -297,6 +298,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
         mbar_init(drain_bar, 2);                 // one commit from each MMA warp
         mbar_init(fsync_bar, C::kFW);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         *fin_flag = 0;
         fence_mbar_init();
@@ -325,6 +327,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     if (warp < 4) {
         if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegWg0));
     }
+    int issued = 0;                                      // copies a producer thread has issued
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------------ producers
         // warp 0: activation tiles (two 2-D tensor copies per group); warp 2: weight records (one
@@ -359,13 +362,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     }
                 }
             }
-            if (!ok || *abort_flag) {
-                // Let every copy already issued land before the CTA can exit.
-                const int first = i > depth ? i - depth : 0;
-                for (int j = first; j < i; ++j)
-                    mbar_wait_plain(is_x ? xfull_bar(j % depth) : wfull_bar(j % depth), (j / depth) & 1,
-                                    prm.timeout_cycles);
-            }
+            issued = i;                                  // drained at the end if the CTA gives up
         }
         __syncwarp();
     } else if (warp == 1 || warp == 3) {
@@ -381,7 +378,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
             int i = 0;
-            bool ok = true;
+            // (tests) a wait that nothing ends: it runs out, records the timeout, stops the CTA
+            bool ok = !(prm.test_stall && mine == 0) || mbar_wait(stall_bar, 0, ctl);
             while (ok && sch.next(seg)) {
                 const ProblemDesc& P = prm.prob[seg.prob];
                 const int rows = P.M - seg.mt * NT;
@@ -416,7 +414,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             }
             // Every MMA issued so far completes before the CTA frees its tensor memory.
             mma_commit(drain_bar);
-            mbar_wait_plain(drain_bar, 0, prm.timeout_cycles);
+            mbar_wait_plain(drain_bar, 0, drain_limit(prm.timeout_cycles));
         }
         __syncwarp();
     } else if (warp < 4 + C::kDQW) {
@@ -669,6 +667,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+    // A CTA that gave up (any role's wait ran out; the flag is final after the barrier above) lets
+    // every copy its producers issued land before it exits: the last ring's worth of each.
+    if ((warp == 0 || warp == 2) && lane == 0 && *abort_flag) {
+        const bool is_x = warp == 0;
+        const int depth = is_x ? C::kXStages : C::kWStages;
+        for (int j = issued > depth ? issued - depth : 0; j < issued; ++j)
+            mbar_wait_plain(is_x ? xfull_bar(j % depth) : wfull_bar(j % depth), (j / depth) & 1,
+                            drain_limit(prm.timeout_cycles));
     }
 }
 

@@ -50,6 +50,7 @@ struct GemmParams {
     int* counters;           // [total_tiles - dp_tiles], zero between calls
     unsigned int* status;    // device status word (timeouts)
     long long timeout_cycles;
+    int test_stall;          // 1: one wait per CTA on a barrier nothing arrives on (tests)
 };
 
 }  // namespace wq4
