@@ -114,6 +114,20 @@ def mm_problem(p, rows=None) -> np.ndarray:
     return mm(p.X_bits, p.Wq, p.S_bits, p.M, p.N, p.K, p.dtype, p.qtype, p.Z, p.group_size, rows)
 
 
+def epilogue(Y_acc: np.ndarray, dtype: str, alpha: float = 1.0, C_bits=None, beta: float = 0.0,
+             bias_bits=None) -> np.ndarray:
+    """D = alpha * Y_acc + beta * C + bias[n] in fp64: the epilogue with a source operand of the
+    pages' kernels ("sm90_gemm_array_tma_warpspecialized_cooperative.hpp", the epilogue's C load
+    and its alpha / beta), plus a per-column (weight-row) bias. C [M][N] and bias [N] are 16-bit
+    like Y; C is read only when beta is non-zero."""
+    D = float(alpha) * np.asarray(Y_acc, dtype=np.float64)
+    if beta != 0.0:
+        D = D + float(beta) * decode16(np.asarray(C_bits).reshape(D.shape), dtype)
+    if bias_bits is not None:
+        D = D + decode16(np.asarray(bias_bits), dtype)[None, :]
+    return D
+
+
 def grouped_mm(problems) -> list:
     """The pointer-array variant: every problem independently (empty problems give empty Y)."""
     return [mm_problem(p) for p in problems]

@@ -140,6 +140,36 @@ def test_oracle_group_sizes_equal_exact_brute_force(qtype, gmode, shape):
             assert abs(Yref[m, n] - float(exact[m][n])) <= bound, (m, n)
 
 
+# ---------------------------------------------------------------- epilogue (alpha, C, beta, bias)
+def test_epilogue_exact_brute_force():
+    """D[m][n] = alpha * sum_k x w + beta * C[m][n] + bias[n], every term an exact Fraction."""
+    p = I.make_problem(2, 8, 256, "bf16", "u4_zp", seed=77)
+    rng = np.random.default_rng(5)
+    C = I.f32_to_bits(rng.standard_normal((2, 8)).astype(np.float32), "bf16")
+    bias = I.f32_to_bits(rng.standard_normal(8).astype(np.float32), "bf16")
+    alpha, beta = 0.75, -1.5                                   # both exact in binary
+    D = O.epilogue(O.mm_problem(p), "bf16", alpha, C, beta, bias)
+    exact, sum_abs = brute_force(p)
+    for m in range(2):
+        for n in range(8):
+            e = Fraction(alpha) * exact[m][n] + Fraction(beta) * bf16_exact(int(C[m, n])) + bf16_exact(int(bias[n]))
+            bound = (p.K + 2) * 2.0 ** -53 * (float(sum_abs[m][n]) + abs(beta * float(bf16_exact(int(C[m, n])))) + 1) * 1.01
+            assert abs(D[m, n] - float(e)) <= bound
+
+
+def test_epilogue_closed_forms():
+    p = I.make_problem(3, 16, 128, "fp16", "u4b8", seed=78)
+    Y = O.mm_problem(p)
+    C = I.f32_to_bits(np.full((3, 16), 0.5, np.float32), "fp16")
+    assert np.array_equal(O.epilogue(Y, "fp16"), Y)                       # identity epilogue
+    assert np.array_equal(O.epilogue(Y, "fp16", 0.0, C, 1.0), np.full((3, 16), 0.5))   # alpha 0: D = C
+    bias = I.f32_to_bits(np.arange(16, dtype=np.float32), "fp16")
+    assert np.array_equal(O.epilogue(Y, "fp16", 1.0, None, 0.0, bias) - Y, np.tile(np.arange(16.0), (3, 1)))
+    # beta = 0 never reads C (a C of NaN changes nothing)
+    Cnan = np.full((3, 16), 0x7E00, np.uint16)
+    assert np.array_equal(O.epilogue(Y, "fp16", 2.0, Cnan, 0.0), 2.0 * Y)
+
+
 # ---------------------------------------------------------------- closed forms
 def _codes_at_zero(N, K, qtype, rng):
     if qtype == "u4b8":
