@@ -104,6 +104,19 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
            int dtype, int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream);
 
 /* Workspace bytes for wq4_grouped_mm with these P problems (host arrays of shapes). */
+/* Y = alpha * (X . dequant(W)^T) + beta * C + bias, the epilogue with a source operand of the
+ * pages' kernels ("sm90_gemm_array_tma_warpspecialized_cooperative.hpp": the epilogue loads C
+ * and combines it with alpha and beta) plus a bias per output column:
+ *   C     [M][N] dtype, row-major, 16-byte aligned; read only when beta != 0 (may then be NULL
+ *         only if beta == 0); C may be Y itself (in place: every element is read, then written,
+ *         by the same thread).
+ *   bias  [N] dtype, 16-byte aligned, or NULL.
+ * Computed in fp32 (alpha * acc, then + beta * C, then + bias) and rounded to dtype once.
+ * Everything else as wq4_mm (same workspace rule, same plans). */
+int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size,
+              int dtype, int qtype, float alpha, const void* C, float beta, const void* bias,
+              void* workspace, size_t workspace_bytes, wq4_stream_t stream);
+
 int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
                                 size_t* bytes);
 

@@ -77,6 +77,15 @@ def test_prepack_argument_rules(clib):
     assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
 
 
+def test_mm_ex_argument_rules(clib):
+    ex = clib.wq4_mm_ex
+    assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, None, 0.5, None, None, 0, None) == wq4.ERR_INVALID  # beta needs C
+    assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, MIS, 0.5, None, None, 0, None) == wq4.ERR_ALIGN
+    assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, None, 0.0, MIS, None, 0, None) == wq4.ERR_ALIGN
+    assert ex(A16, A16b, A16c, 8, 128, 128, 64, 0, 0, 1.0, None, 0.0, None, None, 0, None) == wq4.ERR_UNSUPPORTED
+    assert ex(A16, A16b, A16c, 0, 128, 128, 128, 0, 0, 1.0, None, 0.0, None, None, 0, None) == wq4.OK  # M = 0
+
+
 def test_grouped_argument_rules(clib):
     arr = ctypes.c_int * 2
     ptrs = ctypes.c_void_p * 2

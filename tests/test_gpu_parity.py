@@ -265,6 +265,30 @@ def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
     assert_parity(y_as_f64(lib.mm(X, blob, p.N), "bf16"), O.mm_problem(p), "after a timeout")
 
 
+@pytest.mark.parametrize("M,N,K,dtype,split_all,in_place", [
+    (200, 14336, 256, "bf16", 0, False), (200, 14336, 256, "bf16", 1, False), (100, 256, 1152, "fp16", 0, False),
+    (8, 512, 1024, "bf16", 0, False), (24, 256, 512, "fp16", 0, True), (300, 384, 512, "bf16", 0, True)])
+def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
+    """Y = alpha acc + beta C + bias on the data-parallel, K-split, cluster and decode paths, and
+    in place (C is Y)."""
+    import torch
+    lib = opts
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)
+    p = I.make_problem(M, N, K, dtype, "u4_zp", seed=M * 3 + N + K)
+    rng = np.random.default_rng(M + N)
+    C_bits = I.f32_to_bits(rng.standard_normal((M, N)).astype(np.float32), dtype)
+    bias_bits = I.f32_to_bits(rng.standard_normal(N).astype(np.float32), dtype)
+    alpha, beta = 0.5, -1.25
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, dtype)
+    C = to_cuda16(C_bits, dtype)
+    bias = to_cuda16(bias_bits, dtype)
+    out = C if in_place else torch.empty((M, N), dtype=C.dtype, device="cuda")
+    Y = lib.mm(X, blob, N, qtype="u4_zp", out=out, alpha=alpha, C=C, beta=beta, bias=bias)
+    ref = O.epilogue(O.mm_problem(p), dtype, alpha, C_bits, beta, bias_bits)
+    assert_parity(y_as_f64(Y, dtype), ref, "epilogue %s" % ((M, N, K, split_all, in_place),))
+
+
 def test_mm_cluster_larger_than_groups(opts):
     """A cluster never gets more CTAs than the tile has groups (here K = 256: two groups)."""
     lib = opts

@@ -56,6 +56,8 @@ def load_library(path: str = LIB_PATH):
         "wq4_unprepack": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp]),
         "wq4_workspace_bytes": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]),
         "wq4_mm": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_mm_ex": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, vp,
+                              ctypes.c_float, vp, vp, c_size, vp]),
         "wq4_grouped_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm": (c_int, [c_int, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_mm_static_scratch": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp]),
@@ -183,8 +185,10 @@ def alloc_workspace(nbytes: int, device="cuda"):
     return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
 
 
-def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_size: int = GROUP):
-    """Y[M,N] = X[M,K] . dequant(W)^T for a prepacked weight blob (prepacked with group_size)."""
+def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_size: int = GROUP,
+       alpha: float = 1.0, C=None, beta: float = 0.0, bias=None):
+    """Y[M,N] = X[M,K] . dequant(W)^T for a prepacked weight blob (prepacked with group_size).
+    With alpha / C / beta / bias given: Y = alpha (X . dequant(W)^T) + beta C + bias (wq4_mm_ex)."""
     torch = _torch()
     lib = load_library()
     M, K = X.shape
@@ -194,8 +198,15 @@ def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_siz
         workspace = alloc_workspace(workspace_bytes(M, N, K, group_size), X.device) if M > 0 else None
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_n = workspace.numel() if workspace is not None else 0
-    _check(lib.wq4_mm(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K, group_size,
-                      _dtype_code(X), QTYPES[qtype], ws_ptr, ws_n, _stream(X.device)), "wq4_mm")
+    if alpha == 1.0 and beta == 0.0 and C is None and bias is None:
+        _check(lib.wq4_mm(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K,
+                          group_size, _dtype_code(X), QTYPES[qtype], ws_ptr, ws_n, _stream(X.device)), "wq4_mm")
+        return out
+    cp = _cuda(C, "C") if C is not None else None
+    bp = _cuda(bias, "bias") if bias is not None else None
+    _check(lib.wq4_mm_ex(_cuda(X, "X"), _cuda(blob, "blob"), _cuda(out, "Y") if M > 0 else None, M, N, K,
+                         group_size, _dtype_code(X), QTYPES[qtype], float(alpha), cp, float(beta), bp, ws_ptr, ws_n,
+                         _stream(X.device)), "wq4_mm_ex")
     return out
 
 

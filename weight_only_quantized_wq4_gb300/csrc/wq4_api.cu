@@ -307,7 +307,8 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
 
 template <int MAXP>
 int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void* const* Wp, void* const* Y,
-             int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+             int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st,
+             const EpilogueArgs* epi = nullptr) {
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc) return rc;
@@ -354,6 +355,13 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
     prm->status = dev->status;
     prm->timeout_cycles = timeout_cycles();
     prm->test_stall = g_opt.test_stall;
+    if (epi) {   // single-problem calls only (wq4_mm_ex)
+        prm->has_epi = 1;
+        prm->alpha = epi->alpha;
+        prm->beta = epi->beta;
+        prm->prob[0].c = epi->c;
+        prm->prob[0].bias = epi->bias;
+    }
 
     if (trace_on()) {
         std::fprintf(stderr,
@@ -525,8 +533,9 @@ int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
     return wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
 }
 
-int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
-           void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
+static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype,
+                   int qtype, const EpilogueArgs* epi, void* workspace, size_t workspace_bytes,
+                   wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if (M < 0) return WQ4_ERR_INVALID;
@@ -547,7 +556,7 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
         int grid = 0, rb = 0;
         const cudaError_t e = launch_decode(X, Wp, Y, M, N, K, dtype, qtype, dev->sm_count, dev->status,
                                             timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0,
-                                            g_opt.test_stall, &grid, &rb, stream);
+                                            g_opt.test_stall, epi, &grid, &rb, stream);
         if (trace_on())
             std::fprintf(stderr, "[wq4] decode kernel: M=%d N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n", M, N, K,
                          grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
@@ -557,7 +566,21 @@ int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int grou
     const void* xs[1] = {X};
     const void* ws[1] = {Wp};
     void* ys[1] = {Y};
-    return run_gemm<1>(shapes, xs, ws, ys, dtype, qtype, workspace, workspace_bytes, stream);
+    return run_gemm<1>(shapes, xs, ws, ys, dtype, qtype, workspace, workspace_bytes, stream, epi);
+}
+
+int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
+           void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
+    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, nullptr, workspace, workspace_bytes, stream);
+}
+
+int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
+              float alpha, const void* C, float beta, const void* bias, void* workspace, size_t workspace_bytes,
+              wq4_stream_t stream) {
+    if (beta != 0.f && !C) return WQ4_ERR_INVALID;
+    if ((C && !aligned16(C)) || (bias && !aligned16(bias))) return WQ4_ERR_ALIGN;
+    const EpilogueArgs epi{alpha, beta, beta != 0.f ? C : nullptr, bias};
+    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, &epi, workspace, workspace_bytes, stream);
 }
 
 int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* const* X, const void* const* Wp,

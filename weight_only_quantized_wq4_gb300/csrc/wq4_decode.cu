@@ -28,6 +28,7 @@
 #include <cstring>
 
 #include "wq4_device.cuh"
+#include "wq4_launch.h"
 #include "wq4_params.h"
 
 namespace wq4 {
@@ -46,6 +47,10 @@ struct DecodeParams {
     unsigned int* status;
     long long timeout_cycles;
     int test_stall;          // 1: thread 0 of each CTA waits on a barrier nothing arrives on (tests)
+    int has_epi;             // 1: Y = alpha acc + beta C + bias (else Y = acc)
+    float alpha, beta;
+    const void* c;           // [M][N], read when beta != 0 (may be Y itself)
+    const void* bias;        // [N] or null
 };
 
 constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, zero points
@@ -79,6 +84,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+template <bool BF16>
+__device__ __forceinline__ float dec_to_float(uint16_t b) {
+    if constexpr (BF16) {
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    } else {
+        return __half2float(__ushort_as_half(b));
+    }
 }
 
 template <bool BF16>
@@ -333,11 +347,18 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
                 const int m = nb * 8 + 2 * c + (t & 1);
                 const int n = n0 + (t >> 1) * 8;
                 if (m < prm.M) {
+                    float val = v[t];
+                    if (prm.has_epi) {   // alpha acc + beta C + bias in fp32, rounded once below
+                        val *= prm.alpha;
+                        if (prm.beta != 0.f)
+                            val = fmaf(prm.beta, dec_to_float<BF16>(static_cast<const uint16_t*>(prm.c)[static_cast<size_t>(m) * prm.N + n]), val);
+                        if (prm.bias) val += dec_to_float<BF16>(static_cast<const uint16_t*>(prm.bias)[n]);
+                    }
                     uint16_t o;
                     if constexpr (BF16) {
-                        o = __bfloat16_as_ushort(__float2bfloat16_rn(v[t]));
+                        o = __bfloat16_as_ushort(__float2bfloat16_rn(val));
                     } else {
-                        o = __half_as_ushort(__float2half_rn(v[t]));
+                        o = __half_as_ushort(__float2half_rn(val));
                     }
                     y[static_cast<size_t>(m) * prm.N + n] = o;
                 }
@@ -411,7 +432,8 @@ static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int gr
 // Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
 cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
                           int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
-                          bool pdl, int test_stall, int* grid_out, int* rb_out, cudaStream_t st) {
+                          bool pdl, int test_stall, const EpilogueArgs* epi, int* grid_out, int* rb_out,
+                          cudaStream_t st) {
     using Enc = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -449,6 +471,13 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     p.status = status;
     p.timeout_cycles = timeout_cycles;
     p.test_stall = test_stall;
+    if (epi) {
+        p.has_epi = 1;
+        p.alpha = epi->alpha;
+        p.beta = epi->beta;
+        p.c = epi->c;
+        p.bias = epi->bias;
+    }
     const int grid = (p.n_blocks + rb - 1) / rb;
     *grid_out = grid;
     *rb_out = rb;

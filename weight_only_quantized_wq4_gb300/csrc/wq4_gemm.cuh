@@ -228,6 +228,20 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
     }
 }
 
+// The epilogue with a source operand (after the C load and alpha / beta of the epilogue in
+// "sm90_gemm_array_tma_warpspecialized_cooperative.hpp"), plus a bias per weight row:
+// alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once by the caller. C may be Y itself:
+// each element is read and then written by the same thread.
+template <bool BF16, int MAXP>
+__device__ __forceinline__ float epilogue_value(const GemmParams<MAXP>& prm, const ProblemDesc& P, float v, int m,
+                                                int n) {
+    float r = prm.alpha * v;
+    if (prm.beta != 0.f)
+        r = fmaf(prm.beta, scale_to_float<BF16>(static_cast<const uint16_t*>(P.c)[static_cast<size_t>(m) * P.N + n]), r);
+    if (P.bias) r += scale_to_float<BF16>(static_cast<const uint16_t*>(P.bias)[n]);
+    return r;
+}
+
 // (d0, d1) += a * (b0, b1) with one packed fp32 FMA (fma.rn.f32x2).
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a, uint32_t b0, uint32_t b1) {
     uint64_t d, bb, cc, aa;
@@ -614,7 +628,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
             for (int j = 0; j < C::kNC; ++j) {
                 const int m = m0 + j;
-                if (m < P.M) y[static_cast<size_t>(m) * P.N + n] = float_to_out<BF16>(acc[j]);
+                if (m < P.M)
+                    y[static_cast<size_t>(m) * P.N + n] =
+                        float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, acc[j], m, n) : acc[j]);
             }
         }
         if (prm.cluster_split > 0) {
@@ -650,7 +666,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m0 + c + j;
-                        if (m < P.M) y[static_cast<size_t>(m) * P.N + n] = float_to_out<BF16>(sum[j]);
+                        if (m < P.M)
+                            y[static_cast<size_t>(m) * P.N + n] =
+                                float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, sum[j], m, n) : sum[j]);
                     }
                 }
             }

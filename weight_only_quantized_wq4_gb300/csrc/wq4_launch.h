@@ -7,6 +7,13 @@
 
 namespace wq4 {
 
+// Epilogue of wq4_mm_ex: Y = alpha acc + beta C + bias (C read only when beta != 0).
+struct EpilogueArgs {
+    float alpha, beta;
+    const void* c;
+    const void* bias;
+};
+
 // `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
 cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
                              bool pdl, cudaStream_t st);
@@ -23,7 +30,8 @@ cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool 
 bool decode_fits(int M, int K);
 cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, int K, int dtype, int qtype,
                           int sm_count, unsigned int* status, long long timeout_cycles, void* encode_fn_ptr,
-                          bool pdl, int test_stall, int* grid_out, int* rb_out, cudaStream_t st);
+                          bool pdl, int test_stall, const EpilogueArgs* epi, int* grid_out, int* rb_out,
+                          cudaStream_t st);
 
 cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st);

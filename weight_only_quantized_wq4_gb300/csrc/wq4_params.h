@@ -18,6 +18,8 @@ __host__ __device__ constexpr int tile_record_bytes(bool zp) { return zp ? 8576 
 struct ProblemDesc {
     const uint8_t* wp;       // first tile record (blob + kBlobHeader)
     void* y;                 // [M][N] row-major
+    const void* c;           // epilogue source [M][N] (read when beta != 0), or null
+    const void* bias;        // epilogue bias [N], or null
     int M, N, K;
     int n_tiles;             // N / 128
     int m_tiles;             // ceil(M / token tile), 0 for an empty problem
@@ -51,6 +53,8 @@ struct GemmParams {
     unsigned int* status;    // device status word (timeouts)
     long long timeout_cycles;
     int test_stall;          // 1: one wait per CTA on a barrier nothing arrives on (tests)
+    int has_epi;             // 1: Y = alpha acc + beta C + bias (else Y = acc)
+    float alpha, beta;
 };
 
 }  // namespace wq4
