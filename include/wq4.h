@@ -146,6 +146,23 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K,
 int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size,
                           int dtype, int qtype, wq4_stream_t stream);
 
+/* Grouped GEMM whose token counts are known only on the device (tokens routed to experts by a
+ * kernel on the same stream): the grouped call of "sm90_gemm_array_tma_warpspecialized_cooperative.hpp"
+ * with its problem shapes in device memory.
+ *   M_dev   DEVICE array of P int token counts, read when the work starts (stream order);
+ *           each is clamped to [0, M_cap[p]].
+ *   M_cap   HOST array: rows that X[p] and Y[p] hold (the capacity of each problem's buffers).
+ *   N, K, X, Wp, Y, group_size, dtype, qtype as in wq4_grouped_mm; X[p] is [M_cap[p]][K[p]] and
+ *           only its first M_dev[p] rows matter; rows of Y[p] beyond M_dev[p] are not written.
+ *   workspace  wq4_grouped_device_m_workspace_bytes(P) bytes, 16-byte aligned (the tile table
+ *           a set-up kernel writes before the GEMM); no zero fill needed.
+ * The plan (token tile, grid) is made for the capacities, with every tile whole. */
+int wq4_grouped_device_m_workspace_bytes(int P, size_t* bytes);
+int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int* N, const int* K,
+                            const void* const* X, const void* const* Wp, void* const* Y,
+                            int group_size, int dtype, int qtype,
+                            void* workspace, size_t workspace_bytes, wq4_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------ *
  * Errors and options.
  * ------------------------------------------------------------------------------------------ */

@@ -289,6 +289,34 @@ def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     assert_parity(y_as_f64(Y, dtype), ref, "epilogue %s" % ((M, N, K, split_all, in_place),))
 
 
+@pytest.mark.parametrize("qtype,dtype", [("u4b8", "bf16"), ("u4_zp", "fp16")])
+def test_grouped_device_resident_counts(lib, qtype, dtype):
+    """Token counts in device memory, written by a kernel right before the call: clamped to the
+    capacity, zero-count problems skipped, rows past each count untouched."""
+    import torch
+    caps = [64, 16, 256, 160, 128, 40]
+    Ns = [256, 384, 256, 128, 256, 128]
+    Ks = [512, 1024, 512, 768, 512, 256]
+    want = [37, 0, 256, 129, 5, 999]                   # 999 > capacity 40: clamped
+    probs = [I.make_problem(c, n, k, dtype, qtype, seed=300 + i) for i, (c, n, k) in enumerate(zip(caps, Ns, Ks))]
+    Xs = [to_cuda16(p.X_bits, dtype) for p in probs]
+    blobs = [gpu_prepack(lib, p) for p in probs]
+    outs = [torch.full((c, n), float("nan"), dtype=Xs[0].dtype, device="cuda") for c, n in zip(caps, Ns)]
+    for o in outs:
+        o.view(torch.int16).fill_(0x7E01)
+    M_host = torch.tensor(want, dtype=torch.int32)
+    M_dev = M_host.cuda() * 1 - 0                       # produced by kernels on the stream
+    lib.grouped_mm_device_m(Xs, blobs, M_dev, Ns, qtype=qtype, outs=outs)
+    assert lib.get_last_error() == lib.OK
+    for p, o, c, w in zip(probs, outs, caps, want):
+        m = max(0, min(w, c))
+        got = from_cuda16(o)
+        if m:
+            ref = O.mm_problem(p, rows=range(m))
+            assert_parity(O.decode16(got[:m], dtype), ref, "device counts, M=%d" % m)
+        assert np.all(got[m:] == 0x7E01), "rows past the count were written"
+
+
 def test_mm_cluster_larger_than_groups(opts):
     """A cluster never gets more CTAs than the tile has groups (here K = 256: two groups)."""
     lib = opts

@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH):
         "wq4_grouped_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm": (c_int, [c_int, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_mm_static_scratch": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp]),
+        "wq4_grouped_device_m_workspace_bytes": (c_int, [c_int, ctypes.POINTER(c_size)]),
+        "wq4_grouped_mm_device_m": (c_int, [c_int, vp, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_get_last_error": (c_int, [vp]),
         "wq4_set_option": (c_int, [c_int, ll]),
         "wq4_get_option": (ll, [c_int]),
@@ -231,4 +233,34 @@ def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4
     _check(lib.wq4_grouped_mm(P, arr(*Ms), arr(*Ns), arr(*Ks), xp, wp, yp, GROUP, _dtype_code(Xs[0]), QTYPES[qtype],
                               _cuda(workspace, "workspace"), workspace.numel(), _stream(Xs[0].device)),
            "wq4_grouped_mm")
+    return list(outs)
+
+
+def grouped_mm_device_m(Xs: Sequence, blobs: Sequence, M_dev, N: Sequence[int], qtype: str = "u4b8",
+                        workspace=None, outs: Optional[Sequence] = None, group_size: int = GROUP):
+    """Grouped GEMM with the token counts in device memory (``M_dev``: int32 CUDA tensor [P]).
+    Xs[p] holds M_cap = Xs[p].shape[0] rows (its capacity); only the first M_dev[p] rows of each
+    Y[p] are written."""
+    torch = _torch()
+    lib = load_library()
+    P = len(Xs)
+    caps = [int(x.shape[0]) for x in Xs]
+    Ks = [int(x.shape[1]) for x in Xs]
+    Ns = [int(n) for n in N]
+    if M_dev.dtype != torch.int32 or not M_dev.is_cuda or M_dev.numel() != P:
+        raise ValueError("M_dev must be an int32 CUDA tensor with one entry per problem")
+    if outs is None:
+        outs = [torch.empty((c, n), dtype=x.dtype, device=x.device) for x, c, n in zip(Xs, caps, Ns)]
+    if workspace is None:
+        nb = ctypes.c_size_t(0)
+        _check(lib.wq4_grouped_device_m_workspace_bytes(P, ctypes.byref(nb)), "wq4_grouped_device_m_workspace_bytes")
+        workspace = torch.empty(int(nb.value), dtype=torch.uint8, device=Xs[0].device)
+    arr = ctypes.c_int * P
+    ptrs = ctypes.c_void_p * P
+    xp = ptrs(*[x.data_ptr() if c > 0 else None for x, c in zip(Xs, caps)])
+    wp = ptrs(*[b.data_ptr() for b in blobs])
+    yp = ptrs(*[y.data_ptr() if c > 0 else None for y, c in zip(outs, caps)])
+    _check(lib.wq4_grouped_mm_device_m(P, _cuda(M_dev, "M_dev"), arr(*caps), arr(*Ns), arr(*Ks), xp, wp, yp, group_size,
+                                       _dtype_code(Xs[0]), QTYPES[qtype], _cuda(workspace, "workspace"),
+                                       workspace.numel(), _stream(Xs[0].device)), "wq4_grouped_mm_device_m")
     return list(outs)

@@ -604,6 +604,114 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
     return run_gemm<kMaxGroupedProblems>(shapes, X, Wp, Y, dtype, qtype, workspace, workspace_bytes, stream);
 }
 
+// ------------------------------------------------------------------ device-resident shapes
+namespace wq4 {
+struct DynSetup {
+    int P, nt;
+    int cap[kMaxGroupedProblems];
+    int n_tiles[kMaxGroupedProblems];
+};
+
+// Turns the device array of token counts into the GEMM's tile table: counts clamped to
+// [0, capacity], tiles per problem, first tile of each problem, total (one thread; P <= 64).
+__global__ void dyn_table_kernel(const int* __restrict__ M_dev, const __grid_constant__ DynSetup su, DynTable* t) {
+    if (threadIdx.x != 0) return;
+    int acc = 0;
+    for (int p = 0; p < su.P; ++p) {
+        int m = M_dev[p];
+        m = m < 0 ? 0 : (m > su.cap[p] ? su.cap[p] : m);
+        t->M[p] = m;
+        t->tile_begin[p] = acc;
+        acc += (m + su.nt - 1) / su.nt * su.n_tiles[p];
+    }
+    t->total_tiles = acc;
+}
+}  // namespace wq4
+
+int wq4_grouped_device_m_workspace_bytes(int P, size_t* bytes) {
+    if (!bytes || P <= 0) return WQ4_ERR_INVALID;
+    if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
+    *bytes = (sizeof(DynTable) + 255) / 256 * 256;
+    return WQ4_OK;
+}
+
+int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int* N, const int* K,
+                            const void* const* X, const void* const* Wp, void* const* Y, int group_size, int dtype,
+                            int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if (P <= 0 || !M_dev || !M_cap || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
+    if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(M_dev) & 3) return WQ4_ERR_ALIGN;
+    if (!workspace || workspace_bytes < (sizeof(DynTable) + 255) / 256 * 256) return WQ4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return WQ4_ERR_ALIGN;
+    for (int p = 0; p < P; ++p) {
+        if (M_cap[p] < 0) return WQ4_ERR_INVALID;
+        if ((rc = check_nk(N[p], K[p]))) return rc;
+        if ((rc = check_group(group_size, K[p]))) return rc;
+        if (M_cap[p] > 0) {
+            if (!X[p] || !Wp[p] || !Y[p]) return WQ4_ERR_INVALID;
+            if (!aligned16(X[p]) || !aligned16(Wp[p]) || !aligned16(Y[p])) return WQ4_ERR_ALIGN;
+        }
+    }
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    // Plan for the capacities: the token tile and the grid; every tile whole (the tile count is
+    // known only on the device).
+    const int nt = token_tile_for(M_cap, P);
+    long long max_tiles = 0;
+    auto* prm = new (std::nothrow) GemmParams<kMaxGroupedProblems>();
+    if (!prm) return WQ4_ERR_CUDA;
+    std::memset(static_cast<void*>(prm), 0, sizeof(*prm));
+    DynSetup su;
+    std::memset(static_cast<void*>(&su), 0, sizeof(su));
+    su.P = P;
+    su.nt = nt;
+    for (int p = 0; p < P; ++p) {
+        ProblemDesc& d = prm->prob[p];
+        d.wp = static_cast<const uint8_t*>(Wp[p]) + kBlobHeader;
+        d.y = Y[p];
+        d.M = M_cap[p];
+        d.N = N[p];
+        d.K = K[p];
+        d.n_tiles = N[p] / kTileN;
+        d.m_tiles = (M_cap[p] + nt - 1) / nt;
+        d.k_groups = K[p] / kTileK;
+        d.tile_begin = static_cast<int>(max_tiles);
+        max_tiles += static_cast<long long>(d.m_tiles) * d.n_tiles;
+        su.cap[p] = M_cap[p];
+        su.n_tiles[p] = d.n_tiles;
+        if (M_cap[p] > 0) {
+            rc = encode_x_map(&prm->xmap[p], X[p], M_cap[p], K[p], dtype, nt);
+            if (rc) {
+                delete prm;
+                return rc;
+            }
+        }
+    }
+    if (max_tiles >= (1LL << 30)) {
+        delete prm;
+        return WQ4_ERR_UNSUPPORTED;
+    }
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(dev->sm_count, max_tiles)));
+    prm->num_problems = P;
+    prm->total_tiles = static_cast<int>(max_tiles);
+    prm->dp_tiles = static_cast<int>(max_tiles);
+    prm->num_ctas = grid;
+    prm->status = dev->status;
+    prm->timeout_cycles = timeout_cycles();
+    prm->test_stall = g_opt.test_stall;
+    prm->dyn = static_cast<const DynTable*>(workspace);
+    dyn_table_kernel<<<1, 32, 0, stream>>>(M_dev, su, static_cast<DynTable*>(workspace));
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = dispatch(prm, true, nt, dtype, qtype, grid, stream);
+    if (trace_on())
+        std::fprintf(stderr, "[wq4] device-resident shapes: problems=%d token_tile=%d grid=%d max_tiles=%lld (%s)\n", P,
+                     nt, grid, max_tiles, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+    delete prm;
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
 int wq4_get_last_error(wq4_stream_t stream) {
     const cudaError_t se = cudaStreamSynchronize(stream);
     DeviceInfo* dev = nullptr;

@@ -114,9 +114,12 @@ struct Sched {
         u_end = p.sk_unit_begin + (p.sk_units * (c + 1)) / p.num_ctas;
     }
 
+    // first tile of problem p: from the parameters, or from the device table
+    __device__ int tile_begin(int p) const { return prm.dyn ? prm.dyn->tile_begin[p] : prm.prob[p].tile_begin; }
+
     __device__ int problem_of_tile(int t) const {
         int p = 0;
-        while (p + 1 < prm.num_problems && prm.prob[p + 1].tile_begin <= t) ++p;
+        while (p + 1 < prm.num_problems && tile_begin(p + 1) <= t) ++p;
         return p;
     }
 
@@ -144,12 +147,12 @@ struct Sched {
             s.slot = kSlotCluster;
             return true;
         }
-        if (dp_t < prm.dp_tiles) {
+        if (dp_t < (prm.dyn ? prm.dyn->total_tiles : prm.dp_tiles)) {
             const int t = dp_t;
             dp_t += prm.num_ctas;
             const int p = problem_of_tile(t);
             const ProblemDesc& P = prm.prob[p];
-            const int local = t - P.tile_begin;
+            const int local = t - tile_begin(p);
             s.prob = p;
             s.tile = t;
             s.mt = local / P.n_tiles;
@@ -182,6 +185,12 @@ struct Sched {
         return false;
     }
 };
+
+// Rows (tokens) of problem p: from the parameters, or from the device table.
+template <int MAXP>
+__device__ __forceinline__ int problem_rows(const GemmParams<MAXP>& prm, int p) {
+    return prm.dyn ? prm.dyn->M[p] : prm.prob[p].M;
+}
 
 // CTA whose K-split range holds split-relative unit v (ranges [floor(c U / C), floor((c+1) U / C))).
 __device__ __forceinline__ int sk_cta_of(int v, int U, int C) {
@@ -396,7 +405,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             bool ok = !(prm.test_stall && mine == 0) || mbar_wait(stall_bar, 0, ctl);
             while (ok && sch.next(seg)) {
                 const ProblemDesc& P = prm.prob[seg.prob];
-                const int rows = P.M - seg.mt * NT;
+                const int rows = problem_rows(prm, seg.prob) - seg.mt * NT;
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
@@ -557,6 +566,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 
             // ---------------------------------------------------------- tile epilogue
             const ProblemDesc& P = prm.prob[seg.prob];
+            const int Mrows = problem_rows(prm, seg.prob);
             const int n = seg.nt * kTileN + r;
             const int m0 = seg.mt * NT + col0;
             if (seg.slot == kSlotCluster) {
@@ -628,7 +638,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
             for (int j = 0; j < C::kNC; ++j) {
                 const int m = m0 + j;
-                if (m < P.M)
+                if (m < Mrows)
                     y[static_cast<size_t>(m) * P.N + n] =
                         float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, acc[j], m, n) : acc[j]);
             }
@@ -637,6 +647,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             cluster_sync();   // every rank's partial is in its shared memory
             if (cluster_rank() == 0) {
                 const ProblemDesc& P = prm.prob[seg.prob];
+                const int Mrows = P.M;
                 const int S = prm.cluster_split;
                 const int n = seg.nt * kTileN + r;
                 const int m0 = seg.mt * NT + col0;
@@ -666,7 +677,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m0 + c + j;
-                        if (m < P.M)
+                        if (m < Mrows)
                             y[static_cast<size_t>(m) * P.N + n] =
                                 float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, sum[j], m, n) : sum[j]);
                     }

@@ -28,6 +28,16 @@ struct ProblemDesc {
     int unit_begin;          // global index of the problem's first (tile, group) unit
 };
 
+// Problem sizes known only on the device (tokens routed to experts by a kernel): a set-up kernel
+// writes this table from the device array of token counts; the GEMM then reads M, the tile counts
+// and the first tile of each problem from here instead of its parameters (whole tiles only).
+struct DynTable {
+    int total_tiles;
+    int pad[3];
+    int M[kMaxGroupedProblems];
+    int tile_begin[kMaxGroupedProblems];
+};
+
 // A tile is (problem, m_tile, n_tile); inside a problem tiles run m-major (consecutive tiles
 // share the same activation rows and walk the weight tiles), so the CTAs working at one time
 // share operands in L2. Tiles [0, dp_tiles) are processed whole, tile t by CTA t % num_ctas.
@@ -55,6 +65,7 @@ struct GemmParams {
     int test_stall;          // 1: one wait per CTA on a barrier nothing arrives on (tests)
     int has_epi;             // 1: Y = alpha acc + beta C + bias (else Y = acc)
     float alpha, beta;
+    const DynTable* dyn;     // device-resident problem sizes (see DynTable), or null
 };
 
 }  // namespace wq4
