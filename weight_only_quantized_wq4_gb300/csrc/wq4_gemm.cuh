@@ -73,7 +73,11 @@ struct GemmCfg {
     // (64 columns each). With two, the dequantisation of group g waits for the MMAs of group
     // g - 2 and that chain, not the tensor pipe, sets the pace; a third or fourth buffer lets it
     // run further ahead. In shared memory (the comparison path) two.
-    static constexpr int kABufs = !ATMEM ? 2 : (512 - 2 * NT) / 64 >= 4 ? 4 : (512 - 2 * NT) / 64;
+    // P buffers (group partials). Two: at NT = 128 three P buffers with two operand buffers were
+    // measured slower than two P buffers with four operand buffers (the dequantisation chain
+    // binds before the fold chain does).
+    static constexpr int kPBufs = 2;
+    static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * NT) / 64 >= 4 ? 4 : (512 - kPBufs * NT) / 64;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
@@ -83,8 +87,8 @@ struct GemmCfg {
     static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kWRingBytes) / kXStageBytes;
     static constexpr int kXStages = kXStagesFit > 16 ? 16 : kXStagesFit;
     static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
-    static constexpr int kColA = 2 * NT;                     // TMEM column of A buffer 0
-    static constexpr int kTmemNeed = 2 * NT + (ATMEM ? 64 * kABufs : 0);
+    static constexpr int kColA = kPBufs * NT;                // TMEM column of A buffer 0
+    static constexpr int kTmemNeed = kPBufs * NT + (ATMEM ? 64 * kABufs : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
     static_assert(kXStages >= 2 && kWStages <= 16, "shared memory");
@@ -289,12 +293,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     auto afull_bar = [&](int a) { return s_bar + 8u * (64 + a); };
     auto aempty_bar = [&](int a) { return s_bar + 8u * (68 + a); };
     auto pfull_bar = [&](int b) { return s_bar + 8u * (72 + b); };
-    auto pempty_bar = [&](int b) { return s_bar + 8u * (74 + b); };
+    auto pempty_bar = [&](int b) { return s_bar + 8u * (76 + b); };
     auto wrec_of = [&](int i) { return s_w0 + (i % C::kWStages) * C::kWStageBytes; };
-    const uint32_t drain_bar = s_bar + 8u * 76;
-    const uint32_t fsync_bar = s_bar + 8u * 77;   // fold warps meet here in the split epilogue
-    const uint32_t stall_bar = s_bar + 8u * 78;   // never arrived on (test of the timeout path)
-    uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 80;
+    const uint32_t drain_bar = s_bar + 8u * 80;
+    const uint32_t fsync_bar = s_bar + 8u * 81;   // fold warps meet here in the split epilogue
+    const uint32_t stall_bar = s_bar + 8u * 82;   // never arrived on (test of the timeout path)
+    uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 88;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
     volatile int* const fin_flag = reinterpret_cast<volatile int*>(gmisc + 8);
@@ -315,7 +319,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             mbar_init(afull_bar(a), C::kDQW);
             mbar_init(aempty_bar(a), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kPBufs; ++b) {
             mbar_init(pfull_bar(b), 1);
             mbar_init(pempty_bar(b), C::kFW);
         }
@@ -411,8 +415,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
                     if ((i & 1) != mine) continue;
                     const int s = i % C::kXStages;
-                    const int b = i & 1;                        // P buffer
-                    const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                    const int b = i % C::kPBufs;                // P buffer
+                    const uint32_t u = static_cast<uint32_t>(i / C::kPBufs) & 1u;
                     const int a = i % C::kABufs;                // A buffer
                     if (!mbar_wait(xfull_bar(s), (i / C::kXStages) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(afull_bar(a), (i / C::kABufs) & 1, ctl)) { ok = false; break; }
@@ -526,8 +530,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         while (ok && sch.next(seg)) {
             for (int g = seg.g0; g < seg.g1; ++g, ++i) {
                 const int s = i % C::kWStages;
-                const int b = i & 1;
-                const uint32_t u = static_cast<uint32_t>(i >> 1) & 1u;
+                const int b = i % C::kPBufs;
+                const uint32_t u = static_cast<uint32_t>(i / C::kPBufs) & 1u;
                 if (!mbar_wait(pfull_bar(b), u, ctl)) { ok = false; break; }
                 if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
                 tc_fence_after();
