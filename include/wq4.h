@@ -89,9 +89,10 @@ int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int q
  * ------------------------------------------------------------------------------------------ */
 
 /* Workspace bytes wq4_mm needs on the current device for this shape (partial sums of K-split
- * tiles and their arrival counters). The workspace must be zero-filled once when allocated;
- * every completed call leaves its counters at zero again. Calls that may overlap on the GPU
- * need separate workspaces. */
+ * tiles and their arrival counters) under the current options; 0 when the call takes the
+ * decode kernel (M <= 32), which uses none (workspace may then be NULL). The workspace must be
+ * zero-filled once when allocated; every completed call leaves its counters at zero again.
+ * Calls that may overlap on the GPU need separate workspaces. */
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
 
 /* Y = X . dequant(Wp)^T.

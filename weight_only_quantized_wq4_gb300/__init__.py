@@ -196,8 +196,9 @@ def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_siz
     M, K = X.shape
     if out is None:
         out = torch.empty((M, N), dtype=X.dtype, device=X.device)
-    if workspace is None:
-        workspace = alloc_workspace(workspace_bytes(M, N, K, group_size), X.device) if M > 0 else None
+    if workspace is None and M > 0:
+        nbytes = workspace_bytes(M, N, K, group_size)
+        workspace = alloc_workspace(nbytes, X.device) if nbytes > 0 else None   # decode sizes need none
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_n = workspace.numel() if workspace is not None else 0
     if alpha == 1.0 and beta == 0.0 and C is None and bias is None:

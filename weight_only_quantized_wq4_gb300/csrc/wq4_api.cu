@@ -112,6 +112,13 @@ int check_group(int group_size, int K) {
     return WQ4_OK;
 }
 
+// wq4_mm takes the decode kernel (no workspace) for this M, K under the current options.
+bool uses_decode_kernel(int M, int K) {
+    const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
+                             !g_opt.cluster && !g_opt.a_in_smem;
+    return decode_fits(M, K) && (g_opt.decode == 1 || auto_decode);
+}
+
 int check_nk(int N, int K) {
     if (N <= 0 || K <= 0) return WQ4_ERR_INVALID;
     if (N % kTileN || K % kTileK) return WQ4_ERR_UNSUPPORTED;
@@ -530,7 +537,9 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
 }
 
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
-    return wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
+    const int rc = wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
+    if (rc == WQ4_OK && M > 0 && uses_decode_kernel(M, K)) *bytes = 0;   // that kernel needs none
+    return rc;
 }
 
 static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype,
@@ -545,10 +554,7 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
     if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
     // decode-sized M: the warp-level MMA kernel (whole row blocks per CTA, no workspace)
-    const bool decode_ok = decode_fits(M, K);
-    const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
-                             !g_opt.cluster && !g_opt.a_in_smem;
-    if (decode_ok && (g_opt.decode == 1 || auto_decode)) {
+    if (uses_decode_kernel(M, K)) {
         DeviceInfo* dev = nullptr;
         if ((rc = device_info(&dev))) return rc;
         EncodeTiledFn fn = encode_fn();

@@ -124,15 +124,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
-// Bounded wait without the abort protocol (used only on the way out of an aborted CTA).
-__device__ __forceinline__ bool mbar_wait_plain_dec(uint32_t bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > limit) return false;
-    }
-    return true;
-}
-
 template <int NB, bool BF16, bool ZP>
 __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
     using C = DecCfg<NB>;
@@ -326,7 +317,7 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     // A CTA that gave up (the flag is final after the barrier above; a warp waits only for the
     // activation pieces of its own groups) lets every activation copy land before it exits.
     if (threadIdx.x == 0 && *abort_flag) {
-        for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain_dec(s_bar + 8 * q, 0, drain_limit(prm.timeout_cycles));
+        for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain(s_bar + 8 * q, 0, drain_limit(prm.timeout_cycles));
     }
     if (active && ks == 0) {
         uint16_t* y = reinterpret_cast<uint16_t*>(prm.y);

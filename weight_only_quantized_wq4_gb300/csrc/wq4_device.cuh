@@ -61,6 +61,15 @@ __host__ __device__ inline long long drain_limit(long long timeout_cycles) {
     return timeout_cycles > kDrainCycles ? timeout_cycles : kDrainCycles;
 }
 
+// Bounded wait without the abort protocol (the drains of a CTA that gave up).
+__device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
 // Shared state every role consults so that one timed-out wait stops the whole CTA.
 struct WaitCtl {
     volatile int* abort_flag;      // shared memory
@@ -261,10 +270,6 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
 
 __device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
     asm volatile("st.relaxed.gpu.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

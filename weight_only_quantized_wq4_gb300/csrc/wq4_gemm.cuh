@@ -265,14 +265,6 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a, uint32_t b0,
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
 }
 
-__device__ __forceinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, long long limit) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > limit) return false;
-    }
-    return true;
-}
-
 template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
 __global__ void __launch_bounds__(GemmCfg<NT, ZP, ATMEM>::kThreads, 1)
 wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
