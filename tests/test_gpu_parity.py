@@ -146,6 +146,8 @@ DECODE = [
     (8, 384, 8960, "bf16", "u4_zp"), (9, 512, 1024, "bf16", "u4b8"), (16, 1024, 2048, "fp16", "u4b8"),
     (17, 256, 640, "bf16", "u4_zp"), (24, 128, 1024, "fp16", "u4b8"), (32, 2048, 2048, "bf16", "u4_zp"),
     (3, 14336, 512, "bf16", "u4b8"),
+    # 17..32 tokens whose activations do not fit at once: two launches of at most 16 rows
+    (24, 512, 4096, "bf16", "u4b8"), (32, 384, 2560, "fp16", "u4_zp"), (17, 256, 4096, "bf16", "u4_zp"),
 ]
 
 
@@ -267,7 +269,8 @@ def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
 
 @pytest.mark.parametrize("M,N,K,dtype,split_all,in_place", [
     (200, 14336, 256, "bf16", 0, False), (200, 14336, 256, "bf16", 1, False), (100, 256, 1152, "fp16", 0, False),
-    (8, 512, 1024, "bf16", 0, False), (24, 256, 512, "fp16", 0, True), (300, 384, 512, "bf16", 0, True)])
+    (8, 512, 1024, "bf16", 0, False), (24, 256, 512, "fp16", 0, True), (300, 384, 512, "bf16", 0, True),
+    (28, 256, 4096, "fp16", 0, True)])
 def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     """Y = alpha acc + beta C + bias on the data-parallel, K-split, cluster and decode paths, and
     in place (C is Y)."""

@@ -112,12 +112,22 @@ int check_group(int group_size, int K) {
     return WQ4_OK;
 }
 
-// wq4_mm takes the decode kernel (no workspace) for this M, K under the current options.
-bool uses_decode_kernel(int M, int K) {
+// Rows per decode-kernel launch when wq4_mm takes that kernel (no workspace) for this M, N, K
+// under the current options, else 0. Up to 32 tokens in one launch when their activations fit
+// in shared memory; beyond that (17..32 tokens at large K) two launches of at most 16 tokens each
+// for weights up to 24 Mi elements, which read the weights twice and still beat the
+// tensor-core kernel there (measured, 32 tokens: N = K = 4096 12.96 vs 18.3 us; at N = 14336,
+// K = 4096 the tensor-core kernel is faster, 26.6 vs 27.7 us).
+int decode_rows_per_launch(int M, int N, int K) {
     const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
                              !g_opt.cluster && !g_opt.a_in_smem;
-    return decode_fits(M, K) && (g_opt.decode == 1 || auto_decode);
+    if (!(g_opt.decode == 1 || auto_decode)) return 0;
+    if (decode_fits(M, K)) return M;
+    if (M > 16 && M <= 32 && decode_fits(16, K) && static_cast<long long>(N) * K <= 24LL * 1024 * 1024) return 16;
+    return 0;
 }
+
+bool uses_decode_kernel(int M, int N, int K) { return decode_rows_per_launch(M, N, K) > 0; }
 
 int check_nk(int N, int K) {
     if (N <= 0 || K <= 0) return WQ4_ERR_INVALID;
@@ -538,7 +548,7 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
 
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
     const int rc = wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
-    if (rc == WQ4_OK && M > 0 && uses_decode_kernel(M, K)) *bytes = 0;   // that kernel needs none
+    if (rc == WQ4_OK && M > 0 && uses_decode_kernel(M, N, K)) *bytes = 0;   // that kernel needs none
     return rc;
 }
 
@@ -554,19 +564,30 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
     if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
     // decode-sized M: the warp-level MMA kernel (whole row blocks per CTA, no workspace)
-    if (uses_decode_kernel(M, K)) {
+    if (const int rows = decode_rows_per_launch(M, N, K)) {
         DeviceInfo* dev = nullptr;
         if ((rc = device_info(&dev))) return rc;
         EncodeTiledFn fn = encode_fn();
         if (!fn) return WQ4_ERR_CUDA;
-        int grid = 0, rb = 0;
-        const cudaError_t e = launch_decode(X, Wp, Y, M, N, K, dtype, qtype, dev->sm_count, dev->status,
-                                            timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0,
-                                            g_opt.test_stall, epi, &grid, &rb, stream);
-        if (trace_on())
-            std::fprintf(stderr, "[wq4] decode kernel: M=%d N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n", M, N, K,
-                         grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
-        return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+        for (int m0 = 0; m0 < M; m0 += rows) {   // one launch, or two of at most 16 rows
+            const int mr = M - m0 < rows ? M - m0 : rows;
+            const uint8_t* x = static_cast<const uint8_t*>(X) + static_cast<size_t>(m0) * K * 2;
+            uint8_t* y = static_cast<uint8_t*>(Y) + static_cast<size_t>(m0) * N * 2;
+            EpilogueArgs e_part;
+            if (epi) {
+                e_part = *epi;
+                if (e_part.c) e_part.c = static_cast<const uint8_t*>(e_part.c) + static_cast<size_t>(m0) * N * 2;
+            }
+            int grid = 0, rb = 0;
+            const cudaError_t e = launch_decode(x, Wp, y, mr, N, K, dtype, qtype, dev->sm_count, dev->status,
+                                                timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0,
+                                                g_opt.test_stall, epi ? &e_part : nullptr, &grid, &rb, stream);
+            if (trace_on())
+                std::fprintf(stderr, "[wq4] decode kernel: M=%d (rows %d..%d) N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n",
+                             M, m0, m0 + mr, N, K, grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+            if (e != cudaSuccess) return WQ4_ERR_CUDA;
+        }
+        return WQ4_OK;
     }
     std::vector<Shape> shapes{{M, N, K}};
     const void* xs[1] = {X};
