@@ -566,8 +566,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             const int n = seg.nt * kTileN + r;
             const int m0 = seg.mt * NT + col0;
             if (seg.slot == kSlotCluster) {
-                // partial sum to this CTA's shared memory (the stages are idle now); rank 0 of the
-                // cluster adds the S partials after the cluster barrier below
+                // partial sum to this CTA's shared memory (the stages are idle now); after the
+                // cluster barrier below every rank adds the S partials of its slice of columns
 #pragma unroll
                 for (int j = 0; j < C::kNC; ++j)
                     asm volatile("st.shared.f32 [%0], %1;" ::"r"(s_x0 + ((col0 + j) * 128 + r) * 4), "f"(acc[j])
@@ -641,16 +641,20 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
         if (prm.cluster_split > 0) {
             cluster_sync();   // every rank's partial is in its shared memory
-            if (cluster_rank() == 0) {
+            {
+                // Each rank of the cluster adds the S partials (in rank order) for its own slice of
+                // the token columns, [rank NT / S, (rank + 1) NT / S), and writes that slice of Y:
+                // the reads through distributed shared memory are spread over the cluster.
                 const ProblemDesc& P = prm.prob[seg.prob];
                 const int Mrows = P.M;
                 const int S = prm.cluster_split;
+                const int q = static_cast<int>(cluster_rank());
                 const int n = seg.nt * kTileN + r;
-                const int m0 = seg.mt * NT + col0;
+                const int cb = max((q * NT) / S, col0), ce = min(((q + 1) * NT) / S, col0 + C::kNC);
                 constexpr int kBatch = C::kNC <= 64 ? 4 : 2;   // parts of a 16-column batch loaded together
                 uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
-#pragma unroll
-                for (int c = 0; c < C::kNC; c += 16) {
+                for (int c = cb; c < ce; c += 16) {
+                    const int nc = ce - c < 16 ? ce - c : 16;
                     float sum[16];
                     for (int q0 = 0; q0 < S; q0 += kBatch) {
                         float v[kBatch][16];
@@ -659,7 +663,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             if (q0 + b < S) {
                                 const uint32_t base = map_to_rank(s_x0, static_cast<uint32_t>(q0 + b));
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) v[b][j] = ld_cluster_f32(base + ((col0 + c + j) * 128 + r) * 4);
+                                for (int j = 0; j < 16; ++j)
+                                    if (j < nc) v[b][j] = ld_cluster_f32(base + ((c + j) * 128 + r) * 4);
                             }
                         }
 #pragma unroll
@@ -672,14 +677,14 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c + j;
-                        if (m < Mrows)
+                        const int m = seg.mt * NT + c + j;
+                        if (j < nc && m < Mrows)
                             y[static_cast<size_t>(m) * P.N + n] =
                                 float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, sum[j], m, n) : sum[j]);
                     }
                 }
             }
-            cluster_sync();   // no CTA leaves while rank 0 still reads its shared memory
+            cluster_sync();   // no CTA leaves while another still reads its shared memory
         }
     }
     if (prm.cluster_split > 0 && warp < 4 + C::kDQW) {
