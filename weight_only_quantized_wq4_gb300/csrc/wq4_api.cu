@@ -115,15 +115,15 @@ int check_group(int group_size, int K) {
 // Rows per decode-kernel launch when wq4_mm takes that kernel (no workspace) for this M, N, K
 // under the current options, else 0. Up to 32 tokens in one launch when their activations fit
 // in shared memory; beyond that (17..32 tokens at large K) two launches of at most 16 tokens each
-// for weights up to 24 Mi elements, which read the weights twice and still beat the
-// tensor-core kernel there (measured, 32 tokens: N = K = 4096 12.96 vs 18.3 us; at N = 14336,
-// K = 4096 the tensor-core kernel is faster, 26.6 vs 27.7 us).
+// for weights up to 12 Mi elements, which read the weights twice and still beat the
+// tensor-core kernel there (measured, 32 tokens, K = 4096: N = 2048 8.8 vs 11.3 us; at N = 4096
+// the two are even, beyond it the tensor-core kernel wins).
 int decode_rows_per_launch(int M, int N, int K) {
     const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
                              !g_opt.cluster && !g_opt.a_in_smem;
     if (!(g_opt.decode == 1 || auto_decode)) return 0;
     if (decode_fits(M, K)) return M;
-    if (M > 16 && M <= 32 && decode_fits(16, K) && static_cast<long long>(N) * K <= 24LL * 1024 * 1024) return 16;
+    if (M > 16 && M <= 32 && decode_fits(16, K) && static_cast<long long>(N) * K <= 12LL * 1024 * 1024) return 16;
     return 0;
 }
 
@@ -223,7 +223,9 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     if (g_opt.cluster >= 2) {
         S = g_opt.cluster;
     } else if (g_opt.cluster == 0 && !g_opt.split_all && !g_opt.grid && tiles * 2 <= sm_count) {
-        S = static_cast<int>(std::min<long long>(8, sm_count / tiles));
+        // clusters of 8 only for at most 8 tiles: 16 clusters of 8 did not fit in one wave
+        // (N = 2048, 16 tiles: 19.7 us with 8, 11.3 us with 4)
+        S = static_cast<int>(std::min<long long>(tiles <= 8 ? 8 : 4, sm_count / tiles));
     }
     S = std::min(S, min_kg);
     if (S >= 2) {
@@ -420,7 +422,9 @@ int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
     if (g_opt.cluster >= 2) {
         S = g_opt.cluster;
     } else if (g_opt.cluster == 0 && !g_opt.split_all && !g_opt.grid && tiles * 2 <= sm_count) {
-        S = static_cast<int>(std::min<long long>(8, sm_count / tiles));
+        // clusters of 8 only for at most 8 tiles: 16 clusters of 8 did not fit in one wave
+        // (N = 2048, 16 tiles: 19.7 us with 8, 11.3 us with 4)
+        S = static_cast<int>(std::min<long long>(tiles <= 8 ? 8 : 4, sm_count / tiles));
     }
     S = std::min(S, kg);
     if (S >= 2) {
