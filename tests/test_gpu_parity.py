@@ -148,6 +148,9 @@ DECODE = [
     (3, 14336, 512, "bf16", "u4b8"),
     # 17..32 tokens whose activations do not fit at once: two launches of at most 16 rows
     (24, 512, 4096, "bf16", "u4b8"), (32, 384, 2560, "fp16", "u4_zp"), (17, 256, 4096, "bf16", "u4_zp"),
+    # three row blocks per CTA (one warp idle), long K at 8 tokens
+    (7, 7296, 3840, "fp16", "u4_zp"), (2, 6144, 1024, "fp16", "u4b8"), (8, 256, 8960, "bf16", "u4b8"),
+    (8, 4096, 6144, "bf16", "u4_zp"),
 ]
 
 
@@ -158,6 +161,43 @@ def test_decode_kernel(opts, M, N, K, dtype, qtype):
     lib.set_option(lib.OPT_DECODE, 1)
     p = I.make_problem(M, N, K, dtype, qtype, seed=M * 13 + N + K)
     assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "decode %s" % ((M, N, K, dtype, qtype),))
+
+
+def test_decode_chain_in_a_graph(opts):
+    """Programmatic dependent launch on the decode kernel: a graph of calls, each call's activations
+    the previous call's output (N = K). The same bits as plain stream order, and the first call
+    matches the oracle."""
+    import torch
+    lib = opts
+    M, K = 8, 4096
+    ps = [I.make_problem(M, K, K, "bf16", "u4b8", seed=900 + i) for i in range(6)]
+    blobs = [gpu_prepack(lib, p) for p in ps]
+    X0 = to_cuda16(ps[0].X_bits, "bf16")
+    torch.cuda.synchronize()
+
+    def chain(pdl):
+        lib.set_option(lib.OPT_PDL, pdl)
+        st = torch.cuda.Stream()
+        outs = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in ps]
+        with torch.cuda.stream(st):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                x = X0
+                for i in range(len(ps)):
+                    lib.mm(x, blobs[i], K, qtype="u4b8", out=outs[i])
+                    x = outs[i]
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+        assert lib.get_last_error() == lib.OK
+        return [from_cuda16(o) for o in outs]
+
+    a = chain(0)
+    b = chain(-1)
+    for i in range(len(ps)):
+        assert np.array_equal(a[i], b[i]), "call %d differs with programmatic launch" % i
+    assert_parity(O.decode16(a[0], "bf16"), O.mm_problem(ps[0]), "decode chain call 0")
 
 
 def test_decode_kernel_deterministic(opts):
@@ -240,13 +280,14 @@ def test_gemm_back_to_back_in_a_graph(opts, M, split_all):
 
 
 @pytest.mark.parametrize("M,N,K,split_all", [(100, 256, 1152, 0), (200, 14336, 256, 0), (200, 14336, 256, 1),
-                                           (8, 512, 1024, 0), (24, 256, 512, 0)])
+                                           (8, 512, 1024, 0), (24, 256, 512, 0), (4, 14336, 4096, 0)])
 def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
     """Failure detection without a fault: each CTA waits once on a barrier that nothing arrives on
     (WQ4_OPT_TEST_STALL) under a short bound (2e5 cycles, ~0.1 ms); the wait runs out, the CTA
     stops, lets its copies and MMAs finish, frees its tensor memory and exits. The host reads
     WQ4_ERR_TIMEOUT, the status word is cleared, and the next call (normal bound, fresh
-    workspace) is correct. Cluster (M=100), data-parallel, K-split and both decode shapes."""
+    workspace) is correct. Cluster (M=100), data-parallel, K-split and decode shapes (one and six
+    row blocks per CTA)."""
     import torch
     lib = opts
     p = I.make_problem(M, N, K, "bf16", "u4b8", seed=M + N + K)
@@ -270,7 +311,7 @@ def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
 @pytest.mark.parametrize("M,N,K,dtype,split_all,in_place", [
     (200, 14336, 256, "bf16", 0, False), (200, 14336, 256, "bf16", 1, False), (100, 256, 1152, "fp16", 0, False),
     (8, 512, 1024, "bf16", 0, False), (24, 256, 512, "fp16", 0, True), (300, 384, 512, "bf16", 0, True),
-    (28, 256, 4096, "fp16", 0, True)])
+    (28, 256, 4096, "fp16", 0, True), (6, 14336, 4096, "bf16", 0, True)])
 def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     """Y = alpha acc + beta C + bias on the data-parallel, K-split, cluster and decode paths, and
     in place (C is Y)."""
