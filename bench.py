@@ -10,6 +10,11 @@ on the launching stream, max over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
+Variants of a workload (measured like the workload itself; the default line uses none):
+  --group-size G / --no-scales   other group sizes, or uint4b8 without scales (direct conversion)
+  --epilogue                     Y = X.dequant(W)^T + C + bias through wq4_mm_ex (C, bias read)
+  --device-m                     grouped workload with its token counts in device memory
+
 With N > 1 (launched by torch.distributed.run) every rank runs its own replica of the workload
 (weak scaling; the GEMM needs no exchange) and value = all ranks' work / max time.
 --impl reference times the CPU oracle (fp64 NumPy) on this host's cores instead.
@@ -58,6 +63,44 @@ def kernel_source_hash() -> str:
             h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def variant_of(args):
+    """Non-default variant flags as config entries (empty for the plain workload)."""
+    v = {}
+    if args.group_size != I.GROUP:
+        v["group_size"] = args.group_size
+    if args.no_scales:
+        v["scales"] = "none (direct conversion)"
+    if args.epilogue:
+        v["epilogue"] = "Y = acc + C + bias (wq4_mm_ex)"
+    if args.device_m:
+        v["token_counts"] = "device memory (wq4_grouped_mm_device_m)"
+    return v
+
+
+def make_inputs(args):
+    """The workload's seeded problems, drawn with the variant's group size / scales."""
+    spec = dict(I.WORKLOADS[args.workload])
+    kind = spec.pop("kind")
+    if args.no_scales and spec["qtype"] != I.U4B8:
+        raise SystemExit("--no-scales applies to uint4b8 weights")
+    if kind == "mm":
+        return I.make_problem(**spec, group_size=args.group_size, scaled=not args.no_scales)
+    if args.group_size != I.GROUP or args.no_scales or args.epilogue:
+        raise SystemExit("--group-size, --no-scales and --epilogue apply to single-problem workloads")
+    return I.make_grouped(**spec)
+
+
+def variant_bytes(p, args):
+    """Algorithmic bytes of one problem under the variant: the scales it really has, and C and
+    bias read by the epilogue."""
+    b = I.algorithmic_bytes(p.M, p.N, p.K, p.qtype, args.group_size)
+    if args.no_scales:
+        b -= 2 * (p.K // args.group_size) * p.N
+    if args.epilogue:
+        b += 2 * p.M * p.N + 2 * p.N
+    return b
 
 
 def workload_shapes(name, probs):
@@ -142,11 +185,18 @@ def run_gpu(args, rank, world, local_rank):
         wq4.set_option(wq4.OPT_A_IN_SMEM, 1)
     pk = peaks()
 
-    probs = I.make_workload(args.workload)
+    probs = make_inputs(args)
     grouped = isinstance(probs, list)
+    if args.device_m and not grouped:
+        raise SystemExit("--device-m applies to the grouped workload")
     plist = probs if grouped else [probs]
     byts, flops, cfg, dtype = workload_shapes(args.workload, probs)
+    variant = variant_of(args)
+    if variant:
+        byts = sum(variant_bytes(p, args) for p in plist)
+        cfg = dict(cfg, **variant)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    G = args.group_size
 
     def c16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
@@ -156,16 +206,25 @@ def run_gpu(args, rank, world, local_rank):
 
     # one resident copy of the inputs, prepacked once
     base_X = [c16(p.X_bits) if p.M > 0 else torch.empty((0, p.K), dtype=tdt, device=dev) for p in plist]
-    base_W = [wq4.prepack(c32(p.Wq), c16(p.S_bits), c32(p.Z) if p.Z is not None else None, qtype=p.qtype)
+    base_W = [wq4.prepack(c32(p.Wq), c16(p.S_bits) if p.S_bits is not None else None,
+                          c32(p.Z) if p.Z is not None else None, qtype=p.qtype, group_size=G, dtype=dtype)
               for p in plist]
+    rng = np.random.default_rng(7)
+    base_C = [c16(I.f32_to_bits(rng.standard_normal((p.M, p.N)).astype(np.float32), dtype)) for p in plist] \
+        if args.epilogue else None
+    base_b = [c16(I.f32_to_bits(rng.standard_normal(p.N).astype(np.float32), dtype)) for p in plist] \
+        if args.epilogue else None
     torch.cuda.synchronize()
     qtype = plist[0].qtype
-    if grouped:
+    if args.device_m:
+        ws_bytes = wq4.grouped_device_m_workspace_bytes(len(plist))
+    elif grouped:
         ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
     else:
-        ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K)
+        ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G)
     set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in base_W) + \
-        sum(p.M * p.N * 2 for p in plist) + ws_bytes
+        sum(p.M * p.N * 2 for p in plist) * (2 if args.epilogue else 1) + ws_bytes
+    M_dev = torch.tensor([p.M for p in plist], dtype=torch.int32, device=dev) if args.device_m else None
     R = max(2, math.ceil(3 * L2_BYTES / set_bytes))
     copies = []
     for r in range(R):
@@ -173,15 +232,24 @@ def run_gpu(args, rank, world, local_rank):
         Ws = [w.clone() for w in base_W]
         Ys = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
         ws = wq4.alloc_workspace(ws_bytes, dev)
-        copies.append((Xs, Ws, Ys, ws))
+        Cs = [c.clone() for c in base_C] if args.epilogue else None
+        copies.append((Xs, Ws, Ys, ws, Cs))
     torch.cuda.synchronize()
 
-    def step(c):
-        Xs, Ws, Ys, ws = copies[c % R]
-        if grouped:
+    def call(Xs, Ws, Ys, ws, Cs, bias):
+        if args.device_m:
+            wq4.grouped_mm_device_m(Xs, Ws, M_dev, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys)
+        elif grouped:
             wq4.grouped_mm(Xs, Ws, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys)
+        elif args.epilogue:
+            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G, C=Cs[0],
+                   beta=1.0, bias=bias[0])
         else:
-            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0])
+            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G)
+
+    def step(c):
+        Xs, Ws, Ys, ws, Cs = copies[c % R]
+        call(Xs, Ws, Ys, ws, Cs, base_b)
 
     stream = torch.cuda.Stream(dev)
     K, W = args.steps, args.warmup
@@ -240,11 +308,13 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the public API from pinned host buffers: H2D of the step's inputs
     # (activations and the prepacked weight), the call, D2H of the result.
-    e2e = None if args.profile_run else run_e2e(args, wq4, plist, base_W, grouped, qtype, ws_bytes, dev, tdt,
+    e2e = None if args.profile_run else run_e2e(args, plist, base_W, base_C, base_b, call, ws_bytes, dev, tdt,
                                                  byts, flops, bound)
 
     traffic = None
     try:
+        if variant:
+            raise LookupError("no capture of the variant")
         with open(PROFILE_TRAFFIC) as f:
             tr = json.load(f)
         ent = tr.get(args.workload)
@@ -279,34 +349,38 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "e2e": e2e,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run:
+    if variant:
+        out["cpu_baseline"] = None   # the oracle's row-sampled step covers the plain workloads only
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run:
         out["cpu_baseline"] = cpu_baseline(args.workload, probs, byts, flops, bound, budget_s=args.cpu_seconds)
     return out
 
 
-def run_e2e(args, wq4, plist, base_W, grouped, qtype, ws_bytes, dev, tdt, byts, flops, bound):
+def run_e2e(args, plist, base_W, base_C, base_b, call, ws_bytes, dev, tdt, byts, flops, bound):
+    """The same call from pinned host buffers: H2D of the step's inputs (activations, prepacked
+    weight, and C and bias with the epilogue), the call, D2H of the result."""
     import torch
+    import weight_only_quantized_wq4_gb300 as wq4
     steps = max(3, min(args.steps, 20))
     hX = [torch.from_numpy(np.ascontiguousarray(p.X_bits).view(np.int16)).view(tdt).pin_memory() for p in plist]
     hW = [w.cpu().pin_memory() for w in base_W]
+    hC = [c.cpu().pin_memory() for c in base_C] if base_C is not None else []
+    hb = [b.cpu().pin_memory() for b in base_b] if base_b is not None else []
     hY = [torch.empty((p.M, p.N), dtype=tdt).pin_memory() for p in plist]
     dX = [torch.empty_like(x, device=dev) for x in hX]
     dW = [torch.empty_like(w, device=dev) for w in hW]
+    dC = [torch.empty_like(c, device=dev) for c in hC]
+    db = [torch.empty_like(b, device=dev) for b in hb]
     dY = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
     ws = wq4.alloc_workspace(ws_bytes, dev)
     stream = torch.cuda.Stream(dev)
-    h2d = sum(x.numel() * 2 for x in hX) + sum(w.numel() for w in hW)
+    h2d = sum(t.numel() * t.element_size() for t in hX + hW + hC + hb)
     d2h = sum(y.numel() * 2 for y in hY)
 
     def one():
-        for a, b in zip(dX, hX):
+        for a, b in zip(dX + dW + dC + db, hX + hW + hC + hb):
             a.copy_(b, non_blocking=True)
-        for a, b in zip(dW, hW):
-            a.copy_(b, non_blocking=True)
-        if grouped:
-            wq4.grouped_mm(dX, dW, [p.N for p in plist], qtype=qtype, workspace=ws, outs=dY)
-        else:
-            wq4.mm(dX[0], dW[0], plist[0].N, qtype=qtype, workspace=ws, out=dY[0])
+        call(dX, dW, dY, ws, dC or None, db or None)
         for a, b in zip(hY, dY):
             a.copy_(b, non_blocking=True)
 
@@ -453,6 +527,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--a-in-smem", action="store_true", help="dequantised operand via shared memory")
+    ap.add_argument("--group-size", type=int, default=I.GROUP, help="variant: quantisation group size")
+    ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
+    ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")
+    ap.add_argument("--device-m", action="store_true", help="variant: grouped token counts in device memory")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up and the timed replay (for profiler runs): no soak, e2e or CPU baseline")
     args = ap.parse_args()

@@ -237,6 +237,14 @@ def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4
     return list(outs)
 
 
+def grouped_device_m_workspace_bytes(P: int) -> int:
+    """Workspace of wq4_grouped_mm_device_m for P problems (the device tile table)."""
+    nb = ctypes.c_size_t(0)
+    _check(load_library().wq4_grouped_device_m_workspace_bytes(P, ctypes.byref(nb)),
+           "wq4_grouped_device_m_workspace_bytes")
+    return int(nb.value)
+
+
 def grouped_mm_device_m(Xs: Sequence, blobs: Sequence, M_dev, N: Sequence[int], qtype: str = "u4b8",
                         workspace=None, outs: Optional[Sequence] = None, group_size: int = GROUP):
     """Grouped GEMM with the token counts in device memory (``M_dev``: int32 CUDA tensor [P]).
@@ -253,9 +261,7 @@ def grouped_mm_device_m(Xs: Sequence, blobs: Sequence, M_dev, N: Sequence[int], 
     if outs is None:
         outs = [torch.empty((c, n), dtype=x.dtype, device=x.device) for x, c, n in zip(Xs, caps, Ns)]
     if workspace is None:
-        nb = ctypes.c_size_t(0)
-        _check(lib.wq4_grouped_device_m_workspace_bytes(P, ctypes.byref(nb)), "wq4_grouped_device_m_workspace_bytes")
-        workspace = torch.empty(int(nb.value), dtype=torch.uint8, device=Xs[0].device)
+        workspace = torch.empty(grouped_device_m_workspace_bytes(P), dtype=torch.uint8, device=Xs[0].device)
     arr = ctypes.c_int * P
     ptrs = ctypes.c_void_p * P
     xp = ptrs(*[x.data_ptr() if c > 0 else None for x, c in zip(Xs, caps)])

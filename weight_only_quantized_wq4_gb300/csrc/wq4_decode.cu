@@ -309,6 +309,35 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     }
     cp_async_wait<0>();
 
+    // the epilogue's C values and bias for the rows this warp writes, loaded now so that their
+    // latency overlaps the exchange of partials below (each element is read here and written
+    // later by the same thread, so C may be Y itself)
+    const bool writer = active && ks == 0;
+    const int n0 = block * 16 + g;
+    uint16_t cv[NB][4];
+    float bv[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) cv[nb][t] = 0;
+    if (writer && prm.has_epi) {
+        if (prm.beta != 0.f) {
+            const uint16_t* cp = static_cast<const uint16_t*>(prm.c);
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int m = nb * 8 + 2 * c + (t & 1);
+                    if (m < prm.M) cv[nb][t] = cp[static_cast<size_t>(m) * prm.N + n0 + (t >> 1) * 8];
+                }
+        }
+        if (prm.bias) {
+            const uint16_t* bp = static_cast<const uint16_t*>(prm.bias);
+            bv[0] = dec_to_float<BF16>(bp[n0]);
+            bv[1] = dec_to_float<BF16>(bp[n0 + 8]);
+        }
+    }
+
     // slice partials -> shared memory, then slice 0 adds them in slice order and writes Y
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
@@ -320,9 +349,8 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     if (threadIdx.x == 0 && *abort_flag) {
         for (int q = 0; q < prm.x_pieces; ++q) mbar_wait_plain(s_bar + 8 * q, 0, drain_limit(prm.timeout_cycles));
     }
-    if (active && ks == 0) {
+    if (writer) {
         uint16_t* y = reinterpret_cast<uint16_t*>(prm.y);
-        const int n0 = block * 16 + g;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -342,9 +370,8 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
                     float val = v[t];
                     if (prm.has_epi) {   // alpha acc + beta C + bias in fp32, rounded once below
                         val *= prm.alpha;
-                        if (prm.beta != 0.f)
-                            val = fmaf(prm.beta, dec_to_float<BF16>(static_cast<const uint16_t*>(prm.c)[static_cast<size_t>(m) * prm.N + n]), val);
-                        if (prm.bias) val += dec_to_float<BF16>(static_cast<const uint16_t*>(prm.bias)[n]);
+                        if (prm.beta != 0.f) val = fmaf(prm.beta, dec_to_float<BF16>(cv[nb][t]), val);
+                        if (prm.bias) val += bv[t >> 1];
                     }
                     uint16_t o;
                     if constexpr (BF16) {

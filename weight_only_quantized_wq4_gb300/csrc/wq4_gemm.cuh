@@ -241,18 +241,50 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
     }
 }
 
-// The epilogue with a source operand (after the C load and alpha / beta of the epilogue in
-// "sm90_gemm_array_tma_warpspecialized_cooperative.hpp"), plus a bias per weight row:
-// alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once by the caller. C may be Y itself:
-// each element is read and then written by the same thread.
+// Writes Y[m0 + j][n] for j < nc (at most 16) and m0 + j < Mrows, with the epilogue when the call
+// has one: alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once (after the C load and
+// alpha / beta of the epilogue in "sm90_gemm_array_tma_warpspecialized_cooperative.hpp", plus a
+// bias per weight row). The C values of 8 columns at a time are loaded together (independent
+// loads in flight at once) before those outputs are formed; C may be Y itself, each element being read and
+// then written by the same thread. `bias` is the row's bias as float (used only when the problem
+// has one).
 template <bool BF16, int MAXP>
-__device__ __forceinline__ float epilogue_value(const GemmParams<MAXP>& prm, const ProblemDesc& P, float v, int m,
-                                                int n) {
-    float r = prm.alpha * v;
-    if (prm.beta != 0.f)
-        r = fmaf(prm.beta, scale_to_float<BF16>(static_cast<const uint16_t*>(P.c)[static_cast<size_t>(m) * P.N + n]), r);
-    if (P.bias) r += scale_to_float<BF16>(static_cast<const uint16_t*>(P.bias)[n]);
-    return r;
+__device__ __forceinline__ void store_cols16(const GemmParams<MAXP>& prm, const ProblemDesc& P, const float (&v)[16],
+                                             int nc, int m0, int n, int Mrows, float bias) {
+    uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
+    if (!prm.has_epi) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < nc && m0 + j < Mrows) y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(v[j]);
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < 16; h += 8) {
+        uint16_t cv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cv[j] = 0;
+        if (prm.beta != 0.f) {
+            const uint16_t* c = static_cast<const uint16_t*>(P.c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (h + j < nc && m0 + h + j < Mrows) cv[j] = c[static_cast<size_t>(m0 + h + j) * P.N + n];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (h + j < nc && m0 + h + j < Mrows) {
+                float r = prm.alpha * v[h + j];
+                if (prm.beta != 0.f) r = fmaf(prm.beta, scale_to_float<BF16>(cv[j]), r);
+                if (P.bias) r += bias;
+                y[static_cast<size_t>(m0 + h + j) * P.N + n] = float_to_out<BF16>(r);
+            }
+        }
+    }
+}
+
+// The row's bias as float, 0 without one (or without the epilogue).
+template <bool BF16, int MAXP>
+__device__ __forceinline__ float row_bias(const GemmParams<MAXP>& prm, const ProblemDesc& P, int n) {
+    return (prm.has_epi && P.bias) ? scale_to_float<BF16>(static_cast<const uint16_t*>(P.bias)[n]) : 0.f;
 }
 
 // (d0, d1) += a * (b0, b1) with one packed fp32 FMA (fma.rn.f32x2).
@@ -630,13 +662,13 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     }
                 }
             }
-            uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
+            const float bias = row_bias<BF16>(prm, P, n);
 #pragma unroll
-            for (int j = 0; j < C::kNC; ++j) {
-                const int m = m0 + j;
-                if (m < Mrows)
-                    y[static_cast<size_t>(m) * P.N + n] =
-                        float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, acc[j], m, n) : acc[j]);
+            for (int j0 = 0; j0 < C::kNC; j0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = j0 + j < C::kNC ? acc[j0 + j] : 0.f;
+                store_cols16<BF16>(prm, P, v, C::kNC - j0 < 16 ? C::kNC - j0 : 16, m0 + j0, n, Mrows, bias);
             }
         }
         if (prm.cluster_split > 0) {
@@ -652,7 +684,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int n = seg.nt * kTileN + r;
                 const int cb = max((q * NT) / S, col0), ce = min(((q + 1) * NT) / S, col0 + C::kNC);
                 constexpr int kBatch = C::kNC <= 64 ? 4 : 2;   // parts of a 16-column batch loaded together
-                uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
+                const float bias = row_bias<BF16>(prm, P, n);
                 for (int c = cb; c < ce; c += 16) {
                     const int nc = ce - c < 16 ? ce - c : 16;
                     float sum[16];
@@ -675,13 +707,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             }
                         }
                     }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = seg.mt * NT + c + j;
-                        if (j < nc && m < Mrows)
-                            y[static_cast<size_t>(m) * P.N + n] =
-                                float_to_out<BF16>(prm.has_epi ? epilogue_value<BF16>(prm, P, sum[j], m, n) : sum[j]);
-                    }
+                    store_cols16<BF16>(prm, P, sum, nc, seg.mt * NT + c, n, Mrows, bias);
                 }
             }
             cluster_sync();   // no CTA leaves while another still reads its shared memory
