@@ -1,0 +1,56 @@
+"""Host logic of bench.py that needs no GPU: the workload variants (group size, no scales, the
+epilogue, device-resident token counts) and their algorithmic byte counts."""
+import types
+
+import numpy as np
+import pytest
+
+import bench
+import wq4_inputs as I
+
+
+def _args(**kw):
+    a = dict(workload="decode_m8_n4096_k4096_bf16_u4b8", group_size=I.GROUP, no_scales=False, epilogue=False,
+             device_m=False)
+    a.update(kw)
+    return types.SimpleNamespace(**a)
+
+
+def test_plain_workload_is_unchanged():
+    """No variant flag: the same seeded inputs, bytes and config as the named workload."""
+    for name in I.WORKLOADS:
+        a = _args(workload=name)
+        assert bench.variant_of(a) == {}
+        got, ref = bench.make_inputs(a), I.make_workload(name)
+        got = got if isinstance(got, list) else [got]
+        ref = ref if isinstance(ref, list) else [ref]
+        assert len(got) == len(ref)
+        for g, r in zip(got, ref):
+            assert (g.M, g.N, g.K, g.qtype, g.dtype) == (r.M, r.N, r.K, r.qtype, r.dtype)
+            assert np.array_equal(g.X_bits, r.X_bits) and np.array_equal(g.Wq, r.Wq)
+            assert np.array_equal(g.S_bits, r.S_bits)
+            assert bench.variant_bytes(g, a) == I.algorithmic_bytes(r.M, r.N, r.K, r.qtype)
+
+
+def test_variant_bytes():
+    """Scales counted as the variant has them; C and bias read once by the epilogue."""
+    M, N, K = 8, 4096, 4096
+    base = I.algorithmic_bytes(M, N, K, I.U4B8)
+    p = bench.make_inputs(_args(group_size=K))
+    assert p.S_bits.shape == (1, N)
+    assert bench.variant_bytes(p, _args(group_size=K)) == base - 2 * (K // 128 - 1) * N
+    p = bench.make_inputs(_args(no_scales=True))
+    assert p.S_bits is None
+    assert bench.variant_bytes(p, _args(no_scales=True)) == base - 2 * (K // 128) * N
+    p = bench.make_inputs(_args(epilogue=True))
+    assert bench.variant_bytes(p, _args(epilogue=True)) == base + 2 * M * N + 2 * N
+    assert set(bench.variant_of(_args(epilogue=True, group_size=512))) == {"epilogue", "group_size"}
+
+
+def test_variant_rules():
+    with pytest.raises(SystemExit):        # zero points need their scales
+        bench.make_inputs(_args(workload="asym_m128_n14336_k4096_bf16_u4zp", no_scales=True))
+    with pytest.raises(SystemExit):        # the grouped call has no epilogue
+        bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", epilogue=True))
+    g = bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", device_m=True))
+    assert isinstance(g, list) and sum(p.M for p in g) == 1024
