@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     bool ok = !(prm.test_stall && threadIdx.x == 0) || mbar_wait(stall_bar, 0, ctl);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;                 // the whole warp stops with it
     int x_piece = -1;                                                 // last activation piece waited for
+    // activation piece of the current group, tracked as the groups advance by KS (no division
+    // per group): group ks + i KS lies in piece `piece`, which ends before group piece_end
+    int piece = ks / prm.x_gp, piece_end = (piece + 1) * prm.x_gp, grp = ks;
 
     // activation addresses: token row m = 8 nb + g sits at 128-byte row (panel * Mpad + m) whose
     // swizzle key is (row & 7) = g; the lane's 16-byte chunk in a panel is (4 (j & 1) + c) ^ g
@@ -225,8 +228,11 @@ __global__ void __launch_bounds__(dec_warps(NB) * 32, 1) wq4_decode_kernel(const
     const uint32_t a_off = g * 16 + 4 * c;                            // word c of row g in a chunk
 
     constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
-    for (int i = 0; i < n_my && ok; ++i) {
-        const int piece = (ks + i * KS) / prm.x_gp;                   // activation piece of this group
+    for (int i = 0; i < n_my && ok; ++i, grp += KS) {
+        while (grp >= piece_end) {
+            ++piece;
+            piece_end += prm.x_gp;
+        }
         if (piece != x_piece) {
             ok = mbar_wait(s_bar + 8 * piece, 0, ctl);
             x_piece = piece;
