@@ -60,6 +60,8 @@ struct GemmCfg {
     static constexpr int kChunks = 4 / kKParts;              // 32-element K chunks per dequant thread
     static constexpr int kColParts = kFW / 4;                // fold warps per TMEM lane quarter
     static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
+    // epilogue: C values loaded together per thread (16 at NT = 192 spill the bf16 fold warps)
+    static constexpr int kEpiBatch = NT >= 192 ? 8 : 16;
     static constexpr int kRec = tile_record_bytes(ZP);
     static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
     // Two rings: activation tiles (two panels per group; consumed by the MMA, released by its
@@ -241,42 +243,39 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
     }
 }
 
-// Writes Y[m0 + j][n] for j < nc (at most 16) and m0 + j < Mrows, with the epilogue when the call
-// has one: alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once (after the C load and
-// alpha / beta of the epilogue in "sm90_gemm_array_tma_warpspecialized_cooperative.hpp", plus a
-// bias per weight row). The C values of 8 columns at a time are loaded together (independent
-// loads in flight at once) before those outputs are formed; C may be Y itself, each element being read and
-// then written by the same thread. `bias` is the row's bias as float (used only when the problem
-// has one).
-template <bool BF16, int MAXP>
-__device__ __forceinline__ void store_cols16(const GemmParams<MAXP>& prm, const ProblemDesc& P, const float (&v)[16],
-                                             int nc, int m0, int n, int Mrows, float bias) {
+// Writes Y[m0 + j][n] = v[j0 + j] for j < nc (at most B) and m0 + j < Mrows, with the epilogue
+// when the call has one: alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once (after the C
+// load and alpha / beta of the epilogue in "sm90_gemm_array_tma_warpspecialized_cooperative.hpp",
+// plus a bias per weight row). The C values of the B columns are loaded together (independent
+// loads in flight at once) before those outputs are formed; C may be Y itself, each element being
+// read and then written by the same thread. `bias` is the row's bias as float (used only when the
+// problem has one).
+template <bool BF16, int B, int MAXP, int NV>
+__device__ __forceinline__ void store_cols(const GemmParams<MAXP>& prm, const ProblemDesc& P, const float (&v)[NV],
+                                           int j0, int nc, int m0, int n, int Mrows, float bias) {
     uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
     if (!prm.has_epi) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (j < nc && m0 + j < Mrows) y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(v[j]);
+        for (int j = 0; j < B; ++j)
+            if (j < nc && m0 + j < Mrows) y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(v[j0 + j]);
         return;
     }
+    uint16_t cv[B];
 #pragma unroll
-    for (int h = 0; h < 16; h += 8) {
-        uint16_t cv[8];
+    for (int j = 0; j < B; ++j) cv[j] = 0;
+    if (prm.beta != 0.f) {
+        const uint16_t* c = static_cast<const uint16_t*>(P.c);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cv[j] = 0;
-        if (prm.beta != 0.f) {
-            const uint16_t* c = static_cast<const uint16_t*>(P.c);
+        for (int j = 0; j < B; ++j)
+            if (j < nc && m0 + j < Mrows) cv[j] = c[static_cast<size_t>(m0 + j) * P.N + n];
+    }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (h + j < nc && m0 + h + j < Mrows) cv[j] = c[static_cast<size_t>(m0 + h + j) * P.N + n];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (h + j < nc && m0 + h + j < Mrows) {
-                float r = prm.alpha * v[h + j];
-                if (prm.beta != 0.f) r = fmaf(prm.beta, scale_to_float<BF16>(cv[j]), r);
-                if (P.bias) r += bias;
-                y[static_cast<size_t>(m0 + h + j) * P.N + n] = float_to_out<BF16>(r);
-            }
+    for (int j = 0; j < B; ++j) {
+        if (j < nc && m0 + j < Mrows) {
+            float r = prm.alpha * v[j0 + j];
+            if (prm.beta != 0.f) r = fmaf(prm.beta, scale_to_float<BF16>(cv[j]), r);
+            if (P.bias) r += bias;
+            y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(r);
         }
     }
 }
@@ -663,13 +662,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 }
             }
             const float bias = row_bias<BF16>(prm, P, n);
+            constexpr int kB = C::kEpiBatch;
 #pragma unroll
-            for (int j0 = 0; j0 < C::kNC; j0 += 16) {
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = j0 + j < C::kNC ? acc[j0 + j] : 0.f;
-                store_cols16<BF16>(prm, P, v, C::kNC - j0 < 16 ? C::kNC - j0 : 16, m0 + j0, n, Mrows, bias);
-            }
+            for (int j0 = 0; j0 < C::kNC; j0 += kB)
+                store_cols<BF16, kB>(prm, P, acc, j0, C::kNC - j0 < kB ? C::kNC - j0 : kB, m0 + j0, n, Mrows, bias);
         }
         if (prm.cluster_split > 0) {
             cluster_sync();   // every rank's partial is in its shared memory
@@ -707,7 +703,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             }
                         }
                     }
-                    store_cols16<BF16>(prm, P, sum, nc, seg.mt * NT + c, n, Mrows, bias);
+                    constexpr int kB = C::kEpiBatch;
+#pragma unroll
+                    for (int h = 0; h < 16; h += kB)
+                        store_cols<BF16, kB>(prm, P, sum, h, nc - h < 0 ? 0 : (nc - h < kB ? nc - h : kB),
+                                             seg.mt * NT + c + h, n, Mrows, bias);
                 }
             }
             cluster_sync();   // no CTA leaves while another still reads its shared memory
