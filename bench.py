@@ -345,7 +345,7 @@ def run_gpu(args, rank, world, local_rank):
         "tflops": round(tfl, 3), "gbs": round(gbs, 1),
         "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 4),
         "roofline": roof,
-        "gpu_launches": K,
+        "gpu_launches": K * (2 if args.device_m else 1),   # device counts: the tile-table kernel too
         "clocks": clocks,
         "e2e": e2e,
     }
