@@ -58,9 +58,10 @@ constexpr int kDecStage = 1024 + 32 + 16;                     // codes, scales, 
 constexpr int kDecMaxX = 140 * 1024;                          // activation bytes held per CTA
 constexpr int kDecXPieces = 8;                                // most activation copies per CTA
 
-// warps per CTA: more warps hide the MMA and shared-memory latencies; with one token block a
-// thread needs few registers, so 32 warps fit
-__host__ __device__ constexpr int dec_warps(int nb) { return nb == 1 ? 32 : 16; }
+// warps per CTA: 16 at every token-block count (at one block 32 warps with half the groups each
+// were measured ~1 % slower: the group loop is issue-bound, and fewer warps run more groups per
+// loop setup)
+__host__ __device__ constexpr int dec_warps(int) { return 16; }
 
 template <int NB>
 struct DecCfg {
@@ -485,8 +486,8 @@ cudaError_t launch_decode(const void* X, const void* Wp, void* Y, int M, int N, 
     p.k_groups = K / kTileK;
     p.n_blocks = N / 16;
     // fewest row blocks per CTA that keeps the grid within one wave; each CTA's warps split K into
-    // warps / rb slices (warps beyond rb * slices stay idle: at N = 14336, 6 blocks and 5 slices
-    // on 150 CTAs beat 8 blocks and 4 slices on 112 CTAs by a quarter less work per SM)
+    // warps / rb slices (warps beyond rb * slices stay idle: at N = 14336, 6 blocks on 150 CTAs
+    // beat 8 blocks on 112 CTAs by a quarter less work per SM)
     const int warps = dec_warps(nb);
     int rb = (p.n_blocks + sm_count - 1) / sm_count;
     if (rb > warps) rb = warps;
