@@ -2,7 +2,8 @@
  * wq4 — W4A16 mixed-input GEMM for NVIDIA GB300 (sm_103a), C ABI.
  *
  * Computes Y[M,N] = X[M,K] . dequant(Wq)[N,K]^T with X, the scales and Y in bf16 or fp16,
- * 4-bit weight codes, one scale per group of 128 consecutive K elements and fp32 accumulation.
+ * 4-bit weight codes, one scale (and zero point) per group of G consecutive K elements (G = 128
+ * by default; or no scales) and fp32 accumulation.
  *
  * The problem statement follows "aphrodite-engine/kernels/quantization/machete/
  * machete_mainloop.cuh": its header comment (weights prepacked once, then Y = mm(X, B_prepacked);
@@ -43,7 +44,8 @@ enum {
     WQ4_OK = 0,
     WQ4_ERR_INVALID = -1,      /* bad shape, null pointer, zero pointer given/missing, bad enum */
     WQ4_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned (TMA rule) */
-    WQ4_ERR_UNSUPPORTED = -3,  /* valid for the method, not built here (group size != 128, ...) */
+    WQ4_ERR_UNSUPPORTED = -3,  /* valid for the method, not built here (a group size that is not a
+                                  multiple of 128 dividing K, N or K not multiples of 128, ...) */
     WQ4_ERR_WORKSPACE = -4,    /* workspace missing or smaller than the *_workspace_bytes answer */
     WQ4_ERR_CUDA = -5,         /* a CUDA runtime call failed (no device, launch failure, ...) */
     WQ4_ERR_TIMEOUT = -6       /* a kernel's bounded pipeline wait ran out (see wq4_get_last_error) */
@@ -90,7 +92,8 @@ int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int q
 
 /* Workspace bytes wq4_mm needs on the current device for this shape (partial sums of K-split
  * tiles and their arrival counters) under the current options; 0 when the call takes the
- * decode kernel (M <= 32), which uses none (workspace may then be NULL). The workspace must be
+ * decode kernel (at most 32 tokens, where that kernel applies: WQ4_OPT_DECODE), which uses none
+ * (workspace may then be NULL). The workspace must be
  * zero-filled once when allocated; every completed call leaves its counters at zero again.
  * Calls that may overlap on the GPU need separate workspaces. */
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
@@ -104,7 +107,6 @@ int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
 int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size,
            int dtype, int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream);
 
-/* Workspace bytes for wq4_grouped_mm with these P problems (host arrays of shapes). */
 /* Y = alpha * (X . dequant(W)^T) + beta * C + bias, the epilogue with a source operand of the
  * pages' kernels ("sm90_gemm_array_tma_warpspecialized_cooperative.hpp": the epilogue loads C
  * and combines it with alpha and beta) plus a bias per output column:
@@ -118,6 +120,8 @@ int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int g
               int dtype, int qtype, float alpha, const void* C, float beta, const void* bias,
               void* workspace, size_t workspace_bytes, wq4_stream_t stream);
 
+/* Workspace bytes for wq4_grouped_mm with these P problems (host arrays of shapes); the same
+ * zero-fill rule as wq4_workspace_bytes. */
 int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
                                 size_t* bytes);
 
