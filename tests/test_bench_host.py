@@ -54,3 +54,26 @@ def test_variant_rules():
         bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", epilogue=True))
     g = bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", device_m=True))
     assert isinstance(g, list) and sum(p.M for p in g) == 1024
+
+
+def test_reference_arm_line(capsys):
+    """bench.py --impl reference (the oracle on the host cores) prints one JSON line with the keys
+    the driver reads, on the default workload's metric and config."""
+    import json
+    import sys
+    argv = sys.argv
+    sys.argv = ["bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"]
+    try:
+        bench.main()
+    finally:
+        sys.argv = argv
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD and d["value"] > 0
+    assert {"value", "unit", "cores", "kind", "sample"} <= set(d["cpu_baseline"])
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
