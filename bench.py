@@ -183,6 +183,8 @@ def run_gpu(args, rank, world, local_rank):
     wq4.load_library()
     if args.a_in_smem:
         wq4.set_option(wq4.OPT_A_IN_SMEM, 1)
+    if args.const_weights:
+        wq4.set_option(wq4.OPT_CONST_WEIGHTS, 1)
     pk = peaks()
 
     probs = make_inputs(args)
@@ -527,6 +529,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--a-in-smem", action="store_true", help="dequantised operand via shared memory")
+    ap.add_argument("--const-weights", action="store_true",
+                    help="declare the prepacked weights constant (WQ4_OPT_CONST_WEIGHTS)")
     ap.add_argument("--group-size", type=int, default=I.GROUP, help="variant: quantisation group size")
     ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
     ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")

@@ -212,7 +212,10 @@ enum {
     WQ4_OPT_CLUSTER = 7,
     WQ4_OPT_DECODE = 8,
     WQ4_OPT_PDL = 9,
-    WQ4_OPT_TEST_STALL = 10
+    WQ4_OPT_TEST_STALL = 10,
+    WQ4_OPT_CONST_WEIGHTS = 11,
+    WQ4_OPT_DECODE_DEPTH = 12,
+    WQ4_OPT_DECODE_TRIGGER = 13
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

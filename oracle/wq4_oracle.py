@@ -38,7 +38,7 @@ TILE_N = 128            # weight rows per blob tile
 TILE_K = 128            # K elements per blob tile (one quantisation group)
 HEADER_BYTES = 256
 BLOB_MAGIC = 0x50345157  # bytes "WQ4P" little-endian
-BLOB_VERSION = 1
+BLOB_VERSION = 2
 DTYPE_CODE = {"bf16": 0, "fp16": 1}
 QTYPE_CODE = {"u4b8": 0, "u4_zp": 1}
 ONE_BITS = {"bf16": 0x3F80, "fp16": 0x3C00}   # 1.0, the scale slot of a weight without scales
@@ -151,11 +151,20 @@ def check_tolerance(Y_out: np.ndarray, Y_ref: np.ndarray, atol: float = 1e-2, rt
 # --------------------------------------------------------------------------------------------
 # Prepacked blob (the library's weight format)
 # --------------------------------------------------------------------------------------------
+BLOCK_ROWS = 16         # weight rows per block (one warp-level MMA's rows)
+BLOCKS = TILE_N // BLOCK_ROWS
+
+
+def block_bytes(qtype: str) -> int:
+    """Bytes of one 16-row block of a tile record: 1024 B of codes, 32 B of scales and, in
+    zero-point mode, 8 B of zero points, padded to a multiple of 16 B."""
+    raw = 1024 + 32 + (8 if qtype == "u4_zp" else 0)
+    return (raw + 15) // 16 * 16
+
+
 def tile_bytes(qtype: str) -> int:
-    """Bytes of one (128-row, 128-K) tile record: 8192 B of codes, 256 B of scales and, in
-    zero-point mode, 64 B of zero points, padded to a multiple of 128 B."""
-    raw = 8192 + 256 + (64 if qtype == "u4_zp" else 0)
-    return (raw + 127) // 128 * 128
+    """Bytes of one (128-row, 128-K) tile record: eight 16-row blocks."""
+    return BLOCKS * block_bytes(qtype)
 
 
 def prepacked_bytes(N: int, K: int, qtype: str, group_size: int = GROUP) -> int:
@@ -165,6 +174,8 @@ def prepacked_bytes(N: int, K: int, qtype: str, group_size: int = GROUP) -> int:
 # position of element e (0..7) of an 8-element run inside its 32-bit word: even elements take
 # nibbles 0..3, odd elements nibbles 4..7, so (word >> 4i) & 0x000F000F holds elements 2i, 2i+1.
 NIBBLE_POS = np.array([0, 4, 1, 5, 2, 6, 3, 7], dtype=np.uint32)
+# 16-bit slot s of a block's scale area holds row (s // 2) + 8 (s % 2): rows r and r + 8 side by side
+SCALE_SLOT_ROW = np.array([(s // 2) + 8 * (s % 2) for s in range(BLOCK_ROWS)])
 
 
 def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
@@ -175,19 +186,22 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
     below takes the scale (and zero point) of quantisation group 128 g // G, so every 128-K record
     carries its own copy. ``S_bits`` None (no scales): every scale slot holds 1.0.
 
-    Layout:
-      * header, 256 B of little-endian uint32: magic "WQ4P", version 1, N, K, group size,
+    Layout (version 2):
+      * header, 256 B of little-endian uint32: magic "WQ4P", version 2, N, K, group size,
         dtype code (bf16 0, fp16 1), qtype code (u4b8 0, u4_zp 1), tile bytes, N/128, K/128,
         then zeros.
       * tile records in order (nt, g), nt = 0..N/128-1 outer, g = 0..K/128-1 inner, record
-        (nt, g) at byte 256 + (nt * K/128 + g) * tile_bytes.  Inside a record:
-          - codes, 8192 B: 16-byte chunk number (j * 128 + r) holds row n = 128 nt + r and
-            K elements 128 g + 32 j + [0, 32), j = 0..3.  Word w = 0..3 of the chunk holds the
-            eight elements 128 g + 32 j + 8 w + e, e = 0..7, element e in nibble NIBBLE_POS[e].
-          - scales, 256 B at offset 8192: the 16-bit scale of (row 128 nt + r, group g) at 2 r.
-          - zero points (u4_zp only), 64 B at offset 8448: the zero point of (row 128 nt + r,
-            group g) in bits [4 (r % 8), 4 (r % 8) + 4) of little-endian word r // 8.
-          - zero padding up to tile_bytes.
+        (nt, g) at byte 256 + (nt * K/128 + g) * tile_bytes.  A record is eight blocks of
+        block_bytes each; block b (at b * block_bytes) covers rows n = 128 nt + 16 b + rr,
+        rr = 0..15, and the record's K elements 128 g + [0, 128):
+          - codes, 1024 B: 16-byte chunk number (16 j + rr) holds row rr and K elements
+            128 g + 32 j + [0, 32), j = 0..3.  Word w = 0..3 of the chunk holds the eight elements
+            128 g + 32 j + 8 w + e, e = 0..7, element e in nibble NIBBLE_POS[e].
+          - scales, 32 B at offset 1024: the 16-bit scale of row rr at byte 4 (rr % 8) + 2 (rr // 8)
+            (rows rr and rr + 8 share one 32-bit word).
+          - zero points (u4_zp only), 8 B at offset 1056: the zero point of row rr in byte rr % 8,
+            low nibble for rr < 8, high nibble for rr >= 8.
+          - zero padding up to block_bytes.
     """
     if group_size % TILE_K or K % group_size or N % TILE_N or K % TILE_K:
         raise ValueError("the blob format needs N, K multiples of 128 and a group size that is a "
@@ -195,7 +209,7 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
     nT, nG = N // TILE_N, K // TILE_K
     # record g (K elements 128 g ... 128 g + 127) lies in quantisation group (128 g) // G
     src = (np.arange(nG) * TILE_K) // group_size
-    tb = tile_bytes(qtype)
+    tb, bb = tile_bytes(qtype), block_bytes(qtype)
     blob = np.zeros(prepacked_bytes(N, K, qtype), dtype=np.uint8)
     hdr = np.zeros(HEADER_BYTES // 4, dtype=np.uint32)
     hdr[:10] = [BLOB_MAGIC, BLOB_VERSION, N, K, group_size, DTYPE_CODE[dtype], QTYPE_CODE[qtype],
@@ -203,24 +217,25 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
     blob[:HEADER_BYTES] = hdr.view(np.uint8)
 
     q = unpack_u4(Wq, K).astype(np.uint32)                      # [N][K]
-    # axes: nt, r, g, j, w, e
-    q6 = q.reshape(nT, TILE_N, nG, 4, 4, 8)
-    words = np.bitwise_or.reduce(q6 << (4 * NIBBLE_POS), axis=-1)   # [nt][r][g][j][w]
-    words = words.transpose(0, 2, 3, 1, 4)                      # [nt][g][j][r][w]
-    codes = np.ascontiguousarray(words).view(np.uint8).reshape(nT, nG, 8192)
+    # axes: nt, b, rr, g, j, w, e
+    q7 = q.reshape(nT, BLOCKS, BLOCK_ROWS, nG, 4, 4, 8)
+    words = np.bitwise_or.reduce(q7 << (4 * NIBBLE_POS), axis=-1)  # [nt][b][rr][g][j][w]
+    words = words.transpose(0, 3, 1, 4, 2, 5)                   # [nt][g][b][j][rr][w]
+    codes = np.ascontiguousarray(words).view(np.uint8).reshape(nT, nG, BLOCKS, 1024)
 
-    recs = blob[HEADER_BYTES:].reshape(nT, nG, tb)
-    recs[:, :, :8192] = codes
+    blocks = blob[HEADER_BYTES:].reshape(nT, nG, BLOCKS, bb)
+    blocks[:, :, :, :1024] = codes
     if S_bits is None:                                          # no scales: 1.0 in every slot
         S_rows = np.full((nG, N), ONE_BITS[dtype], dtype=np.uint16)
     else:
         S_rows = np.asarray(S_bits, dtype=np.uint16).reshape(K // group_size, N)[src]
-    S = S_rows.reshape(nG, nT, TILE_N)                          # [g][nt][r]
-    recs[:, :, 8192:8448] = np.ascontiguousarray(S.transpose(1, 0, 2)).view(np.uint8).reshape(nT, nG, 256)
+    S = S_rows.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
+    blocks[:, :, :, 1024:1056] = np.ascontiguousarray(S.transpose(1, 0, 2, 3)).view(np.uint8).reshape(
+        nT, nG, BLOCKS, 32)
     if qtype == "u4_zp":
-        z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, TILE_N)  # [g][nt][r]
-        zw = _pack_rows(z.transpose(1, 0, 2))                              # [nt][g][16] uint32
-        recs[:, :, 8448:8512] = np.ascontiguousarray(zw).view(np.uint8).reshape(nT, nG, 64)
+        z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, BLOCKS, BLOCK_ROWS)
+        zb = (z[..., :8] | (z[..., 8:] << 4)).astype(np.uint8)              # [g][nt][b][8]
+        blocks[:, :, :, 1056:1064] = zb.transpose(1, 0, 2, 3)
     return blob
 
 
@@ -235,18 +250,20 @@ def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str, group_si
     quantisation group j is read from its first record, 128-K record j G / 128."""
     nT, nG = N // TILE_N, K // TILE_K
     first = (np.arange(K // group_size) * group_size) // TILE_K
-    tb = tile_bytes(qtype)
-    recs = np.asarray(blob, dtype=np.uint8)[HEADER_BYTES:HEADER_BYTES + nT * nG * tb].reshape(nT, nG, tb)
-    words = np.ascontiguousarray(recs[:, :, :8192]).view(np.uint32).reshape(nT, nG, 4, TILE_N, 4)
-    words = words.transpose(0, 3, 1, 2, 4)                      # [nt][r][g][j][w]
-    q6 = (words[..., None] >> (4 * NIBBLE_POS)) & np.uint32(0xF)  # [..][e]
-    q = q6.reshape(N, K).astype(np.uint8)
-    S = np.ascontiguousarray(recs[:, :, 8192:8448]).view(np.uint16).reshape(nT, nG, TILE_N)
-    S_bits = np.ascontiguousarray(np.ascontiguousarray(S.transpose(1, 0, 2)).reshape(nG, N)[first])
+    tb, bb = tile_bytes(qtype), block_bytes(qtype)
+    blocks = np.asarray(blob, dtype=np.uint8)[HEADER_BYTES:HEADER_BYTES + nT * nG * tb].reshape(nT, nG, BLOCKS, bb)
+    words = np.ascontiguousarray(blocks[..., :1024]).view(np.uint32).reshape(nT, nG, BLOCKS, 4, BLOCK_ROWS, 4)
+    words = words.transpose(0, 2, 4, 1, 3, 5)                  # [nt][b][rr][g][j][w]
+    q7 = (words[..., None] >> (4 * NIBBLE_POS)) & np.uint32(0xF)  # [..][e]
+    q = q7.reshape(N, K).astype(np.uint8)
+    slots = np.ascontiguousarray(blocks[..., 1024:1056]).view(np.uint16).reshape(nT, nG, BLOCKS, BLOCK_ROWS)
+    S = np.empty_like(slots)
+    S[..., SCALE_SLOT_ROW] = slots                              # back to row order
+    S_bits = np.ascontiguousarray(np.ascontiguousarray(S.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
     Z = None
     if qtype == "u4_zp":
-        zw = np.ascontiguousarray(recs[:, :, 8448:8512]).view(np.uint32).reshape(nT, nG, 16)
-        z = unpack_u4(zw, TILE_N)                                # [nt][g][r]
-        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2)).reshape(nG, N)[first])
+        zb = blocks[..., 1056:1064].astype(np.uint32)            # [nt][g][b][8]
+        z = np.concatenate([zb & 0xF, zb >> 4], axis=-1)         # rows 0..7, then 8..15
+        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
     Wq = _pack_rows(q)
     return Wq.astype(np.uint32), S_bits, (None if Z is None else Z.astype(np.uint32))

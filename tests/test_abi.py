@@ -115,5 +115,15 @@ def test_options(clib):
     assert clib.wq4_set_option(wq4.OPT_PDL, 0) == wq4.OK
     assert clib.wq4_set_option(wq4.OPT_TEST_STALL, 2) == wq4.ERR_INVALID
     assert clib.wq4_set_option(wq4.OPT_TEST_STALL, 0) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_CONST_WEIGHTS, 2) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_CONST_WEIGHTS, 1) == wq4.OK
+    assert clib.wq4_get_option(wq4.OPT_CONST_WEIGHTS) == 1
+    assert clib.wq4_set_option(wq4.OPT_CONST_WEIGHTS, 0) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_DECODE_DEPTH, 1) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_DECODE_DEPTH, 17) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_DECODE_DEPTH, 4) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_DECODE_DEPTH, 0) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_DECODE_TRIGGER, 2) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_DECODE_TRIGGER, 0) == wq4.OK
     assert clib.wq4_set_option(99, 1) == wq4.ERR_INVALID
     assert clib.wq4_get_option(99) == -1

@@ -18,7 +18,8 @@ def opts(lib):
     """Options set inside a test are reset afterwards."""
     yield lib
     for key in (lib.OPT_TOKEN_TILE, lib.OPT_GRID, lib.OPT_SPLIT_ALL, lib.OPT_A_IN_SMEM, lib.OPT_TIMEOUT_CYCLES,
-                lib.OPT_CLUSTER, lib.OPT_DECODE, lib.OPT_PDL, lib.OPT_TEST_STALL):
+                lib.OPT_CLUSTER, lib.OPT_DECODE, lib.OPT_PDL, lib.OPT_TEST_STALL, lib.OPT_CONST_WEIGHTS,
+                lib.OPT_DECODE_DEPTH, lib.OPT_DECODE_TRIGGER):
         lib.set_option(key, 0)
 
 
@@ -154,13 +155,119 @@ DECODE = [
 ]
 
 
+@pytest.mark.parametrize("const", [0, 1])
 @pytest.mark.parametrize("M,N,K,dtype,qtype", DECODE)
-def test_decode_kernel(opts, M, N, K, dtype, qtype):
-    """The warp-level-MMA kernel for at most 32 tokens (forced on)."""
+def test_decode_kernel(opts, M, N, K, dtype, qtype, const):
+    """The warp-level-MMA kernel for at most 32 tokens (forced on), in stream order and with
+    constant weights (weights copied before the kernel ahead completes)."""
     lib = opts
     lib.set_option(lib.OPT_DECODE, 1)
+    lib.set_option(lib.OPT_CONST_WEIGHTS, const)
     p = I.make_problem(M, N, K, dtype, qtype, seed=M * 13 + N + K)
     assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "decode %s" % ((M, N, K, dtype, qtype),))
+
+
+@pytest.mark.parametrize("depth,trigger,const", [(2, 0, 0), (3, 1, 0), (2, 0, 1), (5, 0, 1), (16, 1, 1)])
+@pytest.mark.parametrize("M,N,K,qtype", [(8, 4096, 4096, "u4b8"), (5, 2944, 8960, "u4_zp"), (16, 768, 1408, "u4b8"),
+                                         (7, 4864, 4096, "u4_zp"), (12, 2432, 8192, "u4b8")])
+def test_decode_ring_and_modes(opts, depth, trigger, const, M, N, K, qtype):
+    """The decode kernel's weight ring (forced depths, so the ring wraps many times; K not a
+    multiple of 8 groups leaves a short last stage), the two trigger points and the constant-weights
+    mode (header check and first weight copies before the wait on the kernel ahead)."""
+    lib = opts
+    lib.set_option(lib.OPT_DECODE, 1)
+    lib.set_option(lib.OPT_DECODE_DEPTH, depth)
+    lib.set_option(lib.OPT_DECODE_TRIGGER, trigger)
+    lib.set_option(lib.OPT_CONST_WEIGHTS, const)
+    p = I.make_problem(M, N, K, "bf16", qtype, seed=M + N + K + depth)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "decode ring %s" % ((depth, trigger, const),))
+    assert lib.get_last_error() == lib.OK
+
+
+def _mismatched_calls(lib, p, blob, X):
+    """Calls whose arguments disagree with the blob's header (nothing else wrong)."""
+    yield "qtype", dict(qtype="u4_zp" if p.qtype == "u4b8" else "u4b8")
+    yield "group size", dict(qtype=p.qtype, group_size=p.K)
+    yield "N", dict(qtype=p.qtype, N=p.N // 2)
+
+
+@pytest.mark.parametrize("M,const", [(8, 0), (8, 1), (100, 0), (300, 0)])
+def test_blob_header_mismatch_is_reported(opts, M, const):
+    """A blob passed with a qtype, group size or N other than the ones it was prepacked with: the
+    kernels compare the blob's header with the call before they read any record, record
+    WQ4_ERR_INVALID and stop; the next correct call is fine. Decode (M = 8, stream order and
+    constant weights), cluster split (M = 100) and data-parallel (M = 300) paths."""
+    import torch
+    lib = opts
+    lib.set_option(lib.OPT_CONST_WEIGHTS, const)
+    p = I.make_problem(M, 1024, 1024, "bf16", "u4b8", seed=M + 17)
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, "bf16")
+    torch.cuda.synchronize()
+    for what, kw in _mismatched_calls(lib, p, blob, X):
+        N = kw.get("N", p.N)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        lib.mm(X, blob, N, qtype=kw["qtype"], out=Y, group_size=kw.get("group_size", 128))
+        assert lib.get_last_error() == lib.ERR_INVALID, what
+        assert lib.get_last_error() == lib.OK
+    assert_parity(y_as_f64(lib.mm(X, blob, p.N), "bf16"), O.mm_problem(p), "after a header mismatch")
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 4096, 4096), (100, 256, 1152), (300, 512, 1024)])
+def test_header_check_paths_agree(opts, M, N, K):
+    """A blob written by wq4_prepack for these arguments is streamed while its header is checked; a
+    copy of it made by other means (here a tensor clone) is checked before any record is read. Both
+    paths give the same bits, on the decode, cluster-split and data-parallel plans."""
+    lib = opts
+    p = I.make_problem(M, N, K, "bf16", "u4_zp", seed=M + N)
+    blob = gpu_prepack(lib, p)
+    copy = blob.clone()
+    X = to_cuda16(p.X_bits, "bf16")
+    for const in (0, 1):
+        lib.set_option(lib.OPT_CONST_WEIGHTS, const)
+        a = from_cuda16(lib.mm(X, blob, N, qtype="u4_zp"))
+        b = from_cuda16(lib.mm(X, copy, N, qtype="u4_zp"))
+        assert np.array_equal(a, b)
+        assert lib.get_last_error() == lib.OK
+    assert_parity(O.decode16(a, "bf16"), O.mm_problem(p), "header check paths")
+
+
+def test_decode_const_weights_chain_matches_stream_order(opts):
+    """With constant weights the decode kernel reads the blob before the kernel ahead completes;
+    in a graph of calls where each call's activations are the previous call's output, the result
+    must equal plain stream order bit for bit."""
+    import torch
+    lib = opts
+    M, K = 8, 4096
+    ps = [I.make_problem(M, K, K, "bf16", "u4b8", seed=950 + i) for i in range(6)]
+    blobs = [gpu_prepack(lib, p) for p in ps]
+    X0 = to_cuda16(ps[0].X_bits, "bf16")
+    torch.cuda.synchronize()
+
+    def chain(const, pdl):
+        lib.set_option(lib.OPT_CONST_WEIGHTS, const)
+        lib.set_option(lib.OPT_PDL, pdl)
+        st = torch.cuda.Stream()
+        outs = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in ps]
+        with torch.cuda.stream(st):
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                x = X0
+                for i in range(len(ps)):
+                    lib.mm(x, blobs[i], K, qtype="u4b8", out=outs[i])
+                    x = outs[i]
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+        assert lib.get_last_error() == lib.OK
+        return [from_cuda16(o) for o in outs]
+
+    a = chain(1, 0)
+    b = chain(0, -1)
+    for i in range(len(ps)):
+        assert np.array_equal(a[i], b[i]), "call %d differs with constant weights" % i
+    assert_parity(O.decode16(a[0], "bf16"), O.mm_problem(ps[0]), "const-weights chain call 0")
 
 
 def test_decode_chain_in_a_graph(opts):

@@ -288,31 +288,37 @@ def test_tolerance_check():
 # ---------------------------------------------------------------- blob layout
 def _brute_blob(p) -> np.ndarray:
     """The blob built one element at a time straight from the layout's wording (record g carries
-    the scale and zero point of quantisation group 128 g // G; no scales: 1.0 = 0x3F80 / 0x3C00)."""
-    tb = O.tile_bytes(p.qtype)
+    the scale and zero point of quantisation group 128 g // G; no scales: 1.0 = 0x3F80 / 0x3C00):
+    record (nt, g) is eight 16-row blocks of 1056 B (uint4b8) or 1072 B (zero points); in block b,
+    row rr's K elements 32 j + [0, 32) form 16-byte chunk 16 j + rr, its scale sits at byte
+    1024 + 4 (rr % 8) + 2 (rr // 8), its zero point in byte 1056 + rr % 8 (high nibble for rr >= 8)."""
+    bb = 1072 if p.qtype == "u4_zp" else 1056
+    tb = 8 * bb
     nG = p.K // 128
     G = p.group_size
     blob = np.zeros(O.prepacked_bytes(p.N, p.K, p.qtype), np.uint8)
-    hdr = [O.BLOB_MAGIC, 1, p.N, p.K, G, O.DTYPE_CODE[p.dtype], O.QTYPE_CODE[p.qtype], tb, p.N // 128, nG]
+    hdr = [O.BLOB_MAGIC, 2, p.N, p.K, G, O.DTYPE_CODE[p.dtype], O.QTYPE_CODE[p.qtype], tb, p.N // 128, nG]
     for i, v in enumerate(hdr):
         blob[4 * i:4 * i + 4] = list(int(v).to_bytes(4, "little"))
     pos = {0: 0, 2: 1, 4: 2, 6: 3, 1: 4, 3: 5, 5: 6, 7: 7}
     for n in range(p.N):
+        nt, b, rr = n // 128, (n % 128) // 16, n % 16
         for k in range(p.K):
-            nt, r, g, kk = n // 128, n % 128, k // 128, k % 128
+            g, kk = k // 128, k % 128
             j, w, e = kk // 32, (kk % 32) // 8, kk % 8
-            rec = 256 + (nt * nG + g) * tb
-            byte_off = rec + (j * 128 + r) * 16 + 4 * w + pos[e] // 2
+            blk = 256 + (nt * nG + g) * tb + b * bb
+            byte_off = blk + (16 * j + rr) * 16 + 4 * w + pos[e] // 2
             shift = 4 * (pos[e] % 2)
             blob[byte_off] |= int(p.q[n, k]) << shift
     for g in range(nG):
         for n in range(p.N):
-            rec = 256 + ((n // 128) * nG + g) * tb
-            r = n % 128
+            nt, b, rr = n // 128, (n % 128) // 16, n % 16
+            blk = 256 + (nt * nG + g) * tb + b * bb
             sbits = int(p.S_bits[(128 * g) // G, n]) if p.S_bits is not None else (0x3F80 if p.dtype == "bf16" else 0x3C00)
-            blob[rec + 8192 + 2 * r: rec + 8192 + 2 * r + 2] = list(sbits.to_bytes(2, "little"))
+            so = blk + 1024 + 4 * (rr % 8) + 2 * (rr // 8)
+            blob[so:so + 2] = list(sbits.to_bytes(2, "little"))
             if p.qtype == "u4_zp":
-                blob[rec + 8448 + r // 2] |= int(p.z[(128 * g) // G, n]) << (4 * (r % 2))
+                blob[blk + 1056 + rr % 8] |= int(p.z[(128 * g) // G, n]) << (4 * (rr // 8))
     return blob
 
 
@@ -354,5 +360,5 @@ def test_blob_round_trip(qtype, dtype):
     if qtype == "u4_zp":
         assert np.array_equal(Z, p.Z)
     hdr = blob[:40].view(np.uint32)
-    assert hdr.tolist() == [O.BLOB_MAGIC, 1, 384, 640, 128, O.DTYPE_CODE[dtype], O.QTYPE_CODE[qtype],
+    assert hdr.tolist() == [O.BLOB_MAGIC, 2, 384, 640, 128, O.DTYPE_CODE[dtype], O.QTYPE_CODE[qtype],
                             O.tile_bytes(qtype), 3, 5]

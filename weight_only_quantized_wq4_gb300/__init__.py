@@ -21,6 +21,7 @@ DTYPES = {"bf16": 0, "fp16": 1}
 QTYPES = {"u4b8": 0, "u4_zp": 1}
 OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM, OPT_CLUSTER = 1, 2, 3, 4, 5, 6, 7
 OPT_DECODE, OPT_PDL, OPT_TEST_STALL = 8, 9, 10
+OPT_CONST_WEIGHTS, OPT_DECODE_DEPTH, OPT_DECODE_TRIGGER = 11, 12, 13
 GROUP = 128
 
 _lib = None

@@ -23,6 +23,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "wq4.h"
@@ -49,6 +50,9 @@ struct Options {
     int decode = 0;           // 0 automatic, -1 never, 1 always when the shape allows it
     int pdl = 0;              // 0 programmatic dependent launch on, -1 off
     int test_stall = 0;       // 1: kernels wait once on a barrier nothing arrives on (tests)
+    int const_weights = 0;    // 1: blobs are not written by pending work; weights are read early
+    int decode_depth = 0;     // decode weight ring slots, 0 = automatic
+    int decode_trigger = 0;   // 0: the next kernel is let in once the activations landed, 1: at once
 };
 Options g_opt;
 
@@ -97,6 +101,33 @@ long long timeout_cycles() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Blobs this process wrote with wq4_prepack, with the arguments they were written for. A GEMM call
+// whose arguments match its blob's entry lets the kernels stream weight records at once, checking
+// the blob header alongside; a call on any other blob (made by other means, or passed with other
+// arguments) waits for the device-side header check before the first record is read, so that a
+// blob smaller than the call expects is never read past its end.
+struct BlobKey {
+    int N, K, G, dtype, qtype;
+    bool operator==(const BlobKey& o) const {
+        return N == o.N && K == o.K && G == o.G && dtype == o.dtype && qtype == o.qtype;
+    }
+};
+std::mutex g_blob_mu;
+std::unordered_map<uintptr_t, BlobKey> g_blobs;
+constexpr size_t kMaxBlobEntries = 1 << 16;
+
+void blob_register(const void* wp, const BlobKey& k) {
+    std::lock_guard<std::mutex> lk(g_blob_mu);
+    if (g_blobs.size() >= kMaxBlobEntries) g_blobs.clear();
+    g_blobs[reinterpret_cast<uintptr_t>(wp)] = k;
+}
+
+bool blob_trusted(const void* wp, const BlobKey& k) {
+    std::lock_guard<std::mutex> lk(g_blob_mu);
+    const auto it = g_blobs.find(reinterpret_cast<uintptr_t>(wp));
+    return it != g_blobs.end() && it->second == k;
+}
 
 int check_types(int group_size, int dtype, int qtype) {
     if (dtype != WQ4_BF16 && dtype != WQ4_FP16) return WQ4_ERR_INVALID;
@@ -326,7 +357,7 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
 
 template <int MAXP>
 int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void* const* Wp, void* const* Y,
-             int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st,
+             int group_size, int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st,
              const EpilogueArgs* epi = nullptr) {
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
@@ -362,6 +393,13 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
         }
     }
     prm->num_problems = static_cast<int>(shapes.size());
+    prm->hdr_trusted = 1;
+    for (size_t p = 0; p < shapes.size(); ++p)
+        if (shapes[p].M > 0 && !blob_trusted(Wp[p], BlobKey{shapes[p].N, shapes[p].K, group_size, dtype, qtype}))
+            prm->hdr_trusted = 0;
+    prm->group_size = group_size;
+    prm->dtype = dtype;
+    prm->qtype = qtype;
     prm->total_tiles = pl.total_tiles;
     prm->dp_tiles = pl.dp_tiles;
     prm->num_ctas = pl.grid;
@@ -513,7 +551,9 @@ int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros, i
     if (!aligned16(Wq) || (scales && !aligned16(scales)) || !aligned16(Wp_out) || (zeros && !aligned16(zeros)))
         return WQ4_ERR_ALIGN;
     const cudaError_t e = launch_prepack(Wq, scales, zeros, N, K, group_size, dtype, qtype, Wp_out, stream);
-    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+    if (e != cudaSuccess) return WQ4_ERR_CUDA;
+    blob_register(Wp_out, BlobKey{N, K, group_size, dtype, qtype});
+    return WQ4_OK;
 }
 
 int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype, uint32_t* Wq_out,
@@ -582,13 +622,24 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
                 e_part = *epi;
                 if (e_part.c) e_part.c = static_cast<const uint8_t*>(e_part.c) + static_cast<size_t>(m0) * N * 2;
             }
-            int grid = 0, rb = 0;
-            const cudaError_t e = launch_decode(x, Wp, y, mr, N, K, dtype, qtype, dev->sm_count, dev->status,
-                                                timeout_cycles(), reinterpret_cast<void*>(fn), g_opt.pdl == 0,
-                                                g_opt.test_stall, epi ? &e_part : nullptr, &grid, &rb, stream);
+            DecodeLaunch L;
+            L.sm_count = dev->sm_count;
+            L.status = dev->status;
+            L.timeout_cycles = timeout_cycles();
+            L.encode_fn = reinterpret_cast<void*>(fn);
+            L.pdl = g_opt.pdl == 0;
+            L.test_stall = g_opt.test_stall;
+            L.const_weights = g_opt.const_weights;
+            L.trigger_late = g_opt.decode_trigger == 0 ? 1 : 0;
+            L.depth = g_opt.decode_depth;
+            L.hdr_trusted = blob_trusted(Wp, BlobKey{N, K, group_size, dtype, qtype}) ? 1 : 0;
+            int grid = 0, depth = 0;
+            const cudaError_t e = launch_decode(L, x, Wp, y, mr, N, K, group_size, dtype, qtype, epi ? &e_part : nullptr,
+                                                &grid, &depth, stream);
             if (trace_on())
-                std::fprintf(stderr, "[wq4] decode kernel: M=%d (rows %d..%d) N=%d K=%d grid=%d row_blocks_per_cta=%d (%s)\n",
-                             M, m0, m0 + mr, N, K, grid, rb, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+                std::fprintf(stderr, "[wq4] decode kernel: M=%d (rows %d..%d) N=%d K=%d grid=%d ring=%d const_weights=%d "
+                             "header_alongside=%d (%s)\n", M, m0, m0 + mr, N, K, grid, depth, g_opt.const_weights,
+                             L.hdr_trusted, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
             if (e != cudaSuccess) return WQ4_ERR_CUDA;
         }
         return WQ4_OK;
@@ -597,7 +648,7 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
     const void* xs[1] = {X};
     const void* ws[1] = {Wp};
     void* ys[1] = {Y};
-    return run_gemm<1>(shapes, xs, ws, ys, dtype, qtype, workspace, workspace_bytes, stream, epi);
+    return run_gemm<1>(shapes, xs, ws, ys, group_size, dtype, qtype, workspace, workspace_bytes, stream, epi);
 }
 
 int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
@@ -632,7 +683,7 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
         }
         shapes.push_back({M[p], N[p], K[p]});
     }
-    return run_gemm<kMaxGroupedProblems>(shapes, X, Wp, Y, dtype, qtype, workspace, workspace_bytes, stream);
+    return run_gemm<kMaxGroupedProblems>(shapes, X, Wp, Y, group_size, dtype, qtype, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ device-resident shapes
@@ -726,6 +777,9 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
     }
     const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(dev->sm_count, max_tiles)));
     prm->num_problems = P;
+    prm->group_size = group_size;
+    prm->dtype = dtype;
+    prm->qtype = qtype;
     prm->total_tiles = static_cast<int>(max_tiles);
     prm->dp_tiles = static_cast<int>(max_tiles);
     prm->num_ctas = grid;
@@ -753,7 +807,7 @@ int wq4_get_last_error(wq4_stream_t stream) {
     if (st) {
         const unsigned int zero = 0;
         cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
-        return WQ4_ERR_TIMEOUT;
+        return (st & kStatusBadBlob) ? WQ4_ERR_INVALID : WQ4_ERR_TIMEOUT;
     }
     if (se != cudaSuccess || cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     return WQ4_OK;
@@ -799,6 +853,18 @@ int wq4_set_option(int key, long long value) {
             if (value < 0 || value > 1) return WQ4_ERR_INVALID;
             g_opt.test_stall = static_cast<int>(value);
             return WQ4_OK;
+        case WQ4_OPT_CONST_WEIGHTS:
+            if (value < 0 || value > 1) return WQ4_ERR_INVALID;
+            g_opt.const_weights = static_cast<int>(value);
+            return WQ4_OK;
+        case WQ4_OPT_DECODE_DEPTH:
+            if (value != 0 && (value < 2 || value > 16)) return WQ4_ERR_INVALID;
+            g_opt.decode_depth = static_cast<int>(value);
+            return WQ4_OK;
+        case WQ4_OPT_DECODE_TRIGGER:
+            if (value < 0 || value > 1) return WQ4_ERR_INVALID;
+            g_opt.decode_trigger = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -815,6 +881,9 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_DECODE: return g_opt.decode;
         case WQ4_OPT_PDL: return g_opt.pdl;
         case WQ4_OPT_TEST_STALL: return g_opt.test_stall;
+        case WQ4_OPT_CONST_WEIGHTS: return g_opt.const_weights;
+        case WQ4_OPT_DECODE_DEPTH: return g_opt.decode_depth;
+        case WQ4_OPT_DECODE_TRIGGER: return g_opt.decode_trigger;
         default: return -1;
     }
 }
@@ -855,6 +924,9 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
     d.k_groups = K / kTileK;
     if ((rc = encode_x_map(&prm.xmap[0], X, M, K, dtype, pl.nt))) return rc;
     prm.num_problems = 1;
+    prm.group_size = group_size;
+    prm.dtype = dtype;
+    prm.qtype = qtype;
     prm.total_tiles = pl.total_tiles;
     prm.dp_tiles = pl.dp_tiles;
     prm.num_ctas = pl.grid;

@@ -14,10 +14,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "wq4_params.h"
+
 namespace wq4 {
 
-// Error codes written to the device status word.
-enum : uint32_t { kStatusTimeout = 1u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -203,6 +203,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "memory");
 }
 
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+        "%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -262,6 +276,33 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------------------ misc
+// The blob header against the call (magic, version, N, K, group size, dtype, qtype, record bytes),
+// checked before a kernel reads any record: after "machete_mainloop.cuh", can_implement, which
+// rejects arguments that do not describe the operands, here applied to the weight's own header.
+// The header is fetched with an evict-last L2 policy: 256 bytes per weight stay in L2 between calls
+// while the weight records stream through with evict-first, so the check is usually an L2 hit.
+struct BlobHeader {
+    uint4 a, b;
+};
+__device__ __forceinline__ BlobHeader load_blob_header(const uint32_t* hdr) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    BlobHeader h;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(h.a.x), "=r"(h.a.y), "=r"(h.a.z), "=r"(h.a.w) : "l"(hdr), "l"(pol));
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(h.b.x), "=r"(h.b.y), "=r"(h.b.z), "=r"(h.b.w) : "l"(hdr + 4), "l"(pol));
+    return h;
+}
+__device__ __forceinline__ bool blob_header_matches(const BlobHeader& h, int N, int K, int G, int dtype, int qtype) {
+    return h.a.x == kBlobMagic && h.a.y == kBlobVersion && h.a.z == static_cast<uint32_t>(N) &&
+           h.a.w == static_cast<uint32_t>(K) && h.b.x == static_cast<uint32_t>(G) && h.b.y == static_cast<uint32_t>(dtype) &&
+           h.b.z == static_cast<uint32_t>(qtype) && h.b.w == static_cast<uint32_t>(tile_record_bytes(qtype == 1));
+}
+__device__ __forceinline__ bool blob_header_ok(const uint32_t* hdr, int N, int K, int G, int dtype, int qtype) {
+    return blob_header_matches(load_blob_header(hdr), N, K, G, dtype, qtype);
+}
+
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

@@ -87,7 +87,10 @@ struct GemmCfg {
     // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
     static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
     static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kWRingBytes) / kXStageBytes;
-    static constexpr int kXStages = kXStagesFit > 16 ? 16 : kXStagesFit;
+    // An even count: the two MMA warps take alternate groups, so each then owns every other slot
+    // and waits on consecutive phases of it (a parity wait is unambiguous one phase ahead only; with
+    // an odd count a warp would skip the other warp's phase of a slot).
+    static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
     static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
     static constexpr int kColA = kPBufs * NT;                // TMEM column of A buffer 0
     static constexpr int kTmemNeed = kPBufs * NT + (ATMEM ? 64 * kABufs : 0);
@@ -378,6 +381,28 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         if constexpr (C::kRegSplit) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegWg0));
     }
     int issued = 0;                                      // copies a producer thread has issued
+    // Every problem's blob header against the call: by the weight producer's warp before its first
+    // record copy, or (blobs prepacked here for these arguments) by lanes 1..31 of MMA warp 1 while
+    // the copies already stream; a mismatch stops the CTA and is reported as WQ4_ERR_INVALID.
+    bool hdr_ok = true;
+    const bool hdr_alongside = prm.hdr_trusted != 0;
+    if ((warp == 2 && !hdr_alongside) || (warp == 1 && hdr_alongside && lane > 0)) {
+        const unsigned int mask = hdr_alongside ? 0xfffffffeu : 0xffffffffu;
+        const int l0 = hdr_alongside ? 1 : 0, nl = hdr_alongside ? 31 : 32;
+        bool mine = true;
+        for (int p = lane - l0; p < prm.num_problems; p += nl) {
+            const ProblemDesc& P = prm.prob[p];
+            if (P.m_tiles > 0)
+                mine = blob_header_ok(reinterpret_cast<const uint32_t*>(P.wp - kBlobHeader), P.N, P.K, prm.group_size,
+                                      prm.dtype, prm.qtype) && mine;
+        }
+        hdr_ok = __all_sync(mask, mine ? 1 : 0) != 0;
+        if (!hdr_ok && lane == l0) {
+            atomicOr(prm.status, kStatusBadBlob);
+            *abort_flag = 1;
+        }
+        if (warp == 1) hdr_ok = true;                    // the MMA issuer (lane 0) is unaffected here
+    }
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------------ producers
         // warp 0: activation tiles (two 2-D tensor copies per group); warp 2: weight records (one
@@ -390,7 +415,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
             int i = 0;
-            bool ok = true;
+            bool ok = hdr_ok;
             while (ok && sch.next(seg)) {
                 const ProblemDesc& P = prm.prob[seg.prob];
                 const uint64_t pol_w = P.m_tiles == 1 ? pol_stream : pol_keep;
@@ -487,8 +512,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 uint32_t sub;
                 if constexpr (ZP) {
                     uint32_t zb;
-                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + 8448 + (r >> 1)));
-                    const uint32_t z = (zb >> ((r & 1) * 4)) & 0xFu;
+                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + rec_zero_off(true, r)));
+                    const uint32_t z = (zb >> (((r >> 3) & 1) * 4)) & 0xFu;
                     sub = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
                 } else {
                     sub = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
@@ -496,7 +521,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                 for (int jj = 0; jj < C::kChunks; ++jj) {
                     const int j = part * C::kChunks + jj;
-                    const uint4 v = lds128(rec + (j * 128 + r) * 16);
+                    const uint4 v = lds128(rec + rec_code_off(ZP, r, j));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
                     uint32_t out[16];
 #pragma unroll
@@ -560,7 +585,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 tc_fence_after();
                 const uint32_t rec = wrec_of(i);
                 uint32_t sbits;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + 8192 + 2 * r));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(ZP, r)));
                 const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
                 if (g == seg.g0) {
 #pragma unroll

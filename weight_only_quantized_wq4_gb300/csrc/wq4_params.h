@@ -10,10 +10,36 @@ constexpr int kTileN = 128;          // weight rows per tile (the MMA's M side a
 constexpr int kTileK = 128;          // K elements per tile = one quantisation group
 constexpr int kBlobHeader = 256;     // bytes before the first tile record of a prepacked blob
 constexpr int kMaxGroupedProblems = 64;
+constexpr uint32_t kBlobMagic = 0x50345157u;   // "WQ4P"
+constexpr uint32_t kBlobVersion = 2;
 
-// Bytes of one (128-row, 128-K) record of the prepacked blob: 8192 B of codes, 256 B of
-// scales, 64 B of zero points in zero-point mode, padded to 128 B.
-__host__ __device__ constexpr int tile_record_bytes(bool zp) { return zp ? 8576 : 8448; }
+// Bits of the device status word: a bounded pipeline wait ran out; a blob header did not match
+// the call's arguments.
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadBlob = 2u };
+
+// A (128-row, 128-K) record of the prepacked blob is eight blocks of 16 weight rows. Block b
+// holds, for its rows rr = 0..15: 1024 B of codes (16-byte chunk 16 j + rr = the row's K elements
+// 32 j + [0, 32)), 32 B of scales (row rr at byte 4 (rr % 8) + 2 (rr / 8)) and, in zero-point mode,
+// 8 B of zero points (row rr in byte rr % 8, high nibble for rr >= 8), padded to 16 B. A block is
+// one contiguous run, so a kernel that owns a few 16-row blocks stages exactly those with one
+// tensor copy per run of groups, and a kernel that owns whole tiles copies the record at once.
+constexpr int kBlockRows = 16;
+constexpr int kBlockCodes = 1024;
+constexpr int kBlockScaleOff = 1024;
+constexpr int kBlockZeroOff = 1056;
+__host__ __device__ constexpr int block_bytes(bool zp) { return zp ? 1072 : 1056; }
+__host__ __device__ constexpr int tile_record_bytes(bool zp) { return 8 * block_bytes(zp); }
+// Byte offsets, inside a record, of row r's (0..127) 16-byte code chunk j, its scale and the byte
+// holding its zero point (nibble (r / 8) & 1).
+__host__ __device__ constexpr int rec_code_off(bool zp, int r, int j) {
+    return (r >> 4) * block_bytes(zp) + (16 * j + (r & 15)) * 16;
+}
+__host__ __device__ constexpr int rec_scale_off(bool zp, int r) {
+    return (r >> 4) * block_bytes(zp) + kBlockScaleOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
+}
+__host__ __device__ constexpr int rec_zero_off(bool zp, int r) {
+    return (r >> 4) * block_bytes(zp) + kBlockZeroOff + (r & 7);
+}
 
 struct ProblemDesc {
     const uint8_t* wp;       // first tile record (blob + kBlobHeader)
@@ -66,6 +92,9 @@ struct GemmParams {
     int has_epi;             // 1: Y = alpha acc + beta C + bias (else Y = acc)
     float alpha, beta;
     const DynTable* dyn;     // device-resident problem sizes (see DynTable), or null
+    int group_size, dtype, qtype;   // what every problem's blob header must say
+    int hdr_trusted;         // 1: every blob was prepacked here for these arguments (records may be read
+                             // while the headers are being checked); 0: check before the first read
 };
 
 }  // namespace wq4

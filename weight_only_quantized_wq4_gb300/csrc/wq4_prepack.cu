@@ -1,20 +1,20 @@
 // Prepack and its inverse: reorder packed 4-bit weights, scales and zero points into the tile
 // records the GEMM streams (the offline weight reordering of "machete_mainloop.cuh", header
-// comment, with a layout made for this kernel).
+// comment, with a layout made for this hardware).
 //
-// Blob: a 256-byte header of little-endian uint32 (magic "WQ4P", version 1, N, K, group size,
-// dtype code, qtype code, record bytes, N/128, K/128, then zeros), then one record per
-// (n_tile, group) in n_tile-major order. A record holds
-//   * 8192 B of codes: 16-byte chunk (j * 128 + r) = row 128 n_tile + r, K elements
-//     128 g + 32 j + [0, 32); its word w holds elements 8w + e (e = 0..7) of that run with element
-//     e in nibble e/2 + 4 (e % 2), so that (word >> 4i) & 0x000F000F holds elements 2i, 2i+1.
-//     A dequant thread then reads its row's 32-element runs with one 128-bit load, and the 32
-//     threads of a warp read 512 consecutive bytes;
-//   * 256 B of scales, row r at byte 2r (the scale of the quantisation group the record lies in:
-//     with a group size G that is a multiple of 128, record g carries group 128 g / G; without
-//     scales every slot holds 1.0);
-//   * (zero-point mode) 64 B of zero points, row r in nibble r % 8 of word r / 8; then zero
-//     padding to 8576 B.
+// Blob (version 2): a 256-byte header of little-endian uint32 (magic "WQ4P", version 2, N, K,
+// group size, dtype code, qtype code, record bytes, N/128, K/128, then zeros), then one record
+// per (n_tile, group) in n_tile-major order. A record is eight blocks of 16 weight rows
+// (wq4_params.h); block b of record (nt, g) holds, for rows n = 128 nt + 16 b + rr:
+//   * 1024 B of codes: 16-byte chunk (16 j + rr) = row rr's K elements 128 g + 32 j + [0, 32); its
+//     word w holds elements 8w + e (e = 0..7) of that run with element e in nibble e/2 + 4 (e % 2),
+//     so that (word >> 4i) & 0x000F000F holds elements 2i, 2i+1. A thread that owns a row reads a
+//     32-element run with one 128-bit load; a warp's 8-row 16-byte pieces are 128 contiguous bytes;
+//   * 32 B of scales, row rr at byte 4 (rr % 8) + 2 (rr / 8) (the scale of the quantisation group
+//     the record lies in: with a group size G that is a multiple of 128, record g carries group
+//     128 g / G; without scales every slot holds 1.0);
+//   * (zero-point mode) 8 B of zero points, row rr in byte rr % 8 (high nibble for rr >= 8), then
+//     zero padding to 1072 B.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,8 +22,6 @@
 #include "wq4_params.h"
 
 namespace wq4 {
-
-constexpr uint32_t kBlobMagic = 0x50345157u;
 
 __device__ __forceinline__ uint32_t interleave_codes(uint32_t in) {
     uint32_t out = 0;
@@ -40,71 +38,79 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t in) {
 }
 
 // Byte offset (from the first record) of the code word holding elements [8 kw, 8 kw + 8) of row n.
-__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, int rec) {
+__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, bool zp) {
     const int g = kw >> 4, j = (kw >> 2) & 3, w = kw & 3;
     const int nt = n >> 7, r = n & 127;
-    return (static_cast<size_t>(nt) * k_groups + g) * rec + static_cast<size_t>((j * 128 + r) * 16 + 4 * w);
+    return (static_cast<size_t>(nt) * k_groups + g) * tile_record_bytes(zp) +
+           static_cast<size_t>(rec_code_off(zp, r, j) + 4 * w);
 }
 
 __global__ void prepack_codes_kernel(const uint32_t* __restrict__ wq, uint8_t* __restrict__ recs, int N,
-                                     int K, int rec) {
+                                     int K, bool zp) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(idx / kwords), kw = static_cast<int>(idx % kwords);
-        *reinterpret_cast<uint32_t*>(recs + code_word_offset(n, kw, K / 128, rec)) = interleave_codes(wq[idx]);
+        *reinterpret_cast<uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp)) = interleave_codes(wq[idx]);
     }
 }
 
 __global__ void unprepack_codes_kernel(const uint8_t* __restrict__ recs, uint32_t* __restrict__ wq, int N,
-                                       int K, int rec) {
+                                       int K, bool zp) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(idx / kwords), kw = static_cast<int>(idx % kwords);
-        wq[idx] = deinterleave_codes(*reinterpret_cast<const uint32_t*>(recs + code_word_offset(n, kw, K / 128, rec)));
+        wq[idx] = deinterleave_codes(*reinterpret_cast<const uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp)));
     }
 }
 
-// Scales (one thread per (group, row)), zero-point words (one per (group, 8 rows)), record
-// padding and the header.
+// Scales (one thread per (group, row)), zero points and padding (one thread per (group, 16-row
+// block): the eight zero-point bytes of a block combine two of the API's words), and the header.
 __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const uint32_t* __restrict__ zeros,
-                                    uint8_t* __restrict__ blob, int N, int K, int G, int dtype, int qtype, int rec) {
+                                    uint8_t* __restrict__ blob, int N, int K, int G, int dtype, int qtype) {
+    const bool zp = zeros != nullptr;
+    const int rec = tile_record_bytes(zp);
     const uint16_t one = dtype == 0 ? 0x3F80u : 0x3C00u;     // 1.0 in bf16 / fp16
     const int ng = K / 128, nT = N / 128;
     uint8_t* recs = blob + kBlobHeader;
     const long long n_scale = static_cast<long long>(ng) * N;
-    const long long n_zero = zeros ? static_cast<long long>(ng) * (N / 8) : 0;
-    const int pad_words = (rec - (8192 + 256 + (zeros ? 64 : 0))) / 4;
-    const long long n_pad = static_cast<long long>(ng) * nT * pad_words;
-    const long long total = n_scale + n_zero + n_pad + 64;
+    const long long n_block = zp ? static_cast<long long>(ng) * (N / kBlockRows) : 0;
+    const long long total = n_scale + n_block + 64;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
             const int g = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
             const int src = (g * 128) / G;                           // quantisation group of record g
             uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            reinterpret_cast<uint16_t*>(r + 8192)[n & 127] = scales ? scales[static_cast<size_t>(src) * N + n] : one;
-        } else if (idx < n_scale + n_zero) {
+            *reinterpret_cast<uint16_t*>(r + rec_scale_off(zp, n & 127)) =
+                scales ? scales[static_cast<size_t>(src) * N + n] : one;
+        } else if (idx < n_scale + n_block) {
             const long long z = idx - n_scale;
-            const int g = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
+            const int g = static_cast<int>(z / (N / kBlockRows)), blk = static_cast<int>(z % (N / kBlockRows));
             const int src = (g * 128) / G;
-            uint8_t* r = recs + (static_cast<size_t>(wz >> 4) * ng + g) * rec;
-            reinterpret_cast<uint32_t*>(r + 8448)[wz & 15] = zeros[static_cast<size_t>(src) * (N / 8) + wz];
-        } else if (idx < n_scale + n_zero + n_pad) {
-            const long long z = idx - n_scale - n_zero;
-            const long long rr = z / pad_words;
-            const int w = static_cast<int>(z % pad_words);
-            uint8_t* r = recs + rr * rec;
-            reinterpret_cast<uint32_t*>(r + (rec - 4 * pad_words))[w] = 0u;
+            const uint32_t lo = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk];       // rows 16 blk + 0..7
+            const uint32_t hi = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk + 1];   // rows 16 blk + 8..15
+            uint32_t w[2] = {0u, 0u};
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const uint32_t byte = ((lo >> (4 * p)) & 0xFu) | (((hi >> (4 * p)) & 0xFu) << 4);
+                w[p >> 2] |= byte << (8 * (p & 3));
+            }
+            uint8_t* r = recs + (static_cast<size_t>(blk >> 3) * ng + g) * rec + (blk & 7) * block_bytes(true);
+            uint32_t* zw = reinterpret_cast<uint32_t*>(r + kBlockZeroOff);
+            zw[0] = w[0];
+            zw[1] = w[1];
+            zw[2] = 0u;                                              // padding up to 1072 B
+            zw[3] = 0u;
         } else {
-            const int w = static_cast<int>(idx - n_scale - n_zero - n_pad);
+            const int w = static_cast<int>(idx - n_scale - n_block);
             uint32_t v = 0;
             switch (w) {
                 case 0: v = kBlobMagic; break;
-                case 1: v = 1u; break;
+                case 1: v = kBlobVersion; break;
                 case 2: v = static_cast<uint32_t>(N); break;
                 case 3: v = static_cast<uint32_t>(K); break;
                 case 4: v = static_cast<uint32_t>(G); break;
@@ -122,7 +128,8 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
 
 // Output row j (quantisation group j) is read from its first record, 128-K record j G / 128.
 __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t* __restrict__ scales,
-                                      uint32_t* __restrict__ zeros, int N, int K, int G, int rec) {
+                                      uint32_t* __restrict__ zeros, int N, int K, int G, bool zp) {
+    const int rec = tile_record_bytes(zp);
     const int ng = K / 128, nq = K / G;
     const uint8_t* recs = blob + kBlobHeader;
     const long long n_scale = scales ? static_cast<long long>(nq) * N : 0;
@@ -133,13 +140,22 @@ __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t
             const int j = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
             const int g = (j * G) / 128;
             const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            scales[idx] = reinterpret_cast<const uint16_t*>(r + 8192)[n & 127];
+            scales[idx] = *reinterpret_cast<const uint16_t*>(r + rec_scale_off(zp, n & 127));
         } else {
+            // API word wz: rows 8 wz .. 8 wz + 7, the low (wz even) or high (wz odd) nibbles of a block
             const long long z = idx - n_scale;
             const int j = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
             const int g = (j * G) / 128;
-            const uint8_t* r = recs + (static_cast<size_t>(wz >> 4) * ng + g) * rec;
-            zeros[z] = reinterpret_cast<const uint32_t*>(r + 8448)[wz & 15];
+            const int n0 = 8 * wz;
+            const uint8_t* r = recs + (static_cast<size_t>(n0 >> 7) * ng + g) * rec;
+            uint32_t out = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rr = (n0 + i) & 127;
+                const uint32_t byte = r[rec_zero_off(true, rr)];
+                out |= ((byte >> (4 * ((rr >> 3) & 1))) & 0xFu) << (4 * i);
+            }
+            zeros[z] = out;
         }
     }
 }
@@ -153,29 +169,29 @@ static int grid_for(long long work, int threads) {
 
 cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st) {
-    const int rec = tile_record_bytes(qtype == 1);
+    const bool zp = qtype == 1;
     uint8_t* b = static_cast<uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
-    prepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, b + kBlobHeader, N, K, rec);
+    prepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, b + kBlobHeader, N, K, zp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
     prepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(static_cast<const uint16_t*>(scales), zeros, b, N, K, G,
-                                                            dtype, qtype, rec);
+                                                            dtype, qtype);
     return cudaGetLastError();
 }
 
 cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, uint32_t* wq, void* scales,
                              uint32_t* zeros, cudaStream_t st) {
-    const int rec = tile_record_bytes(qtype == 1);
+    const bool zp = qtype == 1;
     const uint8_t* b = static_cast<const uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
-    unprepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(b + kBlobHeader, wq, N, K, rec);
+    unprepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(b + kBlobHeader, wq, N, K, zp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
     unprepack_side_kernel<<<grid_for(side, 256), 256, 0, st>>>(b, static_cast<uint16_t*>(scales), zeros, N, K, G,
-                                                              rec);
+                                                              zp);
     return cudaGetLastError();
 }
 
