@@ -2,13 +2,21 @@
 """Benchmark of the W4A16 GEMM on GB300 (one JSON line on stdout).
 
 A step is one call of the hot path (wq4_mm, or wq4_grouped_mm for the grouped workload) on one
-batch of seeded synthetic input already resident in HBM; the weight is prepacked once before
-timing (prepack is the offline step of the method). K steps are replayed from a CUDA graph
-over rotating copies of every input so that the data each launch reads was evicted from L2 by
-the launches in between (the rotating set is larger than L2). Time is taken with CUDA events
-on the launching stream, max over ranks.
+batch of seeded synthetic input already resident in HBM; every weight is prepacked before timing
+(prepack is the offline step of the method). Each workload keeps R rotating copies of all its
+inputs (each weight prepacked into its own blob; R x working set > 3 x L2), and a CUDA graph of
+L = max(K, R) launches walks them, so the data each launch reads was evicted from L2 by the
+launches in between. After an untimed soak, 7 replays are timed with CUDA events on the launching
+stream (max over ranks); the line reports the median per launch and the min / max.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+The default run measures the five workloads one after the other. The headline (value, roofline,
+e2e, cpu_baseline) is the decode workload with constant weights (WQ4_OPT_CONST_WEIGHTS: weights
+prepacked once and not written by pending work, so the decode kernel streams them before the
+kernel ahead completes); its stream-ordered number is in "stream_ordered", and every workload's
+own line (rate, roofline, clocks) is under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--stream-order]
+                  [--impl reference]
 
 Variants of a workload (measured like the workload itself; the default line uses none):
   --group-size G / --no-scales   other group sizes, or uint4b8 without scales (direct conversion)
@@ -173,158 +181,174 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------ GPU arm
-def run_gpu(args, rank, world, local_rank):
-    import torch
-    import weight_only_quantized_wq4_gb300 as wq4
+ALL_WORKLOADS = ["tiny_m16_n256_k512_fp16_u4b8", "decode_m8_n4096_k4096_bf16_u4b8", "asym_m128_n14336_k4096_bf16_u4zp",
+                 "prefill_m4096_n4096_k14336_bf16_u4b8", "grouped_8x_n14336_k4096_summ1024_bf16_u4b8"]
+REPLAYS = 7
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wq4.build()
-    wq4.load_library()
-    if args.a_in_smem:
-        wq4.set_option(wq4.OPT_A_IN_SMEM, 1)
-    if args.const_weights:
-        wq4.set_option(wq4.OPT_CONST_WEIGHTS, 1)
-    pk = peaks()
 
-    probs = make_inputs(args)
-    grouped = isinstance(probs, list)
-    if args.device_m and not grouped:
-        raise SystemExit("--device-m applies to the grouped workload")
-    plist = probs if grouped else [probs]
-    byts, flops, cfg, dtype = workload_shapes(args.workload, probs)
-    variant = variant_of(args)
-    if variant:
-        byts = sum(variant_bytes(p, args) for p in plist)
-        cfg = dict(cfg, **variant)
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
-    G = args.group_size
+class Workload:
+    """One workload resident in HBM: R rotating copies of every input (each weight prepacked with
+    wq4_prepack into its own blob), so that the data each launch reads was evicted from L2 by the
+    launches in between, and the call a step makes."""
 
-    def c16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
+    def __init__(self, args, name, dev, use_variant):
+        import torch
+        import weight_only_quantized_wq4_gb300 as wq4
+        self.name = name
+        self.args = args
+        self.dev = dev
+        vargs = args if use_variant else argparse.Namespace(group_size=I.GROUP, no_scales=False, epilogue=False,
+                                                           device_m=False, workload=name)
+        self.vargs = vargs
+        probs = make_inputs(argparse.Namespace(**dict(vars(vargs), workload=name)))
+        self.probs = probs
+        self.grouped = isinstance(probs, list)
+        if vargs.device_m and not self.grouped:
+            raise SystemExit("--device-m applies to the grouped workload")
+        plist = probs if self.grouped else [probs]
+        self.plist = plist
+        byts, flops, cfg, dtype = workload_shapes(name, probs)
+        self.variant = variant_of(vargs)
+        if self.variant:
+            byts = sum(variant_bytes(p, vargs) for p in plist)
+            cfg = dict(cfg, **self.variant)
+        self.byts, self.flops, self.cfg, self.dtype = byts, flops, cfg, dtype
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+        self.tdt = tdt
+        G = vargs.group_size
 
-    def c32(words):
-        return torch.from_numpy(np.ascontiguousarray(words).view(np.int32)).to(dev)
+        def c16(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(dev)
 
-    # one resident copy of the inputs, prepacked once
-    base_X = [c16(p.X_bits) if p.M > 0 else torch.empty((0, p.K), dtype=tdt, device=dev) for p in plist]
-    base_W = [wq4.prepack(c32(p.Wq), c16(p.S_bits) if p.S_bits is not None else None,
-                          c32(p.Z) if p.Z is not None else None, qtype=p.qtype, group_size=G, dtype=dtype)
-              for p in plist]
-    rng = np.random.default_rng(7)
-    base_C = [c16(I.f32_to_bits(rng.standard_normal((p.M, p.N)).astype(np.float32), dtype)) for p in plist] \
-        if args.epilogue else None
-    base_b = [c16(I.f32_to_bits(rng.standard_normal(p.N).astype(np.float32), dtype)) for p in plist] \
-        if args.epilogue else None
-    torch.cuda.synchronize()
-    qtype = plist[0].qtype
-    if args.device_m:
-        ws_bytes = wq4.grouped_device_m_workspace_bytes(len(plist))
-    elif grouped:
-        ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
-    else:
-        ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G)
-    set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in base_W) + \
-        sum(p.M * p.N * 2 for p in plist) * (2 if args.epilogue else 1) + ws_bytes
-    M_dev = torch.tensor([p.M for p in plist], dtype=torch.int32, device=dev) if args.device_m else None
-    R = max(2, math.ceil(3 * L2_BYTES / set_bytes))
-    copies = []
-    for r in range(R):
-        Xs = [x.clone() for x in base_X]
-        Ws = [w.clone() for w in base_W]
-        Ys = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
-        ws = wq4.alloc_workspace(ws_bytes, dev)
-        Cs = [c.clone() for c in base_C] if args.epilogue else None
-        copies.append((Xs, Ws, Ys, ws, Cs))
-    torch.cuda.synchronize()
+        def c32(words):
+            return torch.from_numpy(np.ascontiguousarray(words).view(np.int32)).to(dev)
 
-    def call(Xs, Ws, Ys, ws, Cs, bias):
-        if args.device_m:
-            wq4.grouped_mm_device_m(Xs, Ws, M_dev, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys)
-        elif grouped:
-            wq4.grouped_mm(Xs, Ws, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys)
-        elif args.epilogue:
-            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G, C=Cs[0],
-                   beta=1.0, bias=bias[0])
+        src = [(c32(p.Wq), c16(p.S_bits) if p.S_bits is not None else None, c32(p.Z) if p.Z is not None else None)
+               for p in plist]
+
+        def blobs():
+            return [wq4.prepack(wq, sc, z, qtype=p.qtype, group_size=G, dtype=dtype) for (wq, sc, z), p in zip(src, plist)]
+
+        base_X = [c16(p.X_bits) if p.M > 0 else torch.empty((0, p.K), dtype=tdt, device=dev) for p in plist]
+        self.base_W = blobs()
+        rng = np.random.default_rng(7)
+        self.base_C = [c16(I.f32_to_bits(rng.standard_normal((p.M, p.N)).astype(np.float32), dtype)) for p in plist] \
+            if vargs.epilogue else None
+        self.base_b = [c16(I.f32_to_bits(rng.standard_normal(p.N).astype(np.float32), dtype)) for p in plist] \
+            if vargs.epilogue else None
+        qtype = plist[0].qtype
+        if vargs.device_m:
+            self.ws_bytes = wq4.grouped_device_m_workspace_bytes(len(plist))
+        elif self.grouped:
+            self.ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
         else:
-            wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G)
-
-    def step(c):
-        Xs, Ws, Ys, ws, Cs = copies[c % R]
-        call(Xs, Ws, Ys, ws, Cs, base_b)
-
-    stream = torch.cuda.Stream(dev)
-    K, W = args.steps, args.warmup
-    use_graph = not args.no_graph
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            step(i)
+            self.ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G)
+        self.set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in self.base_W) + \
+            sum(p.M * p.N * 2 for p in plist) * (2 if vargs.epilogue else 1) + self.ws_bytes
+        M_dev = torch.tensor([p.M for p in plist], dtype=torch.int32, device=dev) if vargs.device_m else None
+        self.R = max(2, math.ceil(3 * L2_BYTES / self.set_bytes))
+        self.copies = []
+        for r in range(self.R):
+            Xs = [x.clone() for x in base_X]
+            Ws = self.base_W if r == 0 else blobs()
+            Ys = [torch.empty((p.M, p.N), dtype=tdt, device=dev) for p in plist]
+            ws = wq4.alloc_workspace(self.ws_bytes, dev)
+            Cs = [c.clone() for c in self.base_C] if vargs.epilogue else None
+            self.copies.append((Xs, Ws, Ys, ws, Cs))
+        del src
         torch.cuda.synchronize()
-        graph = None
-        if use_graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                for i in range(K):
-                    step(i)
-            torch.cuda.synchronize()
-    assert wq4.get_last_error(dev) == 0
+        grouped = self.grouped
 
-    def timed_region():
-        with torch.cuda.stream(stream):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if graph is not None:
-                graph.replay()
+        def call(Xs, Ws, Ys, ws, Cs, bias):
+            if vargs.device_m:
+                wq4.grouped_mm_device_m(Xs, Ws, M_dev, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys,
+                                        group_size=G)
+            elif grouped:
+                wq4.grouped_mm(Xs, Ws, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys, group_size=G)
+            elif vargs.epilogue:
+                wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G, C=Cs[0],
+                       beta=1.0, bias=bias[0])
             else:
-                for i in range(K):
-                    step(i)
-            e1.record(stream)
-            e1.synchronize()
-            return e0.elapsed_time(e1)
+                wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G)
 
-    sampler = ClockSampler(local_rank)
-    if not args.profile_run:
-        sampler.start()
-        time.sleep(0.3)
-    # soak (not timed): the same replay, so that the clock samples below see this load
-    t_soak = time.time()
-    while not args.profile_run and time.time() - t_soak < 1.0:
-        timed_region()
-    _barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    ms_total = timed_region()
-    torch.cuda.synchronize()
-    t1 = time.time()
-    _barrier(world)
-    sampler.stop()
-    clocks = sampler.summary(t_soak, t1)
-    assert wq4.get_last_error(dev) == 0
-    ms_total = _max_over_ranks(ms_total, world)
+        self.call = call
+        self.launches_per_step = 2 if vargs.device_m else 1     # device counts: the tile-table kernel too
 
-    ms = ms_total / K
-    gbs = byts / (ms * 1e-3) / 1e9
-    tfl = flops / (ms * 1e-3) / 1e12
-    bound = bound_of(byts, flops, pk)
+    def step(self, c):
+        Xs, Ws, Ys, ws, Cs = self.copies[c % self.R]
+        self.call(Xs, Ws, Ys, ws, Cs, self.base_b)
 
-    # end to end through the public API from pinned host buffers: H2D of the step's inputs
-    # (activations and the prepacked weight), the call, D2H of the result.
-    e2e = None if args.profile_run else run_e2e(args, plist, base_W, base_C, base_b, call, ws_bytes, dev, tdt,
-                                                 byts, flops, bound)
+    def time(self, steps, warmup, world, soak_s, no_graph=False):
+        """W eager warm-up steps, then a CUDA graph of L = max(steps, R) launches (so one replay walks
+        every rotating copy); after an untimed soak of replays, REPLAYS timed replays, each between
+        a barrier and a synchronize, timed with CUDA events on the launching stream; per-launch
+        times (max over ranks) and the wall-clock window of soak + timing (for the clock record)."""
+        import torch
+        import weight_only_quantized_wq4_gb300 as wq4
+        L = max(steps, self.R)
+        stream = torch.cuda.Stream(self.dev)
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                self.step(i)
+            torch.cuda.synchronize()
+            graph = None
+            if not no_graph:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for i in range(L):
+                        self.step(i)
+                torch.cuda.synchronize()
+        assert wq4.get_last_error(self.dev) == 0
 
+        def replay():
+            with torch.cuda.stream(stream):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if graph is not None:
+                    graph.replay()
+                else:
+                    for i in range(L):
+                        self.step(i)
+                e1.record(stream)
+                e1.synchronize()
+                return e0.elapsed_time(e1)
+
+        t_soak = time.time()
+        replay()
+        while time.time() - t_soak < soak_s:
+            replay()
+        per_launch = []
+        for _ in range(REPLAYS):
+            _barrier(world)
+            torch.cuda.synchronize()
+            ms = replay()
+            torch.cuda.synchronize()
+            per_launch.append(_max_over_ranks(ms, world) / L)
+        t_end = time.time()
+        _barrier(world)
+        assert wq4.get_last_error(self.dev) == 0
+        del graph
+        return per_launch, L, t_soak, t_end
+
+
+def summarize(w, per_launch, L, pk, world, clocks):
+    """Median per-launch time, both rates, the roofline of the bound this workload sits under."""
+    ms = statistics.median(per_launch)
+    gbs = w.byts / (ms * 1e-3) / 1e9
+    tfl = w.flops / (ms * 1e-3) / 1e12
+    bound = bound_of(w.byts, w.flops, pk)
     traffic = None
     try:
-        if variant:
+        if w.variant:
             raise LookupError("no capture of the variant")
         with open(PROFILE_TRAFFIC) as f:
             tr = json.load(f)
-        ent = tr.get(args.workload)
+        ent = tr.get(w.name)
         if ent and ent.get("kernel_hash") == kernel_source_hash():
             traffic = ent["bytes_per_launch"]
     except Exception:
         pass
-
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": traffic,
@@ -336,25 +360,91 @@ def run_gpu(args, rank, world, local_rank):
                 "peak_source": pk["src"] + " (bf16 burst)",
                 "frac_vs_sustained": round(tfl / pk["bf16_sust"], 4)}
         value, unit = tfl * world, "TFLOP/s"
+    return {"value": round(value, 3), "unit": unit, "ms_per_step": ms,
+            "ms_per_step_min": min(per_launch), "ms_per_step_max": max(per_launch),
+            "tflops": round(tfl, 3), "gbs": round(gbs, 1), "roofline": roof, "clocks": clocks,
+            "launches_per_replay": L, "bound": bound}
 
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import weight_only_quantized_wq4_gb300 as wq4
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wq4.build()
+    wq4.load_library()
+    if args.a_in_smem:
+        wq4.set_option(wq4.OPT_A_IN_SMEM, 1)
+    pk = peaks()
+    names = [args.workload] if args.workload else ALL_WORKLOADS
+    headline = args.workload or DEFAULT_WORKLOAD
+    soak = 0.0 if args.profile_run else 1.0
+
+    sampler = ClockSampler(local_rank)
+    if not args.profile_run:
+        sampler.start()
+        time.sleep(0.3)
+    results = {}
+    head = None
+    for name in names:
+        w = Workload(args, name, dev, use_variant=(name == headline))
+        is_decode = w.plist[0].M <= 32 and not w.grouped
+        modes = [("stream", 0)]
+        if is_decode and not args.stream_order:
+            modes = [("const", 1), ("stream", 0)]        # constant weights first: the headline
+        out = {}
+        for mode, cw in modes:
+            wq4.set_option(wq4.OPT_CONST_WEIGHTS, cw)
+            per, L, t0, t1 = w.time(args.steps, args.warmup, world, soak, args.no_graph)
+            out[mode] = summarize(w, per, L, pk, world, sampler.summary(t0, t1) if not args.profile_run else None)
+        wq4.set_option(wq4.OPT_CONST_WEIGHTS, 0)
+        first = out[modes[0][0]]
+        entry = dict(first, config=w.cfg, weights="constant (WQ4_OPT_CONST_WEIGHTS)" if modes[0][0] == "const"
+                     else "stream order")
+        if len(modes) > 1:
+            entry["stream_ordered"] = {k: out["stream"][k] for k in ("value", "unit", "ms_per_step", "ms_per_step_min",
+                                                                    "ms_per_step_max", "roofline", "clocks")}
+        results[name] = entry
+        if name == headline:
+            head = (w, first, out.get("stream"), modes[0][0])
+        else:
+            del w
+            torch.cuda.empty_cache()
+    sampler.stop()
+
+    w, first, stream_res, mode = head
+    bound = first["bound"]
+    # end to end through the public API from pinned host buffers: H2D of the step's inputs (the
+    # activations and the prepacked weight), the call, D2H of the result. The weight is written by
+    # a copy on the stream every step, so this runs in stream order (no constant-weight promise).
+    e2e = None if args.profile_run else run_e2e(args, w.plist, w.base_W, w.base_C, w.base_b, w.call, w.ws_bytes, dev,
+                                                 w.tdt, w.byts, w.flops, bound)
+    cfg = dict(w.cfg, weights=("constant: prepacked once, read before the kernel ahead completes "
+                               "(WQ4_OPT_CONST_WEIGHTS=1)") if mode == "const" else "stream order",
+               l2="rotating %d input copies (%.0f MB, each weight prepacked into its own blob) > L2" % (
+                   w.R, w.R * w.set_bytes / 1e6),
+               launch=("CUDA graph of %d launches" % first["launches_per_replay"]) if not args.no_graph
+               else "eager launches",
+               timing="median of %d replays (per-launch min %.6f ms, max %.6f ms)" % (
+                   REPLAYS, first["ms_per_step_min"], first["ms_per_step_max"]),
+               parallelism="replicas" if world > 1 else "single GPU")
     out = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-        "data": "synthetic (seeded numpy, wq4_inputs)",
-        "config": dict(cfg, l2="rotating %d input copies (%.0f MB) > L2 per launch" % (R, R * set_bytes / 1e6),
-                       launch="CUDA graph of K launches" if use_graph else "eager launches",
-                       parallelism="replicas" if world > 1 else "single GPU"),
-        "tflops": round(tfl, 3), "gbs": round(gbs, 1),
-        "frac_hbm_nominal_8tbs": round(gbs / 8000.0, 4),
-        "roofline": roof,
-        "gpu_launches": K * (2 if args.device_m else 1),   # device counts: the tile-table kernel too
-        "clocks": clocks,
+        "metric": METRIC, "value": first["value"], "unit": first["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": first["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy, wq4_inputs)", "config": cfg,
+        "tflops": first["tflops"], "gbs": first["gbs"], "frac_hbm_nominal_8tbs": round(first["gbs"] / 8000.0, 4),
+        "roofline": first["roofline"],
+        "gpu_launches": first["launches_per_replay"] * w.launches_per_step * REPLAYS,
+        "clocks": first["clocks"],
         "e2e": e2e,
+        "stream_ordered": results[headline].get("stream_ordered"),
+        "workloads": results,
     }
-    if variant:
+    if w.variant:
         out["cpu_baseline"] = None   # the oracle's row-sampled step covers the plain workloads only
     elif rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_run:
-        out["cpu_baseline"] = cpu_baseline(args.workload, probs, byts, flops, bound, budget_s=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(headline, w.probs, w.byts, w.flops, bound, budget_s=args.cpu_seconds)
     return out
 
 
@@ -481,8 +571,9 @@ def cpu_baseline(name, probs, byts, flops, bound, budget_s=15.0):
 
 def run_reference(args, rank, world):
     pk = peaks()
-    probs = I.make_workload(args.workload)
-    byts, flops, cfg, dtype = workload_shapes(args.workload, probs)
+    name = args.workload or DEFAULT_WORKLOAD
+    probs = I.make_workload(name)
+    byts, flops, cfg, dtype = workload_shapes(name, probs)
     bound = bound_of(byts, flops, pk)
     per_step = max(0.05, min(2.0, 120.0 / (args.steps + args.warmup)))
     frac = calibrate(probs, per_step)
@@ -523,14 +614,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(I.WORKLOADS),
+                    help="one workload only (default: all five, the decode one as the headline)")
     ap.add_argument("--impl", default="wq4", choices=["wq4", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--a-in-smem", action="store_true", help="dequantised operand via shared memory")
-    ap.add_argument("--const-weights", action="store_true",
-                    help="declare the prepacked weights constant (WQ4_OPT_CONST_WEIGHTS)")
+    ap.add_argument("--stream-order", action="store_true",
+                    help="decode headline in stream order (default: constant weights, WQ4_OPT_CONST_WEIGHTS)")
     ap.add_argument("--group-size", type=int, default=I.GROUP, help="variant: quantisation group size")
     ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
     ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")

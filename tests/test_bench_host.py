@@ -77,3 +77,10 @@ def test_reference_arm_line(capsys):
     assert d["config"]["workload"] == bench.DEFAULT_WORKLOAD and d["value"] > 0
     assert {"value", "unit", "cores", "kind", "sample"} <= set(d["cpu_baseline"])
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_default_run_covers_every_workload():
+    """The default bench run measures every named workload, the decode one as the headline."""
+    assert sorted(bench.ALL_WORKLOADS) == sorted(I.WORKLOADS)
+    assert bench.DEFAULT_WORKLOAD in bench.ALL_WORKLOADS
+    assert bench.REPLAYS >= 5

@@ -173,11 +173,11 @@ def workspace_bytes(M: int, N: int, K: int, group_size: int = GROUP) -> int:
     return int(out.value)
 
 
-def grouped_workspace_bytes(Ms: Sequence[int], Ns: Sequence[int], Ks: Sequence[int]) -> int:
+def grouped_workspace_bytes(Ms: Sequence[int], Ns: Sequence[int], Ks: Sequence[int], group_size: int = GROUP) -> int:
     P = len(Ms)
     arr = ctypes.c_int * P
     out = ctypes.c_size_t(0)
-    _check(load_library().wq4_grouped_workspace_bytes(P, arr(*Ms), arr(*Ns), arr(*Ks), GROUP, ctypes.byref(out)),
+    _check(load_library().wq4_grouped_workspace_bytes(P, arr(*Ms), arr(*Ns), arr(*Ks), group_size, ctypes.byref(out)),
            "wq4_grouped_workspace_bytes")
     return int(out.value)
 
@@ -215,8 +215,9 @@ def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_siz
 
 
 def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4b8", workspace=None,
-               outs: Optional[Sequence] = None):
-    """Independent problems Y_p = X_p . dequant(W_p)^T in one launch."""
+               outs: Optional[Sequence] = None, group_size: int = GROUP):
+    """Independent problems Y_p = X_p . dequant(W_p)^T in one launch (every blob prepacked with
+    group_size)."""
     torch = _torch()
     lib = load_library()
     P = len(Xs)
@@ -226,13 +227,13 @@ def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4
     if outs is None:
         outs = [torch.empty((m, n), dtype=x.dtype, device=x.device) for x, m, n in zip(Xs, Ms, Ns)]
     if workspace is None:
-        workspace = alloc_workspace(grouped_workspace_bytes(Ms, Ns, Ks), Xs[0].device)
+        workspace = alloc_workspace(grouped_workspace_bytes(Ms, Ns, Ks, group_size), Xs[0].device)
     arr = ctypes.c_int * P
     ptrs = ctypes.c_void_p * P
     xp = ptrs(*[x.data_ptr() if m > 0 else None for x, m in zip(Xs, Ms)])
     wp = ptrs(*[b.data_ptr() for b in blobs])
     yp = ptrs(*[y.data_ptr() if m > 0 else None for y, m in zip(outs, Ms)])
-    _check(lib.wq4_grouped_mm(P, arr(*Ms), arr(*Ns), arr(*Ks), xp, wp, yp, GROUP, _dtype_code(Xs[0]), QTYPES[qtype],
+    _check(lib.wq4_grouped_mm(P, arr(*Ms), arr(*Ns), arr(*Ks), xp, wp, yp, group_size, _dtype_code(Xs[0]), QTYPES[qtype],
                               _cuda(workspace, "workspace"), workspace.numel(), _stream(Xs[0].device)),
            "wq4_grouped_mm")
     return list(outs)
