@@ -135,19 +135,26 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K,
                    int group_size, int dtype, int qtype,
                    void* workspace, size_t workspace_bytes, wq4_stream_t stream);
 
-/* Same computation and result as wq4_mm, for callers that cannot allocate device memory or
- * hand the library a buffer: code that must not call cudaMalloc (for instance inside a section
- * where allocation would stall or break a stream capture, or a plugin whose host runtime owns
- * every device allocation). There is no counterpart in the pages: it only changes where the
- * K-split scratch lives. Instead of a caller workspace it uses one fixed 24 MiB array in the
- * library's device memory (every GPU that loads the library holds it until the process exits);
- * shapes whose plan needs more return WQ4_ERR_WORKSPACE. It allocates nothing: no cudaMalloc,
- * no cudaFree, no allocating library call. The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture. The array is shared by all calls on a device and keeps the last call's
- * contents; each call clears the part that must start at zero (an async memset on `stream`).
- * Calls that overlap on the GPU (other streams, or concurrently running graphs) race on the
- * array and must be serialised by the caller. Arguments and errors as wq4_mm. */
+/* Same computation as wq4_mm, for callers that cannot allocate device memory or hand the
+ * library a buffer: code that must not call cudaMalloc (for instance inside a section where
+ * allocation would stall or break a stream capture, or a plugin whose host runtime owns every
+ * device allocation). There is no counterpart in the pages: it only changes where the K-split
+ * scratch lives. Instead of a caller workspace it uses one fixed 24 MiB array in the library's
+ * device memory (every GPU that loads the library holds it until the process exits).
+ * Plans: calls that wq4_mm sends to the decode kernel go there too (no scratch). A GEMM plan
+ * whose K-split scratch fits the array is wq4_mm's own; one that would need more (for example
+ * 4096 tokens x N = 4096, whose 192-token tiles need 30 MB) keeps every tile whole instead.
+ * Results: bit-identical to wq4_mm's under the same options when the plan is wq4_mm's; with
+ * tiles kept whole, the same fp32 sums added in another order (equal within rounding, not bit
+ * for bit). WQ4_ERR_WORKSPACE only when an option forces a split (WQ4_OPT_GRID,
+ * WQ4_OPT_SPLIT_ALL) whose scratch exceeds the array.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current, whatever the shape; make that first call before any stream capture. The array is
+ * shared by all calls on a device and keeps the last call's contents; each call that uses it
+ * clears the part that must start at zero (an async memset on `stream`). Calls that overlap on
+ * the GPU (other streams, or concurrently running graphs) race on the array and must be
+ * serialised by the caller. Arguments and errors as wq4_mm. */
 int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size,
                           int dtype, int qtype, wq4_stream_t stream);
 

@@ -1,6 +1,7 @@
 """wq4_mm_static_scratch: the variant of wq4_mm for callers that cannot allocate device memory
-(its K-split scratch is a fixed array inside the library). Called through the C ABI, it must give
-wq4_mm's result, call after call. This file is collected last on purpose."""
+(its K-split scratch is a fixed array inside the library). Called through the C ABI, call after
+call, it must give wq4_mm's bits where wq4_mm's plan fits the array, and the same sums within the
+parity tolerance where it keeps the tiles whole instead. This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -22,7 +23,44 @@ def _call(lib, X, blob, Y, p):
                                       lib.QTYPES[p.qtype], stream)
 
 
-def test_static_scratch_matches_wq4_mm_twice(lib):
+STATIC_SCRATCH_BYTES = 24 << 20
+
+# (M, N, K, dtype, qtype): the decode kernel (M = 8), cluster-split and whole tiles (M = 128), and
+# two K-split plans whose scratch would exceed the fixed array (M = 1024 and the 4096-token
+# prefill shape), which then keep their tiles whole.
+SHAPES = [(8, 4096, 4096, "bf16", "u4b8"), (128, 14336, 4096, "bf16", "u4_zp"),
+          (1024, 4096, 4096, "bf16", "u4b8"), (4096, 4096, 14336, "bf16", "u4b8")]
+
+
+@pytest.mark.parametrize("M,N,K,dtype,qtype", SHAPES)
+def test_static_scratch_default_options(lib, M, N, K, dtype, qtype):
+    p = I.make_problem(M, N, K, dtype, qtype, seed=3000 + M)
+    blob = gpu_prepack(lib, p)
+    X = to_cuda16(p.X_bits, p.dtype)
+    ws = lib.workspace_bytes(M, N, K)
+    want_bits = from_cuda16(lib.mm(X, blob, p.N, qtype=p.qtype))
+    rows = None if M <= 128 else np.random.default_rng(M).choice(M, 48, replace=False)
+    ref = O.mm_problem(p, rows)
+    for _ in range(2):
+        Y = torch.full((p.M, p.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert _call(lib, X, blob, Y, p) == lib.OK
+        assert lib.get_last_error() == lib.OK
+        got_bits = from_cuda16(Y)
+        if ws <= STATIC_SCRATCH_BYTES:
+            # the same plan as wq4_mm: the same bits
+            assert np.array_equal(got_bits, want_bits)
+        else:
+            # tiles kept whole: the same sums in another order
+            st = O.check_tolerance(O.decode16(got_bits, p.dtype), O.decode16(want_bits, p.dtype))
+            assert st["violations"] == 0, st
+        got = O.decode16(got_bits, p.dtype)
+        st = O.check_tolerance(got if rows is None else got[rows], ref)
+        assert st["violations"] == 0, st
+    if M >= 1024:
+        assert ws > STATIC_SCRATCH_BYTES   # the re-planned case is the one exercised
+
+
+def test_static_scratch_split_matches_wq4_mm_twice(lib):
     # Every tile goes through the K-split path (split over CTAs, partial sums and tile counters
     # in scratch), whatever the planner would pick for this shape on its own.
     p = I.make_problem(128, 14336, 1024, "bf16", "u4_zp", seed=2024)

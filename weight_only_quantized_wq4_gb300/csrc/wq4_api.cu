@@ -24,7 +24,6 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
-#include <vector>
 
 #include "wq4.h"
 #include "wq4_launch.h"
@@ -181,7 +180,9 @@ struct Plan {
     int cluster = 0;
     size_t counters_bytes = 0;
     size_t partials_bytes = 0;
-    std::vector<int> m_tiles, tile_begin, unit_begin;
+    int m_tiles[kMaxGroupedProblems] = {};
+    int tile_begin[kMaxGroupedProblems] = {};
+    int unit_begin[kMaxGroupedProblems] = {};
     size_t workspace() const { return counters_bytes + partials_bytes; }
 };
 
@@ -211,10 +212,10 @@ int token_tile_for(const int* M, int P) {
     return best;
 }
 
-int pick_token_tile(const std::vector<Shape>& shapes) {
-    std::vector<int> Ms;
-    for (const Shape& s : shapes) Ms.push_back(s.M);
-    return token_tile_for(Ms.data(), static_cast<int>(Ms.size()));
+int pick_token_tile(const Shape* shapes, int P) {
+    int Ms[kMaxGroupedProblems];
+    for (int p = 0; p < P; ++p) Ms[p] = shapes[p].M;
+    return token_tile_for(Ms, P);
 }
 
 // Splitting the last partial wave of tiles over all CTAs pays only if it saves more (tile, group)
@@ -229,14 +230,19 @@ bool keep_tiles_whole(long long tiles, long long units, int C) {
     return whole <= split;
 }
 
-int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
-    pl->nt = pick_token_tile(shapes);
+// The launch plan for P problems (P <= kMaxGroupedProblems). ws_cap bounds the workspace the plan
+// may ask for: a K-split plan that would need more keeps every tile whole instead (no workspace;
+// the same sums in another order), unless an option forces the split (then the caller's size
+// check fails).
+int make_plan(const Shape* shapes, int P, int sm_count, size_t ws_cap, Plan* pl) {
+    pl->nt = pick_token_tile(shapes, P);
     long long tiles = 0, units = 0;
-    for (const Shape& s : shapes) {
+    for (int p = 0; p < P; ++p) {
+        const Shape& s = shapes[p];
         const int mt = s.M > 0 ? (s.M + pl->nt - 1) / pl->nt : 0;
-        pl->m_tiles.push_back(mt);
-        pl->tile_begin.push_back(static_cast<int>(tiles));
-        pl->unit_begin.push_back(static_cast<int>(units));
+        pl->m_tiles[p] = mt;
+        pl->tile_begin[p] = static_cast<int>(tiles);
+        pl->unit_begin[p] = static_cast<int>(units);
         const long long t = static_cast<long long>(mt) * (s.N / kTileN);
         tiles += t;
         units += t * (s.K / kTileK);
@@ -248,7 +254,7 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     // Few tiles (e.g. decode-sized M): clusters of S CTAs split each tile's K range and add their
     // partial sums through distributed shared memory (no global workspace, no atomics).
     int min_kg = 1 << 30;
-    for (size_t p = 0; p < shapes.size(); ++p)
+    for (int p = 0; p < P; ++p)
         if (pl->m_tiles[p] > 0) min_kg = std::min(min_kg, shapes[p].K / kTileK);
     int S = 0;
     if (g_opt.cluster >= 2) {
@@ -270,20 +276,21 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
     }
 
     int C = g_opt.grid ? g_opt.grid : sm_count;
-    // whole waves of tiles are processed data-parallel; the rest is K-split over all CTAs
-    int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
-    if (dp < tiles && keep_tiles_whole(tiles, units, C)) dp = static_cast<int>(tiles);
-    if (dp == tiles && !g_opt.split_all) {
+    auto all_whole = [&] {
         pl->grid = static_cast<int>(std::min<long long>(C, tiles));
-        pl->dp_tiles = dp;
+        pl->dp_tiles = static_cast<int>(tiles);
         pl->sk_unit_begin = static_cast<int>(units);
         pl->sk_units = 0;
         return WQ4_OK;
-    }
+    };
+    // whole waves of tiles are processed data-parallel; the rest is K-split over all CTAs
+    int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
+    if (dp < tiles && keep_tiles_whole(tiles, units, C)) dp = static_cast<int>(tiles);
+    if (dp == tiles && !g_opt.split_all) return all_whole();
     // units of the K-split region
     auto units_before = [&](int tile) {
         int p = 0;
-        while (p + 1 < static_cast<int>(shapes.size()) && pl->tile_begin[p + 1] <= tile) ++p;
+        while (p + 1 < P && pl->tile_begin[p + 1] <= tile) ++p;
         return pl->unit_begin[p] + static_cast<long long>(tile - pl->tile_begin[p]) * (shapes[p].K / kTileK);
     };
     long long sk_begin = units_before(dp);
@@ -299,12 +306,18 @@ int make_plan(const std::vector<Shape>& shapes, int sm_count, Plan* pl) {
         C = static_cast<int>(std::min<long long>(C, want));
     }
     if (sk_units * static_cast<long long>(C) >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
+    const size_t counters = ((static_cast<size_t>(tiles - dp) * 4) + 255) / 256 * 256;
+    const size_t partials = static_cast<size_t>(2) * C * pl->nt * kTileN * 4;
+    if (counters + partials > ws_cap && !g_opt.split_all && !g_opt.grid) {
+        C = g_opt.grid ? g_opt.grid : sm_count;
+        return all_whole();
+    }
     pl->grid = C;
     pl->dp_tiles = dp;
     pl->sk_unit_begin = static_cast<int>(sk_begin);
     pl->sk_units = static_cast<int>(sk_units);
-    pl->counters_bytes = ((static_cast<size_t>(tiles - dp) * 4) + 255) / 256 * 256;
-    pl->partials_bytes = static_cast<size_t>(2) * C * pl->nt * kTileN * 4;
+    pl->counters_bytes = counters;
+    pl->partials_bytes = partials;
     return WQ4_OK;
 }
 
@@ -355,24 +368,32 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
     }
 }
 
+// Plans and launches the GEMM kernel for P problems. With fixed_scratch the workspace is the
+// library's own array (kept between calls): the plan is bounded by its size and the counters it
+// uses are cleared on `st` first; otherwise it is the caller's (counters already zero).
 template <int MAXP>
-int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void* const* Wp, void* const* Y,
-             int group_size, int dtype, int qtype, void* workspace, size_t workspace_bytes, cudaStream_t st,
-             const EpilogueArgs* epi = nullptr) {
+int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const* Wp, void* const* Y,
+             int group_size, int dtype, int qtype, void* workspace, size_t workspace_bytes, bool fixed_scratch,
+             cudaStream_t st, const EpilogueArgs* epi = nullptr) {
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc) return rc;
     Plan pl;
-    rc = make_plan(shapes, dev->sm_count, &pl);
+    rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes : SIZE_MAX, &pl);
     if (rc) return rc;
     if (pl.total_tiles == 0) return WQ4_OK;
-    if (pl.workspace() > 0 && (workspace == nullptr || workspace_bytes < pl.workspace())) return WQ4_ERR_WORKSPACE;
+    if (pl.workspace() > 0 && (workspace == nullptr || workspace_bytes < pl.workspace())) {
+        if (trace_on())
+            std::fprintf(stderr, "[wq4] the plan needs %zu bytes of workspace, %zu given\n", pl.workspace(),
+                         workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+        return WQ4_ERR_WORKSPACE;
+    }
     if (pl.workspace() > 0 && !aligned16(workspace)) return WQ4_ERR_ALIGN;
 
-    auto* prm = new (std::nothrow) GemmParams<MAXP>();
-    if (!prm) return WQ4_ERR_CUDA;
+    GemmParams<MAXP> params;
+    GemmParams<MAXP>* prm = &params;
     std::memset(static_cast<void*>(prm), 0, sizeof(GemmParams<MAXP>));
-    for (size_t p = 0; p < shapes.size(); ++p) {
+    for (int p = 0; p < P; ++p) {
         ProblemDesc& d = prm->prob[p];
         d.wp = static_cast<const uint8_t*>(Wp[p]) + kBlobHeader;
         d.y = Y[p];
@@ -386,15 +407,12 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
         d.unit_begin = pl.unit_begin[p];
         if (d.M > 0) {
             rc = encode_x_map(&prm->xmap[p], X[p], d.M, d.K, dtype, pl.nt);
-            if (rc) {
-                delete prm;
-                return rc;
-            }
+            if (rc) return rc;
         }
     }
-    prm->num_problems = static_cast<int>(shapes.size());
+    prm->num_problems = P;
     prm->hdr_trusted = 1;
-    for (size_t p = 0; p < shapes.size(); ++p)
+    for (int p = 0; p < P; ++p)
         if (shapes[p].M > 0 && !blob_trusted(Wp[p], BlobKey{shapes[p].N, shapes[p].K, group_size, dtype, qtype}))
             prm->hdr_trusted = 0;
     prm->group_size = group_size;
@@ -420,15 +438,17 @@ int run_gemm(const std::vector<Shape>& shapes, const void* const* X, const void*
         prm->prob[0].bias = epi->bias;
     }
 
+    // the fixed array keeps the previous call's contents: the arrival counters must start at zero
+    if (fixed_scratch && pl.counters_bytes && cudaMemsetAsync(workspace, 0, pl.counters_bytes, st) != cudaSuccess)
+        return WQ4_ERR_CUDA;
     if (trace_on()) {
         std::fprintf(stderr,
-                     "[wq4] problems=%zu token_tile=%d grid=%d cluster=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s "
-                     "ws=%zu\n",
-                     shapes.size(), pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.dp_tiles, pl.sk_units,
-                     g_opt.a_in_smem ? "smem" : "tmem", pl.workspace());
+                     "[wq4] problems=%d token_tile=%d grid=%d cluster=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s "
+                     "ws=%zu%s\n",
+                     P, pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.dp_tiles, pl.sk_units,
+                     g_opt.a_in_smem ? "smem" : "tmem", pl.workspace(), fixed_scratch ? " (fixed array)" : "");
     }
     const cudaError_t e = dispatch(prm, MAXP > 1, pl.nt, dtype, qtype, pl.grid, st);
-    delete prm;
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
@@ -440,63 +460,6 @@ constexpr size_t kStaticScratchBytes = static_cast<size_t>(24) << 20;
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 uint8_t* g_static_scratch_addr[kMaxDevices];   // device address of the array, per device
 std::mutex g_static_mu;
-
-// The plan of make_plan for a single problem, with fixed-size state only (no heap use).
-struct PlanOne {
-    int nt = 0, grid = 0, total_tiles = 0, dp_tiles = 0, sk_unit_begin = 0, sk_units = 0, cluster = 0, m_tiles = 0;
-    size_t counters_bytes = 0, partials_bytes = 0;
-};
-
-int make_plan_one(int M, int N, int K, int sm_count, PlanOne* pl) {
-    pl->nt = token_tile_for(&M, 1);
-    pl->m_tiles = M > 0 ? (M + pl->nt - 1) / pl->nt : 0;
-    const int kg = K / kTileK;
-    const long long tiles = static_cast<long long>(pl->m_tiles) * (N / kTileN);
-    const long long units = tiles * kg;
-    if (units >= (1LL << 30) || tiles >= (1LL << 30)) return WQ4_ERR_UNSUPPORTED;
-    pl->total_tiles = static_cast<int>(tiles);
-    if (tiles == 0) return WQ4_OK;
-    int S = 0;
-    if (g_opt.cluster >= 2) {
-        S = g_opt.cluster;
-    } else if (g_opt.cluster == 0 && !g_opt.split_all && !g_opt.grid && tiles * 2 <= sm_count) {
-        // clusters of 8 only for at most 8 tiles: 16 clusters of 8 did not fit in one wave
-        // (N = 2048, 16 tiles: 19.7 us with 8, 11.3 us with 4)
-        S = static_cast<int>(std::min<long long>(tiles <= 8 ? 8 : 4, sm_count / tiles));
-    }
-    S = std::min(S, kg);
-    if (S >= 2) {
-        if (tiles * S >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
-        pl->cluster = S;
-        pl->grid = static_cast<int>(tiles * S);
-        pl->sk_unit_begin = static_cast<int>(units);
-        return WQ4_OK;
-    }
-    int C = g_opt.grid ? g_opt.grid : sm_count;
-    int dp = g_opt.split_all ? 0 : static_cast<int>((tiles / C) * C);
-    if (dp < tiles && keep_tiles_whole(tiles, units, C)) dp = static_cast<int>(tiles);
-    if (dp == tiles && !g_opt.split_all) {
-        pl->grid = static_cast<int>(std::min<long long>(C, tiles));
-        pl->dp_tiles = dp;
-        pl->sk_unit_begin = static_cast<int>(units);
-        return WQ4_OK;
-    }
-    long long sk_begin = static_cast<long long>(dp) * kg;
-    if (dp >= C && units - sk_begin < 2LL * C) {
-        dp -= C;
-        sk_begin = static_cast<long long>(dp) * kg;
-    }
-    const long long sk_units = units - sk_begin;
-    if (dp == 0 && !g_opt.grid) C = static_cast<int>(std::min<long long>(C, std::max<long long>(1, sk_units / 4)));
-    if (sk_units * static_cast<long long>(C) >= (1LL << 31)) return WQ4_ERR_UNSUPPORTED;
-    pl->grid = C;
-    pl->dp_tiles = dp;
-    pl->sk_unit_begin = static_cast<int>(sk_begin);
-    pl->sk_units = static_cast<int>(sk_units);
-    pl->counters_bytes = ((static_cast<size_t>(tiles - dp) * 4) + 255) / 256 * 256;
-    pl->partials_bytes = static_cast<size_t>(2) * C * pl->nt * kTileN * 4;
-    return WQ4_OK;
-}
 
 // Device address of g_static_scratch on the current device, looked up once per device.
 int static_scratch(uint8_t** out) {
@@ -575,17 +538,17 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
     if (!bytes || P <= 0 || P > kMaxGroupedProblems || !M || !N || !K) return WQ4_ERR_INVALID;
     int rc = check_types(group_size, WQ4_BF16, WQ4_U4B8);
     if (rc) return rc;
-    std::vector<Shape> shapes;
+    Shape shapes[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
         if ((rc = check_nk(N[p], K[p]))) return rc;
         if ((rc = check_group(group_size, K[p]))) return rc;
-        shapes.push_back({M[p], N[p], K[p]});
+        shapes[p] = Shape{M[p], N[p], K[p]};
     }
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev))) return rc;
     Plan pl;
-    if ((rc = make_plan(shapes, dev->sm_count, &pl))) return rc;
+    if ((rc = make_plan(shapes, P, dev->sm_count, SIZE_MAX, &pl))) return rc;
     *bytes = pl.workspace();
     return WQ4_OK;
 }
@@ -597,7 +560,7 @@ int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
 }
 
 static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype,
-                   int qtype, const EpilogueArgs* epi, void* workspace, size_t workspace_bytes,
+                   int qtype, const EpilogueArgs* epi, void* workspace, size_t workspace_bytes, bool fixed_scratch,
                    wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
@@ -644,16 +607,17 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
         }
         return WQ4_OK;
     }
-    std::vector<Shape> shapes{{M, N, K}};
+    const Shape shape{M, N, K};
     const void* xs[1] = {X};
     const void* ws[1] = {Wp};
     void* ys[1] = {Y};
-    return run_gemm<1>(shapes, xs, ws, ys, group_size, dtype, qtype, workspace, workspace_bytes, stream, epi);
+    return run_gemm<1>(&shape, 1, xs, ws, ys, group_size, dtype, qtype, workspace, workspace_bytes, fixed_scratch,
+                       stream, epi);
 }
 
 int wq4_mm(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
            void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
-    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, nullptr, workspace, workspace_bytes, stream);
+    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, nullptr, workspace, workspace_bytes, false, stream);
 }
 
 int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype, int qtype,
@@ -662,7 +626,7 @@ int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int g
     if (beta != 0.f && !C) return WQ4_ERR_INVALID;
     if ((C && !aligned16(C)) || (bias && !aligned16(bias))) return WQ4_ERR_ALIGN;
     const EpilogueArgs epi{alpha, beta, beta != 0.f ? C : nullptr, bias};
-    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, &epi, workspace, workspace_bytes, stream);
+    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, &epi, workspace, workspace_bytes, false, stream);
 }
 
 int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* const* X, const void* const* Wp,
@@ -672,7 +636,7 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
     if (rc) return rc;
     if (P <= 0 || !M || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
-    std::vector<Shape> shapes;
+    Shape shapes[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
         if ((rc = check_nk(N[p], K[p]))) return rc;
@@ -681,9 +645,10 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
             if (!X[p] || !Wp[p] || !Y[p]) return WQ4_ERR_INVALID;
             if (!aligned16(X[p]) || !aligned16(Wp[p]) || !aligned16(Y[p])) return WQ4_ERR_ALIGN;
         }
-        shapes.push_back({M[p], N[p], K[p]});
+        shapes[p] = Shape{M[p], N[p], K[p]};
     }
-    return run_gemm<kMaxGroupedProblems>(shapes, X, Wp, Y, group_size, dtype, qtype, workspace, workspace_bytes, stream);
+    return run_gemm<kMaxGroupedProblems>(shapes, P, X, Wp, Y, group_size, dtype, qtype, workspace, workspace_bytes,
+                                         false, stream);
 }
 
 // ------------------------------------------------------------------ device-resident shapes
@@ -892,59 +857,11 @@ int wq4_mm_static_scratch(const void* X, const void* Wp, void* Y, int M, int N, 
                           int qtype, wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
-    if (M < 0) return WQ4_ERR_INVALID;
-    if ((rc = check_nk(N, K))) return rc;
-    if ((rc = check_group(group_size, K))) return rc;
-    if (M == 0) return WQ4_OK;
-    if (!X || !Wp || !Y) return WQ4_ERR_INVALID;
-    if (!aligned16(X) || !aligned16(Wp) || !aligned16(Y)) return WQ4_ERR_ALIGN;
-    DeviceInfo* dev = nullptr;
-    if ((rc = device_info(&dev))) return rc;
+    // resolved before the shape is looked at, so that a device's first call always does the
+    // lookup, even one that needs no scratch (M == 0, or a decode-sized M)
     uint8_t* scratch = nullptr;
     if ((rc = static_scratch(&scratch))) return rc;
-    PlanOne pl;
-    if ((rc = make_plan_one(M, N, K, dev->sm_count, &pl))) return rc;
-    if (pl.total_tiles == 0) return WQ4_OK;
-    if (pl.counters_bytes + pl.partials_bytes > kStaticScratchBytes) {
-        if (trace_on())
-            std::fprintf(stderr, "[wq4] wq4_mm_static_scratch: needs %zu bytes of scratch, the fixed array has %zu\n",
-                         pl.counters_bytes + pl.partials_bytes, kStaticScratchBytes);
-        return WQ4_ERR_WORKSPACE;
-    }
-    GemmParams<1> prm;
-    std::memset(static_cast<void*>(&prm), 0, sizeof(prm));
-    ProblemDesc& d = prm.prob[0];
-    d.wp = static_cast<const uint8_t*>(Wp) + kBlobHeader;
-    d.y = Y;
-    d.M = M;
-    d.N = N;
-    d.K = K;
-    d.n_tiles = N / kTileN;
-    d.m_tiles = pl.m_tiles;
-    d.k_groups = K / kTileK;
-    if ((rc = encode_x_map(&prm.xmap[0], X, M, K, dtype, pl.nt))) return rc;
-    prm.num_problems = 1;
-    prm.group_size = group_size;
-    prm.dtype = dtype;
-    prm.qtype = qtype;
-    prm.total_tiles = pl.total_tiles;
-    prm.dp_tiles = pl.dp_tiles;
-    prm.num_ctas = pl.grid;
-    prm.sk_unit_begin = pl.sk_unit_begin;
-    prm.sk_units = pl.sk_units;
-    prm.cluster_split = pl.cluster;
-    prm.counters = pl.counters_bytes ? reinterpret_cast<int*>(scratch) : nullptr;
-    prm.partials = pl.partials_bytes ? reinterpret_cast<float*>(scratch + pl.counters_bytes) : nullptr;
-    prm.status = dev->status;
-    prm.timeout_cycles = timeout_cycles();
-    prm.test_stall = g_opt.test_stall;
-    // the array keeps the previous call's contents: the arrival counters must start at zero
-    if (pl.counters_bytes && cudaMemsetAsync(scratch, 0, pl.counters_bytes, stream) != cudaSuccess) return WQ4_ERR_CUDA;
-    if (trace_on())
-        std::fprintf(stderr, "[wq4] static scratch: token_tile=%d grid=%d cluster=%d tiles=%d sk_units=%d scratch=%zu\n",
-                     pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.sk_units, pl.counters_bytes + pl.partials_bytes);
-    const cudaError_t e = dispatch(&prm, false, pl.nt, dtype, qtype, pl.grid, stream);
-    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+    return mm_impl(X, Wp, Y, M, N, K, group_size, dtype, qtype, nullptr, scratch, kStaticScratchBytes, true, stream);
 }
 
 }  // extern "C"
