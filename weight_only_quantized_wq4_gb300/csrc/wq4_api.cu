@@ -418,6 +418,7 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     prm->group_size = group_size;
     prm->dtype = dtype;
     prm->qtype = qtype;
+    prm->nib = nibble_consts(dtype == WQ4_BF16);
     prm->total_tiles = pl.total_tiles;
     prm->dp_tiles = pl.dp_tiles;
     prm->num_ctas = pl.grid;
@@ -745,6 +746,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
     prm->group_size = group_size;
     prm->dtype = dtype;
     prm->qtype = qtype;
+    prm->nib = nibble_consts(dtype == WQ4_BF16);
     prm->total_tiles = static_cast<int>(max_tiles);
     prm->dp_tiles = static_cast<int>(max_tiles);
     prm->num_ctas = grid;

@@ -67,6 +67,7 @@ struct DecodeParams {
     float alpha, beta;
     const void* c;           // [M][N], read when beta != 0 (may be Y itself)
     const void* bias;        // [N] or null
+    NibbleConsts nib;        // nibble_consts(dtype == bf16)
 };
 
 template <int NB>
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
     }
     if (active && ok) {
         const uint32_t ld_off = 256u * (lane >> 4) + 16u * ((lane & 7) + 8 * ((lane >> 3) & 1));
-        constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
+        const NibbleConsts nib = prm.nib;
         int next_g = ks;                                                // next group of this slice
         int sd = 0;                                                     // stage's slot within the block's Db
         uint32_t ph = 0;
@@ -343,8 +344,8 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             // bit logic on the integer pipe, the exact subtraction on the fp16/bf16 one
-                            lo[e] = dec_sub2<BF16>(((wlo >> (4 * e)) & 0x000F000Fu) | kMagic, sub_lo);
-                            hi[e] = dec_sub2<BF16>(((whi >> (4 * e)) & 0x000F000Fu) | kMagic, sub_hi);
+                            lo[e] = dec_sub2<BF16>(and_or(wlo >> (4 * e), nib.mask, nib.magic), sub_lo);
+                            hi[e] = dec_sub2<BF16>(and_or(whi >> (4 * e), nib.mask, nib.magic), sub_hi);
                         }
                         const uint32_t a0[4] = {lo[0], hi[0], lo[1], hi[1]};
                         const uint32_t a1[4] = {lo[2], hi[2], lo[3], hi[3]};
@@ -546,6 +547,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     p.group_size = group_size;
     p.dtype = dtype;
     p.qtype = qtype;
+    p.nib = nibble_consts(dtype == 0);
     p.k_groups = K / kTileK;
     p.n_blocks = N / kBlockRows;
     p.n_stages = (p.k_groups + kDecStageGroups - 1) / kDecStageGroups;

@@ -223,9 +223,8 @@ __device__ __forceinline__ uint32_t sub2(uint32_t a, uint32_t b) {
 // unit in the last place is 1, gives 128 + q (1024 + q) exactly; subtracting 128 + z (1024 + z),
 // also exact, leaves q - z.
 template <bool BF16>
-__device__ __forceinline__ uint32_t codes_to_pair(uint32_t w, uint32_t sub) {
-    constexpr uint32_t kMagic = BF16 ? 0x43004300u : 0x64006400u;
-    return sub2<BF16>((w & 0x000F000Fu) | kMagic, sub);
+__device__ __forceinline__ uint32_t codes_to_pair(uint32_t w, uint32_t sub, const NibbleConsts& nc) {
+    return sub2<BF16>(and_or(w, nc.mask, nc.magic), sub);
 }
 
 template <bool BF16>
@@ -498,6 +497,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         const int q4 = warp & 3;
         const int part = (warp - 4) >> 2;
         const int r = 32 * q4 + lane;
+        const NibbleConsts nib = prm.nib;
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
         int i = 0;
@@ -527,7 +527,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub);
+                        for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub, nib);
                     }
                     if constexpr (ATMEM) {
                         tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + a * 64 + 16 * j, out);
