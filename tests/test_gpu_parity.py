@@ -167,13 +167,14 @@ def test_decode_kernel(opts, M, N, K, dtype, qtype, const):
     assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "decode %s" % ((M, N, K, dtype, qtype),))
 
 
-@pytest.mark.parametrize("depth,trigger,const", [(2, 0, 0), (3, 1, 0), (2, 0, 1), (5, 0, 1), (16, 1, 1)])
+@pytest.mark.parametrize("depth,trigger,const", [(2, 0, 0), (3, 1, 0), (2, 0, 1), (5, 0, 1), (16, 1, 1), (0, 0, 1)])
 @pytest.mark.parametrize("M,N,K,qtype", [(8, 4096, 4096, "u4b8"), (5, 2944, 8960, "u4_zp"), (16, 768, 1408, "u4b8"),
-                                         (7, 4864, 4096, "u4_zp"), (12, 2432, 8192, "u4b8")])
+                                         (7, 4864, 4096, "u4_zp"), (12, 2432, 8192, "u4b8"), (3, 11264, 2048, "u4b8")])
 def test_decode_ring_and_modes(opts, depth, trigger, const, M, N, K, qtype):
     """The decode kernel's weight ring (forced depths, so the ring wraps many times; K not a
     multiple of 8 groups leaves a short last stage), the two trigger points and the constant-weights
-    mode (header check and first weight copies before the wait on the kernel ahead)."""
+    mode (header check and first weight copies before the wait on the kernel ahead); depth 0 is the
+    automatic ring, and N = 11264 gives a CTA 4 or 5 blocks."""
     lib = opts
     lib.set_option(lib.OPT_DECODE, 1)
     lib.set_option(lib.OPT_DECODE_DEPTH, depth)

@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 const uint32_t xg = s_x + static_cast<uint32_t>(gg) * (2 * C::kMpad * 128);
                 const uint8_t* const xe = sm + (xg - sbase) + xo_even;
                 const uint8_t* const xd = sm + (xg - sbase) + xo_odd;
-                float pr[NB][4];
+                // two independent MMA chains, one per 64-element half of the group (half the
+                // dependent latency of one chain over the group), added at the fold
+                float pr[2][NB][4];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t w[4];                                      // (2q, g) (2q, g+8) (2q+1, g) (2q+1, g+8)
@@ -353,12 +355,12 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                         for (int nb = 0; nb < NB; ++nb) {
                             const uint4 xb = *reinterpret_cast<const uint4*>(((j & 1) ? xd : xe) +
                                                                              (j >> 1) * C::kMpad * 128 + nb * 8 * 128);
-                            if (j == 0) {
-                                mma16816_z<BF16>(pr[nb], a0, xb.x, xb.y);
+                            if (h == 0) {
+                                mma16816_z<BF16>(pr[q][nb], a0, xb.x, xb.y);
                             } else {
-                                mma16816<BF16>(pr[nb], a0, xb.x, xb.y);
+                                mma16816<BF16>(pr[q][nb], a0, xb.x, xb.y);
                             }
-                            mma16816<BF16>(pr[nb], a1, xb.z, xb.w);
+                            mma16816<BF16>(pr[q][nb], a1, xb.z, xb.w);
                         }
                     }
                 }
@@ -367,10 +369,10 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 const float s_hi = dec_to_float<BF16>(sw >> 16);
 #pragma unroll
                 for (int nb = 0; nb < NB; ++nb) {
-                    acc[nb][0] = fmaf(s_lo, pr[nb][0], acc[nb][0]);
-                    acc[nb][1] = fmaf(s_lo, pr[nb][1], acc[nb][1]);
-                    acc[nb][2] = fmaf(s_hi, pr[nb][2], acc[nb][2]);
-                    acc[nb][3] = fmaf(s_hi, pr[nb][3], acc[nb][3]);
+                    acc[nb][0] = fmaf(s_lo, pr[0][nb][0] + pr[1][nb][0], acc[nb][0]);
+                    acc[nb][1] = fmaf(s_lo, pr[0][nb][1] + pr[1][nb][1], acc[nb][1]);
+                    acc[nb][2] = fmaf(s_hi, pr[0][nb][2] + pr[1][nb][2], acc[nb][2]);
+                    acc[nb][3] = fmaf(s_hi, pr[0][nb][3] + pr[1][nb][3], acc[nb][3]);
                 }
             }
             __syncwarp();
@@ -454,15 +456,24 @@ static int decode_smem_bytes(int nb, int K, int depth, bool zp) {
 }
 
 // Ring depth: the deepest that fits, capped by the items a CTA has and, while the activations are
-// small enough, by the size at which a CTA of the next launch still fits beside this one.
-static int decode_depth(int nb, int K, bool zp, int items_max, int d_min, int forced) {
+// small enough, by the size at which a CTA of the next launch still fits beside this one - unless
+// that size leaves a block a single slot (no double buffering: each stage then waits a full HBM
+// round trip) where the full size gives it two (measured, 8 tokens, N = 14336, K = 4096, constant
+// weights: 6 blocks per CTA, 10.5 us with two CTAs per SM and one slot per block, 8.9 us with one
+// CTA per SM and two slots per block).
+static int decode_depth(int nb, int K, bool zp, int items_max, int nbc, int forced) {
+    const int d_min = nbc > 2 ? nbc : 2;
     int d = forced > 0 ? forced : kDecMaxDepth;
     if (d > items_max) d = items_max;
     if (d < d_min) d = d_min;
     const bool small_x = dec_x_region(nb, K) <= 64 * 1024;
     while (d > d_min && decode_smem_bytes(nb, K, d, zp) > kDecMaxSmem) --d;
     if (forced <= 0 && small_x) {
-        while (d > d_min && decode_smem_bytes(nb, K, d, zp) > kDecCoResident) --d;
+        int dc = d;
+        while (dc > d_min && decode_smem_bytes(nb, K, dc, zp) > kDecCoResident) --dc;
+        const bool co_double = dc >= items_max || dc >= 2 * nbc;
+        const bool full_double = d >= items_max || d >= 2 * nbc;
+        if (co_double || !full_double) d = dc;
     }
     return d;
 }
@@ -559,7 +570,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     if (cap < 1) return cudaErrorInvalidConfiguration;
     if (p.n_blocks > cap * grid) grid = (p.n_blocks + cap - 1) / cap;
     const int nbc_max = (p.n_blocks + grid - 1) / grid;
-    p.depth = decode_depth(nb, K, zp, nbc_max * p.n_stages, nbc_max > 2 ? nbc_max : 2, L.depth);
+    p.depth = decode_depth(nb, K, zp, nbc_max * p.n_stages, nbc_max, L.depth);
     if (decode_smem_bytes(nb, K, p.depth, zp) > kDecMaxSmem) return cudaErrorInvalidConfiguration;
     p.status = L.status;
     p.timeout_cycles = L.timeout_cycles;
