@@ -10,8 +10,11 @@ What it computes (plain definitions, fp64, no blocking or reordering):
 * dequantisation, after "machete_mainloop.cuh", ``transform_A_kblock`` and
   ``get_conversion_mode``: a 4-bit code q is up-converted, offset by its zero point (8 for the
   uint4b8 type, the stored per-group z in zero-point mode) and multiplied by its group's scale:
-  W[n, k] = (q[n, k] - z[n, k // G]) * s[n, k // G].  The value is formed exactly in fp64; where
-  and how a kernel rounds it is the kernel's business, the oracle holds the exact number.
+  W[n, k] = (q[n, k] - z[n, k // G]) * s[n, k // G].  In the float-zero mode (the page's
+  scale-with-zero conversion: the zero, a value of the scale type, is added after the scale
+  multiply) W[n, k] = q[n, k] * s[n, k // G] + zf[n, k // G].  The value is formed exactly in
+  fp64; where and how a kernel rounds it is the kernel's business, the oracle holds the exact
+  number.
 * the product, after the header comment of "machete_mainloop.cuh" (Y = X W^t, computed there as
   Y^t = W^t X^t): Y[m, n] = sum_k X[m, k] * W[n, k], in fp64 with ``numpy.matmul``.
 * one scale row per group of G consecutive K elements, groups starting at K = 0, G, 2G, ...
@@ -26,8 +29,10 @@ What it computes (plain definitions, fp64, no blocking or reordering):
 
 Pins (tests/test_oracle_pins.py) tie each function to something other than itself: exact
 rational brute force with hand-decoded floating-point bits, closed forms (one-hot, identity,
-all-zero), the per-group scale invariant, the uint4b8 == zero-point(8) identity, IEEE bit
-patterns, the nibble order, and a per-element brute-force placement of the blob layout.
+all-zero; for float zeros: one-hot and zero codes against exact group sums), the per-group scale
+invariant, the uint4b8 == zero-point(8) identity, the float-zero == integer-zero identity where
+-z s is exact, IEEE bit patterns, the nibble order, and a per-element brute-force placement of
+the blob layout.
 """
 from __future__ import annotations
 
@@ -40,7 +45,7 @@ HEADER_BYTES = 256
 BLOB_MAGIC = 0x50345157  # bytes "WQ4P" little-endian
 BLOB_VERSION = 2
 DTYPE_CODE = {"bf16": 0, "fp16": 1}
-QTYPE_CODE = {"u4b8": 0, "u4_zp": 1}
+QTYPE_CODE = {"u4b8": 0, "u4_zp": 1, "u4_fzp": 2}
 ONE_BITS = {"bf16": 0x3F80, "fp16": 0x3C00}   # 1.0, the scale slot of a weight without scales
 
 
@@ -78,6 +83,8 @@ def zero_points(N: int, K: int, qtype: str, Z_words=None, group_size: int = GROU
         return np.full((ng, N), 8, dtype=np.int64)
     if qtype == "u4_zp":
         return unpack_u4(Z_words, N).astype(np.int64).reshape(ng, N)
+    if qtype == "u4_fzp":                                       # the offset is a float (below)
+        return np.zeros((ng, N), dtype=np.int64)
     raise ValueError(qtype)
 
 
@@ -86,7 +93,10 @@ def dequantize(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
     """W[n, k] = (q[n, k] - z[k // G, n]) * s[k // G, n] in fp64 (exact: |q - z| <= 15 times a
     16-bit scale needs at most 15 significant bits).  Without scales (``S_bits`` None) the value
     is the converted code itself, q - z: the direct-conversion mode of "machete_mainloop.cuh",
-    ``get_conversion_mode`` (no scale operand given)."""
+    ``get_conversion_mode`` (no scale operand given).  Float-zero mode (``qtype`` "u4_fzp",
+    ``Z_words`` the zeros' 16-bit bits [K/G][N]): W[n, k] = q[n, k] * s + zf, exact in fp64 when
+    the exponents of q s (at most 15 significant bits) and zf (at most 11) are within 27 of each
+    other, as for every input drawn here."""
     if K % group_size:
         raise ValueError("K must be a multiple of the group size")
     q = unpack_u4(Wq, K).astype(np.int64)                       # [N][K]
@@ -95,7 +105,13 @@ def dequantize(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
     g_of_k = np.arange(K) // group_size
     zk = z[g_of_k, :].T                                         # [N][K]
     sk = s[g_of_k, :].T                                         # [N][K]
-    return (q - zk).astype(np.float64) * sk
+    W = (q - zk).astype(np.float64) * sk
+    if qtype == "u4_fzp":
+        if S_bits is None:
+            raise ValueError("float zeros need scales")
+        zf = decode16(Z_words, dtype).reshape(K // group_size, N)
+        W = W + zf[g_of_k, :].T
+    return W
 
 
 def mm(X_bits, Wq, S_bits, M: int, N: int, K: int, dtype: str, qtype: str, Z_words=None,
@@ -157,8 +173,9 @@ BLOCKS = TILE_N // BLOCK_ROWS
 
 def block_bytes(qtype: str) -> int:
     """Bytes of one 16-row block of a tile record: 1024 B of codes, 32 B of scales and, in
-    zero-point mode, 8 B of zero points, padded to a multiple of 16 B."""
-    raw = 1024 + 32 + (8 if qtype == "u4_zp" else 0)
+    zero-point mode, 8 B of zero points (float-zero mode: 32 B of float zeros), padded to a
+    multiple of 16 B."""
+    raw = 1024 + 32 + {"u4b8": 0, "u4_zp": 8, "u4_fzp": 32}[qtype]
     return (raw + 15) // 16 * 16
 
 
@@ -188,7 +205,7 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
 
     Layout (version 2):
       * header, 256 B of little-endian uint32: magic "WQ4P", version 2, N, K, group size,
-        dtype code (bf16 0, fp16 1), qtype code (u4b8 0, u4_zp 1), tile bytes, N/128, K/128,
+        dtype code (bf16 0, fp16 1), qtype code (u4b8 0, u4_zp 1, u4_fzp 2), tile bytes, N/128, K/128,
         then zeros.
       * tile records in order (nt, g), nt = 0..N/128-1 outer, g = 0..K/128-1 inner, record
         (nt, g) at byte 256 + (nt * K/128 + g) * tile_bytes.  A record is eight blocks of
@@ -201,6 +218,8 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
             (rows rr and rr + 8 share one 32-bit word).
           - zero points (u4_zp only), 8 B at offset 1056: the zero point of row rr in byte rr % 8,
             low nibble for rr < 8, high nibble for rr >= 8.
+          - float zeros (u4_fzp only), 32 B at offset 1056, placed like the scales: the 16-bit
+            zero of row rr at byte 1056 + 4 (rr % 8) + 2 (rr // 8).
           - zero padding up to block_bytes.
     """
     if group_size % TILE_K or K % group_size or N % TILE_N or K % TILE_K:
@@ -236,6 +255,13 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
         z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, BLOCKS, BLOCK_ROWS)
         zb = (z[..., :8] | (z[..., 8:] << 4)).astype(np.uint8)              # [g][nt][b][8]
         blocks[:, :, :, 1056:1064] = zb.transpose(1, 0, 2, 3)
+    if qtype == "u4_fzp":
+        if S_bits is None:
+            raise ValueError("float zeros need scales")
+        ZF = np.asarray(Z_words, dtype=np.uint16).reshape(K // group_size, N)[src]
+        ZF = ZF.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
+        blocks[:, :, :, 1056:1088] = np.ascontiguousarray(ZF.transpose(1, 0, 2, 3)).view(np.uint8).reshape(
+            nT, nG, BLOCKS, 32)
     return blob
 
 
@@ -246,8 +272,9 @@ def _pack_rows(z: np.ndarray) -> np.ndarray:
 
 
 def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str, group_size: int = GROUP):
-    """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] or None);
-    quantisation group j is read from its first record, 128-K record j G / 128."""
+    """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] uint32 for
+    u4_zp, [K/G][N] uint16 float zeros for u4_fzp, else None); quantisation group j is read from
+    its first record, 128-K record j G / 128."""
     nT, nG = N // TILE_N, K // TILE_K
     first = (np.arange(K // group_size) * group_size) // TILE_K
     tb, bb = tile_bytes(qtype), block_bytes(qtype)
@@ -264,6 +291,11 @@ def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str, group_si
     if qtype == "u4_zp":
         zb = blocks[..., 1056:1064].astype(np.uint32)            # [nt][g][b][8]
         z = np.concatenate([zb & 0xF, zb >> 4], axis=-1)         # rows 0..7, then 8..15
-        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
+        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2, 3)).reshape(nG, N)[first]).astype(np.uint32)
+    if qtype == "u4_fzp":
+        zs = np.ascontiguousarray(blocks[..., 1056:1088]).view(np.uint16).reshape(nT, nG, BLOCKS, BLOCK_ROWS)
+        ZF = np.empty_like(zs)
+        ZF[..., SCALE_SLOT_ROW] = zs
+        Z = np.ascontiguousarray(np.ascontiguousarray(ZF.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
     Wq = _pack_rows(q)
-    return Wq.astype(np.uint32), S_bits, (None if Z is None else Z.astype(np.uint32))
+    return Wq.astype(np.uint32), S_bits, Z

@@ -43,6 +43,35 @@ def _dq_scale_rows_swapped(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_s
     return out[::-1].copy()                          # rows of W attached to the wrong outputs
 
 
+def _fzp_parts(Wq, S_bits, N, K, dtype, Z_words, group_size):
+    q = W.unpack_u4(Wq, K).astype(np.float64)
+    g = np.arange(K) // group_size
+    s = W.decode16(S_bits, dtype)[g, :].T
+    zf = W.decode16(Z_words, dtype).reshape(K // group_size, N)[g, :].T
+    return q, s, zf
+
+
+def _dq_fzp_zero_before_scale(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    if qtype != "u4_fzp":
+        return _good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+    q, s, zf = _fzp_parts(Wq, S_bits, N, K, dtype, Z_words, group_size)
+    return (q + zf) * s
+
+
+def _dq_fzp_zero_dropped(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    if qtype != "u4_fzp":
+        return _good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+    q, s, zf = _fzp_parts(Wq, S_bits, N, K, dtype, Z_words, group_size)
+    return q * s
+
+
+def _dq_fzp_zero_subtracted(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+    if qtype != "u4_fzp":
+        return _good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+    q, s, zf = _fzp_parts(Wq, S_bits, N, K, dtype, Z_words, group_size)
+    return q * s - zf
+
+
 def _unpack_big_endian(words, length):
     words = np.asarray(words, dtype=np.uint32)
     shifts = 28 - 4 * np.arange(8, dtype=np.uint32)
@@ -62,6 +91,9 @@ MUTANTS = {
     "weight rows permuted": ("dequantize", _dq_scale_rows_swapped),
     "big-endian nibbles": ("unpack_u4", _unpack_big_endian),
     "bf16 decoded as fp16": ("decode16", _decode_bf16_as_fp16),
+    "float zero added before the scale": ("dequantize", _dq_fzp_zero_before_scale),
+    "float zero dropped": ("dequantize", _dq_fzp_zero_dropped),
+    "float zero subtracted": ("dequantize", _dq_fzp_zero_subtracted),
 }
 
 
@@ -73,6 +105,9 @@ def _pins_all_pass():
         lambda: pins.test_group_scale_invariant("u4b8"),
         lambda: pins.test_decode16_bit_patterns(),
         lambda: pins.test_nibble_order_is_little_endian(),
+        lambda: pins.test_oracle_equals_exact_brute_force("fp16", "u4_fzp", (1, 8, 128)),
+        lambda: pins.test_float_zero_one_hot_closed_form(),
+        lambda: pins.test_float_zero_alone_is_group_sums(),
     ]
     for c in checks:
         try:

@@ -59,11 +59,15 @@ def brute_force(p):
             for k in range(p.K):
                 qv = nibble_hex(p.Wq[n, k // 8], k % 8)
                 g = k // G
-                zv = 8 if p.qtype == "u4b8" else nibble_hex(p.Z[g, n // 8], n % 8)
                 sv = exact16(int(p.S_bits[g, n]), p.dtype) if p.S_bits is not None else Fraction(1)
                 xv = exact16(int(p.X_bits[m, k]), p.dtype)
-                acc += xv * (qv - zv) * sv
-                aabs += abs(xv * (qv - zv) * sv)
+                if p.qtype == "u4_fzp":                     # code times scale, plus the float zero
+                    wv = qv * sv + exact16(int(p.Z[g, n]), p.dtype)
+                else:
+                    zv = 8 if p.qtype == "u4b8" else nibble_hex(p.Z[g, n // 8], n % 8)
+                    wv = (qv - zv) * sv
+                acc += xv * wv
+                aabs += abs(xv * wv)
             row.append(acc)
             arow.append(aabs)
         Y.append(row)
@@ -104,7 +108,7 @@ def test_input_rounding_is_rne():
 
 # ---------------------------------------------------------------- brute force
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])
+@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp", "u4_fzp"])
 @pytest.mark.parametrize("shape", [(1, 8, 128), (3, 16, 256), (2, 8, 384)])
 def test_oracle_equals_exact_brute_force(dtype, qtype, shape):
     M, N, K = shape
@@ -246,6 +250,57 @@ def test_u4b8_equals_zero_point_8():
     assert np.array_equal(O.mm_problem(p), O.mm_problem(pz))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_float_zero_equals_integer_zero_when_exact(dtype):
+    """Float-zero mode with zf = -z s, for scales of at most 4 significant bits (so that z s,
+    z <= 9, is exact in the 16-bit type), gives the integer zero-point mode's result bit for bit."""
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 32, 384
+    q = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    z = rng.integers(6, 10, (K // 128, N)).astype(np.uint8)
+    s = rng.integers(8, 16, (K // 128, N)) * 2.0 ** -10                  # m 2^-10, m in 8..15
+    S = I.f32_to_bits(s.astype(np.float32), dtype)
+    zs = -z.astype(np.float64) * s
+    ZF = I.f32_to_bits(zs.astype(np.float32), dtype)
+    assert np.array_equal(O.decode16(ZF, dtype), zs)                     # the premise: exact
+    X = I.f32_to_bits(rng.standard_normal((M, K)).astype(np.float32), dtype)
+    p_int = I.problem_from_codes(X, q, S, z, dtype, "u4_zp")
+    p_flt = I.problem_from_codes(X, q, S, ZF, dtype, "u4_fzp")
+    assert np.array_equal(O.mm_problem(p_int), O.mm_problem(p_flt))
+
+
+def test_float_zero_one_hot_closed_form():
+    """X one-hot at k*: Y[m, n] = x_m (q[n, k*] s[g*, n] + zf[g*, n]), g* = k* // 128 (exact)."""
+    rng = np.random.default_rng(22)
+    M, N, K, k_star = 4, 16, 512, 301
+    p0 = I.make_problem(M, N, K, "bf16", "u4_fzp", seed=22)
+    X = np.zeros((M, K), np.uint16)
+    X[:, k_star] = I.f32_to_bits(rng.standard_normal(M).astype(np.float32), "bf16")
+    p = I.problem_from_codes(X, p0.q, p0.S_bits, p0.Z, "bf16", "u4_fzp")
+    Y = O.mm_problem(p)
+    g = k_star // 128
+    for m in range(M):
+        for n in range(N):
+            w = int(p.q[n, k_star]) * bf16_exact(int(p.S_bits[g, n])) + bf16_exact(int(p.Z[g, n]))
+            assert Y[m, n] == float(bf16_exact(int(X[m, k_star])) * w)
+
+
+def test_float_zero_alone_is_group_sums():
+    """Codes all 0: Y[m, n] = sum_g zf[g, n] * (sum of X[m, k] over group g), exact rationals."""
+    rng = np.random.default_rng(23)
+    M, N, K = 2, 8, 384
+    p0 = I.make_problem(M, N, K, "fp16", "u4_fzp", seed=23)
+    p = I.problem_from_codes(p0.X_bits, np.zeros((N, K), np.uint8), p0.S_bits, p0.Z, "fp16", "u4_fzp")
+    Y = O.mm_problem(p)
+    for m in range(M):
+        gsum = [sum((fp16_exact(int(p.X_bits[m, k])) for k in range(128 * g, 128 * g + 128)), Fraction(0))
+                for g in range(K // 128)]
+        for n in range(N):
+            exact = sum((fp16_exact(int(p.Z[g, n])) * gsum[g] for g in range(K // 128)), Fraction(0))
+            assert abs(Y[m, n] - float(exact)) <= 1e-12 * (1 + abs(float(exact)))
+    del rng
+
+
 def test_linearity_in_x():
     rng = np.random.default_rng(9)
     p = I.make_problem(4, 32, 256, "bf16", "u4b8", seed=9)
@@ -289,10 +344,11 @@ def test_tolerance_check():
 def _brute_blob(p) -> np.ndarray:
     """The blob built one element at a time straight from the layout's wording (record g carries
     the scale and zero point of quantisation group 128 g // G; no scales: 1.0 = 0x3F80 / 0x3C00):
-    record (nt, g) is eight 16-row blocks of 1056 B (uint4b8) or 1072 B (zero points); in block b,
-    row rr's K elements 32 j + [0, 32) form 16-byte chunk 16 j + rr, its scale sits at byte
-    1024 + 4 (rr % 8) + 2 (rr // 8), its zero point in byte 1056 + rr % 8 (high nibble for rr >= 8)."""
-    bb = 1072 if p.qtype == "u4_zp" else 1056
+    record (nt, g) is eight 16-row blocks of 1056 B (uint4b8), 1072 B (zero points) or 1088 B
+    (float zeros); in block b, row rr's K elements 32 j + [0, 32) form 16-byte chunk 16 j + rr,
+    its scale sits at byte 1024 + 4 (rr % 8) + 2 (rr // 8), its zero point in byte 1056 + rr % 8
+    (high nibble for rr >= 8), its float zero at byte 1056 + 4 (rr % 8) + 2 (rr // 8)."""
+    bb = {"u4b8": 1056, "u4_zp": 1072, "u4_fzp": 1088}[p.qtype]
     tb = 8 * bb
     nG = p.K // 128
     G = p.group_size
@@ -319,16 +375,20 @@ def _brute_blob(p) -> np.ndarray:
             blob[so:so + 2] = list(sbits.to_bytes(2, "little"))
             if p.qtype == "u4_zp":
                 blob[blk + 1056 + rr % 8] |= int(p.z[(128 * g) // G, n]) << (4 * (rr // 8))
+            if p.qtype == "u4_fzp":                         # float zeros placed like the scales
+                zo = blk + 1056 + 4 * (rr % 8) + 2 * (rr // 8)
+                blob[zo:zo + 2] = list(int(p.Z[(128 * g) // G, n]).to_bytes(2, "little"))
     return blob
 
 
-@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])
+@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp", "u4_fzp"])
 def test_blob_layout_brute_force(qtype):
     p = I.make_problem(1, 256, 256, "bf16", qtype, seed=13)
     assert np.array_equal(O.prepack(p.Wq, p.S_bits, p.N, p.K, p.dtype, p.qtype, p.Z), _brute_blob(p))
 
 
 @pytest.mark.parametrize("qtype,G,scaled,dtype", [("u4_zp", 256, True, "bf16"), ("u4b8", 512, True, "fp16"),
+                                                  ("u4_fzp", 256, True, "fp16"),
                                                   ("u4b8", 128, False, "bf16"), ("u4b8", 256, False, "fp16")])
 def test_blob_layout_group_sizes_brute_force(qtype, G, scaled, dtype):
     p = I.make_problem(1, 256, 512, dtype, qtype, seed=G + 1, group_size=G, scaled=scaled)
@@ -338,7 +398,7 @@ def test_blob_layout_group_sizes_brute_force(qtype, G, scaled, dtype):
     assert np.array_equal(Wq, p.Wq)
     if scaled:
         assert np.array_equal(S, p.S_bits)
-    if qtype == "u4_zp":
+    if qtype in ("u4_zp", "u4_fzp"):
         assert np.array_equal(Z, p.Z)
 
 
@@ -349,7 +409,7 @@ def test_blob_rejects_unsupported_group_sizes():
             O.prepack(p.Wq, np.zeros((512 // 64, 128), np.uint16), p.N, p.K, p.dtype, p.qtype, group_size=G)
 
 
-@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])
+@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp", "u4_fzp"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_blob_round_trip(qtype, dtype):
     p = I.make_problem(1, 384, 640, dtype, qtype, seed=14)
@@ -357,7 +417,7 @@ def test_blob_round_trip(qtype, dtype):
     assert blob.size == O.prepacked_bytes(p.N, p.K, qtype)
     Wq, S, Z = O.unprepack(blob, p.N, p.K, dtype, qtype)
     assert np.array_equal(Wq, p.Wq) and np.array_equal(S, p.S_bits)
-    if qtype == "u4_zp":
+    if qtype in ("u4_zp", "u4_fzp"):
         assert np.array_equal(Z, p.Z)
     hdr = blob[:40].view(np.uint32)
     assert hdr.tolist() == [O.BLOB_MAGIC, 2, 384, 640, 128, O.DTYPE_CODE[dtype], O.QTYPE_CODE[qtype],

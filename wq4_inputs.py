@@ -10,12 +10,15 @@ Input formats (the layouts the public API takes):
 * ``Wq``      uint32 [N][K/8]    4-bit weight codes q in [0, 15], eight per word along K; code of
                                  element k = 8*j + i sits in bits [4i, 4i+4) of word j.
 * ``S_bits``  uint16 [K/G][N]    one scale per (group, weight row), N contiguous, raw 16-bit bits.
-* ``Z``       uint32 [K/G][N/8]  (uint4 + zero-point mode only) zero points z in [0, 15], eight per
-                                 word along N with the same little-endian nibble order.
+* ``Z``       uint32 [K/G][N/8]  (uint4 + zero-point mode) zero points z in [0, 15], eight per
+                                 word along N with the same little-endian nibble order;
+              uint16 [K/G][N]    (uint4 + float-zero mode) one pre-scaled float zero per (group,
+                                 weight row), raw 16-bit bits, like the scales.
 
 Draw recipe (seed = 1000 + the workload's 1-based index): one ``numpy.random.default_rng(seed)``
 draws, in this order, X ~ N(0, 1) in fp32, the codes q ~ U{0..15}, the scales s ~ U[0.005, 0.02]
-in fp32, the zero points z ~ U{6..9} (zero-point mode only). The grouped workload draws X for
+in fp32, the zero points z ~ U{6..9} (zero-point mode) or the float zeros ~ U[-0.18, -0.03] in
+fp32 (float-zero mode). The grouped workload draws X for
 all sum_M rows first, then each problem's q, s (and z) in problem order, then the token split
 M_p ~ Multinomial(sum_M, uniform); problem p takes the next M_p rows of X. fp32 draws are rounded
 to the 16-bit type with round-to-nearest-even.
@@ -32,6 +35,7 @@ BF16 = "bf16"
 FP16 = "fp16"
 U4B8 = "u4b8"      # stored code minus 8
 U4_ZP = "u4_zp"    # stored code minus a per-group zero point
+U4_FZP = "u4_fzp"  # stored code times the scale plus a per-group float zero (pre-scaled)
 
 
 def f32_to_bits(a: np.ndarray, dtype: str) -> np.ndarray:
@@ -68,8 +72,9 @@ class Problem:
     q: np.ndarray                    # uint8  [N][K]  (the codes before packing, for tests)
     Wq: np.ndarray                   # uint32 [N][K/8]
     S_bits: Optional[np.ndarray]     # uint16 [K/G][N]; None = no scales (direct conversion)
-    z: Optional[np.ndarray] = None   # uint8  [K/G][N]
-    Z: Optional[np.ndarray] = None   # uint32 [K/G][N/8]
+    z: Optional[np.ndarray] = None   # uint8  [K/G][N] (u4_zp)
+    Z: Optional[np.ndarray] = None   # zero points as the API takes them: uint32 [K/G][N/8] of 4-bit
+                                     # values (u4_zp), or uint16 [K/G][N] float zeros (u4_fzp)
     group_size: int = GROUP
 
 
@@ -84,6 +89,9 @@ def problem_from_codes(X_bits, q, S_bits, z, dtype, qtype, group_size=GROUP) -> 
     if qtype == U4_ZP:
         z = np.ascontiguousarray(z, dtype=np.uint8)
         Z = pack_u4(z)
+    elif qtype == U4_FZP:                   # z holds the float zeros' 16-bit patterns
+        Z = np.ascontiguousarray(z, dtype=np.uint16)
+        z = None
     else:
         z = None
     return Problem(M, N, K, dtype, qtype, X_bits, q, pack_u4(q), S_bits, z, Z, group_size)
@@ -96,6 +104,8 @@ def _draw(rng, M, N, K, dtype, qtype, X_bits=None, group_size=GROUP, scaled=True
     ng = K // group_size
     S_bits = f32_to_bits(rng.uniform(0.005, 0.02, size=(ng, N)).astype(np.float32), dtype) if scaled else None
     z = rng.integers(6, 10, size=(ng, N), dtype=np.uint8) if qtype == U4_ZP else None
+    if qtype == U4_FZP:                     # about -z s for z in 6..9 and s in the scale range
+        z = f32_to_bits(rng.uniform(-0.18, -0.03, size=(ng, N)).astype(np.float32), dtype)
     return problem_from_codes(X_bits, q, S_bits, z, dtype, qtype, group_size)
 
 
