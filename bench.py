@@ -21,6 +21,7 @@ own line (rate, roofline, clocks) is under "workloads".
 Variants of a workload (measured like the workload itself; the default line uses none):
   --group-size G / --no-scales   other group sizes, or uint4b8 without scales (direct conversion)
   --epilogue                     Y = X.dequant(W)^T + C + bias through wq4_mm_ex (C, bias read)
+  --float-zeros                  the workload's weight in the float-zero format (value = q s + zf)
   --device-m                     grouped workload with its token counts in device memory
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own replica of the workload
@@ -84,6 +85,8 @@ def variant_of(args):
         v["epilogue"] = "Y = acc + C + bias (wq4_mm_ex)"
     if args.device_m:
         v["token_counts"] = "device memory (wq4_grouped_mm_device_m)"
+    if getattr(args, "float_zeros", False):
+        v["qtype"] = "u4_fzp (value = q s + zf, float zero per group and row)"
     return v
 
 
@@ -93,10 +96,12 @@ def make_inputs(args):
     kind = spec.pop("kind")
     if args.no_scales and spec["qtype"] != I.U4B8:
         raise SystemExit("--no-scales applies to uint4b8 weights")
+    if getattr(args, "float_zeros", False):
+        spec["qtype"] = I.U4_FZP
     if kind == "mm":
         return I.make_problem(**spec, group_size=args.group_size, scaled=not args.no_scales)
-    if args.group_size != I.GROUP or args.no_scales or args.epilogue:
-        raise SystemExit("--group-size, --no-scales and --epilogue apply to single-problem workloads")
+    if args.group_size != I.GROUP or args.no_scales or args.epilogue or getattr(args, "float_zeros", False):
+        raise SystemExit("--group-size, --no-scales, --epilogue and --float-zeros apply to single-problem workloads")
     return I.make_grouped(**spec)
 
 
@@ -198,7 +203,7 @@ class Workload:
         self.args = args
         self.dev = dev
         vargs = args if use_variant else argparse.Namespace(group_size=I.GROUP, no_scales=False, epilogue=False,
-                                                           device_m=False, workload=name)
+                                                           device_m=False, float_zeros=False, workload=name)
         self.vargs = vargs
         probs = make_inputs(argparse.Namespace(**dict(vars(vargs), workload=name)))
         self.probs = probs
@@ -223,8 +228,12 @@ class Workload:
         def c32(words):
             return torch.from_numpy(np.ascontiguousarray(words).view(np.int32)).to(dev)
 
-        src = [(c32(p.Wq), c16(p.S_bits) if p.S_bits is not None else None, c32(p.Z) if p.Z is not None else None)
-               for p in plist]
+        def zeros(p):
+            if p.Z is None:
+                return None
+            return c16(p.Z) if p.qtype == I.U4_FZP else c32(p.Z)
+
+        src = [(c32(p.Wq), c16(p.S_bits) if p.S_bits is not None else None, zeros(p)) for p in plist]
 
         def blobs():
             return [wq4.prepack(wq, sc, z, qtype=p.qtype, group_size=G, dtype=dtype) for (wq, sc, z), p in zip(src, plist)]
@@ -242,7 +251,7 @@ class Workload:
         elif self.grouped:
             self.ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
         else:
-            self.ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G)
+            self.ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G, plist[0].qtype)
         self.set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in self.base_W) + \
             sum(p.M * p.N * 2 for p in plist) * (2 if vargs.epilogue else 1) + self.ws_bytes
         M_dev = torch.tensor([p.M for p in plist], dtype=torch.int32, device=dev) if vargs.device_m else None
@@ -627,6 +636,7 @@ def main():
     ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
     ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")
     ap.add_argument("--device-m", action="store_true", help="variant: grouped token counts in device memory")
+    ap.add_argument("--float-zeros", action="store_true", help="variant: the weight in the float-zero format")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up and the timed replay (for profiler runs): no soak, e2e or CPU baseline")
     args = ap.parse_args()

@@ -21,7 +21,10 @@
  *  - Arguments are checked before anything is launched; on a negative status nothing was
  *    launched and no buffer was touched.
  *  - dtype: WQ4_BF16 or WQ4_FP16; X, the scales and Y share it. qtype: WQ4_U4B8 (value =
- *    code - 8) or WQ4_U4_ZP (value = code - z with a 4-bit zero point per group and row).
+ *    (code - 8) s), WQ4_U4_ZP (value = (code - z) s with a 4-bit zero point per group and row) or
+ *    WQ4_U4_FZP (value = code s + zf with a float zero of the dtype per group and row, added after
+ *    the scale: the scale-with-zero conversion of "machete_mainloop.cuh", transform_A_kblock;
+ *    single-problem calls only).
  *  - group_size G: a multiple of 128 that divides K (G == K: one scale per row, channel-wise;
  *    "machete_mainloop.cuh", can_implement and load); other sizes give WQ4_ERR_UNSUPPORTED.
  *    N and K multiples of 128; M >= 0. The G passed to the GEMM calls must be the one the
@@ -51,7 +54,7 @@ enum {
     WQ4_ERR_TIMEOUT = -6       /* a kernel's bounded pipeline wait ran out (see wq4_get_last_error) */
 };
 enum { WQ4_BF16 = 0, WQ4_FP16 = 1 };
-enum { WQ4_U4B8 = 0, WQ4_U4_ZP = 1 };
+enum { WQ4_U4B8 = 0, WQ4_U4_ZP = 1, WQ4_U4_FZP = 2 };
 
 /* Library version (major * 10000 + minor * 100 + patch) and a text for a status code. */
 int wq4_version(void);
@@ -71,19 +74,20 @@ size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype);
  *   scales  [K/G][N] dtype, N contiguous (one scale per group and row); NULL for a weight
  *           without scales (WQ4_U4B8 only: the value is code - 8, the direct conversion of
  *           "machete_mainloop.cuh", get_conversion_mode), stored as 1.0.
- *   zeros   [K/G][N/8] uint32, zero point of row n = 8j+i in bits [4i, 4i+4) of word j;
- *           required for WQ4_U4_ZP and must be NULL for WQ4_U4B8.
+ *   zeros   WQ4_U4_ZP: [K/G][N/8] uint32, zero point of row n = 8j+i in bits [4i, 4i+4) of
+ *           word j. WQ4_U4_FZP: [K/G][N] dtype, the float zero of each (group, row), N
+ *           contiguous like the scales. Required for both (with scales); NULL for WQ4_U4B8.
  *   Wp_out  wq4_prepacked_bytes(...) bytes, 16-byte aligned; fully overwritten.
  * Integer work: the blob is a bit-exact permutation of the inputs. */
-int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros,
+int wq4_prepack(const uint32_t* Wq, const void* scales, const void* zeros,
                 int N, int K, int group_size, int dtype, int qtype,
                 void* Wp_out, wq4_stream_t stream);
 
 /* Exact inverse of wq4_prepack (a test and export aid), with the same G: group j of scales_out
- * [K/G][N] and zeros_out is read from its first 128-K record. zeros_out must be NULL for U4B8;
- * scales_out may be NULL (not written). */
+ * [K/G][N] and zeros_out (wq4_prepack's zeros layout for the qtype) is read from its first 128-K
+ * record. zeros_out must be NULL for U4B8; scales_out may be NULL (not written). */
 int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype,
-                  uint32_t* Wq_out, void* scales_out, uint32_t* zeros_out, wq4_stream_t stream);
+                  uint32_t* Wq_out, void* scales_out, void* zeros_out, wq4_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------ *
  * GEMM ("machete_mainloop.cuh": transform_A_kblock defines the dequantised value (code - zero)
@@ -97,6 +101,12 @@ int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int q
  * zero-filled once when allocated; every completed call leaves its counters at zero again.
  * Calls that may overlap on the GPU need separate workspaces. */
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
+
+/* wq4_workspace_bytes for a given qtype. WQ4_U4_FZP on the tensor-core path (not the decode
+ * kernel) adds a table of per-(128-K group, token) activation sums that a pre-pass writes on the
+ * stream before the GEMM: ceil(K/128) x (M rounded up to the token tile) fp32 after the plan's
+ * own bytes (256-byte aligned). For the other qtypes the answer equals wq4_workspace_bytes. */
+int wq4_workspace_bytes_ex(int M, int N, int K, int group_size, int qtype, size_t* bytes);
 
 /* Y = X . dequant(Wp)^T.
  *   X   [M][K] dtype row-major, 16-byte aligned.

@@ -35,6 +35,8 @@ def test_prepacked_bytes(clib):
     assert clib.wq4_prepacked_bytes(128, 1024, 384, 0) == 0       # 384 does not divide K
     assert clib.wq4_prepacked_bytes(128, 1024, 256, 0) == 256 + 8 * 8448   # one record per 128 K
     assert clib.wq4_prepacked_bytes(128, 640, 640, 1) == 256 + 5 * 8576    # channel-wise (G = K)
+    assert clib.wq4_prepacked_bytes(256, 512, 128, 2) == 256 + 2 * 4 * 8704  # float zeros: 1088-byte blocks
+    assert clib.wq4_prepacked_bytes(128, 128, 128, 3) == 0                   # no such qtype
 
 
 A16 = ctypes.c_void_p(0x10000)     # 16-byte aligned fake device addresses (never dereferenced)
@@ -75,6 +77,9 @@ def test_prepack_argument_rules(clib):
     assert pp(A16, A16b, None, 128, 256, 64, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED   # G not a multiple of 128
     assert pp(MIS, A16b, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN
     assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
+    assert pp(A16, A16b, A16c, 128, 128, 128, 0, 2, A16c, None) != wq4.ERR_INVALID   # float zeros with scales
+    assert pp(A16, A16b, None, 128, 128, 128, 0, 2, A16c, None) == wq4.ERR_INVALID   # float zeros missing
+    assert pp(A16, None, A16c, 128, 128, 128, 0, 2, A16c, None) == wq4.ERR_INVALID   # float zeros need scales
 
 
 def test_mm_ex_argument_rules(clib):

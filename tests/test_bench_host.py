@@ -84,3 +84,14 @@ def test_default_run_covers_every_workload():
     assert sorted(bench.ALL_WORKLOADS) == sorted(I.WORKLOADS)
     assert bench.DEFAULT_WORKLOAD in bench.ALL_WORKLOADS
     assert bench.REPLAYS >= 5
+
+
+def test_float_zeros_variant():
+    """--float-zeros draws the workload's weight in the float-zero format and counts its zeros."""
+    a = _args(workload="asym_m128_n14336_k4096_bf16_u4zp", float_zeros=True)
+    p = bench.make_inputs(a)
+    assert p.qtype == I.U4_FZP and p.Z.dtype == np.uint16 and p.Z.shape == (p.K // 128, p.N)
+    assert bench.variant_of(a)["qtype"].startswith("u4_fzp")
+    assert bench.variant_bytes(p, a) == I.algorithmic_bytes(p.M, p.N, p.K, I.U4B8) + 2 * (p.K // 128) * p.N
+    with pytest.raises(SystemExit):
+        bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", float_zeros=True))

@@ -25,7 +25,8 @@ def opts(lib):
 
 # ------------------------------------------------------------------------------ prepack
 PREPACK_SHAPES = [(128, 128, "bf16", "u4b8"), (256, 512, "fp16", "u4b8"), (384, 256, "bf16", "u4_zp"),
-                  (512, 640, "fp16", "u4_zp"), (4096, 4096, "bf16", "u4b8"), (14336, 4096, "bf16", "u4_zp")]
+                  (512, 640, "fp16", "u4_zp"), (384, 256, "bf16", "u4_fzp"), (512, 640, "fp16", "u4_fzp"),
+                  (4096, 4096, "bf16", "u4b8"), (14336, 4096, "bf16", "u4_zp"), (4096, 4096, "bf16", "u4_fzp")]
 
 
 @pytest.mark.parametrize("N,K,dtype,qtype", PREPACK_SHAPES)
@@ -37,7 +38,7 @@ def test_prepack_bit_exact(lib, N, K, dtype, qtype):
     assert np.array_equal(blob, ref)
 
 
-@pytest.mark.parametrize("N,K,dtype,qtype", PREPACK_SHAPES[:4])
+@pytest.mark.parametrize("N,K,dtype,qtype", PREPACK_SHAPES[:6])
 def test_unprepack_round_trip(lib, N, K, dtype, qtype):
     p = I.make_problem(1, N, K, dtype, qtype, seed=3 * N + K)
     Wq, S, Z = lib.unprepack(gpu_prepack(lib, p), N, K, dtype, qtype)
@@ -45,6 +46,8 @@ def test_unprepack_round_trip(lib, N, K, dtype, qtype):
     assert np.array_equal(from_cuda16(S), p.S_bits)
     if qtype == "u4_zp":
         assert np.array_equal(from_cuda32(Z), p.Z)
+    elif qtype == "u4_fzp":
+        assert np.array_equal(from_cuda16(Z), p.Z)
     else:
         assert Z is None
 
@@ -70,6 +73,7 @@ SMALL = [
 GROUP_MODES = [
     (256, 512, "bf16", "u4_zp", 256, True), (384, 640, "fp16", "u4b8", 640, True),
     (256, 384, "bf16", "u4b8", 128, False), (128, 1024, "fp16", "u4b8", 512, False),
+    (256, 1024, "bf16", "u4_fzp", 512, True),
 ]
 
 
@@ -84,12 +88,15 @@ def test_prepack_group_sizes_bit_exact(lib, N, K, dtype, qtype, G, scaled):
         assert np.array_equal(from_cuda16(S), p.S_bits)
     if qtype == "u4_zp":
         assert np.array_equal(from_cuda32(Z), p.Z)
+    if qtype == "u4_fzp":
+        assert np.array_equal(from_cuda16(Z), p.Z)
 
 
 GROUP_MM = [
     (40, 256, 1024, "bf16", "u4_zp", 256, True), (200, 384, 512, "fp16", "u4b8", 512, True),
     (64, 256, 768, "bf16", "u4b8", 128, False), (130, 256, 2048, "bf16", "u4b8", 2048, True),
     (8, 512, 1024, "bf16", "u4_zp", 512, True), (5, 256, 640, "fp16", "u4b8", 128, False),
+    (6, 256, 1024, "bf16", "u4_fzp", 512, True), (150, 384, 1024, "fp16", "u4_fzp", 1024, True),
 ]
 
 
@@ -439,6 +446,63 @@ def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     Y = lib.mm(X, blob, N, qtype="u4_zp", out=out, alpha=alpha, C=C, beta=beta, bias=bias)
     ref = O.epilogue(O.mm_problem(p), dtype, alpha, C_bits, beta, bias_bits)
     assert_parity(y_as_f64(Y, dtype), ref, "epilogue %s" % ((M, N, K, split_all, in_place),))
+
+
+# ------------------------------------------------------------------------------ float zeros
+FZP_MM = [(1, 128, 128, "bf16"), (8, 4096, 4096, "bf16"), (5, 2944, 8960, "bf16"), (16, 768, 1408, "fp16"),
+          (33, 256, 512, "fp16"), (100, 1024, 2048, "bf16"), (300, 384, 512, "fp16"), (128, 14336, 4096, "bf16"),
+          (777, 256, 1024, "bf16")]
+
+
+@pytest.mark.parametrize("M,N,K,dtype", FZP_MM)
+def test_mm_float_zeros(lib, M, N, K, dtype):
+    """value = q s + zf (zero added after the scale) on both kernels: decode sizes (activation
+    sums from an all-ones MMA) and the tensor-core path (activation sums from a pre-pass)."""
+    p = I.make_problem(M, N, K, dtype, "u4_fzp", seed=M + 2 * N + K)
+    assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "float zeros %s" % ((M, N, K, dtype),))
+
+
+@pytest.mark.parametrize("token_tile,split_all,cluster", [(128, 1, 0), (192, 0, 0), (64, 0, 4), (16, 0, 0),
+                                                          (160, 1, 0)])
+def test_mm_float_zeros_schedules(opts, token_tile, split_all, cluster):
+    """Each CTA adds the zero term of its own groups: K-split, cluster and whole-tile plans."""
+    lib = opts
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)
+    lib.set_option(lib.OPT_CLUSTER, cluster)
+    p = I.make_problem(150, 512, 2048, "bf16", "u4_fzp", seed=token_tile + split_all + cluster)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "schedule %s" % ((token_tile, split_all, cluster),))
+
+
+@pytest.mark.parametrize("M", [6, 200])
+def test_mm_float_zeros_epilogue(opts, M):
+    lib = opts
+    N, K, dtype = 384, 1024, "fp16"
+    p = I.make_problem(M, N, K, dtype, "u4_fzp", seed=M + 5)
+    rng = np.random.default_rng(M)
+    C_bits = I.f32_to_bits(rng.standard_normal((M, N)).astype(np.float32), dtype)
+    bias_bits = I.f32_to_bits(rng.standard_normal(N).astype(np.float32), dtype)
+    Y = lib.mm(to_cuda16(p.X_bits, dtype), gpu_prepack(lib, p), N, qtype="u4_fzp", alpha=0.5,
+               C=to_cuda16(C_bits, dtype), beta=-1.25, bias=to_cuda16(bias_bits, dtype))
+    ref = O.epilogue(O.mm_problem(p), dtype, 0.5, C_bits, -1.25, bias_bits)
+    assert_parity(y_as_f64(Y, dtype), ref, "float zeros epilogue M=%d" % M)
+
+
+def test_float_zeros_contract(lib):
+    """The activation-sum table is in the workspace query of the tensor-core path only; grouped
+    calls refuse the mode; a float-zero blob read as another qtype is reported."""
+    assert lib.workspace_bytes(8, 4096, 4096, qtype="u4_fzp") == 0
+    assert lib.workspace_bytes(300, 512, 1024, qtype="u4_fzp") >= 4 * 8 * 300
+    assert lib.workspace_bytes(300, 512, 1024, qtype="u4_fzp") > lib.workspace_bytes(300, 512, 1024)
+    probs = I.make_grouped(64, 2, 256, 512, "bf16", "u4_fzp", seed=4, M_list=[30, 34])
+    with pytest.raises(lib.Wq4Error) as e:
+        _grouped(lib, probs, "u4_fzp")
+    assert e.value.status == lib.ERR_UNSUPPORTED
+    p = I.make_problem(40, 256, 512, "bf16", "u4_fzp", seed=41)
+    blob = gpu_prepack(lib, p)
+    lib.mm(to_cuda16(p.X_bits, "bf16"), blob, p.N, qtype="u4_zp")
+    assert lib.get_last_error() == lib.ERR_INVALID
+    assert_parity(y_as_f64(gpu_mm(lib, p, blob=blob), "bf16"), O.mm_problem(p), "after the mismatch")
 
 
 @pytest.mark.parametrize("qtype,dtype", [("u4b8", "bf16"), ("u4_zp", "fp16")])

@@ -25,11 +25,12 @@ def _call(lib, X, blob, Y, p):
 
 STATIC_SCRATCH_BYTES = 24 << 20
 
-# (M, N, K, dtype, qtype): the decode kernel (M = 8), cluster-split and whole tiles (M = 128), and
-# two K-split plans whose scratch would exceed the fixed array (M = 1024 and the 4096-token
-# prefill shape), which then keep their tiles whole.
+# (M, N, K, dtype, qtype): the decode kernel (M = 8), cluster-split and whole tiles (M = 128), two
+# K-split plans whose scratch would exceed the fixed array (M = 1024 and the 4096-token prefill
+# shape), which then keep their tiles whole, and float zeros (the activation-sum table in the array).
 SHAPES = [(8, 4096, 4096, "bf16", "u4b8"), (128, 14336, 4096, "bf16", "u4_zp"),
-          (1024, 4096, 4096, "bf16", "u4b8"), (4096, 4096, 14336, "bf16", "u4b8")]
+          (1024, 4096, 4096, "bf16", "u4b8"), (4096, 4096, 14336, "bf16", "u4b8"),
+          (300, 512, 1024, "bf16", "u4_fzp")]
 
 
 @pytest.mark.parametrize("M,N,K,dtype,qtype", SHAPES)
@@ -37,7 +38,7 @@ def test_static_scratch_default_options(lib, M, N, K, dtype, qtype):
     p = I.make_problem(M, N, K, dtype, qtype, seed=3000 + M)
     blob = gpu_prepack(lib, p)
     X = to_cuda16(p.X_bits, p.dtype)
-    ws = lib.workspace_bytes(M, N, K)
+    ws = lib.workspace_bytes(M, N, K, qtype=qtype)
     want_bits = from_cuda16(lib.mm(X, blob, p.N, qtype=p.qtype))
     rows = None if M <= 128 else np.random.default_rng(M).choice(M, 48, replace=False)
     ref = O.mm_problem(p, rows)

@@ -30,7 +30,9 @@ def from_cuda32(t) -> np.ndarray:
 
 
 def gpu_prepack(wq4, p):
-    Z = to_cuda32(p.Z) if p.Z is not None else None
+    Z = None
+    if p.Z is not None:
+        Z = to_cuda16(p.Z, p.dtype) if p.qtype == "u4_fzp" else to_cuda32(p.Z)
     S = to_cuda16(p.S_bits, p.dtype) if p.S_bits is not None else None
     return wq4.prepack(to_cuda32(p.Wq), S, Z, qtype=p.qtype, group_size=p.group_size, dtype=p.dtype)
 

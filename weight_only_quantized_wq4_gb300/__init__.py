@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "wq4.h")
 
 OK, ERR_INVALID, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 DTYPES = {"bf16": 0, "fp16": 1}
-QTYPES = {"u4b8": 0, "u4_zp": 1}
+QTYPES = {"u4b8": 0, "u4_zp": 1, "u4_fzp": 2}
 OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM, OPT_CLUSTER = 1, 2, 3, 4, 5, 6, 7
 OPT_DECODE, OPT_PDL, OPT_TEST_STALL = 8, 9, 10
 OPT_CONST_WEIGHTS, OPT_DECODE_DEPTH, OPT_DECODE_TRIGGER = 11, 12, 13
@@ -56,6 +56,7 @@ def load_library(path: str = LIB_PATH):
         "wq4_prepack": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, vp]),
         "wq4_unprepack": (c_int, [vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp]),
         "wq4_workspace_bytes": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]),
+        "wq4_workspace_bytes_ex": (c_int, [c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(c_size)]),
         "wq4_mm": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_mm_ex": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, ctypes.c_float, vp,
                               ctypes.c_float, vp, vp, c_size, vp]),
@@ -136,8 +137,8 @@ def prepacked_bytes(N: int, K: int, qtype: str = "u4b8", group_size: int = GROUP
 
 def prepack(Wq, scales, zeros=None, qtype: str = "u4b8", group_size: int = GROUP, dtype: str = "bf16"):
     """Wq: int32 [N][K/8] (packed codes), scales: bf16/fp16 [K/G][N] or None (no scales, uint4b8
-    only; ``dtype`` then names the activation type), zeros: int32 [K/G][N/8] or None. Returns the
-    prepacked blob (uint8 CUDA tensor)."""
+    only; ``dtype`` then names the activation type), zeros: int32 [K/G][N/8] (u4_zp), bf16/fp16
+    float zeros [K/G][N] (u4_fzp) or None. Returns the prepacked blob (uint8 CUDA tensor)."""
     torch = _torch()
     lib = load_library()
     N, K = Wq.shape[0], Wq.shape[1] * 8
@@ -154,22 +155,28 @@ def prepack(Wq, scales, zeros=None, qtype: str = "u4b8", group_size: int = GROUP
 
 
 def unprepack(blob, N: int, K: int, dtype: str = "bf16", qtype: str = "u4b8", group_size: int = GROUP):
-    """Inverse of prepack: (Wq int32 [N][K/8], scales [K/G][N], zeros int32 [K/G][N/8] or None)."""
+    """Inverse of prepack: (Wq int32 [N][K/8], scales [K/G][N], zeros: int32 [K/G][N/8] (u4_zp),
+    float zeros [K/G][N] (u4_fzp) or None)."""
     torch = _torch()
     lib = load_library()
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     Wq = torch.empty((N, K // 8), dtype=torch.int32, device=blob.device)
     sc = torch.empty((K // group_size, N), dtype=tdt, device=blob.device)
-    zs = torch.empty((K // group_size, N // 8), dtype=torch.int32, device=blob.device) if qtype == "u4_zp" else None
+    zs = None
+    if qtype == "u4_zp":
+        zs = torch.empty((K // group_size, N // 8), dtype=torch.int32, device=blob.device)
+    elif qtype == "u4_fzp":
+        zs = torch.empty((K // group_size, N), dtype=tdt, device=blob.device)
     _check(lib.wq4_unprepack(_cuda(blob, "blob"), N, K, group_size, DTYPES[dtype], QTYPES[qtype], _cuda(Wq, "Wq"),
                              _cuda(sc, "scales"), _cuda(zs, "zeros") if zs is not None else None,
                              _stream(blob.device)), "wq4_unprepack")
     return Wq, sc, zs
 
 
-def workspace_bytes(M: int, N: int, K: int, group_size: int = GROUP) -> int:
+def workspace_bytes(M: int, N: int, K: int, group_size: int = GROUP, qtype: str = "u4b8") -> int:
     out = ctypes.c_size_t(0)
-    _check(load_library().wq4_workspace_bytes(M, N, K, group_size, ctypes.byref(out)), "wq4_workspace_bytes")
+    _check(load_library().wq4_workspace_bytes_ex(M, N, K, group_size, QTYPES[qtype], ctypes.byref(out)),
+           "wq4_workspace_bytes_ex")
     return int(out.value)
 
 
@@ -198,7 +205,7 @@ def mm(X, blob, N: int, qtype: str = "u4b8", workspace=None, out=None, group_siz
     if out is None:
         out = torch.empty((M, N), dtype=X.dtype, device=X.device)
     if workspace is None and M > 0:
-        nbytes = workspace_bytes(M, N, K, group_size)
+        nbytes = workspace_bytes(M, N, K, group_size, qtype)
         workspace = alloc_workspace(nbytes, X.device) if nbytes > 0 else None   # decode sizes need none
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_n = workspace.numel() if workspace is not None else 0

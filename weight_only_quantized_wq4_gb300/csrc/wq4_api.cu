@@ -15,6 +15,7 @@
 // tiles' (tile, group) units are divided evenly over the CTAs and K-split tiles are summed in a
 // fixed order (deterministic).
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -130,7 +131,7 @@ bool blob_trusted(const void* wp, const BlobKey& k) {
 
 int check_types(int group_size, int dtype, int qtype) {
     if (dtype != WQ4_BF16 && dtype != WQ4_FP16) return WQ4_ERR_INVALID;
-    if (qtype != WQ4_U4B8 && qtype != WQ4_U4_ZP) return WQ4_ERR_INVALID;
+    if (qtype != WQ4_U4B8 && qtype != WQ4_U4_ZP && qtype != WQ4_U4_FZP) return WQ4_ERR_INVALID;
     if (group_size <= 0) return WQ4_ERR_INVALID;
     return WQ4_OK;
 }
@@ -357,7 +358,8 @@ int encode_x_map(CUtensorMap* map, const void* X, int M, int K, int dtype, int n
 }
 
 cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int grid, cudaStream_t st) {
-    const bool bf16 = dtype == WQ4_BF16, zp = qtype == WQ4_U4_ZP, a_tmem = !g_opt.a_in_smem;
+    const bool bf16 = dtype == WQ4_BF16, a_tmem = !g_opt.a_in_smem;
+    const int zp = qtype;                                       // record layout of the format
     const bool pdl = g_opt.pdl == 0;
     switch (nt) {
         case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
@@ -366,6 +368,42 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
         case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
         default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
     }
+}
+
+// Float-zero mode: xsum[g][m] = the sum of X[m][128 g .. 128 g + 127] in fp32, 0 for rows m >= M
+// up to the padded row length ld. One warp per (g, m): each lane adds its 4 consecutive elements
+// in order, then a butterfly over the warp; lane 0's result is stored (the same order every run).
+template <bool BF16>
+__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, float* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const long long wpb = blockDim.x / 32;
+    const long long total = static_cast<long long>(K / kTileK) * ld;
+    for (long long w = blockIdx.x * wpb + threadIdx.x / 32; w < total; w += gridDim.x * wpb) {
+        const int g = static_cast<int>(w / ld), m = static_cast<int>(w % ld);
+        float v = 0.f;
+        if (m < M) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(X + static_cast<size_t>(m) * K + kTileK * g + 4 * lane);
+            const uint32_t e[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if constexpr (BF16) {
+                    v += __uint_as_float(e[i] << 16);
+                } else {
+                    v += __half2float(__ushort_as_half(static_cast<unsigned short>(e[i])));
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) out[static_cast<size_t>(g) * ld + m] = v;
+    }
+}
+
+// Bytes of the float-zero activation-sum table for one problem at token tile nt (0 otherwise).
+size_t xsum_table_bytes(int qtype, const Shape& s, int nt) {
+    if (qtype != WQ4_U4_FZP || s.M <= 0) return 0;
+    const size_t ld = static_cast<size_t>((s.M + nt - 1) / nt) * nt;
+    return static_cast<size_t>(s.K / kTileK) * ld * 4;
 }
 
 // Plans and launches the GEMM kernel for P problems. With fixed_scratch the workspace is the
@@ -378,17 +416,23 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc) return rc;
+    if (qtype == WQ4_U4_FZP && MAXP > 1) return WQ4_ERR_UNSUPPORTED;   // float zeros: single problems
+    // float zeros: the activation-sum table follows the plan's part of the workspace
+    const size_t xsum_bytes = xsum_table_bytes(qtype, shapes[0], pick_token_tile(shapes, P));
+    if (fixed_scratch && xsum_bytes + 256 > workspace_bytes) return WQ4_ERR_WORKSPACE;
     Plan pl;
-    rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes : SIZE_MAX, &pl);
+    rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes - xsum_bytes - 256 : SIZE_MAX, &pl);
     if (rc) return rc;
     if (pl.total_tiles == 0) return WQ4_OK;
-    if (pl.workspace() > 0 && (workspace == nullptr || workspace_bytes < pl.workspace())) {
+    const size_t xsum_off = xsum_bytes ? (pl.workspace() + 255) / 256 * 256 : 0;
+    const size_t need = xsum_bytes ? xsum_off + xsum_bytes : pl.workspace();
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) {
         if (trace_on())
-            std::fprintf(stderr, "[wq4] the plan needs %zu bytes of workspace, %zu given\n", pl.workspace(),
+            std::fprintf(stderr, "[wq4] the plan needs %zu bytes of workspace, %zu given\n", need,
                          workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
         return WQ4_ERR_WORKSPACE;
     }
-    if (pl.workspace() > 0 && !aligned16(workspace)) return WQ4_ERR_ALIGN;
+    if (need > 0 && !aligned16(workspace)) return WQ4_ERR_ALIGN;
 
     GemmParams<MAXP> params;
     GemmParams<MAXP>* prm = &params;
@@ -442,6 +486,21 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     // the fixed array keeps the previous call's contents: the arrival counters must start at zero
     if (fixed_scratch && pl.counters_bytes && cudaMemsetAsync(workspace, 0, pl.counters_bytes, st) != cudaSuccess)
         return WQ4_ERR_CUDA;
+    if (xsum_bytes) {                                           // the pre-pass, in stream order before the GEMM
+        float* xs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + xsum_off);
+        const int ld = pl.m_tiles[0] * pl.nt;
+        prm->xsum = xs;
+        prm->xsum_ld = ld;
+        const long long warps = static_cast<long long>(shapes[0].K / kTileK) * ld;
+        const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 65535));
+        const uint16_t* x16 = static_cast<const uint16_t*>(X[0]);
+        if (dtype == WQ4_BF16) {
+            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, xs);
+        } else {
+            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, xs);
+        }
+        if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
+    }
     if (trace_on()) {
         std::fprintf(stderr,
                      "[wq4] problems=%d token_tile=%d grid=%d cluster=%d tiles=%d dp_tiles=%d sk_units=%d a_src=%s "
@@ -500,18 +559,18 @@ const char* wq4_status_string(int status) {
 
 size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype) {
     if (check_types(group_size, WQ4_BF16, qtype) || check_nk(N, K) || check_group(group_size, K)) return 0;
-    return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype == WQ4_U4_ZP);
+    return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype);
 }
 
-int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros, int N, int K, int group_size,
+int wq4_prepack(const uint32_t* Wq, const void* scales, const void* zeros, int N, int K, int group_size,
                 int dtype, int qtype, void* Wp_out, wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if ((rc = check_nk(N, K))) return rc;
     if ((rc = check_group(group_size, K))) return rc;
     if (!Wq || !Wp_out) return WQ4_ERR_INVALID;
-    if (!scales && qtype == WQ4_U4_ZP) return WQ4_ERR_INVALID;    // zero points need scales
-    if ((qtype == WQ4_U4_ZP) != (zeros != nullptr)) return WQ4_ERR_INVALID;
+    if (!scales && qtype != WQ4_U4B8) return WQ4_ERR_INVALID;    // zero points need scales
+    if ((qtype != WQ4_U4B8) != (zeros != nullptr)) return WQ4_ERR_INVALID;
     if (!aligned16(Wq) || (scales && !aligned16(scales)) || !aligned16(Wp_out) || (zeros && !aligned16(zeros)))
         return WQ4_ERR_ALIGN;
     const cudaError_t e = launch_prepack(Wq, scales, zeros, N, K, group_size, dtype, qtype, Wp_out, stream);
@@ -521,13 +580,13 @@ int wq4_prepack(const uint32_t* Wq, const void* scales, const uint32_t* zeros, i
 }
 
 int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int qtype, uint32_t* Wq_out,
-                  void* scales_out, uint32_t* zeros_out, wq4_stream_t stream) {
+                  void* scales_out, void* zeros_out, wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if ((rc = check_nk(N, K))) return rc;
     if ((rc = check_group(group_size, K))) return rc;
     if (!Wp || !Wq_out) return WQ4_ERR_INVALID;
-    if ((qtype == WQ4_U4_ZP) != (zeros_out != nullptr)) return WQ4_ERR_INVALID;
+    if ((qtype != WQ4_U4B8) != (zeros_out != nullptr)) return WQ4_ERR_INVALID;
     if (!aligned16(Wp) || !aligned16(Wq_out) || (scales_out && !aligned16(scales_out)) ||
         (zeros_out && !aligned16(zeros_out)))
         return WQ4_ERR_ALIGN;
@@ -551,6 +610,20 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
     Plan pl;
     if ((rc = make_plan(shapes, P, dev->sm_count, SIZE_MAX, &pl))) return rc;
     *bytes = pl.workspace();
+    return WQ4_OK;
+}
+
+int wq4_workspace_bytes_ex(int M, int N, int K, int group_size, int qtype, size_t* bytes) {
+    int rc = check_types(group_size, WQ4_BF16, qtype);
+    if (rc) return rc;
+    if ((rc = wq4_workspace_bytes(M, N, K, group_size, bytes))) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    if (M > 0 && !uses_decode_kernel(M, N, K)) {
+        const Shape sh{M, N, K};
+        const size_t xs = xsum_table_bytes(qtype, sh, pick_token_tile(&sh, 1));
+        if (xs) *bytes = (*bytes + 255) / 256 * 256 + xs;
+    }
     return WQ4_OK;
 }
 
@@ -636,7 +709,7 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if (P <= 0 || !M || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
-    if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
+    if (P > kMaxGroupedProblems || qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;
     Shape shapes[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
@@ -688,6 +761,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
                             int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
+    if (qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;        // float zeros: single problems
     if (P <= 0 || !M_dev || !M_cap || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(M_dev) & 3) return WQ4_ERR_ALIGN;

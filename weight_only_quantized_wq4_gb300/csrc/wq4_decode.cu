@@ -77,7 +77,7 @@ struct DecCfg {
     static constexpr int kRedBytes = kDecWarps * NB * 32 * 16;              // per-warp partials
 };
 
-__host__ __device__ constexpr int dec_stage_bytes(bool zp) { return kDecStageGroups * block_bytes(zp); }
+__host__ __device__ constexpr int dec_stage_bytes(int qt) { return kDecStageGroups * block_bytes(qt); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
     asm volatile(
@@ -158,11 +158,11 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
-template <int NB, bool BF16, bool ZP>
+template <int NB, bool BF16, int QT>
 __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
     using C = DecCfg<NB>;
-    constexpr int kBB = block_bytes(ZP);
-    constexpr int kStage = dec_stage_bytes(ZP);
+    constexpr int kBB = block_bytes(QT);
+    constexpr int kStage = dec_stage_bytes(QT);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -321,10 +321,16 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 const uint8_t* const up = sm + (ua - sbase);
                 const uint32_t sw = *reinterpret_cast<const uint32_t*>(up + kBlockScaleOff + 4 * g);
                 uint32_t sub_lo, sub_hi;                                // base + z of rows g, g + 8 (packed pair)
-                if constexpr (ZP) {
+                float zf_lo = 0.f, zf_hi = 0.f;                         // float zeros of rows g, g + 8
+                if constexpr (QT == kQtU4Zp) {
                     const uint32_t zb = up[kBlockZeroOff + g];
                     sub_lo = ((BF16 ? 0x4300u : 0x6400u) | (zb & 0xFu)) * 0x10001u;
                     sub_hi = ((BF16 ? 0x4300u : 0x6400u) | (zb >> 4)) * 0x10001u;
+                } else if constexpr (QT == kQtU4FZp) {
+                    sub_lo = sub_hi = BF16 ? 0x43004300u : 0x64006400u;   // the code itself
+                    const uint32_t zw = *reinterpret_cast<const uint32_t*>(up + kBlockZeroOff + 4 * g);
+                    zf_lo = dec_to_float<BF16>(zw & 0xFFFFu);
+                    zf_hi = dec_to_float<BF16>(zw >> 16);
                 } else {
                     sub_lo = sub_hi = BF16 ? 0x43084308u : 0x64086408u;
                 }
@@ -334,6 +340,11 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 // two independent MMA chains, one per 64-element half of the group (half the
                 // dependent latency of one chain over the group), added at the fold
                 float pr[2][NB][4];
+                // float zeros: the group's activation sum per token, from an MMA with an all-ones A
+                // (the tensor pipe has room; the integer pipe does not)
+                float ps[NB][4];
+                constexpr uint32_t kOnes = BF16 ? 0x3F803F80u : 0x3C003C00u;
+                const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     uint32_t w[4];                                      // (2q, g) (2q, g+8) (2q+1, g) (2q+1, g+8)
@@ -361,6 +372,14 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                                 mma16816<BF16>(pr[q][nb], a0, xb.x, xb.y);
                             }
                             mma16816<BF16>(pr[q][nb], a1, xb.z, xb.w);
+                            if constexpr (QT == kQtU4FZp) {
+                                if (j == 0) {
+                                    mma16816_z<BF16>(ps[nb], ones, xb.x, xb.y);
+                                } else {
+                                    mma16816<BF16>(ps[nb], ones, xb.x, xb.y);
+                                }
+                                mma16816<BF16>(ps[nb], ones, xb.z, xb.w);
+                            }
                         }
                     }
                 }
@@ -373,6 +392,12 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                     acc[nb][1] = fmaf(s_lo, pr[0][nb][1] + pr[1][nb][1], acc[nb][1]);
                     acc[nb][2] = fmaf(s_hi, pr[0][nb][2] + pr[1][nb][2], acc[nb][2]);
                     acc[nb][3] = fmaf(s_hi, pr[0][nb][3] + pr[1][nb][3], acc[nb][3]);
+                    if constexpr (QT == kQtU4FZp) {
+                        acc[nb][0] = fmaf(zf_lo, ps[nb][0], acc[nb][0]);
+                        acc[nb][1] = fmaf(zf_lo, ps[nb][1], acc[nb][1]);
+                        acc[nb][2] = fmaf(zf_hi, ps[nb][2], acc[nb][2]);
+                        acc[nb][3] = fmaf(zf_hi, ps[nb][3], acc[nb][3]);
+                    }
                 }
             }
             __syncwarp();
@@ -451,7 +476,7 @@ static int dec_x_region(int nb, int K) {
     return ((x > red ? x : red) + 127) & ~127;
 }
 
-static int decode_smem_bytes(int nb, int K, int depth, bool zp) {
+static int decode_smem_bytes(int nb, int K, int depth, int zp) {
     return 1024 + dec_x_region(nb, K) + depth * dec_stage_bytes(zp) + 8 * (2 * kDecMaxDepth + kDecMaxPieces + 1) + 16;
 }
 
@@ -461,7 +486,7 @@ static int decode_smem_bytes(int nb, int K, int depth, bool zp) {
 // round trip) where the full size gives it two (measured, 8 tokens, N = 14336, K = 4096, constant
 // weights: 6 blocks per CTA, 10.5 us with two CTAs per SM and one slot per block, 8.9 us with one
 // CTA per SM and two slots per block).
-static int decode_depth(int nb, int K, bool zp, int items_max, int nbc, int forced) {
+static int decode_depth(int nb, int K, int zp, int items_max, int nbc, int forced) {
     const int d_min = nbc > 2 ? nbc : 2;
     int d = forced > 0 ? forced : kDecMaxDepth;
     if (d > items_max) d = items_max;
@@ -482,13 +507,13 @@ bool decode_fits(int M, int K) {
     if (M < 1 || M > 32) return false;
     const int n_st = (K / kTileK + kDecStageGroups - 1) / kDecStageGroups;
     if (n_st > kDecMaxPieces) return false;
-    return decode_smem_bytes(dec_nb(M), K, 2, true) <= kDecMaxSmem;
+    return decode_smem_bytes(dec_nb(M), K, 2, kQtU4FZp) <= kDecMaxSmem;   // the largest records
 }
 
-template <int NB, bool BF16, bool ZP>
+template <int NB, bool BF16, int QT>
 static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStream_t st) {
-    auto kern = wq4_decode_kernel<NB, BF16, ZP>;
-    const int smem = decode_smem_bytes(NB, p.K, p.depth, ZP);
+    auto kern = wq4_decode_kernel<NB, BF16, QT>;
+    const int smem = decode_smem_bytes(NB, p.K, p.depth, QT);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -507,9 +532,12 @@ static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStre
 }
 
 template <int NB>
-static cudaError_t pick_decode(const DecodeParams& p, bool bf16, bool zp, int grid, bool pdl, cudaStream_t st) {
-    if (bf16) return zp ? go_decode<NB, true, true>(p, grid, pdl, st) : go_decode<NB, true, false>(p, grid, pdl, st);
-    return zp ? go_decode<NB, false, true>(p, grid, pdl, st) : go_decode<NB, false, false>(p, grid, pdl, st);
+static cudaError_t pick_decode(const DecodeParams& p, bool bf16, int qt, int grid, bool pdl, cudaStream_t st) {
+    switch (qt) {
+        case kQtU4B8: return bf16 ? go_decode<NB, true, kQtU4B8>(p, grid, pdl, st) : go_decode<NB, false, kQtU4B8>(p, grid, pdl, st);
+        case kQtU4Zp: return bf16 ? go_decode<NB, true, kQtU4Zp>(p, grid, pdl, st) : go_decode<NB, false, kQtU4Zp>(p, grid, pdl, st);
+        default: return bf16 ? go_decode<NB, true, kQtU4FZp>(p, grid, pdl, st) : go_decode<NB, false, kQtU4FZp>(p, grid, pdl, st);
+    }
 }
 
 // Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
@@ -521,7 +549,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
     const Enc enc = reinterpret_cast<Enc>(L.encode_fn);
     const int nb = dec_nb(M);
-    const bool zp = qtype == 1;
+    const int zp = qtype;                                       // record layout of the format
     DecodeParams p;
     std::memset(static_cast<void*>(&p), 0, sizeof(p));
     {

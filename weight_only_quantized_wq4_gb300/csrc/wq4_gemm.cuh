@@ -39,7 +39,7 @@
 
 namespace wq4 {
 
-template <int NT, bool ZP, bool ATMEM>
+template <int NT, int QT, bool ATMEM>
 struct GemmCfg {
     static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 160 || NT == 192, "token tile");
     // Four warpgroups: WG0 = the two TMA producer warps (0, 2) and the two MMA warps (1, 3);
@@ -62,7 +62,7 @@ struct GemmCfg {
     static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
     // epilogue: C values loaded together per thread (16 at NT = 192 spill the bf16 fold warps)
     static constexpr int kEpiBatch = NT >= 192 ? 8 : 16;
-    static constexpr int kRec = tile_record_bytes(ZP);
+    static constexpr int kRec = tile_record_bytes(QT);
     static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
     // Two rings: activation tiles (two panels per group; consumed by the MMA, released by its
     // commit) and weight records (codes + scales + zeros; released once the dequant warps and
@@ -298,10 +298,10 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a, uint32_t b0,
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
 }
 
-template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
-__global__ void __launch_bounds__(GemmCfg<NT, ZP, ATMEM>::kThreads, 1)
+template <int NT, bool BF16, int QT, int MAXP, bool ATMEM>
+__global__ void __launch_bounds__(GemmCfg<NT, QT, ATMEM>::kThreads, 1)
 wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
-    using C = GemmCfg<NT, ZP, ATMEM>;
+    using C = GemmCfg<NT, QT, ATMEM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -510,18 +510,20 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
                 const uint32_t rec = wrec_of(i);
                 uint32_t sub;
-                if constexpr (ZP) {
+                if constexpr (QT == kQtU4Zp) {
                     uint32_t zb;
-                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + rec_zero_off(true, r)));
+                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + rec_zero_off(QT, r)));
                     const uint32_t z = (zb >> (((r >> 3) & 1) * 4)) & 0xFu;
                     sub = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
+                } else if constexpr (QT == kQtU4FZp) {
+                    sub = BF16 ? 0x43004300u : 0x64006400u;   // the code itself; its zero is added at the fold
                 } else {
                     sub = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
                 }
 #pragma unroll
                 for (int jj = 0; jj < C::kChunks; ++jj) {
                     const int j = part * C::kChunks + jj;
-                    const uint4 v = lds128(rec + rec_code_off(ZP, r, j));
+                    const uint4 v = lds128(rec + rec_code_off(QT, r, j));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
                     uint32_t out[16];
 #pragma unroll
@@ -585,8 +587,24 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 tc_fence_after();
                 const uint32_t rec = wrec_of(i);
                 uint32_t sbits;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(ZP, r)));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(QT, r)));
                 const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
+                // float zeros: acc += zf * (sum of the group's activations per token), the sums read
+                // from the table a pre-pass wrote (xsum[g][m], this thread's columns contiguous)
+                float zf = 0.f;
+                const float* srow = nullptr;
+                if constexpr (QT == kQtU4FZp) {
+                    uint32_t zbits;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(zbits) : "r"(rec + rec_fzero_off(QT, r)));
+                    zf = scale_to_float<BF16>(static_cast<uint16_t>(zbits));
+                    srow = prm.xsum + static_cast<size_t>(g) * prm.xsum_ld + seg.mt * NT + col0;
+                    // the next group's sums into L1 now (one lane: every lane reads the same row)
+                    if (lane == 0 && g + 1 < seg.g1) {
+#pragma unroll
+                        for (int off = 0; off < C::kNC * 4; off += 128)
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(srow + prm.xsum_ld) + off));
+                    }
+                }
                 if (g == seg.g0) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
@@ -604,8 +622,18 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         if (q < nbc) tmem_ld16(t_lane + b * NT + col0 + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < kBatchCols; j += 2)
-                        if (j < nbc) fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                    for (int j = 0; j < kBatchCols; j += 4) {
+                        // (columns come in multiples of 16: j < nbc covers j + 3 too)
+                        if (j < nbc) {
+                            fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                            fma2(acc[c + j + 2], acc[c + j + 3], sc, v[j + 2], v[j + 3]);
+                            if constexpr (QT == kQtU4FZp) {
+                                const float4 sv = __ldg(reinterpret_cast<const float4*>(srow + c + j));
+                                fma2(acc[c + j], acc[c + j + 1], zf, __float_as_uint(sv.x), __float_as_uint(sv.y));
+                                fma2(acc[c + j + 2], acc[c + j + 3], zf, __float_as_uint(sv.z), __float_as_uint(sv.w));
+                            }
+                        }
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -761,10 +789,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 }
 
 // Host-side launcher for one instantiation (cluster = S CTAs per cluster in cluster mode, else 1).
-template <int NT, bool BF16, bool ZP, int MAXP, bool ATMEM>
+template <int NT, bool BF16, int QT, int MAXP, bool ATMEM>
 cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, bool pdl, cudaStream_t stream) {
-    using C = GemmCfg<NT, ZP, ATMEM>;
-    auto kern = wq4_gemm_kernel<NT, BF16, ZP, MAXP, ATMEM>;
+    using C = GemmCfg<NT, QT, ATMEM>;
+    auto kern = wq4_gemm_kernel<NT, BF16, QT, MAXP, ATMEM>;
     if constexpr (C::kRegSplit) {
         // The register split assumes 128 registers per thread at launch; a build that launched
         // with fewer would leave the fold warps' setmaxnreg.inc waiting forever. Refuse it.

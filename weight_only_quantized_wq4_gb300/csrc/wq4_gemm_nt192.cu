@@ -4,27 +4,32 @@
 
 namespace wq4 {
 
-template <bool GROUPED, bool BF16, bool ZP, bool ATMEM>
+template <bool GROUPED, bool BF16, int QT, bool ATMEM>
 static cudaError_t go(const void* p, int grid, bool pdl, cudaStream_t st) {
     constexpr int MAXP = GROUPED ? kMaxGroupedProblems : 1;
-    return launch_gemm<192, BF16, ZP, MAXP, ATMEM>(*static_cast<const GemmParams<MAXP>*>(p), grid, pdl, st);
+    return launch_gemm<192, BF16, QT, MAXP, ATMEM>(*static_cast<const GemmParams<MAXP>*>(p), grid, pdl, st);
 }
 
-template <bool GROUPED, bool BF16, bool ZP>
+template <bool GROUPED, bool BF16, int QT>
 static cudaError_t pick_a(const void* p, bool a_tmem, int grid, bool pdl, cudaStream_t st) {
-    return a_tmem ? go<GROUPED, BF16, ZP, true>(p, grid, pdl, st) : go<GROUPED, BF16, ZP, false>(p, grid, pdl, st);
+    return a_tmem ? go<GROUPED, BF16, QT, true>(p, grid, pdl, st) : go<GROUPED, BF16, QT, false>(p, grid, pdl, st);
 }
 
-template <bool GROUPED>
-static cudaError_t pick_types(const void* p, bool bf16, bool zp, bool a_tmem, int grid, bool pdl, cudaStream_t st) {
-    if (bf16) return zp ? pick_a<GROUPED, true, true>(p, a_tmem, grid, pdl, st) : pick_a<GROUPED, true, false>(p, a_tmem, grid, pdl, st);
-    return zp ? pick_a<GROUPED, false, true>(p, a_tmem, grid, pdl, st) : pick_a<GROUPED, false, false>(p, a_tmem, grid, pdl, st);
+template <bool GROUPED, bool BF16>
+static cudaError_t pick_q(const void* p, int qt, bool a_tmem, int grid, bool pdl, cudaStream_t st) {
+    switch (qt) {
+        case kQtU4B8: return pick_a<GROUPED, BF16, kQtU4B8>(p, a_tmem, grid, pdl, st);
+        case kQtU4Zp: return pick_a<GROUPED, BF16, kQtU4Zp>(p, a_tmem, grid, pdl, st);
+        default:   // float zeros: single-problem calls only (the activation sums are per call)
+            if constexpr (GROUPED) return cudaErrorInvalidValue;
+            else return pick_a<GROUPED, BF16, kQtU4FZp>(p, a_tmem, grid, pdl, st);
+    }
 }
 
-cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                              bool pdl, cudaStream_t st) {
-    return grouped ? pick_types<true>(params, bf16, zp, a_tmem, grid, pdl, st)
-                   : pick_types<false>(params, bf16, zp, a_tmem, grid, pdl, st);
+    if (grouped) return bf16 ? pick_q<true, true>(params, qt, a_tmem, grid, pdl, st) : pick_q<true, false>(params, qt, a_tmem, grid, pdl, st);
+    return bf16 ? pick_q<false, true>(params, qt, a_tmem, grid, pdl, st) : pick_q<false, false>(params, qt, a_tmem, grid, pdl, st);
 }
 
 }  // namespace wq4

@@ -15,15 +15,15 @@ struct EpilogueArgs {
 };
 
 // `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
-cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                               bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                               bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, bool zp, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
                               bool pdl, cudaStream_t st);
 
 // Decode-sized M (<= 32 tokens): warp-level MMA kernel, no workspace.
@@ -44,9 +44,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
                           int group_size, int dtype, int qtype, const EpilogueArgs* epi, int* grid_out,
                           int* depth_out, cudaStream_t st);
 
-cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
+cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const void* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st);
 cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, uint32_t* wq, void* scales,
-                             uint32_t* zeros, cudaStream_t st);
+                             void* zeros, cudaStream_t st);
 
 }  // namespace wq4

@@ -17,28 +17,38 @@ constexpr uint32_t kBlobVersion = 2;
 // the call's arguments.
 enum : uint32_t { kStatusTimeout = 1u, kStatusBadBlob = 2u };
 
+// Weight formats (the blob header's qtype code): uint4b8 (value = (q - 8) s), uint4 with a 4-bit
+// zero point per (group, row) (value = (q - z) s), uint4 with a float zero per (group, row), added
+// after the scale (value = q s + zf: the scale-with-zero conversion of "machete_mainloop.cuh",
+// transform_A_kblock).
+enum : int { kQtU4B8 = 0, kQtU4Zp = 1, kQtU4FZp = 2 };
+
 // A (128-row, 128-K) record of the prepacked blob is eight blocks of 16 weight rows. Block b
 // holds, for its rows rr = 0..15: 1024 B of codes (16-byte chunk 16 j + rr = the row's K elements
-// 32 j + [0, 32)), 32 B of scales (row rr at byte 4 (rr % 8) + 2 (rr / 8)) and, in zero-point mode,
-// 8 B of zero points (row rr in byte rr % 8, high nibble for rr >= 8), padded to 16 B. A block is
-// one contiguous run, so a kernel that owns a few 16-row blocks stages exactly those with one
-// tensor copy per run of groups, and a kernel that owns whole tiles copies the record at once.
+// 32 j + [0, 32)), 32 B of scales (row rr at byte 4 (rr % 8) + 2 (rr / 8)), then in zero-point mode
+// 8 B of zero points (row rr in byte rr % 8, high nibble for rr >= 8) padded to 16 B, in float-zero
+// mode 32 B of float zeros placed like the scales. A block is one contiguous run, so a kernel that
+// owns a few 16-row blocks stages exactly those with one tensor copy per run of groups, and a
+// kernel that owns whole tiles copies the record at once.
 constexpr int kBlockRows = 16;
 constexpr int kBlockCodes = 1024;
 constexpr int kBlockScaleOff = 1024;
 constexpr int kBlockZeroOff = 1056;
-__host__ __device__ constexpr int block_bytes(bool zp) { return zp ? 1072 : 1056; }
-__host__ __device__ constexpr int tile_record_bytes(bool zp) { return 8 * block_bytes(zp); }
-// Byte offsets, inside a record, of row r's (0..127) 16-byte code chunk j, its scale and the byte
-// holding its zero point (nibble (r / 8) & 1).
-__host__ __device__ constexpr int rec_code_off(bool zp, int r, int j) {
-    return (r >> 4) * block_bytes(zp) + (16 * j + (r & 15)) * 16;
+__host__ __device__ constexpr int block_bytes(int qt) { return qt == kQtU4Zp ? 1072 : qt == kQtU4FZp ? 1088 : 1056; }
+__host__ __device__ constexpr int tile_record_bytes(int qt) { return 8 * block_bytes(qt); }
+// Byte offsets, inside a record, of row r's (0..127) 16-byte code chunk j, its scale, the byte
+// holding its zero point (nibble (r / 8) & 1) and its float zero.
+__host__ __device__ constexpr int rec_code_off(int qt, int r, int j) {
+    return (r >> 4) * block_bytes(qt) + (16 * j + (r & 15)) * 16;
 }
-__host__ __device__ constexpr int rec_scale_off(bool zp, int r) {
-    return (r >> 4) * block_bytes(zp) + kBlockScaleOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
+__host__ __device__ constexpr int rec_scale_off(int qt, int r) {
+    return (r >> 4) * block_bytes(qt) + kBlockScaleOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
 }
-__host__ __device__ constexpr int rec_zero_off(bool zp, int r) {
-    return (r >> 4) * block_bytes(zp) + kBlockZeroOff + (r & 7);
+__host__ __device__ constexpr int rec_zero_off(int qt, int r) {
+    return (r >> 4) * block_bytes(qt) + kBlockZeroOff + (r & 7);
+}
+__host__ __device__ constexpr int rec_fzero_off(int qt, int r) {
+    return (r >> 4) * block_bytes(qt) + kBlockZeroOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
 }
 
 struct ProblemDesc {
@@ -108,6 +118,8 @@ struct GemmParams {
     int hdr_trusted;         // 1: every blob was prepacked here for these arguments (records may be read
                              // while the headers are being checked); 0: check before the first read
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
+    const float* xsum;       // float-zero mode: xsum[g][m] = sum of X[m][128 g .. 128 g + 127] (fp32),
+    int xsum_ld;             // rows of xsum_ld >= m_tiles * token tile floats (zero past M)
 };
 
 }  // namespace wq4

@@ -14,7 +14,7 @@
 //     the record lies in: with a group size G that is a multiple of 128, record g carries group
 //     128 g / G; without scales every slot holds 1.0);
 //   * (zero-point mode) 8 B of zero points, row rr in byte rr % 8 (high nibble for rr >= 8), then
-//     zero padding to 1072 B.
+//     zero padding to 1072 B; (float-zero mode) 32 B of float zeros placed like the scales (1088 B).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,7 +38,7 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t in) {
 }
 
 // Byte offset (from the first record) of the code word holding elements [8 kw, 8 kw + 8) of row n.
-__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, bool zp) {
+__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, int zp) {
     const int g = kw >> 4, j = (kw >> 2) & 3, w = kw & 3;
     const int nt = n >> 7, r = n & 127;
     return (static_cast<size_t>(nt) * k_groups + g) * tile_record_bytes(zp) +
@@ -46,7 +46,7 @@ __device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, 
 }
 
 __global__ void prepack_codes_kernel(const uint32_t* __restrict__ wq, uint8_t* __restrict__ recs, int N,
-                                     int K, bool zp) {
+                                     int K, int zp) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -57,7 +57,7 @@ __global__ void prepack_codes_kernel(const uint32_t* __restrict__ wq, uint8_t* _
 }
 
 __global__ void unprepack_codes_kernel(const uint8_t* __restrict__ recs, uint32_t* __restrict__ wq, int N,
-                                       int K, bool zp) {
+                                       int K, int zp) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -67,17 +67,20 @@ __global__ void unprepack_codes_kernel(const uint8_t* __restrict__ recs, uint32_
     }
 }
 
-// Scales (one thread per (group, row)), zero points and padding (one thread per (group, 16-row
-// block): the eight zero-point bytes of a block combine two of the API's words), and the header.
-__global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const uint32_t* __restrict__ zeros,
+// Scales and float zeros (one thread per (group, row)), zero points and padding (one thread per
+// (group, 16-row block): the eight zero-point bytes of a block combine two of the API's words),
+// and the header.
+__global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const void* __restrict__ zeros_in,
                                     uint8_t* __restrict__ blob, int N, int K, int G, int dtype, int qtype) {
-    const bool zp = zeros != nullptr;
+    const int zp = qtype;                                            // record layout of this format
+    const uint32_t* zeros = static_cast<const uint32_t*>(zeros_in);  // 4-bit zero points (zero-point mode)
+    const uint16_t* fzeros = static_cast<const uint16_t*>(zeros_in); // float zeros (float-zero mode)
     const int rec = tile_record_bytes(zp);
     const uint16_t one = dtype == 0 ? 0x3F80u : 0x3C00u;     // 1.0 in bf16 / fp16
     const int ng = K / 128, nT = N / 128;
     uint8_t* recs = blob + kBlobHeader;
     const long long n_scale = static_cast<long long>(ng) * N;
-    const long long n_block = zp ? static_cast<long long>(ng) * (N / kBlockRows) : 0;
+    const long long n_block = qtype == kQtU4Zp ? static_cast<long long>(ng) * (N / kBlockRows) : 0;
     const long long total = n_scale + n_block + 64;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -87,6 +90,8 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
             uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
             *reinterpret_cast<uint16_t*>(r + rec_scale_off(zp, n & 127)) =
                 scales ? scales[static_cast<size_t>(src) * N + n] : one;
+            if (qtype == kQtU4FZp)
+                *reinterpret_cast<uint16_t*>(r + rec_fzero_off(zp, n & 127)) = fzeros[static_cast<size_t>(src) * N + n];
         } else if (idx < n_scale + n_block) {
             const long long z = idx - n_scale;
             const int g = static_cast<int>(z / (N / kBlockRows)), blk = static_cast<int>(z % (N / kBlockRows));
@@ -99,7 +104,7 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
                 const uint32_t byte = ((lo >> (4 * p)) & 0xFu) | (((hi >> (4 * p)) & 0xFu) << 4);
                 w[p >> 2] |= byte << (8 * (p & 3));
             }
-            uint8_t* r = recs + (static_cast<size_t>(blk >> 3) * ng + g) * rec + (blk & 7) * block_bytes(true);
+            uint8_t* r = recs + (static_cast<size_t>(blk >> 3) * ng + g) * rec + (blk & 7) * block_bytes(kQtU4Zp);
             uint32_t* zw = reinterpret_cast<uint32_t*>(r + kBlockZeroOff);
             zw[0] = w[0];
             zw[1] = w[1];
@@ -128,12 +133,14 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const u
 
 // Output row j (quantisation group j) is read from its first record, 128-K record j G / 128.
 __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t* __restrict__ scales,
-                                      uint32_t* __restrict__ zeros, int N, int K, int G, bool zp) {
+                                      void* __restrict__ zeros_out, int N, int K, int G, int zp) {
     const int rec = tile_record_bytes(zp);
     const int ng = K / 128, nq = K / G;
     const uint8_t* recs = blob + kBlobHeader;
+    uint32_t* zeros = static_cast<uint32_t*>(zeros_out);
+    uint16_t* fzeros = static_cast<uint16_t*>(zeros_out);
     const long long n_scale = scales ? static_cast<long long>(nq) * N : 0;
-    const long long n_zero = zeros ? static_cast<long long>(nq) * (N / 8) : 0;
+    const long long n_zero = zeros_out ? static_cast<long long>(nq) * (zp == kQtU4FZp ? N : N / 8) : 0;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n_scale + n_zero;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
@@ -141,6 +148,12 @@ __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t
             const int g = (j * G) / 128;
             const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
             scales[idx] = *reinterpret_cast<const uint16_t*>(r + rec_scale_off(zp, n & 127));
+        } else if (zp == kQtU4FZp) {
+            const long long z = idx - n_scale;
+            const int j = static_cast<int>(z / N), n = static_cast<int>(z % N);
+            const int g = (j * G) / 128;
+            const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
+            fzeros[z] = *reinterpret_cast<const uint16_t*>(r + rec_fzero_off(zp, n & 127));
         } else {
             // API word wz: rows 8 wz .. 8 wz + 7, the low (wz even) or high (wz odd) nibbles of a block
             const long long z = idx - n_scale;
@@ -152,7 +165,7 @@ __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rr = (n0 + i) & 127;
-                const uint32_t byte = r[rec_zero_off(true, rr)];
+                const uint32_t byte = r[rec_zero_off(kQtU4Zp, rr)];
                 out |= ((byte >> (4 * ((rr >> 3) & 1))) & 0xFu) << (4 * i);
             }
             zeros[z] = out;
@@ -167,9 +180,9 @@ static int grid_for(long long work, int threads) {
     return static_cast<int>(b);
 }
 
-cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_t* zeros, int N, int K, int G,
+cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const void* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st) {
-    const bool zp = qtype == 1;
+    const int zp = qtype;
     uint8_t* b = static_cast<uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
     prepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, b + kBlobHeader, N, K, zp);
@@ -182,8 +195,8 @@ cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const uint32_
 }
 
 cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, uint32_t* wq, void* scales,
-                             uint32_t* zeros, cudaStream_t st) {
-    const bool zp = qtype == 1;
+                             void* zeros, cudaStream_t st) {
+    const int zp = qtype;
     const uint8_t* b = static_cast<const uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
     unprepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(b + kBlobHeader, wq, N, K, zp);

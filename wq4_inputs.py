@@ -166,6 +166,8 @@ def algorithmic_bytes(M: int, N: int, K: int, qtype: str, group_size: int = GROU
     b = 2 * M * K + N * K // 2 + 2 * ng * N + 2 * M * N
     if qtype == U4_ZP:
         b += ng * N // 2
+    if qtype == U4_FZP:
+        b += 2 * ng * N
     return b
 
 
