@@ -171,21 +171,27 @@ BLOCK_ROWS = 16         # weight rows per block (one warp-level MMA's rows)
 BLOCKS = TILE_N // BLOCK_ROWS
 
 
-def block_bytes(qtype: str) -> int:
-    """Bytes of one 16-row block of a tile record: 1024 B of codes, 32 B of scales and, in
-    zero-point mode, 8 B of zero points (float-zero mode: 32 B of float zeros), padded to a
-    multiple of 16 B."""
-    raw = 1024 + 32 + {"u4b8": 0, "u4_zp": 8, "u4_fzp": 32}[qtype]
+def halves(group_size: int) -> int:
+    """Scale sets per 128-K record: 2 for G = 64 (one per 64-K half), else 1."""
+    return 2 if group_size == 64 else 1
+
+
+def block_bytes(qtype: str, group_size: int = GROUP) -> int:
+    """Bytes of one 16-row block of a tile record: 1024 B of codes, 32 B of scales per scale set
+    and, per set, 8 B of zero points (zero-point mode) or 32 B of float zeros (float-zero mode),
+    padded to a multiple of 16 B."""
+    H = halves(group_size)
+    raw = 1024 + 32 * H + H * {"u4b8": 0, "u4_zp": 8, "u4_fzp": 32}[qtype]
     return (raw + 15) // 16 * 16
 
 
-def tile_bytes(qtype: str) -> int:
+def tile_bytes(qtype: str, group_size: int = GROUP) -> int:
     """Bytes of one (128-row, 128-K) tile record: eight 16-row blocks."""
-    return BLOCKS * block_bytes(qtype)
+    return BLOCKS * block_bytes(qtype, group_size)
 
 
 def prepacked_bytes(N: int, K: int, qtype: str, group_size: int = GROUP) -> int:
-    return HEADER_BYTES + (N // TILE_N) * (K // TILE_K) * tile_bytes(qtype)
+    return HEADER_BYTES + (N // TILE_N) * (K // TILE_K) * tile_bytes(qtype, group_size)
 
 
 # position of element e (0..7) of an 8-element run inside its 32-bit word: even elements take
@@ -199,9 +205,11 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
             group_size: int = GROUP) -> np.ndarray:
     """Blob bytes (uint8) for one weight.
 
-    Group sizes: G a multiple of 128 dividing K (G = K: one scale per row). Record g of the layout
-    below takes the scale (and zero point) of quantisation group 128 g // G, so every 128-K record
-    carries its own copy. ``S_bits`` None (no scales): every scale slot holds 1.0.
+    Group sizes: G a multiple of 128 dividing K (G = K: one scale per row), or G = 64. Record g
+    of the layout below has H scale sets (H = 2 for G = 64, else 1); set h covers the record's K
+    elements 64 h + [0, 128 / H) and takes the scale (and zero point) of quantisation group
+    (128 g + 64 h) // G, so every record carries its own copies. ``S_bits`` None (no scales):
+    every scale slot holds 1.0.
 
     Layout (version 2):
       * header, 256 B of little-endian uint32: magic "WQ4P", version 2, N, K, group size,
@@ -214,22 +222,21 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
           - codes, 1024 B: 16-byte chunk number (16 j + rr) holds row rr and K elements
             128 g + 32 j + [0, 32), j = 0..3.  Word w = 0..3 of the chunk holds the eight elements
             128 g + 32 j + 8 w + e, e = 0..7, element e in nibble NIBBLE_POS[e].
-          - scales, 32 B at offset 1024: the 16-bit scale of row rr at byte 4 (rr % 8) + 2 (rr // 8)
-            (rows rr and rr + 8 share one 32-bit word).
-          - zero points (u4_zp only), 8 B at offset 1056: the zero point of row rr in byte rr % 8,
-            low nibble for rr < 8, high nibble for rr >= 8.
-          - float zeros (u4_fzp only), 32 B at offset 1056, placed like the scales: the 16-bit
-            zero of row rr at byte 1056 + 4 (rr % 8) + 2 (rr // 8).
+          - scales, 32 B per set at offset 1024 + 32 h: the 16-bit scale of row rr at byte
+            4 (rr % 8) + 2 (rr // 8) of the set (rows rr and rr + 8 share one 32-bit word).
+          - zero points (u4_zp only), 8 B per set at offset 1024 + 32 H + 8 h: the zero point of
+            row rr in byte rr % 8, low nibble for rr < 8, high nibble for rr >= 8.
+          - float zeros (u4_fzp only), 32 B per set at offset 1024 + 32 H + 32 h, placed like the
+            scales: the 16-bit zero of row rr at byte 4 (rr % 8) + 2 (rr // 8) of the set.
           - zero padding up to block_bytes.
     """
-    if group_size % TILE_K or K % group_size or N % TILE_N or K % TILE_K:
-        raise ValueError("the blob format needs N, K multiples of 128 and a group size that is a "
+    if (group_size % TILE_K and group_size != 64) or K % group_size or N % TILE_N or K % TILE_K:
+        raise ValueError("the blob format needs N, K multiples of 128 and a group size of 64 or a "
                          "multiple of 128 dividing K")
     nT, nG = N // TILE_N, K // TILE_K
-    # record g (K elements 128 g ... 128 g + 127) lies in quantisation group (128 g) // G
-    src = (np.arange(nG) * TILE_K) // group_size
-    tb, bb = tile_bytes(qtype), block_bytes(qtype)
-    blob = np.zeros(prepacked_bytes(N, K, qtype), dtype=np.uint8)
+    H = halves(group_size)
+    tb, bb = tile_bytes(qtype, group_size), block_bytes(qtype, group_size)
+    blob = np.zeros(prepacked_bytes(N, K, qtype, group_size), dtype=np.uint8)
     hdr = np.zeros(HEADER_BYTES // 4, dtype=np.uint32)
     hdr[:10] = [BLOB_MAGIC, BLOB_VERSION, N, K, group_size, DTYPE_CODE[dtype], QTYPE_CODE[qtype],
                 tb, nT, nG]
@@ -244,24 +251,28 @@ def prepack(Wq, S_bits, N: int, K: int, dtype: str, qtype: str, Z_words=None,
 
     blocks = blob[HEADER_BYTES:].reshape(nT, nG, BLOCKS, bb)
     blocks[:, :, :, :1024] = codes
-    if S_bits is None:                                          # no scales: 1.0 in every slot
-        S_rows = np.full((nG, N), ONE_BITS[dtype], dtype=np.uint16)
-    else:
-        S_rows = np.asarray(S_bits, dtype=np.uint16).reshape(K // group_size, N)[src]
-    S = S_rows.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
-    blocks[:, :, :, 1024:1056] = np.ascontiguousarray(S.transpose(1, 0, 2, 3)).view(np.uint8).reshape(
-        nT, nG, BLOCKS, 32)
-    if qtype == "u4_zp":
-        z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, BLOCKS, BLOCK_ROWS)
-        zb = (z[..., :8] | (z[..., 8:] << 4)).astype(np.uint8)              # [g][nt][b][8]
-        blocks[:, :, :, 1056:1064] = zb.transpose(1, 0, 2, 3)
-    if qtype == "u4_fzp":
-        if S_bits is None:
-            raise ValueError("float zeros need scales")
-        ZF = np.asarray(Z_words, dtype=np.uint16).reshape(K // group_size, N)[src]
-        ZF = ZF.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
-        blocks[:, :, :, 1056:1088] = np.ascontiguousarray(ZF.transpose(1, 0, 2, 3)).view(np.uint8).reshape(
-            nT, nG, BLOCKS, 32)
+    zoff = 1024 + 32 * H                                        # start of the zero area
+    for h in range(H):
+        # set h of record g covers K elements 128 g + 64 h ...: quantisation group (128 g + 64 h) // G
+        src = (np.arange(nG) * TILE_K + 64 * h) // group_size
+        if S_bits is None:                                      # no scales: 1.0 in every slot
+            S_rows = np.full((nG, N), ONE_BITS[dtype], dtype=np.uint16)
+        else:
+            S_rows = np.asarray(S_bits, dtype=np.uint16).reshape(K // group_size, N)[src]
+        S = S_rows.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
+        blocks[:, :, :, 1024 + 32 * h:1056 + 32 * h] = np.ascontiguousarray(S.transpose(1, 0, 2, 3)).view(
+            np.uint8).reshape(nT, nG, BLOCKS, 32)
+        if qtype == "u4_zp":
+            z = unpack_u4(Z_words, N).reshape(K // group_size, N)[src].reshape(nG, nT, BLOCKS, BLOCK_ROWS)
+            zb = (z[..., :8] | (z[..., 8:] << 4)).astype(np.uint8)              # [g][nt][b][8]
+            blocks[:, :, :, zoff + 8 * h:zoff + 8 * h + 8] = zb.transpose(1, 0, 2, 3)
+        if qtype == "u4_fzp":
+            if S_bits is None:
+                raise ValueError("float zeros need scales")
+            ZF = np.asarray(Z_words, dtype=np.uint16).reshape(K // group_size, N)[src]
+            ZF = ZF.reshape(nG, nT, BLOCKS, BLOCK_ROWS)[..., SCALE_SLOT_ROW]     # [g][nt][b][slot]
+            blocks[:, :, :, zoff + 32 * h:zoff + 32 * h + 32] = np.ascontiguousarray(
+                ZF.transpose(1, 0, 2, 3)).view(np.uint8).reshape(nT, nG, BLOCKS, 32)
     return blob
 
 
@@ -274,28 +285,36 @@ def _pack_rows(z: np.ndarray) -> np.ndarray:
 def unprepack(blob: np.ndarray, N: int, K: int, dtype: str, qtype: str, group_size: int = GROUP):
     """Inverse of ``prepack``: (Wq [N][K/8] uint32, S_bits [K/G][N] uint16, Z [K/G][N/8] uint32 for
     u4_zp, [K/G][N] uint16 float zeros for u4_fzp, else None); quantisation group j is read from
-    its first record, 128-K record j G / 128."""
+    the first record and scale set holding it: record j G // 128, set (j G % 128) // 64."""
     nT, nG = N // TILE_N, K // TILE_K
-    first = (np.arange(K // group_size) * group_size) // TILE_K
-    tb, bb = tile_bytes(qtype), block_bytes(qtype)
+    H = halves(group_size)
+    start = np.arange(K // group_size) * group_size
+    first, half = start // TILE_K, (start % TILE_K) // 64
+    tb, bb = tile_bytes(qtype, group_size), block_bytes(qtype, group_size)
     blocks = np.asarray(blob, dtype=np.uint8)[HEADER_BYTES:HEADER_BYTES + nT * nG * tb].reshape(nT, nG, BLOCKS, bb)
     words = np.ascontiguousarray(blocks[..., :1024]).view(np.uint32).reshape(nT, nG, BLOCKS, 4, BLOCK_ROWS, 4)
     words = words.transpose(0, 2, 4, 1, 3, 5)                  # [nt][b][rr][g][j][w]
     q7 = (words[..., None] >> (4 * NIBBLE_POS)) & np.uint32(0xF)  # [..][e]
     q = q7.reshape(N, K).astype(np.uint8)
-    slots = np.ascontiguousarray(blocks[..., 1024:1056]).view(np.uint16).reshape(nT, nG, BLOCKS, BLOCK_ROWS)
-    S = np.empty_like(slots)
-    S[..., SCALE_SLOT_ROW] = slots                              # back to row order
-    S_bits = np.ascontiguousarray(np.ascontiguousarray(S.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
+
+    def rows16(lo):                                             # a 32-byte slot area -> [nG][N] row order
+        slots = np.ascontiguousarray(blocks[..., lo:lo + 32]).view(np.uint16).reshape(nT, nG, BLOCKS, BLOCK_ROWS)
+        out = np.empty_like(slots)
+        out[..., SCALE_SLOT_ROW] = slots
+        return np.ascontiguousarray(out.transpose(1, 0, 2, 3)).reshape(nG, N)
+
+    zoff = 1024 + 32 * H
+    S_sets = np.stack([rows16(1024 + 32 * h) for h in range(H)])            # [H][nG][N]
+    S_bits = np.ascontiguousarray(S_sets[half, first])
     Z = None
     if qtype == "u4_zp":
-        zb = blocks[..., 1056:1064].astype(np.uint32)            # [nt][g][b][8]
-        z = np.concatenate([zb & 0xF, zb >> 4], axis=-1)         # rows 0..7, then 8..15
-        Z = _pack_rows(np.ascontiguousarray(z.transpose(1, 0, 2, 3)).reshape(nG, N)[first]).astype(np.uint32)
+        zsets = []
+        for h in range(H):
+            zb = blocks[..., zoff + 8 * h:zoff + 8 * h + 8].astype(np.uint32)  # [nt][g][b][8]
+            z = np.concatenate([zb & 0xF, zb >> 4], axis=-1)                   # rows 0..7, then 8..15
+            zsets.append(np.ascontiguousarray(z.transpose(1, 0, 2, 3)).reshape(nG, N))
+        Z = _pack_rows(np.stack(zsets)[half, first]).astype(np.uint32)
     if qtype == "u4_fzp":
-        zs = np.ascontiguousarray(blocks[..., 1056:1088]).view(np.uint16).reshape(nT, nG, BLOCKS, BLOCK_ROWS)
-        ZF = np.empty_like(zs)
-        ZF[..., SCALE_SLOT_ROW] = zs
-        Z = np.ascontiguousarray(np.ascontiguousarray(ZF.transpose(1, 0, 2, 3)).reshape(nG, N)[first])
+        Z = np.ascontiguousarray(np.stack([rows16(zoff + 32 * h) for h in range(H)])[half, first])
     Wq = _pack_rows(q)
     return Wq.astype(np.uint32), S_bits, Z

@@ -122,17 +122,18 @@ def test_oracle_equals_exact_brute_force(dtype, qtype, shape):
             assert abs(Yref[m, n] - float(exact[m][n])) <= bound, (m, n, Yref[m, n], float(exact[m][n]))
 
 
-# one scale row per 256 K, one per row (G = K), and no scales at all (direct conversion)
-GMODES = [(256, True), ("K", True), (128, False)]
+# one scale row per 256 K, one per row (G = K), one per 64 K (two per 128-K record), and no
+# scales at all (direct conversion)
+GMODES = [(256, True), ("K", True), (64, True), (128, False)]
 
 
-@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp"])
+@pytest.mark.parametrize("qtype", ["u4b8", "u4_zp", "u4_fzp"])
 @pytest.mark.parametrize("gmode", GMODES)
 @pytest.mark.parametrize("shape", [(1, 8, 256), (2, 8, 512)])
 def test_oracle_group_sizes_equal_exact_brute_force(qtype, gmode, shape):
     M, N, K = shape
     G, scaled = (K if gmode[0] == "K" else gmode[0]), gmode[1]
-    if not scaled and qtype == "u4_zp":
+    if not scaled and qtype != "u4b8":
         pytest.skip("direct conversion has no zero points")
     p = I.make_problem(M, N, K, "bf16", qtype, seed=K + G + M, group_size=G, scaled=scaled)
     assert (p.S_bits is None) == (not scaled) and (scaled is False or p.S_bits.shape == (K // G, N))
@@ -342,17 +343,22 @@ def test_tolerance_check():
 
 # ---------------------------------------------------------------- blob layout
 def _brute_blob(p) -> np.ndarray:
-    """The blob built one element at a time straight from the layout's wording (record g carries
-    the scale and zero point of quantisation group 128 g // G; no scales: 1.0 = 0x3F80 / 0x3C00):
-    record (nt, g) is eight 16-row blocks of 1056 B (uint4b8), 1072 B (zero points) or 1088 B
-    (float zeros); in block b, row rr's K elements 32 j + [0, 32) form 16-byte chunk 16 j + rr,
-    its scale sits at byte 1024 + 4 (rr % 8) + 2 (rr // 8), its zero point in byte 1056 + rr % 8
-    (high nibble for rr >= 8), its float zero at byte 1056 + 4 (rr % 8) + 2 (rr // 8)."""
-    bb = {"u4b8": 1056, "u4_zp": 1072, "u4_fzp": 1088}[p.qtype]
+    """The blob built one element at a time straight from the layout's wording (no scales: 1.0 =
+    0x3F80 / 0x3C00): record (nt, g) is eight 16-row blocks; a block has H scale sets (H = 2 for
+    G = 64, else 1), set h covering the record's K elements from 64 h and carrying the scale (and
+    zero) of quantisation group (128 g + 64 h) // G; block bytes 1024 + 32 H (uint4b8), plus 8 H
+    padded to 16 (zero points) or plus 32 H (float zeros); in block b, row rr's K elements
+    32 j + [0, 32) form 16-byte chunk 16 j + rr, its scale of set h sits at byte
+    1024 + 32 h + 4 (rr % 8) + 2 (rr // 8), its zero point of set h in byte 1024 + 32 H + 8 h + rr % 8
+    (high nibble for rr >= 8), its float zero of set h at byte 1024 + 32 H + 32 h + 4 (rr % 8) + 2 (rr // 8)."""
+    G = p.group_size
+    H = 2 if G == 64 else 1
+    bb = 1024 + 32 * H + {"u4b8": 0, "u4_zp": 8 * H, "u4_fzp": 32 * H}[p.qtype]
+    bb = (bb + 15) // 16 * 16
     tb = 8 * bb
     nG = p.K // 128
-    G = p.group_size
-    blob = np.zeros(O.prepacked_bytes(p.N, p.K, p.qtype), np.uint8)
+    blob = np.zeros(256 + (p.N // 128) * nG * tb, np.uint8)
+    assert blob.size == O.prepacked_bytes(p.N, p.K, p.qtype, G)
     hdr = [O.BLOB_MAGIC, 2, p.N, p.K, G, O.DTYPE_CODE[p.dtype], O.QTYPE_CODE[p.qtype], tb, p.N // 128, nG]
     for i, v in enumerate(hdr):
         blob[4 * i:4 * i + 4] = list(int(v).to_bytes(4, "little"))
@@ -367,17 +373,19 @@ def _brute_blob(p) -> np.ndarray:
             shift = 4 * (pos[e] % 2)
             blob[byte_off] |= int(p.q[n, k]) << shift
     for g in range(nG):
-        for n in range(p.N):
-            nt, b, rr = n // 128, (n % 128) // 16, n % 16
-            blk = 256 + (nt * nG + g) * tb + b * bb
-            sbits = int(p.S_bits[(128 * g) // G, n]) if p.S_bits is not None else (0x3F80 if p.dtype == "bf16" else 0x3C00)
-            so = blk + 1024 + 4 * (rr % 8) + 2 * (rr // 8)
-            blob[so:so + 2] = list(sbits.to_bytes(2, "little"))
-            if p.qtype == "u4_zp":
-                blob[blk + 1056 + rr % 8] |= int(p.z[(128 * g) // G, n]) << (4 * (rr // 8))
-            if p.qtype == "u4_fzp":                         # float zeros placed like the scales
-                zo = blk + 1056 + 4 * (rr % 8) + 2 * (rr // 8)
-                blob[zo:zo + 2] = list(int(p.Z[(128 * g) // G, n]).to_bytes(2, "little"))
+        for h in range(H):
+            src = (128 * g + 64 * h) // G
+            for n in range(p.N):
+                nt, b, rr = n // 128, (n % 128) // 16, n % 16
+                blk = 256 + (nt * nG + g) * tb + b * bb
+                sbits = int(p.S_bits[src, n]) if p.S_bits is not None else (0x3F80 if p.dtype == "bf16" else 0x3C00)
+                so = blk + 1024 + 32 * h + 4 * (rr % 8) + 2 * (rr // 8)
+                blob[so:so + 2] = list(sbits.to_bytes(2, "little"))
+                if p.qtype == "u4_zp":
+                    blob[blk + 1024 + 32 * H + 8 * h + rr % 8] |= int(p.z[src, n]) << (4 * (rr // 8))
+                if p.qtype == "u4_fzp":                     # float zeros placed like the scales
+                    zo = blk + 1024 + 32 * H + 32 * h + 4 * (rr % 8) + 2 * (rr // 8)
+                    blob[zo:zo + 2] = list(int(p.Z[src, n]).to_bytes(2, "little"))
     return blob
 
 
@@ -388,7 +396,9 @@ def test_blob_layout_brute_force(qtype):
 
 
 @pytest.mark.parametrize("qtype,G,scaled,dtype", [("u4_zp", 256, True, "bf16"), ("u4b8", 512, True, "fp16"),
-                                                  ("u4_fzp", 256, True, "fp16"),
+                                                  ("u4_fzp", 256, True, "fp16"), ("u4b8", 64, True, "bf16"),
+                                                  ("u4_zp", 64, True, "fp16"), ("u4_fzp", 64, True, "bf16"),
+                                                  ("u4b8", 64, False, "fp16"),
                                                   ("u4b8", 128, False, "bf16"), ("u4b8", 256, False, "fp16")])
 def test_blob_layout_group_sizes_brute_force(qtype, G, scaled, dtype):
     p = I.make_problem(1, 256, 512, dtype, qtype, seed=G + 1, group_size=G, scaled=scaled)
@@ -404,9 +414,9 @@ def test_blob_layout_group_sizes_brute_force(qtype, G, scaled, dtype):
 
 def test_blob_rejects_unsupported_group_sizes():
     p = I.make_problem(1, 128, 512, "bf16", "u4b8", seed=3)
-    for G in (64, 384):
+    for G in (32, 384, 192):
         with pytest.raises(ValueError):
-            O.prepack(p.Wq, np.zeros((512 // 64, 128), np.uint16), p.N, p.K, p.dtype, p.qtype, group_size=G)
+            O.prepack(p.Wq, np.zeros((512 // 32, 128), np.uint16), p.N, p.K, p.dtype, p.qtype, group_size=G)
 
 
 @pytest.mark.parametrize("qtype", ["u4b8", "u4_zp", "u4_fzp"])
