@@ -31,7 +31,10 @@ def test_prepacked_bytes(clib):
     assert clib.wq4_prepacked_bytes(4096, 4096, 128, 0) == 256 + 32 * 32 * 8448
     assert clib.wq4_prepacked_bytes(14336, 4096, 128, 1) == 256 + 112 * 32 * 8576
     assert clib.wq4_prepacked_bytes(100, 4096, 128, 0) == 0       # N not a multiple of 128
-    assert clib.wq4_prepacked_bytes(128, 4096, 64, 0) == 0        # group size 64 not built
+    assert clib.wq4_prepacked_bytes(128, 4096, 64, 0) == 256 + 32 * 8 * 1088   # G = 64: two scale sets
+    assert clib.wq4_prepacked_bytes(128, 4096, 64, 1) == 256 + 32 * 8 * 1104
+    assert clib.wq4_prepacked_bytes(128, 4096, 64, 2) == 256 + 32 * 8 * 1152
+    assert clib.wq4_prepacked_bytes(128, 4096, 32, 0) == 0        # group size 32 not built
     assert clib.wq4_prepacked_bytes(128, 1024, 384, 0) == 0       # 384 does not divide K
     assert clib.wq4_prepacked_bytes(128, 1024, 256, 0) == 256 + 8 * 8448   # one record per 128 K
     assert clib.wq4_prepacked_bytes(128, 640, 640, 1) == 256 + 5 * 8576    # channel-wise (G = K)
@@ -55,7 +58,7 @@ def test_mm_argument_rules(clib):
     assert _mm(clib, N=100) == wq4.ERR_UNSUPPORTED
     assert _mm(clib, K=200) == wq4.ERR_UNSUPPORTED
     assert _mm(clib, G=0) == wq4.ERR_INVALID                      # group size must be non-zero
-    assert _mm(clib, G=64) == wq4.ERR_UNSUPPORTED
+    assert _mm(clib, G=32) == wq4.ERR_UNSUPPORTED                 # neither 64 nor a multiple of 128
     assert _mm(clib, dt=7) == wq4.ERR_INVALID
     assert _mm(clib, qt=9) == wq4.ERR_INVALID
     assert _mm(clib, X=None) == wq4.ERR_INVALID
@@ -74,7 +77,8 @@ def test_prepack_argument_rules(clib):
     assert pp(A16, None, A16c, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_INVALID   # zero points need scales
     assert pp(A16, A16b, None, 128, 256, 256, 0, 0, A16c, None) != wq4.ERR_UNSUPPORTED  # G = 256 divides K
     assert pp(A16, A16b, None, 128, 256, 384, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED  # G does not divide K
-    assert pp(A16, A16b, None, 128, 256, 64, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED   # G not a multiple of 128
+    assert pp(A16, A16b, None, 128, 256, 32, 0, 0, A16c, None) == wq4.ERR_UNSUPPORTED   # G neither 64 nor a multiple of 128
+    assert pp(A16, A16b, None, 128, 256, 64, 0, 0, A16c, None) != wq4.ERR_UNSUPPORTED   # G = 64
     assert pp(MIS, A16b, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN
     assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
     assert pp(A16, A16b, A16c, 128, 128, 128, 0, 2, A16c, None) != wq4.ERR_INVALID   # float zeros with scales
@@ -87,7 +91,7 @@ def test_mm_ex_argument_rules(clib):
     assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, None, 0.5, None, None, 0, None) == wq4.ERR_INVALID  # beta needs C
     assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, MIS, 0.5, None, None, 0, None) == wq4.ERR_ALIGN
     assert ex(A16, A16b, A16c, 8, 128, 128, 128, 0, 0, 1.0, None, 0.0, MIS, None, 0, None) == wq4.ERR_ALIGN
-    assert ex(A16, A16b, A16c, 8, 128, 128, 64, 0, 0, 1.0, None, 0.0, None, None, 0, None) == wq4.ERR_UNSUPPORTED
+    assert ex(A16, A16b, A16c, 8, 128, 128, 32, 0, 0, 1.0, None, 0.0, None, None, 0, None) == wq4.ERR_UNSUPPORTED
     assert ex(A16, A16b, A16c, 0, 128, 128, 128, 0, 0, 1.0, None, 0.0, None, None, 0, None) == wq4.OK  # M = 0
 
 

@@ -73,7 +73,8 @@ SMALL = [
 GROUP_MODES = [
     (256, 512, "bf16", "u4_zp", 256, True), (384, 640, "fp16", "u4b8", 640, True),
     (256, 384, "bf16", "u4b8", 128, False), (128, 1024, "fp16", "u4b8", 512, False),
-    (256, 1024, "bf16", "u4_fzp", 512, True),
+    (256, 1024, "bf16", "u4_fzp", 512, True), (256, 512, "bf16", "u4b8", 64, True), (384, 640, "fp16", "u4_zp", 64, True),
+    (256, 384, "bf16", "u4_fzp", 64, True), (128, 256, "fp16", "u4b8", 64, False),
 ]
 
 
@@ -97,6 +98,10 @@ GROUP_MM = [
     (64, 256, 768, "bf16", "u4b8", 128, False), (130, 256, 2048, "bf16", "u4b8", 2048, True),
     (8, 512, 1024, "bf16", "u4_zp", 512, True), (5, 256, 640, "fp16", "u4b8", 128, False),
     (6, 256, 1024, "bf16", "u4_fzp", 512, True), (150, 384, 1024, "fp16", "u4_fzp", 1024, True),
+    (8, 4096, 4096, "bf16", "u4b8", 64, True), (5, 2944, 8960, "bf16", "u4_zp", 64, True),
+    (16, 768, 1408, "fp16", "u4_fzp", 64, True), (100, 1024, 2048, "bf16", "u4b8", 64, True),
+    (300, 384, 512, "fp16", "u4_zp", 64, True), (777, 256, 1024, "bf16", "u4_fzp", 64, True),
+    (129, 512, 768, "bf16", "u4b8", 64, False),
 ]
 
 
@@ -446,6 +451,20 @@ def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     Y = lib.mm(X, blob, N, qtype="u4_zp", out=out, alpha=alpha, C=C, beta=beta, bias=bias)
     ref = O.epilogue(O.mm_problem(p), dtype, alpha, C_bits, beta, bias_bits)
     assert_parity(y_as_f64(Y, dtype), ref, "epilogue %s" % ((M, N, K, split_all, in_place),))
+
+
+@pytest.mark.parametrize("token_tile,split_all,cluster,qtype", [(16, 0, 0, "u4b8"), (64, 1, 0, "u4_zp"),
+                                                                (128, 0, 0, "u4b8"), (64, 0, 4, "u4_fzp"),
+                                                                (16, 1, 0, "u4_fzp")])
+def test_mm_group_64_schedules(opts, token_tile, split_all, cluster, qtype):
+    """G = 64 (two scale sets per record, a partial per 64-K half): tiles of 16 and 64 tokens,
+    a forced 128 taken down to 64, K-split and cluster plans."""
+    lib = opts
+    lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
+    lib.set_option(lib.OPT_SPLIT_ALL, split_all)
+    lib.set_option(lib.OPT_CLUSTER, cluster)
+    p = I.make_problem(150, 512, 2048, "bf16", qtype, seed=token_tile + 3 * split_all + cluster, group_size=64)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "G=64 %s" % ((token_tile, split_all, cluster),))
 
 
 # ------------------------------------------------------------------------------ float zeros

@@ -137,9 +137,10 @@ int check_types(int group_size, int dtype, int qtype) {
 }
 
 // Group sizes of this build: multiples of the 128-element K tile that divide K (group_size == K is
-// the channel-wise case); every 128-K record of the blob then carries its group's scale.
+// the channel-wise case), every 128-K record of the blob then carrying its group's scale; and 64,
+// each record then carrying two scale sets (one per 64-K half).
 int check_group(int group_size, int K) {
-    if (group_size % kTileK || K % group_size) return WQ4_ERR_UNSUPPORTED;
+    if ((group_size % kTileK && group_size != 64) || K % group_size) return WQ4_ERR_UNSUPPORTED;
     return WQ4_OK;
 }
 
@@ -213,10 +214,13 @@ int token_tile_for(const int* M, int P) {
     return best;
 }
 
-int pick_token_tile(const Shape* shapes, int P) {
+// With two scale sets per record (group size 64) a tile's partials take twice the tensor-memory
+// columns: at most 64 tokens then.
+int pick_token_tile(const Shape* shapes, int P, int group_size) {
     int Ms[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) Ms[p] = shapes[p].M;
-    return token_tile_for(Ms, P);
+    const int nt = token_tile_for(Ms, P);
+    return scale_sets(group_size) == 2 && nt > 64 ? 64 : nt;
 }
 
 // Splitting the last partial wave of tiles over all CTAs pays only if it saves more (tile, group)
@@ -235,8 +239,8 @@ bool keep_tiles_whole(long long tiles, long long units, int C) {
 // may ask for: a K-split plan that would need more keeps every tile whole instead (no workspace;
 // the same sums in another order), unless an option forces the split (then the caller's size
 // check fails).
-int make_plan(const Shape* shapes, int P, int sm_count, size_t ws_cap, Plan* pl) {
-    pl->nt = pick_token_tile(shapes, P);
+int make_plan(const Shape* shapes, int P, int sm_count, size_t ws_cap, int group_size, Plan* pl) {
+    pl->nt = pick_token_tile(shapes, P, group_size);
     long long tiles = 0, units = 0;
     for (int p = 0; p < P; ++p) {
         const Shape& s = shapes[p];
@@ -357,39 +361,42 @@ int encode_x_map(CUtensorMap* map, const void* X, int M, int K, int dtype, int n
     return r == CUDA_SUCCESS ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
-cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int grid, cudaStream_t st) {
+cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int group_size, int grid,
+                     cudaStream_t st) {
+    const int H = scale_sets(group_size);
     const bool bf16 = dtype == WQ4_BF16, a_tmem = !g_opt.a_in_smem;
     const int zp = qtype;                                       // record layout of the format
     const bool pdl = g_opt.pdl == 0;
     switch (nt) {
-        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
-        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
-        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
-        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
-        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, grid, pdl, st);
+        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
+        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
+        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
+        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
+        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
     }
 }
 
-// Float-zero mode: xsum[g][m] = the sum of X[m][128 g .. 128 g + 127] in fp32, 0 for rows m >= M
-// up to the padded row length ld. One warp per (g, m): each lane adds its 4 consecutive elements
-// in order, then a butterfly over the warp; lane 0's result is stored (the same order every run).
+// Float-zero mode: xsum[g][m] = the sum of X[m][span g .. span g + span - 1] in fp32 (span = 128,
+// or 64 with two scale sets per record), 0 for rows m >= M up to the padded row length ld. One warp
+// per (g, m): each lane adds its span / 32 consecutive elements in order, then a butterfly over the
+// warp; lane 0's result is stored (the same order every run).
 template <bool BF16>
-__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, float* __restrict__ out) {
+__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, int span, float* __restrict__ out) {
     const int lane = threadIdx.x & 31;
+    const int per = span / 32;
     const long long wpb = blockDim.x / 32;
-    const long long total = static_cast<long long>(K / kTileK) * ld;
+    const long long total = static_cast<long long>(K / span) * ld;
     for (long long w = blockIdx.x * wpb + threadIdx.x / 32; w < total; w += gridDim.x * wpb) {
         const int g = static_cast<int>(w / ld), m = static_cast<int>(w % ld);
         float v = 0.f;
         if (m < M) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(X + static_cast<size_t>(m) * K + kTileK * g + 4 * lane);
-            const uint32_t e[4] = {raw.x & 0xFFFFu, raw.x >> 16, raw.y & 0xFFFFu, raw.y >> 16};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            const uint16_t* xp = X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * g + per * lane;
+            for (int i = 0; i < per; ++i) {
+                const uint32_t e = xp[i];
                 if constexpr (BF16) {
-                    v += __uint_as_float(e[i] << 16);
+                    v += __uint_as_float(e << 16);
                 } else {
-                    v += __half2float(__ushort_as_half(static_cast<unsigned short>(e[i])));
+                    v += __half2float(__ushort_as_half(static_cast<unsigned short>(e)));
                 }
             }
         }
@@ -400,10 +407,10 @@ __global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld
 }
 
 // Bytes of the float-zero activation-sum table for one problem at token tile nt (0 otherwise).
-size_t xsum_table_bytes(int qtype, const Shape& s, int nt) {
+size_t xsum_table_bytes(int qtype, const Shape& s, int nt, int group_size) {
     if (qtype != WQ4_U4_FZP || s.M <= 0) return 0;
     const size_t ld = static_cast<size_t>((s.M + nt - 1) / nt) * nt;
-    return static_cast<size_t>(s.K / kTileK) * ld * 4;
+    return static_cast<size_t>(s.K / kTileK) * scale_sets(group_size) * ld * 4;
 }
 
 // Plans and launches the GEMM kernel for P problems. With fixed_scratch the workspace is the
@@ -418,10 +425,11 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     if (rc) return rc;
     if (qtype == WQ4_U4_FZP && MAXP > 1) return WQ4_ERR_UNSUPPORTED;   // float zeros: single problems
     // float zeros: the activation-sum table follows the plan's part of the workspace
-    const size_t xsum_bytes = xsum_table_bytes(qtype, shapes[0], pick_token_tile(shapes, P));
+    const size_t xsum_bytes = xsum_table_bytes(qtype, shapes[0], pick_token_tile(shapes, P, group_size), group_size);
     if (fixed_scratch && xsum_bytes + 256 > workspace_bytes) return WQ4_ERR_WORKSPACE;
     Plan pl;
-    rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes - xsum_bytes - 256 : SIZE_MAX, &pl);
+    rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes - xsum_bytes - 256 : SIZE_MAX, group_size,
+                   &pl);
     if (rc) return rc;
     if (pl.total_tiles == 0) return WQ4_OK;
     const size_t xsum_off = xsum_bytes ? (pl.workspace() + 255) / 256 * 256 : 0;
@@ -491,13 +499,14 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
         const int ld = pl.m_tiles[0] * pl.nt;
         prm->xsum = xs;
         prm->xsum_ld = ld;
-        const long long warps = static_cast<long long>(shapes[0].K / kTileK) * ld;
+        const int span = kTileK / scale_sets(group_size);
+        const long long warps = static_cast<long long>(shapes[0].K / span) * ld;
         const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 65535));
         const uint16_t* x16 = static_cast<const uint16_t*>(X[0]);
         if (dtype == WQ4_BF16) {
-            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, xs);
+            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, xs);
         } else {
-            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, xs);
+            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, xs);
         }
         if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     }
@@ -508,7 +517,7 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
                      P, pl.nt, pl.grid, pl.cluster, pl.total_tiles, pl.dp_tiles, pl.sk_units,
                      g_opt.a_in_smem ? "smem" : "tmem", pl.workspace(), fixed_scratch ? " (fixed array)" : "");
     }
-    const cudaError_t e = dispatch(prm, MAXP > 1, pl.nt, dtype, qtype, pl.grid, st);
+    const cudaError_t e = dispatch(prm, MAXP > 1, pl.nt, dtype, qtype, group_size, pl.grid, st);
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
@@ -559,7 +568,7 @@ const char* wq4_status_string(int status) {
 
 size_t wq4_prepacked_bytes(int N, int K, int group_size, int qtype) {
     if (check_types(group_size, WQ4_BF16, qtype) || check_nk(N, K) || check_group(group_size, K)) return 0;
-    return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype);
+    return kBlobHeader + static_cast<size_t>(N / kTileN) * (K / kTileK) * tile_record_bytes(qtype, scale_sets(group_size));
 }
 
 int wq4_prepack(const uint32_t* Wq, const void* scales, const void* zeros, int N, int K, int group_size,
@@ -608,7 +617,7 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev))) return rc;
     Plan pl;
-    if ((rc = make_plan(shapes, P, dev->sm_count, SIZE_MAX, &pl))) return rc;
+    if ((rc = make_plan(shapes, P, dev->sm_count, SIZE_MAX, group_size, &pl))) return rc;
     *bytes = pl.workspace();
     return WQ4_OK;
 }
@@ -621,7 +630,7 @@ int wq4_workspace_bytes_ex(int M, int N, int K, int group_size, int qtype, size_
     if ((rc = device_info(&dev))) return rc;
     if (M > 0 && !uses_decode_kernel(M, N, K)) {
         const Shape sh{M, N, K};
-        const size_t xs = xsum_table_bytes(qtype, sh, pick_token_tile(&sh, 1));
+        const size_t xs = xsum_table_bytes(qtype, sh, pick_token_tile(&sh, 1, group_size), group_size);
         if (xs) *bytes = (*bytes + 255) / 256 * 256 + xs;
     }
     return WQ4_OK;
@@ -780,7 +789,8 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
     if ((rc = device_info(&dev))) return rc;
     // Plan for the capacities: the token tile and the grid; every tile whole (the tile count is
     // known only on the device).
-    const int nt = token_tile_for(M_cap, P);
+    const int nt0 = token_tile_for(M_cap, P);
+    const int nt = scale_sets(group_size) == 2 && nt0 > 64 ? 64 : nt0;   // see pick_token_tile
     long long max_tiles = 0;
     auto* prm = new (std::nothrow) GemmParams<kMaxGroupedProblems>();
     if (!prm) return WQ4_ERR_CUDA;
@@ -830,7 +840,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
     prm->dyn = static_cast<const DynTable*>(workspace);
     dyn_table_kernel<<<1, 32, 0, stream>>>(M_dev, su, static_cast<DynTable*>(workspace));
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) e = dispatch(prm, true, nt, dtype, qtype, grid, stream);
+    if (e == cudaSuccess) e = dispatch(prm, true, nt, dtype, qtype, group_size, grid, stream);
     if (trace_on())
         std::fprintf(stderr, "[wq4] device-resident shapes: problems=%d token_tile=%d grid=%d max_tiles=%lld (%s)\n", P,
                      nt, grid, max_tiles, e == cudaSuccess ? "ok" : cudaGetErrorString(e));

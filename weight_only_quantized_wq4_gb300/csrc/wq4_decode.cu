@@ -77,7 +77,7 @@ struct DecCfg {
     static constexpr int kRedBytes = kDecWarps * NB * 32 * 16;              // per-warp partials
 };
 
-__host__ __device__ constexpr int dec_stage_bytes(int qt) { return kDecStageGroups * block_bytes(qt); }
+__host__ __device__ constexpr int dec_stage_bytes(int qt, int H = 1) { return kDecStageGroups * block_bytes(qt, H); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
     asm volatile(
@@ -158,11 +158,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
-template <int NB, bool BF16, int QT>
+template <int NB, bool BF16, int QT, int H>
 __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
     using C = DecCfg<NB>;
-    constexpr int kBB = block_bytes(QT);
-    constexpr int kStage = dec_stage_bytes(QT);
+    constexpr int kBB = block_bytes(QT, H);
+    constexpr int kStage = dec_stage_bytes(QT, H);
+    constexpr int kZ = block_zero_off(H);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -319,34 +320,42 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 const int gg = next_g;
                 const uint32_t ua = st + (gg - g_lo) * kBB;             // this block's record of group gg
                 const uint8_t* const up = sm + (ua - sbase);
-                const uint32_t sw = *reinterpret_cast<const uint32_t*>(up + kBlockScaleOff + 4 * g);
-                uint32_t sub_lo, sub_hi;                                // base + z of rows g, g + 8 (packed pair)
-                float zf_lo = 0.f, zf_hi = 0.f;                         // float zeros of rows g, g + 8
-                if constexpr (QT == kQtU4Zp) {
-                    const uint32_t zb = up[kBlockZeroOff + g];
-                    sub_lo = ((BF16 ? 0x4300u : 0x6400u) | (zb & 0xFu)) * 0x10001u;
-                    sub_hi = ((BF16 ? 0x4300u : 0x6400u) | (zb >> 4)) * 0x10001u;
-                } else if constexpr (QT == kQtU4FZp) {
-                    sub_lo = sub_hi = BF16 ? 0x43004300u : 0x64006400u;   // the code itself
-                    const uint32_t zw = *reinterpret_cast<const uint32_t*>(up + kBlockZeroOff + 4 * g);
-                    zf_lo = dec_to_float<BF16>(zw & 0xFFFFu);
-                    zf_hi = dec_to_float<BF16>(zw >> 16);
-                } else {
-                    sub_lo = sub_hi = BF16 ? 0x43084308u : 0x64086408u;
+                // per scale set q (one per 64-K half with a group size of 64, else one for both
+                // halves): the scale word, the packed subtrahend base + z, the float zeros of rows g, g + 8
+                uint32_t sw[H], sub_lo[H], sub_hi[H];
+                float zf_lo[H], zf_hi[H];
+#pragma unroll
+                for (int q = 0; q < H; ++q) {
+                    sw[q] = *reinterpret_cast<const uint32_t*>(up + kBlockScaleOff + 32 * q + 4 * g);
+                    zf_lo[q] = zf_hi[q] = 0.f;
+                    if constexpr (QT == kQtU4Zp) {
+                        const uint32_t zb = up[kZ + 8 * q + g];
+                        sub_lo[q] = ((BF16 ? 0x4300u : 0x6400u) | (zb & 0xFu)) * 0x10001u;
+                        sub_hi[q] = ((BF16 ? 0x4300u : 0x6400u) | (zb >> 4)) * 0x10001u;
+                    } else if constexpr (QT == kQtU4FZp) {
+                        sub_lo[q] = sub_hi[q] = BF16 ? 0x43004300u : 0x64006400u;   // the code itself
+                        const uint32_t zw = *reinterpret_cast<const uint32_t*>(up + kZ + 32 * q + 4 * g);
+                        zf_lo[q] = dec_to_float<BF16>(zw & 0xFFFFu);
+                        zf_hi[q] = dec_to_float<BF16>(zw >> 16);
+                    } else {
+                        sub_lo[q] = sub_hi[q] = BF16 ? 0x43084308u : 0x64086408u;
+                    }
                 }
                 const uint32_t xg = s_x + static_cast<uint32_t>(gg) * (2 * C::kMpad * 128);
                 const uint8_t* const xe = sm + (xg - sbase) + xo_even;
                 const uint8_t* const xd = sm + (xg - sbase) + xo_odd;
                 // two independent MMA chains, one per 64-element half of the group (half the
-                // dependent latency of one chain over the group), added at the fold
+                // dependent latency of one chain over the group), added (or scaled apart) at the fold
                 float pr[2][NB][4];
-                // float zeros: the group's activation sum per token, from an MMA with an all-ones A
-                // (the tensor pipe has room; the integer pipe does not)
-                float ps[NB][4];
+                // float zeros: the activation sum per token of each scale set's K range, from an
+                // MMA with an all-ones A (the tensor pipe has room; the integer pipe does not)
+                float ps[H][NB][4];
                 constexpr uint32_t kOnes = BF16 ? 0x3F803F80u : 0x3C003C00u;
                 const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
+                    constexpr int kOne = 0;
+                    const int qs = H == 2 ? q : kOne;                  // this half's scale set
                     uint32_t w[4];                                      // (2q, g) (2q, g+8) (2q+1, g) (2q+1, g+8)
                     ldsm_x4(ua + 512u * q + ld_off, w[0], w[1], w[2], w[3]);
 #pragma unroll
@@ -357,8 +366,8 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             // bit logic on the integer pipe, the exact subtraction on the fp16/bf16 one
-                            lo[e] = dec_sub2<BF16>(and_or(wlo >> (4 * e), nib.mask, nib.magic), sub_lo);
-                            hi[e] = dec_sub2<BF16>(and_or(whi >> (4 * e), nib.mask, nib.magic), sub_hi);
+                            lo[e] = dec_sub2<BF16>(and_or(wlo >> (4 * e), nib.mask, nib.magic), sub_lo[qs]);
+                            hi[e] = dec_sub2<BF16>(and_or(whi >> (4 * e), nib.mask, nib.magic), sub_hi[qs]);
                         }
                         const uint32_t a0[4] = {lo[0], hi[0], lo[1], hi[1]};
                         const uint32_t a1[4] = {lo[2], hi[2], lo[3], hi[3]};
@@ -373,30 +382,45 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                             }
                             mma16816<BF16>(pr[q][nb], a1, xb.z, xb.w);
                             if constexpr (QT == kQtU4FZp) {
-                                if (j == 0) {
-                                    mma16816_z<BF16>(ps[nb], ones, xb.x, xb.y);
+                                if (h == 0 && (q == 0 || H == 2)) {
+                                    mma16816_z<BF16>(ps[qs][nb], ones, xb.x, xb.y);
                                 } else {
-                                    mma16816<BF16>(ps[nb], ones, xb.x, xb.y);
+                                    mma16816<BF16>(ps[qs][nb], ones, xb.x, xb.y);
                                 }
-                                mma16816<BF16>(ps[nb], ones, xb.z, xb.w);
+                                mma16816<BF16>(ps[qs][nb], ones, xb.z, xb.w);
                             }
                         }
                     }
                 }
-                // group scale of rows g and g + 8 (one 32-bit word), in fp32
-                const float s_lo = dec_to_float<BF16>(sw & 0xFFFFu);
-                const float s_hi = dec_to_float<BF16>(sw >> 16);
+                // group scales of rows g and g + 8 (one 32-bit word per set), in fp32
 #pragma unroll
                 for (int nb = 0; nb < NB; ++nb) {
-                    acc[nb][0] = fmaf(s_lo, pr[0][nb][0] + pr[1][nb][0], acc[nb][0]);
-                    acc[nb][1] = fmaf(s_lo, pr[0][nb][1] + pr[1][nb][1], acc[nb][1]);
-                    acc[nb][2] = fmaf(s_hi, pr[0][nb][2] + pr[1][nb][2], acc[nb][2]);
-                    acc[nb][3] = fmaf(s_hi, pr[0][nb][3] + pr[1][nb][3], acc[nb][3]);
+                    if constexpr (H == 1) {
+                        const float s_lo = dec_to_float<BF16>(sw[0] & 0xFFFFu);
+                        const float s_hi = dec_to_float<BF16>(sw[0] >> 16);
+                        acc[nb][0] = fmaf(s_lo, pr[0][nb][0] + pr[1][nb][0], acc[nb][0]);
+                        acc[nb][1] = fmaf(s_lo, pr[0][nb][1] + pr[1][nb][1], acc[nb][1]);
+                        acc[nb][2] = fmaf(s_hi, pr[0][nb][2] + pr[1][nb][2], acc[nb][2]);
+                        acc[nb][3] = fmaf(s_hi, pr[0][nb][3] + pr[1][nb][3], acc[nb][3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const float s_lo = dec_to_float<BF16>(sw[q] & 0xFFFFu);
+                            const float s_hi = dec_to_float<BF16>(sw[q] >> 16);
+                            acc[nb][0] = fmaf(s_lo, pr[q][nb][0], acc[nb][0]);
+                            acc[nb][1] = fmaf(s_lo, pr[q][nb][1], acc[nb][1]);
+                            acc[nb][2] = fmaf(s_hi, pr[q][nb][2], acc[nb][2]);
+                            acc[nb][3] = fmaf(s_hi, pr[q][nb][3], acc[nb][3]);
+                        }
+                    }
                     if constexpr (QT == kQtU4FZp) {
-                        acc[nb][0] = fmaf(zf_lo, ps[nb][0], acc[nb][0]);
-                        acc[nb][1] = fmaf(zf_lo, ps[nb][1], acc[nb][1]);
-                        acc[nb][2] = fmaf(zf_hi, ps[nb][2], acc[nb][2]);
-                        acc[nb][3] = fmaf(zf_hi, ps[nb][3], acc[nb][3]);
+#pragma unroll
+                        for (int q = 0; q < H; ++q) {
+                            acc[nb][0] = fmaf(zf_lo[q], ps[q][nb][0], acc[nb][0]);
+                            acc[nb][1] = fmaf(zf_lo[q], ps[q][nb][1], acc[nb][1]);
+                            acc[nb][2] = fmaf(zf_hi[q], ps[q][nb][2], acc[nb][2]);
+                            acc[nb][3] = fmaf(zf_hi[q], ps[q][nb][3], acc[nb][3]);
+                        }
                     }
                 }
             }
@@ -476,8 +500,8 @@ static int dec_x_region(int nb, int K) {
     return ((x > red ? x : red) + 127) & ~127;
 }
 
-static int decode_smem_bytes(int nb, int K, int depth, int zp) {
-    return 1024 + dec_x_region(nb, K) + depth * dec_stage_bytes(zp) + 8 * (2 * kDecMaxDepth + kDecMaxPieces + 1) + 16;
+static int decode_smem_bytes(int nb, int K, int depth, int zp, int H) {
+    return 1024 + dec_x_region(nb, K) + depth * dec_stage_bytes(zp, H) + 8 * (2 * kDecMaxDepth + kDecMaxPieces + 1) + 16;
 }
 
 // Ring depth: the deepest that fits, capped by the items a CTA has and, while the activations are
@@ -486,16 +510,16 @@ static int decode_smem_bytes(int nb, int K, int depth, int zp) {
 // round trip) where the full size gives it two (measured, 8 tokens, N = 14336, K = 4096, constant
 // weights: 6 blocks per CTA, 10.5 us with two CTAs per SM and one slot per block, 8.9 us with one
 // CTA per SM and two slots per block).
-static int decode_depth(int nb, int K, int zp, int items_max, int nbc, int forced) {
+static int decode_depth(int nb, int K, int zp, int H, int items_max, int nbc, int forced) {
     const int d_min = nbc > 2 ? nbc : 2;
     int d = forced > 0 ? forced : kDecMaxDepth;
     if (d > items_max) d = items_max;
     if (d < d_min) d = d_min;
     const bool small_x = dec_x_region(nb, K) <= 64 * 1024;
-    while (d > d_min && decode_smem_bytes(nb, K, d, zp) > kDecMaxSmem) --d;
+    while (d > d_min && decode_smem_bytes(nb, K, d, zp, H) > kDecMaxSmem) --d;
     if (forced <= 0 && small_x) {
         int dc = d;
-        while (dc > d_min && decode_smem_bytes(nb, K, dc, zp) > kDecCoResident) --dc;
+        while (dc > d_min && decode_smem_bytes(nb, K, dc, zp, H) > kDecCoResident) --dc;
         const bool co_double = dc >= items_max || dc >= 2 * nbc;
         const bool full_double = d >= items_max || d >= 2 * nbc;
         if (co_double || !full_double) d = dc;
@@ -507,13 +531,13 @@ bool decode_fits(int M, int K) {
     if (M < 1 || M > 32) return false;
     const int n_st = (K / kTileK + kDecStageGroups - 1) / kDecStageGroups;
     if (n_st > kDecMaxPieces) return false;
-    return decode_smem_bytes(dec_nb(M), K, 2, kQtU4FZp) <= kDecMaxSmem;   // the largest records
+    return decode_smem_bytes(dec_nb(M), K, 2, kQtU4FZp, 2) <= kDecMaxSmem;   // the largest records
 }
 
-template <int NB, bool BF16, int QT>
+template <int NB, bool BF16, int QT, int H>
 static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStream_t st) {
-    auto kern = wq4_decode_kernel<NB, BF16, QT>;
-    const int smem = decode_smem_bytes(NB, p.K, p.depth, QT);
+    auto kern = wq4_decode_kernel<NB, BF16, QT, H>;
+    const int smem = decode_smem_bytes(NB, p.K, p.depth, QT, H);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -531,13 +555,18 @@ static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStre
     return cudaGetLastError();
 }
 
-template <int NB>
-static cudaError_t pick_decode(const DecodeParams& p, bool bf16, int qt, int grid, bool pdl, cudaStream_t st) {
+template <int NB, int H>
+static cudaError_t pick_decode_q(const DecodeParams& p, bool bf16, int qt, int grid, bool pdl, cudaStream_t st) {
     switch (qt) {
-        case kQtU4B8: return bf16 ? go_decode<NB, true, kQtU4B8>(p, grid, pdl, st) : go_decode<NB, false, kQtU4B8>(p, grid, pdl, st);
-        case kQtU4Zp: return bf16 ? go_decode<NB, true, kQtU4Zp>(p, grid, pdl, st) : go_decode<NB, false, kQtU4Zp>(p, grid, pdl, st);
-        default: return bf16 ? go_decode<NB, true, kQtU4FZp>(p, grid, pdl, st) : go_decode<NB, false, kQtU4FZp>(p, grid, pdl, st);
+        case kQtU4B8: return bf16 ? go_decode<NB, true, kQtU4B8, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4B8, H>(p, grid, pdl, st);
+        case kQtU4Zp: return bf16 ? go_decode<NB, true, kQtU4Zp, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4Zp, H>(p, grid, pdl, st);
+        default: return bf16 ? go_decode<NB, true, kQtU4FZp, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4FZp, H>(p, grid, pdl, st);
     }
+}
+
+template <int NB>
+static cudaError_t pick_decode(const DecodeParams& p, bool bf16, int qt, int H, int grid, bool pdl, cudaStream_t st) {
+    return H == 2 ? pick_decode_q<NB, 2>(p, bf16, qt, grid, pdl, st) : pick_decode_q<NB, 1>(p, bf16, qt, grid, pdl, st);
 }
 
 // Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
@@ -550,6 +579,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     const Enc enc = reinterpret_cast<Enc>(L.encode_fn);
     const int nb = dec_nb(M);
     const int zp = qtype;                                       // record layout of the format
+    const int H = scale_sets(group_size);
     DecodeParams p;
     std::memset(static_cast<void*>(&p), 0, sizeof(p));
     {
@@ -565,11 +595,11 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     }
     {
         // the blob's records as 16-row blocks: (u64 words of a block, block, group, n-tile)
-        const int bb = block_bytes(zp);
+        const int bb = block_bytes(zp, H);
         const cuuint64_t dims[4] = {static_cast<cuuint64_t>(bb / 8), 8, static_cast<cuuint64_t>(K / kTileK),
                                     static_cast<cuuint64_t>(N / kTileN)};
-        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(bb), static_cast<cuuint64_t>(tile_record_bytes(zp)),
-                                       static_cast<cuuint64_t>(tile_record_bytes(zp)) * (K / kTileK)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(bb), static_cast<cuuint64_t>(tile_record_bytes(zp, H)),
+                                       static_cast<cuuint64_t>(tile_record_bytes(zp, H)) * (K / kTileK)};
         const cuuint32_t box[4] = {static_cast<cuuint32_t>(bb / 8), 1, kDecStageGroups, 1};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
         const CUresult r = enc(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
@@ -593,13 +623,13 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     // one CTA per SM; a CTA owns at most as many blocks as it has ring slots (one per block at
     // least) and warps (16): beyond that, more CTAs than SMs
     int grid = L.sm_count < p.n_blocks ? L.sm_count : p.n_blocks;
-    int cap = (kDecMaxSmem - decode_smem_bytes(nb, K, 0, zp)) / dec_stage_bytes(zp);
+    int cap = (kDecMaxSmem - decode_smem_bytes(nb, K, 0, zp, H)) / dec_stage_bytes(zp, H);
     if (cap > kDecWarps) cap = kDecWarps;
     if (cap < 1) return cudaErrorInvalidConfiguration;
     if (p.n_blocks > cap * grid) grid = (p.n_blocks + cap - 1) / cap;
     const int nbc_max = (p.n_blocks + grid - 1) / grid;
-    p.depth = decode_depth(nb, K, zp, nbc_max * p.n_stages, nbc_max, L.depth);
-    if (decode_smem_bytes(nb, K, p.depth, zp) > kDecMaxSmem) return cudaErrorInvalidConfiguration;
+    p.depth = decode_depth(nb, K, zp, H, nbc_max * p.n_stages, nbc_max, L.depth);
+    if (decode_smem_bytes(nb, K, p.depth, zp, H) > kDecMaxSmem) return cudaErrorInvalidConfiguration;
     p.status = L.status;
     p.timeout_cycles = L.timeout_cycles;
     p.test_stall = L.test_stall;
@@ -617,9 +647,9 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
     *depth_out = p.depth;
     const bool bf16 = dtype == 0;
     switch (nb) {
-        case 1: return pick_decode<1>(p, bf16, zp, grid, L.pdl, st);
-        case 2: return pick_decode<2>(p, bf16, zp, grid, L.pdl, st);
-        default: return pick_decode<4>(p, bf16, zp, grid, L.pdl, st);
+        case 1: return pick_decode<1>(p, bf16, zp, H, grid, L.pdl, st);
+        case 2: return pick_decode<2>(p, bf16, zp, H, grid, L.pdl, st);
+        default: return pick_decode<4>(p, bf16, zp, H, grid, L.pdl, st);
     }
 }
 

@@ -297,7 +297,8 @@ __device__ __forceinline__ BlobHeader load_blob_header(const uint32_t* hdr) {
 __device__ __forceinline__ bool blob_header_matches(const BlobHeader& h, int N, int K, int G, int dtype, int qtype) {
     return h.a.x == kBlobMagic && h.a.y == kBlobVersion && h.a.z == static_cast<uint32_t>(N) &&
            h.a.w == static_cast<uint32_t>(K) && h.b.x == static_cast<uint32_t>(G) && h.b.y == static_cast<uint32_t>(dtype) &&
-           h.b.z == static_cast<uint32_t>(qtype) && h.b.w == static_cast<uint32_t>(tile_record_bytes(qtype));
+           h.b.z == static_cast<uint32_t>(qtype) &&
+           h.b.w == static_cast<uint32_t>(tile_record_bytes(qtype, scale_sets(G)));
 }
 __device__ __forceinline__ bool blob_header_ok(const uint32_t* hdr, int N, int K, int G, int dtype, int qtype) {
     return blob_header_matches(load_blob_header(hdr), N, K, G, dtype, qtype);

@@ -39,9 +39,12 @@
 
 namespace wq4 {
 
-template <int NT, int QT, bool ATMEM>
+template <int NT, int QT, bool ATMEM, int H>
 struct GemmCfg {
     static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 160 || NT == 192, "token tile");
+    // H scale sets per 128-K record (2 for a group size of 64): each group's MMAs accumulate into
+    // H partials of NT columns (K 0..63 and 64..127 apart), each folded with its own scale.
+    static_assert(H == 1 || (H == 2 && NT <= 64), "two scale sets need a token tile of at most 64");
     // Four warpgroups: WG0 = the two TMA producer warps (0, 2) and the two MMA warps (1, 3);
     // then the dequant warps; then the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
     static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
@@ -62,7 +65,7 @@ struct GemmCfg {
     static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
     // epilogue: C values loaded together per thread (16 at NT = 192 spill the bf16 fold warps)
     static constexpr int kEpiBatch = NT >= 192 ? 8 : 16;
-    static constexpr int kRec = tile_record_bytes(QT);
+    static constexpr int kRec = tile_record_bytes(QT, H);
     static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
     // Two rings: activation tiles (two panels per group; consumed by the MMA, released by its
     // commit) and weight records (codes + scales + zeros; released once the dequant warps and
@@ -79,7 +82,8 @@ struct GemmCfg {
     // measured slower than two P buffers with four operand buffers (the dequantisation chain
     // binds before the fold chain does).
     static constexpr int kPBufs = 2;
-    static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * NT) / 64 >= 4 ? 4 : (512 - kPBufs * NT) / 64;
+    static constexpr int kPCols = H * NT;                    // tensor-memory columns of one P buffer
+    static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * kPCols) / 64 >= 4 ? 4 : (512 - kPBufs * kPCols) / 64;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
@@ -92,8 +96,8 @@ struct GemmCfg {
     // an odd count a warp would skip the other warp's phase of a slot).
     static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
     static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
-    static constexpr int kColA = kPBufs * NT;                // TMEM column of A buffer 0
-    static constexpr int kTmemNeed = kPBufs * NT + (ATMEM ? 64 * kABufs : 0);
+    static constexpr int kColA = kPBufs * kPCols;            // TMEM column of A buffer 0
+    static constexpr int kTmemNeed = kPBufs * kPCols + (ATMEM ? 64 * kABufs : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
     static_assert(kXStages >= 2 && kWStages <= 16, "shared memory");
@@ -298,10 +302,10 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a, uint32_t b0,
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
 }
 
-template <int NT, bool BF16, int QT, int MAXP, bool ATMEM>
-__global__ void __launch_bounds__(GemmCfg<NT, QT, ATMEM>::kThreads, 1)
+template <int NT, bool BF16, int QT, int MAXP, bool ATMEM, int H>
+__global__ void __launch_bounds__(GemmCfg<NT, QT, ATMEM, H>::kThreads, 1)
 wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
-    using C = GemmCfg<NT, QT, ATMEM>;
+    using C = GemmCfg<NT, QT, ATMEM, H>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -469,16 +473,18 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     if (!mbar_wait(afull_bar(a), (i / C::kABufs) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * NT);
                     const uint32_t xs = s_x0 + s * C::kXStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
+                        // K panel kk / 4; with two scale sets each panel has its own partial
+                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kPCols + (H == 2 ? (kk >> 2) * NT : 0));
+                        const bool accum = H == 2 ? (kk & 3) > 0 : kk > 0;
                         const uint64_t bdesc = make_sdesc_sw128(xs + (kk >> 2) * C::kXPanel + (kk & 3) * 32);
                         if constexpr (ATMEM) {
-                            mma_ts(d_tmem, tmem_base + C::kColA + a * 64 + kk * 8, bdesc, idesc, kk > 0);
+                            mma_ts(d_tmem, tmem_base + C::kColA + a * 64 + kk * 8, bdesc, idesc, accum);
                         } else {
                             const uint64_t adesc = make_sdesc_sw128(s_A + a * C::kABuf + (kk >> 2) * (C::kABuf / 2) + (kk & 3) * 32);
-                            mma_ss(d_tmem, adesc, bdesc, idesc, kk > 0);
+                            mma_ss(d_tmem, adesc, bdesc, idesc, accum);
                         }
                     }
                     mma_commit(pfull_bar(b));
@@ -509,21 +515,25 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
                 if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
                 const uint32_t rec = wrec_of(i);
-                uint32_t sub;
-                if constexpr (QT == kQtU4Zp) {
-                    uint32_t zb;
-                    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + rec_zero_off(QT, r)));
-                    const uint32_t z = (zb >> (((r >> 3) & 1) * 4)) & 0xFu;
-                    sub = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
-                } else if constexpr (QT == kQtU4FZp) {
-                    sub = BF16 ? 0x43004300u : 0x64006400u;   // the code itself; its zero is added at the fold
-                } else {
-                    sub = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
+                uint32_t subs[H];                             // per scale set
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    if constexpr (QT == kQtU4Zp) {
+                        uint32_t zb;
+                        asm volatile("ld.shared.u8 %0, [%1];" : "=r"(zb) : "r"(rec + rec_zero_off(QT, r, H, h)));
+                        const uint32_t z = (zb >> (((r >> 3) & 1) * 4)) & 0xFu;
+                        subs[h] = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
+                    } else if constexpr (QT == kQtU4FZp) {
+                        subs[h] = BF16 ? 0x43004300u : 0x64006400u;   // the code itself; its zero is added at the fold
+                    } else {
+                        subs[h] = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
+                    }
                 }
 #pragma unroll
                 for (int jj = 0; jj < C::kChunks; ++jj) {
                     const int j = part * C::kChunks + jj;
-                    const uint4 v = lds128(rec + rec_code_off(QT, r, j));
+                    const uint32_t sub = subs[H == 2 ? (j >> 1) : 0];   // 32-K chunk j lies in set j / 2
+                    const uint4 v = lds128(rec + rec_code_off(QT, r, j, H));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
                     uint32_t out[16];
 #pragma unroll
@@ -586,51 +596,55 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t rec = wrec_of(i);
-                uint32_t sbits;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(QT, r)));
-                const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
-                // float zeros: acc += zf * (sum of the group's activations per token), the sums read
-                // from the table a pre-pass wrote (xsum[g][m], this thread's columns contiguous)
-                float zf = 0.f;
-                const float* srow = nullptr;
-                if constexpr (QT == kQtU4FZp) {
-                    uint32_t zbits;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(zbits) : "r"(rec + rec_fzero_off(QT, r)));
-                    zf = scale_to_float<BF16>(static_cast<uint16_t>(zbits));
-                    srow = prm.xsum + static_cast<size_t>(g) * prm.xsum_ld + seg.mt * NT + col0;
-                    // the next group's sums into L1 now (one lane: every lane reads the same row)
-                    if (lane == 0 && g + 1 < seg.g1) {
-#pragma unroll
-                        for (int off = 0; off < C::kNC * 4; off += 128)
-                            asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(srow + prm.xsum_ld) + off));
-                    }
-                }
                 if (g == seg.g0) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
                 }
-                // P in batches of up to 64 columns per wait (the loads of a batch overlap)
-                // (the last batch may be shorter: 80 columns = 48 + 32)
-                constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
 #pragma unroll
-                for (int c = 0; c < C::kNC; c += kBatchCols) {
-                    constexpr int kLeft = C::kNC;
-                    const int nbc = kLeft - c < kBatchCols ? kLeft - c : kBatchCols;
-                    uint32_t v[kBatchCols];
+                for (int h = 0; h < H; ++h) {                   // scale set h: its partial, scale and zero
+                    uint32_t sbits;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(QT, r, H, h)));
+                    const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
+                    // float zeros: acc += zf * (sum of the set's activations per token), the sums read
+                    // from the table a pre-pass wrote (xsum[g H + h][m], this thread's columns contiguous)
+                    float zf = 0.f;
+                    const float* srow = nullptr;
+                    if constexpr (QT == kQtU4FZp) {
+                        uint32_t zbits;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(zbits) : "r"(rec + rec_fzero_off(QT, r, H, h)));
+                        zf = scale_to_float<BF16>(static_cast<uint16_t>(zbits));
+                        srow = prm.xsum + static_cast<size_t>(g * H + h) * prm.xsum_ld + seg.mt * NT + col0;
+                        // the next row of sums into L1 now (one lane: every lane reads the same row)
+                        if (lane == 0 && (h + 1 < H || g + 1 < seg.g1)) {
 #pragma unroll
-                    for (int q = 0; q < kBatchCols; q += 16)
-                        if (q < nbc) tmem_ld16(t_lane + b * NT + col0 + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
-                    tmem_ld_wait();
+                            for (int off = 0; off < C::kNC * 4; off += 128)
+                                asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(srow + prm.xsum_ld) + off));
+                        }
+                    }
+                    // P in batches of up to 64 columns per wait (the loads of a batch overlap)
+                    // (the last batch may be shorter: 80 columns = 48 + 32)
+                    constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
+                    const uint32_t t_p = t_lane + b * C::kPCols + h * NT + col0;
 #pragma unroll
-                    for (int j = 0; j < kBatchCols; j += 4) {
-                        // (columns come in multiples of 16: j < nbc covers j + 3 too)
-                        if (j < nbc) {
-                            fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
-                            fma2(acc[c + j + 2], acc[c + j + 3], sc, v[j + 2], v[j + 3]);
-                            if constexpr (QT == kQtU4FZp) {
-                                const float4 sv = __ldg(reinterpret_cast<const float4*>(srow + c + j));
-                                fma2(acc[c + j], acc[c + j + 1], zf, __float_as_uint(sv.x), __float_as_uint(sv.y));
-                                fma2(acc[c + j + 2], acc[c + j + 3], zf, __float_as_uint(sv.z), __float_as_uint(sv.w));
+                    for (int c = 0; c < C::kNC; c += kBatchCols) {
+                        constexpr int kLeft = C::kNC;
+                        const int nbc = kLeft - c < kBatchCols ? kLeft - c : kBatchCols;
+                        uint32_t v[kBatchCols];
+#pragma unroll
+                        for (int q = 0; q < kBatchCols; q += 16)
+                            if (q < nbc) tmem_ld16(t_p + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < kBatchCols; j += 4) {
+                            // (columns come in multiples of 16: j < nbc covers j + 3 too)
+                            if (j < nbc) {
+                                fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                                fma2(acc[c + j + 2], acc[c + j + 3], sc, v[j + 2], v[j + 3]);
+                                if constexpr (QT == kQtU4FZp) {
+                                    const float4 sv = __ldg(reinterpret_cast<const float4*>(srow + c + j));
+                                    fma2(acc[c + j], acc[c + j + 1], zf, __float_as_uint(sv.x), __float_as_uint(sv.y));
+                                    fma2(acc[c + j + 2], acc[c + j + 3], zf, __float_as_uint(sv.z), __float_as_uint(sv.w));
+                                }
                             }
                         }
                     }
@@ -789,10 +803,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 }
 
 // Host-side launcher for one instantiation (cluster = S CTAs per cluster in cluster mode, else 1).
-template <int NT, bool BF16, int QT, int MAXP, bool ATMEM>
+template <int NT, bool BF16, int QT, int MAXP, bool ATMEM, int H>
 cudaError_t launch_gemm(const GemmParams<MAXP>& p, int grid, bool pdl, cudaStream_t stream) {
-    using C = GemmCfg<NT, QT, ATMEM>;
-    auto kern = wq4_gemm_kernel<NT, BF16, QT, MAXP, ATMEM>;
+    using C = GemmCfg<NT, QT, ATMEM, H>;
+    auto kern = wq4_gemm_kernel<NT, BF16, QT, MAXP, ATMEM, H>;
     if constexpr (C::kRegSplit) {
         // The register split assumes 128 registers per thread at launch; a build that launched
         // with fewer would leave the fold warps' setmaxnreg.inc waiting forever. Refuse it.

@@ -15,15 +15,15 @@ struct EpilogueArgs {
 };
 
 // `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
-cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
                               bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
                               bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int grid,
+cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
                               bool pdl, cudaStream_t st);
 
 // Decode-sized M (<= 32 tokens): warp-level MMA kernel, no workspace.

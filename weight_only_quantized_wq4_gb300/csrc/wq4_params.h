@@ -25,30 +25,34 @@ enum : int { kQtU4B8 = 0, kQtU4Zp = 1, kQtU4FZp = 2 };
 
 // A (128-row, 128-K) record of the prepacked blob is eight blocks of 16 weight rows. Block b
 // holds, for its rows rr = 0..15: 1024 B of codes (16-byte chunk 16 j + rr = the row's K elements
-// 32 j + [0, 32)), 32 B of scales (row rr at byte 4 (rr % 8) + 2 (rr / 8)), then in zero-point mode
-// 8 B of zero points (row rr in byte rr % 8, high nibble for rr >= 8) padded to 16 B, in float-zero
-// mode 32 B of float zeros placed like the scales. A block is one contiguous run, so a kernel that
-// owns a few 16-row blocks stages exactly those with one tensor copy per run of groups, and a
-// kernel that owns whole tiles copies the record at once.
+// 32 j + [0, 32)), then H scale sets (H = 2 for a group size of 64, set h covering the record's K
+// elements from 64 h; else H = 1) of 32 B each (row rr at byte 4 (rr % 8) + 2 (rr / 8) of the
+// set), then per set the zeros: in zero-point mode 8 B (row rr in byte rr % 8, high nibble for
+// rr >= 8), in float-zero mode 32 B placed like the scales; padded to 16 B. A block is one
+// contiguous run, so a kernel that owns a few 16-row blocks stages exactly those with one tensor
+// copy per run of groups, and a kernel that owns whole tiles copies the record at once.
 constexpr int kBlockRows = 16;
 constexpr int kBlockCodes = 1024;
 constexpr int kBlockScaleOff = 1024;
-constexpr int kBlockZeroOff = 1056;
-__host__ __device__ constexpr int block_bytes(int qt) { return qt == kQtU4Zp ? 1072 : qt == kQtU4FZp ? 1088 : 1056; }
-__host__ __device__ constexpr int tile_record_bytes(int qt) { return 8 * block_bytes(qt); }
-// Byte offsets, inside a record, of row r's (0..127) 16-byte code chunk j, its scale, the byte
-// holding its zero point (nibble (r / 8) & 1) and its float zero.
-__host__ __device__ constexpr int rec_code_off(int qt, int r, int j) {
-    return (r >> 4) * block_bytes(qt) + (16 * j + (r & 15)) * 16;
+__host__ __device__ constexpr int scale_sets(int group_size) { return group_size == 64 ? 2 : 1; }
+__host__ __device__ constexpr int block_zero_off(int H) { return kBlockScaleOff + 32 * H; }
+__host__ __device__ constexpr int block_bytes(int qt, int H = 1) {
+    return (block_zero_off(H) + H * (qt == kQtU4Zp ? 8 : qt == kQtU4FZp ? 32 : 0) + 15) / 16 * 16;
 }
-__host__ __device__ constexpr int rec_scale_off(int qt, int r) {
-    return (r >> 4) * block_bytes(qt) + kBlockScaleOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
+__host__ __device__ constexpr int tile_record_bytes(int qt, int H = 1) { return 8 * block_bytes(qt, H); }
+// Byte offsets, inside a record, of row r's (0..127) 16-byte code chunk j, its scale of set h, the
+// byte holding its zero point of set h (nibble (r / 8) & 1) and its float zero of set h.
+__host__ __device__ constexpr int rec_code_off(int qt, int r, int j, int H = 1) {
+    return (r >> 4) * block_bytes(qt, H) + (16 * j + (r & 15)) * 16;
 }
-__host__ __device__ constexpr int rec_zero_off(int qt, int r) {
-    return (r >> 4) * block_bytes(qt) + kBlockZeroOff + (r & 7);
+__host__ __device__ constexpr int rec_scale_off(int qt, int r, int H = 1, int h = 0) {
+    return (r >> 4) * block_bytes(qt, H) + kBlockScaleOff + 32 * h + 4 * (r & 7) + 2 * ((r >> 3) & 1);
 }
-__host__ __device__ constexpr int rec_fzero_off(int qt, int r) {
-    return (r >> 4) * block_bytes(qt) + kBlockZeroOff + 4 * (r & 7) + 2 * ((r >> 3) & 1);
+__host__ __device__ constexpr int rec_zero_off(int qt, int r, int H = 1, int h = 0) {
+    return (r >> 4) * block_bytes(qt, H) + block_zero_off(H) + 8 * h + (r & 7);
+}
+__host__ __device__ constexpr int rec_fzero_off(int qt, int r, int H = 1, int h = 0) {
+    return (r >> 4) * block_bytes(qt, H) + block_zero_off(H) + 32 * h + 4 * (r & 7) + 2 * ((r >> 3) & 1);
 }
 
 struct ProblemDesc {

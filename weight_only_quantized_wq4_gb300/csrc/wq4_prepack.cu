@@ -10,9 +10,9 @@
 //     word w holds elements 8w + e (e = 0..7) of that run with element e in nibble e/2 + 4 (e % 2),
 //     so that (word >> 4i) & 0x000F000F holds elements 2i, 2i+1. A thread that owns a row reads a
 //     32-element run with one 128-bit load; a warp's 8-row 16-byte pieces are 128 contiguous bytes;
-//   * 32 B of scales, row rr at byte 4 (rr % 8) + 2 (rr / 8) (the scale of the quantisation group
-//     the record lies in: with a group size G that is a multiple of 128, record g carries group
-//     128 g / G; without scales every slot holds 1.0);
+//   * 32 B of scales per scale set, row rr at byte 4 (rr % 8) + 2 (rr / 8) of the set (one set with
+//     a group size G that is a multiple of 128, record g carrying group 128 g / G; two with G = 64,
+//     set h carrying group 2 g + h; without scales every slot holds 1.0);
 //   * (zero-point mode) 8 B of zero points, row rr in byte rr % 8 (high nibble for rr >= 8), then
 //     zero padding to 1072 B; (float-zero mode) 32 B of float zeros placed like the scales (1088 B).
 #include <cuda_runtime.h>
@@ -38,44 +38,45 @@ __device__ __forceinline__ uint32_t deinterleave_codes(uint32_t in) {
 }
 
 // Byte offset (from the first record) of the code word holding elements [8 kw, 8 kw + 8) of row n.
-__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, int zp) {
+__device__ __forceinline__ size_t code_word_offset(int n, int kw, int k_groups, int zp, int H) {
     const int g = kw >> 4, j = (kw >> 2) & 3, w = kw & 3;
     const int nt = n >> 7, r = n & 127;
-    return (static_cast<size_t>(nt) * k_groups + g) * tile_record_bytes(zp) +
-           static_cast<size_t>(rec_code_off(zp, r, j) + 4 * w);
+    return (static_cast<size_t>(nt) * k_groups + g) * tile_record_bytes(zp, H) +
+           static_cast<size_t>(rec_code_off(zp, r, j, H) + 4 * w);
 }
 
 __global__ void prepack_codes_kernel(const uint32_t* __restrict__ wq, uint8_t* __restrict__ recs, int N,
-                                     int K, int zp) {
+                                     int K, int zp, int H) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(idx / kwords), kw = static_cast<int>(idx % kwords);
-        *reinterpret_cast<uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp)) = interleave_codes(wq[idx]);
+        *reinterpret_cast<uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp, H)) = interleave_codes(wq[idx]);
     }
 }
 
 __global__ void unprepack_codes_kernel(const uint8_t* __restrict__ recs, uint32_t* __restrict__ wq, int N,
-                                       int K, int zp) {
+                                       int K, int zp, int H) {
     const int kwords = K / 8;
     const long long total = static_cast<long long>(N) * kwords;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int n = static_cast<int>(idx / kwords), kw = static_cast<int>(idx % kwords);
-        wq[idx] = deinterleave_codes(*reinterpret_cast<const uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp)));
+        wq[idx] = deinterleave_codes(*reinterpret_cast<const uint32_t*>(recs + code_word_offset(n, kw, K / 128, zp, H)));
     }
 }
 
-// Scales and float zeros (one thread per (group, row)), zero points and padding (one thread per
-// (group, 16-row block): the eight zero-point bytes of a block combine two of the API's words),
-// and the header.
+// Scales and float zeros (one thread per (record, row), every scale set), zero points and padding
+// (one thread per (record, 16-row block): the eight zero-point bytes of a block combine two of the
+// API's words), and the header. Set h of record g carries quantisation group (128 g + 64 h) / G.
 __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const void* __restrict__ zeros_in,
                                     uint8_t* __restrict__ blob, int N, int K, int G, int dtype, int qtype) {
     const int zp = qtype;                                            // record layout of this format
+    const int H = scale_sets(G);
     const uint32_t* zeros = static_cast<const uint32_t*>(zeros_in);  // 4-bit zero points (zero-point mode)
     const uint16_t* fzeros = static_cast<const uint16_t*>(zeros_in); // float zeros (float-zero mode)
-    const int rec = tile_record_bytes(zp);
+    const int rec = tile_record_bytes(zp, H);
     const uint16_t one = dtype == 0 ? 0x3F80u : 0x3C00u;     // 1.0 in bf16 / fp16
     const int ng = K / 128, nT = N / 128;
     uint8_t* recs = blob + kBlobHeader;
@@ -86,30 +87,35 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const v
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
             const int g = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
-            const int src = (g * 128) / G;                           // quantisation group of record g
             uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            *reinterpret_cast<uint16_t*>(r + rec_scale_off(zp, n & 127)) =
-                scales ? scales[static_cast<size_t>(src) * N + n] : one;
-            if (qtype == kQtU4FZp)
-                *reinterpret_cast<uint16_t*>(r + rec_fzero_off(zp, n & 127)) = fzeros[static_cast<size_t>(src) * N + n];
+            for (int h = 0; h < H; ++h) {
+                const int src = (g * 128 + 64 * h) / G;              // quantisation group of set h
+                *reinterpret_cast<uint16_t*>(r + rec_scale_off(zp, n & 127, H, h)) =
+                    scales ? scales[static_cast<size_t>(src) * N + n] : one;
+                if (qtype == kQtU4FZp)
+                    *reinterpret_cast<uint16_t*>(r + rec_fzero_off(zp, n & 127, H, h)) =
+                        fzeros[static_cast<size_t>(src) * N + n];
+            }
         } else if (idx < n_scale + n_block) {
             const long long z = idx - n_scale;
             const int g = static_cast<int>(z / (N / kBlockRows)), blk = static_cast<int>(z % (N / kBlockRows));
-            const int src = (g * 128) / G;
-            const uint32_t lo = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk];       // rows 16 blk + 0..7
-            const uint32_t hi = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk + 1];   // rows 16 blk + 8..15
-            uint32_t w[2] = {0u, 0u};
+            uint8_t* r = recs + (static_cast<size_t>(blk >> 3) * ng + g) * rec + (blk & 7) * block_bytes(kQtU4Zp, H);
+            uint32_t* zw = reinterpret_cast<uint32_t*>(r + block_zero_off(H));
+            for (int h = 0; h < H; ++h) {
+                const int src = (g * 128 + 64 * h) / G;
+                const uint32_t lo = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk];       // rows 16 blk + 0..7
+                const uint32_t hi = zeros[static_cast<size_t>(src) * (N / 8) + 2 * blk + 1];   // rows 16 blk + 8..15
+                uint32_t w[2] = {0u, 0u};
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const uint32_t byte = ((lo >> (4 * p)) & 0xFu) | (((hi >> (4 * p)) & 0xFu) << 4);
-                w[p >> 2] |= byte << (8 * (p & 3));
+                for (int p = 0; p < 8; ++p) {
+                    const uint32_t byte = ((lo >> (4 * p)) & 0xFu) | (((hi >> (4 * p)) & 0xFu) << 4);
+                    w[p >> 2] |= byte << (8 * (p & 3));
+                }
+                zw[2 * h] = w[0];
+                zw[2 * h + 1] = w[1];
             }
-            uint8_t* r = recs + (static_cast<size_t>(blk >> 3) * ng + g) * rec + (blk & 7) * block_bytes(kQtU4Zp);
-            uint32_t* zw = reinterpret_cast<uint32_t*>(r + kBlockZeroOff);
-            zw[0] = w[0];
-            zw[1] = w[1];
-            zw[2] = 0u;                                              // padding up to 1072 B
-            zw[3] = 0u;
+            // zero padding up to the block's end (8 B with one set, none with two)
+            for (int i = 2 * H; i < (block_bytes(kQtU4Zp, H) - block_zero_off(H)) / 4; ++i) zw[i] = 0u;
         } else {
             const int w = static_cast<int>(idx - n_scale - n_block);
             uint32_t v = 0;
@@ -131,10 +137,12 @@ __global__ void prepack_side_kernel(const uint16_t* __restrict__ scales, const v
     }
 }
 
-// Output row j (quantisation group j) is read from its first record, 128-K record j G / 128.
+// Output row j (quantisation group j) is read from the first record and scale set holding it:
+// record j G / 128, set (j G % 128) / 64.
 __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t* __restrict__ scales,
                                       void* __restrict__ zeros_out, int N, int K, int G, int zp) {
-    const int rec = tile_record_bytes(zp);
+    const int H = scale_sets(G);
+    const int rec = tile_record_bytes(zp, H);
     const int ng = K / 128, nq = K / G;
     const uint8_t* recs = blob + kBlobHeader;
     uint32_t* zeros = static_cast<uint32_t*>(zeros_out);
@@ -145,27 +153,27 @@ __global__ void unprepack_side_kernel(const uint8_t* __restrict__ blob, uint16_t
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
         if (idx < n_scale) {
             const int j = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
-            const int g = (j * G) / 128;
+            const int g = (j * G) / 128, h = ((j * G) % 128) / 64;
             const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            scales[idx] = *reinterpret_cast<const uint16_t*>(r + rec_scale_off(zp, n & 127));
+            scales[idx] = *reinterpret_cast<const uint16_t*>(r + rec_scale_off(zp, n & 127, H, h));
         } else if (zp == kQtU4FZp) {
             const long long z = idx - n_scale;
             const int j = static_cast<int>(z / N), n = static_cast<int>(z % N);
-            const int g = (j * G) / 128;
+            const int g = (j * G) / 128, h = ((j * G) % 128) / 64;
             const uint8_t* r = recs + (static_cast<size_t>(n >> 7) * ng + g) * rec;
-            fzeros[z] = *reinterpret_cast<const uint16_t*>(r + rec_fzero_off(zp, n & 127));
+            fzeros[z] = *reinterpret_cast<const uint16_t*>(r + rec_fzero_off(zp, n & 127, H, h));
         } else {
             // API word wz: rows 8 wz .. 8 wz + 7, the low (wz even) or high (wz odd) nibbles of a block
             const long long z = idx - n_scale;
             const int j = static_cast<int>(z / (N / 8)), wz = static_cast<int>(z % (N / 8));
-            const int g = (j * G) / 128;
+            const int g = (j * G) / 128, h = ((j * G) % 128) / 64;
             const int n0 = 8 * wz;
             const uint8_t* r = recs + (static_cast<size_t>(n0 >> 7) * ng + g) * rec;
             uint32_t out = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int rr = (n0 + i) & 127;
-                const uint32_t byte = r[rec_zero_off(kQtU4Zp, rr)];
+                const uint32_t byte = r[rec_zero_off(kQtU4Zp, rr, H, h)];
                 out |= ((byte >> (4 * ((rr >> 3) & 1))) & 0xFu) << (4 * i);
             }
             zeros[z] = out;
@@ -185,7 +193,7 @@ cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const void* z
     const int zp = qtype;
     uint8_t* b = static_cast<uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
-    prepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, b + kBlobHeader, N, K, zp);
+    prepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(wq, b + kBlobHeader, N, K, zp, scale_sets(G));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
@@ -199,7 +207,7 @@ cudaError_t launch_unprepack(const void* blob, int N, int K, int G, int qtype, u
     const int zp = qtype;
     const uint8_t* b = static_cast<const uint8_t*>(blob);
     const long long words = static_cast<long long>(N) * (K / 8);
-    unprepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(b + kBlobHeader, wq, N, K, zp);
+    unprepack_codes_kernel<<<grid_for(words, 256), 256, 0, st>>>(b + kBlobHeader, wq, N, K, zp, scale_sets(G));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long side = static_cast<long long>(K / 128) * N * 2;
