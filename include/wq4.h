@@ -185,6 +185,36 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
                             int group_size, int dtype, int qtype,
                             void* workspace, size_t workspace_bytes, wq4_stream_t stream);
 
+/* Grouped GEMM whose per-problem pointers live in device memory (written by a kernel on the same
+ * stream, for example the expert buffers of a token router): the grouped call of
+ * "sm90_gemm_array_tma_warpspecialized_cooperative.hpp" with its pointer arrays in device memory
+ * and any number of problems up to 4096.
+ *   M, N, K   HOST arrays of P shapes (the plan needs them); M[p] == 0 skips problem p (its
+ *             pointers are not read).
+ *   X_dev, Wp_dev, Y_dev   DEVICE arrays of P device pointers (8-byte aligned arrays), read when
+ *             the work starts (stream order); per-problem layouts as in wq4_mm.
+ *   group_size, dtype, qtype   shared by every problem; float zeros (WQ4_U4_FZP) are not
+ *             supported here (WQ4_ERR_UNSUPPORTED).
+ *   workspace  wq4_grouped_dev_ptrs_workspace_bytes(...) bytes, 128-byte aligned, zero-filled
+ *             before its first use (the K-split counters come first and are left at zero by
+ *             every call that completes; the rest, the problem table and one 128-byte activation
+ *             tensor map per problem, is rewritten by every call). Calls that share a workspace
+ *             must be in stream order.
+ * A set-up kernel on `stream` reads the pointers, checks each non-empty problem's pointers (non-null,
+ * 16-byte aligned) and blob header, writes its descriptor and its activation tensor map (encoded
+ * on the host for its shape, the X address replaced on the device); then the GEMM runs the
+ * plan wq4_grouped_mm would make for these shapes, reading the problems from the table. A problem
+ * that fails the device-side check is skipped (its Y is not written) and wq4_get_last_error then
+ * reports WQ4_ERR_INVALID; the other problems are computed. Host-side argument errors as
+ * wq4_grouped_mm, plus WQ4_ERR_ALIGN for a pointer array not 8-byte aligned or a workspace not
+ * 128-byte aligned. Results are bit-identical to wq4_grouped_mm's for the same problems. */
+int wq4_grouped_dev_ptrs_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
+                                         size_t* bytes);
+int wq4_grouped_mm_dev_ptrs(int P, const int* M, const int* N, const int* K,
+                            const void* const* X_dev, const void* const* Wp_dev, void* const* Y_dev,
+                            int group_size, int dtype, int qtype,
+                            void* workspace, size_t workspace_bytes, wq4_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------ *
  * Errors and options.
  * ------------------------------------------------------------------------------------------ */
@@ -228,6 +258,12 @@ int wq4_get_last_error(wq4_stream_t stream);
  *                           1024 K); 0 = automatic, 2..16 = forced
  *   WQ4_OPT_DECODE_TRIGGER  0 = the decode kernel lets the next kernel on the stream start once its
  *                           activations have landed (default), 1 = at once
+ *   WQ4_OPT_VERIFY_DEV_PTRS 1 = (tests) wq4_grouped_mm_dev_ptrs stops after its set-up kernels: it
+ *                           synchronises the stream, reads back the activation tensor maps they
+ *                           patched and compares each byte for byte with the map the host encoder
+ *                           makes for the same address and row count; WQ4_OK when every map
+ *                           matches, WQ4_ERR_UNSUPPORTED otherwise (the differing bytes printed
+ *                           under WQ4_OPT_TRACE). The GEMM is not launched. 0 = off
  * Returns WQ4_ERR_INVALID for an unknown key or value. */
 enum {
     WQ4_OPT_TOKEN_TILE = 1,
@@ -242,7 +278,8 @@ enum {
     WQ4_OPT_TEST_STALL = 10,
     WQ4_OPT_CONST_WEIGHTS = 11,
     WQ4_OPT_DECODE_DEPTH = 12,
-    WQ4_OPT_DECODE_TRIGGER = 13
+    WQ4_OPT_DECODE_TRIGGER = 13,
+    WQ4_OPT_VERIFY_DEV_PTRS = 14
 };
 int wq4_set_option(int key, long long value);
 long long wq4_get_option(int key);

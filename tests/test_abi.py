@@ -112,6 +112,26 @@ def test_grouped_argument_rules(clib):
     assert rc not in (wq4.ERR_INVALID, wq4.ERR_ALIGN)
 
 
+def test_dev_ptrs_argument_rules(clib):
+    """Host-side checks of wq4_grouped_mm_dev_ptrs: every one answers before any device work."""
+    g = clib.wq4_grouped_mm_dev_ptrs
+
+    def call(P=2, M=(8, 8), N=(128, 128), K=(128, 128), X=A16, W=A16b, Y=A16c, G=128, qt=0):
+        arr = ctypes.c_int * len(M)
+        return g(P, arr(*M), arr(*N), arr(*K), X, W, Y, G, 0, qt, None, 0, None)
+
+    assert call(P=0) == wq4.ERR_INVALID
+    assert call(P=4097, M=(8,) * 4097, N=(128,) * 4097, K=(128,) * 4097) == wq4.ERR_UNSUPPORTED
+    assert call(M=(8, -1)) == wq4.ERR_INVALID
+    assert call(N=(128, 96)) == wq4.ERR_UNSUPPORTED
+    assert call(K=(128, 384), G=256) == wq4.ERR_UNSUPPORTED
+    assert call(qt=2) == wq4.ERR_UNSUPPORTED                          # float zeros: single problems
+    assert call(X=None) == wq4.ERR_INVALID
+    assert call(Y=ctypes.c_void_p(0x10004)) == wq4.ERR_ALIGN           # pointer arrays: 8-byte aligned
+    rc = call(P=5, M=(1, 9, 300, 2, 0), N=(128,) * 5, K=(128, 256, 384, 512, 640))   # shapes all differ
+    assert rc not in (wq4.ERR_INVALID, wq4.ERR_ALIGN, wq4.ERR_UNSUPPORTED)
+
+
 def test_options(clib):
     assert clib.wq4_set_option(1, 64) == wq4.OK
     assert clib.wq4_get_option(1) == 64
@@ -134,5 +154,7 @@ def test_options(clib):
     assert clib.wq4_set_option(wq4.OPT_DECODE_DEPTH, 0) == wq4.OK
     assert clib.wq4_set_option(wq4.OPT_DECODE_TRIGGER, 2) == wq4.ERR_INVALID
     assert clib.wq4_set_option(wq4.OPT_DECODE_TRIGGER, 0) == wq4.OK
+    assert clib.wq4_set_option(wq4.OPT_VERIFY_DEV_PTRS, 2) == wq4.ERR_INVALID
+    assert clib.wq4_set_option(wq4.OPT_VERIFY_DEV_PTRS, 0) == wq4.OK
     assert clib.wq4_set_option(99, 1) == wq4.ERR_INVALID
     assert clib.wq4_get_option(99) == -1

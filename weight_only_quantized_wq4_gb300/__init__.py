@@ -21,7 +21,7 @@ DTYPES = {"bf16": 0, "fp16": 1}
 QTYPES = {"u4b8": 0, "u4_zp": 1, "u4_fzp": 2}
 OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM, OPT_CLUSTER = 1, 2, 3, 4, 5, 6, 7
 OPT_DECODE, OPT_PDL, OPT_TEST_STALL = 8, 9, 10
-OPT_CONST_WEIGHTS, OPT_DECODE_DEPTH, OPT_DECODE_TRIGGER = 11, 12, 13
+OPT_CONST_WEIGHTS, OPT_DECODE_DEPTH, OPT_DECODE_TRIGGER, OPT_VERIFY_DEV_PTRS = 11, 12, 13, 14
 GROUP = 128
 
 _lib = None
@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH):
         "wq4_mm_static_scratch": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp]),
         "wq4_grouped_device_m_workspace_bytes": (c_int, [c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm_device_m": (c_int, [c_int, vp, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_grouped_dev_ptrs_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
+        "wq4_grouped_mm_dev_ptrs": (c_int, [c_int, ip, ip, ip, vp, vp, vp, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_get_last_error": (c_int, [vp]),
         "wq4_set_option": (c_int, [c_int, ll]),
         "wq4_get_option": (ll, [c_int]),
@@ -280,3 +282,36 @@ def grouped_mm_device_m(Xs: Sequence, blobs: Sequence, M_dev, N: Sequence[int], 
                                        _dtype_code(Xs[0]), QTYPES[qtype], _cuda(workspace, "workspace"),
                                        workspace.numel(), _stream(Xs[0].device)), "wq4_grouped_mm_device_m")
     return list(outs)
+
+
+def grouped_dev_ptrs_workspace_bytes(M: Sequence[int], N: Sequence[int], K: Sequence[int],
+                                     group_size: int = GROUP) -> int:
+    """Workspace of wq4_grouped_mm_dev_ptrs for these shapes."""
+    P = len(M)
+    arr = ctypes.c_int * P
+    nb = ctypes.c_size_t(0)
+    _check(load_library().wq4_grouped_dev_ptrs_workspace_bytes(P, arr(*M), arr(*N), arr(*K), group_size,
+                                                                ctypes.byref(nb)),
+           "wq4_grouped_dev_ptrs_workspace_bytes")
+    return int(nb.value)
+
+
+def grouped_mm_dev_ptrs(M: Sequence[int], N: Sequence[int], K: Sequence[int], X_ptrs, W_ptrs, Y_ptrs,
+                        dtype: str = "bf16", qtype: str = "u4b8", workspace=None, group_size: int = GROUP):
+    """Grouped GEMM whose per-problem pointers are in device memory: X_ptrs, W_ptrs, Y_ptrs are int64
+    CUDA tensors [P] of device addresses (written by any kernel earlier on the stream); the shapes
+    M, N, K are host lists. Results land in the Y buffers the addresses name."""
+    torch = _torch()
+    lib = load_library()
+    P = len(M)
+    for t, nm in ((X_ptrs, "X_ptrs"), (W_ptrs, "W_ptrs"), (Y_ptrs, "Y_ptrs")):
+        if t.dtype != torch.int64 or not t.is_cuda or t.numel() != P:
+            raise ValueError("%s must be an int64 CUDA tensor with one address per problem" % nm)
+    dev = X_ptrs.device
+    if workspace is None:
+        workspace = alloc_workspace(grouped_dev_ptrs_workspace_bytes(M, N, K, group_size), dev)
+    arr = ctypes.c_int * P
+    _check(lib.wq4_grouped_mm_dev_ptrs(P, arr(*M), arr(*N), arr(*K), _cuda(X_ptrs, "X_ptrs"), _cuda(W_ptrs, "W_ptrs"),
+                                       _cuda(Y_ptrs, "Y_ptrs"), group_size, DTYPES[dtype], QTYPES[qtype],
+                                       _cuda(workspace, "workspace"), workspace.numel(), _stream(dev)),
+           "wq4_grouped_mm_dev_ptrs")

@@ -23,10 +23,13 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "wq4.h"
+#include "wq4_device.cuh"
 #include "wq4_launch.h"
 #include "wq4_params.h"
 
@@ -53,6 +56,7 @@ struct Options {
     int const_weights = 0;    // 1: blobs are not written by pending work; weights are read early
     int decode_depth = 0;     // decode weight ring slots, 0 = automatic
     int decode_trigger = 0;   // 0: the next kernel is let in once the activations landed, 1: at once
+    int verify_dev_ptrs = 0;  // 1: the device-pointer grouped call stops after its set-up and checks its maps
 };
 Options g_opt;
 
@@ -182,9 +186,9 @@ struct Plan {
     int cluster = 0;
     size_t counters_bytes = 0;
     size_t partials_bytes = 0;
-    int m_tiles[kMaxGroupedProblems] = {};
-    int tile_begin[kMaxGroupedProblems] = {};
-    int unit_begin[kMaxGroupedProblems] = {};
+    int m_tiles[kMaxDevPtrProblems] = {};
+    int tile_begin[kMaxDevPtrProblems] = {};
+    int unit_begin[kMaxDevPtrProblems] = {};
     size_t workspace() const { return counters_bytes + partials_bytes; }
 };
 
@@ -217,7 +221,7 @@ int token_tile_for(const int* M, int P) {
 // With two scale sets per record (group size 64) a tile's partials take twice the tensor-memory
 // columns: at most 64 tokens then.
 int pick_token_tile(const Shape* shapes, int P, int group_size) {
-    int Ms[kMaxGroupedProblems];
+    int Ms[kMaxDevPtrProblems];
     for (int p = 0; p < P; ++p) Ms[p] = shapes[p].M;
     const int nt = token_tile_for(Ms, P);
     return scale_sets(group_size) == 2 && nt > 64 ? 64 : nt;
@@ -457,6 +461,7 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
         d.k_groups = shapes[p].K / kTileK;
         d.tile_begin = pl.tile_begin[p];
         d.unit_begin = pl.unit_begin[p];
+        d.valid = 1;
         if (d.M > 0) {
             rc = encode_x_map(&prm->xmap[p], X[p], d.M, d.K, dtype, pl.nt);
             if (rc) return rc;
@@ -758,6 +763,60 @@ __global__ void dyn_table_kernel(const int* __restrict__ M_dev, const __grid_con
 }
 }  // namespace wq4
 
+namespace wq4 {
+// Device-resident per-problem pointers: one thread per problem of this launch's chunk writes the
+// problem's descriptor (pointers read from the device arrays, shape and tile ranges from the
+// launch parameters) and, for a non-empty problem, its activation tensor map: the map the host
+// encoded for its shape copied into the table, then its global address replaced in place
+// (tensormap.replace) and released to the tensor-map proxy. A null or misaligned pointer,
+// or a blob whose header does not match the call, marks the problem invalid (the GEMM skips its
+// tiles) and sets the status word's bad-argument bit.
+__global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup su, const void* const* __restrict__ X,
+                                 const void* const* __restrict__ W, void* const* __restrict__ Y,
+                                 ProblemDesc* __restrict__ tab, CUtensorMap* __restrict__ maps,
+                                 unsigned int* status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= su.count) return;
+    const int p = su.p0 + i;
+    ProblemDesc d;
+    memset(&d, 0, sizeof(d));
+    d.M = su.M[i];
+    d.N = su.N[i];
+    d.K = su.K[i];
+    d.n_tiles = su.N[i] / kTileN;
+    d.m_tiles = su.m_tiles[i];
+    d.k_groups = su.K[i] / kTileK;
+    d.tile_begin = su.tile_begin[i];
+    d.unit_begin = su.unit_begin[i];
+    d.valid = 1;
+    if (d.M > 0) {
+        const void* x = X[p];
+        const void* w = W[p];
+        void* y = Y[p];
+        const bool ok = x && w && y &&
+                        ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
+                          reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
+                        blob_header_ok(static_cast<const uint32_t*>(w), d.N, d.K, su.group_size, su.dtype, su.qtype);
+        if (ok) {
+            d.wp = static_cast<const uint8_t*>(w) + kBlobHeader;
+            d.y = y;
+            const uint4* src = reinterpret_cast<const uint4*>(&su.tmpl[i]);
+            uint4* dst = reinterpret_cast<uint4*>(&maps[p]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dst[k] = src[k];
+            asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
+                         "l"(reinterpret_cast<uint64_t>(x))
+                         : "memory");
+            asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+        } else {
+            d.valid = 0;
+            atomicOr(status, kStatusBadBlob);
+        }
+    }
+    tab[p] = d;
+}
+}  // namespace wq4
+
 int wq4_grouped_device_m_workspace_bytes(int P, size_t* bytes) {
     if (!bytes || P <= 0) return WQ4_ERR_INVALID;
     if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
@@ -810,6 +869,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
         d.m_tiles = (M_cap[p] + nt - 1) / nt;
         d.k_groups = K[p] / kTileK;
         d.tile_begin = static_cast<int>(max_tiles);
+        d.valid = 1;
         max_tiles += static_cast<long long>(d.m_tiles) * d.n_tiles;
         su.cap[p] = M_cap[p];
         su.n_tiles[p] = d.n_tiles;
@@ -845,6 +905,169 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
         std::fprintf(stderr, "[wq4] device-resident shapes: problems=%d token_tile=%d grid=%d max_tiles=%lld (%s)\n", P,
                      nt, grid, max_tiles, e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     delete prm;
+    return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ device-resident pointers
+namespace wq4 {
+namespace {
+// Workspace of the device-pointer grouped call: the plan's K-split part (counters first, zero
+// between calls), then the problem table, then one 128-byte activation map per problem.
+struct PtrLayout {
+    size_t tab_off, map_off, total;
+};
+PtrLayout ptr_layout(const Plan& pl, int P) {
+    PtrLayout L;
+    L.tab_off = (pl.workspace() + 255) / 256 * 256;
+    L.map_off = (L.tab_off + static_cast<size_t>(P) * sizeof(ProblemDesc) + 127) / 128 * 128;
+    L.total = L.map_off + static_cast<size_t>(P) * sizeof(CUtensorMap);
+    return L;
+}
+
+int ptr_shapes(int P, const int* M, const int* N, const int* K, int group_size, Shape* shapes) {
+    int rc = WQ4_OK;
+    for (int p = 0; p < P; ++p) {
+        if (M[p] < 0) return WQ4_ERR_INVALID;
+        if ((rc = check_nk(N[p], K[p]))) return rc;
+        if ((rc = check_group(group_size, K[p]))) return rc;
+        shapes[p] = Shape{M[p], N[p], K[p]};
+    }
+    return WQ4_OK;
+}
+
+// Reads back the maps the set-up kernels wrote and compares each with the host encoder's map for
+// the same address and row count (the test aid of WQ4_OPT_VERIFY_DEV_PTRS).
+int verify_ptr_maps(int P, const Shape* shapes, const void* const* X_dev, const uint8_t* maps_dev, int dtype, int nt,
+                    cudaStream_t st) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return WQ4_ERR_CUDA;
+    std::vector<const void*> xs(P);
+    std::vector<uint8_t> got(static_cast<size_t>(P) * sizeof(CUtensorMap));
+    if (cudaMemcpy(xs.data(), X_dev, sizeof(void*) * P, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(got.data(), maps_dev, got.size(), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return WQ4_ERR_CUDA;
+    int bad = 0;
+    for (int p = 0; p < P; ++p) {
+        if (shapes[p].M == 0 || !xs[p] || !aligned16(xs[p])) continue;
+        CUtensorMap want;
+        const int rc = encode_x_map(&want, xs[p], shapes[p].M, shapes[p].K, dtype, nt);
+        if (rc) return rc;
+        const uint8_t* g = got.data() + static_cast<size_t>(p) * sizeof(CUtensorMap);
+        const uint8_t* w = reinterpret_cast<const uint8_t*>(&want);
+        const int bad_before = bad;
+        for (size_t b = 0; b < sizeof(CUtensorMap); ++b) bad += g[b] != w[b];
+        if (trace_on() && bad != bad_before)
+            std::fprintf(stderr, "[wq4] map %d differs: X=%p M=%d K=%d\n", p, xs[p], shapes[p].M, shapes[p].K);
+        if (trace_on() && bad != bad_before && bad_before == 0) {   // the first mismatching map in full
+            std::fprintf(stderr, "[wq4] problem %d (M=%d K=%d, X=%p): map bytes differ\n", p, shapes[p].M, shapes[p].K,
+                         xs[p]);
+            for (int row = 0; row < 8; ++row) {
+                std::fprintf(stderr, "[wq4]  %3d device", row * 16);
+                for (int b = 0; b < 16; ++b) std::fprintf(stderr, " %02x", g[row * 16 + b]);
+                std::fprintf(stderr, "\n[wq4]      host  ");
+                for (int b = 0; b < 16; ++b) std::fprintf(stderr, " %02x", w[row * 16 + b]);
+                std::fprintf(stderr, "\n");
+            }
+        }
+    }
+    if (trace_on() && bad) std::fprintf(stderr, "[wq4] %d map bytes differ in all\n", bad);
+    return bad ? WQ4_ERR_UNSUPPORTED : WQ4_OK;
+}
+}  // namespace
+}  // namespace wq4
+
+int wq4_grouped_dev_ptrs_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
+                                         size_t* bytes) {
+    if (!bytes || P <= 0 || !M || !N || !K) return WQ4_ERR_INVALID;
+    if (P > kMaxDevPtrProblems) return WQ4_ERR_UNSUPPORTED;
+    int rc = check_types(group_size, WQ4_BF16, WQ4_U4B8);
+    if (rc) return rc;
+    std::vector<Shape> shapes(P);
+    if ((rc = ptr_shapes(P, M, N, K, group_size, shapes.data()))) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    auto pl = std::make_unique<Plan>();
+    if ((rc = make_plan(shapes.data(), P, dev->sm_count, SIZE_MAX, group_size, pl.get()))) return rc;
+    *bytes = ptr_layout(*pl, P).total;
+    return WQ4_OK;
+}
+
+int wq4_grouped_mm_dev_ptrs(int P, const int* M, const int* N, const int* K, const void* const* X_dev,
+                            const void* const* Wp_dev, void* const* Y_dev, int group_size, int dtype, int qtype,
+                            void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
+    int rc = check_types(group_size, dtype, qtype);
+    if (rc) return rc;
+    if (P <= 0 || !M || !N || !K || !X_dev || !Wp_dev || !Y_dev) return WQ4_ERR_INVALID;
+    if (P > kMaxDevPtrProblems || qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(X_dev) | reinterpret_cast<uintptr_t>(Wp_dev) |
+         reinterpret_cast<uintptr_t>(Y_dev)) & 7u)
+        return WQ4_ERR_ALIGN;
+    std::vector<Shape> shapes(P);
+    if ((rc = ptr_shapes(P, M, N, K, group_size, shapes.data()))) return rc;
+    DeviceInfo* dev = nullptr;
+    if ((rc = device_info(&dev))) return rc;
+    auto pl = std::make_unique<Plan>();
+    if ((rc = make_plan(shapes.data(), P, dev->sm_count, SIZE_MAX, group_size, pl.get()))) return rc;
+    if (pl->total_tiles == 0) return WQ4_OK;
+    const PtrLayout L = ptr_layout(*pl, P);
+    if (!workspace || workspace_bytes < L.total) return WQ4_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 127u) return WQ4_ERR_ALIGN;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto* tab = reinterpret_cast<ProblemDesc*>(ws + L.tab_off);
+    auto* maps = reinterpret_cast<CUtensorMap*>(ws + L.map_off);
+
+    auto su = std::make_unique<PtrSetup>();
+    std::memset(static_cast<void*>(su.get()), 0, sizeof(PtrSetup));
+    su->group_size = group_size;
+    su->dtype = dtype;
+    su->qtype = qtype;
+    for (int p0 = 0; p0 < P; p0 += kPtrSetupChunk) {
+        const int cnt = std::min(kPtrSetupChunk, P - p0);
+        su->p0 = p0;
+        su->count = cnt;
+        for (int i = 0; i < cnt; ++i) {
+            const int p = p0 + i;
+            su->M[i] = M[p];
+            su->N[i] = N[p];
+            su->K[i] = K[p];
+            su->m_tiles[i] = pl->m_tiles[p];
+            su->tile_begin[i] = pl->tile_begin[p];
+            su->unit_begin[i] = pl->unit_begin[p];
+            // the stand-in address (the workspace: any 16-byte aligned one) is replaced on the device
+            if (M[p] > 0 && (rc = encode_x_map(&su->tmpl[i], workspace, M[p], K[p], dtype, pl->nt))) return rc;
+        }
+        ptr_setup_kernel<<<(cnt + 127) / 128, 128, 0, stream>>>(*su, X_dev, Wp_dev, Y_dev, tab, maps, dev->status);
+        if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
+    }
+    if (g_opt.verify_dev_ptrs)
+        return verify_ptr_maps(P, shapes.data(), X_dev, ws + L.map_off, dtype, pl->nt, stream);
+
+    GemmParams<1> prm;
+    std::memset(static_cast<void*>(&prm), 0, sizeof(prm));
+    prm.prob_tab = tab;
+    prm.xmap_tab = maps;
+    prm.num_problems = P;
+    prm.group_size = group_size;
+    prm.dtype = dtype;
+    prm.qtype = qtype;
+    prm.nib = nibble_consts(dtype == WQ4_BF16);
+    prm.total_tiles = pl->total_tiles;
+    prm.dp_tiles = pl->dp_tiles;
+    prm.num_ctas = pl->grid;
+    prm.sk_unit_begin = pl->sk_unit_begin;
+    prm.sk_units = pl->sk_units;
+    prm.cluster_split = pl->cluster;
+    prm.counters = pl->counters_bytes ? reinterpret_cast<int*>(ws) : nullptr;
+    prm.partials = pl->partials_bytes ? reinterpret_cast<float*>(ws + pl->counters_bytes) : nullptr;
+    prm.status = dev->status;
+    prm.timeout_cycles = timeout_cycles();
+    prm.test_stall = g_opt.test_stall;
+    const cudaError_t e = dispatch(&prm, false, pl->nt, dtype, qtype, group_size, pl->grid, stream);
+    if (trace_on())
+        std::fprintf(stderr,
+                     "[wq4] device pointers: problems=%d token_tile=%d grid=%d cluster=%d tiles=%d "
+                     "dp_tiles=%d sk_units=%d ws=%zu (%s)\n",
+                     P, pl->nt, pl->grid, pl->cluster, pl->total_tiles, pl->dp_tiles, pl->sk_units, L.total,
+                     e == cudaSuccess ? "ok" : cudaGetErrorString(e));
     return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
 }
 
@@ -916,6 +1139,10 @@ int wq4_set_option(int key, long long value) {
             if (value < 0 || value > 1) return WQ4_ERR_INVALID;
             g_opt.decode_trigger = static_cast<int>(value);
             return WQ4_OK;
+        case WQ4_OPT_VERIFY_DEV_PTRS:
+            if (value < 0 || value > 1) return WQ4_ERR_INVALID;
+            g_opt.verify_dev_ptrs = static_cast<int>(value);
+            return WQ4_OK;
         default: return WQ4_ERR_INVALID;
     }
 }
@@ -935,6 +1162,7 @@ long long wq4_get_option(int key) {
         case WQ4_OPT_CONST_WEIGHTS: return g_opt.const_weights;
         case WQ4_OPT_DECODE_DEPTH: return g_opt.decode_depth;
         case WQ4_OPT_DECODE_TRIGGER: return g_opt.decode_trigger;
+        case WQ4_OPT_VERIFY_DEV_PTRS: return g_opt.verify_dev_ptrs;
         default: return -1;
     }
 }

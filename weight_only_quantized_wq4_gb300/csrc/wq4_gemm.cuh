@@ -113,6 +113,17 @@ struct Seg {
 };
 constexpr int kSlotCluster = -2;
 
+// Problem p's descriptor and activation map: from the kernel parameters, or from the tables a
+// set-up kernel wrote into the workspace (device-resident per-problem pointers).
+template <int MAXP>
+__device__ __forceinline__ const ProblemDesc& prob_at(const GemmParams<MAXP>& prm, int p) {
+    return prm.prob_tab ? prm.prob_tab[p] : prm.prob[p];
+}
+template <int MAXP>
+__device__ __forceinline__ const CUtensorMap* xmap_at(const GemmParams<MAXP>& prm, int p) {
+    return prm.xmap_tab ? &prm.xmap_tab[p] : &prm.xmap[p];
+}
+
 template <int MAXP>
 struct Sched {
     const GemmParams<MAXP>& prm;
@@ -128,18 +139,25 @@ struct Sched {
     }
 
     // first tile of problem p: from the parameters, or from the device table
-    __device__ int tile_begin(int p) const { return prm.dyn ? prm.dyn->tile_begin[p] : prm.prob[p].tile_begin; }
+    __device__ int tile_begin(int p) const { return prm.dyn ? prm.dyn->tile_begin[p] : prob_at(prm, p).tile_begin; }
 
+    // the last problem whose first tile (unit) is <= t (v): a binary search (begins are non-decreasing)
     __device__ int problem_of_tile(int t) const {
-        int p = 0;
-        while (p + 1 < prm.num_problems && tile_begin(p + 1) <= t) ++p;
-        return p;
+        int lo = 0, hi = prm.num_problems - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tile_begin(mid) <= t) lo = mid; else hi = mid - 1;
+        }
+        return lo;
     }
 
     __device__ int problem_of_unit(int v) const {
-        int p = 0;
-        while (p + 1 < prm.num_problems && prm.prob[p + 1].unit_begin <= v) ++p;
-        return p;
+        int lo = 0, hi = prm.num_problems - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prob_at(prm, mid).unit_begin <= v) lo = mid; else hi = mid - 1;
+        }
+        return lo;
     }
 
     __device__ bool next(Seg& s) {
@@ -149,7 +167,8 @@ struct Sched {
             const int S = prm.cluster_split;
             const int t = cta / S, q = cta % S;
             const int p = problem_of_tile(t);
-            const ProblemDesc& P = prm.prob[p];
+            const ProblemDesc& P = prob_at(prm, p);
+            if (!P.valid) return false;
             const int local = t - P.tile_begin;
             s.prob = p;
             s.tile = t;
@@ -160,11 +179,12 @@ struct Sched {
             s.slot = kSlotCluster;
             return true;
         }
-        if (dp_t < (prm.dyn ? prm.dyn->total_tiles : prm.dp_tiles)) {
+        while (dp_t < (prm.dyn ? prm.dyn->total_tiles : prm.dp_tiles)) {
             const int t = dp_t;
             dp_t += prm.num_ctas;
             const int p = problem_of_tile(t);
-            const ProblemDesc& P = prm.prob[p];
+            const ProblemDesc& P = prob_at(prm, p);
+            if (!P.valid) continue;                      // every role skips the same tiles
             const int local = t - tile_begin(p);
             s.prob = p;
             s.tile = t;
@@ -175,14 +195,18 @@ struct Sched {
             s.slot = -1;
             return true;
         }
-        if (u < u_end) {
+        while (u < u_end) {
             const int p = problem_of_unit(u);
-            const ProblemDesc& P = prm.prob[p];
+            const ProblemDesc& P = prob_at(prm, p);
             const int local = u - P.unit_begin;
             const int tl = local / P.k_groups;
             const int g = local - tl * P.k_groups;
             const int left = u_end - u;
             const int take = left < (P.k_groups - g) ? left : (P.k_groups - g);
+            if (!P.valid) {
+                u += take;
+                continue;
+            }
             s.prob = p;
             s.tile = P.tile_begin + tl;
             s.mt = tl / P.n_tiles;
@@ -202,7 +226,7 @@ struct Sched {
 // Rows (tokens) of problem p: from the parameters, or from the device table.
 template <int MAXP>
 __device__ __forceinline__ int problem_rows(const GemmParams<MAXP>& prm, int p) {
-    return prm.dyn ? prm.dyn->M[p] : prm.prob[p].M;
+    return prm.dyn ? prm.dyn->M[p] : prob_at(prm, p).M;
 }
 
 // CTA whose K-split range holds split-relative unit v (ranges [floor(c U / C), floor((c+1) U / C))).
@@ -359,7 +383,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         *fin_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && !prm.prob_tab) {      // (device tables: written by the kernel ahead)
         for (int p = 0; p < prm.num_problems; ++p) {
             if (prm.prob[p].m_tiles > 0) prefetch_tensormap(&prm.xmap[p]);   // empty problems have no map
         }
@@ -387,15 +411,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     // Every problem's blob header against the call: by the weight producer's warp before its first
     // record copy, or (blobs prepacked here for these arguments) by lanes 1..31 of MMA warp 1 while
     // the copies already stream; a mismatch stops the CTA and is reported as WQ4_ERR_INVALID.
+    // (Device tables: the set-up kernel checked every header and marked mismatches invalid.)
     bool hdr_ok = true;
     const bool hdr_alongside = prm.hdr_trusted != 0;
-    if ((warp == 2 && !hdr_alongside) || (warp == 1 && hdr_alongside && lane > 0)) {
+    if (!prm.prob_tab && ((warp == 2 && !hdr_alongside) || (warp == 1 && hdr_alongside && lane > 0))) {
         const unsigned int mask = hdr_alongside ? 0xfffffffeu : 0xffffffffu;
         const int l0 = hdr_alongside ? 1 : 0, nl = hdr_alongside ? 31 : 32;
         bool mine = true;
         for (int p = lane - l0; p < prm.num_problems; p += nl) {
-            const ProblemDesc& P = prm.prob[p];
-            if (P.m_tiles > 0)
+            const ProblemDesc& P = prob_at(prm, p);
+            if (P.m_tiles > 0 && P.valid)
                 mine = blob_header_ok(reinterpret_cast<const uint32_t*>(P.wp - kBlobHeader), P.N, P.K, prm.group_size,
                                       prm.dtype, prm.qtype) && mine;
         }
@@ -418,12 +443,20 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
             int i = 0;
+            int last_prob = -1;
             bool ok = hdr_ok;
             while (ok && sch.next(seg)) {
-                const ProblemDesc& P = prm.prob[seg.prob];
+                const ProblemDesc& P = prob_at(prm, seg.prob);
                 const uint64_t pol_w = P.m_tiles == 1 ? pol_stream : pol_keep;
                 const uint8_t* wrec = P.wp + (static_cast<size_t>(seg.nt) * P.k_groups + seg.g0) * C::kRec;
-                const CUtensorMap* xmap = &prm.xmap[seg.prob];
+                const CUtensorMap* xmap = xmap_at(prm, seg.prob);
+                if (is_x && prm.xmap_tab && seg.prob != last_prob) {
+                    // a map patched in global memory by the set-up kernel: acquire it for the
+                    // tensor-map proxy before the first copy that uses it
+                    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(xmap))
+                                 : "memory");
+                    last_prob = seg.prob;
+                }
                 for (int g = seg.g0; g < seg.g1; ++g, ++i, wrec += C::kRec) {
                     const int s = i % depth;
                     const uint32_t par = ((i / depth) & 1) ^ 1;
@@ -459,7 +492,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             // (tests) a wait that nothing ends: it runs out, records the timeout, stops the CTA
             bool ok = !(prm.test_stall && mine == 0) || mbar_wait(stall_bar, 0, ctl);
             while (ok && sch.next(seg)) {
-                const ProblemDesc& P = prm.prob[seg.prob];
+                const ProblemDesc& P = prob_at(prm, seg.prob);
                 const int rows = problem_rows(prm, seg.prob) - seg.mt * NT;
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
@@ -585,6 +618,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         };
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
+        seg.prob = -1;                                   // stays -1 if the CTA gets no tile
         int i = 0;
         bool ok = true;
         while (ok && sch.next(seg)) {
@@ -659,7 +693,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             if (!ok) break;
 
             // ---------------------------------------------------------- tile epilogue
-            const ProblemDesc& P = prm.prob[seg.prob];
+            const ProblemDesc& P = prob_at(prm, seg.prob);
             const int Mrows = problem_rows(prm, seg.prob);
             const int n = seg.nt * kTileN + r;
             const int m0 = seg.mt * NT + col0;
@@ -736,11 +770,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
         if (prm.cluster_split > 0) {
             cluster_sync();   // every rank's partial is in its shared memory
-            {
+            if (seg.prob >= 0) {   // (the whole cluster skips a tile of a problem marked invalid)
                 // Each rank of the cluster adds the S partials (in rank order) for its own slice of
                 // the token columns, [rank NT / S, (rank + 1) NT / S), and writes that slice of Y:
                 // the reads through distributed shared memory are spread over the cluster.
-                const ProblemDesc& P = prm.prob[seg.prob];
+                const ProblemDesc& P = prob_at(prm, seg.prob);
                 const int Mrows = P.M;
                 const int S = prm.cluster_split;
                 const int q = static_cast<int>(cluster_rank());

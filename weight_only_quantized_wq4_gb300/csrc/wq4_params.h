@@ -66,7 +66,26 @@ struct ProblemDesc {
     int k_groups;            // K / 128
     int tile_begin;          // global index of the problem's first tile
     int unit_begin;          // global index of the problem's first (tile, group) unit
+    int valid;               // 0: its pointers failed the device-side check (its tiles are skipped)
+    int pad;
 };
+
+// Per-problem pointers in device memory (wq4_grouped_mm_dev_ptrs): a set-up kernel on the stream
+// writes each problem's descriptor and activation tensor map into the workspace (any number of
+// problems up to kMaxDevPtrProblems); the GEMM reads them from there instead of its parameters.
+constexpr int kMaxDevPtrProblems = 4096;
+constexpr int kPtrSetupChunk = 128;       // problems per set-up launch (its parameters hold their maps)
+struct PtrSetup {
+    // Problem i's activation map, encoded on the host for its rows and K with a stand-in address;
+    // the set-up kernel replaces only the global address. (The encoder also derives a flag from the
+    // tensor's total size, which replacing the row count on the device would leave stale.)
+    CUtensorMap tmpl[kPtrSetupChunk];
+    int p0, count;                        // problems [p0, p0 + count) of this launch
+    int group_size, dtype, qtype;         // what every blob header must say
+    int M[kPtrSetupChunk], N[kPtrSetupChunk], K[kPtrSetupChunk];
+    int m_tiles[kPtrSetupChunk], tile_begin[kPtrSetupChunk], unit_begin[kPtrSetupChunk];
+};
+static_assert(sizeof(PtrSetup) <= 32000, "kernel parameter space");
 
 // Problem sizes known only on the device (tokens routed to experts by a kernel): a set-up kernel
 // writes this table from the device array of token counts; the GEMM then reads M, the tile counts
@@ -124,6 +143,8 @@ struct GemmParams {
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
     const float* xsum;       // float-zero mode: xsum[g][m] = sum of X[m][128 g .. 128 g + 127] (fp32),
     int xsum_ld;             // rows of xsum_ld >= m_tiles * token tile floats (zero past M)
+    const ProblemDesc* prob_tab;    // device-resident problem table (num_problems entries), or null
+    const CUtensorMap* xmap_tab;    // their activation tensor maps (patched on the device), or null
 };
 
 }  // namespace wq4
