@@ -23,6 +23,7 @@ Variants of a workload (measured like the workload itself; the default line uses
   --epilogue                     Y = X.dequant(W)^T + C + bias through wq4_mm_ex (C, bias read)
   --float-zeros                  the workload's weight in the float-zero format (value = q s + zf)
   --device-m                     grouped workload with its token counts in device memory
+  --dev-ptrs                     grouped workload with its X / W / Y pointers in device memory
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own replica of the workload
 (weak scaling; the GEMM needs no exchange) and value = all ranks' work / max time.
@@ -85,6 +86,8 @@ def variant_of(args):
         v["epilogue"] = "Y = acc + C + bias (wq4_mm_ex)"
     if args.device_m:
         v["token_counts"] = "device memory (wq4_grouped_mm_device_m)"
+    if getattr(args, "dev_ptrs", False):
+        v["pointers"] = "device memory (wq4_grouped_mm_dev_ptrs)"
     if getattr(args, "float_zeros", False):
         v["qtype"] = "u4_fzp (value = q s + zf, float zero per group and row)"
     return v
@@ -203,13 +206,17 @@ class Workload:
         self.args = args
         self.dev = dev
         vargs = args if use_variant else argparse.Namespace(group_size=I.GROUP, no_scales=False, epilogue=False,
-                                                           device_m=False, float_zeros=False, workload=name)
+                                                           device_m=False, float_zeros=False, dev_ptrs=False,
+                                                           workload=name)
         self.vargs = vargs
         probs = make_inputs(argparse.Namespace(**dict(vars(vargs), workload=name)))
         self.probs = probs
         self.grouped = isinstance(probs, list)
-        if vargs.device_m and not self.grouped:
-            raise SystemExit("--device-m applies to the grouped workload")
+        dev_ptrs = getattr(vargs, "dev_ptrs", False)
+        if (vargs.device_m or dev_ptrs) and not self.grouped:
+            raise SystemExit("--device-m and --dev-ptrs apply to the grouped workload")
+        if vargs.device_m and dev_ptrs:
+            raise SystemExit("--device-m and --dev-ptrs are separate calls")
         plist = probs if self.grouped else [probs]
         self.plist = plist
         byts, flops, cfg, dtype = workload_shapes(name, probs)
@@ -248,6 +255,9 @@ class Workload:
         qtype = plist[0].qtype
         if vargs.device_m:
             self.ws_bytes = wq4.grouped_device_m_workspace_bytes(len(plist))
+        elif dev_ptrs:
+            self.ws_bytes = wq4.grouped_dev_ptrs_workspace_bytes([p.M for p in plist], [p.N for p in plist],
+                                                                 [p.K for p in plist], G)
         elif self.grouped:
             self.ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
         else:
@@ -268,8 +278,26 @@ class Workload:
         torch.cuda.synchronize()
         grouped = self.grouped
 
+        ptr_arrays = {}     # device pointer arrays per set of buffers, made before any timing or capture
+
+        def dev_ptr_arrays(Xs, Ws, Ys):
+            key = tuple(t.data_ptr() for t in Xs + Ws + Ys)
+            if key not in ptr_arrays:
+                ptr_arrays[key] = [torch.tensor([t.data_ptr() for t in ts], dtype=torch.int64, device=dev)
+                                   for ts in (Xs, Ws, Ys)]
+            return ptr_arrays[key]
+
+        if dev_ptrs:
+            for Xs, Ws, Ys, _, _ in self.copies:
+                dev_ptr_arrays(Xs, Ws, Ys)
+        self.dev_ptr_arrays = dev_ptr_arrays
+
         def call(Xs, Ws, Ys, ws, Cs, bias):
-            if vargs.device_m:
+            if dev_ptrs:
+                wq4.grouped_mm_dev_ptrs([p.M for p in plist], [p.N for p in plist], [p.K for p in plist],
+                                        *dev_ptr_arrays(Xs, Ws, Ys), dtype=dtype, qtype=qtype, workspace=ws,
+                                        group_size=G)
+            elif vargs.device_m:
                 wq4.grouped_mm_device_m(Xs, Ws, M_dev, [p.N for p in plist], qtype=qtype, workspace=ws, outs=Ys,
                                         group_size=G)
             elif grouped:
@@ -281,7 +309,8 @@ class Workload:
                 wq4.mm(Xs[0], Ws[0], plist[0].N, qtype=qtype, workspace=ws, out=Ys[0], group_size=G)
 
         self.call = call
-        self.launches_per_step = 2 if vargs.device_m else 1     # device counts: the tile-table kernel too
+        # device counts: the tile-table kernel too; device pointers: one set-up launch per 128 problems
+        self.launches_per_step = 2 if vargs.device_m else (1 + (len(plist) + 127) // 128 if dev_ptrs else 1)
 
     def step(self, c):
         Xs, Ws, Ys, ws, Cs = self.copies[c % self.R]
@@ -636,6 +665,7 @@ def main():
     ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
     ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")
     ap.add_argument("--device-m", action="store_true", help="variant: grouped token counts in device memory")
+    ap.add_argument("--dev-ptrs", action="store_true", help="variant: grouped X / W / Y pointers in device memory")
     ap.add_argument("--float-zeros", action="store_true", help="variant: the weight in the float-zero format")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up and the timed replay (for profiler runs): no soak, e2e or CPU baseline")

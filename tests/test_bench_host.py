@@ -54,6 +54,9 @@ def test_variant_rules():
         bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", epilogue=True))
     g = bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", device_m=True))
     assert isinstance(g, list) and sum(p.M for p in g) == 1024
+    a = _args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", dev_ptrs=True)
+    assert bench.variant_of(a) == {"pointers": "device memory (wq4_grouped_mm_dev_ptrs)"}
+    assert sum(p.M for p in bench.make_inputs(a)) == 1024
 
 
 def test_reference_arm_line(capsys):

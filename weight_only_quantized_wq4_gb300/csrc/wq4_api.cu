@@ -763,6 +763,7 @@ __global__ void dyn_table_kernel(const int* __restrict__ M_dev, const __grid_con
 }
 }  // namespace wq4
 
+extern "C++" {
 namespace wq4 {
 // Device-resident per-problem pointers: one thread per problem of this launch's chunk writes the
 // problem's descriptor (pointers read from the device arrays, shape and tile ranges from the
@@ -771,10 +772,16 @@ namespace wq4 {
 // (tensormap.replace) and released to the tensor-map proxy. A null or misaligned pointer,
 // or a blob whose header does not match the call, marks the problem invalid (the GEMM skips its
 // tiles) and sets the status word's bad-argument bit.
-__global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup su, const void* const* __restrict__ X,
+template <int C>
+__global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup<C> su, const void* const* __restrict__ X,
                                  const void* const* __restrict__ W, void* const* __restrict__ Y,
                                  ProblemDesc* __restrict__ tab, CUtensorMap* __restrict__ maps,
                                  unsigned int* status) {
+    // Launched with programmatic dependent launch: the GEMM behind it may start its set-up at once
+    // (it reads the tables only after this grid has completed); the pointer arrays and the tables
+    // are touched only after the kernel ahead (which may write the former or read the latter) has.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= su.count) return;
     const int p = su.p0 + i;
@@ -793,6 +800,12 @@ __global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup su, const void
         const void* x = X[p];
         const void* w = W[p];
         void* y = Y[p];
+        // the host-encoded map goes to the table while the pointers load (an invalid problem's map
+        // is never used)
+        const uint4* src = reinterpret_cast<const uint4*>(&su.tmpl[i]);
+        uint4* dst = reinterpret_cast<uint4*>(&maps[p]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[k] = src[k];
         const bool ok = x && w && y &&
                         ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) |
                           reinterpret_cast<uintptr_t>(y)) & 15u) == 0 &&
@@ -800,10 +813,6 @@ __global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup su, const void
         if (ok) {
             d.wp = static_cast<const uint8_t*>(w) + kBlobHeader;
             d.y = y;
-            const uint4* src = reinterpret_cast<const uint4*>(&su.tmpl[i]);
-            uint4* dst = reinterpret_cast<uint4*>(&maps[p]);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) dst[k] = src[k];
             asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
                          "l"(reinterpret_cast<uint64_t>(x))
                          : "memory");
@@ -816,6 +825,7 @@ __global__ void ptr_setup_kernel(const __grid_constant__ PtrSetup su, const void
     tab[p] = d;
 }
 }  // namespace wq4
+}  // extern "C++"
 
 int wq4_grouped_device_m_workspace_bytes(int P, size_t* bytes) {
     if (!bytes || P <= 0) return WQ4_ERR_INVALID;
@@ -909,6 +919,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
 }
 
 // ------------------------------------------------------------------ device-resident pointers
+extern "C++" {
 namespace wq4 {
 namespace {
 // Workspace of the device-pointer grouped call: the plan's K-split part (counters first, zero
@@ -972,8 +983,53 @@ int verify_ptr_maps(int P, const Shape* shapes, const void* const* X_dev, const 
     if (trace_on() && bad) std::fprintf(stderr, "[wq4] %d map bytes differ in all\n", bad);
     return bad ? WQ4_ERR_UNSUPPORTED : WQ4_OK;
 }
+// Launches the set-up kernel over P problems, C per launch (their maps in its parameters).
+template <int C>
+int ptr_setup(int P, const int* M, const int* N, const int* K, const Plan& pl, const void* const* X_dev,
+              const void* const* Wp_dev, void* const* Y_dev, int group_size, int dtype, int qtype, void* stand_in,
+              ProblemDesc* tab, CUtensorMap* maps, unsigned int* status, cudaStream_t stream) {
+    auto su = std::make_unique<PtrSetup<C>>();
+    std::memset(static_cast<void*>(su.get()), 0, sizeof(PtrSetup<C>));
+    su->group_size = group_size;
+    su->dtype = dtype;
+    su->qtype = qtype;
+    for (int p0 = 0; p0 < P; p0 += C) {
+        const int cnt = std::min(C, P - p0);
+        su->p0 = p0;
+        su->count = cnt;
+        for (int i = 0; i < cnt; ++i) {
+            const int p = p0 + i;
+            su->M[i] = M[p];
+            su->N[i] = N[p];
+            su->K[i] = K[p];
+            su->m_tiles[i] = pl.m_tiles[p];
+            su->tile_begin[i] = pl.tile_begin[p];
+            su->unit_begin[i] = pl.unit_begin[p];
+            // the stand-in address (the workspace: any 16-byte aligned one) is replaced on the device
+            if (M[p] > 0) {
+                const int rc = encode_x_map(&su->tmpl[i], stand_in, M[p], K[p], dtype, pl.nt);
+                if (rc) return rc;
+            }
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((cnt + 127) / 128, 1, 1);
+        cfg.blockDim = dim3(C < 128 ? C : 128, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = g_opt.pdl == 0 ? 1 : 0;
+        if (cudaLaunchKernelEx(&cfg, ptr_setup_kernel<C>, static_cast<const PtrSetup<C>&>(*su), X_dev, Wp_dev, Y_dev,
+                               tab, maps, status) != cudaSuccess ||
+            cudaGetLastError() != cudaSuccess)
+            return WQ4_ERR_CUDA;
+    }
+    return WQ4_OK;
+}
 }  // namespace
 }  // namespace wq4
+}  // extern "C++"
 
 int wq4_grouped_dev_ptrs_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
                                          size_t* bytes) {
@@ -1015,29 +1071,11 @@ int wq4_grouped_mm_dev_ptrs(int P, const int* M, const int* N, const int* K, con
     auto* tab = reinterpret_cast<ProblemDesc*>(ws + L.tab_off);
     auto* maps = reinterpret_cast<CUtensorMap*>(ws + L.map_off);
 
-    auto su = std::make_unique<PtrSetup>();
-    std::memset(static_cast<void*>(su.get()), 0, sizeof(PtrSetup));
-    su->group_size = group_size;
-    su->dtype = dtype;
-    su->qtype = qtype;
-    for (int p0 = 0; p0 < P; p0 += kPtrSetupChunk) {
-        const int cnt = std::min(kPtrSetupChunk, P - p0);
-        su->p0 = p0;
-        su->count = cnt;
-        for (int i = 0; i < cnt; ++i) {
-            const int p = p0 + i;
-            su->M[i] = M[p];
-            su->N[i] = N[p];
-            su->K[i] = K[p];
-            su->m_tiles[i] = pl->m_tiles[p];
-            su->tile_begin[i] = pl->tile_begin[p];
-            su->unit_begin[i] = pl->unit_begin[p];
-            // the stand-in address (the workspace: any 16-byte aligned one) is replaced on the device
-            if (M[p] > 0 && (rc = encode_x_map(&su->tmpl[i], workspace, M[p], K[p], dtype, pl->nt))) return rc;
-        }
-        ptr_setup_kernel<<<(cnt + 127) / 128, 128, 0, stream>>>(*su, X_dev, Wp_dev, Y_dev, tab, maps, dev->status);
-        if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
-    }
+    rc = P <= kPtrSetupSmall ? ptr_setup<kPtrSetupSmall>(P, M, N, K, *pl, X_dev, Wp_dev, Y_dev, group_size, dtype, qtype,
+                                                         workspace, tab, maps, dev->status, stream)
+                             : ptr_setup<kPtrSetupChunk>(P, M, N, K, *pl, X_dev, Wp_dev, Y_dev, group_size, dtype, qtype,
+                                                         workspace, tab, maps, dev->status, stream);
+    if (rc) return rc;
     if (g_opt.verify_dev_ptrs)
         return verify_ptr_maps(P, shapes.data(), X_dev, ws + L.map_off, dtype, pl->nt, stream);
 

@@ -75,17 +75,19 @@ struct ProblemDesc {
 // problems up to kMaxDevPtrProblems); the GEMM reads them from there instead of its parameters.
 constexpr int kMaxDevPtrProblems = 4096;
 constexpr int kPtrSetupChunk = 128;       // problems per set-up launch (its parameters hold their maps)
+constexpr int kPtrSetupSmall = 16;        // a call with at most this many problems: a small parameter block
+template <int C>
 struct PtrSetup {
     // Problem i's activation map, encoded on the host for its rows and K with a stand-in address;
     // the set-up kernel replaces only the global address. (The encoder also derives a flag from the
     // tensor's total size, which replacing the row count on the device would leave stale.)
-    CUtensorMap tmpl[kPtrSetupChunk];
+    CUtensorMap tmpl[C];
     int p0, count;                        // problems [p0, p0 + count) of this launch
     int group_size, dtype, qtype;         // what every blob header must say
-    int M[kPtrSetupChunk], N[kPtrSetupChunk], K[kPtrSetupChunk];
-    int m_tiles[kPtrSetupChunk], tile_begin[kPtrSetupChunk], unit_begin[kPtrSetupChunk];
+    int M[C], N[C], K[C];
+    int m_tiles[C], tile_begin[C], unit_begin[C];
 };
-static_assert(sizeof(PtrSetup) <= 32000, "kernel parameter space");
+static_assert(sizeof(PtrSetup<kPtrSetupChunk>) <= 32000, "kernel parameter space");
 
 // Problem sizes known only on the device (tokens routed to experts by a kernel): a set-up kernel
 // writes this table from the device array of token counts; the GEMM then reads M, the tile counts
