@@ -159,7 +159,7 @@ def test_dev_ptrs_group_size(lib):
     c.run()
     assert lib.get_last_error() == lib.OK
     c.check("G=256")
-    c = Case(lib, [40, 0, 64, 3], [(256, 512)], seed=6, group_size=64)
+    c = Case(lib, [40, 0, 300, 3], [(256, 512)], seed=6, group_size=64)
     c.run()
     assert lib.get_last_error() == lib.OK
     c.check("G=64")

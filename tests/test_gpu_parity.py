@@ -101,7 +101,8 @@ GROUP_MM = [
     (8, 4096, 4096, "bf16", "u4b8", 64, True), (5, 2944, 8960, "bf16", "u4_zp", 64, True),
     (16, 768, 1408, "fp16", "u4_fzp", 64, True), (100, 1024, 2048, "bf16", "u4b8", 64, True),
     (300, 384, 512, "fp16", "u4_zp", 64, True), (777, 256, 1024, "bf16", "u4_fzp", 64, True),
-    (129, 512, 768, "bf16", "u4b8", 64, False),
+    (129, 512, 768, "bf16", "u4b8", 64, False), (500, 384, 1024, "bf16", "u4_zp", 64, True),
+    (1000, 256, 512, "fp16", "u4b8", 64, True), (384, 512, 640, "bf16", "u4_fzp", 64, True),
 ]
 
 
@@ -453,12 +454,13 @@ def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     assert_parity(y_as_f64(Y, dtype), ref, "epilogue %s" % ((M, N, K, split_all, in_place),))
 
 
-@pytest.mark.parametrize("token_tile,split_all,cluster,qtype", [(16, 0, 0, "u4b8"), (64, 1, 0, "u4_zp"),
-                                                                (128, 0, 0, "u4b8"), (64, 0, 4, "u4_fzp"),
-                                                                (16, 1, 0, "u4_fzp")])
+@pytest.mark.parametrize("token_tile,split_all,cluster,qtype", [
+    (16, 0, 0, "u4b8"), (64, 1, 0, "u4_zp"), (128, 0, 0, "u4b8"), (64, 0, 4, "u4_fzp"), (16, 1, 0, "u4_fzp"),
+    (128, 1, 0, "u4_zp"), (160, 0, 0, "u4b8"), (192, 0, 0, "u4_zp"), (192, 1, 0, "u4b8"), (192, 0, 2, "u4b8"),
+    (128, 0, 0, "u4_fzp"), (192, 0, 0, "u4_fzp"), (160, 1, 0, "u4_fzp")])
 def test_mm_group_64_schedules(opts, token_tile, split_all, cluster, qtype):
-    """G = 64 (two scale sets per record, a partial per 64-K half): tiles of 16 and 64 tokens,
-    a forced 128 taken down to 64, K-split and cluster plans."""
+    """G = 64 (two scale sets per record, a partial per 64-K half, MMA warp h issuing half h of
+    every group): every token tile, K-split and cluster plans."""
     lib = opts
     lib.set_option(lib.OPT_TOKEN_TILE, token_tile)
     lib.set_option(lib.OPT_SPLIT_ALL, split_all)

@@ -218,13 +218,11 @@ int token_tile_for(const int* M, int P) {
     return best;
 }
 
-// With two scale sets per record (group size 64) a tile's partials take twice the tensor-memory
-// columns: at most 64 tokens then.
-int pick_token_tile(const Shape* shapes, int P, int group_size) {
+// The token tile for these problems (any group size).
+int pick_token_tile(const Shape* shapes, int P, int /*group_size*/) {
     int Ms[kMaxDevPtrProblems];
     for (int p = 0; p < P; ++p) Ms[p] = shapes[p].M;
-    const int nt = token_tile_for(Ms, P);
-    return scale_sets(group_size) == 2 && nt > 64 ? 64 : nt;
+    return token_tile_for(Ms, P);
 }
 
 // Splitting the last partial wave of tiles over all CTAs pays only if it saves more (tile, group)
@@ -367,17 +365,19 @@ int encode_x_map(CUtensorMap* map, const void* X, int M, int K, int dtype, int n
 
 cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qtype, int group_size, int grid,
                      cudaStream_t st) {
-    const int H = scale_sets(group_size);
+    const bool two = scale_sets(group_size) == 2;
     const bool bf16 = dtype == WQ4_BF16, a_tmem = !g_opt.a_in_smem;
-    const int zp = qtype;                                       // record layout of the format
+    const int qt = qtype;                                       // record layout of the format
     const bool pdl = g_opt.pdl == 0;
+#define WQ4_GO(NT) (two ? launch_gemm_nt##NT##_h2 : launch_gemm_nt##NT##_h1)(params, grouped, bf16, qt, a_tmem, grid, pdl, st)
     switch (nt) {
-        case 16: return launch_gemm_nt16(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
-        case 64: return launch_gemm_nt64(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
-        case 128: return launch_gemm_nt128(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
-        case 160: return launch_gemm_nt160(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
-        default: return launch_gemm_nt192(params, grouped, bf16, zp, a_tmem, H, grid, pdl, st);
+        case 16: return WQ4_GO(16);
+        case 64: return WQ4_GO(64);
+        case 128: return WQ4_GO(128);
+        case 160: return WQ4_GO(160);
+        default: return WQ4_GO(192);
     }
+#undef WQ4_GO
 }
 
 // Float-zero mode: xsum[g][m] = the sum of X[m][span g .. span g + span - 1] in fp32 (span = 128,
@@ -858,8 +858,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
     if ((rc = device_info(&dev))) return rc;
     // Plan for the capacities: the token tile and the grid; every tile whole (the tile count is
     // known only on the device).
-    const int nt0 = token_tile_for(M_cap, P);
-    const int nt = scale_sets(group_size) == 2 && nt0 > 64 ? 64 : nt0;   // see pick_token_tile
+    const int nt = token_tile_for(M_cap, P);
     long long max_tiles = 0;
     auto* prm = new (std::nothrow) GemmParams<kMaxGroupedProblems>();
     if (!prm) return WQ4_ERR_CUDA;

@@ -42,9 +42,9 @@ namespace wq4 {
 template <int NT, int QT, bool ATMEM, int H>
 struct GemmCfg {
     static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 160 || NT == 192, "token tile");
-    // H scale sets per 128-K record (2 for a group size of 64): each group's MMAs accumulate into
-    // H partials of NT columns (K 0..63 and 64..127 apart), each folded with its own scale.
-    static_assert(H == 1 || (H == 2 && NT <= 64), "two scale sets need a token tile of at most 64");
+    // H scale sets per 128-K record (2 for a group size of 64): the MMAs of each 64-K half of a
+    // group accumulate into a partial of their own, folded with the half's scale.
+    static_assert(H == 1 || H == 2, "scale sets");
     // Four warpgroups: WG0 = the two TMA producer warps (0, 2) and the two MMA warps (1, 3);
     // then the dequant warps; then the fold warps. Any four consecutive warps cover the four TMEM lane quarters (warp % 4).
     static constexpr int kDQW = NT <= 64 ? 8 : 4;            // dequant warps
@@ -78,11 +78,18 @@ struct GemmCfg {
     // (64 columns each). With two, the dequantisation of group g waits for the MMAs of group
     // g - 2 and that chain, not the tensor pipe, sets the pace; a third or fourth buffer lets it
     // run further ahead. In shared memory (the comparison path) two.
-    // P buffers (group partials). Two: at NT = 128 three P buffers with two operand buffers were
-    // measured slower than two P buffers with four operand buffers (the dequantisation chain
-    // binds before the fold chain does).
-    static constexpr int kPBufs = 2;
-    static constexpr int kPCols = H * NT;                    // tensor-memory columns of one P buffer
+    // P buffers (partials), NT columns each. One scale set: two, one per MMA warp (the warps take
+    // alternate groups); at NT = 128 three P buffers with two operand buffers were measured slower
+    // than two P buffers with four operand buffers (the dequantisation chain binds before the fold
+    // chain does). Two scale sets: MMA warp h issues half h of every group into buffers of its
+    // own, two each where tensor memory leaves two operand buffers beside them, else one; so
+    // every buffer is walked in consecutive phases by a single issuer.
+    static constexpr int kPBufs = H == 1 ? 2 : (4 * NT + 2 * 64 <= 512 ? 4 : 2);
+    static constexpr int kPPerHalf = kPBufs / H;             // P buffers of one issuer
+    static constexpr int kPCols = NT;                        // tensor-memory columns of one P buffer
+    // the P buffer of group i's partial h, and the round (phase parity) of its use
+    __device__ static int pbuf(int i, int h) { return h + H * (i % kPPerHalf); }
+    __device__ static uint32_t pround(int i) { return static_cast<uint32_t>(i / kPPerHalf) & 1u; }
     static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * kPCols) / 64 >= 4 ? 4 : (512 - kPBufs * kPCols) / 64;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
     static constexpr int kBarBytes = 1024;
@@ -360,9 +367,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        // a stage or operand buffer is released by the commit of each MMA warp that read it: the
+        // one that issued the group, or both with two scale sets (one half each)
         for (int s = 0; s < C::kXStages; ++s) {
             mbar_init(xfull_bar(s), 1);
-            mbar_init(xempty_bar(s), 1);
+            mbar_init(xempty_bar(s), H);
         }
         for (int s = 0; s < C::kWStages; ++s) {
             mbar_init(wfull_bar(s), 1);
@@ -370,7 +379,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         }
         for (int a = 0; a < C::kABufs; ++a) {
             mbar_init(afull_bar(a), C::kDQW);
-            mbar_init(aempty_bar(a), 1);
+            mbar_init(aempty_bar(a), H);
         }
         for (int b = 0; b < C::kPBufs; ++b) {
             mbar_init(pfull_bar(b), 1);
@@ -497,21 +506,21 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
                 for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                    if ((i & 1) != mine) continue;
+                    if (H == 1 && (i & 1) != mine) continue;    // one scale set: alternate groups
                     const int s = i % C::kXStages;
-                    const int b = i % C::kPBufs;                // P buffer
-                    const uint32_t u = static_cast<uint32_t>(i / C::kPBufs) & 1u;
+                    const int b = C::pbuf(i, H == 1 ? 0 : mine);   // P buffer (two sets: half `mine`)
+                    const uint32_t u = C::pround(i);
                     const int a = i % C::kABufs;                // A buffer
                     if (!mbar_wait(xfull_bar(s), (i / C::kXStages) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(afull_bar(a), (i / C::kABufs) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t xs = s_x0 + s * C::kXStageBytes;
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kPCols);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        // K panel kk / 4; with two scale sets each panel has its own partial
-                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * C::kPCols + (H == 2 ? (kk >> 2) * NT : 0));
-                        const bool accum = H == 2 ? (kk & 3) > 0 : kk > 0;
+                    for (int k = 0; k < 8 / H; ++k) {
+                        const int kk = (H == 2 ? 4 * mine : 0) + k;    // K step (panel kk / 4)
+                        const bool accum = k > 0;
                         const uint64_t bdesc = make_sdesc_sw128(xs + (kk >> 2) * C::kXPanel + (kk & 3) * 32);
                         if constexpr (ATMEM) {
                             mma_ts(d_tmem, tmem_base + C::kColA + a * 64 + kk * 8, bdesc, idesc, accum);
@@ -624,18 +633,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         while (ok && sch.next(seg)) {
             for (int g = seg.g0; g < seg.g1; ++g, ++i) {
                 const int s = i % C::kWStages;
-                const int b = i % C::kPBufs;
-                const uint32_t u = static_cast<uint32_t>(i / C::kPBufs) & 1u;
-                if (!mbar_wait(pfull_bar(b), u, ctl)) { ok = false; break; }
                 if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
-                tc_fence_after();
                 const uint32_t rec = wrec_of(i);
                 if (g == seg.g0) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
                 }
-#pragma unroll
+#pragma unroll 1
                 for (int h = 0; h < H; ++h) {                   // scale set h: its partial, scale and zero
+                    const int b = C::pbuf(i, h);
                     uint32_t sbits;
                     asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(QT, r, H, h)));
                     const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
@@ -655,10 +661,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                                 asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(srow + prm.xsum_ld) + off));
                         }
                     }
+                    if (!mbar_wait(pfull_bar(b), C::pround(i), ctl)) { ok = false; break; }
+                    tc_fence_after();
                     // P in batches of up to 64 columns per wait (the loads of a batch overlap)
                     // (the last batch may be shorter: 80 columns = 48 + 32)
                     constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
-                    const uint32_t t_p = t_lane + b * C::kPCols + h * NT + col0;
+                    const uint32_t t_p = t_lane + b * C::kPCols + col0;
 #pragma unroll
                     for (int c = 0; c < C::kNC; c += kBatchCols) {
                         constexpr int kLeft = C::kNC;
@@ -682,13 +690,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             }
                         }
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(pempty_bar(b));    // the MMAs may reuse this partial
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(pempty_bar(b));
-                    mbar_arrive(wempty_bar(s));
-                }
+                if (!ok) break;
+                if (lane == 0) mbar_arrive(wempty_bar(s));
             }
             if (!ok) break;
 

@@ -1,4 +1,4 @@
-// Launchers of the GEMM instantiations (one translation unit per token tile) and of prepack.
+// Launchers of the GEMM instantiations and of prepack.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -14,17 +14,23 @@ struct EpilogueArgs {
     const void* bias;
 };
 
-// `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>.
-cudaError_t launch_gemm_nt16(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
-                             bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt64(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
-                             bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt128(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
-                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt160(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
-                              bool pdl, cudaStream_t st);
-cudaError_t launch_gemm_nt192(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, int scale_sets, int grid,
-                              bool pdl, cudaStream_t st);
+// `params` points to a GemmParams<1> (grouped == false) or GemmParams<kMaxGroupedProblems>. One
+// launcher per token tile (16, 64, 128, 160, 192) and scale-set count (h1: one scale per 128-K
+// record, h2: two, group size 64), each in its own translation unit (wq4_gemm_nt*_h*.cu).
+#define WQ4_DECLARE_GEMM_UNIT(NT, H)                                                                  \
+    cudaError_t launch_gemm_nt##NT##_h##H(const void* params, bool grouped, bool bf16, int qt, bool a_tmem, \
+                                          int grid, bool pdl, cudaStream_t st);
+WQ4_DECLARE_GEMM_UNIT(16, 1)
+WQ4_DECLARE_GEMM_UNIT(16, 2)
+WQ4_DECLARE_GEMM_UNIT(64, 1)
+WQ4_DECLARE_GEMM_UNIT(64, 2)
+WQ4_DECLARE_GEMM_UNIT(128, 1)
+WQ4_DECLARE_GEMM_UNIT(128, 2)
+WQ4_DECLARE_GEMM_UNIT(160, 1)
+WQ4_DECLARE_GEMM_UNIT(160, 2)
+WQ4_DECLARE_GEMM_UNIT(192, 1)
+WQ4_DECLARE_GEMM_UNIT(192, 2)
+#undef WQ4_DECLARE_GEMM_UNIT
 
 // Decode-sized M (<= 32 tokens): warp-level MMA kernel, no workspace.
 struct DecodeLaunch {
