@@ -15,6 +15,7 @@
 // tiles' (tile, group) units are divided evenly over the CTAs and K-split tiles are summed in a
 // fixed order (deterministic).
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -380,21 +381,27 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
 #undef WQ4_GO
 }
 
-// Float-zero mode: xsum[g][m] = the sum of X[m][span g .. span g + span - 1] in fp32 (span = 128,
-// or 64 with two scale sets per record), 0 for rows m >= M up to the padded row length ld. One warp
-// per (g, m): each lane adds its span / 32 consecutive elements in order, then a butterfly over the
-// warp; lane 0's result is stored (the same order every run).
+// Float-zero mode: the activation sums of every (token m, zero group z) for the GEMM's zero steps,
+// xs = the sum of X[m][span z .. span z + span - 1] in fp32 (span = 128, or 64 with two scale sets
+// per record), split into hi = xs rounded to the 16-bit type and lo = xs - hi rounded likewise
+// (hi + lo carries 16 (bf16) or 22 (fp16) significant bits). Table [ld][2 zpad] of 16-bit values:
+// hi at column z, lo at column zpad + z; zero for rows m >= M (up to ld) and for z >= K / span (up
+// to zpad, a multiple of 64), so that a zero step's copies never read past it and the masked-off
+// zeros never meet a NaN. One warp per (z, m): each lane adds its span / 32 consecutive elements in
+// order, then a butterfly over the warp (the same order every run).
 template <bool BF16>
-__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, int span, float* __restrict__ out) {
+__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, int span, int zpad,
+                            uint16_t* __restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int per = span / 32;
+    const int nz = K / span;
     const long long wpb = blockDim.x / 32;
-    const long long total = static_cast<long long>(K / span) * ld;
+    const long long total = static_cast<long long>(zpad) * ld;
     for (long long w = blockIdx.x * wpb + threadIdx.x / 32; w < total; w += gridDim.x * wpb) {
-        const int g = static_cast<int>(w / ld), m = static_cast<int>(w % ld);
+        const int z = static_cast<int>(w / ld), m = static_cast<int>(w % ld);
         float v = 0.f;
-        if (m < M) {
-            const uint16_t* xp = X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * g + per * lane;
+        if (m < M && z < nz) {
+            const uint16_t* xp = X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * z + per * lane;
             for (int i = 0; i < per; ++i) {
                 const uint32_t e = xp[i];
                 if constexpr (BF16) {
@@ -406,15 +413,35 @@ __global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) out[static_cast<size_t>(g) * ld + m] = v;
+        if (lane == 0) {
+            uint16_t hi, lo;
+            if constexpr (BF16) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                hi = __bfloat16_as_ushort(h);
+                lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+            } else {
+                const __half h = __float2half_rn(v);
+                hi = __half_as_ushort(h);
+                lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
+            }
+            uint16_t* row = out + static_cast<size_t>(m) * 2 * zpad;
+            row[z] = hi;
+            row[zpad + z] = lo;
+        }
     }
 }
 
-// Bytes of the float-zero activation-sum table for one problem at token tile nt (0 otherwise).
+// Zero groups of a problem (K / span) rounded up to a whole zero step (64).
+int zero_groups_padded(int K, int group_size) {
+    const int nz = K / (kTileK / scale_sets(group_size));
+    return (nz + 63) / 64 * 64;
+}
+
+// Bytes of the float-zero sums table for one problem at token tile nt (0 otherwise).
 size_t xsum_table_bytes(int qtype, const Shape& s, int nt, int group_size) {
     if (qtype != WQ4_U4_FZP || s.M <= 0) return 0;
     const size_t ld = static_cast<size_t>((s.M + nt - 1) / nt) * nt;
-    return static_cast<size_t>(s.K / kTileK) * scale_sets(group_size) * ld * 4;
+    return ld * 2 * zero_groups_padded(s.K, group_size) * 2;
 }
 
 // Plans and launches the GEMM kernel for P problems. With fixed_scratch the workspace is the
@@ -500,18 +527,30 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     if (fixed_scratch && pl.counters_bytes && cudaMemsetAsync(workspace, 0, pl.counters_bytes, st) != cudaSuccess)
         return WQ4_ERR_CUDA;
     if (xsum_bytes) {                                           // the pre-pass, in stream order before the GEMM
-        float* xs = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + xsum_off);
+        uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + xsum_off);
         const int ld = pl.m_tiles[0] * pl.nt;
-        prm->xsum = xs;
-        prm->xsum_ld = ld;
+        const int zpad = zero_groups_padded(shapes[0].K, group_size);
         const int span = kTileK / scale_sets(group_size);
-        const long long warps = static_cast<long long>(shapes[0].K / span) * ld;
+        {
+            EncodeTiledFn fn = encode_fn();
+            if (!fn) return WQ4_ERR_CUDA;
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * zpad), static_cast<cuuint64_t>(ld)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * zpad) * 2};
+            const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pl.nt)};
+            const cuuint32_t estr[2] = {1, 1};
+            if (fn(&prm->sxmap, dtype == WQ4_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   xs, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return WQ4_ERR_CUDA;
+        }
+        prm->sx_lo_col = zpad;
+        const long long warps = static_cast<long long>(zpad) * ld;
         const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 65535));
         const uint16_t* x16 = static_cast<const uint16_t*>(X[0]);
         if (dtype == WQ4_BF16) {
-            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, xs);
+            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, zpad, xs);
         } else {
-            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, xs);
+            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, zpad, xs);
         }
         if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     }

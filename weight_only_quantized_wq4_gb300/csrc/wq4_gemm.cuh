@@ -92,17 +92,30 @@ struct GemmCfg {
     __device__ static uint32_t pround(int i) { return static_cast<uint32_t>(i / kPPerHalf) & 1u; }
     static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * kPCols) / 64 >= 4 ? 4 : (512 - kPBufs * kPCols) / 64;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
+    // Float zeros: the zero term sum over groups of zf[n][g] * (sum of X[m] over group g) runs on
+    // the tensor core as one extra step (a "zero step") after every kZRec records of a segment and
+    // after its last: A = the rows' float zeros of those records' kZRec * H zero groups (64 at
+    // most), B = the activation sums split into a high and a low 16-bit part (a pre-pass table
+    // copied like an activation tile, high part in K 0..63 and low part in K 64..127, each against
+    // the same zeros). The dequant warps stage each row's zeros in shared memory as they pass
+    // (row stride 132 B: the 32 lanes of a warp write different banks), one copy per dequant warp
+    // of a lane quarter.
+    static constexpr bool kZ = QT == kQtU4FZp;
+    static constexpr int kZRec = 64 / H;                     // records per zero step
+    static constexpr int kZRow = 132;                        // staging bytes per row
+    static constexpr int kZBytes = kZ ? ((NT <= 64 ? 2 : 1) * 128 * kZRow + 1023) / 1024 * 1024 : 0;
+    __device__ static bool zstep_after(int g, int g1) { return kZ && ((g + 1) % kZRec == 0 || g + 1 == g1); }
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
-    static constexpr int kWStages = NT <= 16 ? 16 : (ATMEM ? 8 : 6);
+    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? 8 : (kZ ? 4 : 6));
     // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
     static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
-    static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kWRingBytes) / kXStageBytes;
+    static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kZBytes - kWRingBytes) / kXStageBytes;
     // An even count: the two MMA warps take alternate groups, so each then owns every other slot
     // and waits on consecutive phases of it (a parity wait is unambiguous one phase ahead only; with
     // an odd count a warp would skip the other warp's phase of a slot).
     static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
-    static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kBarBytes;
     static constexpr int kColA = kPBufs * kPCols;            // TMEM column of A buffer 0
     static constexpr int kTmemNeed = kPBufs * kPCols + (ATMEM ? 64 * kABufs : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
@@ -345,7 +358,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t s_x0 = sbase;                                         // activation ring
     const uint32_t s_w0 = s_x0 + C::kXStages * C::kXStageBytes;           // weight-record ring
     const uint32_t s_A = s_w0 + C::kWRingBytes;
-    const uint32_t s_bar = s_A + C::kABytes;
+    const uint32_t s_Z = s_A + C::kABytes;                                // float-zero staging
+    const uint32_t s_bar = s_Z + C::kZBytes;
     auto xfull_bar = [&](int s) { return s_bar + 8u * s; };
     auto xempty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
     auto wfull_bar = [&](int s) { return s_bar + 8u * (32 + s); };
@@ -354,7 +368,6 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     auto aempty_bar = [&](int a) { return s_bar + 8u * (68 + a); };
     auto pfull_bar = [&](int b) { return s_bar + 8u * (72 + b); };
     auto pempty_bar = [&](int b) { return s_bar + 8u * (76 + b); };
-    auto wrec_of = [&](int i) { return s_w0 + (i % C::kWStages) * C::kWStageBytes; };
     const uint32_t drain_bar = s_bar + 8u * 80;
     const uint32_t fsync_bar = s_bar + 8u * 81;   // fold warps meet here in the split epilogue
     const uint32_t stall_bar = s_bar + 8u * 82;   // never arrived on (test of the timeout path)
@@ -466,19 +479,32 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                                  : "memory");
                     last_prob = seg.prob;
                 }
-                for (int g = seg.g0; g < seg.g1; ++g, ++i, wrec += C::kRec) {
-                    const int s = i % depth;
-                    const uint32_t par = ((i / depth) & 1) ^ 1;
+                for (int g = seg.g0; g < seg.g1; ++g, wrec += C::kRec) {
                     if (is_x) {
-                        if (!mbar_wait(xempty_bar(s), par, ctl)) { ok = false; break; }
-                        const uint32_t stage = s_x0 + s * C::kXStageBytes;
-                        mbar_arrive_expect_tx(xfull_bar(s), 2 * C::kXPanel);
-                        tma_load_2d(stage, xmap, xfull_bar(s), g * kTileK, seg.mt * NT, pol_keep);
-                        tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                        // the group's activation tile, then (float zeros) a zero step's sums
+                        const int nstep = C::zstep_after(g, seg.g1) ? 2 : 1;
+                        for (int t = 0; t < nstep; ++t, ++i) {
+                            const int s = i % depth;
+                            if (!mbar_wait(xempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
+                            const uint32_t stage = s_x0 + s * C::kXStageBytes;
+                            mbar_arrive_expect_tx(xfull_bar(s), 2 * C::kXPanel);
+                            if (t == 0) {
+                                tma_load_2d(stage, xmap, xfull_bar(s), g * kTileK, seg.mt * NT, pol_keep);
+                                tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                            } else {                     // zero groups [64 zc, 64 zc + 64): high, then low part
+                                const int zc = (g * H) / 64;
+                                tma_load_2d(stage, &prm.sxmap, xfull_bar(s), 64 * zc, seg.mt * NT, pol_stream);
+                                tma_load_2d(stage + C::kXPanel, &prm.sxmap, xfull_bar(s), prm.sx_lo_col + 64 * zc,
+                                            seg.mt * NT, pol_stream);
+                            }
+                        }
+                        if (!ok) break;
                     } else {
-                        if (!mbar_wait(wempty_bar(s), par, ctl)) { ok = false; break; }
+                        const int s = i % depth;
+                        if (!mbar_wait(wempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(wfull_bar(s), C::kRec);
                         bulk_load(s_w0 + s * C::kWStageBytes, wrec, C::kRec, wfull_bar(s), pol_w);
+                        ++i;
                     }
                 }
             }
@@ -505,8 +531,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int rows = problem_rows(prm, seg.prob) - seg.mt * NT;
                 const int n_valid = rows < NT ? rows : NT;
                 const uint32_t idesc = make_idesc(BF16, 128, static_cast<uint32_t>((n_valid + 15) & ~15));
-                for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                    if (H == 1 && (i & 1) != mine) continue;    // one scale set: alternate groups
+                for (int g = seg.g0; g < seg.g1 && ok; ++g)
+                for (int t = 0, nstep = C::zstep_after(g, seg.g1) ? 2 : 1; t < nstep; ++t, ++i) {
+                    // step i: group g, or (t = 1) the zero step after it; both alike here
+                    if (H == 1 && (i & 1) != mine) continue;    // one scale set: alternate steps
                     const int s = i % C::kXStages;
                     const int b = C::pbuf(i, H == 1 ? 0 : mine);   // P buffer (two sets: half `mine`)
                     const uint32_t u = C::pround(i);
@@ -546,17 +574,43 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         const int part = (warp - 4) >> 2;
         const int r = 32 * q4 + lane;
         const NibbleConsts nib = prm.nib;
+        // this thread's float-zero staging row (one copy per dequant warp of a lane quarter)
+        const uint32_t zrow = s_Z + static_cast<uint32_t>((part * 128 + r) * C::kZRow);
+        // stores one 32-K chunk (16 pairs) of the operand in buffer a
+        auto put_chunk = [&](int a, int j, const uint32_t (&out)[16]) {
+            if constexpr (ATMEM) {
+                tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + a * 64 + 16 * j, out);
+            } else {
+                const uint32_t pbase = s_A + a * C::kABuf + (j >> 1) * (C::kABuf / 2) + r * 128;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t chunk = static_cast<uint32_t>((4 * (j & 1) + w) ^ (r & 7));
+                    sts128(pbase + chunk * 16, out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+                }
+            }
+        };
+        auto operand_done = [&](int a) {                 // buffer a written: hand it to the MMA warps
+            if constexpr (ATMEM) {
+                tmem_st_wait();
+                tc_fence_before();
+            } else {
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull_bar(a));
+        };
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
-        int i = 0;
+        int i = 0;                                       // steps (groups and zero steps)
+        int wi = 0;                                      // weight records
         bool ok = true;
         while (ok && sch.next(seg)) {
-            for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                const int s = i % C::kWStages;
+            for (int g = seg.g0; g < seg.g1; ++g, ++i, ++wi) {
+                const int s = wi % C::kWStages;
                 const int a = i % C::kABufs;
-                if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
+                if (!mbar_wait(wfull_bar(s), (wi / C::kWStages) & 1, ctl)) { ok = false; break; }
                 if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
-                const uint32_t rec = wrec_of(i);
+                const uint32_t rec = s_w0 + s * C::kWStageBytes;
                 uint32_t subs[H];                             // per scale set
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
@@ -566,7 +620,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         const uint32_t z = (zb >> (((r >> 3) & 1) * 4)) & 0xFu;
                         subs[h] = ((BF16 ? 0x4300u : 0x6400u) | z) * 0x10001u;
                     } else if constexpr (QT == kQtU4FZp) {
-                        subs[h] = BF16 ? 0x43004300u : 0x64006400u;   // the code itself; its zero is added at the fold
+                        subs[h] = BF16 ? 0x43004300u : 0x64006400u;   // the code itself; its zero goes to a zero step
+                        uint32_t zfb;
+                        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(zfb) : "r"(rec + rec_fzero_off(QT, r, H, h)));
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(zrow + 2 * ((g * H + h) % 64)), "r"(zfb) : "memory");
                     } else {
                         subs[h] = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
                     }
@@ -583,27 +640,36 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub, nib);
                     }
-                    if constexpr (ATMEM) {
-                        tmem_st16(tmem_base + (static_cast<uint32_t>(32 * q4) << 16) + C::kColA + a * 64 + 16 * j, out);
-                    } else {
-                        const uint32_t pbase = s_A + a * C::kABuf + (j >> 1) * (C::kABuf / 2) + r * 128;
+                    put_chunk(a, j, out);
+                }
+                operand_done(a);
+                if (lane == 0) mbar_arrive(wempty_bar(s));
+                if (C::zstep_after(g, seg.g1)) {
+                    // zero step: the staged zeros of this chunk's zero groups that lie in the segment
+                    // (K 0..63 and again K 64..127, against the high and the low part of the sums);
+                    // the rest of the 64 are zero
+                    ++i;
+                    const int a2 = i % C::kABufs;
+                    if (!mbar_wait(aempty_bar(a2), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
+                    const int zc = (g * H) / 64;
+                    const int zlo = max(seg.g0 * H - 64 * zc, 0), zhi = (g + 1) * H - 64 * zc;
+#pragma unroll 1
+                    for (int jj = 0; jj < C::kChunks; ++jj) {
+                        const int j = part * C::kChunks + jj;
+                        const int z0 = 32 * (j & 1);
+                        uint32_t out[16];
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const uint32_t chunk = static_cast<uint32_t>((4 * (j & 1) + w) ^ (r & 7));
-                            sts128(pbase + chunk * 16, out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+                        for (int q = 0; q < 16; ++q) {
+                            const int z = z0 + 2 * q;
+                            uint32_t wv;
+                            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wv) : "r"(zrow + 2 * z));
+                            const uint32_t lo_ok = (z >= zlo && z < zhi) ? 0x0000FFFFu : 0u;
+                            const uint32_t hi_ok = (z + 1 >= zlo && z + 1 < zhi) ? 0xFFFF0000u : 0u;
+                            out[q] = wv & (lo_ok | hi_ok);
                         }
+                        put_chunk(a2, j, out);
                     }
-                }
-                if constexpr (ATMEM) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                } else {
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(afull_bar(a));
-                    mbar_arrive(wempty_bar(s));
+                    operand_done(a2);
                 }
             }
         }
@@ -628,74 +694,69 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
         seg.prob = -1;                                   // stays -1 if the CTA gets no tile
-        int i = 0;
+        // acc += sc * (partial b, this thread's columns); then the partial goes back to the MMAs
+        auto fold_partial = [&](int b, uint32_t round, float sc) -> bool {
+            if (!mbar_wait(pfull_bar(b), round, ctl)) return false;
+            tc_fence_after();
+            // P in batches of up to 64 columns per wait (the loads of a batch overlap)
+            // (the last batch may be shorter: 80 columns = 48 + 32)
+            constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
+            const uint32_t t_p = t_lane + b * C::kPCols + col0;
+#pragma unroll
+            for (int c = 0; c < C::kNC; c += kBatchCols) {
+                constexpr int kLeft = C::kNC;
+                const int nbc = kLeft - c < kBatchCols ? kLeft - c : kBatchCols;
+                uint32_t v[kBatchCols];
+#pragma unroll
+                for (int q = 0; q < kBatchCols; q += 16)
+                    if (q < nbc) tmem_ld16(t_p + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < kBatchCols; j += 4) {
+                    // (columns come in multiples of 16: j < nbc covers j + 3 too)
+                    if (j < nbc) {
+                        fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
+                        fma2(acc[c + j + 2], acc[c + j + 3], sc, v[j + 2], v[j + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pempty_bar(b));
+            return true;
+        };
+        int i = 0;                                       // steps (groups and zero steps)
+        int wi = 0;                                      // weight records
         bool ok = true;
         while (ok && sch.next(seg)) {
-            for (int g = seg.g0; g < seg.g1; ++g, ++i) {
-                const int s = i % C::kWStages;
-                if (!mbar_wait(wfull_bar(s), (i / C::kWStages) & 1, ctl)) { ok = false; break; }
-                const uint32_t rec = wrec_of(i);
+            for (int g = seg.g0; g < seg.g1; ++g, ++i, ++wi) {
+                const int s = wi % C::kWStages;
+                if (!mbar_wait(wfull_bar(s), (wi / C::kWStages) & 1, ctl)) { ok = false; break; }
+                const uint32_t rec = s_w0 + s * C::kWStageBytes;
                 if (g == seg.g0) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
                 }
-#pragma unroll 1
-                for (int h = 0; h < H; ++h) {                   // scale set h: its partial, scale and zero
-                    const int b = C::pbuf(i, h);
+                float sc[H];                                    // the record's scale per set
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
                     uint32_t sbits;
                     asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sbits) : "r"(rec + rec_scale_off(QT, r, H, h)));
-                    const float sc = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
-                    // float zeros: acc += zf * (sum of the set's activations per token), the sums read
-                    // from the table a pre-pass wrote (xsum[g H + h][m], this thread's columns contiguous)
-                    float zf = 0.f;
-                    const float* srow = nullptr;
-                    if constexpr (QT == kQtU4FZp) {
-                        uint32_t zbits;
-                        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(zbits) : "r"(rec + rec_fzero_off(QT, r, H, h)));
-                        zf = scale_to_float<BF16>(static_cast<uint16_t>(zbits));
-                        srow = prm.xsum + static_cast<size_t>(g * H + h) * prm.xsum_ld + seg.mt * NT + col0;
-                        // the next row of sums into L1 now (one lane: every lane reads the same row)
-                        if (lane == 0 && (h + 1 < H || g + 1 < seg.g1)) {
-#pragma unroll
-                            for (int off = 0; off < C::kNC * 4; off += 128)
-                                asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(srow + prm.xsum_ld) + off));
-                        }
-                    }
-                    if (!mbar_wait(pfull_bar(b), C::pround(i), ctl)) { ok = false; break; }
-                    tc_fence_after();
-                    // P in batches of up to 64 columns per wait (the loads of a batch overlap)
-                    // (the last batch may be shorter: 80 columns = 48 + 32)
-                    constexpr int kBatchCols = C::kNC <= 64 ? C::kNC : 48;
-                    const uint32_t t_p = t_lane + b * C::kPCols + col0;
-#pragma unroll
-                    for (int c = 0; c < C::kNC; c += kBatchCols) {
-                        constexpr int kLeft = C::kNC;
-                        const int nbc = kLeft - c < kBatchCols ? kLeft - c : kBatchCols;
-                        uint32_t v[kBatchCols];
-#pragma unroll
-                        for (int q = 0; q < kBatchCols; q += 16)
-                            if (q < nbc) tmem_ld16(t_p + c + q, *reinterpret_cast<uint32_t(*)[16]>(&v[q]));
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < kBatchCols; j += 4) {
-                            // (columns come in multiples of 16: j < nbc covers j + 3 too)
-                            if (j < nbc) {
-                                fma2(acc[c + j], acc[c + j + 1], sc, v[j], v[j + 1]);
-                                fma2(acc[c + j + 2], acc[c + j + 3], sc, v[j + 2], v[j + 3]);
-                                if constexpr (QT == kQtU4FZp) {
-                                    const float4 sv = __ldg(reinterpret_cast<const float4*>(srow + c + j));
-                                    fma2(acc[c + j], acc[c + j + 1], zf, __float_as_uint(sv.x), __float_as_uint(sv.y));
-                                    fma2(acc[c + j + 2], acc[c + j + 3], zf, __float_as_uint(sv.z), __float_as_uint(sv.w));
-                                }
-                            }
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(pempty_bar(b));    // the MMAs may reuse this partial
+                    sc[h] = scale_to_float<BF16>(static_cast<uint16_t>(sbits));
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wempty_bar(s));      // (the scales are read: the record may go)
+#pragma unroll 1
+                for (int h = 0; h < H; ++h)                     // scale set h: its partial with its scale
+                    if (!fold_partial(C::pbuf(i, h), C::pround(i), h == 0 ? sc[0] : sc[H - 1])) { ok = false; break; }
                 if (!ok) break;
-                if (lane == 0) mbar_arrive(wempty_bar(s));
+                if (C::zstep_after(g, seg.g1)) {                // float zeros: the zero step, scale 1
+                    ++i;
+#pragma unroll 1
+                    for (int h = 0; h < H; ++h)
+                        if (!fold_partial(C::pbuf(i, h), C::pround(i), 1.0f)) { ok = false; break; }
+                    if (!ok) break;
+                }
             }
             if (!ok) break;
 

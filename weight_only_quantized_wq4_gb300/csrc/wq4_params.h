@@ -143,8 +143,9 @@ struct GemmParams {
     int hdr_trusted;         // 1: every blob was prepacked here for these arguments (records may be read
                              // while the headers are being checked); 0: check before the first read
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
-    const float* xsum;       // float-zero mode: xsum[g][m] = sum of X[m][128 g .. 128 g + 127] (fp32),
-    int xsum_ld;             // rows of xsum_ld >= m_tiles * token tile floats (zero past M)
+    CUtensorMap sxmap;       // float-zero mode: the activation sums per (token, zero group), split
+                             // into high and low 16-bit parts: [rows][sx_lo_col] high, then low;
+    int sx_lo_col;           // box (64, token tile), 128B swizzle (single-problem calls)
     const ProblemDesc* prob_tab;    // device-resident problem table (num_problems entries), or null
     const CUtensorMap* xmap_tab;    // their activation tensor maps (patched on the device), or null
 };
