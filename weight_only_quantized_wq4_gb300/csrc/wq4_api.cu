@@ -387,47 +387,51 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
 // (hi + lo carries 16 (bf16) or 22 (fp16) significant bits). Table [ld][2 zpad] of 16-bit values:
 // hi at column z, lo at column zpad + z; zero for rows m >= M (up to ld) and for z >= K / span (up
 // to zpad, a multiple of 64), so that a zero step's copies never read past it and the masked-off
-// zeros never meet a NaN. One warp per (z, m): each lane adds its span / 32 consecutive elements in
-// order, then a butterfly over the warp (the same order every run).
+// zeros never meet a NaN. One thread per (m, z), consecutive threads on consecutive z of a row:
+// 16-byte loads of its span, added in K order (the same order every run). Launched with
+// programmatic dependent launch: the GEMM behind it may set up at once, and X is read only once
+// the kernel ahead (which may write it) has completed.
 template <bool BF16>
 __global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, int span, int zpad,
                             uint16_t* __restrict__ out) {
-    const int lane = threadIdx.x & 31;
-    const int per = span / 32;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int nz = K / span;
-    const long long wpb = blockDim.x / 32;
     const long long total = static_cast<long long>(zpad) * ld;
-    for (long long w = blockIdx.x * wpb + threadIdx.x / 32; w < total; w += gridDim.x * wpb) {
-        const int z = static_cast<int>(w / ld), m = static_cast<int>(w % ld);
+    for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+         t += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int m = static_cast<int>(t / zpad), z = static_cast<int>(t % zpad);
         float v = 0.f;
         if (m < M && z < nz) {
-            const uint16_t* xp = X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * z + per * lane;
-            for (int i = 0; i < per; ++i) {
-                const uint32_t e = xp[i];
-                if constexpr (BF16) {
-                    v += __uint_as_float(e << 16);
-                } else {
-                    v += __half2float(__ushort_as_half(static_cast<unsigned short>(e)));
+            const uint4* xp = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * z);
+            for (int c = 0; c < span / 8; ++c) {
+                const uint4 q = __ldg(xp + c);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (BF16) {
+                        v += __uint_as_float(w[e] << 16);
+                        v += __uint_as_float(w[e] & 0xFFFF0000u);
+                    } else {
+                        v += __half2float(__ushort_as_half(static_cast<unsigned short>(w[e] & 0xFFFFu)));
+                        v += __half2float(__ushort_as_half(static_cast<unsigned short>(w[e] >> 16)));
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) {
-            uint16_t hi, lo;
-            if constexpr (BF16) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(v);
-                hi = __bfloat16_as_ushort(h);
-                lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
-            } else {
-                const __half h = __float2half_rn(v);
-                hi = __half_as_ushort(h);
-                lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
-            }
-            uint16_t* row = out + static_cast<size_t>(m) * 2 * zpad;
-            row[z] = hi;
-            row[zpad + z] = lo;
+        uint16_t hi, lo;
+        if constexpr (BF16) {
+            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+            hi = __bfloat16_as_ushort(h);
+            lo = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(h)));
+        } else {
+            const __half h = __float2half_rn(v);
+            hi = __half_as_ushort(h);
+            lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
         }
+        uint16_t* row = out + static_cast<size_t>(m) * 2 * zpad;
+        row[z] = hi;
+        row[zpad + z] = lo;
     }
 }
 
@@ -544,15 +548,23 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
                 return WQ4_ERR_CUDA;
         }
         prm->sx_lo_col = zpad;
-        const long long warps = static_cast<long long>(zpad) * ld;
-        const int blocks = static_cast<int>(std::min<long long>((warps + 7) / 8, 65535));
+        const long long threads = static_cast<long long>(zpad) * ld;
+        const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, 65535));
         const uint16_t* x16 = static_cast<const uint16_t*>(X[0]);
-        if (dtype == WQ4_BF16) {
-            xsum_kernel<true><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, zpad, xs);
-        } else {
-            xsum_kernel<false><<<blocks, 256, 0, st>>>(x16, shapes[0].M, shapes[0].K, ld, span, zpad, xs);
-        }
-        if (cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(blocks, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = g_opt.pdl == 0 ? 1 : 0;
+        const int M0 = shapes[0].M, K0 = shapes[0].K;
+        const cudaError_t e = dtype == WQ4_BF16
+                                  ? cudaLaunchKernelEx(&cfg, xsum_kernel<true>, x16, M0, K0, ld, span, zpad, xs)
+                                  : cudaLaunchKernelEx(&cfg, xsum_kernel<false>, x16, M0, K0, ld, span, zpad, xs);
+        if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     }
     if (trace_on()) {
         std::fprintf(stderr,
