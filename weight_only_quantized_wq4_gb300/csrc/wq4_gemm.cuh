@@ -52,10 +52,11 @@ struct GemmCfg {
     static constexpr int kWarps = 4 + kDQW + kFW;
     // With wide token tiles the fold warps hold 64..96 fp32 accumulators each: registers move
     // to them from the other warpgroups (setmaxnreg). Launched with 128 per thread, the split
-    // (128 x 56 + 128 x 96 + 256 x 176 = 64512 for NT >= 128; 128 x 56 + 256 x 96 + 128 x 200 =
-    // 57344 for NT = 64) stays within the 512 x 128 = 65536 launched.
+    // (128 x 56 + 128 x 104 + 256 x 176 = 65536 for NT >= 128; 128 x 56 + 256 x 96 + 128 x 200 =
+    // 57344 for NT = 64) stays within the 512 x 128 = 65536 launched. The dequant warps hold one
+    // group's operand (64 words at NT >= 128) while the previous group's stores complete.
     static constexpr bool kRegSplit = NT >= 64;
-    static constexpr int kRegWg0 = 56, kRegDequant = 96, kRegFold = NT == 64 ? 200 : 176;
+    static constexpr int kRegWg0 = 56, kRegDequant = NT >= 128 ? 104 : 96, kRegFold = NT == 64 ? 200 : 176;
     static_assert(!kRegSplit || (128 * kRegWg0 + 32 * kDQW * kRegDequant + 32 * kFW * kRegFold <= kWarps * 32 * 128),
                   "register split exceeds the launched registers");
     static constexpr int kThreads = kWarps * 32;
@@ -599,6 +600,14 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             __syncwarp();
             if (lane == 0) mbar_arrive(afull_bar(a));
         };
+        // Software-pipelined: a step's operand is computed into registers first, then the previous
+        // step's stores are waited for and that buffer handed to the MMA warps, then this step's
+        // stores are issued, so the store latency overlaps the next step's bit work.
+        int pend_a = -1;                                 // buffer whose stores are in flight
+        auto handover = [&]() {
+            if (pend_a >= 0) operand_done(pend_a);
+            pend_a = -1;
+        };
         Sched<MAXP> sch(prm, blockIdx.x);
         Seg seg;
         int i = 0;                                       // steps (groups and zero steps)
@@ -609,7 +618,6 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 const int s = wi % C::kWStages;
                 const int a = i % C::kABufs;
                 if (!mbar_wait(wfull_bar(s), (wi / C::kWStages) & 1, ctl)) { ok = false; break; }
-                if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
                 const uint32_t rec = s_w0 + s * C::kWStageBytes;
                 uint32_t subs[H];                             // per scale set
 #pragma unroll
@@ -628,36 +636,41 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         subs[h] = BF16 ? 0x43084308u : 0x64086408u;   // 128 + 8 (bf16), 1024 + 8 (fp16)
                     }
                 }
+                uint32_t out[C::kChunks][16];
 #pragma unroll
                 for (int jj = 0; jj < C::kChunks; ++jj) {
                     const int j = part * C::kChunks + jj;
                     const uint32_t sub = subs[H == 2 ? (j >> 1) : 0];   // 32-K chunk j lies in set j / 2
                     const uint4 v = lds128(rec + rec_code_off(QT, r, j, H));
                     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t out[16];
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) out[4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub, nib);
+                        for (int e = 0; e < 4; ++e) out[jj][4 * w + e] = codes_to_pair<BF16>(wv[w] >> (4 * e), sub, nib);
                     }
-                    put_chunk(a, j, out);
                 }
-                operand_done(a);
-                if (lane == 0) mbar_arrive(wempty_bar(s));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wempty_bar(s));      // (the record is read)
+                handover();
+                if (!mbar_wait(aempty_bar(a), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
+#pragma unroll
+                for (int jj = 0; jj < C::kChunks; ++jj) put_chunk(a, part * C::kChunks + jj, out[jj]);
+                pend_a = a;
                 if (C::zstep_after(g, seg.g1)) {
                     // zero step: the staged zeros of this chunk's zero groups that lie in the segment
                     // (K 0..63 and again K 64..127, against the high and the low part of the sums);
                     // the rest of the 64 are zero
                     ++i;
                     const int a2 = i % C::kABufs;
-                    if (!mbar_wait(aempty_bar(a2), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
                     const int zc = (g * H) / 64;
                     const int zlo = max(seg.g0 * H - 64 * zc, 0), zhi = (g + 1) * H - 64 * zc;
+                    handover();
+                    if (!mbar_wait(aempty_bar(a2), ((i / C::kABufs) & 1) ^ 1u, ctl)) { ok = false; break; }
 #pragma unroll 1
                     for (int jj = 0; jj < C::kChunks; ++jj) {
                         const int j = part * C::kChunks + jj;
                         const int z0 = 32 * (j & 1);
-                        uint32_t out[16];
+                        uint32_t zo[16];
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
                             const int z = z0 + 2 * q;
@@ -665,12 +678,19 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wv) : "r"(zrow + 2 * z));
                             const uint32_t lo_ok = (z >= zlo && z < zhi) ? 0x0000FFFFu : 0u;
                             const uint32_t hi_ok = (z + 1 >= zlo && z + 1 < zhi) ? 0xFFFF0000u : 0u;
-                            out[q] = wv & (lo_ok | hi_ok);
+                            zo[q] = wv & (lo_ok | hi_ok);
                         }
-                        put_chunk(a2, j, out);
+                        put_chunk(a2, j, zo);
                     }
-                    operand_done(a2);
+                    pend_a = a2;
                 }
+            }
+        }
+        if (pend_a >= 0) {                               // the last step's operand
+            if (ok) {
+                handover();
+            } else if constexpr (ATMEM) {
+                tmem_st_wait();                          // no store in flight when the tensor memory is freed
             }
         }
     } else {
