@@ -103,8 +103,8 @@ def make_inputs(args):
         spec["qtype"] = I.U4_FZP
     if kind == "mm":
         return I.make_problem(**spec, group_size=args.group_size, scaled=not args.no_scales)
-    if args.group_size != I.GROUP or args.no_scales or args.epilogue or getattr(args, "float_zeros", False):
-        raise SystemExit("--group-size, --no-scales, --epilogue and --float-zeros apply to single-problem workloads")
+    if args.group_size != I.GROUP or args.no_scales or args.epilogue:
+        raise SystemExit("--group-size, --no-scales and --epilogue apply to single-problem workloads")
     return I.make_grouped(**spec)
 
 
@@ -259,7 +259,8 @@ class Workload:
             self.ws_bytes = wq4.grouped_dev_ptrs_workspace_bytes([p.M for p in plist], [p.N for p in plist],
                                                                  [p.K for p in plist], G)
         elif self.grouped:
-            self.ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist])
+            self.ws_bytes = wq4.grouped_workspace_bytes([p.M for p in plist], [p.N for p in plist], [p.K for p in plist],
+                                                        G, plist[0].qtype)
         else:
             self.ws_bytes = wq4.workspace_bytes(plist[0].M, plist[0].N, plist[0].K, G, plist[0].qtype)
         self.set_bytes = sum(x.numel() * 2 for x in base_X) + sum(w.numel() for w in self.base_W) + \

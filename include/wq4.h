@@ -24,11 +24,12 @@
  *    (code - 8) s), WQ4_U4_ZP (value = (code - z) s with a 4-bit zero point per group and row) or
  *    WQ4_U4_FZP (value = code s + zf with a float zero of the dtype per group and row, added after
  *    the scale: the scale-with-zero conversion of "machete_mainloop.cuh", transform_A_kblock;
- *    single-problem calls only).
- *  - group_size G: a multiple of 128 that divides K (G == K: one scale per row, channel-wise;
- *    "machete_mainloop.cuh", can_implement and load); other sizes give WQ4_ERR_UNSUPPORTED.
- *    N and K multiples of 128; M >= 0. The G passed to the GEMM calls must be the one the
- *    weight was prepacked with (the blob itself holds one scale per 128-K record).
+ *    not with device-resident shapes or pointers).
+ *  - group_size G: 64, or a multiple of 128 that divides K (G == K: one scale per row,
+ *    channel-wise; "machete_mainloop.cuh", can_implement and load); other sizes give
+ *    WQ4_ERR_UNSUPPORTED. N and K multiples of 128; M >= 0. The G passed to the GEMM calls must
+ *    be the one the weight was prepacked with (the blob holds one scale set per 128-K record,
+ *    two with G = 64).
  */
 #ifndef WQ4_H_
 #define WQ4_H_
@@ -103,9 +104,10 @@ int wq4_unprepack(const void* Wp, int N, int K, int group_size, int dtype, int q
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes);
 
 /* wq4_workspace_bytes for a given qtype. WQ4_U4_FZP on the tensor-core path (not the decode
- * kernel) adds a table of per-(128-K group, token) activation sums that a pre-pass writes on the
- * stream before the GEMM: ceil(K/128) x (M rounded up to the token tile) fp32 after the plan's
- * own bytes (256-byte aligned). For the other qtypes the answer equals wq4_workspace_bytes. */
+ * kernel) adds a table of activation sums that a pre-pass writes on the stream before the GEMM
+ * (per token and zero group of 128 K, or 64 with G = 64, split into a high and a low 16-bit
+ * part): (M rounded up to the token tile) x 2 x (zero groups rounded up to 64) x 2 bytes after the
+ * plan's own bytes (256-byte aligned). For the other qtypes the answer equals wq4_workspace_bytes. */
 int wq4_workspace_bytes_ex(int M, int N, int K, int group_size, int qtype, size_t* bytes);
 
 /* Y = X . dequant(Wp)^T.
@@ -134,6 +136,11 @@ int wq4_mm_ex(const void* X, const void* Wp, void* Y, int M, int N, int K, int g
  * zero-fill rule as wq4_workspace_bytes. */
 int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K, int group_size,
                                 size_t* bytes);
+
+/* The same for a weight format: float zeros (WQ4_U4_FZP) add the activation-sum tables of the
+ * problems' zero steps (see wq4_workspace_bytes_ex); other formats as wq4_grouped_workspace_bytes. */
+int wq4_grouped_workspace_bytes_ex(int P, const int* M, const int* N, const int* K, int group_size,
+                                   int qtype, size_t* bytes);
 
 /* P independent problems Y_p = X_p . dequant(Wp_p)^T in one launch (P <= 64).
  *   M, N, K            host arrays of P shapes; M[p] == 0 skips problem p (its pointers are

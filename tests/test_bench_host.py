@@ -96,5 +96,5 @@ def test_float_zeros_variant():
     assert p.qtype == I.U4_FZP and p.Z.dtype == np.uint16 and p.Z.shape == (p.K // 128, p.N)
     assert bench.variant_of(a)["qtype"].startswith("u4_fzp")
     assert bench.variant_bytes(p, a) == I.algorithmic_bytes(p.M, p.N, p.K, I.U4B8) + 2 * (p.K // 128) * p.N
-    with pytest.raises(SystemExit):
-        bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", float_zeros=True))
+    g = bench.make_inputs(_args(workload="grouped_8x_n14336_k4096_summ1024_bf16_u4b8", float_zeros=True))
+    assert all(q.qtype == I.U4_FZP and q.Z.dtype == np.uint16 for q in g) and sum(q.M for q in g) == 1024

@@ -510,14 +510,22 @@ def test_mm_float_zeros_epilogue(opts, M):
 
 
 def test_float_zeros_contract(lib):
-    """The activation-sum table is in the workspace query of the tensor-core path only; grouped
-    calls refuse the mode; a float-zero blob read as another qtype is reported."""
+    """The activation-sum tables are in the workspace query of the tensor-core path only (a table
+    per non-empty problem in the grouped query); device-resident shapes refuse the mode; a
+    float-zero blob read as another qtype is reported."""
+    import torch
     assert lib.workspace_bytes(8, 4096, 4096, qtype="u4_fzp") == 0
-    assert lib.workspace_bytes(300, 512, 1024, qtype="u4_fzp") >= 4 * 8 * 300
+    # at least 300 rows (M rounded up to the token tile) x 2 x 64 padded zero groups x 2 bytes
+    assert lib.workspace_bytes(300, 512, 1024, qtype="u4_fzp") >= 300 * 2 * 64 * 2
     assert lib.workspace_bytes(300, 512, 1024, qtype="u4_fzp") > lib.workspace_bytes(300, 512, 1024)
+    Ms, Ns, Ks = [30, 0, 34], [256, 256, 256], [512, 512, 512]
+    assert (lib.grouped_workspace_bytes(Ms, Ns, Ks, qtype="u4_fzp")
+            >= lib.grouped_workspace_bytes(Ms, Ns, Ks) + 2 * 64 * 2 * 64 * 2)
     probs = I.make_grouped(64, 2, 256, 512, "bf16", "u4_fzp", seed=4, M_list=[30, 34])
+    Xs = [to_cuda16(q.X_bits, "bf16") for q in probs]
     with pytest.raises(lib.Wq4Error) as e:
-        _grouped(lib, probs, "u4_fzp")
+        lib.grouped_mm_device_m(Xs, [gpu_prepack(lib, q) for q in probs],
+                                torch.tensor([30, 34], dtype=torch.int32, device="cuda"), [256, 256], qtype="u4_fzp")
     assert e.value.status == lib.ERR_UNSUPPORTED
     p = I.make_problem(40, 256, 512, "bf16", "u4_fzp", seed=41)
     blob = gpu_prepack(lib, p)
@@ -631,6 +639,23 @@ def test_grouped_small(lib, M_list):
         assert Y.shape == (p.M, p.N)
         if p.M:
             assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "grouped M=%d" % p.M)
+
+
+@pytest.mark.parametrize("dtype,G,M_list", [("bf16", 128, [0, 17, 40, 0, 200]), ("fp16", 128, [5, 130, 64]),
+                                             ("bf16", 64, [33, 0, 150, 8]), ("fp16", 512, [70, 1, 0])])
+def test_grouped_float_zeros(lib, dtype, G, M_list):
+    """Float zeros in the grouped call: every problem's zero steps read its own sums table."""
+    Ks = [1024, 512, 2048, 1024, 512][:len(M_list)]
+    Ns = [256, 384, 128, 256, 128][:len(M_list)]
+    probs = [I.make_problem(m, n, k, dtype, "u4_fzp", seed=60 + i, group_size=G)
+             for i, (m, n, k) in enumerate(zip(M_list, Ns, Ks))]
+    blobs = [gpu_prepack(lib, p) for p in probs]
+    Xs = [to_cuda16(p.X_bits, dtype) for p in probs]
+    outs = lib.grouped_mm(Xs, blobs, Ns, qtype="u4_fzp", group_size=G)
+    assert lib.get_last_error() == lib.OK
+    for p, Y in zip(probs, outs):
+        if p.M:
+            assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), "grouped float zeros %s" % ((p.M, p.N, p.K, G),))
 
 
 def test_grouped_mixed_shapes(lib):

@@ -62,6 +62,7 @@ def load_library(path: str = LIB_PATH):
                               ctypes.c_float, vp, vp, c_size, vp]),
         "wq4_grouped_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm": (c_int, [c_int, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
+        "wq4_grouped_workspace_bytes_ex": (c_int, [c_int, ip, ip, ip, c_int, c_int, ctypes.POINTER(c_size)]),
         "wq4_mm_static_scratch": (c_int, [vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp]),
         "wq4_grouped_device_m_workspace_bytes": (c_int, [c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm_device_m": (c_int, [c_int, vp, ip, ip, ip, vpp, vpp, vpp, c_int, c_int, c_int, vp, c_size, vp]),
@@ -182,12 +183,14 @@ def workspace_bytes(M: int, N: int, K: int, group_size: int = GROUP, qtype: str 
     return int(out.value)
 
 
-def grouped_workspace_bytes(Ms: Sequence[int], Ns: Sequence[int], Ks: Sequence[int], group_size: int = GROUP) -> int:
+def grouped_workspace_bytes(Ms: Sequence[int], Ns: Sequence[int], Ks: Sequence[int], group_size: int = GROUP,
+                            qtype: str = "u4b8") -> int:
     P = len(Ms)
     arr = ctypes.c_int * P
     out = ctypes.c_size_t(0)
-    _check(load_library().wq4_grouped_workspace_bytes(P, arr(*Ms), arr(*Ns), arr(*Ks), group_size, ctypes.byref(out)),
-           "wq4_grouped_workspace_bytes")
+    _check(load_library().wq4_grouped_workspace_bytes_ex(P, arr(*Ms), arr(*Ns), arr(*Ks), group_size, QTYPES[qtype],
+                                                         ctypes.byref(out)),
+           "wq4_grouped_workspace_bytes_ex")
     return int(out.value)
 
 
@@ -236,7 +239,7 @@ def grouped_mm(Xs: Sequence, blobs: Sequence, N: Sequence[int], qtype: str = "u4
     if outs is None:
         outs = [torch.empty((m, n), dtype=x.dtype, device=x.device) for x, m, n in zip(Xs, Ms, Ns)]
     if workspace is None:
-        workspace = alloc_workspace(grouped_workspace_bytes(Ms, Ns, Ks, group_size), Xs[0].device)
+        workspace = alloc_workspace(grouped_workspace_bytes(Ms, Ns, Ks, group_size, qtype), Xs[0].device)
     arr = ctypes.c_int * P
     ptrs = ctypes.c_void_p * P
     xp = ptrs(*[x.data_ptr() if m > 0 else None for x, m in zip(Xs, Ms)])

@@ -384,27 +384,41 @@ cudaError_t dispatch(const void* params, bool grouped, int nt, int dtype, int qt
 // Float-zero mode: the activation sums of every (token m, zero group z) for the GEMM's zero steps,
 // xs = the sum of X[m][span z .. span z + span - 1] in fp32 (span = 128, or 64 with two scale sets
 // per record), split into hi = xs rounded to the 16-bit type and lo = xs - hi rounded likewise
-// (hi + lo carries 16 (bf16) or 22 (fp16) significant bits). Table [ld][2 zpad] of 16-bit values:
-// hi at column z, lo at column zpad + z; zero for rows m >= M (up to ld) and for z >= K / span (up
-// to zpad, a multiple of 64), so that a zero step's copies never read past it and the masked-off
-// zeros never meet a NaN. One thread per (m, z), consecutive threads on consecutive z of a row:
-// 16-byte loads of its span, added in K order (the same order every run). Launched with
-// programmatic dependent launch: the GEMM behind it may set up at once, and X is read only once
-// the kernel ahead (which may write it) has completed.
+// (hi + lo carries 16 (bf16) or 22 (fp16) significant bits). One table per problem, [ld][2 zpad]
+// 16-bit values: hi at column z, lo at column zpad + z; zero for rows m >= M (up to ld) and for
+// z >= K / span (up to zpad, a multiple of 64), so that a zero step's copies never read past it and
+// the masked-off zeros never meet a NaN. One thread per (problem, m, z), consecutive threads on
+// consecutive z of a row: 16-byte loads of its span, added in K order (the same order every run).
+// Launched with programmatic dependent launch: the GEMM behind it may set up at once, and X is
+// read only once the kernel ahead (which may write it) has completed.
+struct XsumJob {
+    const uint16_t* X;
+    uint16_t* out;
+    int M, K, ld, zpad;
+    long long begin;             // first thread of this problem
+};
+struct XsumBatch {
+    int P, span;
+    long long total;             // threads over all problems
+    XsumJob job[kMaxGroupedProblems];
+};
+
 template <bool BF16>
-__global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld, int span, int zpad,
-                            uint16_t* __restrict__ out) {
+__global__ void xsum_kernel(const __grid_constant__ XsumBatch b) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int nz = K / span;
-    const long long total = static_cast<long long>(zpad) * ld;
-    for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+    for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < b.total;
          t += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int m = static_cast<int>(t / zpad), z = static_cast<int>(t % zpad);
+        int p = 0;
+        while (p + 1 < b.P && b.job[p + 1].begin <= t) ++p;
+        const XsumJob& J = b.job[p];
+        const long long u = t - J.begin;
+        const int m = static_cast<int>(u / J.zpad), z = static_cast<int>(u % J.zpad);
         float v = 0.f;
-        if (m < M && z < nz) {
-            const uint4* xp = reinterpret_cast<const uint4*>(X + static_cast<size_t>(m) * K + static_cast<size_t>(span) * z);
-            for (int c = 0; c < span / 8; ++c) {
+        if (m < J.M && z < J.K / b.span) {
+            const uint4* xp =
+                reinterpret_cast<const uint4*>(J.X + static_cast<size_t>(m) * J.K + static_cast<size_t>(b.span) * z);
+            for (int c = 0; c < b.span / 8; ++c) {
                 const uint4 q = __ldg(xp + c);
                 const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -429,9 +443,9 @@ __global__ void xsum_kernel(const uint16_t* __restrict__ X, int M, int K, int ld
             hi = __half_as_ushort(h);
             lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
         }
-        uint16_t* row = out + static_cast<size_t>(m) * 2 * zpad;
+        uint16_t* row = J.out + static_cast<size_t>(m) * 2 * J.zpad;
         row[z] = hi;
-        row[zpad + z] = lo;
+        row[J.zpad + z] = lo;
     }
 }
 
@@ -448,6 +462,16 @@ size_t xsum_table_bytes(int qtype, const Shape& s, int nt, int group_size) {
     return ld * 2 * zero_groups_padded(s.K, group_size) * 2;
 }
 
+// The tables of all P problems, each 256-byte aligned: total bytes (offsets relative to the first).
+size_t xsum_tables_bytes(int qtype, const Shape* shapes, int P, int nt, int group_size, size_t* offs = nullptr) {
+    size_t total = 0;
+    for (int p = 0; p < P; ++p) {
+        if (offs) offs[p] = total;
+        total += (xsum_table_bytes(qtype, shapes[p], nt, group_size) + 255) / 256 * 256;
+    }
+    return total;
+}
+
 // Plans and launches the GEMM kernel for P problems. With fixed_scratch the workspace is the
 // library's own array (kept between calls): the plan is bounded by its size and the counters it
 // uses are cleared on `st` first; otherwise it is the caller's (counters already zero).
@@ -458,9 +482,10 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc) return rc;
-    if (qtype == WQ4_U4_FZP && MAXP > 1) return WQ4_ERR_UNSUPPORTED;   // float zeros: single problems
-    // float zeros: the activation-sum table follows the plan's part of the workspace
-    const size_t xsum_bytes = xsum_table_bytes(qtype, shapes[0], pick_token_tile(shapes, P, group_size), group_size);
+    // float zeros: the activation-sum tables follow the plan's part of the workspace
+    size_t xsum_rel[MAXP];
+    const size_t xsum_bytes = xsum_tables_bytes(qtype, shapes, P, pick_token_tile(shapes, P, group_size), group_size,
+                                                xsum_rel);
     if (fixed_scratch && xsum_bytes + 256 > workspace_bytes) return WQ4_ERR_WORKSPACE;
     Plan pl;
     rc = make_plan(shapes, P, dev->sm_count, fixed_scratch ? workspace_bytes - xsum_bytes - 256 : SIZE_MAX, group_size,
@@ -531,28 +556,36 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     if (fixed_scratch && pl.counters_bytes && cudaMemsetAsync(workspace, 0, pl.counters_bytes, st) != cudaSuccess)
         return WQ4_ERR_CUDA;
     if (xsum_bytes) {                                           // the pre-pass, in stream order before the GEMM
-        uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + xsum_off);
-        const int ld = pl.m_tiles[0] * pl.nt;
-        const int zpad = zero_groups_padded(shapes[0].K, group_size);
-        const int span = kTileK / scale_sets(group_size);
-        {
-            EncodeTiledFn fn = encode_fn();
-            if (!fn) return WQ4_ERR_CUDA;
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return WQ4_ERR_CUDA;
+        XsumBatch xb;
+        std::memset(static_cast<void*>(&xb), 0, sizeof(xb));
+        xb.span = kTileK / scale_sets(group_size);
+        for (int p = 0; p < P; ++p) {
+            if (shapes[p].M <= 0) continue;
+            uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + xsum_off + xsum_rel[p]);
+            const int ld = pl.m_tiles[p] * pl.nt;
+            const int zpad = zero_groups_padded(shapes[p].K, group_size);
             const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * zpad), static_cast<cuuint64_t>(ld)};
             const cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * zpad) * 2};
             const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pl.nt)};
             const cuuint32_t estr[2] = {1, 1};
-            if (fn(&prm->sxmap, dtype == WQ4_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                   xs, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            if (fn(&prm->sxmap[p], dtype == WQ4_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   2, xs, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return WQ4_ERR_CUDA;
+            XsumJob& J = xb.job[xb.P++];
+            J.X = static_cast<const uint16_t*>(X[p]);
+            J.out = xs;
+            J.M = shapes[p].M;
+            J.K = shapes[p].K;
+            J.ld = ld;
+            J.zpad = zpad;
+            J.begin = xb.total;
+            xb.total += static_cast<long long>(ld) * zpad;
         }
-        prm->sx_lo_col = zpad;
-        const long long threads = static_cast<long long>(zpad) * ld;
-        const int blocks = static_cast<int>(std::min<long long>((threads + 255) / 256, 65535));
-        const uint16_t* x16 = static_cast<const uint16_t*>(X[0]);
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(blocks, 1, 1);
+        cfg.gridDim = dim3(static_cast<unsigned>(std::min<long long>((xb.total + 255) / 256, 65535)), 1, 1);
         cfg.blockDim = dim3(256, 1, 1);
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -560,10 +593,8 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = g_opt.pdl == 0 ? 1 : 0;
-        const int M0 = shapes[0].M, K0 = shapes[0].K;
-        const cudaError_t e = dtype == WQ4_BF16
-                                  ? cudaLaunchKernelEx(&cfg, xsum_kernel<true>, x16, M0, K0, ld, span, zpad, xs)
-                                  : cudaLaunchKernelEx(&cfg, xsum_kernel<false>, x16, M0, K0, ld, span, zpad, xs);
+        const cudaError_t e = dtype == WQ4_BF16 ? cudaLaunchKernelEx(&cfg, xsum_kernel<true>, xb)
+                                                : cudaLaunchKernelEx(&cfg, xsum_kernel<false>, xb);
         if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     }
     if (trace_on()) {
@@ -692,6 +723,19 @@ int wq4_workspace_bytes_ex(int M, int N, int K, int group_size, int qtype, size_
     return WQ4_OK;
 }
 
+int wq4_grouped_workspace_bytes_ex(int P, const int* M, const int* N, const int* K, int group_size, int qtype,
+                                   size_t* bytes) {
+    int rc = check_types(group_size, WQ4_BF16, qtype);
+    if (rc) return rc;
+    if ((rc = wq4_grouped_workspace_bytes(P, M, N, K, group_size, bytes))) return rc;
+    if (qtype != WQ4_U4_FZP) return WQ4_OK;
+    Shape shapes[kMaxGroupedProblems];
+    for (int p = 0; p < P; ++p) shapes[p] = Shape{M[p], N[p], K[p]};
+    const size_t xs = xsum_tables_bytes(qtype, shapes, P, pick_token_tile(shapes, P, group_size), group_size);
+    if (xs) *bytes = (*bytes + 255) / 256 * 256 + xs;
+    return WQ4_OK;
+}
+
 int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
     const int rc = wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
     if (rc == WQ4_OK && M > 0 && uses_decode_kernel(M, N, K)) *bytes = 0;   // that kernel needs none
@@ -774,7 +818,7 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
     if (P <= 0 || !M || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
-    if (P > kMaxGroupedProblems || qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;
+    if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
     Shape shapes[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) {
         if (M[p] < 0) return WQ4_ERR_INVALID;
@@ -890,7 +934,7 @@ int wq4_grouped_mm_device_m(int P, const int* M_dev, const int* M_cap, const int
                             int qtype, void* workspace, size_t workspace_bytes, wq4_stream_t stream) {
     int rc = check_types(group_size, dtype, qtype);
     if (rc) return rc;
-    if (qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;        // float zeros: single problems
+    if (qtype == WQ4_U4_FZP) return WQ4_ERR_UNSUPPORTED;        // float zeros: host-known shapes only
     if (P <= 0 || !M_dev || !M_cap || !N || !K || !X || !Wp || !Y) return WQ4_ERR_INVALID;
     if (P > kMaxGroupedProblems) return WQ4_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(M_dev) & 3) return WQ4_ERR_ALIGN;

@@ -494,9 +494,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                                 tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
                             } else {                     // zero groups [64 zc, 64 zc + 64): high, then low part
                                 const int zc = (g * H) / 64;
-                                tma_load_2d(stage, &prm.sxmap, xfull_bar(s), 64 * zc, seg.mt * NT, pol_stream);
-                                tma_load_2d(stage + C::kXPanel, &prm.sxmap, xfull_bar(s), prm.sx_lo_col + 64 * zc,
-                                            seg.mt * NT, pol_stream);
+                                const int zpad = (P.K / (kTileK / H) + 63) / 64 * 64;
+                                const CUtensorMap* sxm = &prm.sxmap[seg.prob];
+                                tma_load_2d(stage, sxm, xfull_bar(s), 64 * zc, seg.mt * NT, pol_stream);
+                                tma_load_2d(stage + C::kXPanel, sxm, xfull_bar(s), zpad + 64 * zc, seg.mt * NT, pol_stream);
                             }
                         }
                         if (!ok) break;

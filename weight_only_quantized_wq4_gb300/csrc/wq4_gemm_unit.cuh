@@ -26,9 +26,7 @@ cudaError_t unit_pick_q(const void* p, int qt, bool a_tmem, int grid, bool pdl, 
     switch (qt) {
         case kQtU4B8: return unit_pick_a<NT, H, GROUPED, BF16, kQtU4B8>(p, a_tmem, grid, pdl, st);
         case kQtU4Zp: return unit_pick_a<NT, H, GROUPED, BF16, kQtU4Zp>(p, a_tmem, grid, pdl, st);
-        default:   // float zeros: single-problem calls only (the activation sums are per call)
-            if constexpr (GROUPED) return cudaErrorInvalidValue;
-            else return unit_pick_a<NT, H, GROUPED, BF16, kQtU4FZp>(p, a_tmem, grid, pdl, st);
+        default: return unit_pick_a<NT, H, GROUPED, BF16, kQtU4FZp>(p, a_tmem, grid, pdl, st);
     }
 }
 

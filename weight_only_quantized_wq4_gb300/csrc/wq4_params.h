@@ -143,9 +143,10 @@ struct GemmParams {
     int hdr_trusted;         // 1: every blob was prepacked here for these arguments (records may be read
                              // while the headers are being checked); 0: check before the first read
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
-    CUtensorMap sxmap;       // float-zero mode: the activation sums per (token, zero group), split
-                             // into high and low 16-bit parts: [rows][sx_lo_col] high, then low;
-    int sx_lo_col;           // box (64, token tile), 128B swizzle (single-problem calls)
+    // float-zero mode: each problem's activation sums per (token, zero group), split into high and
+    // low 16-bit parts: [rows][2 zpad], high in columns [0, zpad), low in [zpad, 2 zpad), zpad =
+    // (K / zero-group span) rounded up to 64; box (64, token tile), 128B swizzle
+    CUtensorMap sxmap[MAXP];
     const ProblemDesc* prob_tab;    // device-resident problem table (num_problems entries), or null
     const CUtensorMap* xmap_tab;    // their activation tensor maps (patched on the device), or null
 };
