@@ -65,7 +65,7 @@ struct GemmCfg {
     static constexpr int kColParts = kFW / 4;                // fold warps per TMEM lane quarter
     static constexpr int kNC = NT / kColParts;               // accumulator columns per fold thread
     // epilogue: C values loaded together per thread (16 at NT = 192 spill the bf16 fold warps)
-    static constexpr int kEpiBatch = NT >= 192 ? 8 : 16;
+    static constexpr int kEpiBatch = 8;
     static constexpr int kRec = tile_record_bytes(QT, H);
     static constexpr int kXPanel = NT * 128;                 // one 64-K panel of NT token rows
     // Two rings: activation tiles (two panels per group; consumed by the MMA, released by its
@@ -108,7 +108,8 @@ struct GemmCfg {
     __device__ static bool zstep_after(int g, int g1) { return kZ && ((g + 1) % kZRec == 0 || g + 1 == g1); }
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
-    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? 8 : (kZ ? 4 : 6));
+    // (7 at NT = 128: the epilogue's C tile then fits beside four activation stages)
+    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? (NT == 128 ? 7 : 8) : (kZ ? 4 : 6));
     // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
     static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
     static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kZBytes - kWRingBytes) / kXStageBytes;
@@ -116,7 +117,12 @@ struct GemmCfg {
     // and waits on consecutive phases of it (a parity wait is unambiguous one phase ahead only; with
     // an odd count a warp would skip the other warp's phase of a slot).
     static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
-    static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kBarBytes;
+    // The fused epilogue's C tile ([NT][128] 16-bit, copied by TMA while the tile's groups run) where
+    // shared memory has room for it; otherwise the fold warps read C from global memory.
+    static constexpr int kCTile = NT * 128 * 2;
+    static constexpr int kCBytes =
+        kMaxDynSmem - (1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kBarBytes) >= kCTile ? kCTile : 0;
+    static constexpr int kSmemBytes = 1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kCBytes + kBarBytes;
     static constexpr int kColA = kPBufs * kPCols;            // TMEM column of A buffer 0
     static constexpr int kTmemNeed = kPBufs * kPCols + (ATMEM ? 64 * kABufs : 0);
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
@@ -295,40 +301,42 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
 }
 
 // Writes Y[m0 + j][n] = v[j0 + j] for j < nc (at most B) and m0 + j < Mrows, with the epilogue
-// when the call has one: alpha * v + beta * C[m][n] + bias[n] in fp32, rounded once (after the C
-// load and alpha / beta of the epilogue in "sm90_gemm_array_tma_warpspecialized_cooperative.hpp",
-// plus a bias per weight row). The C values of the B columns are loaded together (independent
-// loads in flight at once) before those outputs are formed; C may be Y itself, each element being
-// read and then written by the same thread. `bias` is the row's bias as float (used only when the
-// problem has one).
+// when the call has one: alpha * v + bias[n] + beta * C[m][n] in fp32 (after the C load and alpha /
+// beta of the epilogue in "sm90_gemm_array_tma_warpspecialized_cooperative.hpp", plus a bias per
+// weight row), rounded once. The epilogue rewrites the B values in registers without branches and
+// the stores are the plain path's; the C values of the B columns are loaded together (from the
+// tile's copy in shared memory when c_s != 0: this thread's element of the tile's first column),
+// and C may be Y itself, each element being read and then written by the same thread. `bias` is the
+// row's bias as float (0 without one).
 template <bool BF16, int B, int MAXP, int NV>
-__device__ __forceinline__ void store_cols(const GemmParams<MAXP>& prm, const ProblemDesc& P, const float (&v)[NV],
-                                           int j0, int nc, int m0, int n, int Mrows, float bias) {
+__device__ __forceinline__ void store_cols(const GemmParams<MAXP>& prm, const ProblemDesc& P, float (&v)[NV],
+                                           int j0, int nc, int m0, int n, int Mrows, float bias, uint32_t c_s = 0) {
     uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
-    if (!prm.has_epi) {
+    float* r = v + j0;                                   // (rewritten in place: the values are final here)
+    if (prm.has_epi) {
+        const float alpha = prm.alpha, beta = prm.beta;
 #pragma unroll
-        for (int j = 0; j < B; ++j)
-            if (j < nc && m0 + j < Mrows) y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(v[j0 + j]);
-        return;
-    }
-    uint16_t cv[B];
+        for (int j = 0; j < B; ++j) r[j] = fmaf(alpha, r[j], bias);
+        if (beta != 0.f) {
+            uint32_t cv[B];
+            if (c_s) {
 #pragma unroll
-    for (int j = 0; j < B; ++j) cv[j] = 0;
-    if (prm.beta != 0.f) {
-        const uint16_t* c = static_cast<const uint16_t*>(P.c);
+                for (int j = 0; j < B; ++j) {
+                    cv[j] = 0;
+                    if (j < nc) asm volatile("ld.shared.u16 %0, [%1];" : "=r"(cv[j]) : "r"(c_s + (j0 + j) * 256));
+                }
+            } else {
+                const uint16_t* c = static_cast<const uint16_t*>(P.c);
 #pragma unroll
-        for (int j = 0; j < B; ++j)
-            if (j < nc && m0 + j < Mrows) cv[j] = c[static_cast<size_t>(m0 + j) * P.N + n];
-    }
+                for (int j = 0; j < B; ++j) cv[j] = (j < nc && m0 + j < Mrows) ? c[static_cast<size_t>(m0 + j) * P.N + n] : 0u;
+            }
 #pragma unroll
-    for (int j = 0; j < B; ++j) {
-        if (j < nc && m0 + j < Mrows) {
-            float r = prm.alpha * v[j0 + j];
-            if (prm.beta != 0.f) r = fmaf(prm.beta, scale_to_float<BF16>(cv[j]), r);
-            if (P.bias) r += bias;
-            y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(r);
+            for (int j = 0; j < B; ++j) r[j] = fmaf(beta, scale_to_float<BF16>(static_cast<uint16_t>(cv[j])), r[j]);
         }
     }
+#pragma unroll
+    for (int j = 0; j < B; ++j)
+        if (j < nc && m0 + j < Mrows) y[static_cast<size_t>(m0 + j) * P.N + n] = float_to_out<BF16>(r[j]);
 }
 
 // The row's bias as float, 0 without one (or without the epilogue).
@@ -360,7 +368,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t s_w0 = s_x0 + C::kXStages * C::kXStageBytes;           // weight-record ring
     const uint32_t s_A = s_w0 + C::kWRingBytes;
     const uint32_t s_Z = s_A + C::kABytes;                                // float-zero staging
-    const uint32_t s_bar = s_Z + C::kZBytes;
+    const uint32_t s_C = s_Z + C::kZBytes;                                // epilogue C tile
+    const uint32_t s_bar = s_C + C::kCBytes;
     auto xfull_bar = [&](int s) { return s_bar + 8u * s; };
     auto xempty_bar = [&](int s) { return s_bar + 8u * (16 + s); };
     auto wfull_bar = [&](int s) { return s_bar + 8u * (32 + s); };
@@ -372,6 +381,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t drain_bar = s_bar + 8u * 80;
     const uint32_t fsync_bar = s_bar + 8u * 81;   // fold warps meet here in the split epilogue
     const uint32_t stall_bar = s_bar + 8u * 82;   // never arrived on (test of the timeout path)
+    const uint32_t cfull_bar = s_bar + 8u * 83;   // the epilogue's C tile landed
+    const uint32_t cempty_bar = s_bar + 8u * 84;  // ... and was read by the fold warps
+    // C through shared memory: whole tiles of a fused epilogue that reads C, where it fits
+    const bool c_smem = C::kCBytes > 0 && prm.has_epi && prm.beta != 0.f;
     uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 88;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
@@ -402,6 +415,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         mbar_init(drain_bar, 2);                 // one commit from each MMA warp
         mbar_init(fsync_bar, C::kFW);
         mbar_init(stall_bar, 1);
+        mbar_init(cfull_bar, 1);
+        mbar_init(cempty_bar, C::kFW);
         *abort_flag = 0;
         *fin_flag = 0;
         fence_mbar_init();
@@ -746,6 +761,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             if (lane == 0) mbar_arrive(pempty_bar(b));
             return true;
         };
+        int ct = 0;                                      // whole tiles whose C came through shared memory
+        int c_issued = 0;                                // C copies issued (fold warp 0, lane 0)
         int i = 0;                                       // steps (groups and zero steps)
         int wi = 0;                                      // weight records
         bool ok = true;
@@ -757,6 +774,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 if (g == seg.g0) {
 #pragma unroll
                     for (int j = 0; j < C::kNC; ++j) acc[j] = 0.f;
+                    // The epilogue's C load ("sm90_gemm_array_tma_warpspecialized_cooperative.hpp",
+                    // the epilogue load), issued by one fold thread as a whole tile starts, once every
+                    // fold warp has read the previous tile's C: it lands while the tile's groups run.
+                    // (a wait that runs out issues nothing: the epilogue's wait for the copy then runs out)
+                    if (c_smem && seg.slot == -1 && f == 0 && lane == 0 &&
+                        mbar_wait(cempty_bar, static_cast<uint32_t>(ct & 1) ^ 1u, ctl)) {
+                        mbar_arrive_expect_tx(cfull_bar, C::kCTile);
+                        tma_load_2d(s_C, &prm.cmap, cfull_bar, seg.nt * kTileN, seg.mt * NT, policy_evict_first());
+                        c_issued = ct + 1;
+                    }
                 }
                 float sc[H];                                    // the record's scale per set
 #pragma unroll
@@ -853,9 +880,19 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             }
             const float bias = row_bias<BF16>(prm, P, n);
             constexpr int kB = C::kEpiBatch;
+            // a whole tile reads its C from shared memory (copied while its groups ran)
+            const bool cs = c_smem && seg.slot == -1;
+            if (cs && !mbar_wait(cfull_bar, static_cast<uint32_t>(ct & 1), ctl)) { ok = false; break; }
+            const uint32_t c_s = cs ? s_C + static_cast<uint32_t>((col0 * 128 + r) * 2) : 0u;
 #pragma unroll
             for (int j0 = 0; j0 < C::kNC; j0 += kB)
-                store_cols<BF16, kB>(prm, P, acc, j0, C::kNC - j0 < kB ? C::kNC - j0 : kB, m0 + j0, n, Mrows, bias);
+                store_cols<BF16, kB>(prm, P, acc, j0, C::kNC - j0 < kB ? C::kNC - j0 : kB, m0 + j0, n, Mrows, bias,
+                                     c_s);
+            if (cs) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cempty_bar);
+                ++ct;
+            }
         }
         if (prm.cluster_split > 0) {
             cluster_sync();   // every rank's partial is in its shared memory
@@ -902,6 +939,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             }
             cluster_sync();   // no CTA leaves while another still reads its shared memory
         }
+        // the last C copy lands before the CTA can leave (whether or not the epilogue read it)
+        if (f == 0 && lane == 0 && c_issued > 0)
+            mbar_wait_plain(cfull_bar, static_cast<uint32_t>(c_issued - 1) & 1u, drain_limit(prm.timeout_cycles));
     }
     if (prm.cluster_split > 0 && warp < 4 + C::kDQW) {
         cluster_sync();

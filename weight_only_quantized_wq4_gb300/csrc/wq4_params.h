@@ -147,6 +147,9 @@ struct GemmParams {
     // low 16-bit parts: [rows][2 zpad], high in columns [0, zpad), low in [zpad, 2 zpad), zpad =
     // (K / zero-group span) rounded up to 64; box (64, token tile), 128B swizzle
     CUtensorMap sxmap[MAXP];
+    // the fused epilogue's C ([M][N] 16-bit; box (128, token tile), rows past M zero): single-problem
+    // calls with beta != 0, copied into shared memory per whole tile where the kernel has room
+    CUtensorMap cmap;
     const ProblemDesc* prob_tab;    // device-resident problem table (num_problems entries), or null
     const CUtensorMap* xmap_tab;    // their activation tensor maps (patched on the device), or null
 };
