@@ -658,6 +658,49 @@ def test_grouped_float_zeros(lib, dtype, G, M_list):
             assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), "grouped float zeros %s" % ((p.M, p.N, p.K, G),))
 
 
+GROUPED_DECODE = [
+    ("bf16", "u4b8", 128, [8, 8, 8, 8]),
+    ("fp16", "u4_zp", 128, [1, 0, 16, 5, 0]),
+    ("bf16", "u4_fzp", 128, [3, 32, 17]),
+    ("bf16", "u4b8", 64, [12, 0, 7]),
+    ("fp16", "u4_fzp", 64, [2, 9]),
+    ("bf16", "u4_zp", 128, [24, 1]),
+]
+
+
+@pytest.mark.parametrize("dtype,qtype,G,M_list", GROUPED_DECODE)
+def test_grouped_decode_kernel(opts, dtype, qtype, G, M_list):
+    """Grouped calls whose problems all have at most 32 tokens take the decode kernel in one launch
+    (no workspace); the same call with the decode kernel switched off takes the GEMM."""
+    lib = opts
+    Ns = [4096, 512, 1024, 384, 256, 640][:len(M_list)]
+    Ks = [1024, 2048, 512, 1024, 768, 1536][:len(M_list)]
+    probs = [I.make_problem(m, n, k, dtype, qtype, seed=80 + i, group_size=G)
+             for i, (m, n, k) in enumerate(zip(M_list, Ns, Ks))]
+    blobs = [gpu_prepack(lib, p) for p in probs]
+    Xs = [to_cuda16(p.X_bits, dtype) for p in probs]
+    assert lib.grouped_workspace_bytes(M_list, Ns, Ks, G, qtype) == 0
+    for decode in (0, -1):
+        lib.set_option(lib.OPT_DECODE, decode)
+        outs = lib.grouped_mm(Xs, blobs, Ns, qtype=qtype, group_size=G)
+        assert lib.get_last_error() == lib.OK
+        for p, Y in zip(probs, outs):
+            if p.M:
+                assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), "grouped decode=%d %s" % (decode, (p.M, p.N, p.K)))
+
+
+def test_grouped_decode_many_problems(lib):
+    """64 decode-sized problems in one launch, every CTA on blocks of its own problem."""
+    rng = np.random.default_rng(64)
+    M_list = [int(v) for v in rng.integers(0, 9, size=64)]
+    probs = [I.make_problem(m, 256, 512, "bf16", "u4b8", seed=200 + i) for i, m in enumerate(M_list)]
+    outs = _grouped(lib, probs, "u4b8")
+    assert lib.get_last_error() == lib.OK
+    for p, Y in zip(probs, outs):
+        if p.M:
+            assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "64 problems, M=%d" % p.M)
+
+
 def test_grouped_mixed_shapes(lib):
     """Per-problem N and K differ."""
     shapes = [(9, 128, 256), (70, 384, 128), (0, 256, 512), (150, 256, 640)]

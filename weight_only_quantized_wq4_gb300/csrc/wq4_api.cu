@@ -166,6 +166,21 @@ int decode_rows_per_launch(int M, int N, int K) {
 
 bool uses_decode_kernel(int M, int N, int K) { return decode_rows_per_launch(M, N, K) > 0; }
 
+// A grouped call whose non-empty problems all have at most 32 tokens takes the decode kernel, in
+// one launch (under the same options as a single problem does).
+bool grouped_uses_decode(int P, const int* M, const int* K) {
+    const bool auto_decode = g_opt.decode == 0 && !g_opt.token_tile && !g_opt.grid && !g_opt.split_all &&
+                             !g_opt.cluster && !g_opt.a_in_smem;
+    if (!(g_opt.decode == 1 || auto_decode)) return false;
+    int Mmax = 0, Kmax = 0;
+    for (int p = 0; p < P; ++p) {
+        if (M[p] <= 0) continue;
+        Mmax = std::max(Mmax, M[p]);
+        Kmax = std::max(Kmax, K[p]);
+    }
+    return Mmax > 0 && decode_fits(Mmax, Kmax);
+}
+
 int check_nk(int N, int K) {
     if (N <= 0 || K <= 0) return WQ4_ERR_INVALID;
     if (N % kTileN || K % kTileK) return WQ4_ERR_UNSUPPORTED;
@@ -715,6 +730,10 @@ int wq4_grouped_workspace_bytes(int P, const int* M, const int* N, const int* K,
     }
     DeviceInfo* dev = nullptr;
     if ((rc = device_info(&dev))) return rc;
+    if (grouped_uses_decode(P, M, K)) {                        // the decode kernel needs none
+        *bytes = 0;
+        return WQ4_OK;
+    }
     Plan pl;
     if ((rc = make_plan(shapes, P, dev->sm_count, SIZE_MAX, group_size, &pl))) return rc;
     *bytes = pl.workspace();
@@ -740,7 +759,7 @@ int wq4_grouped_workspace_bytes_ex(int P, const int* M, const int* N, const int*
     int rc = check_types(group_size, WQ4_BF16, qtype);
     if (rc) return rc;
     if ((rc = wq4_grouped_workspace_bytes(P, M, N, K, group_size, bytes))) return rc;
-    if (qtype != WQ4_U4_FZP) return WQ4_OK;
+    if (qtype != WQ4_U4_FZP || grouped_uses_decode(P, M, K)) return WQ4_OK;
     Shape shapes[kMaxGroupedProblems];
     for (int p = 0; p < P; ++p) shapes[p] = Shape{M[p], N[p], K[p]};
     const size_t xs = xsum_tables_bytes(qtype, shapes, P, pick_token_tile(shapes, P, group_size), group_size);
@@ -752,6 +771,22 @@ int wq4_workspace_bytes(int M, int N, int K, int group_size, size_t* bytes) {
     const int rc = wq4_grouped_workspace_bytes(1, &M, &N, &K, group_size, bytes);
     if (rc == WQ4_OK && M > 0 && uses_decode_kernel(M, N, K)) *bytes = 0;   // that kernel needs none
     return rc;
+}
+
+// The decode kernel's launch settings from the options.
+static DecodeLaunch decode_launch(DeviceInfo* dev, EncodeTiledFn fn, bool hdr_trusted) {
+    DecodeLaunch L;
+    L.sm_count = dev->sm_count;
+    L.status = dev->status;
+    L.timeout_cycles = timeout_cycles();
+    L.encode_fn = reinterpret_cast<void*>(fn);
+    L.pdl = g_opt.pdl == 0;
+    L.test_stall = g_opt.test_stall;
+    L.const_weights = g_opt.const_weights;
+    L.trigger_late = g_opt.decode_trigger == 0 ? 1 : 0;
+    L.depth = g_opt.decode_depth;
+    L.hdr_trusted = hdr_trusted ? 1 : 0;
+    return L;
 }
 
 static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, int group_size, int dtype,
@@ -780,17 +815,8 @@ static int mm_impl(const void* X, const void* Wp, void* Y, int M, int N, int K, 
                 e_part = *epi;
                 if (e_part.c) e_part.c = static_cast<const uint8_t*>(e_part.c) + static_cast<size_t>(m0) * N * 2;
             }
-            DecodeLaunch L;
-            L.sm_count = dev->sm_count;
-            L.status = dev->status;
-            L.timeout_cycles = timeout_cycles();
-            L.encode_fn = reinterpret_cast<void*>(fn);
-            L.pdl = g_opt.pdl == 0;
-            L.test_stall = g_opt.test_stall;
-            L.const_weights = g_opt.const_weights;
-            L.trigger_late = g_opt.decode_trigger == 0 ? 1 : 0;
-            L.depth = g_opt.decode_depth;
-            L.hdr_trusted = blob_trusted(Wp, BlobKey{N, K, group_size, dtype, qtype}) ? 1 : 0;
+            const DecodeLaunch L =
+                decode_launch(dev, fn, blob_trusted(Wp, BlobKey{N, K, group_size, dtype, qtype}));
             int grid = 0, depth = 0;
             const cudaError_t e = launch_decode(L, x, Wp, y, mr, N, K, group_size, dtype, qtype, epi ? &e_part : nullptr,
                                                 &grid, &depth, stream);
@@ -841,6 +867,37 @@ int wq4_grouped_mm(int P, const int* M, const int* N, const int* K, const void* 
             if (!aligned16(X[p]) || !aligned16(Wp[p]) || !aligned16(Y[p])) return WQ4_ERR_ALIGN;
         }
         shapes[p] = Shape{M[p], N[p], K[p]};
+    }
+    if (grouped_uses_decode(P, M, K)) {
+        // decode-sized: the non-empty problems in one launch of the decode kernel (no workspace)
+        DeviceInfo* dev = nullptr;
+        if ((rc = device_info(&dev))) return rc;
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return WQ4_ERR_CUDA;
+        const void* xs[kMaxGroupedProblems];
+        const void* wps[kMaxGroupedProblems];
+        void* ys[kMaxGroupedProblems];
+        int ms[kMaxGroupedProblems], ns[kMaxGroupedProblems], ks[kMaxGroupedProblems];
+        int n = 0;
+        bool trusted = true;
+        for (int p = 0; p < P; ++p) {
+            if (M[p] == 0) continue;
+            xs[n] = X[p];
+            wps[n] = Wp[p];
+            ys[n] = Y[p];
+            ms[n] = M[p];
+            ns[n] = N[p];
+            ks[n] = K[p];
+            trusted = trusted && blob_trusted(Wp[p], BlobKey{N[p], K[p], group_size, dtype, qtype});
+            ++n;
+        }
+        int grid = 0, depth = 0;
+        const cudaError_t e = launch_decode_grouped(decode_launch(dev, fn, trusted), n, xs, wps, ys, ms, ns, ks, group_size,
+                                                    dtype, qtype, &grid, &depth, stream);
+        if (trace_on())
+            std::fprintf(stderr, "[wq4] grouped decode kernel: problems=%d grid=%d ring=%d (%s)\n", n, grid, depth,
+                         e == cudaSuccess ? "ok" : cudaGetErrorString(e));
+        return e == cudaSuccess ? WQ4_OK : WQ4_ERR_CUDA;
     }
     return run_gemm<kMaxGroupedProblems>(shapes, P, X, Wp, Y, group_size, dtype, qtype, workspace, workspace_bytes,
                                          false, stream);

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <memory>
 
 #include "wq4_device.cuh"
 #include "wq4_launch.h"
@@ -46,15 +47,27 @@ constexpr int kDecMaxDepth = 16;
 constexpr int kDecMaxSmem = 232448;
 constexpr int kDecCoResident = 115712;                  // two CTAs of at most this much fit on one SM
 
-struct DecodeParams {
+// One problem of a launch: its operands, sizes and first CTA (a grouped launch gives each problem
+// a contiguous range of CTAs; each CTA works on row blocks of its own problem only).
+struct DecodeProblem {
     CUtensorMap xmap;        // X: 3-D (64, M, K/64) 16-bit, box (64, Mpad, 16), 128-byte swizzle
     CUtensorMap wmap;        // blob blocks: 4-D (block_bytes / 8, 8, K/128, N/128) u64, box (.., 1, 8, 1)
     const uint32_t* hdr;     // blob header
     void* y;                 // [M][N]
-    int M, N, K, group_size, dtype, qtype;
+    const void* c;           // epilogue C [M][N], read when beta != 0 (may be Y itself); single problems
+    const void* bias;        // epilogue bias [N] or null; single problems
+    int M, N, K;
     int k_groups;
     int n_blocks;            // N / 16
     int n_stages;            // ceil(k_groups / 8): weight stages per block = activation pieces
+    int cta_begin;           // first CTA of this problem
+};
+
+template <int MAXP>
+struct DecodeParams {
+    DecodeProblem prob[MAXP];
+    int num_problems;
+    int group_size, dtype, qtype;
     int depth;               // ring slots
     unsigned int* status;
     long long timeout_cycles;
@@ -65,8 +78,6 @@ struct DecodeParams {
                              // copied while the header is checked (else only after the check passed)
     int has_epi;             // 1: Y = alpha acc + beta C + bias (else Y = acc)
     float alpha, beta;
-    const void* c;           // [M][N], read when beta != 0 (may be Y itself)
-    const void* bias;        // [N] or null
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
 };
 
@@ -158,9 +169,23 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     }
 }
 
-template <int NB, bool BF16, int QT, int H>
-__global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kernel(const __grid_constant__ DecodeParams prm) {
+template <int NB, bool BF16, int QT, int H, int MAXP>
+__global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1)
+    wq4_decode_kernel(const __grid_constant__ DecodeParams<MAXP> prm) {
     using C = DecCfg<NB>;
+    // this CTA's problem (the last whose first CTA is <= blockIdx.x), its index and CTA count there
+    int pidx = 0;
+    if constexpr (MAXP > 1) {
+        int lo = 0, hi = prm.num_problems - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prm.prob[mid].cta_begin <= static_cast<int>(blockIdx.x)) lo = mid; else hi = mid - 1;
+        }
+        pidx = lo;
+    }
+    const DecodeProblem& Q = prm.prob[pidx];
+    const int cta = static_cast<int>(blockIdx.x) - Q.cta_begin;
+    const int ncta = (pidx + 1 < prm.num_problems ? prm.prob[pidx + 1].cta_begin : static_cast<int>(gridDim.x)) - Q.cta_begin;
     constexpr int kBB = block_bytes(QT, H);
     constexpr int kStage = dec_stage_bytes(QT, H);
     constexpr int kZ = block_zero_off(H);
@@ -168,7 +193,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
     const int depth = prm.depth;
-    const int n_st = prm.n_stages;
+    const int n_st = Q.n_stages;
     const uint32_t x_bytes = static_cast<uint32_t>(n_st) * C::kPieceBytes;
     const uint32_t x_region = x_bytes > static_cast<uint32_t>(C::kRedBytes) ? x_bytes : C::kRedBytes;
     const uint32_t s_x = sbase;                                        // activations, later the partials
@@ -183,8 +208,8 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // this CTA's blocks [bb0, bb0 + nbc) and the K slices per block
-    const int bb0 = static_cast<int>((static_cast<long long>(blockIdx.x) * prm.n_blocks) / gridDim.x);
-    const int nbc = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * prm.n_blocks) / gridDim.x) - bb0;
+    const int bb0 = static_cast<int>((static_cast<long long>(cta) * Q.n_blocks) / ncta);
+    const int nbc = static_cast<int>((static_cast<long long>(cta + 1) * Q.n_blocks) / ncta) - bb0;
     const int KS = kDecWarps / nbc;
     const int n_items = nbc * n_st;                                    // weight stages of this CTA
     // Ring slots per block: block b uses slots [b Db, (b + 1) Db), stage s of it slot b Db + s % Db
@@ -195,7 +220,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
     // with constant weights the producer fetches the blob header first thing (its latency then
     // overlaps the set-up below); otherwise only after the kernel ahead has completed
     BlobHeader hdr{};
-    if (warp == kDecWarps && lane == 0 && prm.early) hdr = load_blob_header(prm.hdr);
+    if (warp == kDecWarps && lane == 0 && prm.early) hdr = load_blob_header(Q.hdr);
     if (threadIdx.x == 0) {
         for (int i = 0; i < depth; ++i) {
             mbar_init(full_bar(i), 1);
@@ -214,8 +239,8 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
     if (warp == kDecWarps) {
         // ------------------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tensormap(&prm.xmap);
-            prefetch_tensormap(&prm.wmap);
+            prefetch_tensormap(&Q.xmap);
+            prefetch_tensormap(&Q.wmap);
             const uint64_t pol = policy_evict_first();
             // item `issued` = (stage is, block ib); its slot and the stage's position in the block's slots
             int is = 0, ib = 0, isd = 0;
@@ -224,7 +249,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
                 const int slot = ib * Db + isd;
                 mbar_arrive_expect_tx(full_bar(slot), kStage);
                 const int b = bb0 + ib;
-                tma_load_4d(s_w + slot * kStage, &prm.wmap, full_bar(slot), 0, b & 7, is * kDecStageGroups, b >> 3, pol);
+                tma_load_4d(s_w + slot * kStage, &Q.wmap, full_bar(slot), 0, b & 7, is * kDecStageGroups, b >> 3, pol);
                 ++issued;
                 if (++ib == nbc) {
                     ib = 0;
@@ -242,9 +267,9 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
             if (prm.early) {
                 if (trusted) {
                     while (issued < first) issue_next();
-                    ok = blob_header_matches(hdr, prm.N, prm.K, prm.group_size, prm.dtype, prm.qtype);
+                    ok = blob_header_matches(hdr, Q.N, Q.K, prm.group_size, prm.dtype, prm.qtype);
                 } else {
-                    ok = blob_header_matches(hdr, prm.N, prm.K, prm.group_size, prm.dtype, prm.qtype);
+                    ok = blob_header_matches(hdr, Q.N, Q.K, prm.group_size, prm.dtype, prm.qtype);
                     while (ok && issued < first) issue_next();
                 }
             }
@@ -252,14 +277,14 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
             // activations: one copy per 8 groups (rows past M and K past the end read as zero)
             for (int p = 0; p < n_st; ++p) {
                 mbar_arrive_expect_tx(xfull_bar(p), C::kPieceBytes);
-                tma_load_3d(s_x + p * C::kPieceBytes, &prm.xmap, xfull_bar(p), 0, 0, 2 * kDecStageGroups * p);
+                tma_load_3d(s_x + p * C::kPieceBytes, &Q.xmap, xfull_bar(p), 0, 0, 2 * kDecStageGroups * p);
             }
             if (!prm.early) {
                 if (trusted) {
                     while (issued < first) issue_next();
-                    ok = blob_header_ok(prm.hdr, prm.N, prm.K, prm.group_size, prm.dtype, prm.qtype);
+                    ok = blob_header_ok(Q.hdr, Q.N, Q.K, prm.group_size, prm.dtype, prm.qtype);
                 } else {
-                    ok = blob_header_ok(prm.hdr, prm.N, prm.K, prm.group_size, prm.dtype, prm.qtype);
+                    ok = blob_header_ok(Q.hdr, Q.N, Q.K, prm.group_size, prm.dtype, prm.qtype);
                     while (ok && issued < first) issue_next();
                 }
             }
@@ -310,7 +335,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
             ok = mbar_wait(full_bar(slot), ph, ctl);
             if (!ok) break;
             const int g_lo = s * kDecStageGroups;
-            const int g_hi = min(g_lo + kDecStageGroups, prm.k_groups);
+            const int g_hi = min(g_lo + kDecStageGroups, Q.k_groups);
             const uint32_t st = s_w + slot * kStage;
             if (next_g < g_hi) {                                        // this stage's activation piece
                 ok = mbar_wait(xfull_bar(s), 0, ctl);
@@ -461,21 +486,21 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
     __syncthreads();
     // (consumer threads only: they have all waited for the kernel ahead before touching C or Y)
     const int n_out = nbc * NB * 128;
-    uint16_t* y = reinterpret_cast<uint16_t*>(prm.y);
+    uint16_t* y = reinterpret_cast<uint16_t*>(Q.y);
     for (int t = threadIdx.x; warp < kDecWarps && t < n_out; t += kDecWarps * 32) {
         const int ob = t / (NB * 128), orem = t % (NB * 128);
         const int onb = orem / 128, olane = (orem % 128) >> 2, ot = orem & 3;
         const int om = onb * 8 + 2 * (olane & 3) + (ot & 1);
         const int on = (bb0 + ob) * 16 + (olane >> 2) + (ot >> 1) * 8;
-        if (om >= prm.M) continue;
+        if (om >= Q.M) continue;
         float v = 0.f;
         for (int sl = 0; sl < KS; ++sl)
             v += *reinterpret_cast<const float*>(sm + (((ob * KS + sl) * NB + onb) * 32 + olane) * 16 + 4 * ot);
         if (prm.has_epi) {                                              // alpha acc + beta C + bias, rounded once
             v *= prm.alpha;
             if (prm.beta != 0.f)
-                v = fmaf(prm.beta, dec_to_float<BF16>(static_cast<const uint16_t*>(prm.c)[static_cast<size_t>(om) * prm.N + on]), v);
-            if (prm.bias) v += dec_to_float<BF16>(static_cast<const uint16_t*>(prm.bias)[on]);
+                v = fmaf(prm.beta, dec_to_float<BF16>(static_cast<const uint16_t*>(Q.c)[static_cast<size_t>(om) * Q.N + on]), v);
+            if (Q.bias) v += dec_to_float<BF16>(static_cast<const uint16_t*>(Q.bias)[on]);
         }
         uint16_t o;
         if constexpr (BF16) {
@@ -483,7 +508,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1) wq4_decode_kerne
         } else {
             o = __half_as_ushort(__float2half_rn(v));
         }
-        y[static_cast<size_t>(om) * prm.N + on] = o;
+        y[static_cast<size_t>(om) * Q.N + on] = o;
     }
 }
 
@@ -534,10 +559,9 @@ bool decode_fits(int M, int K) {
     return decode_smem_bytes(dec_nb(M), K, 2, kQtU4FZp, 2) <= kDecMaxSmem;   // the largest records
 }
 
-template <int NB, bool BF16, int QT, int H>
-static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStream_t st) {
-    auto kern = wq4_decode_kernel<NB, BF16, QT, H>;
-    const int smem = decode_smem_bytes(NB, p.K, p.depth, QT, H);
+template <int NB, bool BF16, int QT, int H, int MAXP>
+static cudaError_t go_decode(const DecodeParams<MAXP>& p, int smem, int grid, bool pdl, cudaStream_t st) {
+    auto kern = wq4_decode_kernel<NB, BF16, QT, H, MAXP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -555,43 +579,52 @@ static cudaError_t go_decode(const DecodeParams& p, int grid, bool pdl, cudaStre
     return cudaGetLastError();
 }
 
-template <int NB, int H>
-static cudaError_t pick_decode_q(const DecodeParams& p, bool bf16, int qt, int grid, bool pdl, cudaStream_t st) {
+template <int NB, int H, int MAXP>
+static cudaError_t pick_decode_q(const DecodeParams<MAXP>& p, bool bf16, int qt, int smem, int grid, bool pdl,
+                                 cudaStream_t st) {
     switch (qt) {
-        case kQtU4B8: return bf16 ? go_decode<NB, true, kQtU4B8, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4B8, H>(p, grid, pdl, st);
-        case kQtU4Zp: return bf16 ? go_decode<NB, true, kQtU4Zp, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4Zp, H>(p, grid, pdl, st);
-        default: return bf16 ? go_decode<NB, true, kQtU4FZp, H>(p, grid, pdl, st) : go_decode<NB, false, kQtU4FZp, H>(p, grid, pdl, st);
+        case kQtU4B8:
+            return bf16 ? go_decode<NB, true, kQtU4B8, H>(p, smem, grid, pdl, st)
+                        : go_decode<NB, false, kQtU4B8, H>(p, smem, grid, pdl, st);
+        case kQtU4Zp:
+            return bf16 ? go_decode<NB, true, kQtU4Zp, H>(p, smem, grid, pdl, st)
+                        : go_decode<NB, false, kQtU4Zp, H>(p, smem, grid, pdl, st);
+        default:
+            return bf16 ? go_decode<NB, true, kQtU4FZp, H>(p, smem, grid, pdl, st)
+                        : go_decode<NB, false, kQtU4FZp, H>(p, smem, grid, pdl, st);
     }
 }
 
-template <int NB>
-static cudaError_t pick_decode(const DecodeParams& p, bool bf16, int qt, int H, int grid, bool pdl, cudaStream_t st) {
-    return H == 2 ? pick_decode_q<NB, 2>(p, bf16, qt, grid, pdl, st) : pick_decode_q<NB, 1>(p, bf16, qt, grid, pdl, st);
+template <int MAXP>
+static cudaError_t pick_decode(const DecodeParams<MAXP>& p, int nb, bool bf16, int qt, int H, int smem, int grid,
+                               bool pdl, cudaStream_t st) {
+    switch (nb) {
+        case 1:
+            return H == 2 ? pick_decode_q<1, 2>(p, bf16, qt, smem, grid, pdl, st) : pick_decode_q<1, 1>(p, bf16, qt, smem, grid, pdl, st);
+        case 2:
+            return H == 2 ? pick_decode_q<2, 2>(p, bf16, qt, smem, grid, pdl, st) : pick_decode_q<2, 1>(p, bf16, qt, smem, grid, pdl, st);
+        default:
+            return H == 2 ? pick_decode_q<4, 2>(p, bf16, qt, smem, grid, pdl, st) : pick_decode_q<4, 1>(p, bf16, qt, smem, grid, pdl, st);
+    }
 }
 
-// Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
-cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, void* Y, int M, int N, int K,
-                          int group_size, int dtype, int qtype, const EpilogueArgs* epi, int* grid_out,
-                          int* depth_out, cudaStream_t st) {
-    using Enc = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    const Enc enc = reinterpret_cast<Enc>(L.encode_fn);
-    const int nb = dec_nb(M);
-    const int zp = qtype;                                       // record layout of the format
-    const int H = scale_sets(group_size);
-    DecodeParams p;
-    std::memset(static_cast<void*>(&p), 0, sizeof(p));
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A problem's record: its activation and weight-block maps (rows of X padded to 8 nb), pointers
+// and sizes. False if a map could not be encoded.
+static bool fill_problem(DecodeProblem& q, EncodeFn enc, const void* X, const void* Wp, void* Y, int M, int N, int K,
+                         int nb, int dtype, int zp, int H) {
     {
         const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
         const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(8 * nb), static_cast<cuuint32_t>(2 * kDecStageGroups)};
         const cuuint32_t estr[3] = {1, 1, 1};
-        const CUresult r = enc(&p.xmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                               3, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (enc(&q.xmap, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
     }
     {
         // the blob's records as 16-row blocks: (u64 words of a block, block, group, n-tile)
@@ -602,55 +635,125 @@ cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, 
                                        static_cast<cuuint64_t>(tile_record_bytes(zp, H)) * (K / kTileK)};
         const cuuint32_t box[4] = {static_cast<cuuint32_t>(bb / 8), 1, kDecStageGroups, 1};
         const cuuint32_t estr[4] = {1, 1, 1, 1};
-        const CUresult r = enc(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
-                               const_cast<uint8_t*>(static_cast<const uint8_t*>(Wp) + kBlobHeader), dims, strides, box,
-                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (enc(&q.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 4,
+                const_cast<uint8_t*>(static_cast<const uint8_t*>(Wp) + kBlobHeader), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
     }
-    p.hdr = static_cast<const uint32_t*>(Wp);
-    p.y = Y;
-    p.M = M;
-    p.N = N;
-    p.K = K;
+    q.hdr = static_cast<const uint32_t*>(Wp);
+    q.y = Y;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.k_groups = K / kTileK;
+    q.n_blocks = N / kBlockRows;
+    q.n_stages = (q.k_groups + kDecStageGroups - 1) / kDecStageGroups;
+    return true;
+}
+
+// The parts of a launch that every problem shares, and the launch itself: the grid is the sum of
+// the problems' CTA counts (cta_begin already set); the ring depth and shared memory are sized for
+// the largest K and per-CTA block count.
+template <int MAXP>
+static cudaError_t launch_params(DecodeParams<MAXP>& p, const DecodeLaunch& L, int nb, int Kmax, int nbc_max,
+                                 int items_max, int grid, int group_size, int dtype, int qtype, int* grid_out,
+                                 int* depth_out, cudaStream_t st) {
+    const int zp = qtype;                                       // record layout of the format
+    const int H = scale_sets(group_size);
     p.group_size = group_size;
     p.dtype = dtype;
     p.qtype = qtype;
     p.nib = nibble_consts(dtype == 0);
-    p.k_groups = K / kTileK;
-    p.n_blocks = N / kBlockRows;
-    p.n_stages = (p.k_groups + kDecStageGroups - 1) / kDecStageGroups;
-    // one CTA per SM; a CTA owns at most as many blocks as it has ring slots (one per block at
-    // least) and warps (16): beyond that, more CTAs than SMs
-    int grid = L.sm_count < p.n_blocks ? L.sm_count : p.n_blocks;
-    int cap = (kDecMaxSmem - decode_smem_bytes(nb, K, 0, zp, H)) / dec_stage_bytes(zp, H);
-    if (cap > kDecWarps) cap = kDecWarps;
-    if (cap < 1) return cudaErrorInvalidConfiguration;
-    if (p.n_blocks > cap * grid) grid = (p.n_blocks + cap - 1) / cap;
-    const int nbc_max = (p.n_blocks + grid - 1) / grid;
-    p.depth = decode_depth(nb, K, zp, H, nbc_max * p.n_stages, nbc_max, L.depth);
-    if (decode_smem_bytes(nb, K, p.depth, zp, H) > kDecMaxSmem) return cudaErrorInvalidConfiguration;
+    p.depth = decode_depth(nb, Kmax, zp, H, items_max, nbc_max, L.depth);
+    const int smem = decode_smem_bytes(nb, Kmax, p.depth, zp, H);
+    if (smem > kDecMaxSmem) return cudaErrorInvalidConfiguration;
     p.status = L.status;
     p.timeout_cycles = L.timeout_cycles;
     p.test_stall = L.test_stall;
     p.early = L.const_weights;
     p.trigger_late = L.trigger_late;
     p.hdr_trusted = L.hdr_trusted;
+    *grid_out = grid;
+    *depth_out = p.depth;
+    return pick_decode<MAXP>(p, nb, dtype == 0, zp, H, smem, grid, L.pdl, st);
+}
+
+// Blocks a CTA may own: ring slots (one per block at least, within shared memory) and warps (16).
+static int decode_cap(int nb, int Kmax, int zp, int H) {
+    const int cap = (kDecMaxSmem - decode_smem_bytes(nb, Kmax, 0, zp, H)) / dec_stage_bytes(zp, H);
+    return cap > kDecWarps ? kDecWarps : cap;
+}
+
+// Host entry used by wq4_mm: X [M][K], blob, Y [M][N]; the caller has checked decode_fits().
+cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, void* Y, int M, int N, int K,
+                          int group_size, int dtype, int qtype, const EpilogueArgs* epi, int* grid_out,
+                          int* depth_out, cudaStream_t st) {
+    const int nb = dec_nb(M);
+    const int zp = qtype;
+    const int H = scale_sets(group_size);
+    DecodeParams<1> p;
+    std::memset(static_cast<void*>(&p), 0, sizeof(p));
+    DecodeProblem& q = p.prob[0];
+    if (!fill_problem(q, reinterpret_cast<EncodeFn>(L.encode_fn), X, Wp, Y, M, N, K, nb, dtype, zp, H))
+        return cudaErrorInvalidValue;
+    p.num_problems = 1;
+    // one CTA per SM; a CTA owns at most `cap` blocks: beyond that, more CTAs than SMs
+    int grid = L.sm_count < q.n_blocks ? L.sm_count : q.n_blocks;
+    const int cap = decode_cap(nb, K, zp, H);
+    if (cap < 1) return cudaErrorInvalidConfiguration;
+    if (q.n_blocks > cap * grid) grid = (q.n_blocks + cap - 1) / cap;
+    const int nbc_max = (q.n_blocks + grid - 1) / grid;
     if (epi) {
         p.has_epi = 1;
         p.alpha = epi->alpha;
         p.beta = epi->beta;
-        p.c = epi->c;
-        p.bias = epi->bias;
+        q.c = epi->c;
+        q.bias = epi->bias;
     }
-    *grid_out = grid;
-    *depth_out = p.depth;
-    const bool bf16 = dtype == 0;
-    switch (nb) {
-        case 1: return pick_decode<1>(p, bf16, zp, H, grid, L.pdl, st);
-        case 2: return pick_decode<2>(p, bf16, zp, H, grid, L.pdl, st);
-        default: return pick_decode<4>(p, bf16, zp, H, grid, L.pdl, st);
+    return launch_params(p, L, nb, K, nbc_max, nbc_max * q.n_stages, grid, group_size, dtype, qtype, grid_out,
+                         depth_out, st);
+}
+
+// Host entry used by wq4_grouped_mm when every problem is decode-sized: P problems with M[p] > 0,
+// one launch. Each problem gets CTAs in proportion to its row blocks (at least one, and enough that
+// no CTA owns more than `cap` blocks); a CTA works on blocks of its own problem only.
+cudaError_t launch_decode_grouped(const DecodeLaunch& L, int P, const void* const* X, const void* const* Wp,
+                                  void* const* Y, const int* M, const int* N, const int* K, int group_size, int dtype,
+                                  int qtype, int* grid_out, int* depth_out, cudaStream_t st) {
+    if (P < 1 || P > kMaxGroupedProblems) return cudaErrorInvalidValue;
+    const int zp = qtype;
+    const int H = scale_sets(group_size);
+    int Mmax = 0, Kmax = 0;
+    long long blocks = 0;
+    for (int i = 0; i < P; ++i) {
+        Mmax = M[i] > Mmax ? M[i] : Mmax;
+        Kmax = K[i] > Kmax ? K[i] : Kmax;
+        blocks += N[i] / kBlockRows;
     }
+    const int nb = dec_nb(Mmax);
+    const int cap = decode_cap(nb, Kmax, zp, H);
+    if (cap < 1) return cudaErrorInvalidConfiguration;
+    auto pp = std::make_unique<DecodeParams<kMaxGroupedProblems>>();
+    DecodeParams<kMaxGroupedProblems>& p = *pp;
+    std::memset(static_cast<void*>(&p), 0, sizeof(p));
+    const EncodeFn enc = reinterpret_cast<EncodeFn>(L.encode_fn);
+    int grid = 0, nbc_max = 0, items_max = 0;
+    for (int i = 0; i < P; ++i) {
+        DecodeProblem& q = p.prob[i];
+        if (!fill_problem(q, enc, X[i], Wp[i], Y[i], M[i], N[i], K[i], nb, dtype, zp, H)) return cudaErrorInvalidValue;
+        long long g = (static_cast<long long>(q.n_blocks) * L.sm_count + blocks / 2) / blocks;
+        if (g < 1) g = 1;
+        if (g < (q.n_blocks + cap - 1) / cap) g = (q.n_blocks + cap - 1) / cap;
+        if (g > q.n_blocks) g = q.n_blocks;
+        q.cta_begin = grid;
+        grid += static_cast<int>(g);
+        const int nbc = static_cast<int>((q.n_blocks + g - 1) / g);
+        nbc_max = nbc > nbc_max ? nbc : nbc_max;
+        items_max = nbc * q.n_stages > items_max ? nbc * q.n_stages : items_max;
+    }
+    p.num_problems = P;
+    return launch_params(p, L, nb, Kmax, nbc_max, items_max, grid, group_size, dtype, qtype, grid_out, depth_out, st);
 }
 
 }  // namespace wq4

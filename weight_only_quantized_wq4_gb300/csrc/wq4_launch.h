@@ -49,6 +49,10 @@ bool decode_fits(int M, int K);
 cudaError_t launch_decode(const DecodeLaunch& L, const void* X, const void* Wp, void* Y, int M, int N, int K,
                           int group_size, int dtype, int qtype, const EpilogueArgs* epi, int* grid_out,
                           int* depth_out, cudaStream_t st);
+// P decode-sized problems (every M[p] > 0, decode_fits at the largest M and K) in one launch.
+cudaError_t launch_decode_grouped(const DecodeLaunch& L, int P, const void* const* X, const void* const* Wp,
+                                  void* const* Y, const int* M, const int* N, const int* K, int group_size, int dtype,
+                                  int qtype, int* grid_out, int* depth_out, cudaStream_t st);
 
 cudaError_t launch_prepack(const uint32_t* wq, const void* scales, const void* zeros, int N, int K, int G,
                            int dtype, int qtype, void* blob, cudaStream_t st);
