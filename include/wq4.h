@@ -146,7 +146,9 @@ int wq4_grouped_workspace_bytes_ex(int P, const int* M, const int* N, const int*
  *   M, N, K            host arrays of P shapes; M[p] == 0 skips problem p (its pointers are
  *                      not dereferenced and may be NULL).
  *   X, Wp, Y           host arrays of P device pointers, per-problem layouts as in wq4_mm.
- * All problems share group_size, dtype and qtype. */
+ * All problems share group_size, dtype and qtype. When every non-empty problem has at most 32
+ * tokens (decode-sized experts), the problems' row blocks go through the decode kernel in one
+ * launch, as wq4_mm does for one problem: no workspace (the workspace queries answer 0). */
 int wq4_grouped_mm(int P, const int* M, const int* N, const int* K,
                    const void* const* X, const void* const* Wp, void* const* Y,
                    int group_size, int dtype, int qtype,
