@@ -432,7 +432,11 @@ def test_wait_timeout_reports_status_and_recovers(opts, M, N, K, split_all):
 @pytest.mark.parametrize("M,N,K,dtype,split_all,in_place", [
     (200, 14336, 256, "bf16", 0, False), (200, 14336, 256, "bf16", 1, False), (100, 256, 1152, "fp16", 0, False),
     (8, 512, 1024, "bf16", 0, False), (24, 256, 512, "fp16", 0, True), (300, 384, 512, "bf16", 0, True),
-    (28, 256, 4096, "fp16", 0, True), (6, 14336, 4096, "bf16", 0, True)])
+    (28, 256, 4096, "fp16", 0, True), (6, 14336, 4096, "bf16", 0, True),
+    # one whole tile per CTA (C through the activation stage after the last group), in place
+    (128, 14336, 1024, "bf16", 0, True),
+    # 192-token tiles (C through its own buffer) and K-split tiles (C from global memory)
+    (1000, 8192, 512, "fp16", 0, False), (256, 14336, 512, "bf16", 0, False)])
 def test_mm_epilogue(opts, M, N, K, dtype, split_all, in_place):
     """Y = alpha acc + beta C + bias on the data-parallel, K-split, cluster and decode paths, and
     in place (C is Y)."""
@@ -495,10 +499,10 @@ def test_mm_float_zeros_schedules(opts, token_tile, split_all, cluster):
     assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "schedule %s" % ((token_tile, split_all, cluster),))
 
 
-@pytest.mark.parametrize("M", [6, 200])
-def test_mm_float_zeros_epilogue(opts, M):
+@pytest.mark.parametrize("M,N", [(6, 384), (200, 384), (128, 14336)])
+def test_mm_float_zeros_epilogue(opts, M, N):
     lib = opts
-    N, K, dtype = 384, 1024, "fp16"
+    K, dtype = 1024, "fp16"
     p = I.make_problem(M, N, K, dtype, "u4_fzp", seed=M + 5)
     rng = np.random.default_rng(M)
     C_bits = I.f32_to_bits(rng.standard_normal((M, N)).astype(np.float32), dtype)

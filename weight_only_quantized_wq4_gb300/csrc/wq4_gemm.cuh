@@ -108,8 +108,7 @@ struct GemmCfg {
     __device__ static bool zstep_after(int g, int g1) { return kZ && ((g + 1) % kZRec == 0 || g + 1 == g1); }
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
-    // (7 at NT = 128: the epilogue's C tile then fits beside four activation stages)
-    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? (NT == 128 ? 7 : 8) : (kZ ? 4 : 6));
+    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? 8 : (kZ ? 4 : 6));
     // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
     static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
     static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kZBytes - kWRingBytes) / kXStageBytes;
@@ -118,7 +117,9 @@ struct GemmCfg {
     // an odd count a warp would skip the other warp's phase of a slot).
     static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
     // The fused epilogue's C tile ([NT][128] 16-bit, copied by TMA while the tile's groups run) where
-    // shared memory has room for it; otherwise the fold warps read C from global memory.
+    // shared memory has room for it. Otherwise the C tile of a CTA's last (whole) tile goes into the
+    // activation stage after its last group (one stage holds exactly one C tile), and other tiles'
+    // C is read from global memory.
     static constexpr int kCTile = NT * 128 * 2;
     static constexpr int kCBytes =
         kMaxDynSmem - (1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kBarBytes) >= kCTile ? kCTile : 0;
@@ -385,6 +386,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     const uint32_t cempty_bar = s_bar + 8u * 84;  // ... and was read by the fold warps
     // C through shared memory: whole tiles of a fused epilogue that reads C, where it fits
     const bool c_smem = C::kCBytes > 0 && prm.has_epi && prm.beta != 0.f;
+    // ... or, without room, the CTA's last whole tile through the activation stage after its last step
+    const bool c_xstage = C::kCBytes == 0 && prm.has_epi && prm.beta != 0.f && prm.cluster_split == 0;
     uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 88;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
@@ -480,6 +483,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             const int depth = is_x ? C::kXStages : C::kWStages;
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
+            seg.slot = 0;                                // (no segment yet)
             int i = 0;
             int last_prob = -1;
             bool ok = hdr_ok;
@@ -523,6 +527,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         bulk_load(s_w0 + s * C::kWStageBytes, wrec, C::kRec, wfull_bar(s), pol_w);
                         ++i;
                     }
+                }
+            }
+            if (is_x && ok && c_xstage && seg.slot == -1) {
+                // the fused epilogue's C tile of this CTA's last tile, into the next activation stage
+                const int s = i % depth;
+                if (mbar_wait(xempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) {
+                    mbar_arrive_expect_tx(xfull_bar(s), C::kXStageBytes);
+                    tma_load_2d(s_x0 + s * C::kXStageBytes, &prm.cmap, xfull_bar(s), seg.nt * kTileN, seg.mt * NT,
+                                pol_stream);
+                    ++i;
                 }
             }
             issued = i;                                  // drained at the end if the CTA gives up
@@ -883,7 +897,17 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             // a whole tile reads its C from shared memory (copied while its groups ran)
             const bool cs = c_smem && seg.slot == -1;
             if (cs && !mbar_wait(cfull_bar, static_cast<uint32_t>(ct & 1), ctl)) { ok = false; break; }
-            const uint32_t c_s = cs ? s_C + static_cast<uint32_t>((col0 * 128 + r) * 2) : 0u;
+            uint32_t c_s = cs ? s_C + static_cast<uint32_t>((col0 * 128 + r) * 2) : 0u;
+            if (c_xstage && seg.slot == -1) {
+                // the CTA's last tile: its C is in the activation stage after the last step
+                Sched<MAXP> peek = sch;
+                Seg nx;
+                if (!peek.next(nx)) {
+                    const int sx = i % C::kXStages;
+                    if (!mbar_wait(xfull_bar(sx), static_cast<uint32_t>(i / C::kXStages) & 1u, ctl)) { ok = false; break; }
+                    c_s = s_x0 + static_cast<uint32_t>(sx * C::kXStageBytes + (col0 * 128 + r) * 2);
+                }
+            }
 #pragma unroll
             for (int j0 = 0; j0 < C::kNC; j0 += kB)
                 store_cols<BF16, kB>(prm, P, acc, j0, C::kNC - j0 < kB ? C::kNC - j0 : kB, m0 + j0, n, Mrows, bias,
