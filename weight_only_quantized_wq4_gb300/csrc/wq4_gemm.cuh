@@ -91,7 +91,9 @@ struct GemmCfg {
     // the P buffer of group i's partial h, and the round (phase parity) of its use
     __device__ static int pbuf(int i, int h) { return h + H * (i % kPPerHalf); }
     __device__ static uint32_t pround(int i) { return static_cast<uint32_t>(i / kPPerHalf) & 1u; }
-    static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * kPCols) / 64 >= 4 ? 4 : (512 - kPBufs * kPCols) / 64;
+    // (an even count: at NT = 160 two buffers, one per MMA warp, measured 1 % faster than three
+    // shared by both on the grouped workload)
+    static constexpr int kABufs = !ATMEM ? 2 : (512 - kPBufs * kPCols) / 64 >= 4 ? 4 : ((512 - kPBufs * kPCols) / 64) & ~1;
     static constexpr int kABytes = ATMEM ? 0 : 2 * kABuf;
     // Float zeros: the zero term sum over groups of zf[n][g] * (sum of X[m] over group g) runs on
     // the tensor core as one extra step (a "zero step") after every kZRec records of a segment and
