@@ -39,6 +39,14 @@
 
 namespace wq4 {
 
+// Weight-ring stages that leave `want` activation stages in `avail` bytes of shared memory: the
+// deepest ring of 2..8 stages that does, else 8 (the activation ring then gets what is left).
+constexpr int wring_for_x(int avail, int wstage_bytes, int xstage_bytes, int want) {
+    for (int w = 8; w >= 2; --w)
+        if (((avail - (w * wstage_bytes + 1023) / 1024 * 1024) / xstage_bytes & ~1) >= want) return w;
+    return 8;
+}
+
 template <int NT, int QT, bool ATMEM, int H>
 struct GemmCfg {
     static_assert(NT == 16 || NT == 64 || NT == 128 || NT == 160 || NT == 192, "token tile");
@@ -110,7 +118,15 @@ struct GemmCfg {
     __device__ static bool zstep_after(int g, int g1) { return kZ && ((g + 1) % kZRec == 0 || g + 1 == g1); }
     static constexpr int kBarBytes = 1024;
     static constexpr int kMaxDynSmem = 232448;
-    static constexpr int kWStages = NT <= 16 ? (kZ && !ATMEM ? 8 : 16) : (ATMEM ? 8 : (kZ ? 4 : 6));
+    // Weight ring: 8 stages; with activation tiles of 160 and 192 tokens, as many as leave four
+    // activation stages (measured at prefill, NT = 192: 2 activation + 8 weight stages 421.6 us,
+    // 4 + 4 364.0 us: the activation copies, not the weight records, are the ones that wait).
+    static constexpr int kWStages =
+        NT <= 16 ? (kZ && !ATMEM ? 8 : 16)
+                 : (ATMEM ? (NT >= 160 ? wring_for_x(kMaxDynSmem - 1024 - kBarBytes - kABytes - kZBytes,
+                                                     kWStageBytes, kXStageBytes, 4)
+                                       : 8)
+                          : (kZ ? 4 : 6));
     // the ring is padded to 1024 B so that the operand tiles after it keep their swizzle atoms aligned
     static constexpr int kWRingBytes = (kWStages * kWStageBytes + 1023) / 1024 * 1024;
     static constexpr int kXStagesFit = (kMaxDynSmem - 1024 - kBarBytes - kABytes - kZBytes - kWRingBytes) / kXStageBytes;
