@@ -570,7 +570,8 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
             if (!fn) return WQ4_ERR_CUDA;
             const cuuint64_t dims[2] = {static_cast<cuuint64_t>(shapes[0].N), static_cast<cuuint64_t>(shapes[0].M)};
             const cuuint64_t strides[1] = {static_cast<cuuint64_t>(shapes[0].N) * 2};
-            const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(pl.nt)};
+            // (half the token tile: the kernel copies a C tile as two halves)
+            const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(pl.nt / 2)};
             const cuuint32_t estr[2] = {1, 1};
             if (fn(&prm->cmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(epi->c), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

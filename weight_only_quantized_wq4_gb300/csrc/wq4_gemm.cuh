@@ -135,9 +135,10 @@ struct GemmCfg {
     // an odd count a warp would skip the other warp's phase of a slot).
     static constexpr int kXStages = (kXStagesFit > 16 ? 16 : kXStagesFit) & ~1;
     // The fused epilogue's C tile ([NT][128] 16-bit, copied by TMA while the tile's groups run) where
-    // shared memory has room for it. Otherwise the C tile of a CTA's last (whole) tile goes into the
-    // activation stage after its last group (one stage holds exactly one C tile), and other tiles'
-    // C is read from global memory.
+    // shared memory has room for it. Otherwise a whole tile's C goes through the activation ring: a
+    // "C step" after the tile's last step takes two consecutive activation stages, half the tile's
+    // token rows in each (two stages keep every stage with the MMA warp of its parity; each fold
+    // warp's columns lie in one half).
     static constexpr int kCTile = NT * 128 * 2;
     static constexpr int kCBytes =
         kMaxDynSmem - (1024 + kXStages * kXStageBytes + kWRingBytes + kABytes + kZBytes + kBarBytes) >= kCTile ? kCTile : 0;
@@ -405,7 +406,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     // C through shared memory: whole tiles of a fused epilogue that reads C, where it fits
     const bool c_smem = C::kCBytes > 0 && prm.has_epi && prm.beta != 0.f;
     // ... or, without room, the CTA's last whole tile through the activation stage after its last step
-    const bool c_xstage = C::kCBytes == 0 && prm.has_epi && prm.beta != 0.f && prm.cluster_split == 0;
+    // (where the fold warps split the token columns in two halves, as the C step's stages do)
+    const bool c_xstage = C::kCBytes == 0 && C::kColParts == 2 && prm.has_epi && prm.beta != 0.f &&
+                          prm.cluster_split == 0;
     uint8_t* const gmisc = gbase + (s_bar - sbase) + 8 * 88;
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gmisc);
     volatile int* const abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
@@ -501,7 +504,6 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             const int depth = is_x ? C::kXStages : C::kWStages;
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
-            seg.slot = 0;                                // (no segment yet)
             int i = 0;
             int last_prob = -1;
             bool ok = hdr_ok;
@@ -546,15 +548,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         ++i;
                     }
                 }
-            }
-            if (is_x && ok && c_xstage && seg.slot == -1) {
-                // the fused epilogue's C tile of this CTA's last tile, into the next activation stage
-                const int s = i % depth;
-                if (mbar_wait(xempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) {
-                    mbar_arrive_expect_tx(xfull_bar(s), C::kXStageBytes);
-                    tma_load_2d(s_x0 + s * C::kXStageBytes, &prm.cmap, xfull_bar(s), seg.nt * kTileN, seg.mt * NT,
-                                pol_stream);
-                    ++i;
+                if (is_x && ok && c_xstage && seg.slot == -1) {
+                    // the C step: the tile's C in two halves of NT / 2 token rows, one stage each
+                    for (int hf = 0; hf < 2; ++hf, ++i) {
+                        const int s = i % depth;
+                        if (!mbar_wait(xempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
+                        mbar_arrive_expect_tx(xfull_bar(s), C::kCTile / 2);
+                        tma_load_2d(s_x0 + s * C::kXStageBytes, &prm.cmap, xfull_bar(s), seg.nt * kTileN,
+                                    seg.mt * NT + hf * (NT / 2), pol_stream);
+                    }
                 }
             }
             issued = i;                                  // drained at the end if the CTA gives up
@@ -572,7 +574,8 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         if (lane == 0) {
             Sched<MAXP> sch(prm, blockIdx.x);
             Seg seg;
-            int i = 0;
+            int i = 0;                                   // compute steps (groups and zero steps)
+            int cx = 0;                                  // activation stages taken by C steps (2 each)
             // (tests) a wait that nothing ends: it runs out, records the timeout, stops the CTA
             bool ok = !(prm.test_stall && mine == 0) || mbar_wait(stall_bar, 0, ctl);
             while (ok && sch.next(seg)) {
@@ -584,11 +587,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 for (int t = 0, nstep = C::zstep_after(g, seg.g1) ? 2 : 1; t < nstep; ++t, ++i) {
                     // step i: group g, or (t = 1) the zero step after it; both alike here
                     if (H == 1 && (i & 1) != mine) continue;    // one scale set: alternate steps
-                    const int s = i % C::kXStages;
+                    const int xi = i + cx;                      // its activation stage (same parity as i)
+                    const int s = xi % C::kXStages;
                     const int b = C::pbuf(i, H == 1 ? 0 : mine);   // P buffer (two sets: half `mine`)
                     const uint32_t u = C::pround(i);
                     const int a = i % C::kABufs;                // A buffer
-                    if (!mbar_wait(xfull_bar(s), (i / C::kXStages) & 1, ctl)) { ok = false; break; }
+                    if (!mbar_wait(xfull_bar(s), (xi / C::kXStages) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(afull_bar(a), (i / C::kABufs) & 1, ctl)) { ok = false; break; }
                     if (!mbar_wait(pempty_bar(b), u ^ 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
@@ -609,6 +613,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     mma_commit(pfull_bar(b));
                     mma_commit(aempty_bar(a));
                     mma_commit(xempty_bar(s));
+                }
+                if (ok && c_xstage && seg.slot == -1) {
+                    // the C step: no MMA, but the warp that owns a stage waits for its copy, so that
+                    // it walks every phase of its stages in order (the fold warps release them)
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int xi = i + cx + hf;
+                        if ((H == 1 && (xi & 1) != mine) || !ok) continue;
+                        ok = mbar_wait(xfull_bar(xi % C::kXStages), (xi / C::kXStages) & 1, ctl);
+                    }
+                    cx += 2;
                 }
             }
             // Every MMA issued so far completes before the CTA frees its tensor memory.
@@ -795,6 +809,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
         };
         int ct = 0;                                      // whole tiles whose C came through shared memory
         int c_issued = 0;                                // C copies issued (fold warp 0, lane 0)
+        int cx = 0;                                      // activation stages taken by C steps (2 each)
         int i = 0;                                       // steps (groups and zero steps)
         int wi = 0;                                      // weight records
         bool ok = true;
@@ -813,7 +828,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     if (c_smem && seg.slot == -1 && f == 0 && lane == 0 &&
                         mbar_wait(cempty_bar, static_cast<uint32_t>(ct & 1) ^ 1u, ctl)) {
                         mbar_arrive_expect_tx(cfull_bar, C::kCTile);
-                        tma_load_2d(s_C, &prm.cmap, cfull_bar, seg.nt * kTileN, seg.mt * NT, policy_evict_first());
+                        for (int hf = 0; hf < 2; ++hf)        // (the map's box is half the token rows)
+                            tma_load_2d(s_C + hf * (C::kCTile / 2), &prm.cmap, cfull_bar, seg.nt * kTileN,
+                                        seg.mt * NT + hf * (NT / 2), policy_evict_first());
                         c_issued = ct + 1;
                     }
                 }
@@ -916,15 +933,15 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             const bool cs = c_smem && seg.slot == -1;
             if (cs && !mbar_wait(cfull_bar, static_cast<uint32_t>(ct & 1), ctl)) { ok = false; break; }
             uint32_t c_s = cs ? s_C + static_cast<uint32_t>((col0 * 128 + r) * 2) : 0u;
-            if (c_xstage && seg.slot == -1) {
-                // the CTA's last tile: its C is in the activation stage after the last step
-                Sched<MAXP> peek = sch;
-                Seg nx;
-                if (!peek.next(nx)) {
-                    const int sx = i % C::kXStages;
-                    if (!mbar_wait(xfull_bar(sx), static_cast<uint32_t>(i / C::kXStages) & 1u, ctl)) { ok = false; break; }
-                    c_s = s_x0 + static_cast<uint32_t>(sx * C::kXStageBytes + (col0 * 128 + r) * 2);
+            const bool cstep = c_xstage && seg.slot == -1;
+            if (cstep) {
+                // the C step's stage holding this thread's half of the token rows (col0 is 0 or NT / 2)
+                const int xh = i + cx + col0 / (NT / 2);
+                if (!mbar_wait(xfull_bar(xh % C::kXStages), static_cast<uint32_t>(xh / C::kXStages) & 1u, ctl)) {
+                    ok = false;
+                    break;
                 }
+                c_s = s_x0 + static_cast<uint32_t>((xh % C::kXStages) * C::kXStageBytes + r * 2);
             }
 #pragma unroll
             for (int j0 = 0; j0 < C::kNC; j0 += kB)
@@ -934,6 +951,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(cempty_bar);
                 ++ct;
+            }
+            if (cstep) {
+                // every fold warp has read its half: the two stages go back to the activation ring
+                // (standing in for the MMA warps' commits)
+                if (!fold_sync()) { ok = false; break; }
+                if (f == 0 && lane == 0) {
+                    mbar_arrive_cnt(xempty_bar((i + cx) % C::kXStages), H);
+                    mbar_arrive_cnt(xempty_bar((i + cx + 1) % C::kXStages), H);
+                }
+                cx += 2;
             }
         }
         if (prm.cluster_split > 0) {
