@@ -9,11 +9,12 @@ L = max(K, R) launches walks them, so the data each launch reads was evicted fro
 launches in between. After an untimed soak, 7 replays are timed with CUDA events on the launching
 stream (max over ranks); the line reports the median per launch and the min / max.
 
-The default run measures the five workloads one after the other. The headline (value, roofline,
-e2e, cpu_baseline) is the decode workload with constant weights (WQ4_OPT_CONST_WEIGHTS: weights
-prepacked once and not written by pending work, so the decode kernel streams them before the
-kernel ahead completes); its stream-ordered number is in "stream_ordered", and every workload's
-own line (rate, roofline, clocks) is under "workloads".
+The default run measures the five workloads one after the other, each with constant weights
+(WQ4_OPT_CONST_WEIGHTS: weights prepacked once and not written by pending work, so the kernels
+start streaming them before the kernel ahead completes) and in plain stream order. The headline
+(value, roofline, e2e, cpu_baseline) is the decode workload with constant weights; its
+stream-ordered number is in "stream_ordered", and every workload's own line (rate, roofline,
+clocks, and its stream-ordered figures) is under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--stream-order]
                   [--impl reference]
@@ -428,10 +429,9 @@ def run_gpu(args, rank, world, local_rank):
     head = None
     for name in names:
         w = Workload(args, name, dev, use_variant=(name == headline))
-        is_decode = w.plist[0].M <= 32 and not w.grouped
         modes = [("stream", 0)]
-        if is_decode and not args.stream_order:
-            modes = [("const", 1), ("stream", 0)]        # constant weights first: the headline
+        if not args.stream_order:
+            modes = [("const", 1), ("stream", 0)]        # constant weights first: the reported figure
         out = {}
         for mode, cw in modes:
             wq4.set_option(wq4.OPT_CONST_WEIGHTS, cw)
@@ -661,7 +661,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--a-in-smem", action="store_true", help="dequantised operand via shared memory")
     ap.add_argument("--stream-order", action="store_true",
-                    help="decode headline in stream order (default: constant weights, WQ4_OPT_CONST_WEIGHTS)")
+                    help="every workload in stream order only (default: constant weights, WQ4_OPT_CONST_WEIGHTS, "
+                         "then stream order)")
     ap.add_argument("--group-size", type=int, default=I.GROUP, help="variant: quantisation group size")
     ap.add_argument("--no-scales", action="store_true", help="variant: uint4b8 weights without scales")
     ap.add_argument("--epilogue", action="store_true", help="variant: Y = acc + C + bias (wq4_mm_ex)")

@@ -258,11 +258,12 @@ int wq4_get_last_error(wq4_stream_t stream);
  *                           WQ4_OPT_TIMEOUT_CYCLES bound, the call stops early and
  *                           wq4_get_last_error reports WQ4_ERR_TIMEOUT. 0 = off
  *   WQ4_OPT_CONST_WEIGHTS   1 = the caller promises that no kernel still pending on the stream
- *                           writes a blob that a later decode-kernel call reads: that kernel then
- *                           checks the blob header and copies its first weights before the kernel
- *                           ahead has completed (activations, C and outputs keep stream order).
- *                           Results are undefined if the promise is broken. 0 = stream order for
- *                           every operand (default)
+ *                           writes a blob that a later call reads: the decode kernel then checks
+ *                           the blob header and copies its first weights, and the tensor-core GEMM
+ *                           (problems given on the host) its first ring of weight records, before
+ *                           the kernel ahead has completed (activations, C and outputs keep stream
+ *                           order). Results are undefined if the promise is broken. 0 = stream
+ *                           order for every operand (default)
  *   WQ4_OPT_DECODE_DEPTH    weight ring slots of the decode kernel (one slot = one 16-row block x
  *                           1024 K); 0 = automatic, 2..16 = forced
  *   WQ4_OPT_DECODE_TRIGGER  0 = the decode kernel lets the next kernel on the stream start once its

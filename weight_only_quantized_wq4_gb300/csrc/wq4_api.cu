@@ -546,6 +546,7 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
     prm->group_size = group_size;
     prm->dtype = dtype;
     prm->qtype = qtype;
+    prm->early = g_opt.const_weights;
     prm->nib = nibble_consts(dtype == WQ4_BF16);
     prm->total_tiles = pl.total_tiles;
     prm->dp_tiles = pl.dp_tiles;

@@ -463,7 +463,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
     // split counters and partials, Y) waits for it to complete. Both are no-ops when the launch
     // carries no programmatic dependency.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Under the constant-weights promise (problems in the parameters only) the weight producer
+    // copies its first ring of records, and the header checks read the blobs, before the kernel
+    // ahead completes; the MMA and dequant warps touch only shared and tensor memory and never
+    // wait; the activation producer and the fold warps wait here as every warp does otherwise.
+    const bool w_early = prm.early != 0 && !prm.prob_tab && !prm.dyn;
+    if (!w_early || warp == 0 || warp >= 4 + C::kDQW) asm volatile("griddepcontrol.wait;" ::: "memory");
     const WaitCtl ctl{abort_flag, prm.status, prm.timeout_cycles};
 
     if (warp < 4) {
@@ -507,6 +512,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             int i = 0;
             int last_prob = -1;
             bool ok = hdr_ok;
+            bool dep_done = is_x || !w_early;            // (the early weight producer waits after a ring)
             while (ok && sch.next(seg)) {
                 const ProblemDesc& P = prob_at(prm, seg.prob);
                 const uint64_t pol_w = P.m_tiles == 1 ? pol_stream : pol_keep;
@@ -541,6 +547,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         }
                         if (!ok) break;
                     } else {
+                        if (!dep_done && i == depth) {
+                            asm volatile("griddepcontrol.wait;" ::: "memory");
+                            dep_done = true;
+                        }
                         const int s = i % depth;
                         if (!mbar_wait(wempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(wfull_bar(s), C::kRec);
@@ -559,6 +569,7 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     }
                 }
             }
+            if (!dep_done) asm volatile("griddepcontrol.wait;" ::: "memory");
             issued = i;                                  // drained at the end if the CTA gives up
         }
         __syncwarp();

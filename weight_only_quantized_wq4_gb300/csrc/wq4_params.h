@@ -140,6 +140,8 @@ struct GemmParams {
     float alpha, beta;
     const DynTable* dyn;     // device-resident problem sizes (see DynTable), or null
     int group_size, dtype, qtype;   // what every problem's blob header must say
+    int early;               // 1: the caller's constant-weights promise: the weight records (and blob
+                             // headers) may be read before the kernel ahead on the stream completes
     int hdr_trusted;         // 1: every blob was prepacked here for these arguments (records may be read
                              // while the headers are being checked); 0: check before the first read
     NibbleConsts nib;        // nibble_consts(dtype == bf16)
