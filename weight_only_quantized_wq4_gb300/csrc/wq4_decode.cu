@@ -671,7 +671,10 @@ static cudaError_t launch_params(DecodeParams<MAXP>& p, const DecodeLaunch& L, i
     p.status = L.status;
     p.timeout_cycles = L.timeout_cycles;
     p.test_stall = L.test_stall;
-    p.early = L.const_weights;
+    // (early copies only pay for a blob of some size: at 92 KB, 16 CTAs, they made the call slower)
+    long long wbytes = 0;
+    for (int i = 0; i < p.num_problems; ++i) wbytes += static_cast<long long>(p.prob[i].N) * p.prob[i].K / 2;
+    p.early = L.const_weights && wbytes >= (1LL << 20);
     p.trigger_late = L.trigger_late;
     p.hdr_trusted = L.hdr_trusted;
     *grid_out = grid;
