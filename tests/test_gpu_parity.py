@@ -321,6 +321,37 @@ def test_decode_chain_in_a_graph(opts):
     assert_parity(O.decode16(a[0], "bf16"), O.mm_problem(ps[0]), "decode chain call 0")
 
 
+@pytest.mark.parametrize("M,N,K,mode", [(128, 14336, 1024, "whole"), (300, 512, 2048, "split"),
+                                         (40, 512, 1024, "cluster"), (200, 1024, 512, "grouped")])
+def test_gemm_const_weights(opts, M, N, K, mode):
+    """With the constant-weights promise the GEMM copies weight records before the kernel ahead
+    completes; activations produced by a kernel right before the call still keep stream order."""
+    import torch
+    lib = opts
+    lib.set_option(lib.OPT_CONST_WEIGHTS, 1)
+    if mode == "split":
+        lib.set_option(lib.OPT_SPLIT_ALL, 1)
+        lib.set_option(lib.OPT_GRID, 9)
+    elif mode == "cluster":
+        lib.set_option(lib.OPT_CLUSTER, 4)
+    probs = ([I.make_problem(M, N, K, "bf16", "u4_zp", seed=M + K)] if mode != "grouped" else
+             I.make_grouped(M, 3, N, K, "bf16", "u4b8", seed=M, M_list=[M - 70, 0, 70]))
+    blobs = [gpu_prepack(lib, p) for p in probs]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        # the activations are written on the stream just before each call
+        Xs = [to_cuda16(p.X_bits, "bf16") if p.M else to_cuda16(np.zeros((0, p.K), np.uint16), "bf16") for p in probs]
+        Xs = [(x.float() * 1.0).to(torch.bfloat16) for x in Xs]
+        if mode == "grouped":
+            outs = lib.grouped_mm(Xs, blobs, [p.N for p in probs], qtype="u4b8")
+        else:
+            outs = [lib.mm(Xs[0], blobs[0], N, qtype="u4_zp")]
+        for p, Y in zip(probs, outs):
+            if p.M:
+                assert_parity(y_as_f64(Y, "bf16"), O.mm_problem(p), "const weights %s rep %d" % (mode, rep))
+    assert lib.get_last_error() == lib.OK
+
+
 def test_decode_kernel_deterministic(opts):
     lib = opts
     lib.set_option(lib.OPT_DECODE, 1)
