@@ -98,8 +98,9 @@ class Case:
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_patched_maps_match_host_encoder(opts, dtype):
-    """The set-up kernel's maps (a template's address and row count replaced on the device) equal
-    the host encoder's maps for the same activations, byte for byte; the GEMM is not launched."""
+    """The set-up kernel's maps (a template encoded on the host for the problem's rows and K, its
+    address replaced on the device) equal the host encoder's maps for the same activations, byte
+    for byte; the GEMM is not launched."""
     lib = opts
     rng = np.random.default_rng(7)
     M_list = [int(v) for v in rng.integers(0, 200, size=40)]
