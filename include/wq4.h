@@ -52,7 +52,8 @@ enum {
                                   multiple of 128 dividing K, N or K not multiples of 128, ...) */
     WQ4_ERR_WORKSPACE = -4,    /* workspace missing or smaller than the *_workspace_bytes answer */
     WQ4_ERR_CUDA = -5,         /* a CUDA runtime call failed (no device, launch failure, ...) */
-    WQ4_ERR_TIMEOUT = -6       /* a kernel's bounded pipeline wait ran out (see wq4_get_last_error) */
+    WQ4_ERR_TIMEOUT = -6,      /* a kernel's bounded pipeline wait ran out (see wq4_get_last_error) */
+    WQ4_ERR_BOUNDS = -7        /* debug build only: a kernel's bounds check failed (wq4_last_violation) */
 };
 enum { WQ4_BF16 = 0, WQ4_FP16 = 1 };
 enum { WQ4_U4B8 = 0, WQ4_U4_ZP = 1, WQ4_U4_FZP = 2 };
@@ -228,12 +229,34 @@ int wq4_grouped_mm_dev_ptrs(int P, const int* M, const int* N, const int* K,
  * Errors and options.
  * ------------------------------------------------------------------------------------------ */
 
-/* Synchronises the stream, then reports (and clears) a device-side pipeline timeout recorded
- * by any wq4 kernel on the current device (WQ4_ERR_TIMEOUT), else a pending CUDA error
- * (WQ4_ERR_CUDA), else WQ4_OK. A call whose waits ran out stops early and leaves its outputs
- * undefined; the context stays usable, but a workspace it used must be zero-filled again
- * before the next call (its split counters may be left non-zero). */
+/* Synchronises the stream, then reports (and clears) what any wq4 kernel on the current device
+ * recorded in the device status word: a failed bounds check of the debug build (WQ4_ERR_BOUNDS),
+ * else a blob header that did not match its call (WQ4_ERR_INVALID), else a pipeline timeout
+ * (WQ4_ERR_TIMEOUT); with nothing recorded, a pending CUDA error (WQ4_ERR_CUDA), else WQ4_OK. A
+ * call whose waits ran out stops early and leaves its outputs undefined; the context stays
+ * usable, but a workspace it used must be zero-filled again before the next call (its split
+ * counters may be left non-zero). */
 int wq4_get_last_error(wq4_stream_t stream);
+
+/* Bounds checks: 1 when this library is the debug build (libwq4_debug.so, compiled with
+ * WQ4_DEBUG=1), 0 for the release build, whose kernels carry no checks. The debug build's
+ * kernels check, before each use, every tiled tensor copy's innermost coordinate (a 16-byte
+ * multiple, the box inside the tensor), every weight record's range inside its blob, every
+ * scheduled tile against its problem's M, N and K groups, the K-split workspace slots and
+ * counters, and every output column against N. A failed check never faults or waits: the copy
+ * reads the tensor's origin (or the blob's first record) instead, a store or workspace access is
+ * skipped, the CTA stops at its next pipeline wait, and wq4_get_last_error reports
+ * WQ4_ERR_BOUNDS; the call's outputs are then undefined. */
+int wq4_debug_checks(void);
+
+/* The first violation that the last WQ4_ERR_BOUNDS report read back: record[0] = the check site
+ * (1 tile, 2 activation tile copy, 3 activation sums, 4 weight record, 5 epilogue C copy,
+ * 6 K-split partial slot, 7 K-split counter, 8 output column, 9 decode weight stage, 10 decode
+ * activation piece, 11 problem index), record[1..3] = the offending coordinate or index, then two
+ * values whose meaning depends on the site (listed with the sites in csrc/wq4_check.h). record
+ * must hold 4 ints. Returns 1 and clears the saved violation if there was one, 0 (record zeroed)
+ * otherwise, WQ4_ERR_INVALID for a null record. */
+int wq4_last_violation(int* record);
 
 /* Process-wide tuning and test options (not thread-safe; set before launching):
  *   WQ4_OPT_TOKEN_TILE      force the token tile (16, 64, 128, 160 or 192); 0 = automatic

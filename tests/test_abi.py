@@ -22,9 +22,26 @@ def test_exports_every_declared_symbol(clib):
 
 
 def test_status_strings(clib):
-    for code in (0, -1, -2, -3, -4, -5, -6):
-        assert clib.wq4_status_string(code)
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert clib.wq4_status_string(code) != b"unknown status", code
     assert clib.wq4_version() >= 100
+
+
+def test_release_library_has_no_bounds_checks(clib):
+    assert clib.wq4_debug_checks() == 0
+    rec = (ctypes.c_int * 4)(7, 7, 7, 7)
+    assert clib.wq4_last_violation(rec) == 0 and list(rec) == [0, 0, 0, 0]
+    assert clib.wq4_last_violation(None) == wq4.ERR_INVALID
+
+
+def test_debug_library_builds_and_exports(clib):
+    """libwq4_debug.so: the same sources with the kernels' bounds checks compiled in."""
+    path = wq4.build(debug=True)
+    assert path == wq4.DEBUG_LIB_PATH
+    dlib = ctypes.CDLL(path)
+    for n in wq4.header_functions():
+        assert hasattr(dlib, n), n
+    assert dlib.wq4_debug_checks() == 1
 
 
 def test_prepacked_bytes(clib):

@@ -14,9 +14,10 @@ from typing import List, Optional, Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libwq4.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libwq4_debug.so")   # the bounds-checking build (build(debug=True))
 HEADER = os.path.join(os.path.dirname(PKG), "include", "wq4.h")
 
-OK, ERR_INVALID, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+OK, ERR_INVALID, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, -1, -2, -3, -4, -5, -6, -7
 DTYPES = {"bf16": 0, "fp16": 1}
 QTYPES = {"u4b8": 0, "u4_zp": 1, "u4_fzp": 2}
 OPT_TOKEN_TILE, OPT_GRID, OPT_SPLIT_ALL, OPT_TIMEOUT_CYCLES, OPT_TRACE, OPT_A_IN_SMEM, OPT_CLUSTER = 1, 2, 3, 4, 5, 6, 7
@@ -33,18 +34,21 @@ class Wq4Error(RuntimeError):
         super().__init__("%s: %s (status %d)" % (what, _lib.wq4_status_string(status).decode() if _lib else "?", status))
 
 
-def build(force: bool = False) -> str:
-    from .build import build as _build
-    return _build(force=force)
+def build(force: bool = False, debug: bool = False) -> str:
+    """Build libwq4.so (or, with debug=True, the bounds-checking libwq4_debug.so)."""
+    from .builder import build as _build
+    return _build(force=force, debug=debug)
 
 
 def load_library(path: str = LIB_PATH):
-    """Load libwq4.so (raises if it has not been built)."""
+    """Load libwq4.so (raises if it has not been built); every call of this module goes through
+    the library loaded first (use_library swaps it)."""
     global _lib
     if _lib is not None:
         return _lib
     if not os.path.exists(path):
-        raise RuntimeError("libwq4.so is not built: run `python -m weight_only_quantized_wq4_gb300.build`")
+        raise RuntimeError("%s is not built: run `python -m weight_only_quantized_wq4_gb300.builder`" %
+                           os.path.basename(path))
     lib = ctypes.CDLL(path)
     c_int, c_size, vp, ll = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_longlong
     ip = ctypes.POINTER(ctypes.c_int)
@@ -69,6 +73,8 @@ def load_library(path: str = LIB_PATH):
         "wq4_grouped_dev_ptrs_workspace_bytes": (c_int, [c_int, ip, ip, ip, c_int, ctypes.POINTER(c_size)]),
         "wq4_grouped_mm_dev_ptrs": (c_int, [c_int, ip, ip, ip, vp, vp, vp, c_int, c_int, c_int, vp, c_size, vp]),
         "wq4_get_last_error": (c_int, [vp]),
+        "wq4_debug_checks": (c_int, []),
+        "wq4_last_violation": (c_int, [ip]),
         "wq4_set_option": (c_int, [c_int, ll]),
         "wq4_get_option": (ll, [c_int]),
     }
@@ -78,6 +84,39 @@ def load_library(path: str = LIB_PATH):
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+def use_library(path: str):
+    """Route every call of this module through the library at `path` (libwq4_debug.so, say), loading
+    it if needed; returns the library it replaces (None if none was loaded), for restore_library."""
+    global _lib
+    old = _lib
+    _lib = None
+    try:
+        load_library(path)
+    except Exception:
+        _lib = old
+        raise
+    return old
+
+
+def restore_library(old) -> None:
+    """Undo use_library: route the calls through `old` again."""
+    global _lib
+    _lib = old
+
+
+def debug_checks() -> bool:
+    """True when the library in use is the bounds-checking debug build."""
+    return bool(load_library().wq4_debug_checks())
+
+
+def last_violation():
+    """(site, value, context, context) of the first bounds violation the last ERR_BOUNDS report read
+    back, or None; clears it."""
+    rec = (ctypes.c_int * 4)()
+    seen = load_library().wq4_last_violation(rec)
+    return tuple(rec) if seen == 1 else None
 
 
 def header_functions(path: str = HEADER) -> List[str]:

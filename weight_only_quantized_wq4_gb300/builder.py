@@ -1,6 +1,10 @@
 """Builds libwq4.so in-tree with nvcc for sm_103a (one object per .cu, compiled in parallel).
 
-Usage: python -m weight_only_quantized_wq4_gb300.build [--force]
+With --debug it builds libwq4_debug.so instead: the same sources with -DWQ4_DEBUG=1, whose kernels
+check every copy coordinate, weight record range, scheduled tile and output column before use
+(csrc/wq4_check.h) and report a violation as WQ4_ERR_BOUNDS.
+
+Usage: python -m weight_only_quantized_wq4_gb300.builder [--force] [--debug]
 """
 from __future__ import annotations
 
@@ -16,6 +20,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwq4.so")
+DEBUG_LIB = os.path.join(PKG, "libwq4_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,9 +38,9 @@ def _sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _stamp() -> str:
+def _stamp(flags) -> str:
     h = hashlib.sha256()
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(" ".join(ARCH + flags).encode())
     for d in (CSRC, INCLUDE):
         for f in sorted(os.listdir(d)):
             with open(os.path.join(d, f), "rb") as fh:
@@ -45,21 +50,25 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if sources changed; returns the .so path."""
-    stamp = _stamp()
-    stamp_file = os.path.join(BUILD, "stamp")
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link the library (the bounds-checking one with debug=True) if sources changed;
+    returns the .so path."""
+    lib = DEBUG_LIB if debug else LIB
+    bdir = os.path.join(BUILD, "debug") if debug else BUILD
+    flags = FLAGS + ["-DWQ4_DEBUG=1"] if debug else FLAGS
+    stamp = _stamp(flags)
+    stamp_file = os.path.join(bdir, "stamp")
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read() == stamp:
-                return LIB
-    os.makedirs(BUILD, exist_ok=True)
+                return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
@@ -70,15 +79,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     workers = min(len(srcs), max(1, os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(workers) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

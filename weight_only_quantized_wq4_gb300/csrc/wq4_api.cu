@@ -37,7 +37,9 @@
 namespace wq4 {
 namespace {
 
-__device__ unsigned int g_status;   // device-side error word (bounded-wait timeouts)
+// device-side error word (bounded-wait timeouts, bad blobs, bounds checks), then the first
+// bounds violation of the debug build (site and three values)
+__device__ unsigned int g_status[1 + check::kRecordWords];
 
 constexpr int kMaxDevices = 64;
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;   // ~2 s at 2 GHz
@@ -68,6 +70,7 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+int g_violation[1 + check::kRecordWords];   // the last violation read back (count, site, three values)
 
 bool trace_on() {
     if (g_opt.trace < 0) {
@@ -415,6 +418,7 @@ struct XsumJob {
 struct XsumBatch {
     int P, span;
     long long total;             // threads over all problems
+    unsigned int* status;        // device status word (the debug build's checks)
     XsumJob job[kMaxGroupedProblems];
 };
 
@@ -458,6 +462,7 @@ __global__ void xsum_kernel(const __grid_constant__ XsumBatch b) {
             hi = __half_as_ushort(h);
             lo = __half_as_ushort(__float2half_rn(v - __half2float(h)));
         }
+        if (!WQ4_CHECK(m < J.ld && z < J.zpad, b.status, nullptr, check::kSiteXSums, m, z, J.ld)) continue;
         uint16_t* row = J.out + static_cast<size_t>(m) * 2 * J.zpad;
         row[z] = hi;
         row[J.zpad + z] = lo;
@@ -590,6 +595,7 @@ int run_gemm(const Shape* shapes, int P, const void* const* X, const void* const
         XsumBatch xb;
         std::memset(static_cast<void*>(&xb), 0, sizeof(xb));
         xb.span = kTileK / scale_sets(group_size);
+        xb.status = prm->status;
         for (int p = 0; p < P; ++p) {
             if (shapes[p].M <= 0) continue;
             uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + xsum_off + xsum_rel[p]);
@@ -678,6 +684,7 @@ const char* wq4_status_string(int status) {
         case WQ4_ERR_WORKSPACE: return "workspace missing or too small";
         case WQ4_ERR_CUDA: return "CUDA error";
         case WQ4_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case WQ4_ERR_BOUNDS: return "bounds check failed (debug build)";
         default: return "unknown status";
     }
 }
@@ -1279,15 +1286,33 @@ int wq4_get_last_error(wq4_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc) return rc;
-    unsigned int st = 0;
-    if (cudaMemcpy(&st, dev->status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return WQ4_ERR_CUDA;
+    unsigned int w[1 + check::kRecordWords] = {};
+    if (cudaMemcpy(w, dev->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return WQ4_ERR_CUDA;
+    const unsigned int st = w[0];
     if (st) {
-        const unsigned int zero = 0;
-        cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        const unsigned int zero[1 + check::kRecordWords] = {};
+        cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (st & kStatusBounds) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            g_violation[0] = 1;
+            for (int i = 0; i < check::kRecordWords; ++i) g_violation[1 + i] = static_cast<int>(w[1 + i]);
+            return WQ4_ERR_BOUNDS;
+        }
         return (st & kStatusBadBlob) ? WQ4_ERR_INVALID : WQ4_ERR_TIMEOUT;
     }
     if (se != cudaSuccess || cudaGetLastError() != cudaSuccess) return WQ4_ERR_CUDA;
     return WQ4_OK;
+}
+
+int wq4_debug_checks(void) { return kDebugChecks ? 1 : 0; }
+
+int wq4_last_violation(int* record) {
+    if (!record) return WQ4_ERR_INVALID;
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int seen = g_violation[0];
+    for (int i = 0; i < check::kRecordWords; ++i) record[i] = seen ? g_violation[1 + i] : 0;
+    g_violation[0] = 0;
+    return seen;
 }
 
 int wq4_set_option(int key, long long value) {

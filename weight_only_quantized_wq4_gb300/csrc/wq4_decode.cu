@@ -248,8 +248,10 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1)
             auto issue_next = [&]() {
                 const int slot = ib * Db + isd;
                 mbar_arrive_expect_tx(full_bar(slot), kStage);
-                const int b = bb0 + ib;
-                tma_load_4d(s_w + slot * kStage, &Q.wmap, full_bar(slot), 0, b & 7, is * kDecStageGroups, b >> 3, pol);
+                int b = bb0 + ib, gz = is * kDecStageGroups;   // (a failed check reads the blob's origin)
+                if (!WQ4_CHECK(b >= 0 && b < Q.n_blocks && gz >= 0 && gz < Q.k_groups, prm.status, abort_flag,
+                               check::kSiteDecW, b, gz, Q.n_blocks)) b = gz = 0;
+                tma_load_4d(s_w + slot * kStage, &Q.wmap, full_bar(slot), 0, b & 7, gz, b >> 3, pol);
                 ++issued;
                 if (++ib == nbc) {
                     ib = 0;
@@ -277,7 +279,9 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1)
             // activations: one copy per 8 groups (rows past M and K past the end read as zero)
             for (int p = 0; p < n_st; ++p) {
                 mbar_arrive_expect_tx(xfull_bar(p), C::kPieceBytes);
-                tma_load_3d(s_x + p * C::kPieceBytes, &Q.xmap, xfull_bar(p), 0, 0, 2 * kDecStageGroups * p);
+                int pz = 2 * kDecStageGroups * p;              // first 64-wide K panel of the piece
+                if (!WQ4_CHECK(pz >= 0 && 64 * pz < Q.K, prm.status, abort_flag, check::kSiteDecX, pz, p, Q.K)) pz = 0;
+                tma_load_3d(s_x + p * C::kPieceBytes, &Q.xmap, xfull_bar(p), 0, 0, pz);
             }
             if (!prm.early) {
                 if (trusted) {
@@ -493,6 +497,7 @@ __global__ void __launch_bounds__(kDecThreads, NB == 1 ? 2 : 1)
         const int om = onb * 8 + 2 * (olane & 3) + (ot & 1);
         const int on = (bb0 + ob) * 16 + (olane >> 2) + (ot >> 1) * 8;
         if (om >= Q.M) continue;
+        if (!WQ4_CHECK(on >= 0 && on < Q.N, prm.status, nullptr, check::kSiteYStore, on, om, Q.N)) continue;
         float v = 0.f;
         for (int sl = 0; sl < KS; ++sl)
             v += *reinterpret_cast<const float*>(sm + (((ob * KS + sl) * NB + onb) * 32 + olane) * 16 + 4 * ot);

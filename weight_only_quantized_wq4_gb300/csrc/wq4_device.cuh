@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "wq4_check.h"
 #include "wq4_params.h"
 
 namespace wq4 {

@@ -331,6 +331,7 @@ __device__ __forceinline__ uint16_t float_to_out(float v) {
 template <bool BF16, int B, int MAXP, int NV>
 __device__ __forceinline__ void store_cols(const GemmParams<MAXP>& prm, const ProblemDesc& P, float (&v)[NV],
                                            int j0, int nc, int m0, int n, int Mrows, float bias, uint32_t c_s = 0) {
+    if (!WQ4_CHECK(n >= 0 && n < P.N, prm.status, nullptr, check::kSiteYStore, n, m0, P.N)) return;
     uint16_t* y = reinterpret_cast<uint16_t*>(P.y);
     float* r = v + j0;                                   // (rewritten in place: the values are final here)
     if (prm.has_epi) {
@@ -514,7 +515,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             bool ok = hdr_ok;
             bool dep_done = is_x || !w_early;            // (the early weight producer waits after a ring)
             while (ok && sch.next(seg)) {
+                if (!WQ4_CHECK(seg.prob >= 0 && seg.prob < prm.num_problems, prm.status, abort_flag,
+                               check::kSiteProblem, seg.prob, prm.num_problems, 0)) break;
                 const ProblemDesc& P = prob_at(prm, seg.prob);
+                if (!WQ4_CHECK(check::tile_ok(seg.mt, NT, problem_rows(prm, seg.prob), seg.nt, P.N, seg.g0, seg.g1,
+                                              P.k_groups),
+                               prm.status, abort_flag, check::kSiteTile, seg.mt, seg.nt, seg.g1)) break;
                 const uint64_t pol_w = P.m_tiles == 1 ? pol_stream : pol_keep;
                 const uint8_t* wrec = P.wp + (static_cast<size_t>(seg.nt) * P.k_groups + seg.g0) * C::kRec;
                 const CUtensorMap* xmap = xmap_at(prm, seg.prob);
@@ -535,11 +541,16 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             const uint32_t stage = s_x0 + s * C::kXStageBytes;
                             mbar_arrive_expect_tx(xfull_bar(s), 2 * C::kXPanel);
                             if (t == 0) {
-                                tma_load_2d(stage, xmap, xfull_bar(s), g * kTileK, seg.mt * NT, pol_keep);
-                                tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), g * kTileK + 64, seg.mt * NT, pol_keep);
+                                int kx = g * kTileK;     // (a failed check reads the tensor's origin instead)
+                                if (!WQ4_CHECK(check::tma_x_ok(kx, 2, kTileK, P.K), prm.status, abort_flag,
+                                               check::kSiteXTile, kx, seg.mt * NT, P.K)) kx = 0;
+                                tma_load_2d(stage, xmap, xfull_bar(s), kx, seg.mt * NT, pol_keep);
+                                tma_load_2d(stage + C::kXPanel, xmap, xfull_bar(s), kx + 64, seg.mt * NT, pol_keep);
                             } else {                     // zero groups [64 zc, 64 zc + 64): high, then low part
-                                const int zc = (g * H) / 64;
+                                int zc = (g * H) / 64;
                                 const int zpad = (P.K / (kTileK / H) + 63) / 64 * 64;
+                                if (!WQ4_CHECK(check::tma_x_ok(64 * zc, 2, 64, zpad), prm.status, abort_flag,
+                                               check::kSiteXSums, 64 * zc, seg.mt * NT, zpad)) zc = 0;
                                 const CUtensorMap* sxm = &prm.sxmap[seg.prob];
                                 tma_load_2d(stage, sxm, xfull_bar(s), 64 * zc, seg.mt * NT, pol_stream);
                                 tma_load_2d(stage + C::kXPanel, sxm, xfull_bar(s), zpad + 64 * zc, seg.mt * NT, pol_stream);
@@ -554,7 +565,12 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         const int s = i % depth;
                         if (!mbar_wait(wempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(wfull_bar(s), C::kRec);
-                        bulk_load(s_w0 + s * C::kWStageBytes, wrec, C::kRec, wfull_bar(s), pol_w);
+                        const uint8_t* src = wrec;   // (a failed check reads the blob's first record instead)
+                        if (!WQ4_CHECK(check::span_ok(wrec - P.wp, C::kRec, 0,
+                                                      static_cast<long long>(P.N / kTileN) * P.k_groups * C::kRec) &&
+                                           check::aligned16(reinterpret_cast<uintptr_t>(wrec)),
+                                       prm.status, abort_flag, check::kSiteWRecord, wrec - P.wp, seg.nt, g)) src = P.wp;
+                        bulk_load(s_w0 + s * C::kWStageBytes, src, C::kRec, wfull_bar(s), pol_w);
                         ++i;
                     }
                 }
@@ -564,7 +580,10 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         const int s = i % depth;
                         if (!mbar_wait(xempty_bar(s), ((i / depth) & 1) ^ 1, ctl)) { ok = false; break; }
                         mbar_arrive_expect_tx(xfull_bar(s), C::kCTile / 2);
-                        tma_load_2d(s_x0 + s * C::kXStageBytes, &prm.cmap, xfull_bar(s), seg.nt * kTileN,
+                        int cn = seg.nt * kTileN;
+                        if (!WQ4_CHECK(check::tma_x_ok(cn, 2, kTileN, P.N), prm.status, abort_flag, check::kSiteCTile,
+                                       cn, seg.mt * NT, P.N)) cn = 0;
+                        tma_load_2d(s_x0 + s * C::kXStageBytes, &prm.cmap, xfull_bar(s), cn,
                                     seg.mt * NT + hf * (NT / 2), pol_stream);
                     }
                 }
@@ -839,8 +858,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                     if (c_smem && seg.slot == -1 && f == 0 && lane == 0 &&
                         mbar_wait(cempty_bar, static_cast<uint32_t>(ct & 1) ^ 1u, ctl)) {
                         mbar_arrive_expect_tx(cfull_bar, C::kCTile);
+                        int cn = seg.nt * kTileN;
+                        if (!WQ4_CHECK(check::tma_x_ok(cn, 2, kTileN, prob_at(prm, seg.prob).N), prm.status, abort_flag,
+                                       check::kSiteCTile, cn, seg.mt * NT, prob_at(prm, seg.prob).N)) cn = 0;
                         for (int hf = 0; hf < 2; ++hf)        // (the map's box is half the token rows)
-                            tma_load_2d(s_C + hf * (C::kCTile / 2), &prm.cmap, cfull_bar, seg.nt * kTileN,
+                            tma_load_2d(s_C + hf * (C::kCTile / 2), &prm.cmap, cfull_bar, cn,
                                         seg.mt * NT + hf * (NT / 2), policy_evict_first());
                         c_issued = ct + 1;
                     }
@@ -884,8 +906,11 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
             }
             if (seg.slot >= 0) {
                 float* mine = prm.partials + static_cast<size_t>(seg.slot) * (NT * 128);
+                if (WQ4_CHECK(seg.slot < 2 * prm.num_ctas, prm.status, abort_flag, check::kSitePartial, seg.slot,
+                              seg.tile, 2 * prm.num_ctas)) {
 #pragma unroll
-                for (int j = 0; j < C::kNC; ++j) mine[(col0 + j) * 128 + r] = acc[j];
+                    for (int j = 0; j < C::kNC; ++j) mine[(col0 + j) * 128 + r] = acc[j];
+                }
                 if (!fold_sync()) break;
                 // the units of this tile, relative to the start of the K-split region
                 const int U = prm.sk_units;
@@ -899,11 +924,17 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                         nseg += ((cc * U) / prm.num_ctas < ((cc + 1) * U) / prm.num_ctas) ? 1 : 0;
                     // release this CTA's partial (written by all fold threads before the rendezvous
                     // above) and, for the last arrival, acquire everyone else's
-                    int* cnt = prm.counters + (seg.tile - prm.dp_tiles);
-                    const int old = atomic_add_acq_rel_gpu(cnt, 1);
-                    const int last = (old == nseg - 1) ? 1 : 0;
-                    if (last) st_relaxed_gpu(cnt, 0);
-                    *fin_flag = last;
+                    const int ci = seg.tile - prm.dp_tiles;
+                    if (WQ4_CHECK(ci >= 0 && ci < prm.total_tiles - prm.dp_tiles, prm.status, abort_flag,
+                                  check::kSiteCounter, ci, seg.tile, prm.total_tiles - prm.dp_tiles)) {
+                        int* cnt = prm.counters + ci;
+                        const int old = atomic_add_acq_rel_gpu(cnt, 1);
+                        const int last = (old == nseg - 1) ? 1 : 0;
+                        if (last) st_relaxed_gpu(cnt, 0);
+                        *fin_flag = last;
+                    } else {
+                        *fin_flag = 0;
+                    }
                 }
                 if (!fold_sync()) break;
                 if (!*fin_flag) continue;
@@ -921,7 +952,9 @@ wq4_gemm_kernel(const __grid_constant__ GemmParams<MAXP> prm) {
                             const int start = (c2 * U) / prm.num_ctas;
                             use[b] = c2 <= c_last && start < ((c2 + 1) * U) / prm.num_ctas;
                             if (use[b]) {
-                                const int sl = 2 * c2 + ((c2 == c_first && start < t_u0) ? 1 : 0);
+                                int sl = 2 * c2 + ((c2 == c_first && start < t_u0) ? 1 : 0);
+                                if (!WQ4_CHECK(sl >= 0 && sl < 2 * prm.num_ctas, prm.status, abort_flag,
+                                               check::kSitePartial, sl, seg.tile, 2 * prm.num_ctas)) sl = 0;
                                 const float* src = prm.partials + static_cast<size_t>(sl) * (NT * 128) + r;
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) v[b][j] = __ldcg(src + (col0 + c + j) * 128);

@@ -14,8 +14,8 @@ constexpr uint32_t kBlobMagic = 0x50345157u;   // "WQ4P"
 constexpr uint32_t kBlobVersion = 2;
 
 // Bits of the device status word: a bounded pipeline wait ran out; a blob header did not match
-// the call's arguments.
-enum : uint32_t { kStatusTimeout = 1u, kStatusBadBlob = 2u };
+// the call's arguments; a bounds check of the debug build failed.
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadBlob = 2u, kStatusBounds = 4u };
 
 // Weight formats (the blob header's qtype code): uint4b8 (value = (q - 8) s), uint4 with a 4-bit
 // zero point per (group, row) (value = (q - z) s), uint4 with a float zero per (group, row), added
