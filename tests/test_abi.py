@@ -44,6 +44,23 @@ def test_debug_library_builds_and_exports(clib):
     assert dlib.wq4_debug_checks() == 1
 
 
+def test_binding_swaps_to_the_debug_library(clib):
+    """use_library routes the binding's calls through the debug build; restore_library undoes it."""
+    wq4.build(debug=True)
+    assert not wq4.debug_checks()
+    old = wq4.use_library(wq4.DEBUG_LIB_PATH)
+    try:
+        assert wq4.debug_checks()
+        assert wq4.last_violation() is None
+        assert wq4.prepacked_bytes(4096, 4096) == 256 + 32 * 32 * 8448     # the same ABI through it
+    finally:
+        wq4.restore_library(old)
+    assert not wq4.debug_checks()
+    with pytest.raises(RuntimeError):
+        wq4.use_library(wq4.DEBUG_LIB_PATH + ".missing")
+    assert wq4.load_library() is old                                      # a failed swap keeps the old one
+
+
 def test_prepacked_bytes(clib):
     assert clib.wq4_prepacked_bytes(4096, 4096, 128, 0) == 256 + 32 * 32 * 8448
     assert clib.wq4_prepacked_bytes(14336, 4096, 128, 1) == 256 + 112 * 32 * 8576
