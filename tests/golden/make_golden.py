@@ -22,6 +22,8 @@ import wq4_inputs as I  # noqa: E402
 CASES = {
     "tiny_m16_n256_k512_fp16_u4b8": dict(M=16, N=256, K=512, dtype="fp16", qtype="u4b8", seed=1001),
     "small_m5_n384_k256_bf16_u4zp": dict(M=5, N=384, K=256, dtype="bf16", qtype="u4_zp", seed=77),
+    "small_m7_n256_k512_fp16_u4fzp": dict(M=7, N=256, K=512, dtype="fp16", qtype="u4_fzp", seed=91),
+    "small_m6_n128_k384_bf16_u4zp_g64": dict(M=6, N=128, K=384, dtype="bf16", qtype="u4_zp", seed=64, group_size=64),
 }
 SAMPLES = [(0, 0), (1, 5), (3, 127), (4, 255), (2, 200), (15, 31), (9, 130), (4, 383)]
 
@@ -29,7 +31,7 @@ SAMPLES = [(0, 0), (1, 5), (3, 127), (4, 255), (2, 200), (15, 31), (9, 130), (4,
 def golden(spec):
     p = I.make_problem(**spec)
     Y = O.mm_problem(p)
-    blob = O.prepack(p.Wq, p.S_bits, p.N, p.K, p.dtype, p.qtype, p.Z)
+    blob = O.prepack(p.Wq, p.S_bits, p.N, p.K, p.dtype, p.qtype, p.Z, group_size=p.group_size)
     return {
         "spec": spec,
         "y_row_abs_sums": [float(v).hex() for v in np.abs(Y).sum(axis=1)],
