@@ -180,6 +180,16 @@ def test_decode_kernel(opts, M, N, K, dtype, qtype, const):
     assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "decode %s" % ((M, N, K, dtype, qtype),))
 
 
+@pytest.mark.parametrize("M,K", [(1, 12288), (8, 12288), (8, 12416), (16, 6144), (16, 6272), (32, 6144), (32, 6272)])
+def test_decode_at_its_largest_k(lib, M, K):
+    """Decode-sized M at the largest K whose activations fit in the decode kernel's shared memory at
+    once: 12288 up to 8 tokens and 6144 up to 16, with 17..32 tokens as two 16-row launches at
+    6144. Also one 128-K group beyond it, where the call takes the tensor-core GEMM instead."""
+    dtype, qtype = ("bf16" if M % 2 == 0 else "fp16"), ("u4_zp" if K % 256 else "u4b8")
+    p = I.make_problem(M, 256, K, dtype, qtype, seed=M + K)
+    assert_parity(y_as_f64(gpu_mm(lib, p), dtype), O.mm_problem(p), "largest K %s" % ((M, K),))
+
+
 @pytest.mark.parametrize("depth,trigger,const", [(2, 0, 0), (3, 1, 0), (2, 0, 1), (5, 0, 1), (16, 1, 1), (0, 0, 1)])
 @pytest.mark.parametrize("M,N,K,qtype", [(8, 4096, 4096, "u4b8"), (5, 2944, 8960, "u4_zp"), (16, 768, 1408, "u4b8"),
                                          (7, 4864, 4096, "u4_zp"), (12, 2432, 8192, "u4b8"), (3, 11264, 2048, "u4b8")])
