@@ -155,6 +155,15 @@ def test_mm_long_k(opts, token_tile):
     assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "long K, tile %d" % token_tile)
 
 
+@pytest.mark.parametrize("M,qtype", [(8, "u4b8"), (200, "u4_zp"), (64, "u4_fzp")])
+def test_mm_longest_k(lib, M, qtype):
+    """K = 65536 (512 groups) on the tensor-core path. One or two tiles on 152 SMs, so the planner
+    splits K (over a cluster, or through the workspace) into long group ranges. With float zeros
+    there are 8 zero steps per tile."""
+    p = I.make_problem(M, 128, 65536, "bf16", qtype, seed=M + 65536)
+    assert_parity(y_as_f64(gpu_mm(lib, p), "bf16"), O.mm_problem(p), "K = 65536, M = %d" % M)
+
+
 DECODE = [
     (1, 128, 128, "bf16", "u4b8"), (5, 256, 384, "fp16", "u4_zp"), (8, 4096, 4096, "bf16", "u4b8"),
     (8, 384, 8960, "bf16", "u4_zp"), (9, 512, 1024, "bf16", "u4b8"), (16, 1024, 2048, "fp16", "u4b8"),
