@@ -712,6 +712,33 @@ def test_grouped_float_zeros(lib, dtype, G, M_list):
             assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), "grouped float zeros %s" % ((p.M, p.N, p.K, G),))
 
 
+def test_grouped_calls_with_every_problem_empty(lib):
+    """Every problem with M = 0: host pointer arrays (with and without float zeros), device-resident
+    counts that are all zero, and device pointer arrays. Each call reports OK and leaves its
+    outputs untouched."""
+    import torch
+    from tests.test_gpu_dev_ptrs import SENTINEL, Case
+    Ns, Ks = [256, 128, 384], [512, 1024, 256]
+    for qtype in ("u4_zp", "u4_fzp"):
+        probs = [I.make_problem(4, n, k, "bf16", qtype, seed=90 + i) for i, (n, k) in enumerate(zip(Ns, Ks))]
+        blobs = [gpu_prepack(lib, p) for p in probs]
+        Xs = [to_cuda16(p.X_bits, "bf16") for p in probs]
+        outs = lib.grouped_mm([x[:0] for x in Xs], blobs, Ns, qtype=qtype)
+        assert lib.get_last_error() == lib.OK
+        assert all(o.shape[0] == 0 for o in outs)
+    Ys = [torch.full((4, n), SENTINEL, dtype=torch.int16, device="cuda") for n in Ns]
+    probs = [I.make_problem(4, n, k, "bf16", "u4b8", seed=95 + i) for i, (n, k) in enumerate(zip(Ns, Ks))]
+    M_dev = torch.zeros(3, dtype=torch.int32, device="cuda")
+    lib.grouped_mm_device_m([to_cuda16(p.X_bits, "bf16") for p in probs], [gpu_prepack(lib, p) for p in probs], M_dev,
+                            Ns, outs=[y.view(torch.bfloat16) for y in Ys])
+    assert lib.get_last_error() == lib.OK
+    assert all(bool((y == SENTINEL).all()) for y in Ys), "a zero-count problem was written"
+    c = Case(lib, [0, 0, 0], [(256, 512), (128, 1024)], seed=12)
+    c.run()
+    assert lib.get_last_error() == lib.OK
+    assert bool((c.Y == SENTINEL).all())
+
+
 GROUPED_DECODE = [
     ("bf16", "u4b8", 128, [8, 8, 8, 8]),
     ("fp16", "u4_zp", 128, [1, 0, 16, 5, 0]),
