@@ -72,6 +72,22 @@ def _dq_fzp_zero_subtracted(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_
     return q * s - zf
 
 
+def _dq_with_groups_at_64(gmap):
+    """The oracle's dequantisation, but at G = 64 with group index gmap(k) in place of k // 64."""
+    def dq(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+        if group_size != 64:
+            return _good_dequantize(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size)
+        q = W.unpack_u4(Wq, K).astype(np.int64)
+        z = W.zero_points(N, K, qtype, Z_words, group_size)
+        s = W.decode16(S_bits, dtype) if S_bits is not None else np.ones((K // group_size, N))
+        g = gmap(np.arange(K))
+        out = (q - z[g, :].T).astype(np.float64) * s[g, :].T
+        if qtype == "u4_fzp":
+            out = out + W.decode16(Z_words, dtype).reshape(K // group_size, N)[g, :].T
+        return out
+    return dq
+
+
 def _unpack_big_endian(words, length):
     words = np.asarray(words, dtype=np.uint32)
     shifts = 28 - 4 * np.arange(8, dtype=np.uint32)
@@ -94,6 +110,9 @@ MUTANTS = {
     "float zero added before the scale": ("dequantize", _dq_fzp_zero_before_scale),
     "float zero dropped": ("dequantize", _dq_fzp_zero_dropped),
     "float zero subtracted": ("dequantize", _dq_fzp_zero_subtracted),
+    # G = 64 (two scale sets per 128-K record): the first set used for both halves, or the halves swapped
+    "G = 64 with one scale set per 128 K": ("dequantize", _dq_with_groups_at_64(lambda k: (k // 128) * 2)),
+    "G = 64 with the halves swapped": ("dequantize", _dq_with_groups_at_64(lambda k: (k // 64) ^ 1)),
 }
 
 
@@ -108,6 +127,7 @@ def _pins_all_pass():
         lambda: pins.test_oracle_equals_exact_brute_force("fp16", "u4_fzp", (1, 8, 128)),
         lambda: pins.test_float_zero_one_hot_closed_form(),
         lambda: pins.test_float_zero_alone_is_group_sums(),
+        lambda: pins.test_oracle_group_sizes_equal_exact_brute_force("u4_zp", (64, True), (1, 8, 256)),
     ]
     for c in checks:
         try:
