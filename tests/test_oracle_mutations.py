@@ -3,12 +3,14 @@ of its functions for the duration of a test) makes at least one pin fail."""
 import numpy as np
 import pytest
 
+import oracle as OP
 import oracle.wq4_oracle as W
 import tests.test_oracle_pins as pins
 
 _good_dequantize = W.dequantize
 _good_unpack = W.unpack_u4
 _good_decode = W.decode16
+_good_epilogue = W.epilogue
 
 
 def _dq_zero_index_mod(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
@@ -88,6 +90,33 @@ def _dq_with_groups_at_64(gmap):
     return dq
 
 
+def _epi_bias_scaled(Y_acc, dtype, alpha=1.0, C_bits=None, beta=0.0, bias_bits=None):
+    D = float(alpha) * _good_epilogue(Y_acc, dtype, 1.0, None, 0.0, bias_bits)   # alpha (acc + bias)
+    if beta != 0.0:
+        D = D + float(beta) * W.decode16(np.asarray(C_bits).reshape(D.shape), dtype)
+    return D
+
+
+def _epi_alpha_beta_swapped(Y_acc, dtype, alpha=1.0, C_bits=None, beta=0.0, bias_bits=None):
+    return _good_epilogue(Y_acc, dtype, beta if C_bits is not None else alpha, C_bits,
+                          alpha if C_bits is not None else beta, bias_bits)
+
+
+def _epi_bias_per_token(Y_acc, dtype, alpha=1.0, C_bits=None, beta=0.0, bias_bits=None):
+    D = _good_epilogue(Y_acc, dtype, alpha, C_bits, beta, None)
+    if bias_bits is not None:
+        b = W.decode16(np.asarray(bias_bits), dtype)
+        D = D + b[np.arange(D.shape[0]) % b.size][:, None]       # indexed by token, not by weight row
+    return D
+
+
+def _epi_c_transposed(Y_acc, dtype, alpha=1.0, C_bits=None, beta=0.0, bias_bits=None):
+    if C_bits is None or beta == 0.0:
+        return _good_epilogue(Y_acc, dtype, alpha, C_bits, beta, bias_bits)
+    Ct = np.ascontiguousarray(np.asarray(C_bits).reshape(np.shape(Y_acc)).T).reshape(np.shape(Y_acc))
+    return _good_epilogue(Y_acc, dtype, alpha, Ct, beta, bias_bits)
+
+
 def _unpack_big_endian(words, length):
     words = np.asarray(words, dtype=np.uint32)
     shifts = 28 - 4 * np.arange(8, dtype=np.uint32)
@@ -113,6 +142,11 @@ MUTANTS = {
     # G = 64 (two scale sets per 128-K record): the first set used for both halves, or the halves swapped
     "G = 64 with one scale set per 128 K": ("dequantize", _dq_with_groups_at_64(lambda k: (k // 128) * 2)),
     "G = 64 with the halves swapped": ("dequantize", _dq_with_groups_at_64(lambda k: (k // 64) ^ 1)),
+    # the epilogue D = alpha acc + beta C + bias[n]
+    "epilogue: bias scaled by alpha": ("epilogue", _epi_bias_scaled),
+    "epilogue: alpha and beta swapped": ("epilogue", _epi_alpha_beta_swapped),
+    "epilogue: bias indexed by token": ("epilogue", _epi_bias_per_token),
+    "epilogue: C read transposed": ("epilogue", _epi_c_transposed),
 }
 
 
@@ -128,6 +162,8 @@ def _pins_all_pass():
         lambda: pins.test_float_zero_one_hot_closed_form(),
         lambda: pins.test_float_zero_alone_is_group_sums(),
         lambda: pins.test_oracle_group_sizes_equal_exact_brute_force("u4_zp", (64, True), (1, 8, 256)),
+        lambda: pins.test_epilogue_exact_brute_force(),
+        lambda: pins.test_epilogue_closed_forms(),
     ]
     for c in checks:
         try:
@@ -145,4 +181,6 @@ def test_unmutated_oracle_passes():
 def test_planted_mistake_is_caught(name, monkeypatch):
     attr, fn = MUTANTS[name]
     monkeypatch.setattr(W, attr, fn)
+    if hasattr(OP, attr):                            # the package's own name for it, which the pins call
+        monkeypatch.setattr(OP, attr, fn)
     assert not _pins_all_pass(), name
