@@ -11,6 +11,7 @@ _good_dequantize = W.dequantize
 _good_unpack = W.unpack_u4
 _good_decode = W.decode16
 _good_epilogue = W.epilogue
+_good_prepack = W.prepack
 
 
 def _dq_zero_index_mod(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
@@ -117,6 +118,42 @@ def _epi_c_transposed(Y_acc, dtype, alpha=1.0, C_bits=None, beta=0.0, bias_bits=
     return _good_epilogue(Y_acc, dtype, alpha, Ct, beta, bias_bits)
 
 
+def _pp_from_good(edit):
+    """The oracle's blob with `edit(records, qtype, group_size)` applied to its tile records
+    [N/128][K/128][record bytes] in place."""
+    def pp(Wq, S_bits, N, K, dtype, qtype, Z_words=None, group_size=128):
+        blob = _good_prepack(Wq, S_bits, N, K, dtype, qtype, Z_words, group_size=group_size).copy()
+        recs = blob[W.HEADER_BYTES:].reshape(N // 128, K // 128, W.tile_bytes(qtype, group_size))
+        edit(recs, qtype, group_size)
+        return blob
+    return pp
+
+
+def _records_k_major(recs, qtype, G):
+    recs[...] = recs.transpose(1, 0, 2).reshape(recs.shape).copy()   # (g, nt) order instead of (nt, g)
+
+
+def _scale_sets_swapped(recs, qtype, G):
+    if G != 64:
+        return
+    bb = W.block_bytes(qtype, G)
+    for b in range(8):
+        s0 = b * bb + 1024
+        a = recs[:, :, s0:s0 + 32].copy()
+        recs[:, :, s0:s0 + 32] = recs[:, :, s0 + 32:s0 + 64]
+        recs[:, :, s0 + 32:s0 + 64] = a
+
+
+def _scale_rows_paired_wrong(recs, qtype, G):
+    bb = W.block_bytes(qtype, G)
+    for b in range(8):
+        for w in range(8):                           # rows r and r + 8 of each scale word swapped
+            o = b * bb + 1024 + 4 * w
+            lo = recs[:, :, o:o + 2].copy()
+            recs[:, :, o:o + 2] = recs[:, :, o + 2:o + 4]
+            recs[:, :, o + 2:o + 4] = lo
+
+
 def _unpack_big_endian(words, length):
     words = np.asarray(words, dtype=np.uint32)
     shifts = 28 - 4 * np.arange(8, dtype=np.uint32)
@@ -147,6 +184,10 @@ MUTANTS = {
     "epilogue: alpha and beta swapped": ("epilogue", _epi_alpha_beta_swapped),
     "epilogue: bias indexed by token": ("epilogue", _epi_bias_per_token),
     "epilogue: C read transposed": ("epilogue", _epi_c_transposed),
+    # the prepacked blob's layout
+    "blob records in k-major order": ("prepack", _pp_from_good(_records_k_major)),
+    "blob G = 64 scale sets swapped": ("prepack", _pp_from_good(_scale_sets_swapped)),
+    "blob scales of rows r and r + 8 swapped": ("prepack", _pp_from_good(_scale_rows_paired_wrong)),
 }
 
 
@@ -164,6 +205,8 @@ def _pins_all_pass():
         lambda: pins.test_oracle_group_sizes_equal_exact_brute_force("u4_zp", (64, True), (1, 8, 256)),
         lambda: pins.test_epilogue_exact_brute_force(),
         lambda: pins.test_epilogue_closed_forms(),
+        lambda: pins.test_blob_layout_brute_force("u4_zp"),
+        lambda: pins.test_blob_layout_group_sizes_brute_force("u4_zp", 64, True, "fp16"),
     ]
     for c in checks:
         try:
