@@ -27,6 +27,19 @@ def test_status_strings(clib):
     assert clib.wq4_version() >= 100
 
 
+def test_every_declared_status_has_its_own_text(clib):
+    """Each WQ4_ERR_* code include/wq4.h declares maps to a text of its own, and the binding's
+    constants agree with the header."""
+    import re
+    with open(wq4.HEADER) as f:
+        codes = {n: int(v) for n, v in re.findall(r"\b(WQ4_(?:OK|ERR_[A-Z]+))\s*=\s*(-?\d+)", f.read())}
+    assert len(codes) >= 8
+    texts = {clib.wq4_status_string(v) for v in codes.values()}
+    assert len(texts) == len(codes) and b"unknown status" not in texts
+    for name, v in codes.items():
+        assert getattr(wq4, name[len("WQ4_"):]) == v, name
+
+
 def test_release_library_has_no_bounds_checks(clib):
     assert clib.wq4_debug_checks() == 0
     rec = (ctypes.c_int * 4)(7, 7, 7, 7)
