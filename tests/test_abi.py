@@ -40,6 +40,19 @@ def test_every_declared_status_has_its_own_text(clib):
         assert getattr(wq4, name[len("WQ4_"):]) == v, name
 
 
+def test_every_declared_option_matches_the_binding(clib):
+    """Each WQ4_OPT_* key include/wq4.h declares has the binding's value and reads back as set."""
+    import re
+    with open(wq4.HEADER) as f:
+        keys = {n: int(v) for n, v in re.findall(r"\b(WQ4_OPT_[A-Z_]+)\s*=\s*(\d+)", f.read())}
+    assert len(keys) >= 14
+    for name, v in keys.items():
+        assert getattr(wq4, name[len("WQ4_"):]) == v, name
+    assert clib.wq4_set_option(keys["WQ4_OPT_TOKEN_TILE"], 64) == wq4.OK
+    assert clib.wq4_get_option(keys["WQ4_OPT_TOKEN_TILE"]) == 64
+    assert clib.wq4_set_option(keys["WQ4_OPT_TOKEN_TILE"], 0) == wq4.OK
+
+
 def test_release_library_has_no_bounds_checks(clib):
     assert clib.wq4_debug_checks() == 0
     rec = (ctypes.c_int * 4)(7, 7, 7, 7)
