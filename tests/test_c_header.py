@@ -69,3 +69,21 @@ def test_c_program_compiles_links_and_runs(built):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_readme_c_example_compiles():
+    """The C example in README.md compiles against wq4.h and the CUDA runtime header."""
+    import re
+    gcc, cuda_inc = shutil.which("gcc"), "/usr/local/cuda/include"
+    if not gcc or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("no gcc or CUDA headers")
+    with open(os.path.join(ROOT, "README.md")) as f:
+        blocks = re.findall(r"```c\n(.*?)```", f.read(), flags=re.S)
+    assert len(blocks) == 1
+    os.makedirs(OUT, exist_ok=True)
+    src = os.path.join(OUT, "readme_example.c")
+    with open(src, "w") as f:
+        f.write(blocks[0])
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", cuda_inc,
+                        "-I", os.path.join(ROOT, "include"), src], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
