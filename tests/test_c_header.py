@@ -1,7 +1,7 @@
-"""include/wq4.h is a C header: a C11 program that includes it compiles with gcc under -Wall
--Wextra -pedantic -Werror, links against libwq4.so and calls the entry points that need no GPU.
-Those are the sizes, the status texts, the build flag and the argument rules, which reject bad
-calls before any CUDA work. Runs without a GPU."""
+"""include/wq4.h is a C header. A C11 program that includes it compiles with gcc under -Wall
+-Wextra -pedantic -Werror, links against libwq4.so and calls the entry points that need no GPU:
+the sizes, the status texts, the build flag and the argument rules, which reject bad calls before
+any CUDA work. The C example in README.md compiles against it too. Runs without a GPU."""
 import os
 import shutil
 import subprocess
