@@ -235,7 +235,9 @@ int wq4_grouped_mm_dev_ptrs(int P, const int* M, const int* N, const int* K,
  * (WQ4_ERR_TIMEOUT); with nothing recorded, a pending CUDA error (WQ4_ERR_CUDA), else WQ4_OK. A
  * call whose waits ran out stops early and leaves its outputs undefined; the context stays
  * usable, but a workspace it used must be zero-filled again before the next call (its split
- * counters may be left non-zero). */
+ * counters may be left non-zero). The status word is shared by every stream on the device and is
+ * read, then cleared: a kernel still running on another stream may record between the two, and
+ * that record is lost, so call it while no other wq4 work is in flight to see everything. */
 int wq4_get_last_error(wq4_stream_t stream);
 
 /* Bounds checks: 1 when this library is the debug build (libwq4_debug.so, compiled with
