@@ -712,6 +712,32 @@ def test_grouped_float_zeros(lib, dtype, G, M_list):
             assert_parity(y_as_f64(Y, dtype), O.mm_problem(p), "grouped float zeros %s" % ((p.M, p.N, p.K, G),))
 
 
+def test_trace_names_each_path(opts, capfd):
+    """WQ4_OPT_TRACE = 1: each call prints its plan on stderr, one line per path; 0: nothing."""
+    lib = opts
+    try:
+        lib.set_option(lib.OPT_TRACE, 1)
+        p = I.make_problem(8, 256, 512, "bf16", "u4b8", seed=1)
+        gpu_mm(lib, p)
+        lib.set_option(lib.OPT_TOKEN_TILE, 128)
+        q = I.make_problem(200, 256, 512, "bf16", "u4b8", seed=2)
+        gpu_mm(lib, q)
+        lib.set_option(lib.OPT_TOKEN_TILE, 0)
+        probs = I.make_grouped(20, 2, 256, 512, "bf16", "u4b8", seed=3, M_list=[12, 8])
+        lib.grouped_mm([to_cuda16(r.X_bits, "bf16") for r in probs], [gpu_prepack(lib, r) for r in probs], [256, 256])
+        assert lib.get_last_error() == lib.OK
+        err = capfd.readouterr().err
+        assert "[wq4] decode kernel: M=8" in err, err
+        assert "[wq4] problems=1 token_tile=128" in err, err
+        assert "[wq4] grouped decode kernel: problems=2" in err, err
+        lib.set_option(lib.OPT_TRACE, 0)
+        gpu_mm(lib, p)
+        assert lib.get_last_error() == lib.OK
+        assert "[wq4]" not in capfd.readouterr().err
+    finally:
+        lib.set_option(lib.OPT_TRACE, 0)
+
+
 def test_grouped_calls_with_every_problem_empty(lib):
     """Every problem with M = 0: host pointer arrays (with and without float zeros), device-resident
     counts that are all zero, and device pointer arrays. Each call reports OK and leaves its
