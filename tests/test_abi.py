@@ -141,6 +141,9 @@ def test_prepack_argument_rules(clib):
     assert pp(A16, A16b, None, 128, 256, 64, 0, 0, A16c, None) != wq4.ERR_UNSUPPORTED   # G = 64
     assert pp(MIS, A16b, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN
     assert pp(A16, A16b, MIS, 128, 128, 128, 0, 1, A16c, None) == wq4.ERR_ALIGN
+    assert pp(A16, MIS, None, 128, 128, 128, 0, 0, A16c, None) == wq4.ERR_ALIGN      # scales ("can_implement")
+    assert pp(A16, A16b, None, 128, 128, 128, 0, 0, MIS, None) == wq4.ERR_ALIGN      # the blob
+    assert pp(A16, A16b, MIS, 128, 128, 128, 0, 2, A16c, None) == wq4.ERR_ALIGN      # float zeros
     assert pp(A16, A16b, A16c, 128, 128, 128, 0, 2, A16c, None) != wq4.ERR_INVALID   # float zeros with scales
     assert pp(A16, A16b, None, 128, 128, 128, 0, 2, A16c, None) == wq4.ERR_INVALID   # float zeros missing
     assert pp(A16, None, A16c, 128, 128, 128, 0, 2, A16c, None) == wq4.ERR_INVALID   # float zeros need scales
