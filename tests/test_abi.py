@@ -27,6 +27,22 @@ def test_status_strings(clib):
     assert clib.wq4_version() >= 100
 
 
+def test_unprepack_argument_rules(clib):
+    """wq4_unprepack rejects bad calls before any CUDA work."""
+    up = clib.wq4_unprepack
+    assert up(None, 128, 128, 128, 0, 0, A16b, A16c, None, None) == wq4.ERR_INVALID       # no blob
+    assert up(A16, 128, 128, 128, 0, 0, None, A16c, None, None) == wq4.ERR_INVALID        # no code output
+    assert up(A16, 128, 128, 128, 0, 0, A16b, A16c, A16c, None) == wq4.ERR_INVALID        # zeros for u4b8
+    assert up(A16, 128, 128, 128, 0, 1, A16b, A16c, None, None) == wq4.ERR_INVALID        # zp without zeros
+    assert up(A16, 128, 128, 128, 0, 3, A16b, A16c, None, None) == wq4.ERR_INVALID        # no such qtype
+    assert up(A16, 100, 128, 128, 0, 0, A16b, A16c, None, None) == wq4.ERR_UNSUPPORTED    # N not a multiple of 128
+    assert up(A16, 128, 256, 384, 0, 0, A16b, A16c, None, None) == wq4.ERR_UNSUPPORTED    # G does not divide K
+    assert up(MIS, 128, 128, 128, 0, 0, A16b, A16c, None, None) == wq4.ERR_ALIGN
+    assert up(A16, 128, 128, 128, 0, 0, MIS, A16c, None, None) == wq4.ERR_ALIGN
+    assert up(A16, 128, 128, 128, 0, 0, A16b, MIS, None, None) == wq4.ERR_ALIGN
+    assert up(A16, 128, 128, 128, 0, 1, A16b, A16c, MIS, None) == wq4.ERR_ALIGN
+
+
 def test_every_declared_status_has_its_own_text(clib):
     """Each WQ4_ERR_* code include/wq4.h declares maps to a text of its own, and the binding's
     constants agree with the header."""
