@@ -191,6 +191,33 @@ def test_grouped_argument_rules(clib):
     assert rc not in (wq4.ERR_INVALID, wq4.ERR_ALIGN)
 
 
+def test_device_m_argument_rules(clib):
+    """wq4_grouped_mm_device_m rejects bad calls before any CUDA work."""
+    arr = ctypes.c_int * 2
+    ptrs = ctypes.c_void_p * 2
+    d = clib.wq4_grouped_mm_device_m
+    nb = ctypes.c_size_t(0)
+    assert clib.wq4_grouped_device_m_workspace_bytes(2, ctypes.byref(nb)) == wq4.OK and nb.value > 0
+    ws, wsn = ctypes.c_void_p(0x40000), nb.value
+    X, W, Y = ptrs(A16, A16), ptrs(A16b, A16b), ptrs(A16c, A16c)
+    Mdev = ctypes.c_void_p(0x50000)
+
+    def call(P=2, M_dev=Mdev, cap=(8, 8), N=(128, 128), K=(128, 128), X=X, qtype=0, ws=ws, wsn=wsn):
+        return d(P, M_dev, arr(*cap), arr(*N), arr(*K), X, W, Y, 128, 0, qtype, ws, wsn, None)
+
+    assert call(qtype=2) == wq4.ERR_UNSUPPORTED                 # float zeros need host-known shapes
+    assert call(P=0) == wq4.ERR_INVALID
+    assert call(M_dev=None) == wq4.ERR_INVALID
+    assert call(P=65) == wq4.ERR_UNSUPPORTED
+    assert call(M_dev=ctypes.c_void_p(0x50002)) == wq4.ERR_ALIGN   # int counts: 4-byte aligned
+    assert call(ws=None) == wq4.ERR_WORKSPACE
+    assert call(wsn=16) == wq4.ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p(0x40008)) == wq4.ERR_ALIGN
+    assert call(cap=(8, -1)) == wq4.ERR_INVALID
+    assert call(N=(128, 96)) == wq4.ERR_UNSUPPORTED
+    assert call(X=ptrs(A16, MIS)) == wq4.ERR_ALIGN
+
+
 def test_dev_ptrs_argument_rules(clib):
     """Host-side checks of wq4_grouped_mm_dev_ptrs: every one answers before any device work."""
     g = clib.wq4_grouped_mm_dev_ptrs
