@@ -218,6 +218,34 @@ def test_device_m_argument_rules(clib):
     assert call(X=ptrs(A16, MIS)) == wq4.ERR_ALIGN
 
 
+def test_workspace_query_argument_rules(clib):
+    """The workspace queries and the static-scratch call reject bad arguments before they look at
+    the device."""
+    nb = ctypes.c_size_t(0)
+    out = ctypes.byref(nb)
+    arr = ctypes.c_int * 2
+    assert clib.wq4_workspace_bytes(8, 128, 128, 128, None) == wq4.ERR_INVALID
+    assert clib.wq4_workspace_bytes(-1, 128, 128, 128, out) == wq4.ERR_INVALID
+    assert clib.wq4_workspace_bytes(8, 100, 128, 128, out) == wq4.ERR_UNSUPPORTED
+    assert clib.wq4_workspace_bytes(8, 128, 256, 384, out) == wq4.ERR_UNSUPPORTED     # G does not divide K
+    assert clib.wq4_workspace_bytes(8, 128, 128, 0, out) == wq4.ERR_INVALID
+    assert clib.wq4_workspace_bytes_ex(8, 128, 128, 128, 3, out) == wq4.ERR_INVALID   # no such qtype
+    g = clib.wq4_grouped_workspace_bytes
+    assert g(0, arr(8, 8), arr(128, 128), arr(128, 128), 128, out) == wq4.ERR_INVALID
+    assert g(65, arr(8, 8), arr(128, 128), arr(128, 128), 128, out) == wq4.ERR_INVALID
+    assert g(2, arr(8, -2), arr(128, 128), arr(128, 128), 128, out) == wq4.ERR_INVALID
+    assert g(2, arr(8, 8), arr(128, 128), arr(128, 200), 128, out) == wq4.ERR_UNSUPPORTED
+    assert clib.wq4_grouped_workspace_bytes_ex(2, arr(8, 8), arr(128, 128), arr(128, 128), 128, 7, out) == wq4.ERR_INVALID
+    dp = clib.wq4_grouped_dev_ptrs_workspace_bytes
+    assert dp(0, arr(8, 8), arr(128, 128), arr(128, 128), 128, out) == wq4.ERR_INVALID
+    big = ctypes.c_int * 4097
+    assert dp(4097, big(), big(*([128] * 4097)), big(*([128] * 4097)), 128, out) == wq4.ERR_UNSUPPORTED
+    assert dp(2, arr(8, 8), arr(128, 128), arr(128, 128), 128, None) == wq4.ERR_INVALID
+    st = clib.wq4_mm_static_scratch
+    assert st(A16, A16b, A16c, 8, 128, 128, 128, 2, 0, None) == wq4.ERR_INVALID          # no such dtype
+    assert st(A16, A16b, A16c, 8, 128, 128, 0, 0, 0, None) == wq4.ERR_INVALID            # group size 0
+
+
 def test_dev_ptrs_argument_rules(clib):
     """Host-side checks of wq4_grouped_mm_dev_ptrs: every one answers before any device work."""
     g = clib.wq4_grouped_mm_dev_ptrs
